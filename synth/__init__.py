@@ -1,0 +1,136 @@
+"""Seeded synthetic inputs shared by the CUDA path's tests/bench and by the oracle.
+
+This module only draws random numbers and rounds them to the input storage
+format (bf16 bit patterns, int16).  It holds none of the GEMM or copy
+arithmetic, so both sides can consume the same bits without sharing any code
+that decides a result.
+
+Generator: SplitMix64 in counter form, z_i = mix(seed + (i + 1) * 0x9E3779B97F4A7C15),
+with the published finaliser (Steele, Lea, Flood, "Fast splittable
+pseudorandom number generators", OOPSLA 2014).  Values:
+
+* uniform in [-1, 1):  u = ((z >> 40) - 2**23) / 2**23  (24-bit, exact in fp32)
+* standard normal:     Box-Muller on two 53-bit uniforms, then scaled
+* small integers:      lo + (z mod (hi - lo + 1))
+* int16:               the low 16 bits of z
+
+Rounding to bf16 uses torch's float32 -> bfloat16 conversion (round to
+nearest even); the normal draws go float64 -> float32 -> bfloat16.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+
+import numpy as np
+
+_GOLDEN = np.uint64(0x9E3779B97F4A7C15)
+_M1 = np.uint64(0xBF58476D1CE4E5B9)
+_M2 = np.uint64(0x94D049BB133111EB)
+_CHUNK = 1 << 23
+
+# seeds of the five workloads (A uses base + index, B adds 0x100)
+SEED_BASE = 0x74530000
+
+
+def splitmix64(seed: int, n: int, offset: int = 0) -> np.ndarray:
+    """n SplitMix64 outputs for counters offset+1 .. offset+n (uint64 array)."""
+    out = np.empty(n, dtype=np.uint64)
+    s = np.uint64(seed & 0xFFFFFFFFFFFFFFFF)
+    with np.errstate(over="ignore"):
+        for c0 in range(0, n, _CHUNK):
+            c1 = min(n, c0 + _CHUNK)
+            ctr = np.arange(offset + c0 + 1, offset + c1 + 1, dtype=np.uint64)
+            z = s + ctr * _GOLDEN
+            z = (z ^ (z >> np.uint64(30))) * _M1
+            z = (z ^ (z >> np.uint64(27))) * _M2
+            out[c0:c1] = z ^ (z >> np.uint64(31))
+    return out
+
+
+def _f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    import torch
+
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
+    return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16).copy()
+
+
+def uniform_pm1_bf16(seed: int, shape) -> np.ndarray:
+    """bf16 bit patterns of uniform draws in [-1, 1), row-major ``shape``."""
+    n = int(np.prod(shape))
+    z = splitmix64(seed, n)
+    u = ((z >> np.uint64(40)).astype(np.int64) - (1 << 23)).astype(np.float32) * np.float32(2.0 ** -23)
+    return _f32_to_bf16_bits(u).reshape(shape)
+
+
+def normal_bf16(seed: int, shape, scale: float = 1.0) -> np.ndarray:
+    """bf16 bit patterns of N(0, 1) * scale draws (Box-Muller, cosine branch)."""
+    n = int(np.prod(shape))
+    z = splitmix64(seed, 2 * n)
+    out = np.empty(n, dtype=np.float32)
+    for c0 in range(0, n, _CHUNK):
+        c1 = min(n, c0 + _CHUNK)
+        z1 = z[2 * c0:2 * c1:2]
+        z2 = z[2 * c0 + 1:2 * c1:2]
+        u1 = ((z1 >> np.uint64(11)).astype(np.float64) + 1.0) * 2.0 ** -53  # (0, 1]
+        u2 = (z2 >> np.uint64(11)).astype(np.float64) * 2.0 ** -53  # [0, 1)
+        v = np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * math.pi * u2) * scale
+        out[c0:c1] = v.astype(np.float32)
+    return _f32_to_bf16_bits(out).reshape(shape)
+
+
+def int_uniform_bf16(seed: int, shape, lo: int = -4, hi: int = 4) -> np.ndarray:
+    """bf16 bit patterns of integers uniform in [lo, hi] (exact in bf16 for |v| <= 256)."""
+    n = int(np.prod(shape))
+    z = splitmix64(seed, n)
+    v = (z % np.uint64(hi - lo + 1)).astype(np.int64) + lo
+    return _f32_to_bf16_bits(v.astype(np.float32)).reshape(shape)
+
+
+def int16_uniform(seed: int, n: int) -> np.ndarray:
+    """n int16 values from the low 16 bits of the generator."""
+    z = splitmix64(seed, n)
+    return (z & np.uint64(0xFFFF)).astype(np.uint16).view(np.int16)
+
+
+def one_hot_rows_bf16(n_rows: int, n_cols: int, cols: np.ndarray) -> np.ndarray:
+    """Rows with a single 1.0 at column cols[r] (bf16 bits; 0x3F80 is 1.0)."""
+    out = np.zeros((n_rows, n_cols), dtype=np.uint16)
+    out[np.arange(n_rows), cols] = 0x3F80
+    return out
+
+
+@dataclass(frozen=True)
+class GemmWorkload:
+    name: str
+    M: int
+    N: int
+    K: int
+    out: str  # "bf16" or "f32"
+    dist: str  # "uniform" or "normal"
+    tile: str  # "128x128", "128x256", "256x256"
+    sched: tuple  # schedulers exercised
+    seed_a: int
+    seed_b: int
+
+    def inputs(self):
+        if self.dist == "normal":
+            s = 1.0 / math.sqrt(self.K)
+            return normal_bf16(self.seed_a, (self.M, self.K), s), normal_bf16(self.seed_b, (self.N, self.K), s)
+        return uniform_pm1_bf16(self.seed_a, (self.M, self.K)), uniform_pm1_bf16(self.seed_b, (self.N, self.K))
+
+
+def _w(i, name, M, N, K, out, dist, tile, sched):
+    return GemmWorkload(name, M, N, K, out, dist, tile, sched, SEED_BASE + i, SEED_BASE + i + 0x100)
+
+
+# The GEMM workloads (indices follow the workload list; index 1 is the copy).
+GEMM_256 = _w(0, "gemm 256x256x256 fp32-out 128x128 static", 256, 256, 256, "f32", "uniform", "128x128", ("static",))
+GEMM_4096 = _w(2, "gemm 4096x4096x4096 bf16-out 128x256 static/clc", 4096, 4096, 4096, "bf16", "uniform", "128x256",
+               ("static", "clc"))
+GEMM_8192 = _w(3, "gemm 8192x8192x8192 bf16-out 2-CTA 256x256 clc", 8192, 8192, 8192, "bf16", "normal", "256x256",
+               ("clc",))
+GEMM_RAGGED = _w(4, "gemm 8191x6143x4096 fp32-out ragged contended", 8191, 6143, 4096, "f32", "uniform", "128x256",
+                 ("static", "clc"))
+COPY_N = 1 << 28
+COPY_SEED = SEED_BASE + 1

@@ -1,0 +1,25 @@
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
+    config.addinivalue_line("markers", "slow: full-size workload (seconds of host work)")
+
+
+@pytest.fixture(scope="session")
+def lib():
+    """The CUDA library binding; GPU tests fail loudly if it is missing."""
+    import torch
+
+    if not torch.cuda.is_available():
+        pytest.fail("GPU test collected on a machine without CUDA")
+    import tile_scheduling_gb300 as ts
+
+    return ts
