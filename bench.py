@@ -1,0 +1,422 @@
+"""Benchmark of the tile-scheduled GEMM hot path on one GB300 (or N replicas).
+
+One step = one pass of the whole hot path on the headline workload: a bf16
+GEMM of 8192 x 8192 x 8192 (bf16 output, Cluster Launch Control scheduler,
+2-CTA 256 x 256 tiles) followed by the grid-stride int16 copy of 2^28
+elements.  Inputs are seeded synthetic data already resident in HBM; both
+working sets are larger than L2 (256 MiB of GEMM operands, 1 GiB of copy
+traffic), so no L2 flush is inserted between steps.
+
+``value`` = GEMM TFLOP/s (2*M*N*K per launch / CUDA-event time of the GEMM
+launches, summed over ranks).  The copy's HBM GB/s is reported beside it.
+``e2e`` times the same GEMM through the public call with host buffers: the
+host->device copy of A and B from pinned memory, the GEMM, and the
+device->host read of D are all inside the timed region.
+
+``--impl reference`` times the CPU oracle (the plain fp64 triple loop) on the
+host cores instead, on a bounded sample of the same workload (one row of D per
+step); it is a deliberately slow baseline, not a competitor.
+
+Multi-GPU (torchrun): every rank runs the same independent problem (weak
+scaling, no data-path collective); a barrier brackets the timed region and the
+slowest rank's time is used.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_PATH = os.path.join(ROOT, "profiles", "traffic.json")
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_BF16_SUSTAINED = 1700.0
+KERNEL_SOURCES = ["gemm_kernel.cuh", "ptx.cuh", "gemm_params.h", "gemm_launch.cuh", "copy.cu"]
+
+
+# ------------------------------------------------------------------ helpers
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "tile_scheduling_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_PATH) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS,
+                "bf16_tflops_sustained": FALLBACK_BF16_SUSTAINED, "source": "fallback"}
+
+
+def load_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu capture, if it was taken on the current kernel sources."""
+    try:
+        with open(TRAFFIC_PATH) as f:
+            t = json.load(f)
+        e = t[kernel]
+        if e.get("source_hash") != kernel_source_hash() or e.get("workload") != workload:
+            return None
+        return float(e["bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self._t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self, t0: float, t1: float):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self._t:
+            self._t.join(timeout=5)
+        sms, maxes, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ts_, line in self.lines:
+            if not (t0 <= ts_ <= t1):
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sms.append(float(parts[1]))
+                maxes.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sms:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxes), "reasons": sorted(reasons),
+                "samples": len(sms)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def reduce_times(values, op: str):
+    """Max (or sum) of per-rank floats over the default process group, or the values themselves alone."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()):
+        return list(values)
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor(values, dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
+    return t.cpu().tolist()
+
+
+# ------------------------------------------------------------ our GPU arm
+def run_ours(args, ws, rank, local):
+    import torch
+    import torch.distributed as dist
+
+    import tile_scheduling_gb300 as ts
+
+    torch.cuda.set_device(local)
+    w = synth.GEMM_8192
+    M, N, K = w.M, w.N, w.K
+    A_bits, B_bits = w.inputs()
+    A = torch.from_numpy(A_bits.view(np.int16)).view(torch.bfloat16).cuda()
+    B = torch.from_numpy(B_bits.view(np.int16)).view(torch.bfloat16).cuda()
+    D = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    n_copy = synth.COPY_N
+    src = torch.from_numpy(synth.int16_uniform(synth.COPY_SEED, n_copy)).cuda()
+    dst = torch.empty_like(src)
+    stream = torch.cuda.current_stream()
+    gemm_kw = dict(sched=args.sched, tile=args.tile)
+    info = ts.ts_gemm_launch_info(M, N, K, ts.TS_OUT_BF16, args.sched, tile=args.tile)
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        ts.ts_gemm_bf16_ex(A, B, D, stream=stream, **gemm_kw)
+        if ev:
+            ev[1].record(stream)
+        ts.ts_copy_i16(src, dst, stream=stream)
+        if ev:
+            ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    ts.ts_sync_and_check()
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    outer0, outer1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    outer0.record(stream)
+    for i in range(args.steps):
+        step(events[i])
+    outer1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if ws > 1:
+        dist.barrier()
+    clocks = sampler.stop(t0, t1)
+    ts.ts_sync_and_check()
+
+    gemm_ms = [e[0].elapsed_time(e[1]) for e in events]
+    copy_ms = [e[1].elapsed_time(e[2]) for e in events]
+    total_ms = outer0.elapsed_time(outer1)
+    gemm_sum, copy_sum, total = reduce_times([sum(gemm_ms), sum(copy_ms), total_ms], "max")
+    flops = 2.0 * M * N * K
+    gemm_tflops = ws * flops * args.steps / (gemm_sum * 1e-3) / 1e12
+    copy_bytes = 4.0 * n_copy
+    copy_gbs = ws * copy_bytes * args.steps / (copy_sum * 1e-3) / 1e9
+
+    # end-to-end through the public call with host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, ts, A_bits, B_bits, M, N, K, ws)
+
+    if rank != 0:
+        return None
+    peaks = load_peaks()
+    per_launch_s = gemm_sum * 1e-3 / args.steps
+    achieved = flops / per_launch_s / 1e12
+    workload = f"gemm_bf16 {M}x{N}x{K} bf16-out {args.tile} {args.sched} + copy_i16 n=2^28"
+    roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops_sustained"],
+            "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops_sustained"], 4),
+            "traffic": load_traffic("gemm", f"{M}x{N}x{K} {args.tile} {args.sched}"),
+            "peak_kind": f"{peaks['source']} bf16 sustained (kernel timed inside a long step)",
+            "kernel": "gemm_ws_kernel"}
+    copy_roof = {"bound": "hbm", "achieved": round(copy_gbs / ws, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                 "frac": round(copy_gbs / ws / peaks["hbm_gbs"], 4), "traffic": load_traffic("copy", "n=2^28"),
+                 "peak_kind": f"{peaks['source']} HBM copy", "kernel": "copy_i16_vec_kernel"}
+    line = {
+        "metric": "bf16 GEMM TFLOP/s at 8192^3 (2-CTA 256x256, CLC); int16 copy HBM GB/s",
+        "value": round(gemm_tflops, 2), "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(total / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": workload, "M": M, "N": N, "K": K, "out": "bf16", "tile": args.tile,
+                   "sched": args.sched, "tiles": info["num_tiles"], "grid_ctas": info["grid_ctas"],
+                   "stages": info["stages"], "copy_n": n_copy,
+                   "l2": "inputs larger than L2 (256 MiB GEMM operands, 1 GiB copy traffic); no flush",
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+        "gemm": {"tflops": round(gemm_tflops, 2), "ms_median": round(statistics.median(gemm_ms), 4),
+                 "ms_min": round(min(gemm_ms), 4)},
+        "copy": {"gbs": round(copy_gbs, 1), "ms_median": round(statistics.median(copy_ms), 4),
+                 "roofline": copy_roof},
+        "roofline": roof,
+        "clocks": clocks,
+        "gpu_launches": 2 * args.steps,
+        "e2e": e2e,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args)
+    return line
+
+
+def run_e2e(args, ts, A_bits, B_bits, M, N, K, ws):
+    import torch
+
+    A_h = torch.from_numpy(A_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    B_h = torch.from_numpy(B_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    D_h = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    A = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
+    B = torch.empty((N, K), dtype=torch.bfloat16, device="cuda")
+    D = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def one():
+        A.copy_(A_h, non_blocking=True)
+        B.copy_(B_h, non_blocking=True)
+        ts.ts_gemm_bf16_ex(A, B, D, sched=args.sched, tile=args.tile, stream=stream)
+        D_h.copy_(D, non_blocking=True)
+
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize()
+    steps = max(3, min(args.steps, args.e2e_steps))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = reduce_times([e0.elapsed_time(e1)], "max")[0]
+    ts.ts_sync_and_check()
+    flops = 2.0 * M * N * K
+    return {"value": round(ws * flops * steps / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": int(A_h.numel() * 2 + B_h.numel() * 2), "d2h_bytes_per_step": int(D_h.numel() * 2),
+            "steps": steps, "ms_per_step": round(ms / steps, 4)}
+
+
+# -------------------------------------------------------- CPU oracle arm
+def _oracle_sample_rate(rows: int, threads: int):
+    """Time the oracle's triple loop on `rows` full rows of the 8192^3 workload."""
+    import oracle
+
+    w = synth.GEMM_8192
+    rng = np.random.default_rng(0)
+    A = synth.normal_bf16(w.seed_a, (rows, w.K), 1.0 / np.sqrt(w.K))  # same distribution, first rows' shape
+    B_bits = _B_cache()
+    ii = np.repeat(np.arange(rows), w.N)
+    jj = np.tile(np.arange(w.N), rows)
+    del rng
+    t0 = time.perf_counter()
+    oracle.gemm_entries_f64(A, B_bits, ii, jj, threads=threads)
+    dt = time.perf_counter() - t0
+    return 2.0 * rows * w.N * w.K / dt, dt
+
+
+_BCACHE = {}
+
+
+def _B_cache():
+    if "B" not in _BCACHE:
+        w = synth.GEMM_8192
+        _BCACHE["B"] = synth.normal_bf16(w.seed_b, (w.N, w.K), 1.0 / np.sqrt(w.K))
+    return _BCACHE["B"]
+
+
+def cpu_baseline(args):
+    import oracle
+
+    threads = oracle.default_threads()
+    rows = max(1, args.cpu_rows)
+    rate, dt = _oracle_sample_rate(rows, threads)
+    return {"value": round(rate / 1e12, 8), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{rows} full rows of D (8192 entries each, K=8192) of the 8192^3 workload, fp64 triple loop, "
+                      f"{dt:.1f} s"}
+
+
+def run_reference(args, ws, rank):
+    """The oracle as it stands on the host cores; rank 0 only."""
+    if rank != 0:
+        return None
+    import oracle
+
+    threads = oracle.default_threads()
+    w = synth.GEMM_8192
+    B_bits = _B_cache()
+    A_rows = synth.normal_bf16(w.seed_a, (1, w.K), 1.0 / np.sqrt(w.K))
+    ii = np.zeros(w.N, dtype=np.int64)
+    jj = np.arange(w.N, dtype=np.int64)
+    for _ in range(args.warmup):
+        oracle.gemm_entries_f64(A_rows, B_bits, ii, jj, threads=threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.gemm_entries_f64(A_rows, B_bits, ii, jj, threads=threads)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * w.N * w.K * args.steps
+    value = flops / dt / 1e12
+    sample = f"one row of D per step (8192 entries, K=8192) of the 8192^3 workload, fp64 triple loop"
+    return {"impl": "reference", "metric": "bf16 GEMM TFLOP/s at 8192^3 (2-CTA 256x256, CLC); int16 copy HBM GB/s",
+            "value": round(value, 8), "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt * 1e3 / args.steps, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"gemm_bf16 {w.M}x{w.N}x{w.K} (oracle sample)", "M": w.M, "N": w.N, "K": w.K},
+            "cpu_baseline": {"value": round(value, 8), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 8), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--tile", default="256x256", choices=["128x128", "128x256", "256x256", "auto"])
+    ap.add_argument("--sched", default="clc", choices=["static", "clc"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-rows", type=int, default=16)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    ws, rank, local = dist_env()
+    if args.gpus != ws and ws > 1:
+        ap.error(f"--gpus {args.gpus} but WORLD_SIZE={ws}")
+
+    if args.impl == "reference":
+        line = run_reference(args, ws, rank)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return 0
+
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    try:
+        line = run_ours(args, ws, rank, local)
+    finally:
+        if ws > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,155 @@
+/*
+ * tsgemm -- persistent, warp-specialised bf16 GEMM with static and Cluster
+ * Launch Control tile scheduling, plus a vectorised grid-stride int16 copy,
+ * for one NVIDIA GB300 (sm_103a).
+ *
+ * C ABI: plain pointers and sizes only.  Every device pointer is owned by
+ * the caller; the library never allocates device memory on these paths.  The
+ * only library-owned device state is a small per-device status word that
+ * records a timed-out barrier wait (see ts_sync_and_check).
+ *
+ * Streams are passed as `void *` holding a cudaStream_t (NULL = the legacy
+ * default stream).  Every compute call is asynchronous on that stream and
+ * returns once the launch is queued; none of them synchronises.
+ *
+ * Errors: each call returns a ts_status.  On failure, ts_last_error_detail()
+ * gives a human-readable message for the calling thread.  Argument errors are
+ * detected before any launch, so a failing call never leaves work queued.
+ */
+#ifndef TSGEMM_H
+#define TSGEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TS_OK = 0,
+    TS_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad enum, overlapping copy */
+    TS_ERR_UNSUPPORTED = 2, /* legal request this build cannot run (TMA alignment, size limits) */
+    TS_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed; detail has the CUDA message */
+    TS_ERR_TIMEOUT = 4      /* a kernel gave up on a barrier wait (reported by ts_sync_and_check) */
+} ts_status;
+
+typedef enum { TS_SCHED_STATIC = 0, TS_SCHED_CLC = 1 } ts_sched;
+typedef enum { TS_OUT_BF16 = 0, TS_OUT_F32 = 1 } ts_out_dtype;
+
+typedef enum {
+    TS_TILE_AUTO = 0,
+    TS_TILE_128x128 = 1,      /* one CTA per 128x128 output tile */
+    TS_TILE_128x256 = 2,      /* one CTA per 128x256 output tile */
+    TS_TILE_256x256_2CTA = 3  /* a 2-CTA cluster per 256x256 output tile (cta_group::2 MMA) */
+} ts_tile;
+
+/* Optional knobs for ts_gemm_bf16_ex; zero means "default" for every field. */
+typedef struct {
+    int32_t tile;         /* ts_tile */
+    int32_t max_workers;  /* static scheduler: cap on persistent workers (CTAs or 2-CTA clusters) */
+    int64_t lda;          /* row stride of A in elements (>= K); 0 = K */
+    int64_t ldb;          /* row stride of B in elements (>= K); 0 = K */
+    int64_t ldd;          /* row stride of D in elements (>= N); 0 = N */
+    double timeout_s;     /* per-wait limit for every mbarrier wait in the kernel; 0 = 2 s */
+    int64_t *trace;       /* device buffer of 4 * num_tiles int64, zeroed by the caller, or NULL.
+                             Per tile t: [4t] += 1 per visit, [4t+1] = worker index,
+                             [4t+2] = %globaltimer when the producer started the tile,
+                             [4t+3] = %globaltimer when the epilogue issued its last store. */
+    int32_t raster_group; /* tile raster: consecutive tile ids walk this many tile rows; 0 = 8 */
+    int32_t reserved;
+} ts_gemm_opts;
+
+/* What ts_gemm_bf16_ex would launch for a problem (host-only query). */
+typedef struct {
+    int32_t tile_m, tile_n;  /* output tile of one worker */
+    int32_t cluster;         /* CTAs per worker: 1, or 2 for the 2-CTA tile */
+    int32_t stages;          /* shared-memory ring depth */
+    int64_t tiles_m, tiles_n, num_tiles;
+    int64_t grid_ctas;       /* CTAs launched */
+    int64_t workers;         /* persistent workers resident at once (static) or num_tiles (CLC) */
+    int32_t smem_bytes;      /* dynamic shared memory per CTA */
+    int32_t tma_store;       /* 1 if D is written through TMA stores, 0 for the st.global epilogue */
+} ts_launch_info;
+
+/*
+ * ts_gemm_bf16 -- D = A * B^T with bf16 inputs and fp32 accumulation.
+ *
+ * Definition: D[i][j] = sum_{k<K} A[i][k] * B[j][k] (CUTLASS TS "Pipeline
+ * Groups", Overview: the GEMM mainloop resource graph gmem_ab -> smem_a,
+ * smem_b -> tmem_c -> gmem_d; TS "Resources", per-work-tile scale_d reset).
+ * Tiles are assigned by the static grid-stride rule (TS "Schedules",
+ * Scheduling Shapes; "Cluster Launch Control", static persistent scheduler)
+ * or by Cluster Launch Control work stealing ("Cluster Launch Control", one
+ * CLC request and the overlap loop).  The scheduler changes which CTA computes
+ * a tile, never the result.
+ *
+ *   A     device, bf16 [M][K] row-major (K contiguous), 16-byte aligned
+ *   B     device, bf16 [N][K] row-major (K contiguous), 16-byte aligned
+ *   D     device, [M][N] row-major, bf16 (out = TS_OUT_BF16, rounded to
+ *         nearest even from fp32) or fp32 (TS_OUT_F32)
+ *   M, N, K  sizes, each in [0, 2^31 - 1]
+ *
+ * M == 0 or N == 0: no-op.  K == 0: D is filled with zeros.
+ * A and B rows must start on 16-byte boundaries (K a multiple of 8, or lda/ldb
+ * via ts_gemm_bf16_ex) or the call returns TS_ERR_UNSUPPORTED.  A D whose row
+ * pitch is not a multiple of 16 bytes is written by a plain-store epilogue.
+ * D must not overlap A or B.
+ */
+ts_status ts_gemm_bf16(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K,
+                       int32_t out_dtype, int32_t sched, void *stream);
+
+/* As ts_gemm_bf16, with the knobs above; opts may be NULL. */
+ts_status ts_gemm_bf16_ex(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K,
+                          int32_t out_dtype, int32_t sched, const ts_gemm_opts *opts, void *stream);
+
+/* Fill *info with the launch ts_gemm_bf16_ex would make (no launch, no sync). */
+ts_status ts_gemm_launch_info(int64_t M, int64_t N, int64_t K, int32_t out_dtype, int32_t sched,
+                              const ts_gemm_opts *opts, ts_launch_info *info);
+
+/*
+ * ts_copy_i16 -- dst[i] = src[i] for 0 <= i < n (TS "Resources", the int16
+ * copy example: get_item / set_item guarded by gid < num_entries; TS
+ * "Schedules", the grid-stride domain start = bx * tpb + tx, step = gdimx * tpb).
+ *
+ *   src, dst  device int16 arrays of n elements.  src == dst is a no-op;
+ *             any other overlap is TS_ERR_INVALID_ARG.
+ *   n         element count >= 0.
+ * 16-byte vectors are used when src and dst share their offset modulo 16
+ * bytes; other alignments take an element-wise path with the same result.
+ */
+ts_status ts_copy_i16(const int16_t *src, int16_t *dst, int64_t n, void *stream);
+
+/*
+ * ts_spin -- occupy `ctas` SMs for `duration_ns` nanoseconds (measured with
+ * %globaltimer), to make part of the GPU unavailable to a following kernel.
+ * Each spinning CTA requests the largest opt-in shared memory so that no
+ * GEMM CTA can share its SM.  `started` is a host int32 in page-locked,
+ * device-mapped memory (e.g. cudaHostAlloc or a pinned torch tensor); every
+ * CTA adds 1 to it when it begins.  duration_ns is capped at 10 s; ctas must
+ * be in [1, number of SMs].  This is a measurement helper: the load-imbalance
+ * scenario ("Cluster Launch Control", limits of the static scheduler: SMs
+ * held by another kernel leave a long launch tail).
+ */
+ts_status ts_spin(int32_t ctas, int64_t duration_ns, int32_t *started, void *stream);
+
+/* Wait on the host until *started >= expected or timeout_s passes
+ * (TS_ERR_TIMEOUT).  Reads the counter with volatile loads. */
+ts_status ts_spin_wait_started(const int32_t *started, int32_t expected, double timeout_s);
+
+/* Synchronise `stream`, then report and clear the device status word:
+ * TS_ERR_TIMEOUT if a kernel on the current device gave up on a barrier
+ * wait since the last check (detail names the wait and the block),
+ * TS_ERR_CUDA on an asynchronous CUDA error, TS_OK otherwise. */
+ts_status ts_sync_and_check(void *stream);
+
+/* Number of SMs of the current device (cached), or -1 on error. */
+int32_t ts_num_sms(void);
+
+const char *ts_status_string(ts_status s);
+/* Thread-local message for the last failing call on this thread ("" if none). */
+const char *ts_last_error_detail(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TSGEMM_H */

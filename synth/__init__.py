@@ -14,12 +14,18 @@ pseudorandom number generators", OOPSLA 2014).  Values:
 * small integers:      lo + (z mod (hi - lo + 1))
 * int16:               the low 16 bits of z
 
+The draws are made by synth.c (compiled with gcc on first use); splitmix64()
+here is the same generator in numpy, kept as the readable reference form.
 Rounding to bf16 uses torch's float32 -> bfloat16 conversion (round to
 nearest even); the normal draws go float64 -> float32 -> bfloat16.
 """
 from __future__ import annotations
 
+import ctypes
 import math
+import os
+import subprocess
+import threading
 from dataclasses import dataclass
 
 import numpy as np
@@ -34,7 +40,7 @@ SEED_BASE = 0x74530000
 
 
 def splitmix64(seed: int, n: int, offset: int = 0) -> np.ndarray:
-    """n SplitMix64 outputs for counters offset+1 .. offset+n (uint64 array)."""
+    """n SplitMix64 outputs for counters offset+1 .. offset+n (uint64 array), numpy reference form."""
     out = np.empty(n, dtype=np.uint64)
     s = np.uint64(seed & 0xFFFFFFFFFFFFFFFF)
     with np.errstate(over="ignore"):
@@ -55,42 +61,80 @@ def _f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16).copy()
 
 
+# ------------------------------------------------------------ C generator
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "synth.c")
+_LIB_PATH = os.path.join(_HERE, "_build", "libsynth.so")
+_lib = None
+_lock = threading.Lock()
+
+
+def build(force: bool = False) -> str:
+    """Compile synth.c (gcc, OpenMP) into synth/_build/libsynth.so."""
+    os.makedirs(os.path.dirname(_LIB_PATH), exist_ok=True)
+    if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    subprocess.run(["gcc", "-O2", "-fopenmp", "-ffp-contract=off", "-shared", "-fPIC", "-o", tmp, _SRC, "-lm"],
+                   check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _c():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P, I64, U64 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint64
+            lib.synth_splitmix64.argtypes = [U64, I64, I64, P]
+            lib.synth_uniform_pm1_f32.argtypes = [U64, I64, P]
+            lib.synth_normal_f32.argtypes = [U64, I64, ctypes.c_double, P]
+            lib.synth_int_uniform_f32.argtypes = [U64, I64, ctypes.c_int32, ctypes.c_int32, P]
+            lib.synth_int16.argtypes = [U64, I64, P]
+            _lib = lib
+    return _lib
+
+
+def _seed(seed: int) -> int:
+    return seed & 0xFFFFFFFFFFFFFFFF
+
+
+def splitmix64_fast(seed: int, n: int, offset: int = 0) -> np.ndarray:
+    out = np.empty(n, dtype=np.uint64)
+    _c().synth_splitmix64(_seed(seed), offset, n, out.ctypes.data)
+    return out
+
+
 def uniform_pm1_bf16(seed: int, shape) -> np.ndarray:
     """bf16 bit patterns of uniform draws in [-1, 1), row-major ``shape``."""
     n = int(np.prod(shape))
-    z = splitmix64(seed, n)
-    u = ((z >> np.uint64(40)).astype(np.int64) - (1 << 23)).astype(np.float32) * np.float32(2.0 ** -23)
-    return _f32_to_bf16_bits(u).reshape(shape)
+    f = np.empty(n, dtype=np.float32)
+    _c().synth_uniform_pm1_f32(_seed(seed), n, f.ctypes.data)
+    return _f32_to_bf16_bits(f).reshape(shape)
 
 
 def normal_bf16(seed: int, shape, scale: float = 1.0) -> np.ndarray:
     """bf16 bit patterns of N(0, 1) * scale draws (Box-Muller, cosine branch)."""
     n = int(np.prod(shape))
-    z = splitmix64(seed, 2 * n)
-    out = np.empty(n, dtype=np.float32)
-    for c0 in range(0, n, _CHUNK):
-        c1 = min(n, c0 + _CHUNK)
-        z1 = z[2 * c0:2 * c1:2]
-        z2 = z[2 * c0 + 1:2 * c1:2]
-        u1 = ((z1 >> np.uint64(11)).astype(np.float64) + 1.0) * 2.0 ** -53  # (0, 1]
-        u2 = (z2 >> np.uint64(11)).astype(np.float64) * 2.0 ** -53  # [0, 1)
-        v = np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * math.pi * u2) * scale
-        out[c0:c1] = v.astype(np.float32)
-    return _f32_to_bf16_bits(out).reshape(shape)
+    f = np.empty(n, dtype=np.float32)
+    _c().synth_normal_f32(_seed(seed), n, float(scale), f.ctypes.data)
+    return _f32_to_bf16_bits(f).reshape(shape)
 
 
 def int_uniform_bf16(seed: int, shape, lo: int = -4, hi: int = 4) -> np.ndarray:
     """bf16 bit patterns of integers uniform in [lo, hi] (exact in bf16 for |v| <= 256)."""
     n = int(np.prod(shape))
-    z = splitmix64(seed, n)
-    v = (z % np.uint64(hi - lo + 1)).astype(np.int64) + lo
-    return _f32_to_bf16_bits(v.astype(np.float32)).reshape(shape)
+    f = np.empty(n, dtype=np.float32)
+    _c().synth_int_uniform_f32(_seed(seed), n, lo, hi, f.ctypes.data)
+    return _f32_to_bf16_bits(f).reshape(shape)
 
 
 def int16_uniform(seed: int, n: int) -> np.ndarray:
     """n int16 values from the low 16 bits of the generator."""
-    z = splitmix64(seed, n)
-    return (z & np.uint64(0xFFFF)).astype(np.uint16).view(np.int16)
+    out = np.empty(n, dtype=np.int16)
+    _c().synth_int16(_seed(seed), n, out.ctypes.data)
+    return out
 
 
 def one_hot_rows_bf16(n_rows: int, n_cols: int, cols: np.ndarray) -> np.ndarray:

@@ -1,0 +1,74 @@
+"""The C-ABI library loads and exports every entry point its header declares (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tsgemm.h")
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(ts_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def ts():
+    import tile_scheduling_gb300 as ts
+
+    return ts
+
+
+def test_header_declares_the_api():
+    names = _declared()
+    for n in ("ts_gemm_bf16", "ts_gemm_bf16_ex", "ts_copy_i16", "ts_sync_and_check"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(ts):
+    lib = ctypes.CDLL(ts.LIB_PATH)
+    missing = [n for n in _declared() if not hasattr(lib, n)]
+    assert not missing, f"declared but not exported: {missing}"
+
+
+def test_binding_names_match_header(ts):
+    for n in _declared():
+        assert hasattr(ts, n), f"binding lacks {n}"
+
+
+def test_status_strings(ts):
+    assert ts.ts_status_string(ts.TS_OK) == "TS_OK"
+    assert ts.ts_status_string(ts.TS_ERR_TIMEOUT) == "TS_ERR_TIMEOUT"
+    assert ts.ts_status_string(99) == "TS_ERR_UNKNOWN"
+
+
+def test_argument_errors_need_no_gpu(ts):
+    # rejected before any CUDA call
+    assert ts.ts_gemm_bf16_ptr(0, 0, 0, -1, 4, 4, ts.TS_OUT_F32, stream=0) == ts.TS_ERR_INVALID_ARG
+    assert "sizes" in ts.ts_last_error_detail()
+    assert ts.ts_gemm_bf16_ptr(0, 0, 0, 4, 4, 1 << 31, ts.TS_OUT_F32, stream=0) == ts.TS_ERR_INVALID_ARG
+    assert ts.ts_gemm_bf16_ptr(0, 0, 0, 4, 4, 4, 7, stream=0) == ts.TS_ERR_INVALID_ARG
+    assert ts.ts_gemm_bf16_ptr(0, 0, 0, 4, 4, 4, ts.TS_OUT_F32, sched=5, stream=0) == ts.TS_ERR_INVALID_ARG
+    assert ts.ts_gemm_bf16_ptr(0, 0, 0, 4, 4, 4, ts.TS_OUT_F32, stream=0, tile=9) == ts.TS_ERR_INVALID_ARG
+    assert ts.ts_gemm_bf16_ptr(0, 0, 0, 4, 4, 8, ts.TS_OUT_F32, stream=0, lda=4) == ts.TS_ERR_INVALID_ARG
+    assert ts.ts_copy_i16_ptr(0, 0, -3, stream=0) == ts.TS_ERR_INVALID_ARG
+    assert ts.ts_copy_i16_ptr(0, 0, 0, stream=0) == ts.TS_OK
+    assert ts.ts_copy_i16_ptr(4096, 4100, 8, stream=0) == ts.TS_ERR_INVALID_ARG  # overlap
+    assert ts.ts_copy_i16_ptr(4096, 4096, 8, stream=0) == ts.TS_OK  # src == dst is a no-op
+
+
+def test_header_is_plain_c():
+    # compiles as C99 with no CUDA or torch headers on the include path
+    import subprocess
+    import tempfile
+
+    with tempfile.TemporaryDirectory() as d:
+        c = os.path.join(d, "t.c")
+        with open(c, "w") as f:
+            f.write('#include "tsgemm.h"\nint main(void){ ts_gemm_opts o = {0}; (void)o; return 0; }\n')
+        r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), "-c", c,
+                            "-o", os.path.join(d, "t.o")], capture_output=True, text=True)
+        assert r.returncode == 0, r.stderr

@@ -1,0 +1,222 @@
+"""GPU parity of ts_gemm_bf16 against the CPU oracle (called through the C ABI).
+
+Random inputs must satisfy the error bound in tests/parity.py; integer-valued,
+identity and one-hot inputs must match bit for bit.  Sizes small enough for the
+triple-loop oracle span several tiles and a ragged tail; the full-size
+workloads are checked against the oracle's BLAS route (whole output) or on
+sampled rows.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from parity import as_f64, assert_bit_exact, assert_within_bound, bf16_bits, to_device_bf16
+
+pytestmark = pytest.mark.gpu
+
+TILES = ["128x128", "128x256", "256x256"]
+SCHEDS = ["static", "clc"]
+OUTS = [torch.float32, torch.bfloat16]
+
+
+def _run(ts, A_bits, B_bits, out, **kw):
+    A = to_device_bf16(A_bits)
+    B = to_device_bf16(B_bits)
+    D = torch.full((A.shape[0], B.shape[0]), float("nan"), dtype=out, device="cuda")
+    ts.ts_gemm_bf16_ex(A, B, D, **kw)
+    ts.ts_sync_and_check()
+    return D
+
+
+# -------------------------------------------------------------- workload 0
+def test_gemm_256_fp32_static_128x128(lib):
+    w = synth.GEMM_256
+    A, B = w.inputs()
+    info = lib.ts_gemm_launch_info(w.M, w.N, w.K, lib.TS_OUT_F32, "static", tile="128x128")
+    assert info["num_tiles"] == 4 and info["workers"] == 4 and info["grid_ctas"] == 4
+    D = _run(lib, A, B, torch.float32, sched="static", tile="128x128")
+    ref = oracle.gemm_f64(A, B)
+    S = oracle.gemm_f64(A, B, absolute=True)
+    assert_within_bound(as_f64(D), ref, S, torch.float32, "256^3")
+
+
+# ------------------------------------------------------ exact-value cases
+@pytest.mark.parametrize("tile", TILES)
+@pytest.mark.parametrize("sched", SCHEDS)
+@pytest.mark.parametrize("out", OUTS)
+def test_gemm_integer_bit_exact(lib, tile, sched, out):
+    M, N, K = 600, 520, 328  # ragged in M, N and K
+    A = synth.int_uniform_bf16(101, (M, K))
+    B = synth.int_uniform_bf16(102, (N, K))
+    D = _run(lib, A, B, out, sched=sched, tile=tile)
+    assert_bit_exact(D, oracle.gemm_f64(A, B), f"integer {tile} {sched}")
+
+
+@pytest.mark.parametrize("tile", TILES)
+@pytest.mark.parametrize("sched", SCHEDS)
+def test_gemm_one_hot_selects_columns(lib, tile, sched):
+    M, N, K = 300, 270, 200
+    rng = np.random.default_rng(3)
+    cols = rng.integers(0, K, size=N)
+    A = synth.uniform_pm1_bf16(111, (M, K))
+    B = synth.one_hot_rows_bf16(N, K, cols)
+    D = _run(lib, A, B, torch.bfloat16, sched=sched, tile=tile)
+    assert np.array_equal(bf16_bits(D), A[:, cols])
+
+
+@pytest.mark.parametrize("tile", TILES)
+def test_gemm_identity_returns_a(lib, tile):
+    M, K = 257, 192
+    A = synth.uniform_pm1_bf16(121, (M, K))
+    B = synth.one_hot_rows_bf16(K, K, np.arange(K))
+    D = _run(lib, A, B, torch.float32, sched="static", tile=tile)
+    assert np.array_equal(as_f64(D), oracle.bf16_to_f64(A))
+
+
+# ---------------------------------------------------------- random inputs
+@pytest.mark.parametrize("M,N,K", [(1, 1, 8), (127, 129, 64), (129, 127, 72), (255, 255, 200), (1, 255, 8),
+                                   (255, 1, 136), (384, 640, 1024)])
+@pytest.mark.parametrize("tile", TILES)
+def test_gemm_small_odd_shapes(lib, M, N, K, tile):
+    A = synth.uniform_pm1_bf16(131 + M, (M, K))
+    B = synth.uniform_pm1_bf16(231 + N, (N, K))
+    ref = oracle.gemm_f64(A, B)
+    S = oracle.gemm_f64(A, B, absolute=True)
+    for sched in SCHEDS:
+        for out in OUTS:
+            D = _run(lib, A, B, out, sched=sched, tile=tile)
+            assert_within_bound(as_f64(D), ref, S, out, f"{M}x{N}x{K} {tile} {sched} {out}")
+
+
+@pytest.mark.parametrize("tile", TILES)
+def test_gemm_strided_operands(lib, tile):
+    M, N, K = 300, 200, 136
+    Af = synth.uniform_pm1_bf16(141, (M, K + 24))
+    Bf = synth.uniform_pm1_bf16(142, (N, K + 40))
+    A = to_device_bf16(Af)[:, :K]
+    B = to_device_bf16(Bf)[:, :K]
+    Dfull = torch.zeros((M, N + 8), dtype=torch.float32, device="cuda")
+    D = Dfull[:, :N]
+    lib.ts_gemm_bf16_ex(A, B, D, sched="clc", tile=tile)
+    lib.ts_sync_and_check()
+    ref = oracle.gemm_f64(np.ascontiguousarray(Af[:, :K]), np.ascontiguousarray(Bf[:, :K]))
+    S = oracle.gemm_f64(np.ascontiguousarray(Af[:, :K]), np.ascontiguousarray(Bf[:, :K]), absolute=True)
+    assert_within_bound(as_f64(D), ref, S, torch.float32, "strided")
+    assert torch.all(Dfull[:, N:] == 0)
+
+
+@pytest.mark.parametrize("out", OUTS)
+@pytest.mark.parametrize("tile", TILES)
+def test_gemm_guard_regions_untouched(lib, out, tile):
+    # D lives inside a larger buffer; rows/columns around it hold a sentinel
+    M, N, K = 200, 300, 64
+    A = synth.int_uniform_bf16(151, (M, K))
+    B = synth.int_uniform_bf16(152, (N, K))
+    for pitch_pad in (0, 8, 3):  # 3 makes the pitch unaligned -> plain-store epilogue
+        big = torch.full((M + 64, N + 64 + pitch_pad), 3072.0, dtype=out, device="cuda")
+        D = big[32:32 + M, 32:32 + N]
+        lib.ts_gemm_bf16_ex(to_device_bf16(A), to_device_bf16(B), D, sched="static", tile=tile)
+        lib.ts_sync_and_check()
+        assert_bit_exact(D, oracle.gemm_f64(A, B), f"guard pad={pitch_pad}")
+        mask = torch.ones_like(big, dtype=torch.bool)
+        mask[32:32 + M, 32:32 + N] = False
+        assert torch.all(big[mask] == 3072.0), f"write outside D (pad={pitch_pad})"
+
+
+def test_gemm_unaligned_pitch_fp32_contiguous(lib):
+    # fp32 with N = 6143-like odd width: pitch not a multiple of 16 bytes
+    M, N, K = 130, 131, 64
+    info = lib.ts_gemm_launch_info(M, N, K, lib.TS_OUT_F32, "static", tile="128x256")
+    assert info["tma_store"] == 0
+    A = synth.uniform_pm1_bf16(161, (M, K))
+    B = synth.uniform_pm1_bf16(162, (N, K))
+    D = _run(lib, A, B, torch.float32, sched="clc", tile="128x256")
+    assert_within_bound(as_f64(D), oracle.gemm_f64(A, B), oracle.gemm_f64(A, B, absolute=True), torch.float32,
+                        "odd pitch")
+
+
+# ----------------------------------------------------------- edge cases
+def test_gemm_k_zero_fills_zero(lib):
+    A = torch.empty((0,), dtype=torch.bfloat16, device="cuda")
+    for out in OUTS:
+        D = torch.full((70, 90), 7.0, dtype=out, device="cuda")
+        st = lib.ts_gemm_bf16_ptr(A.data_ptr(), A.data_ptr(), D.data_ptr(), 70, 90, 0,
+                                  lib.TS_OUT_F32 if out == torch.float32 else lib.TS_OUT_BF16)
+        assert st == lib.TS_OK
+        lib.ts_sync_and_check()
+        assert torch.all(D == 0)
+
+
+def test_gemm_empty_m_or_n_is_noop(lib):
+    D = torch.full((4, 4), 3.0, device="cuda")
+    assert lib.ts_gemm_bf16_ptr(0, 0, D.data_ptr(), 0, 4, 64, lib.TS_OUT_F32) == lib.TS_OK
+    assert lib.ts_gemm_bf16_ptr(0, 0, D.data_ptr(), 4, 0, 64, lib.TS_OUT_F32) == lib.TS_OK
+    lib.ts_sync_and_check()
+    assert torch.all(D == 3.0)
+
+
+def test_gemm_rejects_unaligned_rows(lib):
+    A = torch.zeros((64, 12), dtype=torch.bfloat16, device="cuda")  # 24-byte rows
+    B = torch.zeros((64, 12), dtype=torch.bfloat16, device="cuda")
+    D = torch.zeros((64, 64), device="cuda")
+    with pytest.raises(lib.TsError) as e:
+        lib.ts_gemm_bf16(A, B, D)
+    assert e.value.status == lib.TS_ERR_UNSUPPORTED
+
+
+def test_gemm_rejects_overlap(lib):
+    buf = torch.zeros((256, 256), dtype=torch.bfloat16, device="cuda")
+    st = lib.ts_gemm_bf16_ptr(buf.data_ptr(), buf.data_ptr(), buf.data_ptr() + 512, 64, 64, 64, lib.TS_OUT_BF16)
+    assert st == lib.TS_ERR_INVALID_ARG
+
+
+# ----------------------------------------------------- full-size workloads
+@pytest.mark.slow
+@pytest.mark.parametrize("sched", SCHEDS)
+def test_gemm_4096_bf16_128x256(lib, sched):
+    w = synth.GEMM_4096
+    A, B = w.inputs()
+    D = _run(lib, A, B, torch.bfloat16, sched=sched, tile="128x256")
+    ref = oracle.gemm_f64_blas(A, B)
+    S = oracle.gemm_f64_blas(A, B, absolute=True)
+    assert_within_bound(as_f64(D), ref, S, torch.bfloat16, f"4096^3 {sched}")
+
+
+@pytest.mark.slow
+def test_gemm_8192_bf16_2cta_clc_sampled_rows(lib):
+    w = synth.GEMM_8192
+    A, B = w.inputs()
+    D = _run(lib, A, B, torch.bfloat16, sched="clc", tile="256x256")
+    rng = np.random.default_rng(8192)
+    rows = np.unique(np.concatenate([rng.integers(0, w.M, 96), [0, 255, 256, w.M - 1]]))
+    a = oracle.bf16_to_f64(A[rows])
+    b = oracle.bf16_to_f64(B)
+    ref = a @ b.T
+    S = np.abs(a) @ np.abs(b).T
+    got = oracle.bf16_to_f64(bf16_bits(D[torch.as_tensor(rows, device="cuda")]))
+    assert_within_bound(got, ref, S, torch.bfloat16, "8192^3 sampled rows")
+    # every tile column/row block is exercised by the sampled rows' full width; add sampled columns too
+    cols = rng.integers(0, w.N, 64)
+    ii = rng.integers(0, w.M, 64)
+    e, ea = oracle.gemm_entries_f64(A, B, ii, cols)
+    got2 = oracle.bf16_to_f64(bf16_bits(D[torch.as_tensor(ii, device="cuda"), torch.as_tensor(cols, device="cuda")]))
+    assert_within_bound(got2, e, ea, torch.bfloat16, "8192^3 sampled entries")
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("sched", SCHEDS)
+@pytest.mark.parametrize("pitch", [6144, 6143])
+def test_gemm_ragged_fp32(lib, sched, pitch):
+    w = synth.GEMM_RAGGED
+    A, B = w.inputs()
+    Dbuf = torch.full((w.M, pitch), float("nan"), dtype=torch.float32, device="cuda")
+    D = Dbuf[:, :w.N]
+    lib.ts_gemm_bf16_ex(to_device_bf16(A), to_device_bf16(B), D, sched=sched)
+    lib.ts_sync_and_check()
+    ref = oracle.gemm_f64_blas(A, B)
+    S = oracle.gemm_f64_blas(A, B, absolute=True)
+    assert_within_bound(as_f64(D), ref, S, torch.float32, f"ragged {sched} pitch {pitch}")
+    if pitch > w.N:
+        assert torch.isnan(Dbuf[:, w.N:]).all()

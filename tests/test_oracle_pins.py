@@ -44,6 +44,10 @@ def test_splitmix64_published_first_output():
     assert int(synth.splitmix64(0, 1)[0]) == 0xE220A8397B1DCDAF
 
 
+def test_c_generator_matches_numpy_reference_form():
+    assert np.array_equal(synth.splitmix64(5, 1000, offset=37), synth.splitmix64_fast(5, 1000, offset=37))
+
+
 def test_uniform_range_and_exactness():
     a = synth.uniform_pm1_bf16(7, (64, 64))
     v = oracle.bf16_to_f64(a)

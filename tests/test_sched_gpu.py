@@ -1,0 +1,98 @@
+"""Tile-scheduler coverage on the GPU, from the kernel's per-tile trace.
+
+Static: the owner of every tile is the one the grid-stride rule gives
+(oracle.static_owner, pinned by the 12-tile / 4-worker worked example).
+Cluster Launch Control: every tile is visited exactly once, and every worker
+that ran started on the tile of its own block index; results stay identical
+while part of the GPU is held by another kernel.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from parity import assert_bit_exact, to_device_bf16
+
+pytestmark = pytest.mark.gpu
+
+
+def _traced(lib, A_bits, B_bits, out, tile, sched, **kw):
+    M, N = A_bits.shape[0], B_bits.shape[0]
+    info = lib.ts_gemm_launch_info(M, N, A_bits.shape[1], lib.TS_OUT_F32 if out == torch.float32 else lib.TS_OUT_BF16,
+                                   sched, tile=tile, **kw)
+    trace = torch.zeros(4 * info["num_tiles"], dtype=torch.int64, device="cuda")
+    D = torch.full((M, N), float("nan"), dtype=out, device="cuda")
+    lib.ts_gemm_bf16_ex(to_device_bf16(A_bits), to_device_bf16(B_bits), D, sched=sched, tile=tile, trace=trace,
+                        **kw)
+    lib.ts_sync_and_check()
+    return info, trace.view(-1, 4).cpu().numpy(), D
+
+
+@pytest.mark.parametrize("tile", ["128x128", "128x256", "256x256"])
+@pytest.mark.parametrize("max_workers", [0, 7, 1])
+def test_static_owner_follows_grid_stride_rule(lib, tile, max_workers):
+    M, N, K = 1500, 1300, 128
+    A = synth.int_uniform_bf16(301, (M, K))
+    B = synth.int_uniform_bf16(302, (N, K))
+    info, tr, D = _traced(lib, A, B, torch.float32, tile, "static", max_workers=max_workers)
+    if max_workers:
+        assert info["workers"] == min(max_workers, info["num_tiles"])
+    assert np.all(tr[:, 0] == 1), "a tile was not visited exactly once"
+    assert np.array_equal(tr[:, 1], oracle.static_owner(info["num_tiles"], info["workers"]))
+    assert np.all(tr[:, 3] >= tr[:, 2])
+    assert_bit_exact(D, oracle.gemm_f64(A, B), f"static {tile}")
+
+
+@pytest.mark.parametrize("tile", ["128x128", "128x256", "256x256"])
+def test_clc_covers_every_tile_once(lib, tile):
+    M, N, K = 4000, 3000, 64  # many more tiles than resident workers
+    A = synth.int_uniform_bf16(311, (M, K))
+    B = synth.int_uniform_bf16(312, (N, K))
+    info, tr, D = _traced(lib, A, B, torch.bfloat16, tile, "clc")
+    assert info["grid_ctas"] == info["num_tiles"] * info["cluster"]
+    ok, why = oracle.clc_coverage_ok(tr[:, 0], tr[:, 1])
+    assert ok, why
+    # work stealing happened: fewer workers ran than there are tiles
+    assert np.unique(tr[:, 1]).size < info["num_tiles"]
+    ref = oracle.gemm_f64_blas(A, B)
+    assert_bit_exact(D, ref, f"clc {tile}")
+
+
+@pytest.mark.parametrize("sched", ["static", "clc"])
+def test_results_identical_while_sms_are_held(lib, sched):
+    M, N, K = 2048, 2048, 1024
+    A = synth.int_uniform_bf16(321, (M, K))
+    B = synth.int_uniform_bf16(322, (N, K))
+    ref = oracle.gemm_f64_blas(A, B)
+    Ad, Bd = to_device_bf16(A), to_device_bf16(B)
+    side = torch.cuda.Stream()
+    started = torch.zeros(1, dtype=torch.int32).pin_memory()
+    ctas = 32
+    info = lib.ts_gemm_launch_info(M, N, K, lib.TS_OUT_F32, sched, tile="128x256")
+    trace = torch.zeros(4 * info["num_tiles"], dtype=torch.int64, device="cuda")
+    D = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    lib.ts_spin(ctas, 20_000_000, started, stream=side)
+    lib.ts_spin_wait_started(started, ctas, 5.0)
+    lib.ts_gemm_bf16_ex(Ad, Bd, D, sched=sched, tile="128x256", trace=trace)
+    torch.cuda.synchronize()
+    lib.ts_sync_and_check()
+    assert started.item() == ctas
+    assert_bit_exact(D, ref, f"contended {sched}")
+    tr = trace.view(-1, 4).cpu().numpy()
+    if sched == "clc":
+        ok, why = oracle.clc_coverage_ok(tr[:, 0], tr[:, 1])
+        assert ok, why
+    else:
+        assert np.array_equal(tr[:, 1], oracle.static_owner(info["num_tiles"], info["workers"]))
+
+
+def test_spin_rejects_bad_arguments(lib):
+    started = torch.zeros(1, dtype=torch.int32).pin_memory()
+    with pytest.raises(lib.TsError):
+        lib.ts_spin(0, 1000, started)
+    with pytest.raises(lib.TsError):
+        lib.ts_spin(1, -5, started)
+    with pytest.raises(TypeError):
+        lib.ts_spin(1, 1000, torch.zeros(1, dtype=torch.int32))

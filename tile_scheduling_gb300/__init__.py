@@ -1,0 +1,221 @@
+"""Python binding of libtsgemm (persistent bf16 GEMM with static / Cluster Launch
+Control tile scheduling, and the grid-stride int16 copy) for one GB300.
+
+This module only marshals arguments: torch tensors become device pointers and
+sizes, the current torch stream becomes a cudaStream_t, and every computation
+runs in the library's CUDA kernels.  There is no fallback: if the shared
+library is missing or fails to load, importing this package raises.
+
+The C entry points are declared in include/tsgemm.h; the functions here have
+the same names.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libtsgemm.so")
+
+TS_OK, TS_ERR_INVALID_ARG, TS_ERR_UNSUPPORTED, TS_ERR_CUDA, TS_ERR_TIMEOUT = range(5)
+TS_SCHED_STATIC, TS_SCHED_CLC = 0, 1
+TS_OUT_BF16, TS_OUT_F32 = 0, 1
+TS_TILE_AUTO, TS_TILE_128x128, TS_TILE_128x256, TS_TILE_256x256_2CTA = range(4)
+
+_SCHED = {"static": TS_SCHED_STATIC, "clc": TS_SCHED_CLC}
+_TILE = {"auto": TS_TILE_AUTO, "128x128": TS_TILE_128x128, "128x256": TS_TILE_128x256,
+         "256x256": TS_TILE_256x256_2CTA}
+_OUT = {torch.bfloat16: TS_OUT_BF16, torch.float32: TS_OUT_F32}
+
+EXPORTED = ("ts_gemm_bf16", "ts_gemm_bf16_ex", "ts_gemm_launch_info", "ts_copy_i16", "ts_spin",
+            "ts_spin_wait_started", "ts_sync_and_check", "ts_num_sms", "ts_status_string",
+            "ts_last_error_detail")
+
+
+class TsError(RuntimeError):
+    def __init__(self, status: int, detail: str):
+        super().__init__(f"{_status_name(status)}: {detail}")
+        self.status = status
+        self.detail = detail
+
+
+class GemmOpts(ctypes.Structure):
+    _fields_ = [("tile", ctypes.c_int32), ("max_workers", ctypes.c_int32), ("lda", ctypes.c_int64),
+                ("ldb", ctypes.c_int64), ("ldd", ctypes.c_int64), ("timeout_s", ctypes.c_double),
+                ("trace", ctypes.c_void_p), ("raster_group", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+class LaunchInfo(ctypes.Structure):
+    _fields_ = [("tile_m", ctypes.c_int32), ("tile_n", ctypes.c_int32), ("cluster", ctypes.c_int32),
+                ("stages", ctypes.c_int32), ("tiles_m", ctypes.c_int64), ("tiles_n", ctypes.c_int64),
+                ("num_tiles", ctypes.c_int64), ("grid_ctas", ctypes.c_int64), ("workers", ctypes.c_int64),
+                ("smem_bytes", ctypes.c_int32), ("tma_store", ctypes.c_int32)]
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    if not os.path.exists(path):
+        raise ImportError(f"libtsgemm.so not built ({path}); run python -m tile_scheduling_gb300.build")
+    lib = ctypes.CDLL(path)
+    P, I32, I64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    lib.ts_gemm_bf16.argtypes = [P, P, P, I64, I64, I64, I32, I32, P]
+    lib.ts_gemm_bf16_ex.argtypes = [P, P, P, I64, I64, I64, I32, I32, ctypes.POINTER(GemmOpts), P]
+    lib.ts_gemm_launch_info.argtypes = [I64, I64, I64, I32, I32, ctypes.POINTER(GemmOpts),
+                                        ctypes.POINTER(LaunchInfo)]
+    lib.ts_copy_i16.argtypes = [P, P, I64, P]
+    lib.ts_spin.argtypes = [I32, I64, P, P]
+    lib.ts_spin_wait_started.argtypes = [P, I32, ctypes.c_double]
+    lib.ts_sync_and_check.argtypes = [P]
+    lib.ts_num_sms.argtypes = []
+    lib.ts_num_sms.restype = I32
+    lib.ts_status_string.argtypes = [ctypes.c_int]
+    lib.ts_status_string.restype = ctypes.c_char_p
+    lib.ts_last_error_detail.argtypes = []
+    lib.ts_last_error_detail.restype = ctypes.c_char_p
+    for name in ("ts_gemm_bf16", "ts_gemm_bf16_ex", "ts_gemm_launch_info", "ts_copy_i16", "ts_spin",
+                 "ts_spin_wait_started", "ts_sync_and_check"):
+        getattr(lib, name).restype = ctypes.c_int
+    return lib
+
+
+_lib = load_library()
+
+
+def _status_name(s: int) -> str:
+    return _lib.ts_status_string(s).decode()
+
+
+def _check(status: int) -> None:
+    if status != TS_OK:
+        raise TsError(status, _lib.ts_last_error_detail().decode())
+
+
+def _stream_handle(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _sched(s) -> int:
+    return _SCHED[s] if isinstance(s, str) else int(s)
+
+
+def _opts(tile="auto", max_workers=0, lda=0, ldb=0, ldd=0, timeout_s=0.0, trace=None, raster_group=0):
+    o = GemmOpts()
+    o.tile = _TILE[tile] if isinstance(tile, str) else int(tile)
+    o.max_workers = int(max_workers)
+    o.lda, o.ldb, o.ldd = int(lda), int(ldb), int(ldd)
+    o.timeout_s = float(timeout_s)
+    if trace is not None:
+        if trace.dtype != torch.int64 or not trace.is_cuda or not trace.is_contiguous():
+            raise TypeError("trace must be a contiguous int64 CUDA tensor")
+        o.trace = trace.data_ptr()
+    o.raster_group = int(raster_group)
+    return o
+
+
+def _matrix(t: torch.Tensor, name: str, dtype) -> int:
+    if not isinstance(t, torch.Tensor) or t.dtype != dtype:
+        raise TypeError(f"{name} must be a {dtype} tensor")
+    if not t.is_cuda:
+        raise TypeError(f"{name} must be on a CUDA device")
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError(f"{name} must be 2-D with unit column stride")
+    return t.stride(0)
+
+
+def _gemm_args(A, B, D):
+    lda = _matrix(A, "A", torch.bfloat16)
+    ldb = _matrix(B, "B", torch.bfloat16)
+    if D.dtype not in _OUT:
+        raise TypeError("D must be bfloat16 or float32")
+    ldd = _matrix(D, "D", D.dtype)
+    M, K = A.shape
+    N, K2 = B.shape
+    if K2 != K or tuple(D.shape) != (M, N):
+        raise ValueError(f"shape mismatch: A {tuple(A.shape)}, B {tuple(B.shape)}, D {tuple(D.shape)}")
+    return M, N, K, lda, ldb, ldd
+
+
+def ts_gemm_bf16_ex(A: torch.Tensor, B: torch.Tensor, D: torch.Tensor, sched="static", tile="auto",
+                    max_workers=0, timeout_s=0.0, trace=None, raster_group=0, stream=None) -> None:
+    """D = A @ B.T for bf16 A [M, K] and B [N, K]; D [M, N] is bf16 or fp32.
+
+    Rows may be strided (the row stride becomes lda / ldb / ldd).  Asynchronous
+    on ``stream`` (default: torch's current stream)."""
+    M, N, K, lda, ldb, ldd = _gemm_args(A, B, D)
+    o = _opts(tile, max_workers, lda if M > 1 else 0, ldb if N > 1 else 0, ldd if M > 1 else 0, timeout_s, trace,
+              raster_group)
+    _check(_lib.ts_gemm_bf16_ex(ctypes.c_void_p(A.data_ptr()), ctypes.c_void_p(B.data_ptr()),
+                                ctypes.c_void_p(D.data_ptr()), M, N, K, _OUT[D.dtype], _sched(sched),
+                                ctypes.byref(o), _stream_handle(stream)))
+
+
+def ts_gemm_bf16(A: torch.Tensor, B: torch.Tensor, D: torch.Tensor, sched="static", stream=None) -> None:
+    """D = A @ B.T with the default tile choice; all three tensors contiguous."""
+    M, N, K, lda, ldb, ldd = _gemm_args(A, B, D)
+    if (M > 1 and (lda != K or ldd != N)) or (N > 1 and ldb != K):
+        raise ValueError("ts_gemm_bf16 takes dense rows; use ts_gemm_bf16_ex for strided ones")
+    _check(_lib.ts_gemm_bf16(ctypes.c_void_p(A.data_ptr()), ctypes.c_void_p(B.data_ptr()),
+                             ctypes.c_void_p(D.data_ptr()), M, N, K, _OUT[D.dtype], _sched(sched),
+                             _stream_handle(stream)))
+
+
+def ts_gemm_bf16_ptr(A: int, B: int, D: int, M: int, N: int, K: int, out: int, sched=0, stream=None,
+                     **opts) -> int:
+    """Raw-pointer call of ts_gemm_bf16_ex; returns the status without raising."""
+    o = _opts(**opts)
+    return _lib.ts_gemm_bf16_ex(ctypes.c_void_p(A), ctypes.c_void_p(B), ctypes.c_void_p(D), M, N, K, out,
+                                _sched(sched), ctypes.byref(o), _stream_handle(stream))
+
+
+def ts_gemm_launch_info(M: int, N: int, K: int, out=TS_OUT_BF16, sched="static", **opts) -> dict:
+    o = _opts(**opts)
+    info = LaunchInfo()
+    _check(_lib.ts_gemm_launch_info(M, N, K, int(out), _sched(sched), ctypes.byref(o), ctypes.byref(info)))
+    return {f: getattr(info, f) for f, _ in LaunchInfo._fields_}
+
+
+def ts_copy_i16(src: torch.Tensor, dst: torch.Tensor, stream=None) -> None:
+    """dst[i] = src[i] for contiguous int16 CUDA tensors of equal size."""
+    for t, name in ((src, "src"), (dst, "dst")):
+        if t.dtype != torch.int16 or not t.is_cuda or not t.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous int16 CUDA tensor")
+    if src.numel() != dst.numel():
+        raise ValueError("src and dst differ in size")
+    _check(_lib.ts_copy_i16(ctypes.c_void_p(src.data_ptr()), ctypes.c_void_p(dst.data_ptr()), src.numel(),
+                            _stream_handle(stream)))
+
+
+def ts_copy_i16_ptr(src: int, dst: int, n: int, stream=None) -> int:
+    return _lib.ts_copy_i16(ctypes.c_void_p(src), ctypes.c_void_p(dst), n, _stream_handle(stream))
+
+
+def ts_spin(ctas: int, duration_ns: int, started: torch.Tensor, stream=None) -> None:
+    """Hold ``ctas`` SMs for ``duration_ns``; ``started`` is a pinned int32 host tensor."""
+    if started.dtype != torch.int32 or started.is_cuda or not started.is_pinned():
+        raise TypeError("started must be a pinned int32 CPU tensor")
+    _check(_lib.ts_spin(int(ctas), int(duration_ns), ctypes.c_void_p(started.data_ptr()), _stream_handle(stream)))
+
+
+def ts_spin_wait_started(started: torch.Tensor, expected: int, timeout_s: float = 5.0) -> None:
+    _check(_lib.ts_spin_wait_started(ctypes.c_void_p(started.data_ptr()), int(expected), float(timeout_s)))
+
+
+def ts_sync_and_check(stream=None) -> None:
+    _check(_lib.ts_sync_and_check(_stream_handle(stream)))
+
+
+def ts_num_sms() -> int:
+    return int(_lib.ts_num_sms())
+
+
+def ts_status_string(s: int) -> str:
+    return _status_name(s)
+
+
+def ts_last_error_detail() -> str:
+    return _lib.ts_last_error_detail().decode()

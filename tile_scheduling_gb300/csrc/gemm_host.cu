@@ -1,0 +1,268 @@
+// Host side of ts_gemm_bf16: argument checks, tile/grid planning, TMA tensor
+// maps, and the launch.  The scheduler choice only changes the grid: a static
+// persistent grid of resident workers, or (Cluster Launch Control) one block or
+// cluster per tile, whose coordinate i is tile i.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+
+#include "common.h"
+
+namespace ts {
+
+extern const GemmVariant variant_128_1_bf16, variant_128_1_f32, variant_256_1_bf16, variant_256_1_f32,
+    variant_256_2_bf16, variant_256_2_f32;
+
+const GemmVariant *find_variant(int bn, int cg, int out) {
+    static const GemmVariant *const all[] = {&variant_128_1_bf16, &variant_128_1_f32, &variant_256_1_bf16,
+                                             &variant_256_1_f32,  &variant_256_2_bf16, &variant_256_2_f32};
+    for (const GemmVariant *v : all)
+        if (v->bn == bn && v->cg == cg && v->out == out) return v;
+    return nullptr;
+}
+
+namespace {
+
+constexpr int64_t kMaxDim = 0x7fffffffLL;
+constexpr double kDefaultTimeoutS = 2.0;
+constexpr uint64_t kDrainNs = 200ull * 1000 * 1000;
+constexpr int kDefaultRaster = 8;
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn(ts_status *err) {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static cudaError_t got = cudaSuccess;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        got = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
+        if (got == cudaSuccess && q == cudaDriverEntryPointSuccess) fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    if (!fn) *err = got != cudaSuccess ? cuda_fail(got, "cuTensorMapEncodeTiled lookup")
+                                       : fail(TS_ERR_CUDA, "cuTensorMapEncodeTiled not available from the driver");
+    return fn;
+}
+
+// 2-D row-major tensor [rows][cols] with row pitch `ld` elements, copied in
+// boxes of box_rows x box_cols with the 128-byte swizzle.  Out-of-range
+// elements of a load read as zero; a store is clipped to the tensor.
+ts_status make_map(CUtensorMap *m, const void *ptr, CUtensorMapDataType dt, int esize, int64_t rows, int64_t cols,
+                   int64_t ld, int box_rows, int box_cols) {
+    ts_status err = TS_OK;
+    auto fn = encode_fn(&err);
+    if (!fn) return err;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * esize)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, dt, 2, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(TS_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled failed (%d) for a %lld x %lld tensor, pitch %lld B",
+                    static_cast<int>(r), static_cast<long long>(rows), static_cast<long long>(cols),
+                    static_cast<long long>(ld * esize));
+    return TS_OK;
+}
+
+template <class T>
+__global__ void zero_fill_kernel(T *D, int64_t M, int64_t N, int64_t ldd) {
+    const int64_t total = M * N;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t r = i / N, c = i - r * N;
+        D[r * ldd + c] = T(0);
+    }
+}
+
+bool ranges_overlap(const void *a, int64_t abytes, const void *b, int64_t bbytes) {
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + static_cast<uintptr_t>(bbytes) && b0 < a0 + static_cast<uintptr_t>(abytes);
+}
+
+struct Plan {
+    const GemmVariant *v;
+    int tile_m, tile_n, cg;
+    int64_t tiles_m, tiles_n, num_tiles, workers, grid;
+    int64_t lda, ldb, ldd;
+    int tma_store;
+};
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+ts_status plan_gemm(const void *D, int64_t M, int64_t N, int64_t K, int32_t out, int32_t sched,
+                    const ts_gemm_opts *o, Plan *pl) {
+    if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+        return fail(TS_ERR_INVALID_ARG, "sizes must be in [0, 2^31-1] (M=%lld N=%lld K=%lld)",
+                    static_cast<long long>(M), static_cast<long long>(N), static_cast<long long>(K));
+    if (out != TS_OUT_BF16 && out != TS_OUT_F32) return fail(TS_ERR_INVALID_ARG, "out_dtype %d", out);
+    if (sched != TS_SCHED_STATIC && sched != TS_SCHED_CLC) return fail(TS_ERR_INVALID_ARG, "sched %d", sched);
+    ts_gemm_opts z;
+    std::memset(&z, 0, sizeof z);
+    if (!o) o = &z;
+    if (o->tile < TS_TILE_AUTO || o->tile > TS_TILE_256x256_2CTA) return fail(TS_ERR_INVALID_ARG, "tile %d", o->tile);
+    if (o->max_workers < 0 || o->raster_group < 0 || o->timeout_s < 0)
+        return fail(TS_ERR_INVALID_ARG, "negative option");
+    pl->lda = o->lda ? o->lda : K;
+    pl->ldb = o->ldb ? o->ldb : K;
+    pl->ldd = o->ldd ? o->ldd : N;
+    if (pl->lda < K || pl->ldb < K || pl->ldd < N || pl->lda > (int64_t(1) << 38) || pl->ldb > (int64_t(1) << 38) ||
+        pl->ldd > (int64_t(1) << 37))
+        return fail(TS_ERR_INVALID_ARG, "leading dimensions must cover a row (lda=%lld ldb=%lld ldd=%lld)",
+                    static_cast<long long>(pl->lda), static_cast<long long>(pl->ldb),
+                    static_cast<long long>(pl->ldd));
+
+    const int dev = current_device();
+    const int sms = device_sms(dev);
+    if (sms <= 0) return fail(TS_ERR_CUDA, "cannot query the SM count");
+    int tile = o->tile;
+    if (tile == TS_TILE_AUTO) {
+        // Largest tile that still gives every SM work: the 2-CTA tile halves
+        // each SM's share of B traffic, the 128x128 tile suits small outputs.
+        const int64_t t256 = cdiv(M, 256) * cdiv(N, 256);
+        const int64_t t128x256 = cdiv(M, 128) * cdiv(N, 256);
+        if (t256 * 2 >= sms)
+            tile = TS_TILE_256x256_2CTA;
+        else if (t128x256 >= sms)
+            tile = TS_TILE_128x256;
+        else
+            tile = TS_TILE_128x128;
+    }
+    int bn = 256, cg = 1;
+    if (tile == TS_TILE_128x128) bn = 128;
+    if (tile == TS_TILE_256x256_2CTA) cg = 2;
+    pl->v = find_variant(bn, cg, out);
+    if (!pl->v) return fail(TS_ERR_UNSUPPORTED, "no compiled variant for tile %d", tile);
+    pl->cg = cg;
+    pl->tile_m = 128 * cg;
+    pl->tile_n = bn;
+    pl->tiles_m = cdiv(M, pl->tile_m);
+    pl->tiles_n = cdiv(N, pl->tile_n);
+    pl->num_tiles = pl->tiles_m * pl->tiles_n;
+    if (pl->num_tiles * cg > kMaxDim) return fail(TS_ERR_UNSUPPORTED, "too many output tiles");
+    if (sched == TS_SCHED_CLC) {
+        pl->workers = pl->num_tiles;
+    } else {
+        int resident = 0;
+        cudaError_t e = pl->v->max_workers(&resident);
+        if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
+        if (resident <= 0) return fail(TS_ERR_UNSUPPORTED, "kernel cannot be resident on this device");
+        int64_t w = std::min<int64_t>(pl->num_tiles, resident);
+        if (o->max_workers > 0) w = std::min<int64_t>(w, o->max_workers);
+        pl->workers = std::max<int64_t>(w, pl->num_tiles > 0 ? 1 : 0);
+    }
+    pl->grid = pl->workers * cg;
+    const int esize = out == TS_OUT_F32 ? 4 : 2;
+    pl->tma_store = (reinterpret_cast<uintptr_t>(D) % 16 == 0) && ((pl->ldd * esize) % 16 == 0);
+    return TS_OK;
+}
+
+}  // namespace
+}  // namespace ts
+
+extern "C" {
+
+ts_status ts_gemm_launch_info(int64_t M, int64_t N, int64_t K, int32_t out_dtype, int32_t sched,
+                              const ts_gemm_opts *opts, ts_launch_info *info) {
+    if (!info) return ts::fail(TS_ERR_INVALID_ARG, "info is NULL");
+    ts::Plan pl;
+    // alignment of D is unknown here: report the TMA-store epilogue when the pitch allows it
+    ts_status s = ts::plan_gemm(reinterpret_cast<const void *>(uintptr_t(256)), M, N, K, out_dtype, sched, opts, &pl);
+    if (s != TS_OK) return s;
+    info->tile_m = pl.tile_m;
+    info->tile_n = pl.tile_n;
+    info->cluster = pl.cg;
+    info->stages = pl.v->stages;
+    info->tiles_m = pl.tiles_m;
+    info->tiles_n = pl.tiles_n;
+    info->num_tiles = pl.num_tiles;
+    info->grid_ctas = pl.grid;
+    info->workers = pl.workers;
+    info->smem_bytes = pl.v->smem_bytes;
+    info->tma_store = pl.tma_store;
+    return TS_OK;
+}
+
+ts_status ts_gemm_bf16_ex(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K, int32_t out_dtype,
+                          int32_t sched, const ts_gemm_opts *opts, void *stream) {
+    using namespace ts;
+    Plan pl;
+    ts_status s = plan_gemm(D, M, N, K, out_dtype, sched, opts, &pl);
+    if (s != TS_OK) return s;
+    if (M == 0 || N == 0) return TS_OK;
+    if (!D) return fail(TS_ERR_INVALID_ARG, "D is NULL");
+    const int esize = out_dtype == TS_OUT_F32 ? 4 : 2;
+    if (reinterpret_cast<uintptr_t>(D) % esize) return fail(TS_ERR_INVALID_ARG, "D is not aligned to its element size");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int64_t dbytes = ((M - 1) * pl.ldd + N) * esize;
+
+    if (K == 0) {
+        const int64_t total = M * N;
+        const int blocks = static_cast<int>(std::min<int64_t>(cdiv(total, 256), 4096));
+        if (out_dtype == TS_OUT_F32)
+            zero_fill_kernel<float><<<blocks, 256, 0, st>>>(static_cast<float *>(D), M, N, pl.ldd);
+        else
+            zero_fill_kernel<uint16_t><<<blocks, 256, 0, st>>>(static_cast<uint16_t *>(D), M, N, pl.ldd);
+        cudaError_t e = cudaGetLastError();
+        return e == cudaSuccess ? TS_OK : cuda_fail(e, "zero-fill launch");
+    }
+    if (!A || !B) return fail(TS_ERR_INVALID_ARG, "A or B is NULL");
+    if (reinterpret_cast<uintptr_t>(A) % 16 || reinterpret_cast<uintptr_t>(B) % 16)
+        return fail(TS_ERR_UNSUPPORTED, "A and B must start on a 16-byte boundary");
+    if ((pl.lda * 2) % 16 || (pl.ldb * 2) % 16)
+        return fail(TS_ERR_UNSUPPORTED, "rows of A and B must start on 16-byte boundaries (lda, ldb multiples of 8)");
+    const int64_t abytes = ((M - 1) * pl.lda + K) * 2, bbytes = ((N - 1) * pl.ldb + K) * 2;
+    if (ranges_overlap(D, dbytes, A, abytes) || ranges_overlap(D, dbytes, B, bbytes))
+        return fail(TS_ERR_INVALID_ARG, "D overlaps A or B");
+
+    ts_gemm_opts z;
+    std::memset(&z, 0, sizeof z);
+    const ts_gemm_opts *o = opts ? opts : &z;
+
+    GemmLaunch L;
+    std::memset(&L, 0, sizeof L);
+    const int b_rows = pl.tile_n / pl.cg;
+    if ((s = make_map(&L.a, A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, M, K, pl.lda, 128, 64)) != TS_OK) return s;
+    if ((s = make_map(&L.b, B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, N, K, pl.ldb, b_rows, 64)) != TS_OK) return s;
+    if (pl.tma_store) {
+        const CUtensorMapDataType dt =
+            out_dtype == TS_OUT_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+        if ((s = make_map(&L.d, D, dt, esize, M, N, pl.ldd, 32, 128 / esize)) != TS_OK) return s;
+    }
+    unsigned long long *status = device_status_word(&s);
+    if (!status) return s;
+
+    GemmParams &p = L.p;
+    p.M = static_cast<int32_t>(M);
+    p.N = static_cast<int32_t>(N);
+    p.K = static_cast<int32_t>(K);
+    p.tiles_m = static_cast<int32_t>(pl.tiles_m);
+    p.tiles_n = static_cast<int32_t>(pl.tiles_n);
+    p.num_tiles = static_cast<int32_t>(pl.num_tiles);
+    p.num_k_blocks = static_cast<int32_t>(cdiv(K, 64));
+    p.raster_group = o->raster_group > 0 ? o->raster_group : kDefaultRaster;
+    p.sched = sched;
+    p.tma_store = pl.tma_store;
+    p.clc_depth = 2;
+    p.D = D;
+    p.ldd = pl.ldd;
+    const double tmo = o->timeout_s > 0 ? o->timeout_s : kDefaultTimeoutS;
+    p.timeout_ns = static_cast<uint64_t>(std::min(tmo, 60.0) * 1e9);
+    if (p.timeout_ns == 0) p.timeout_ns = 1;
+    p.drain_ns = kDrainNs;
+    p.status = status;
+    p.trace = reinterpret_cast<long long *>(o->trace);
+    L.grid = static_cast<int>(pl.grid);
+    L.stream = st;
+    cudaError_t e = pl.v->launch(L);
+    if (e != cudaSuccess) return cuda_fail(e, "GEMM launch");
+    return TS_OK;
+}
+
+ts_status ts_gemm_bf16(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K, int32_t out_dtype,
+                       int32_t sched, void *stream) {
+    return ts_gemm_bf16_ex(A, B, D, M, N, K, out_dtype, sched, nullptr, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,515 @@
+// Persistent, warp-specialised bf16 GEMM for sm_103a: D = A * B^T.
+//
+// The mainloop is the Merge example of CUTLASS TS "Pipeline Groups"
+// (Overview): gmem_ab -> smem_a, smem_b -> tmem_c -> gmem_d.  A and B share
+// one "full" and one "empty" mbarrier per ring stage (the FusedMerge layout,
+// 2 * S barriers: one producer thread arrives with the summed transaction
+// bytes of both loads, the single MMA consumer waits and releases once).
+//
+// Warp roles (256 threads, one CTA per SM):
+//   warp 0      TMA producer: per k-block, acquire an empty stage, arm the
+//               full barrier with A+B bytes, issue the two tile loads
+//               (TS "Introduction", Load-A skeleton: compute_coords, acquire,
+//               tma_load_a, commit).
+//   warp 1      TMEM allocator and the single MMA-issuing thread: per k-block,
+//               wait full, 4 x tcgen05.mma (K = 16 each), commit -> empty.
+//               The first MMA of every work tile overwrites the accumulator
+//               (TS "Resources", per-work-tile scale_d reset).
+//   warp 2      Cluster Launch Control scheduler (CLC mode only): fetches the
+//               next tile while the current one is computed ("Cluster Launch
+//               Control", overlap loop; TS "Schedules", dynamic persistent
+//               shape with a dedicated scheduler task).
+//   warp 3      barrier initialisation, then idle.
+//   warps 4-7   epilogue: TMEM -> registers (tcgen05.ld, 32 columns per load)
+//               -> fp32 or bf16 -> swizzled shared staging -> TMA store, one
+//               subtile after another (TS "Resources", subtile epilogue:
+//               load_subtile / store at column coordc_n + subtile_idx * 32,
+//               bracketed by tmem_c.wait() / release()).
+//
+// Every role walks the same tile sequence and advances at the same tile
+// boundary (TS "Schedules", Persistent Scheduling).  Static mode: worker w of
+// W takes tiles w, w + W, ... ("Cluster Launch Control", static persistent
+// scheduler).  CLC mode: the grid covers all tiles, block (cluster) i starts
+// on tile i and then takes the coordinates of launches it cancels.
+//
+// Two accumulators of BN fp32 columns live in TMEM, so the epilogue of one
+// tile overlaps the mainloop of the next.  With CG = 2 a CTA pair computes a
+// 256 x BN tile with cta_group::2 MMAs issued by the even CTA: each CTA loads
+// its own 128 rows of A and BN/2 rows of B, both CTAs' loads complete on the
+// even CTA's full barrier, and commits arrive on both CTAs' barriers.
+//
+// Every mbarrier wait is bounded (%globaltimer): on expiry the kernel records
+// the wait in the device status word, raises a CTA-local abort flag, lets
+// every role leave its loop, waits (with its own limit) for copies and MMAs
+// still in flight, frees TMEM and returns.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "gemm_params.h"
+#include "ptx.cuh"
+
+namespace ts {
+
+constexpr int kThreads = 256;
+constexpr int kSmemLimit = 232448;  // 227 KB: largest opt-in dynamic shared memory per CTA
+constexpr int kMaxClcDepth = 2;
+
+template <int BN_, int CG_, int OUT_>
+struct GemmCfg {
+    static constexpr int BN = BN_, CG = CG_, OUT = OUT_;
+    static constexpr int BM = 128;              // accumulator rows per CTA = TMEM lanes
+    static constexpr int TILE_M = BM * CG;      // output rows per worker
+    static constexpr int BK = 64;               // bf16 per 128-byte swizzle row
+    static constexpr int UMMA_K = 16;
+    static constexpr int B_ROWS = BN / CG;      // rows of B loaded by each CTA
+    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int B_BYTES = B_ROWS * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int TX_BYTES = STAGE_BYTES * CG;  // bytes landing on the even CTA's full barrier
+    static constexpr int OUT_BYTES = OUT == OUT_F32 ? 4 : 2;
+    static constexpr int SUB_COLS = 128 / OUT_BYTES;   // store subtile: 128 bytes of a row
+    static constexpr int NUM_SUB = BN / SUB_COLS;
+    static constexpr int EPI_BUF = 32 * 128;           // one warp: 32 rows x 128 bytes
+    static constexpr int EPI_BYTES = 4 * 2 * EPI_BUF;  // 4 warps, double-buffered
+    static constexpr int TMEM_COLS = 2 * BN;           // two accumulators
+    static constexpr int BAR_BYTES = 256;
+    static constexpr int STAGES = (kSmemLimit - 1024 - EPI_BYTES - BAR_BYTES) / STAGE_BYTES;
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
+    // Consumers of one CLC response: producer, MMA, 4 epilogue warps and the
+    // scheduler in the even CTA; producer, 4 epilogue warps and scheduler in the odd one.
+    static constexpr int CLC_CONSUMERS = CG == 1 ? 7 : 13;
+    // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B bf16
+    // (bits 7-9 = 1, 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at
+    // bits 17-22, M >> 4 at bits 24-28.
+    static constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(BN >> 3) << 17) |
+                                      (uint32_t((BM * CG) >> 4) << 24);
+
+    static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N");
+    static_assert(CG == 1 || CG == 2, "cluster size");
+    static_assert(STAGES >= 2, "ring too shallow");
+    static_assert(SMEM_BYTES <= kSmemLimit, "shared memory budget");
+    static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzle atoms must stay 1024-byte aligned");
+    static_assert(2 * STAGES * 8 + 5 * 8 + 2 * kMaxClcDepth * 8 + 16 * kMaxClcDepth + 8 <= BAR_BYTES,
+                  "barrier region");
+};
+
+// Shared-memory matrix descriptor for a K-major tile written by TMA with the
+// 128-byte swizzle: rows of 128 bytes, 8-row atoms 1024 bytes apart.
+//   bits  0-13 start address >> 4      bits 16-29 leading byte offset >> 4 (unused for this layout)
+//   bits 32-45 stride byte offset >> 4 bits 46-48 fixed 0b001
+//   bits 49-51 base offset (0: atoms 1024-aligned)   bits 61-63 layout (2 = 128-byte swizzle)
+__device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t smem_addr) {
+    return uint64_t((smem_addr & 0x3FFFFu) >> 4) | (uint64_t(1) << 16) | (uint64_t(1024 >> 4) << 32) |
+           (uint64_t(1) << 46) | (uint64_t(2) << 61);
+}
+
+__device__ __forceinline__ void report_timeout(const GemmParams &p, int where) {
+    const unsigned long long info = (static_cast<unsigned long long>(where) << 32) | blockIdx.x;
+    if (atomicCAS(&p.status[0], 0ull, 1ull) == 0ull) atomicExch(&p.status[1], info);
+    atomicAdd(&p.status[2], 1ull);
+}
+
+// Bounded phase wait.  honor_abort: give up as soon as another role aborted
+// (role loops); drains pass false and rely on their own limit alone.
+static __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, uint64_t limit_ns, volatile int *abort_flag,
+                                       bool honor_abort, const GemmParams &p, int where) {
+    const uint64_t t0 = globaltimer();
+    for (uint32_t n = 1;; ++n) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((n & 15u) == 0) {
+            if (honor_abort && *abort_flag) return false;
+            if (globaltimer() - t0 > limit_ns) {
+                report_timeout(p, where);
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                           const GemmParams &p, int where) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_slow(bar, parity, p.timeout_ns, abort_flag, true, p, where);
+}
+
+__device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                           const GemmParams &p) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_slow(bar, parity, p.drain_ns, abort_flag, false, p, WAIT_DRAIN);
+}
+
+// Tile id -> (m block, n block): consecutive ids walk `raster_group` tile rows
+// down a column band, so workers running at the same time share B tiles in L2.
+__device__ __forceinline__ void raster(int32_t tile, const GemmParams &p, int32_t &mb, int32_t &nb) {
+    const int32_t G = p.raster_group;
+    const int32_t per_group = G * p.tiles_n;
+    const int32_t g = tile / per_group;
+    const int32_t first_m = g * G;
+    const int32_t gsize = min(G, p.tiles_m - first_m);
+    const int32_t local = tile - g * per_group;
+    mb = first_m + local % gsize;
+    nb = local / gsize;
+}
+
+// Shared-memory map of one CTA.
+template <class C>
+struct Smem {
+    uint32_t a, b, epi;        // tile ring and epilogue staging (shared addresses)
+    uint32_t resp;             // CLC response slots, 16 bytes each
+    uint32_t bars;             // mbarrier array
+    uint32_t *tmem_slot;
+    volatile int *abort_flag;
+
+    __device__ __forceinline__ uint32_t full(int s) const { return bars + 8u * s; }
+    __device__ __forceinline__ uint32_t empty(int s) const { return bars + 8u * (C::STAGES + s); }
+    __device__ __forceinline__ uint32_t tfull(int a) const { return bars + 8u * (2 * C::STAGES + a); }
+    __device__ __forceinline__ uint32_t tempty(int a) const { return bars + 8u * (2 * C::STAGES + 2 + a); }
+    __device__ __forceinline__ uint32_t mma_done() const { return bars + 8u * (2 * C::STAGES + 4); }
+    __device__ __forceinline__ uint32_t clc_full(int r) const { return bars + 8u * (2 * C::STAGES + 5 + r); }
+    __device__ __forceinline__ uint32_t clc_empty(int r) const {
+        return bars + 8u * (2 * C::STAGES + 5 + kMaxClcDepth + r);
+    }
+};
+
+// Consume the next CLC response (one thread per consuming role).  Returns the
+// next tile, or -1 when the cancel failed (no pending launch left) or the
+// kernel is aborting.
+template <class C>
+__device__ __forceinline__ int32_t clc_consume(const Smem<C> &sm, const GemmParams &p, uint32_t &idx) {
+    const uint32_t depth = static_cast<uint32_t>(p.clc_depth);
+    const uint32_t r = idx % depth;
+    const uint32_t ph = (idx / depth) & 1u;
+    ++idx;
+    if (!wait_phase(sm.clc_full(r), ph, sm.abort_flag, p, WAIT_CLC_FULL)) return -1;
+    uint32_t x = 0;
+    const bool ok = clc_query(sm.resp + 16u * r, x);
+    fence_proxy_async_smem();  // our generic read of the slot before the next async write into it
+    if constexpr (C::CG == 1)
+        mbar_arrive(sm.clc_empty(r));
+    else
+        mbar_arrive_cluster(mapa(sm.clc_empty(r), 0));
+    return ok ? static_cast<int32_t>(x / C::CG) : -1;
+}
+
+template <class C>
+__device__ __forceinline__ int32_t next_tile(const Smem<C> &sm, const GemmParams &p, int32_t tile,
+                                             uint32_t &clc_idx) {
+    if (p.sched == SCHED_STATIC) {
+        const int32_t t = tile + static_cast<int32_t>(gridDim.x / C::CG);
+        return t < p.num_tiles ? t : -1;
+    }
+    return clc_consume(sm, p, clc_idx);
+}
+
+template <int BN, int CG, int OUT>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmD, const __grid_constant__ GemmParams p) {
+    using C = GemmCfg<BN, CG, OUT>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *const gbase = smem_raw + (base - raw);
+    Smem<C> sm;
+    sm.a = base;
+    sm.b = sm.a + C::STAGES * C::A_BYTES;
+    sm.epi = sm.b + C::STAGES * C::B_BYTES;
+    sm.resp = sm.epi + C::EPI_BYTES;
+    sm.bars = sm.resp + 16u * kMaxClcDepth;
+    const uint32_t tail = sm.bars + 8u * (2 * C::STAGES + 5 + 2 * kMaxClcDepth);
+    sm.tmem_slot = reinterpret_cast<uint32_t *>(gbase + (tail - base));
+    sm.abort_flag = reinterpret_cast<volatile int *>(gbase + (tail - base) + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;
+    const int32_t worker = static_cast<int32_t>(blockIdx.x / CG);
+
+    // ------------------------------------------------------------ prologue
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+        if (p.tma_store) prefetch_tmap(&tmD);
+    }
+    if (warp == 3 && lane == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(sm.full(s), 1);
+            mbar_init(sm.empty(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(sm.tfull(a), 1);
+            mbar_init(sm.tempty(a), 4 * CG);
+        }
+        mbar_init(sm.mma_done(), 1);
+        for (int r = 0; r < kMaxClcDepth; ++r) {
+            mbar_init(sm.clc_full(r), 1);
+            mbar_init(sm.clc_empty(r), C::CLC_CONSUMERS);
+        }
+        *sm.abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc<CG>(smem_u32(sm.tmem_slot), C::TMEM_COLS);
+        tmem_relinquish<CG>();
+    }
+    tc_fence_before();
+    if constexpr (CG == 2)
+        cluster_sync();
+    else
+        __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(sm.tmem_slot);
+
+    const int32_t first_tile = worker < p.num_tiles ? worker : -1;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int32_t tile = first_tile;
+            uint32_t clc_idx = 0, stage = 0, phase = 0, issued = 0;
+            bool alive = true;
+            while (tile >= 0 && alive) {
+                int32_t mb, nb;
+                raster(tile, p, mb, nb);
+                const int32_t a_row = mb * C::TILE_M + static_cast<int32_t>(rank) * C::BM;
+                const int32_t b_row = nb * BN + static_cast<int32_t>(rank) * C::B_ROWS;
+                if (p.trace && rank == 0) p.trace[4 * tile + 2] = static_cast<long long>(globaltimer());
+                for (int32_t kb = 0; kb < p.num_k_blocks; ++kb) {
+                    if (!wait_phase(sm.empty(stage), phase ^ 1u, sm.abort_flag, p, WAIT_PRODUCER_EMPTY)) {
+                        alive = false;
+                        break;
+                    }
+                    if (rank == 0) mbar_arrive_expect_tx(sm.full(stage), C::TX_BYTES);
+                    const uint32_t da = sm.a + stage * C::A_BYTES;
+                    const uint32_t db = sm.b + stage * C::B_BYTES;
+                    if constexpr (CG == 1) {
+                        tma_load_2d(da, &tmA, sm.full(stage), kb * C::BK, a_row);
+                        tma_load_2d(db, &tmB, sm.full(stage), kb * C::BK, b_row);
+                    } else {
+                        const uint32_t fb = mapa(sm.full(stage), 0);
+                        tma_load_2d_pair(da, &tmA, fb, kb * C::BK, a_row);
+                        tma_load_2d_pair(db, &tmB, fb, kb * C::BK, b_row);
+                    }
+                    ++issued;
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!alive) break;
+                tile = next_tile(sm, p, tile, clc_idx);
+            }
+            // Drain: every issued load has landed (even CTA's full barriers) and
+            // the MMA has released every stage.
+            if (rank == 0) {
+                const uint32_t n = issued < C::STAGES ? issued : C::STAGES;
+                for (uint32_t i = 1; i <= n; ++i) {
+                    const uint32_t b = issued - i;
+                    wait_drain(sm.full(b % C::STAGES), (b / C::STAGES) & 1u, sm.abort_flag, p);
+                }
+            }
+            for (int i = 0; i < C::STAGES; ++i) {
+                if (!wait_drain(sm.empty(stage), phase ^ 1u, sm.abort_flag, p)) break;
+                if (++stage == C::STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0 && rank == 0) {
+            int32_t tile = first_tile;
+            uint32_t clc_idx = 0, stage = 0, phase = 0, acc = 0, acc_phase = 0;
+            bool alive = true;
+            while (tile >= 0 && alive) {
+                if (!wait_phase(sm.tempty(acc), acc_phase ^ 1u, sm.abort_flag, p, WAIT_MMA_TMEM_EMPTY)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * BN;
+                for (int32_t kb = 0; kb < p.num_k_blocks; ++kb) {
+                    if (!wait_phase(sm.full(stage), phase, sm.abort_flag, p, WAIT_MMA_FULL)) {
+                        alive = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t da = sw128_kmajor_desc(sm.a + stage * C::A_BYTES);
+                    const uint64_t db = sw128_kmajor_desc(sm.b + stage * C::B_BYTES);
+#pragma unroll
+                    for (int kk = 0; kk < C::BK / C::UMMA_K; ++kk) {
+                        // +32 bytes per K = 16 step inside the 128-byte swizzle row (encoded >> 4)
+                        mma_bf16<CG>(d_tmem, da + 2u * kk, db + 2u * kk, C::IDESC, (kb | kk) != 0);
+                    }
+                    if constexpr (CG == 1)
+                        mma_commit(sm.empty(stage));
+                    else
+                        mma_commit_pair(sm.empty(stage), 0x3);
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!alive) break;
+                if constexpr (CG == 1)
+                    mma_commit(sm.tfull(acc));
+                else
+                    mma_commit_pair(sm.tfull(acc), 0x3);
+                if (++acc == 2) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+                tile = next_tile(sm, p, tile, clc_idx);
+            }
+            // Every MMA issued by this thread has completed before TMEM is freed.
+            if constexpr (CG == 1)
+                mma_commit(sm.mma_done());
+            else
+                mma_commit_pair(sm.mma_done(), 0x1);
+            wait_drain(sm.mma_done(), 0, sm.abort_flag, p);
+        }
+        __syncwarp();
+    } else if (warp == 2) {
+        // ------------------------------------------------- CLC scheduler
+        if (lane == 0 && p.sched == SCHED_CLC && first_tile >= 0) {
+            uint32_t idx = 0;
+            bool outstanding = false;
+            uint32_t out_r = 0, out_ph = 0;
+            const uint32_t depth = static_cast<uint32_t>(p.clc_depth);
+            for (;;) {
+                const uint32_t r = idx % depth;
+                const uint32_t ph = (idx / depth) & 1u;
+                if (rank == 0) {
+                    if (!wait_phase(sm.clc_empty(r), ph ^ 1u, sm.abort_flag, p, WAIT_SCHED_CLC_EMPTY)) break;
+                    fence_proxy_async_smem();
+                    mbar_arrive_expect_tx(sm.clc_full(r), 16);
+                    if constexpr (CG == 1)
+                        clc_try_cancel(sm.resp + 16u * r, sm.clc_full(r));
+                    else
+                        clc_try_cancel_all(sm.resp + 16u * r, sm.clc_full(r));
+                    outstanding = true;
+                    out_r = r;
+                    out_ph = ph;
+                } else {
+                    // the even CTA's request multicasts its response here: arm our barrier for it
+                    mbar_arrive_expect_tx(sm.clc_full(r), 16);
+                }
+                const int32_t t = clc_consume(sm, p, idx);
+                outstanding = false;
+                if (t < 0) {
+                    // a failed wait leaves the request possibly in flight
+                    if (*sm.abort_flag && rank == 0) outstanding = true;
+                    break;
+                }
+            }
+            if (outstanding) wait_drain(sm.clc_full(out_r), out_ph, sm.abort_flag, p);
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // --------------------------------------------------------- epilogue
+        const int q = warp - 4;  // TMEM lane quarter this warp may access
+        const uint32_t stg = sm.epi + static_cast<uint32_t>(q) * 2u * C::EPI_BUF;
+        int32_t tile = first_tile;
+        uint32_t clc_idx = 0, acc = 0, acc_phase = 0, buf = 0;
+        while (tile >= 0) {
+            int32_t mb, nb;
+            raster(tile, p, mb, nb);
+            const int32_t row0 = mb * C::TILE_M + static_cast<int32_t>(rank) * C::BM + 32 * q;
+            const int32_t col0 = nb * BN;
+            int ok = 1;
+            if (lane == 0) ok = wait_phase(sm.tfull(acc), acc_phase, sm.abort_flag, p, WAIT_EPI_TMEM_FULL);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + acc * BN;
+#pragma unroll 1
+            for (int s = 0; s < C::NUM_SUB; ++s) {
+                uint32_t w[32];
+                if constexpr (OUT == OUT_F32) {
+                    tmem_ld_32x32b_x32(taddr + s * 32, w);
+                    tmem_ld_wait();
+                } else {
+                    uint32_t lo[32], hi[32];
+                    tmem_ld_32x32b_x32(taddr + s * 64, lo);
+                    tmem_ld_32x32b_x32(taddr + s * 64 + 32, hi);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        w[j] = pack_bf16x2(lo[2 * j], lo[2 * j + 1]);
+                        w[16 + j] = pack_bf16x2(hi[2 * j], hi[2 * j + 1]);
+                    }
+                }
+                if (s == C::NUM_SUB - 1) {
+                    // accumulator fully read: hand it back to the MMA issuer
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if constexpr (CG == 1)
+                            mbar_arrive(sm.tempty(acc));
+                        else
+                            mbar_arrive_cluster(mapa(sm.tempty(acc), 0));
+                    }
+                }
+                const int32_t col = col0 + s * C::SUB_COLS;
+                if (p.tma_store) {
+                    if (lane == 0) bulk_wait_read<1>();  // the store that used this buffer has read it
+                    __syncwarp();
+                    const uint32_t row_addr = stg + buf * C::EPI_BUF + static_cast<uint32_t>(lane) * 128u;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        st_shared_v4(row_addr + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4), w[4 * j],
+                                     w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && row0 < p.M && col < p.N) {
+                        tma_store_2d(&tmD, stg + buf * C::EPI_BUF, col, row0);
+                        bulk_commit();
+                    }
+                    buf ^= 1u;
+                } else {
+                    const int32_t row = row0 + lane;
+                    if (row < p.M) {
+                        if constexpr (OUT == OUT_F32) {
+                            float *dst = static_cast<float *>(p.D) + static_cast<int64_t>(row) * p.ldd + col;
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                if (col + j < p.N) dst[j] = __uint_as_float(w[j]);
+                        } else {
+                            uint16_t *dst = static_cast<uint16_t *>(p.D) + static_cast<int64_t>(row) * p.ldd + col;
+#pragma unroll
+                            for (int j = 0; j < 64; ++j)
+                                if (col + j < p.N) dst[j] = static_cast<uint16_t>(w[j >> 1] >> (16 * (j & 1)));
+                        }
+                    }
+                }
+            }
+            if (p.trace && rank == 0 && q == 0 && lane == 0) {
+                atomicAdd(reinterpret_cast<unsigned long long *>(&p.trace[4 * tile]), 1ull);
+                p.trace[4 * tile + 1] = worker;
+                p.trace[4 * tile + 3] = static_cast<long long>(globaltimer());
+            }
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+            int32_t nt = 0;
+            if (lane == 0) nt = next_tile(sm, p, tile, clc_idx);
+            tile = __shfl_sync(0xffffffffu, nt, 0);
+        }
+        if (lane == 0) bulk_wait<0>();
+        __syncwarp();
+    }
+
+    // ------------------------------------------------------------ teardown
+    tc_fence_before();
+    if constexpr (CG == 2)
+        cluster_sync();
+    else
+        __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc<CG>(tmem_base, C::TMEM_COLS);
+}
+
+}  // namespace ts

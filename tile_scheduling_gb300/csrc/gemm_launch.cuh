@@ -1,0 +1,91 @@
+// Host launcher for one instantiation of the GEMM kernel.  Each instance
+// translation unit includes this file and expands TS_GEMM_VARIANT once, so the
+// variants compile in parallel.
+#pragma once
+#include <atomic>
+
+#include "common.h"
+#include "gemm_kernel.cuh"
+
+namespace ts {
+
+template <int BN, int CG, int OUT>
+struct GemmInstance {
+    using C = GemmCfg<BN, CG, OUT>;
+
+    // cudaFuncSetAttribute once per device (bit per device ordinal).
+    static cudaError_t prepare() {
+        static std::atomic<uint64_t> done{0};
+        const int dev = current_device();
+        const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
+        if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+        cudaError_t e = cudaFuncSetAttribute(gemm_ws_kernel<BN, CG, OUT>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+        if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+        return e;
+    }
+
+    static cudaError_t launch(const GemmLaunch &L) {
+        cudaError_t e = prepare();
+        if (e != cudaSuccess) return e;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(L.grid), 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = C::SMEM_BYTES;
+        cfg.stream = L.stream;
+        cudaLaunchAttribute attr[1];
+        if (CG == 2) {
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = 2;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+        }
+        return cudaLaunchKernelEx(&cfg, gemm_ws_kernel<BN, CG, OUT>, L.a, L.b, L.d, L.p);
+    }
+
+    static cudaError_t max_workers(int *out) {
+        cudaError_t e = prepare();
+        if (e != cudaSuccess) return e;
+        if (CG == 1) {
+            int per_sm = 0;
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemm_ws_kernel<BN, CG, OUT>, kThreads,
+                                                              C::SMEM_BYTES);
+            if (e != cudaSuccess) return e;
+            *out = per_sm * device_sms(current_device());
+            return cudaSuccess;
+        }
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * 1024, 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = C::SMEM_BYTES;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        e = cudaOccupancyMaxActiveClusters(&clusters, reinterpret_cast<const void *>(gemm_ws_kernel<BN, CG, OUT>),
+                                           &cfg);
+        if (e != cudaSuccess) return e;
+        *out = clusters;
+        return cudaSuccess;
+    }
+};
+
+}  // namespace ts
+
+#define TS_GEMM_VARIANT(NAME, BN, CG, OUT)                                                                 \
+    namespace ts {                                                                                         \
+    extern const GemmVariant NAME;                                                                         \
+    const GemmVariant NAME = {BN,                                                                          \
+                              CG,                                                                          \
+                              OUT,                                                                         \
+                              GemmCfg<BN, CG, OUT>::STAGES,                                                \
+                              GemmCfg<BN, CG, OUT>::SMEM_BYTES,                                            \
+                              &GemmInstance<BN, CG, OUT>::launch,                                          \
+                              &GemmInstance<BN, CG, OUT>::max_workers};                                    \
+    }

@@ -1,0 +1,43 @@
+// Kernel parameter block and device status layout shared by host and device code.
+#pragma once
+#include <cstdint>
+
+namespace ts {
+
+enum : int32_t { SCHED_STATIC = 0, SCHED_CLC = 1 };
+enum : int32_t { OUT_BF16 = 0, OUT_F32 = 1 };
+
+// Where a bounded wait gave up (reported in the status word).
+enum : int32_t {
+    WAIT_PRODUCER_EMPTY = 1,
+    WAIT_MMA_FULL = 2,
+    WAIT_MMA_TMEM_EMPTY = 3,
+    WAIT_EPI_TMEM_FULL = 4,
+    WAIT_SCHED_CLC_EMPTY = 5,
+    WAIT_CLC_FULL = 6,
+    WAIT_DRAIN = 7,
+};
+
+// Device status word (library-owned, one per device):
+//   [0] first error code (0 = none, 1 = wait timeout)
+//   [1] (where << 32) | blockIdx.x of the first error
+//   [2] number of timed-out waits since the last check
+constexpr int kStatusWords = 4;
+
+struct GemmParams {
+    int32_t M, N, K;
+    int32_t tiles_m, tiles_n, num_tiles, num_k_blocks;
+    int32_t raster_group;  // >= 1
+    int32_t sched;         // SCHED_STATIC / SCHED_CLC
+    int32_t tma_store;     // 1: TMA-store epilogue, 0: st.global epilogue
+    int32_t clc_depth;     // response slots in flight (1 or 2)
+    int32_t pad0;
+    void *D;               // used by the st.global epilogue
+    int64_t ldd;           // elements
+    uint64_t timeout_ns;   // per-wait limit
+    uint64_t drain_ns;     // limit for waiting on copies still in flight at exit
+    unsigned long long *status;
+    long long *trace;      // 4 int64 per tile, or nullptr
+};
+
+}  // namespace ts
