@@ -111,10 +111,13 @@ def test_gemm_strided_operands(lib, tile):
 @pytest.mark.parametrize("tile", TILES)
 def test_gemm_guard_regions_untouched(lib, out, tile):
     # D lives inside a larger buffer; rows/columns around it hold a sentinel
-    M, N, K = 200, 300, 64
+    # N = 301: the right edge is ragged at 16-byte granularity for both dtypes.
+    # pitch N + 64 + pad: pad 0 -> 365 (unaligned, plain-store epilogue);
+    # pad 3 -> 368 and pad 11 -> 376 (16-byte pitch, TMA stores + ragged edge)
+    M, N, K = 200, 301, 64
     A = synth.int_uniform_bf16(151, (M, K))
     B = synth.int_uniform_bf16(152, (N, K))
-    for pitch_pad in (0, 8, 3):  # 3 makes the pitch unaligned -> plain-store epilogue
+    for pitch_pad in (0, 3, 11):
         big = torch.full((M + 64, N + 64 + pitch_pad), 3072.0, dtype=out, device="cuda")
         D = big[32:32 + M, 32:32 + N]
         lib.ts_gemm_bf16_ex(to_device_bf16(A), to_device_bf16(B), D, sched="static", tile=tile)

@@ -56,7 +56,7 @@ class LaunchInfo(ctypes.Structure):
 
 def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     if not os.path.exists(path):
-        raise ImportError(f"libtsgemm.so not built ({path}); run python -m tile_scheduling_gb300.build")
+        raise ImportError(f"libtsgemm.so not built ({path}); run python tile_scheduling_gb300/build.py")
     lib = ctypes.CDLL(path)
     P, I32, I64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
     lib.ts_gemm_bf16.argtypes = [P, P, P, I64, I64, I64, I32, I32, P]

@@ -1,6 +1,6 @@
 """Build libtsgemm.so in-tree: every csrc/*.cu compiled for sm_103a in parallel, then linked.
 
-Usage: python -m tile_scheduling_gb300.build [--force] [--verbose]
+Usage: python tile_scheduling_gb300/build.py [--force] [--verbose]
 """
 from __future__ import annotations
 

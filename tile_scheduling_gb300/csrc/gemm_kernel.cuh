@@ -453,7 +453,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 const int32_t col = col0 + s * C::SUB_COLS;
-                if (p.tma_store) {
+                // Subtiles wholly outside D are skipped (no staging write, no
+                // store group).  A TMA store is used only for boxes whose
+                // columns lie inside D: the store clips rows exactly but a
+                // ragged right edge only to 16-byte granules, so a subtile that
+                // crosses N is written with plain predicated stores instead.
+                if (row0 >= p.M || col >= p.N) continue;
+                if (p.tma_store && col + C::SUB_COLS <= p.N) {
                     if (lane == 0) bulk_wait_read<1>();  // the store that used this buffer has read it
                     __syncwarp();
                     const uint32_t row_addr = stg + buf * C::EPI_BUF + static_cast<uint32_t>(lane) * 128u;
@@ -463,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
                     fence_proxy_async_smem();
                     __syncwarp();
-                    if (lane == 0 && row0 < p.M && col < p.N) {
+                    if (lane == 0) {
                         tma_store_2d(&tmD, stg + buf * C::EPI_BUF, col, row0);
                         bulk_commit();
                     }
