@@ -107,6 +107,28 @@ ts_status ts_gemm_launch_info(int64_t M, int64_t N, int64_t K, int32_t out_dtype
                               const ts_gemm_opts *opts, ts_launch_info *info);
 
 /*
+ * ts_gemm_bf16_checked_noalloc -- ts_gemm_bf16 (default tile choice) plus a
+ * check that the tile scheduler computed every output tile exactly once, for
+ * callers that cannot allocate device memory.  No counterpart in the pages:
+ * it is a packaging of the traced GEMM for such callers.
+ *
+ * The per-tile trace lives in a fixed array inside this library's device image
+ * (room for 65536 output tiles, 2 MiB per device, held until the process
+ * exits) instead of caller memory.  The call allocates nothing.  Its first call
+ * on a device looks the array's address up and should precede any stream
+ * capture.  All calls on a device share the one array: calls that overlap on
+ * the GPU race and must be serialised by the caller.
+ *
+ *   A, B, D, M, N, K, out_dtype, sched   as for ts_gemm_bf16
+ *   bad_tiles  device int32, written asynchronously on `stream` with the number
+ *              of tiles not visited exactly once (0 on success; 0 when no tile
+ *              is scheduled: M, N or K is 0)
+ * Problems with more than 65536 output tiles return TS_ERR_UNSUPPORTED.
+ */
+ts_status ts_gemm_bf16_checked_noalloc(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K,
+                                       int32_t out_dtype, int32_t sched, int32_t *bad_tiles, void *stream);
+
+/*
  * ts_copy_i16 -- dst[i] = src[i] for 0 <= i < n (TS "Resources", the int16
  * copy example: get_item / set_item guarded by gid < num_entries; TS
  * "Schedules", the grid-stride domain start = bx * tpb + tx, step = gdimx * tpb).

@@ -29,7 +29,8 @@ _TILE = {"auto": TS_TILE_AUTO, "128x128": TS_TILE_128x128, "128x256": TS_TILE_12
          "256x256": TS_TILE_256x256_2CTA}
 _OUT = {torch.bfloat16: TS_OUT_BF16, torch.float32: TS_OUT_F32}
 
-EXPORTED = ("ts_gemm_bf16", "ts_gemm_bf16_ex", "ts_gemm_launch_info", "ts_copy_i16", "ts_spin",
+EXPORTED = ("ts_gemm_bf16", "ts_gemm_bf16_ex", "ts_gemm_launch_info", "ts_gemm_bf16_checked_noalloc",
+            "ts_copy_i16", "ts_spin",
             "ts_spin_wait_started", "ts_sync_and_check", "ts_num_sms", "ts_status_string",
             "ts_last_error_detail")
 
@@ -63,6 +64,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ts_gemm_bf16_ex.argtypes = [P, P, P, I64, I64, I64, I32, I32, ctypes.POINTER(GemmOpts), P]
     lib.ts_gemm_launch_info.argtypes = [I64, I64, I64, I32, I32, ctypes.POINTER(GemmOpts),
                                         ctypes.POINTER(LaunchInfo)]
+    lib.ts_gemm_bf16_checked_noalloc.argtypes = [P, P, P, I64, I64, I64, I32, I32, P, P]
     lib.ts_copy_i16.argtypes = [P, P, I64, P]
     lib.ts_spin.argtypes = [I32, I64, P, P]
     lib.ts_spin_wait_started.argtypes = [P, I32, ctypes.c_double]
@@ -73,7 +75,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ts_status_string.restype = ctypes.c_char_p
     lib.ts_last_error_detail.argtypes = []
     lib.ts_last_error_detail.restype = ctypes.c_char_p
-    for name in ("ts_gemm_bf16", "ts_gemm_bf16_ex", "ts_gemm_launch_info", "ts_copy_i16", "ts_spin",
+    for name in ("ts_gemm_bf16", "ts_gemm_bf16_ex", "ts_gemm_launch_info", "ts_gemm_bf16_checked_noalloc",
+                 "ts_copy_i16", "ts_spin",
                  "ts_spin_wait_started", "ts_sync_and_check"):
         getattr(lib, name).restype = ctypes.c_int
     return lib
@@ -162,6 +165,26 @@ def ts_gemm_bf16(A: torch.Tensor, B: torch.Tensor, D: torch.Tensor, sched="stati
     _check(_lib.ts_gemm_bf16(ctypes.c_void_p(A.data_ptr()), ctypes.c_void_p(B.data_ptr()),
                              ctypes.c_void_p(D.data_ptr()), M, N, K, _OUT[D.dtype], _sched(sched),
                              _stream_handle(stream)))
+
+
+def ts_gemm_bf16_checked_noalloc(A: torch.Tensor, B: torch.Tensor, D: torch.Tensor, bad_tiles: torch.Tensor,
+                                 sched="static", stream=None) -> None:
+    """D = A @ B.T plus a tile-coverage check, without any device allocation.
+
+    For callers that cannot call cudaMalloc: the per-tile trace lives in a
+    fixed 2 MiB array inside the library (at most 65536 output tiles) rather
+    than in caller memory.  ``bad_tiles`` (one int32 on the device) receives
+    the number of tiles not computed exactly once.  Calls that overlap on the
+    GPU share that array and race; the first call on a device should come
+    before any stream capture."""
+    M, N, K, lda, ldb, ldd = _gemm_args(A, B, D)
+    if (M > 1 and (lda != K or ldd != N)) or (N > 1 and ldb != K):
+        raise ValueError("dense rows required")
+    if bad_tiles.dtype != torch.int32 or not bad_tiles.is_cuda or bad_tiles.numel() < 1:
+        raise TypeError("bad_tiles must be an int32 CUDA tensor")
+    _check(_lib.ts_gemm_bf16_checked_noalloc(ctypes.c_void_p(A.data_ptr()), ctypes.c_void_p(B.data_ptr()),
+                                             ctypes.c_void_p(D.data_ptr()), M, N, K, _OUT[D.dtype], _sched(sched),
+                                             ctypes.c_void_p(bad_tiles.data_ptr()), _stream_handle(stream)))
 
 
 def ts_gemm_bf16_ptr(A: int, B: int, D: int, M: int, N: int, K: int, out: int, sched=0, stream=None,
