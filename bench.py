@@ -42,17 +42,17 @@ if ROOT not in sys.path:
 import synth  # noqa: E402
 
 PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
-TRAFFIC_PATH = os.path.join(ROOT, "profiles", "traffic.json")
+TRAFFIC_PATH = os.path.join(ROOT, "profiles", "traffic.txt")
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_BF16_SUSTAINED = 1700.0
-KERNEL_SOURCES = ["gemm_kernel.cuh", "ptx.cuh", "gemm_params.h", "gemm_launch.cuh", "copy.cu"]
+KERNEL_SOURCES = {"gemm": ["gemm_kernel.cuh", "ptx.cuh", "gemm_params.h", "gemm_launch.cuh"], "copy": ["copy.cu"]}
 
 
 # ------------------------------------------------------------------ helpers
-def kernel_source_hash() -> str:
+def kernel_source_hash(kernel: str) -> str:
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, "tile_scheduling_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -74,13 +74,15 @@ def load_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from a committed ncu capture, if it was taken on the current kernel sources."""
     try:
         with open(TRAFFIC_PATH) as f:
-            t = json.load(f)
-        e = t[kernel]
-        if e.get("source_hash") != kernel_source_hash() or e.get("workload") != workload:
-            return None
-        return float(e["bytes_per_launch"])
-    except (OSError, KeyError, ValueError):
-        return None
+            for line in f:
+                if line.startswith("#") or not line.strip():
+                    continue
+                k, w, h, b = [x.strip() for x in line.split("|")[:4]]
+                if k == kernel and w == workload and h == kernel_source_hash(kernel):
+                    return float(b)
+    except (OSError, ValueError):
+        pass
+    return None
 
 
 class ClockSampler:
@@ -243,7 +245,7 @@ def run_ours(args, ws, rank, local):
             "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops_sustained"], 4),
             "traffic": load_traffic("gemm", f"{M}x{N}x{K} {args.tile} {args.sched}"),
             "peak_kind": f"{peaks['source']} bf16 sustained (kernel timed inside a long step)",
-            "kernel": "gemm_ws_kernel"}
+            "frac_of_burst_peak": round(achieved / peaks["bf16_tflops"], 4), "kernel": "gemm_ws_kernel"}
     copy_roof = {"bound": "hbm", "achieved": round(copy_gbs / ws, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                  "frac": round(copy_gbs / ws / peaks["hbm_gbs"], 4), "traffic": load_traffic("copy", "n=2^28"),
                  "peak_kind": f"{peaks['source']} HBM copy", "kernel": "copy_i16_vec_kernel"}
@@ -269,6 +271,128 @@ def run_ours(args, ws, rank, local):
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args)
     return line
+
+
+def _event_ms(fn, stream):
+    import torch
+
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    fn()
+    e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1)
+
+
+def run_gemm4096(args, ws, rank, local):
+    """4096^3 bf16-out GEMM with 128x256 tiles: static persistent vs CLC (medians over --steps launches)."""
+    import torch
+
+    import tile_scheduling_gb300 as ts
+
+    torch.cuda.set_device(local)
+    w = synth.GEMM_4096
+    A_bits, B_bits = w.inputs()
+    A = torch.from_numpy(A_bits.view(np.int16)).view(torch.bfloat16).cuda()
+    B = torch.from_numpy(B_bits.view(np.int16)).view(torch.bfloat16).cuda()
+    D = torch.empty((w.M, w.N), dtype=torch.bfloat16, device="cuda")
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")  # > L2: inputs would otherwise stay resident
+    stream = torch.cuda.current_stream()
+    res = {}
+    for sched in ("static", "clc"):
+        for _ in range(args.warmup):
+            ts.ts_gemm_bf16_ex(A, B, D, sched=sched, tile="128x256")
+        ms = []
+        for _ in range(args.steps):
+            flush.zero_()
+            ms.append(_event_ms(lambda: ts.ts_gemm_bf16_ex(A, B, D, sched=sched, tile="128x256"), stream))
+        ts.ts_sync_and_check()
+        med = statistics.median(ms)
+        res[sched] = {"ms_median": round(med, 4), "ms_min": round(min(ms), 4),
+                      "tflops": round(2.0 * w.M * w.N * w.K / (med * 1e-3) / 1e12, 1)}
+    if rank != 0:
+        return None
+    peaks = load_peaks()
+    return {"metric": "bf16 GEMM TFLOP/s, 4096^3 bf16-out, 128x256 tiles, static vs CLC", "unit": "TFLOP/s",
+            "value": res["clc"]["tflops"], "static": res["static"], "clc": res["clc"], "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "dtype": "bf16",
+            "data": "synthetic", "config": {"workload": w.name, "l2": "256 MiB buffer written between launches"},
+            "peak_bf16_tflops_burst": peaks["bf16_tflops"], "peak_source": peaks["source"]}
+
+
+def run_contended(args, ws, rank, local):
+    """Ragged 8191x6143x4096 fp32-out GEMM while a spin kernel holds 32 SMs for half the solo GEMM time.
+
+    Static persistent vs CLC, alternating, --reps pairs; a traced run per scheduler gives the tail
+    (last worker's finish minus the median worker's finish)."""
+    import torch
+
+    import tile_scheduling_gb300 as ts
+
+    torch.cuda.set_device(local)
+    w = synth.GEMM_RAGGED
+    A_bits, B_bits = w.inputs()
+    A = torch.from_numpy(A_bits.view(np.int16)).view(torch.bfloat16).cuda()
+    B = torch.from_numpy(B_bits.view(np.int16)).view(torch.bfloat16).cuda()
+    Dbuf = torch.empty((w.M, 6144), dtype=torch.float32, device="cuda")
+    D = Dbuf[:, :w.N]  # 6144-element pitch: TMA stores, masked at N = 6143
+    stream = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
+    started = torch.zeros(1, dtype=torch.int32).pin_memory()
+    ctas = args.spin_ctas
+    tile = args.tile
+
+    def gemm(sched, trace=None):
+        ts.ts_gemm_bf16_ex(A, B, D, sched=sched, tile=tile, trace=trace)
+
+    solo = {}
+    for sched in ("static", "clc"):
+        for _ in range(args.warmup):
+            gemm(sched)
+        solo[sched] = statistics.median([_event_ms(lambda: gemm(sched), stream) for _ in range(args.reps)])
+    spin_ns = int(0.5 * solo["static"] * 1e6)
+
+    def contended(sched, trace=None):
+        started.zero_()
+        torch.cuda.synchronize()
+        ts.ts_spin(ctas, spin_ns, started, stream=side)
+        ts.ts_spin_wait_started(started, ctas, 5.0)
+        ms = _event_ms(lambda: gemm(sched, trace), stream)
+        torch.cuda.synchronize()
+        return ms
+
+    times = {"static": [], "clc": []}
+    for _ in range(args.reps):
+        for sched in ("static", "clc"):
+            times[sched].append(contended(sched))
+    tails = {}
+    for sched in ("static", "clc"):
+        info = ts.ts_gemm_launch_info(w.M, w.N, w.K, ts.TS_OUT_F32, sched, tile=tile, ldd=6144)
+        trace = torch.zeros(4 * info["num_tiles"], dtype=torch.int64, device="cuda")
+        contended(sched, trace)
+        tr = trace.view(-1, 4).cpu().numpy()
+        t0 = tr[:, 2].min()
+        fin = {}
+        for t in range(tr.shape[0]):
+            fin[int(tr[t, 1])] = max(fin.get(int(tr[t, 1]), 0), int(tr[t, 3]))
+        f = np.array(sorted(fin.values()), dtype=np.float64)
+        tails[sched] = {"workers_ran": len(fin), "tail_us": round((f.max() - np.median(f)) / 1e3, 1),
+                        "span_us": round((f.max() - t0) / 1e3, 1), "visits_ok": bool(np.all(tr[:, 0] == 1))}
+    ts.ts_sync_and_check()
+    if rank != 0:
+        return None
+    flops = 2.0 * w.M * w.N * w.K
+    out = {}
+    for sched in ("static", "clc"):
+        med = statistics.median(times[sched])
+        out[sched] = {"ms_median": round(med, 4), "ms_min": round(min(times[sched]), 4),
+                      "tflops": round(flops / (med * 1e-3) / 1e12, 1), "solo_ms": round(solo[sched], 4),
+                      "solo_tflops": round(flops / (solo[sched] * 1e-3) / 1e12, 1), **tails[sched]}
+    return {"metric": "ragged 8191x6143x4096 fp32-out GEMM TFLOP/s with 32 SMs held for half the solo time",
+            "unit": "TFLOP/s", "value": out["clc"]["tflops"], "static": out["static"], "clc": out["clc"],
+            "clc_speedup_over_static": round(out["static"]["ms_median"] / out["clc"]["ms_median"], 3),
+            "n_gpus": ws, "reps": args.reps, "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "tile": tile, "spin_ctas": ctas, "spin_ns": spin_ns, "ldd": 6144}}
 
 
 def run_e2e(args, ts, A_bits, B_bits, M, N, K, ws):
@@ -335,14 +459,17 @@ def _B_cache():
 
 
 def cpu_baseline(args):
+    """The oracle as it stands, timed on the host cores on a bounded sample (~args.cpu_seconds of work)."""
     import oracle
 
     threads = oracle.default_threads()
-    rows = max(1, args.cpu_rows)
+    w = synth.GEMM_8192
+    probe_rate, _ = _oracle_sample_rate(2, threads)
+    rows = int(max(2, min(1024, args.cpu_seconds * probe_rate / (2.0 * w.N * w.K))))
     rate, dt = _oracle_sample_rate(rows, threads)
     return {"value": round(rate / 1e12, 8), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-            "sample": f"{rows} full rows of D (8192 entries each, K=8192) of the 8192^3 workload, fp64 triple loop, "
-                      f"{dt:.1f} s"}
+            "sample": f"{rows} full rows of D ({rows * w.N} entries, K={w.K}) of the {w.M}x{w.N}x{w.K} workload, "
+                      f"fp64 triple loop over {threads} OpenMP threads, {dt:.1f} s"}
 
 
 def run_reference(args, ws, rank):
@@ -388,7 +515,10 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-rows", type=int, default=16)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--workload", default="headline", choices=["headline", "gemm4096", "contended"])
+    ap.add_argument("--reps", type=int, default=10)
+    ap.add_argument("--spin-ctas", type=int, default=32)
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -407,7 +537,12 @@ def main(argv=None):
 
         dist.init_process_group("nccl")
     try:
-        line = run_ours(args, ws, rank, local)
+        if args.workload == "gemm4096":
+            line = run_gemm4096(args, ws, rank, local)
+        elif args.workload == "contended":
+            line = run_contended(args, ws, rank, local)
+        else:
+            line = run_ours(args, ws, rank, local)
     finally:
         if ws > 1:
             import torch.distributed as dist
