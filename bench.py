@@ -368,7 +368,7 @@ def run_contended(args, ws, rank, local):
     tails = {}
     for sched in ("static", "clc"):
         info = ts.ts_gemm_launch_info(w.M, w.N, w.K, ts.TS_OUT_F32, sched, tile=tile, ldd=6144)
-        trace = torch.zeros(4 * info["num_tiles"], dtype=torch.int64, device="cuda")
+        trace = torch.zeros(4 * info["num_units"], dtype=torch.int64, device="cuda")
         contended(sched, trace)
         tr = trace.view(-1, 4).cpu().numpy()
         t0 = tr[:, 2].min()

@@ -51,12 +51,20 @@ typedef struct {
     int64_t ldb;          /* row stride of B in elements (>= K); 0 = K */
     int64_t ldd;          /* row stride of D in elements (>= N); 0 = N */
     double timeout_s;     /* per-wait limit for every mbarrier wait in the kernel; 0 = 2 s */
-    int64_t *trace;       /* device buffer of 4 * num_tiles int64, zeroed by the caller, or NULL.
-                             Per tile t: [4t] += 1 per visit, [4t+1] = worker index,
-                             [4t+2] = %globaltimer when the producer started the tile,
-                             [4t+3] = %globaltimer when the epilogue issued its last store. */
+    int64_t *trace;       /* device buffer of 4 * num_units int64 (ts_launch_info), zeroed by the
+                             caller, or NULL.  Per work unit u: [4u] += 1 per visit,
+                             [4u+1] = worker index, [4u+2] = %globaltimer when the producer
+                             started the unit, [4u+3] = %globaltimer when the epilogue finished it. */
     int32_t raster_group; /* tile raster: consecutive tile ids walk this many tile rows; 0 = 8 */
-    int32_t reserved;
+    int32_t split_tail;   /* 0: split the last, partial wave of tiles along K when `workspace` is
+                             large enough; -1: never split */
+    void *workspace;      /* device scratch for the split tail (ts_launch_info.workspace_bytes),
+                             256-byte aligned.  Its first 8 KiB hold per-slab counters: zero them
+                             before the first use; every normal launch leaves them zero again
+                             (after TS_ERR_TIMEOUT zero them once more).  The rest holds fp32
+                             partials and needs no initialisation.  Launches that may overlap on
+                             the GPU need separate workspaces. */
+    int64_t workspace_bytes;
 } ts_gemm_opts;
 
 /* What ts_gemm_bf16_ex would launch for a problem (host-only query). */
@@ -66,9 +74,14 @@ typedef struct {
     int32_t stages;          /* shared-memory ring depth */
     int64_t tiles_m, tiles_n, num_tiles;
     int64_t grid_ctas;       /* CTAs launched */
-    int64_t workers;         /* persistent workers resident at once (static) or num_tiles (CLC) */
+    int64_t workers;         /* static: persistent workers launched; CLC: num_units */
     int32_t smem_bytes;      /* dynamic shared memory per CTA */
     int32_t tma_store;       /* 1 if D is written through TMA stores, 0 for the st.global epilogue */
+    int64_t num_units;       /* work units scheduled: whole tiles plus the K parts of split tiles */
+    int64_t split_tiles;     /* tiles of the last wave split along K (0 if none) */
+    int32_t split_parts;     /* K parts per split tile (1 if none) */
+    int32_t resident;        /* workers (CTAs or 2-CTA clusters) that fit on the GPU at once */
+    int64_t workspace_bytes; /* workspace a split tail needs (0 when no split would help) */
 } ts_launch_info;
 
 /*
@@ -88,6 +101,11 @@ typedef struct {
  *   D     device, [M][N] row-major, bf16 (out = TS_OUT_BF16, rounded to
  *         nearest even from fp32) or fp32 (TS_OUT_F32)
  *   M, N, K  sizes, each in [0, 2^31 - 1]
+ *
+ * Work is scheduled in units: whole tiles, and -- when the opts give a
+ * workspace -- the tiles of the last, partial wave split along K so that they
+ * fill the GPU; a split tile's parts are summed in fixed order by the warp
+ * that finishes last, so results do not depend on timing.
  *
  * M == 0 or N == 0: no-op.  K == 0: D is filled with zeros.
  * A and B rows must start on 16-byte boundaries (K a multiple of 8, or lda/ldb

@@ -21,7 +21,7 @@ def _traced(lib, A_bits, B_bits, out, tile, sched, **kw):
     M, N = A_bits.shape[0], B_bits.shape[0]
     info = lib.ts_gemm_launch_info(M, N, A_bits.shape[1], lib.TS_OUT_F32 if out == torch.float32 else lib.TS_OUT_BF16,
                                    sched, tile=tile, **kw)
-    trace = torch.zeros(4 * info["num_tiles"], dtype=torch.int64, device="cuda")
+    trace = torch.zeros(4 * info["num_units"], dtype=torch.int64, device="cuda")
     D = torch.full((M, N), float("nan"), dtype=out, device="cuda")
     lib.ts_gemm_bf16_ex(to_device_bf16(A_bits), to_device_bf16(B_bits), D, sched=sched, tile=tile, trace=trace,
                         **kw)
@@ -37,9 +37,9 @@ def test_static_owner_follows_grid_stride_rule(lib, tile, max_workers):
     B = synth.int_uniform_bf16(302, (N, K))
     info, tr, D = _traced(lib, A, B, torch.float32, tile, "static", max_workers=max_workers)
     if max_workers:
-        assert info["workers"] == min(max_workers, info["num_tiles"])
-    assert np.all(tr[:, 0] == 1), "a tile was not visited exactly once"
-    assert np.array_equal(tr[:, 1], oracle.static_owner(info["num_tiles"], info["workers"]))
+        assert info["workers"] == min(max_workers, info["num_units"])
+    assert np.all(tr[:, 0] == 1), "a work unit was not visited exactly once"
+    assert np.array_equal(tr[:, 1], oracle.static_owner(info["num_units"], info["workers"]))
     assert np.all(tr[:, 3] >= tr[:, 2])
     assert_bit_exact(D, oracle.gemm_f64(A, B), f"static {tile}")
 
@@ -50,11 +50,11 @@ def test_clc_covers_every_tile_once(lib, tile):
     A = synth.int_uniform_bf16(311, (M, K))
     B = synth.int_uniform_bf16(312, (N, K))
     info, tr, D = _traced(lib, A, B, torch.bfloat16, tile, "clc")
-    assert info["grid_ctas"] == info["num_tiles"] * info["cluster"]
+    assert info["grid_ctas"] == info["num_units"] * info["cluster"]
     ok, why = oracle.clc_coverage_ok(tr[:, 0], tr[:, 1])
     assert ok, why
-    # work stealing happened: fewer workers ran than there are tiles
-    assert np.unique(tr[:, 1]).size < info["num_tiles"]
+    # work stealing happened: fewer workers ran than there are units
+    assert np.unique(tr[:, 1]).size < info["num_units"]
     ref = oracle.gemm_f64_blas(A, B)
     assert_bit_exact(D, ref, f"clc {tile}")
 
@@ -70,7 +70,7 @@ def test_results_identical_while_sms_are_held(lib, sched):
     started = torch.zeros(1, dtype=torch.int32).pin_memory()
     ctas = 32
     info = lib.ts_gemm_launch_info(M, N, K, lib.TS_OUT_F32, sched, tile="128x256")
-    trace = torch.zeros(4 * info["num_tiles"], dtype=torch.int64, device="cuda")
+    trace = torch.zeros(4 * info["num_units"], dtype=torch.int64, device="cuda")
     D = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
     torch.cuda.synchronize()
     lib.ts_spin(ctas, 20_000_000, started, stream=side)
@@ -85,7 +85,7 @@ def test_results_identical_while_sms_are_held(lib, sched):
         ok, why = oracle.clc_coverage_ok(tr[:, 0], tr[:, 1])
         assert ok, why
     else:
-        assert np.array_equal(tr[:, 1], oracle.static_owner(info["num_tiles"], info["workers"]))
+        assert np.array_equal(tr[:, 1], oracle.static_owner(info["num_units"], info["workers"]))
 
 
 def test_spin_rejects_bad_arguments(lib):

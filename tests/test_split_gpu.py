@@ -1,0 +1,88 @@
+"""The split tail: the last, partial wave of tiles split along K across idle workers.
+
+Each part writes an fp32 partial to the workspace; the warp that finishes a
+32-row slab last sums the parts in part order and stores D, then re-arms the
+slab counter.  Integer inputs must stay bit-exact, random inputs within the
+bound, the result must not depend on which part finished last, and the
+workspace must come back zeroed.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from parity import as_f64, assert_bit_exact, assert_within_bound, bf16_bits, to_device_bf16
+
+pytestmark = pytest.mark.gpu
+
+# (tile, M, N, K): each leaves a partial last wave on a 152-SM GB300
+CASES = [("128x256", 4096, 4096, 1024), ("256x256", 4096, 5120, 1024), ("128x128", 2600, 2900, 640)]
+
+
+def _info(lib, M, N, K, out, sched, tile, ws):
+    return lib.ts_gemm_launch_info(M, N, K, out, sched, tile=tile, workspace=ws)
+
+
+@pytest.mark.parametrize("tile,M,N,K", CASES)
+@pytest.mark.parametrize("sched", ["static", "clc"])
+def test_split_tail_integer_bit_exact_and_workspace_rearmed(lib, tile, M, N, K, sched):
+    A = synth.int_uniform_bf16(801, (M, K))
+    B = synth.int_uniform_bf16(802, (N, K))
+    need = _info(lib, M, N, K, lib.TS_OUT_F32, sched, tile, None)["workspace_bytes"]
+    assert need > 0, "case must leave a partial last wave"
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    info = _info(lib, M, N, K, lib.TS_OUT_F32, sched, tile, ws)
+    assert info["split_tiles"] > 0 and info["split_parts"] >= 2
+    assert info["num_units"] == info["num_tiles"] + info["split_tiles"] * (info["split_parts"] - 1)
+    trace = torch.zeros(4 * info["num_units"], dtype=torch.int64, device="cuda")
+    D = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    lib.ts_gemm_bf16_ex(to_device_bf16(A), to_device_bf16(B), D, sched=sched, tile=tile, workspace=ws, trace=trace)
+    lib.ts_sync_and_check()
+    assert_bit_exact(D, oracle.gemm_f64_blas(A, B), f"split {tile} {sched}")
+    tr = trace.view(-1, 4).cpu().numpy()
+    if sched == "static":
+        assert np.all(tr[:, 0] == 1)
+        assert np.array_equal(tr[:, 1], oracle.static_owner(info["num_units"], info["workers"]))
+    else:
+        ok, why = oracle.clc_coverage_ok(tr[:, 0], tr[:, 1])
+        assert ok, why
+    # counters re-armed: the workspace's counter region (first 8 KiB) is zero again
+    assert torch.all(ws[:8192] == 0)
+
+
+@pytest.mark.parametrize("tile,M,N,K", CASES)
+@pytest.mark.parametrize("out", [torch.float32, torch.bfloat16])
+def test_split_tail_random_within_bound_and_deterministic(lib, tile, M, N, K, out):
+    A = synth.uniform_pm1_bf16(811, (M, K))
+    B = synth.uniform_pm1_bf16(812, (N, K))
+    ref = oracle.gemm_f64_blas(A, B)
+    S = oracle.gemm_f64_blas(A, B, absolute=True)
+    Ad, Bd = to_device_bf16(A), to_device_bf16(B)
+    results = []
+    for sched in ("clc", "static", "clc"):
+        D = torch.full((M, N), float("nan"), dtype=out, device="cuda")
+        lib.ts_gemm_bf16_ex(Ad, Bd, D, sched=sched, tile=tile)  # cached workspace
+        lib.ts_sync_and_check()
+        assert_within_bound(as_f64(D), ref, S, out, f"split {tile} {sched} {out}")
+        results.append(bf16_bits(D) if out == torch.bfloat16 else D.cpu().numpy())
+    # same units, same summation order: repeatable bit for bit
+    assert np.array_equal(results[0], results[2])
+    # without a workspace the tail is not split; the result stays within the bound
+    D = torch.full((M, N), float("nan"), dtype=out, device="cuda")
+    lib.ts_gemm_bf16_ex(Ad, Bd, D, sched="static", tile=tile, workspace=None)
+    lib.ts_sync_and_check()
+    assert_within_bound(as_f64(D), ref, S, out, f"unsplit {tile} {out}")
+
+
+def test_split_needs_enough_k(lib):
+    # 4 k-blocks cannot be split into parts of at least 4 k-blocks
+    info = lib.ts_gemm_launch_info(4096, 4096, 256, lib.TS_OUT_BF16, "static", tile="128x256")
+    assert info["split_tiles"] == 0 and info["workspace_bytes"] == 0
+
+
+def test_split_disabled_by_option(lib):
+    ws = torch.zeros(64 << 20, dtype=torch.uint8, device="cuda")
+    info = lib.ts_gemm_launch_info(4096, 4096, 1024, lib.TS_OUT_BF16, "static", tile="128x256", workspace=ws,
+                                   split_tail=-1)
+    assert info["split_tiles"] == 0 and info["num_units"] == info["num_tiles"]

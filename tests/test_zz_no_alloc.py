@@ -27,7 +27,7 @@ def test_no_alloc_entry_point_matches_existing_entry_point(lib, sched):
 
     D_old = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
     info = lib.ts_gemm_launch_info(M, N, K, lib.TS_OUT_F32, sched)
-    trace = torch.zeros(4 * info["num_tiles"], dtype=torch.int64, device="cuda")
+    trace = torch.zeros(4 * info["num_units"], dtype=torch.int64, device="cuda")
     lib.ts_gemm_bf16_ex(A, B, D_old, sched=sched, trace=trace)
     lib.ts_sync_and_check()
     assert np.all(trace.view(-1, 4)[:, 0].cpu().numpy() == 1)

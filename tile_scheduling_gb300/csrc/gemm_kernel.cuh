@@ -173,8 +173,35 @@ struct Smem {
     }
 };
 
+// One work unit: a whole output tile, or one K-range of a split tail tile.
+struct Unit {
+    int32_t tile;      // output tile id (raster order)
+    int32_t kb0, kb1;  // k-blocks [kb0, kb1)
+    int32_t tail;      // index among the split tail tiles, or -1 for a whole tile
+    int32_t part;      // K part of a split tile
+};
+
+__device__ __forceinline__ Unit decode_unit(int32_t u, const GemmParams &p) {
+    Unit w;
+    if (u < p.full_tiles) {
+        w.tile = u;
+        w.kb0 = 0;
+        w.kb1 = p.num_k_blocks;
+        w.tail = -1;
+        w.part = 0;
+    } else {
+        const int32_t v = u - p.full_tiles;
+        w.tail = v / p.parts;
+        w.part = v - w.tail * p.parts;
+        w.tile = p.full_tiles + w.tail;
+        w.kb0 = static_cast<int32_t>(static_cast<int64_t>(w.part) * p.num_k_blocks / p.parts);
+        w.kb1 = static_cast<int32_t>(static_cast<int64_t>(w.part + 1) * p.num_k_blocks / p.parts);
+    }
+    return w;
+}
+
 // Consume the next CLC response (one thread per consuming role).  Returns the
-// next tile, or -1 when the cancel failed (no pending launch left) or the
+// next work unit, or -1 when the cancel failed (no pending launch left) or the
 // kernel is aborting.
 template <class C>
 __device__ __forceinline__ int32_t clc_consume(const Smem<C> &sm, const GemmParams &p, uint32_t &idx) {
@@ -194,11 +221,11 @@ __device__ __forceinline__ int32_t clc_consume(const Smem<C> &sm, const GemmPara
 }
 
 template <class C>
-__device__ __forceinline__ int32_t next_tile(const Smem<C> &sm, const GemmParams &p, int32_t tile,
+__device__ __forceinline__ int32_t next_unit(const Smem<C> &sm, const GemmParams &p, int32_t unit,
                                              uint32_t &clc_idx) {
     if (p.sched == SCHED_STATIC) {
-        const int32_t t = tile + static_cast<int32_t>(gridDim.x / C::CG);
-        return t < p.num_tiles ? t : -1;
+        const int32_t u = unit + static_cast<int32_t>(gridDim.x / C::CG);
+        return u < p.num_units ? u : -1;
     }
     return clc_consume(sm, p, clc_idx);
 }
@@ -208,6 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmD, const __grid_constant__ GemmParams p) {
     using C = GemmCfg<BN, CG, OUT>;
+    constexpr int RAW = C::SUB_COLS;  // fp32 accumulator words per lane per store subtile
     extern __shared__ __align__(1024) uint8_t smem_raw[];
 
     const uint32_t raw = smem_u32(smem_raw);
@@ -263,21 +291,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(sm.tmem_slot);
 
-    const int32_t first_tile = worker < p.num_tiles ? worker : -1;
+    const int32_t first_unit = worker < p.num_units ? worker : -1;
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
-            int32_t tile = first_tile;
+            int32_t unit = first_unit;
             uint32_t clc_idx = 0, stage = 0, phase = 0, issued = 0;
             bool alive = true;
-            while (tile >= 0 && alive) {
+            while (unit >= 0 && alive) {
+                const Unit w = decode_unit(unit, p);
                 int32_t mb, nb;
-                raster(tile, p, mb, nb);
+                raster(w.tile, p, mb, nb);
                 const int32_t a_row = mb * C::TILE_M + static_cast<int32_t>(rank) * C::BM;
                 const int32_t b_row = nb * BN + static_cast<int32_t>(rank) * C::B_ROWS;
-                if (p.trace && rank == 0) p.trace[4 * tile + 2] = static_cast<long long>(globaltimer());
-                for (int32_t kb = 0; kb < p.num_k_blocks; ++kb) {
+                if (p.trace && rank == 0) p.trace[4 * unit + 2] = static_cast<long long>(globaltimer());
+                for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!wait_phase(sm.empty(stage), phase ^ 1u, sm.abort_flag, p, WAIT_PRODUCER_EMPTY)) {
                         alive = false;
                         break;
@@ -300,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (!alive) break;
-                tile = next_tile(sm, p, tile, clc_idx);
+                unit = next_unit(sm, p, unit, clc_idx);
             }
             // Drain: every issued load has landed (even CTA's full barriers) and
             // the MMA has released every stage.
@@ -323,14 +352,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
         if (lane == 0 && rank == 0) {
-            int32_t tile = first_tile;
+            int32_t unit = first_unit;
             uint32_t clc_idx = 0, stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool alive = true;
-            while (tile >= 0 && alive) {
+            while (unit >= 0 && alive) {
+                const Unit w = decode_unit(unit, p);
                 if (!wait_phase(sm.tempty(acc), acc_phase ^ 1u, sm.abort_flag, p, WAIT_MMA_TMEM_EMPTY)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
-                for (int32_t kb = 0; kb < p.num_k_blocks; ++kb) {
+                for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!wait_phase(sm.full(stage), phase, sm.abort_flag, p, WAIT_MMA_FULL)) {
                         alive = false;
                         break;
@@ -340,8 +370,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t db = sw128_kmajor_desc(sm.b + stage * C::B_BYTES);
 #pragma unroll
                     for (int kk = 0; kk < C::BK / C::UMMA_K; ++kk) {
-                        // +32 bytes per K = 16 step inside the 128-byte swizzle row (encoded >> 4)
-                        mma_bf16<CG>(d_tmem, da + 2u * kk, db + 2u * kk, C::IDESC, (kb | kk) != 0);
+                        // +32 bytes per K = 16 step inside the 128-byte swizzle row (encoded >> 4);
+                        // the first MMA of a unit overwrites the accumulator
+                        mma_bf16<CG>(d_tmem, da + 2u * kk, db + 2u * kk, C::IDESC, (kb != w.kb0) || (kk != 0));
                     }
                     if constexpr (CG == 1)
                         mma_commit(sm.empty(stage));
@@ -361,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     acc = 0;
                     acc_phase ^= 1u;
                 }
-                tile = next_tile(sm, p, tile, clc_idx);
+                unit = next_unit(sm, p, unit, clc_idx);
             }
             // Every MMA issued by this thread has completed before TMEM is freed.
             if constexpr (CG == 1)
@@ -373,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp == 2) {
         // ------------------------------------------------- CLC scheduler
-        if (lane == 0 && p.sched == SCHED_CLC && first_tile >= 0) {
+        if (lane == 0 && p.sched == SCHED_CLC && first_unit >= 0) {
             uint32_t idx = 0;
             bool outstanding = false;
             uint32_t out_r = 0, out_ph = 0;
@@ -411,36 +442,89 @@ __global__ void __launch_bounds__(kThreads, 1)
         // --------------------------------------------------------- epilogue
         const int q = warp - 4;  // TMEM lane quarter this warp may access
         const uint32_t stg = sm.epi + static_cast<uint32_t>(q) * 2u * C::EPI_BUF;
-        int32_t tile = first_tile;
+        int32_t unit = first_unit;
         uint32_t clc_idx = 0, acc = 0, acc_phase = 0, buf = 0;
-        while (tile >= 0) {
+
+        // Convert one subtile of fp32 accumulator words and write it to D.
+        // Subtiles wholly outside D are skipped (no staging write, no store
+        // group).  A TMA store is used only for boxes whose columns lie inside
+        // D: the store clips rows exactly but a ragged right edge only to
+        // 16-byte granules, so a subtile that crosses N takes plain stores.
+        auto emit = [&](const uint32_t (&v)[RAW], int32_t row0, int32_t col) {
+            if (row0 >= p.M || col >= p.N) return;
+            uint32_t w[32];
+            if constexpr (OUT == OUT_F32) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) w[j] = v[j];
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) w[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
+            }
+            if (p.tma_store && col + C::SUB_COLS <= p.N) {
+                if (lane == 0) bulk_wait_read<1>();  // the store that used this buffer has read it
+                __syncwarp();
+                const uint32_t row_addr = stg + buf * C::EPI_BUF + static_cast<uint32_t>(lane) * 128u;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    st_shared_v4(row_addr + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4), w[4 * j], w[4 * j + 1],
+                                 w[4 * j + 2], w[4 * j + 3]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(&tmD, stg + buf * C::EPI_BUF, col, row0);
+                    bulk_commit();
+                }
+                buf ^= 1u;
+            } else {
+                const int32_t row = row0 + lane;
+                if (row < p.M) {
+                    if constexpr (OUT == OUT_F32) {
+                        float *dst = static_cast<float *>(p.D) + static_cast<int64_t>(row) * p.ldd + col;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (col + j < p.N) dst[j] = __uint_as_float(w[j]);
+                    } else {
+                        uint16_t *dst = static_cast<uint16_t *>(p.D) + static_cast<int64_t>(row) * p.ldd + col;
+#pragma unroll
+                        for (int j = 0; j < 64; ++j)
+                            if (col + j < p.N) dst[j] = static_cast<uint16_t>(w[j >> 1] >> (16 * (j & 1)));
+                    }
+                }
+            }
+        };
+        // fp32 partial of one warp slab (32 rows x BN) of a split unit, laid out so
+        // that every warp-wide 16-byte access covers 512 contiguous bytes.
+        auto slab_of = [&](const Unit &w, int32_t part) -> float4 * {
+            const int64_t slab = (static_cast<int64_t>(w.tail) * p.parts + part) * (CG * 4) + rank * 4 + q;
+            return reinterpret_cast<float4 *>(p.partials + slab * (32 * BN));
+        };
+
+        while (unit >= 0) {
+            const Unit w = decode_unit(unit, p);
             int32_t mb, nb;
-            raster(tile, p, mb, nb);
+            raster(w.tile, p, mb, nb);
             const int32_t row0 = mb * C::TILE_M + static_cast<int32_t>(rank) * C::BM + 32 * q;
             const int32_t col0 = nb * BN;
+            const bool split = w.tail >= 0;
             int ok = 1;
             if (lane == 0) ok = wait_phase(sm.tfull(acc), acc_phase, sm.abort_flag, p, WAIT_EPI_TMEM_FULL);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             tc_fence_after();
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + acc * BN;
+            float4 *const mine = split ? slab_of(w, w.part) : nullptr;
 #pragma unroll 1
             for (int s = 0; s < C::NUM_SUB; ++s) {
-                uint32_t w[32];
-                if constexpr (OUT == OUT_F32) {
-                    tmem_ld_32x32b_x32(taddr + s * 32, w);
-                    tmem_ld_wait();
+                uint32_t v[RAW];
+                if constexpr (RAW == 32) {
+                    tmem_ld_32x32b_x32(taddr + s * 32, v);
                 } else {
-                    uint32_t lo[32], hi[32];
-                    tmem_ld_32x32b_x32(taddr + s * 64, lo);
-                    tmem_ld_32x32b_x32(taddr + s * 64 + 32, hi);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        w[j] = pack_bf16x2(lo[2 * j], lo[2 * j + 1]);
-                        w[16 + j] = pack_bf16x2(hi[2 * j], hi[2 * j + 1]);
-                    }
+                    uint32_t(&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[0]);
+                    uint32_t(&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[32]);
+                    tmem_ld_32x32b_x32(taddr + s * RAW, lo);
+                    tmem_ld_32x32b_x32(taddr + s * RAW + 32, hi);
                 }
+                tmem_ld_wait();
                 if (s == C::NUM_SUB - 1) {
                     // accumulator fully read: hand it back to the MMA issuer
                     tc_fence_before();
@@ -452,57 +536,80 @@ __global__ void __launch_bounds__(kThreads, 1)
                             mbar_arrive_cluster(mapa(sm.tempty(acc), 0));
                     }
                 }
-                const int32_t col = col0 + s * C::SUB_COLS;
-                // Subtiles wholly outside D are skipped (no staging write, no
-                // store group).  A TMA store is used only for boxes whose
-                // columns lie inside D: the store clips rows exactly but a
-                // ragged right edge only to 16-byte granules, so a subtile that
-                // crosses N is written with plain predicated stores instead.
-                if (row0 >= p.M || col >= p.N) continue;
-                if (p.tma_store && col + C::SUB_COLS <= p.N) {
-                    if (lane == 0) bulk_wait_read<1>();  // the store that used this buffer has read it
-                    __syncwarp();
-                    const uint32_t row_addr = stg + buf * C::EPI_BUF + static_cast<uint32_t>(lane) * 128u;
+                if (split) {
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        st_shared_v4(row_addr + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4), w[4 * j],
-                                     w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        tma_store_2d(&tmD, stg + buf * C::EPI_BUF, col, row0);
-                        bulk_commit();
-                    }
-                    buf ^= 1u;
+                    for (int c = 0; c < RAW / 4; ++c)
+                        __stcg(mine + (s * (RAW / 4) + c) * 32 + lane,
+                               make_float4(__uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
+                                           __uint_as_float(v[4 * c + 2]), __uint_as_float(v[4 * c + 3])));
                 } else {
-                    const int32_t row = row0 + lane;
-                    if (row < p.M) {
-                        if constexpr (OUT == OUT_F32) {
-                            float *dst = static_cast<float *>(p.D) + static_cast<int64_t>(row) * p.ldd + col;
+                    emit(v, row0, col0 + s * C::SUB_COLS);
+                }
+            }
+            if (split) {
+                // The last of the `parts` warps to finish this slab sums the
+                // partials in part order and stores D; it also re-arms the counter.
+                __threadfence();
+                __syncwarp();
+                int last = 0;
+                if (lane == 0) {
+                    int32_t *cnt = p.counters + (w.tail * CG + static_cast<int32_t>(rank)) * 4 + q;
+                    last = atomicAdd(cnt, 1) == p.parts - 1;
+                    if (last) atomicExch(cnt, 0);
+                }
+                last = __shfl_sync(0xffffffffu, last, 0);
+                if (last) {
+                    __threadfence();
+#pragma unroll 1
+                    for (int s = 0; s < C::NUM_SUB; ++s) {
+                        uint32_t v[RAW];
+                        // 32 columns at a time: every part's 8 float4 per lane are in
+                        // flight together, then summed in part order 0, 1, ...
 #pragma unroll
-                            for (int j = 0; j < 32; ++j)
-                                if (col + j < p.N) dst[j] = __uint_as_float(w[j]);
-                        } else {
-                            uint16_t *dst = static_cast<uint16_t *>(p.D) + static_cast<int64_t>(row) * p.ldd + col;
+                        for (int ch = 0; ch < RAW / 32; ++ch) {
+                            float4 x[kMaxParts][8];
 #pragma unroll
-                            for (int j = 0; j < 64; ++j)
-                                if (col + j < p.N) dst[j] = static_cast<uint16_t>(w[j >> 1] >> (16 * (j & 1)));
+                            for (int pp = 0; pp < kMaxParts; ++pp) {
+                                if (pp < p.parts) {
+                                    const float4 *src = slab_of(w, pp) + (s * (RAW / 4) + ch * 8) * 32 + lane;
+#pragma unroll
+                                    for (int c = 0; c < 8; ++c) x[pp][c] = __ldcg(src + c * 32);
+                                }
+                            }
+#pragma unroll
+                            for (int c = 0; c < 8; ++c) {
+                                float4 a = x[0][c];
+#pragma unroll
+                                for (int pp = 1; pp < kMaxParts; ++pp) {
+                                    if (pp < p.parts) {
+                                        a.x += x[pp][c].x;
+                                        a.y += x[pp][c].y;
+                                        a.z += x[pp][c].z;
+                                        a.w += x[pp][c].w;
+                                    }
+                                }
+                                v[ch * 32 + 4 * c] = __float_as_uint(a.x);
+                                v[ch * 32 + 4 * c + 1] = __float_as_uint(a.y);
+                                v[ch * 32 + 4 * c + 2] = __float_as_uint(a.z);
+                                v[ch * 32 + 4 * c + 3] = __float_as_uint(a.w);
+                            }
                         }
+                        emit(v, row0, col0 + s * C::SUB_COLS);
                     }
                 }
             }
             if (p.trace && rank == 0 && q == 0 && lane == 0) {
-                atomicAdd(reinterpret_cast<unsigned long long *>(&p.trace[4 * tile]), 1ull);
-                p.trace[4 * tile + 1] = worker;
-                p.trace[4 * tile + 3] = static_cast<long long>(globaltimer());
+                atomicAdd(reinterpret_cast<unsigned long long *>(&p.trace[4 * unit]), 1ull);
+                p.trace[4 * unit + 1] = worker;
+                p.trace[4 * unit + 3] = static_cast<long long>(globaltimer());
             }
             if (++acc == 2) {
                 acc = 0;
                 acc_phase ^= 1u;
             }
-            int32_t nt = 0;
-            if (lane == 0) nt = next_tile(sm, p, tile, clc_idx);
-            tile = __shfl_sync(0xffffffffu, nt, 0);
+            int32_t nu = 0;
+            if (lane == 0) nu = next_unit(sm, p, unit, clc_idx);
+            unit = __shfl_sync(0xffffffffu, nu, 0);
         }
         if (lane == 0) bulk_wait<0>();
         __syncwarp();

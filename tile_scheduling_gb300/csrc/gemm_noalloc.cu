@@ -79,16 +79,16 @@ extern "C" ts_status ts_gemm_bf16_checked_noalloc(const void *A, const void *B, 
     ts_launch_info info;
     ts_status s = ts_gemm_launch_info(M, N, K, out_dtype, sched, nullptr, &info);
     if (s != TS_OK) return s;
-    if (info.num_tiles > kNoAllocMaxTiles)
+    if (info.num_units > kNoAllocMaxTiles)
         return fail(TS_ERR_UNSUPPORTED,
                     "%lld output tiles exceed the %lld-tile scratch of the no-allocation entry point; "
                     "use ts_gemm_bf16_ex with a caller-allocated trace",
-                    static_cast<long long>(info.num_tiles), static_cast<long long>(kNoAllocMaxTiles));
+                    static_cast<long long>(info.num_units), static_cast<long long>(kNoAllocMaxTiles));
     long long *trace = nullptr;
     if ((s = scratch_address(&trace)) != TS_OK) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     // No tile is scheduled when the output is empty or K == 0 (zero fill).
-    const int64_t tiles = (M == 0 || N == 0 || K == 0) ? 0 : info.num_tiles;
+    const int64_t tiles = (M == 0 || N == 0 || K == 0) ? 0 : info.num_units;
     if (tiles > 0) {
         const int blocks = static_cast<int>(std::min<int64_t>((4 * tiles + 255) / 256, 1024));
         clear_trace_kernel<<<blocks, 256, 0, st>>>(trace, 4 * tiles);

@@ -24,9 +24,20 @@ enum : int32_t {
 //   [2] number of timed-out waits since the last check
 constexpr int kStatusWords = 4;
 
+// Most K parts a split tail tile is cut into: the reduction loads every part
+// of a 32-column chunk at once, so this bounds its registers.
+constexpr int kMaxParts = 4;
+
+// Work units: units [0, full_tiles) are whole tiles (unit u = tile u).  The
+// last split_tiles tiles are each split along K into `parts` units; unit
+// full_tiles + t * parts + p covers k-blocks [p * nk / parts, (p + 1) * nk / parts)
+// of tile full_tiles + t.  Split units write fp32 partials to `workspace`; the
+// warp that finishes a 32-row slab last (per-slab counter) sums the parts in
+// order 0..parts-1 and stores D.
 struct GemmParams {
     int32_t M, N, K;
     int32_t tiles_m, tiles_n, num_tiles, num_k_blocks;
+    int32_t num_units, full_tiles, split_tiles, parts;
     int32_t raster_group;  // >= 1
     int32_t sched;         // SCHED_STATIC / SCHED_CLC
     int32_t tma_store;     // 1: TMA-store epilogue, 0: st.global epilogue
@@ -37,7 +48,9 @@ struct GemmParams {
     uint64_t timeout_ns;   // per-wait limit
     uint64_t drain_ns;     // limit for waiting on copies still in flight at exit
     unsigned long long *status;
-    long long *trace;      // 4 int64 per tile, or nullptr
+    long long *trace;      // 4 int64 per work unit, or nullptr
+    int32_t *counters;     // split_tiles * CG * 4 slab counters (zero between launches)
+    float *partials;       // split_tiles * parts * CG * 4 slabs of 32 x BN fp32
 };
 
 }  // namespace ts
