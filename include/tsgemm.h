@@ -84,6 +84,52 @@ typedef struct {
     int64_t workspace_bytes; /* workspace a split tail needs (0 when no split would help) */
 } ts_launch_info;
 
+/* The barrier protocol of one kernel variant: the numbers the kernel
+ * initialises its mbarriers with.  The host-side protocol checker
+ * (tile_scheduling_gb300/protocol.py) models the role loops with them. */
+typedef struct {
+    int32_t cluster;             /* CTAs per worker */
+    int32_t stages;              /* shared-memory ring depth S */
+    int32_t tx_bytes;            /* transaction bytes per stage on the even CTA's full barrier */
+    int32_t full_arrivals;       /* arrivals that complete a full[s] phase (besides the tx bytes) */
+    int32_t empty_arrivals;      /* arrivals that complete an empty[s] phase */
+    int32_t accumulators;        /* TMEM accumulator buffers */
+    int32_t tmem_full_arrivals;  /* arrivals on tmem_full[a] */
+    int32_t tmem_empty_arrivals; /* arrivals on the even CTA's tmem_empty[a] */
+    int32_t clc_slots;           /* CLC response slots */
+    int32_t clc_full_arrivals;   /* arrivals (besides the response bytes) on a CTA's clc_full[r] */
+    int32_t clc_empty_arrivals;  /* arrivals on the even CTA's clc_empty[r]: every consuming role */
+    int32_t clc_response_bytes;
+    int32_t epilogue_warps;      /* epilogue warps per CTA */
+    int32_t stage_bytes;         /* A + B bytes one CTA loads per stage */
+} ts_gemm_protocol;
+
+/* Fill *proto for the kernel variant of `tile` (TS_TILE_128x128, _128x256 or
+ * _256x256_2CTA; TS_TILE_AUTO is TS_ERR_INVALID_ARG) and `out_dtype`.  Host
+ * only; needs no GPU. */
+ts_status ts_gemm_protocol_info(int32_t tile, int32_t out_dtype, ts_gemm_protocol *proto);
+
+/*
+ * ts_protocol_check -- explore every interleaving of a small mbarrier program
+ * (host only).  Restates the idea of the Task Scheduling static verifier
+ * (CUTLASS TS "Introduction": schedules are checked for deadlocks and races
+ * before lowering); tile_scheduling_gb300/protocol.py builds the programs from
+ * this kernel's role loops and ts_gemm_protocol_info.
+ *
+ *   nbars, bar_expected  barriers and the arrivals that complete each phase
+ *   nbufs                buffers (ring stages, TMEM accumulators, CLC slots)
+ *   nroles, role_group   roles; roles of one group (>= 0) run identical programs
+ *   role_offsets         nroles + 1 offsets into ops (in records)
+ *   ops                  8-int32 records (see protocol_check.cu)
+ *   names                role, barrier and buffer names, '\n'-separated, for messages
+ *   max_states           stop after this many distinct states
+ * Returns 0 (no deadlock, no race), 1 (violation; msg says which), 2 (state
+ * limit reached), -1 (bad arguments).  *states_out = distinct states visited.
+ */
+int32_t ts_protocol_check(int32_t nbars, const int32_t *bar_expected, int32_t nbufs, int32_t nroles,
+                          const int32_t *role_group, const int32_t *role_offsets, const int32_t *ops,
+                          const char *names, int64_t max_states, int64_t *states_out, char *msg, int32_t msg_len);
+
 /*
  * ts_gemm_bf16 -- D = A * B^T with bf16 inputs and fp32 accumulation.
  *

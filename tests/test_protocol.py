@@ -1,0 +1,111 @@
+"""The host-side barrier-protocol checker (no GPU needed).
+
+The kernel's role loops, modelled with the arrival counts the kernel itself
+uses (ts_gemm_protocol_info), must be free of deadlocks and races for every
+compiled variant and both schedulers; every planted protocol mistake must be
+caught; and the engine's mbarrier semantics are pinned on tiny hand-written
+programs.
+"""
+import pytest
+
+from tile_scheduling_gb300 import protocol as pc
+
+OP = pc
+
+
+@pytest.fixture(scope="module")
+def ts():
+    import tile_scheduling_gb300 as ts
+
+    return ts
+
+
+# ------------------------------------------------------------ engine semantics
+def _prog(bars, roles, nbufs=1):
+    P = pc.Program()
+    for i, n in enumerate(bars):
+        P.bar(f"b{i}", n)
+    for i in range(nbufs):
+        P.buf(f"x{i}")
+    for name, ops in roles:
+        P.roles.append((name, None, [list(o) + [-1] * (8 - len(o)) for o in ops]))
+    return P
+
+
+def test_engine_fresh_barrier_passes_parity_one_only():
+    ok = _prog([1], [("r", [(OP.OP_WAIT, 0, 1)])])
+    assert pc.check(ok).ok
+    stuck = _prog([1], [("r", [(OP.OP_WAIT, 0, 0)])])
+    r = pc.check(stuck)
+    assert not r.ok and "deadlock" in r.message
+
+
+def test_engine_transaction_bytes_may_land_before_expect_tx():
+    # the copy's complete-tx can overtake the expect-tx; the phase still completes once
+    prog = _prog([1], [("producer", [(OP.OP_TMA, 0, 7, 0, 64), (OP.OP_ARRIVE, 0, 64)]),
+                       ("consumer", [(OP.OP_WAIT, 0, 0), (OP.OP_TREAD, 0, 7)])])
+    assert pc.check(prog).ok
+
+
+def test_engine_reports_reading_before_the_copy_landed():
+    prog = _prog([1], [("producer", [(OP.OP_ARRIVE, 0, 0), (OP.OP_TMA, 0, 7, 0, 0)]),
+                       ("consumer", [(OP.OP_WAIT, 0, 0), (OP.OP_TREAD, 0, 7)])])
+    r = pc.check(prog)
+    assert not r.ok and "read of x0" in r.message
+
+
+def test_engine_reports_over_arrival():
+    prog = _prog([1], [("a", [(OP.OP_ARRIVE, 0, 5)]), ("b", [(OP.OP_ARRIVE, 0, 0)])])
+    r = pc.check(prog)
+    assert not r.ok and "more arrivals" in r.message
+
+
+# ------------------------------------------------------------ kernel protocol
+def test_exported_counts_match_the_role_structure(ts):
+    for tile in ("128x128", "128x256", "256x256"):
+        for out in (ts.TS_OUT_BF16, ts.TS_OUT_F32):
+            p = ts.ts_gemm_protocol_info(tile, out)
+            cg, e = p["cluster"], p["epilogue_warps"]
+            assert p["tx_bytes"] == p["stage_bytes"] * cg
+            assert p["tmem_empty_arrivals"] == e * cg
+            # producer, MMA, scheduler and epilogue warps of the even CTA; producer,
+            # scheduler and epilogue warps of the odd CTA
+            assert p["clc_empty_arrivals"] == (3 + e) + (2 + e if cg == 2 else 0)
+            assert p["full_arrivals"] == p["empty_arrivals"] == p["tmem_full_arrivals"] == 1
+
+
+@pytest.mark.parametrize("tile", ["128x128", "128x256", "256x256"])
+@pytest.mark.parametrize("units", [[1], [2, 3], [3, 1, 2]])
+def test_static_protocol_verified(tile, units):
+    r = pc.check_variant(tile, units, "static", stages=2)
+    assert r.ok, r.message
+
+
+@pytest.mark.parametrize("tile", ["128x256", "256x256"])
+def test_static_protocol_verified_at_the_kernels_ring_depth(tile):
+    r = pc.check_variant(tile, [2, 3], "static")
+    assert r.ok, r.message
+
+
+@pytest.mark.parametrize("units", [[1], [2, 1], [1, 2, 1]])
+def test_clc_protocol_verified_one_cta(units):
+    r = pc.check_variant("128x256", units, "clc")
+    assert r.ok, r.message
+
+
+@pytest.mark.parametrize("units", [[1], [2, 1], [1, 1, 2]])
+def test_clc_protocol_verified_cta_pair(units):
+    # one epilogue warp per CTA modelled; the barriers expect the others' arrivals fewer
+    r = pc.check_variant("256x256", units, "clc", stages=2, epilogue_warps=1)
+    assert r.ok, r.message
+
+
+@pytest.mark.parametrize("mutation", pc.MUTATIONS)
+@pytest.mark.parametrize("tile,sched,warps", [("128x256", "clc", None), ("256x256", "clc", 1),
+                                              ("256x256", "static", 2)])
+def test_planted_mistakes_are_caught(mutation, tile, sched, warps):
+    r = pc.check_variant(tile, [2, 1, 2], sched, stages=2, epilogue_warps=warps, mutate=mutation)
+    if mutation == "clc_empty_count_low" and sched == "static":
+        assert r.ok  # the static scheduler never touches the CLC barriers
+    else:
+        assert not r.ok and r.status == 1, (mutation, r)

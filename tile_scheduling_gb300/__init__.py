@@ -58,6 +58,13 @@ class LaunchInfo(ctypes.Structure):
                 ("workspace_bytes", ctypes.c_int64)]
 
 
+class GemmProtocol(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "cluster", "stages", "tx_bytes", "full_arrivals", "empty_arrivals", "accumulators", "tmem_full_arrivals",
+        "tmem_empty_arrivals", "clc_slots", "clc_full_arrivals", "clc_empty_arrivals", "clc_response_bytes",
+        "epilogue_warps", "stage_bytes")]
+
+
 def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     if not os.path.exists(path):
         raise ImportError(f"libtsgemm.so not built ({path}); run python tile_scheduling_gb300/build.py")
@@ -68,6 +75,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ts_gemm_launch_info.argtypes = [I64, I64, I64, I32, I32, ctypes.POINTER(GemmOpts),
                                         ctypes.POINTER(LaunchInfo)]
     lib.ts_gemm_bf16_checked_noalloc.argtypes = [P, P, P, I64, I64, I64, I32, I32, P, P]
+    lib.ts_gemm_protocol_info.argtypes = [I32, I32, ctypes.POINTER(GemmProtocol)]
+    lib.ts_protocol_check.argtypes = [I32, P, I32, I32, P, P, P, ctypes.c_char_p, I64, ctypes.POINTER(I64),
+                                      ctypes.c_char_p, I32]
+    lib.ts_protocol_check.restype = I32
     lib.ts_copy_i16.argtypes = [P, P, I64, P]
     lib.ts_spin.argtypes = [I32, I64, P, P]
     lib.ts_spin_wait_started.argtypes = [P, I32, ctypes.c_double]
@@ -79,6 +90,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ts_last_error_detail.argtypes = []
     lib.ts_last_error_detail.restype = ctypes.c_char_p
     for name in ("ts_gemm_bf16", "ts_gemm_bf16_ex", "ts_gemm_launch_info", "ts_gemm_bf16_checked_noalloc",
+                 "ts_gemm_protocol_info",
                  "ts_copy_i16", "ts_spin",
                  "ts_spin_wait_started", "ts_sync_and_check"):
         getattr(lib, name).restype = ctypes.c_int
@@ -250,6 +262,14 @@ def ts_gemm_launch_info(M: int, N: int, K: int, out=TS_OUT_BF16, sched="static",
     return _launch_info_raw(M, N, K, out, sched, workspace=ws, split_tail=split_tail, **opts)
 
 
+def ts_gemm_protocol_info(tile="256x256", out=TS_OUT_BF16) -> dict:
+    """Barrier layout and arrival counts of a kernel variant (no GPU needed)."""
+    proto = GemmProtocol()
+    _check(_lib.ts_gemm_protocol_info(_TILE[tile] if isinstance(tile, str) else int(tile), int(out),
+                                      ctypes.byref(proto)))
+    return {f: getattr(proto, f) for f, _ in GemmProtocol._fields_}
+
+
 def ts_copy_i16(src: torch.Tensor, dst: torch.Tensor, stream=None) -> None:
     """dst[i] = src[i] for contiguous int16 CUDA tensors of equal size."""
     for t, name in ((src, "src"), (dst, "dst")):
@@ -274,6 +294,13 @@ def ts_spin(ctas: int, duration_ns: int, started: torch.Tensor, stream=None) -> 
 
 def ts_spin_wait_started(started: torch.Tensor, expected: int, timeout_s: float = 5.0) -> None:
     _check(_lib.ts_spin_wait_started(ctypes.c_void_p(started.data_ptr()), int(expected), float(timeout_s)))
+
+
+def ts_protocol_check(program, max_states: int = 20_000_000):
+    """Explore a barrier-protocol program (see tile_scheduling_gb300.protocol)."""
+    from .protocol import check
+
+    return check(program, max_states)
 
 
 def ts_sync_and_check(stream=None) -> None:

@@ -229,6 +229,22 @@ ts_status ts_gemm_launch_info(int64_t M, int64_t N, int64_t K, int32_t out_dtype
     return TS_OK;
 }
 
+ts_status ts_gemm_protocol_info(int32_t tile, int32_t out_dtype, ts_gemm_protocol *proto) {
+    if (!proto) return ts::fail(TS_ERR_INVALID_ARG, "proto is NULL");
+    if (out_dtype != TS_OUT_BF16 && out_dtype != TS_OUT_F32) return ts::fail(TS_ERR_INVALID_ARG, "out_dtype %d", out_dtype);
+    int bn, cg;
+    switch (tile) {
+        case TS_TILE_128x128: bn = 128, cg = 1; break;
+        case TS_TILE_128x256: bn = 256, cg = 1; break;
+        case TS_TILE_256x256_2CTA: bn = 256, cg = 2; break;
+        default: return ts::fail(TS_ERR_INVALID_ARG, "tile %d (an explicit tile is required)", tile);
+    }
+    const ts::GemmVariant *v = ts::find_variant(bn, cg, out_dtype);
+    if (!v) return ts::fail(TS_ERR_UNSUPPORTED, "no compiled variant for tile %d", tile);
+    *proto = v->protocol;
+    return TS_OK;
+}
+
 ts_status ts_gemm_bf16_ex(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K, int32_t out_dtype,
                           int32_t sched, const ts_gemm_opts *opts, void *stream) {
     using namespace ts;

@@ -76,9 +76,19 @@ struct GemmCfg {
     static constexpr int BAR_BYTES = 256;
     static constexpr int STAGES = (kSmemLimit - 1024 - EPI_BYTES - BAR_BYTES) / STAGE_BYTES;
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
-    // Consumers of one CLC response: producer, MMA, 4 epilogue warps and the
-    // scheduler in the even CTA; producer, 4 epilogue warps and scheduler in the odd one.
-    static constexpr int CLC_CONSUMERS = CG == 1 ? 7 : 13;
+    // Barrier arrival counts (one place: the kernel initialises its barriers
+    // with these, and the host-side protocol checker models them).
+    static constexpr int EPI_WARPS = 4;
+    static constexpr int FULL_ARRIVALS = 1;   // the even CTA's producer (arrive.expect_tx)
+    static constexpr int EMPTY_ARRIVALS = 1;  // one tcgen05.commit per stage use
+    static constexpr int TFULL_ARRIVALS = 1;  // one tcgen05.commit per accumulator use
+    static constexpr int TEMPTY_ARRIVALS = EPI_WARPS * CG;  // every epilogue warp of the CTA pair
+    static constexpr int ACCUMULATORS = 2;
+    static constexpr int CLC_FULL_ARRIVALS = 1;  // this CTA's scheduler thread arms the slot
+    static constexpr int CLC_RESPONSE_BYTES = 16;
+    // Consumers of one CLC response: producer, MMA, the epilogue warps and the
+    // scheduler in the even CTA; producer, epilogue warps and scheduler in the odd one.
+    static constexpr int CLC_CONSUMERS = (3 + EPI_WARPS) + (CG == 2 ? 2 + EPI_WARPS : 0);
     // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B bf16
     // (bits 7-9 = 1, 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at
     // bits 17-22, M >> 4 at bits 24-28.
@@ -264,16 +274,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (warp == 3 && lane == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
-            mbar_init(sm.full(s), 1);
-            mbar_init(sm.empty(s), 1);
+            mbar_init(sm.full(s), C::FULL_ARRIVALS);
+            mbar_init(sm.empty(s), C::EMPTY_ARRIVALS);
         }
-        for (int a = 0; a < 2; ++a) {
-            mbar_init(sm.tfull(a), 1);
-            mbar_init(sm.tempty(a), 4 * CG);
+        for (int a = 0; a < C::ACCUMULATORS; ++a) {
+            mbar_init(sm.tfull(a), C::TFULL_ARRIVALS);
+            mbar_init(sm.tempty(a), C::TEMPTY_ARRIVALS);
         }
         mbar_init(sm.mma_done(), 1);
         for (int r = 0; r < kMaxClcDepth; ++r) {
-            mbar_init(sm.clc_full(r), 1);
+            mbar_init(sm.clc_full(r), C::CLC_FULL_ARRIVALS);
             mbar_init(sm.clc_empty(r), C::CLC_CONSUMERS);
         }
         *sm.abort_flag = 0;
@@ -415,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (rank == 0) {
                     if (!wait_phase(sm.clc_empty(r), ph ^ 1u, sm.abort_flag, p, WAIT_SCHED_CLC_EMPTY)) break;
                     fence_proxy_async_smem();
-                    mbar_arrive_expect_tx(sm.clc_full(r), 16);
+                    mbar_arrive_expect_tx(sm.clc_full(r), C::CLC_RESPONSE_BYTES);
                     if constexpr (CG == 1)
                         clc_try_cancel(sm.resp + 16u * r, sm.clc_full(r));
                     else
@@ -425,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     out_ph = ph;
                 } else {
                     // the even CTA's request multicasts its response here: arm our barrier for it
-                    mbar_arrive_expect_tx(sm.clc_full(r), 16);
+                    mbar_arrive_expect_tx(sm.clc_full(r), C::CLC_RESPONSE_BYTES);
                 }
                 const int32_t t = clc_consume(sm, p, idx);
                 outstanding = false;
@@ -440,6 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp >= 4) {
         // --------------------------------------------------------- epilogue
+        static_assert(C::EPI_WARPS == 4 && kThreads == 256, "warps 4-7 are the epilogue warpgroup");
         const int q = warp - 4;  // TMEM lane quarter this warp may access
         const uint32_t stg = sm.epi + static_cast<uint32_t>(q) * 2u * C::EPI_BUF;
         int32_t unit = first_unit;

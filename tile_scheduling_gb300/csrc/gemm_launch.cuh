@@ -25,6 +25,23 @@ struct GemmInstance {
         return e;
     }
 
+    static constexpr ts_gemm_protocol protocol() {
+        return ts_gemm_protocol{CG,
+                                C::STAGES,
+                                C::TX_BYTES,
+                                C::FULL_ARRIVALS,
+                                C::EMPTY_ARRIVALS,
+                                C::ACCUMULATORS,
+                                C::TFULL_ARRIVALS,
+                                C::TEMPTY_ARRIVALS,
+                                kMaxClcDepth,
+                                C::CLC_FULL_ARRIVALS,
+                                C::CLC_CONSUMERS,
+                                C::CLC_RESPONSE_BYTES,
+                                C::EPI_WARPS,
+                                C::A_BYTES + C::B_BYTES};
+    }
+
     static cudaError_t launch(const GemmLaunch &L) {
         cudaError_t e = prepare();
         if (e != cudaSuccess) return e;
@@ -86,6 +103,7 @@ struct GemmInstance {
                               OUT,                                                                         \
                               GemmCfg<BN, CG, OUT>::STAGES,                                                \
                               GemmCfg<BN, CG, OUT>::SMEM_BYTES,                                            \
+                              GemmInstance<BN, CG, OUT>::protocol(),                                       \
                               &GemmInstance<BN, CG, OUT>::launch,                                          \
                               &GemmInstance<BN, CG, OUT>::max_workers};                                    \
     }

@@ -1,0 +1,355 @@
+// Explicit-state checker of mbarrier protocols (host code only).
+//
+// The CUTLASS Task Scheduling pages check a captured schedule statically for
+// deadlocks and races before lowering it ("Introduction", the verifier behind
+// TaskManager.print_and_verify).  tile_scheduling_gb300/protocol.py restates
+// this library's GEMM role loops as small programs over mbarriers and buffers;
+// this engine explores every interleaving of those programs and of the
+// asynchronous units they drive, depth first, keeping a 64-bit hash of each
+// visited state (hash compaction).
+//
+// Program model.  Barriers start in phase 0 with `expected` pending arrivals
+// and no transaction bytes.  A phase completes when pending arrivals and
+// transaction bytes both reach zero (complete-tx may run ahead of the matching
+// expect-tx and drive the count below zero).  A wait on parity P passes while
+// the number of completed phases has the other parity.  Op records are 8
+// int32 wide:
+//   WAIT   bar parity            ARRIVE bar tx_bytes (expect-tx, then arrive)
+//   TMA    buf tag bar bytes     -> async: buf := tag, then complete-tx(bar)
+//   MMA    sbuf0 sbuf1 acc tag   -> in-order queue: sbufs must hold tag; a tag
+//                                   with k-block > 0 must find tag - 1 in acc
+//   COMMIT bar0 bar1             -> in-order queue: one arrival on each bar
+//   TREAD  buf tag               buf must hold tag
+//   CREQ   slot0 slot1 seq bar0 bar1 bytes  -> async: slots := seq, complete-tx
+//   CREAD  buf seq               buf must hold seq
+// (negative operands mean "none"; tags are unit * 1024 + k-block.)  A role step
+// runs one wait or arrive plus the ops after it that only enqueue work or, after
+// a wait, only check a buffer: their effects become visible later, through the
+// queue or the async completions, which are explored separately.
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "common.h"
+
+namespace ts {
+namespace {
+
+enum : int32_t { OP_WAIT = 0, OP_ARRIVE, OP_TMA, OP_MMA, OP_COMMIT, OP_TREAD, OP_CREQ, OP_CREAD };
+constexpr int kRec = 8;
+constexpr int kMaxQueue = 32;
+constexpr int kMaxAsync = 32;
+
+struct Model {
+    int nbars, nbufs, nroles;
+    const int32_t *expected, *group, *off, *ops;
+    std::vector<std::string> role_name, bar_name, buf_name;
+    // state layout offsets
+    int o_pc, o_bar, o_buf, o_mq, o_asy, len;
+};
+
+struct Checker {
+    const Model &m;
+    std::vector<uint64_t> table;
+    uint64_t mask;
+    int64_t states = 0, max_states;
+    std::string msg;
+
+    Checker(const Model &mm, int64_t maxs) : m(mm), max_states(maxs) {
+        uint64_t cap = 1024;
+        while (cap < static_cast<uint64_t>(2 * maxs + 2)) cap <<= 1;
+        table.assign(cap, 0);
+        mask = cap - 1;
+    }
+
+    static uint64_t hash(const std::vector<int32_t> &s) {
+        uint64_t h = 0x9E3779B97F4A7C15ull;
+        for (int32_t v : s) {
+            h ^= static_cast<uint32_t>(v);
+            h *= 0x100000001B3ull;
+            h ^= h >> 29;
+        }
+        return h ? h : 1;
+    }
+
+    bool insert(const std::vector<int32_t> &s) {  // true if new
+        uint64_t h = hash(s);
+        for (uint64_t i = h & mask;; i = (i + 1) & mask) {
+            if (table[i] == h) return false;
+            if (table[i] == 0) {
+                table[i] = h;
+                ++states;
+                return true;
+            }
+        }
+    }
+
+    void canon(std::vector<int32_t> &s) const {
+        // copies in flight form a set: keep them sorted
+        std::sort(s.begin() + m.o_asy + 1, s.begin() + m.o_asy + 1 + s[m.o_asy]);
+        // roles of one symmetry group run identical programs: keep their pcs sorted
+        for (int i = 0; i < m.nroles; ++i) {
+            if (m.group[i] < 0) continue;
+            for (int j = i + 1; j < m.nroles; ++j)
+                if (m.group[j] == m.group[i] && s[m.o_pc + j] < s[m.o_pc + i]) std::swap(s[m.o_pc + i], s[m.o_pc + j]);
+        }
+    }
+
+    const int32_t *op(int idx) const { return m.ops + static_cast<int64_t>(idx) * kRec; }
+
+    // returns false on over-arrival
+    bool arrive(std::vector<int32_t> &s, int b, int tx) const {
+        int32_t *bs = &s[m.o_bar + 3 * b];
+        bs[1] -= 1;
+        bs[2] += tx;
+        if (bs[1] < 0) return false;
+        if (bs[1] == 0 && bs[2] == 0) {
+            bs[0] += 1;
+            bs[1] = m.expected[b];
+        }
+        return true;
+    }
+    void complete_tx(std::vector<int32_t> &s, int b, int bytes) const {
+        int32_t *bs = &s[m.o_bar + 3 * b];
+        bs[2] -= bytes;
+        if (bs[1] == 0 && bs[2] == 0) {
+            bs[0] += 1;
+            bs[1] = m.expected[b];
+        }
+    }
+    bool push_list(std::vector<int32_t> &s, int o, int cap, int v) const {
+        int32_t &n = s[o];
+        if (n >= cap) return false;
+        s[o + 1 + n] = v;
+        ++n;
+        return true;
+    }
+
+    bool violation(const std::string &what) {
+        msg = what;
+        return false;
+    }
+
+    // Successors of `s`; false if a violation was found (msg set).
+    bool expand(const std::vector<int32_t> &s, std::vector<std::vector<int32_t>> &out, bool &any) {
+        any = false;
+        std::vector<std::pair<int, int>> tried;  // (group, pc)
+        for (int i = 0; i < m.nroles; ++i) {
+            int pc = s[m.o_pc + i];
+            const int end = m.off[i + 1] - m.off[i];
+            if (pc >= end) continue;
+            if (m.group[i] >= 0) {
+                std::pair<int, int> key(m.group[i], pc);
+                if (std::find(tried.begin(), tried.end(), key) != tried.end()) continue;
+                tried.push_back(key);
+            }
+            std::vector<int32_t> t = s;
+            bool first = true, arrived = false;
+            while (pc < end) {
+                const int32_t *o = op(m.off[i] + pc);
+                const int kind = o[0];
+                if ((kind == OP_WAIT || kind == OP_ARRIVE) && !first) break;
+                if ((kind == OP_TREAD || kind == OP_CREAD) && arrived) break;
+                if (kind == OP_WAIT) {
+                    if (t[m.o_bar + 3 * o[1]] % 2 == o[2]) break;
+                } else if (kind == OP_ARRIVE) {
+                    if (!arrive(t, o[1], o[2]))
+                        return violation(m.role_name[i] + ": more arrivals than " + m.bar_name[o[1]] +
+                                         " expects in a phase");
+                    arrived = true;
+                } else if (kind == OP_TMA || kind == OP_CREQ) {
+                    if (!push_list(t, m.o_asy, kMaxAsync, m.off[i] + pc)) return violation("too many copies in flight");
+                } else if (kind == OP_MMA || kind == OP_COMMIT) {
+                    if (!push_list(t, m.o_mq, kMaxQueue, m.off[i] + pc)) return violation("tcgen05 queue too deep");
+                } else if (kind == OP_TREAD) {
+                    if (t[m.o_buf + o[1]] != o[2]) {
+                        char b[256];
+                        snprintf(b, sizeof b, "%s: read of %s found tag %d, expected the finished tile %d",
+                                 m.role_name[i].c_str(), m.buf_name[o[1]].c_str(), t[m.o_buf + o[1]], o[2]);
+                        return violation(b);
+                    }
+                } else if (kind == OP_CREAD) {
+                    if (t[m.o_buf + o[1]] != o[2]) {
+                        char b[256];
+                        snprintf(b, sizeof b, "%s: %s holds response %d, expected response %d",
+                                 m.role_name[i].c_str(), m.buf_name[o[1]].c_str(), t[m.o_buf + o[1]], o[2]);
+                        return violation(b);
+                    }
+                }
+                ++pc;
+                first = false;
+            }
+            if (first) continue;  // blocked at its first op
+            t[m.o_pc + i] = pc;
+            out.push_back(std::move(t));
+            any = true;
+        }
+        // asynchronous copies and CLC responses complete in any order
+        const int na = s[m.o_asy];
+        for (int k = 0; k < na; ++k) {
+            const int idx = s[m.o_asy + 1 + k];
+            bool dup = false;
+            for (int j = 0; j < k; ++j) dup |= s[m.o_asy + 1 + j] == idx;
+            if (dup) continue;
+            std::vector<int32_t> t = s;
+            // remove entry k
+            for (int j = k; j < na - 1; ++j) t[m.o_asy + 1 + j] = t[m.o_asy + 2 + j];
+            t[m.o_asy + na] = -1;
+            t[m.o_asy] = na - 1;
+            const int32_t *o = op(idx);
+            if (o[0] == OP_TMA) {
+                const int nq = s[m.o_mq];
+                for (int q = 0; q < nq; ++q) {
+                    const int32_t *mo = op(s[m.o_mq + 1 + q]);
+                    if (mo[0] == OP_MMA && (mo[1] == o[1] || mo[2] == o[1])) {
+                        char b[256];
+                        snprintf(b, sizeof b, "copy of tag %d overwrote %s before the queued MMA of tag %d read it",
+                                 o[2], m.buf_name[o[1]].c_str(), mo[4]);
+                        return violation(b);
+                    }
+                }
+                t[m.o_buf + o[1]] = o[2];
+                complete_tx(t, o[3], o[4]);
+            } else {
+                for (int j = 1; j <= 2; ++j)
+                    if (o[j] >= 0) t[m.o_buf + o[j]] = o[3];
+                for (int j = 4; j <= 5; ++j)
+                    if (o[j] >= 0) complete_tx(t, o[j], o[6]);
+            }
+            out.push_back(std::move(t));
+            any = true;
+        }
+        // the tcgen05 queue executes in order
+        const int nq = s[m.o_mq];
+        if (nq > 0) {
+            std::vector<int32_t> t = s;
+            for (int j = 0; j < nq - 1; ++j) t[m.o_mq + 1 + j] = t[m.o_mq + 2 + j];
+            t[m.o_mq + nq] = -1;
+            t[m.o_mq] = nq - 1;
+            const int32_t *o = op(s[m.o_mq + 1]);
+            if (o[0] == OP_MMA) {
+                const int tag = o[4];
+                for (int j = 1; j <= 2; ++j) {
+                    if (o[j] >= 0 && s[m.o_buf + o[j]] != tag) {
+                        char b[256];
+                        snprintf(b, sizeof b, "MMA of tag %d read %s holding tag %d", tag, m.buf_name[o[j]].c_str(),
+                                 s[m.o_buf + o[j]]);
+                        return violation(b);
+                    }
+                }
+                if ((tag % 1024) > 0 && s[m.o_buf + o[3]] != tag - 1) {
+                    char b[256];
+                    snprintf(b, sizeof b, "MMA of tag %d accumulated onto tag %d in %s", tag, s[m.o_buf + o[3]],
+                             m.buf_name[o[3]].c_str());
+                    return violation(b);
+                }
+                t[m.o_buf + o[3]] = tag;
+            } else {
+                for (int j = 1; j <= 2; ++j)
+                    if (o[j] >= 0 && !arrive(t, o[j], 0))
+                        return violation("commit: more arrivals than " + m.bar_name[o[j]] + " expects in a phase");
+            }
+            out.push_back(std::move(t));
+            any = true;
+        }
+        return true;
+    }
+
+    int run() {
+        std::vector<int32_t> s0(m.len, 0);
+        for (int b = 0; b < m.nbars; ++b) s0[m.o_bar + 3 * b + 1] = m.expected[b];
+        for (int x = 0; x < m.nbufs; ++x) s0[m.o_buf + x] = -1;
+        for (int k = 0; k < kMaxQueue; ++k) s0[m.o_mq + 1 + k] = -1;
+        for (int k = 0; k < kMaxAsync; ++k) s0[m.o_asy + 1 + k] = -1;
+        insert(s0);
+        std::vector<std::vector<int32_t>> stack{s0}, succ;
+        while (!stack.empty()) {
+            std::vector<int32_t> s = std::move(stack.back());
+            stack.pop_back();
+            succ.clear();
+            bool any = false;
+            if (!expand(s, succ, any)) return 1;
+            if (!any) {
+                std::string blocked;
+                for (int i = 0; i < m.nroles; ++i) {
+                    const int pc = s[m.o_pc + i];
+                    if (pc >= m.off[i + 1] - m.off[i]) continue;
+                    const int32_t *o = op(m.off[i] + pc);
+                    if (!blocked.empty()) blocked += "; ";
+                    blocked += m.role_name[i] + (o[0] == OP_WAIT ? " waiting on " + m.bar_name[o[1]] : " stuck");
+                }
+                if (!blocked.empty()) {
+                    msg = "deadlock: " + blocked;
+                    return 1;
+                }
+                continue;  // every role finished, nothing in flight
+            }
+            for (auto &t : succ) {
+                canon(t);
+                if (insert(t)) {
+                    if (states > max_states) {
+                        msg = "state limit reached";
+                        return 2;
+                    }
+                    stack.push_back(std::move(t));
+                }
+            }
+        }
+        msg = "no deadlock, no race";
+        return 0;
+    }
+};
+
+std::vector<std::string> split_lines(const char *s) {
+    std::vector<std::string> v;
+    std::string cur;
+    for (; s && *s; ++s) {
+        if (*s == '\n') {
+            v.push_back(cur);
+            cur.clear();
+        } else {
+            cur += *s;
+        }
+    }
+    v.push_back(cur);
+    return v;
+}
+
+}  // namespace
+}  // namespace ts
+
+extern "C" int32_t ts_protocol_check(int32_t nbars, const int32_t *bar_expected, int32_t nbufs, int32_t nroles,
+                                     const int32_t *role_group, const int32_t *role_offsets, const int32_t *ops,
+                                     const char *names, int64_t max_states, int64_t *states_out, char *msg,
+                                     int32_t msg_len) {
+    using namespace ts;
+    if (nbars < 0 || nbufs < 0 || nroles <= 0 || !bar_expected || !role_group || !role_offsets || !ops ||
+        max_states <= 0 || !msg || msg_len <= 0)
+        return -1;
+    Model m;
+    m.nbars = nbars;
+    m.nbufs = nbufs;
+    m.nroles = nroles;
+    m.expected = bar_expected;
+    m.group = role_group;
+    m.off = role_offsets;
+    m.ops = ops;
+    std::vector<std::string> nm = split_lines(names);
+    if (static_cast<int>(nm.size()) < nroles + nbars + nbufs) nm.resize(nroles + nbars + nbufs, "?");
+    m.role_name.assign(nm.begin(), nm.begin() + nroles);
+    m.bar_name.assign(nm.begin() + nroles, nm.begin() + nroles + nbars);
+    m.buf_name.assign(nm.begin() + nroles + nbars, nm.begin() + nroles + nbars + nbufs);
+    m.o_pc = 0;
+    m.o_bar = nroles;
+    m.o_buf = m.o_bar + 3 * nbars;
+    m.o_mq = m.o_buf + nbufs;
+    m.o_asy = m.o_mq + 1 + kMaxQueue;
+    m.len = m.o_asy + 1 + kMaxAsync;
+    Checker c(m, max_states);
+    const int rc = c.run();
+    if (states_out) *states_out = c.states;
+    snprintf(msg, static_cast<size_t>(msg_len), "%s", c.msg.c_str());
+    return rc;
+}

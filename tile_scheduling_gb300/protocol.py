@@ -1,0 +1,213 @@
+"""Host-side checker of the GEMM kernel's barrier protocol.
+
+The CUTLASS Task Scheduling pages check a captured schedule for deadlocks,
+races and barrier initialisation before lowering it ("Introduction",
+TaskManager.print_and_verify).  This kernel has no captured schedule: its role
+loops are plain CUDA.  This module restates those loops -- TMA producer of each
+CTA, the MMA issuer, the epilogue warps of each CTA and, under Cluster Launch
+Control, the scheduler and every role's consumption of the responses -- as
+small programs over mbarriers and buffers, with the arrival counts and
+transaction bytes the kernel itself initialises its barriers with
+(ts_gemm_protocol_info).  The native engine ts_protocol_check then explores
+every interleaving of the roles and of the asynchronous units they drive (TMA
+completions in any order, the in-order tcgen05 queue and its commits, CLC
+responses) and reports
+
+* a deadlock: no role can move and nothing is in flight, before every role
+  has finished;
+* a race: an MMA reads a ring stage that does not hold the k-block it expects
+  (overwritten early or not yet landed) or accumulates onto the wrong partial
+  sum, an epilogue reads an accumulator that is not the finished tile, or a
+  CLC response slot is refilled before every role read it.
+
+A model is one worker (a CTA, or a CTA pair) over a short sequence of work
+units.  Epilogue warps run identical, independent programs, so a model may
+keep fewer of them than the kernel has; the barriers they arrive on then
+expect exactly the removed warps' arrivals fewer, so a miscount in the
+kernel's constants still shows.
+"""
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass, field
+
+import numpy as np
+
+from . import _lib
+
+OP_WAIT, OP_ARRIVE, OP_TMA, OP_MMA, OP_COMMIT, OP_TREAD, OP_CREQ, OP_CREAD = range(8)
+MUTATIONS = ("tmem_empty_count_low", "tmem_empty_count_high", "clc_empty_count_low", "tx_bytes_one_cta",
+             "producer_wait_parity", "epilogue_release_before_read", "mma_skip_stage_release")
+
+
+def _tag(unit: int, kb: int) -> int:
+    return unit * 1024 + kb
+
+
+@dataclass
+class Program:
+    bars: list = field(default_factory=list)
+    bar_names: list = field(default_factory=list)
+    bufs: list = field(default_factory=list)
+    roles: list = field(default_factory=list)  # (name, group or None, [op records])
+
+    def bar(self, name: str, count: int) -> int:
+        self.bars.append(int(count))
+        self.bar_names.append(name)
+        return len(self.bars) - 1
+
+    def buf(self, name: str) -> int:
+        self.bufs.append(name)
+        return len(self.bufs) - 1
+
+
+def build_program(proto: dict, units: list, sched: str = "static", epilogue_warps: int | None = None,
+                  stages: int | None = None, mutate: str | None = None) -> Program:
+    """The kernel's role loops for one worker.
+
+    proto           ts_gemm_protocol_info() of the variant.
+    units           k-blocks of each work unit the worker processes, in order.
+    sched           "static", or "clc": after each unit every role consumes one
+                    response; the first len(units) - 1 name a unit, the last fails.
+    epilogue_warps  epilogue warps per CTA to model (default: the kernel's).
+    stages          ring depth to model (default: the kernel's).
+    mutate          plant one protocol mistake (MUTATIONS), for the checker's tests.
+    """
+    if mutate is not None and mutate not in MUTATIONS:
+        raise ValueError(f"unknown mutation {mutate}")
+    cg = proto["cluster"]
+    S = stages or proto["stages"]
+    E = proto["epilogue_warps"] if epilogue_warps is None else epilogue_warps
+    dropped = (proto["epilogue_warps"] - E) * cg  # epilogue warps of the worker not modelled
+    A, R = proto["accumulators"], proto["clc_slots"]
+    P = Program()
+    full = [[P.bar(f"full[{c}][{s}]", proto["full_arrivals"]) for s in range(S)] for c in range(cg)]
+    empty = [[P.bar(f"empty[{c}][{s}]", proto["empty_arrivals"]) for s in range(S)] for c in range(cg)]
+    tfull = [[P.bar(f"tmem_full[{c}][{a}]", proto["tmem_full_arrivals"]) for a in range(A)] for c in range(cg)]
+    tempty_n = proto["tmem_empty_arrivals"] - dropped + {"tmem_empty_count_low": -1,
+                                                          "tmem_empty_count_high": 1}.get(mutate, 0)
+    tempty = [P.bar(f"tmem_empty[{a}]", tempty_n) for a in range(A)]
+    clc_full = [[P.bar(f"clc_full[{c}][{r}]", proto["clc_full_arrivals"]) for r in range(R)] for c in range(cg)]
+    clc_empty_n = proto["clc_empty_arrivals"] - dropped - (1 if mutate == "clc_empty_count_low" else 0)
+    clc_empty = [P.bar(f"clc_empty[{r}]", clc_empty_n) for r in range(R)]
+    stage = [[P.buf(f"stage[{c}][{s}]") for s in range(S)] for c in range(cg)]
+    accb = [P.buf(f"tmem[{a}]") for a in range(A)]
+    slot = [[P.buf(f"clc_slot[{c}][{r}]") for r in range(R)] for c in range(cg)]
+    tx = proto["tx_bytes"] - (proto["stage_bytes"] if mutate == "tx_bytes_one_cta" else 0)
+    clc = sched == "clc"
+
+    def rec(*v):
+        v = list(v) + [-1] * (8 - len(v))
+        return v[:8]
+
+    def consume(ops, c, k):
+        r, ph = k % R, (k // R) & 1
+        ops += [rec(OP_WAIT, clc_full[c][r], ph), rec(OP_CREAD, slot[c][r], k), rec(OP_ARRIVE, clc_empty[r], 0)]
+
+    def adv(i, ph, n):
+        return (0, ph ^ 1) if i + 1 == n else (i + 1, ph)
+
+    for c in range(cg):  # producer of each CTA
+        ops, s, ph, issued = [], 0, 0, 0
+        for u, nk in enumerate(units):
+            for kb in range(nk):
+                ops.append(rec(OP_WAIT, empty[c][s], ph if mutate == "producer_wait_parity" else ph ^ 1))
+                if c == 0:
+                    ops.append(rec(OP_ARRIVE, full[0][s], tx))
+                ops.append(rec(OP_TMA, stage[c][s], _tag(u, kb), full[0][s], proto["stage_bytes"]))
+                issued += 1
+                s, ph = adv(s, ph, S)
+            if clc:
+                consume(ops, c, u)
+        if c == 0:  # drain: the last issued loads landed
+            for i in range(1, min(issued, S) + 1):
+                b = issued - i
+                ops.append(rec(OP_WAIT, full[0][b % S], (b // S) & 1))
+        for _ in range(S):  # drain: the MMA released every stage
+            ops.append(rec(OP_WAIT, empty[c][s], ph ^ 1))
+            s, ph = adv(s, ph, S)
+        P.roles.append((f"producer[{c}]", None, ops))
+
+    ops, s, ph, a, aph = [], 0, 0, 0, 0  # MMA issuer of the even CTA
+    for u, nk in enumerate(units):
+        ops.append(rec(OP_WAIT, tempty[a], aph ^ 1))
+        for kb in range(nk):
+            ops.append(rec(OP_WAIT, full[0][s], ph))
+            ops.append(rec(OP_MMA, stage[0][s], stage[1][s] if cg == 2 else -1, accb[a], _tag(u, kb)))
+            if not (mutate == "mma_skip_stage_release" and u == 0 and kb == 0):
+                ops.append(rec(OP_COMMIT, empty[0][s], empty[1][s] if cg == 2 else -1))
+            s, ph = adv(s, ph, S)
+        ops.append(rec(OP_COMMIT, tfull[0][a], tfull[1][a] if cg == 2 else -1))
+        a, aph = adv(a, aph, A)
+        if clc:
+            consume(ops, 0, u)
+    P.roles.append(("mma", None, ops))
+
+    for c in range(cg):  # epilogue warps of each CTA: one symmetry group per CTA
+        for w in range(E):
+            ops, a, aph = [], 0, 0
+            for u, nk in enumerate(units):
+                ops.append(rec(OP_WAIT, tfull[c][a], aph))
+                read = rec(OP_TREAD, accb[a], _tag(u, nk - 1))
+                release = rec(OP_ARRIVE, tempty[a], 0)
+                ops += [release, read] if mutate == "epilogue_release_before_read" else [read, release]
+                a, aph = adv(a, aph, A)
+                if clc:
+                    consume(ops, c, u)
+            P.roles.append((f"epilogue[{c}][{w}]", f"epilogue[{c}]", ops))
+
+    if clc:  # CLC scheduler of each CTA; the even CTA's request fills every CTA's slot
+        for c in range(cg):
+            ops = []
+            for k in range(len(units)):
+                r, ph2 = k % R, (k // R) & 1
+                if c == 0:
+                    ops += [rec(OP_WAIT, clc_empty[r], ph2 ^ 1),
+                            rec(OP_ARRIVE, clc_full[0][r], proto["clc_response_bytes"]),
+                            rec(OP_CREQ, slot[0][r], slot[1][r] if cg == 2 else -1, k, clc_full[0][r],
+                                clc_full[1][r] if cg == 2 else -1, proto["clc_response_bytes"])]
+                else:
+                    ops.append(rec(OP_ARRIVE, clc_full[c][r], proto["clc_response_bytes"]))
+                consume(ops, c, k)
+            P.roles.append((f"scheduler[{c}]", None, ops))
+    return P
+
+
+@dataclass
+class Result:
+    ok: bool
+    status: int  # 0 verified, 1 violation, 2 state limit
+    states: int
+    message: str
+
+
+def check(P: Program, max_states: int = 20_000_000) -> Result:
+    """Explore every interleaving of the program with the native engine."""
+    groups = {}
+    role_group = [(-1 if g is None else groups.setdefault(g, len(groups))) for _, g, _ in P.roles]
+    offsets = [0]
+    flat = []
+    for _, _, ops in P.roles:
+        flat += ops
+        offsets.append(len(flat))
+    ops = np.ascontiguousarray(np.array(flat, dtype=np.int32).reshape(-1))
+    bars = np.ascontiguousarray(np.array(P.bars, dtype=np.int32))
+    grp = np.ascontiguousarray(np.array(role_group, dtype=np.int32))
+    off = np.ascontiguousarray(np.array(offsets, dtype=np.int32))
+    names = "\n".join([n for n, _, _ in P.roles] + P.bar_names + P.bufs).encode()
+    msg = ctypes.create_string_buffer(512)
+    states = ctypes.c_int64(0)
+    rc = _lib.ts_protocol_check(len(P.bars), bars.ctypes.data, len(P.bufs), len(P.roles), grp.ctypes.data,
+                                off.ctypes.data, ops.ctypes.data, names, int(max_states), ctypes.byref(states), msg,
+                                len(msg))
+    if rc < 0:
+        raise ValueError("ts_protocol_check rejected the program")
+    return Result(rc == 0, rc, int(states.value), msg.value.decode())
+
+
+def check_variant(tile: str, units: list, sched: str = "static", out: int = 0, max_states: int = 20_000_000,
+                  **kw) -> Result:
+    """Check the protocol of a compiled kernel variant on a unit sequence."""
+    from . import ts_gemm_protocol_info
+
+    return check(build_program(ts_gemm_protocol_info(tile, out), units, sched, **kw), max_states)
