@@ -320,6 +320,47 @@ def run_gemm4096(args, ws, rank, local):
             "peak_bf16_tflops_burst": peaks["bf16_tflops"], "peak_source": peaks["source"]}
 
 
+def run_grouped(args, ws, rank, local):
+    """Grouped GEMM whose 16 groups differ in K (64..8192, skewed): static persistent vs CLC."""
+    import torch
+
+    import tile_scheduling_gb300 as ts
+
+    torch.cuda.set_device(local)
+    w = synth.GROUPED
+    off = w.k_offsets()
+    A_bits, B_bits = w.inputs()
+    A = torch.from_numpy(A_bits.view(np.int16)).view(torch.bfloat16).cuda()
+    B = torch.from_numpy(B_bits.view(np.int16)).view(torch.bfloat16).cuda()
+    D = torch.empty((w.groups, w.M, w.N), dtype=torch.bfloat16, device="cuda")
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    flops = 2.0 * w.M * w.N * off[-1]
+    res = {}
+    times = {"static": [], "clc": []}
+    for sched in times:
+        for _ in range(args.warmup):
+            ts.ts_gemm_bf16_grouped(A, B, D, off, sched=sched, tile=args.tile)
+    for _ in range(args.steps):  # alternate so clock drift hits both alike
+        for sched in times:
+            flush.zero_()
+            times[sched].append(_event_ms(lambda: ts.ts_gemm_bf16_grouped(A, B, D, off, sched=sched, tile=args.tile),
+                                          stream))
+    ts.ts_sync_and_check()
+    for sched, v in times.items():
+        med = statistics.median(v)
+        res[sched] = {"ms_median": round(med, 4), "ms_min": round(min(v), 4),
+                      "tflops": round(flops / (med * 1e-3) / 1e12, 1)}
+    if rank != 0:
+        return None
+    return {"metric": "grouped bf16 GEMM TFLOP/s, 16 groups of 2048x2048, K per group 64..8192 (skewed)",
+            "unit": "TFLOP/s", "value": res["clc"]["tflops"], "static": res["static"], "clc": res["clc"],
+            "clc_speedup_over_static": round(res["static"]["ms_median"] / res["clc"]["ms_median"], 3),
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "dtype": "bf16",
+            "data": "synthetic", "config": {"workload": w.name, "k_offsets": off, "tile": args.tile,
+                                            "l2": "256 MiB buffer written between launches"}}
+
+
 def run_contended(args, ws, rank, local):
     """Ragged 8191x6143x4096 fp32-out GEMM while a spin kernel holds 32 SMs for half the solo GEMM time.
 
@@ -516,7 +557,7 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--workload", default="headline", choices=["headline", "gemm4096", "contended"])
+    ap.add_argument("--workload", default="headline", choices=["headline", "gemm4096", "contended", "grouped"])
     ap.add_argument("--reps", type=int, default=10)
     ap.add_argument("--spin-ctas", type=int, default=32)
     args = ap.parse_args(argv)
@@ -541,6 +582,8 @@ def main(argv=None):
             line = run_gemm4096(args, ws, rank, local)
         elif args.workload == "contended":
             line = run_contended(args, ws, rank, local)
+        elif args.workload == "grouped":
+            line = run_grouped(args, ws, rank, local)
         else:
             line = run_ours(args, ws, rank, local)
     finally:

@@ -166,6 +166,37 @@ ts_status ts_gemm_bf16(const void *A, const void *B, void *D, int64_t M, int64_t
 ts_status ts_gemm_bf16_ex(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K,
                           int32_t out_dtype, int32_t sched, const ts_gemm_opts *opts, void *stream);
 
+/*
+ * ts_gemm_bf16_grouped -- a grouped GEMM whose groups differ in K:
+ *
+ *   D[g][i][j] = sum_{k_offsets[g] <= k < k_offsets[g+1]} A[i][k] * B[j][k],   0 <= g < groups
+ *
+ * The per-tile domain of the K loop comes from an offsets array (CUTLASS TS
+ * "Schedules", Dynamic Domain: get_domain_size(tile) = offsets[t + 1] - offsets[t]),
+ * so tiles of different groups cost different amounts -- the situation in which
+ * Cluster Launch Control work stealing pays off ("Cluster Launch Control", when
+ * to use CLC).  This is the shape of, e.g., a per-expert weight gradient, where
+ * each expert sees a different number of tokens.
+ *
+ *   A          device, bf16 [M][lda], columns 0 .. k_offsets[groups] used
+ *   B          device, bf16 [N][ldb]
+ *   D          device, [groups][M][ldd] (group g starts g * M * ldd elements in), bf16 or fp32
+ *   k_offsets  HOST array of groups + 1 non-decreasing multiples of 64 (a group
+ *              may be empty: its D is zero)
+ *   groups     1 .. 256
+ * opts as for ts_gemm_bf16_ex (tile, max_workers, lda/ldb/ldd, timeout_s, trace
+ * with 4 * num_units entries); the split tail is not used.  Work units are the
+ * tiles of group 0, then of group 1, ...
+ */
+ts_status ts_gemm_bf16_grouped(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t groups,
+                               const int64_t *k_offsets, int32_t out_dtype, int32_t sched, const ts_gemm_opts *opts,
+                               void *stream);
+
+/* The launch ts_gemm_bf16_grouped would make (host only). */
+ts_status ts_gemm_grouped_launch_info(int64_t M, int64_t N, int64_t groups, const int64_t *k_offsets,
+                                      int32_t out_dtype, int32_t sched, const ts_gemm_opts *opts,
+                                      ts_launch_info *info);
+
 /* Fill *info with the launch ts_gemm_bf16_ex would make (no launch, no sync). */
 ts_status ts_gemm_launch_info(int64_t M, int64_t N, int64_t K, int32_t out_dtype, int32_t sched,
                               const ts_gemm_opts *opts, ts_launch_info *info);

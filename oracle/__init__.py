@@ -16,6 +16,8 @@ Functions and the passages they follow:
   contraction step, for sizes the loop cannot finish in seconds.
 * ``bf16_rne``: float64 -> bf16 round-to-nearest-even (IEEE 754), the
   conversion the bf16-output epilogue applies to the fp32 accumulator.
+* ``grouped_gemm_f64``: the same sum per group over that group's K slice
+  (TS "Schedules", Dynamic Domain: a per-tile loop bound from an offsets array).
 * ``copy_i16``: dst[gid] = src[gid] for gid < n (TS "Resources", the int16
   copy example; TS "Schedules", the grid-stride domain).
 * ``static_schedule`` / ``static_owner``: worker w takes tiles w, w+W, ...
@@ -155,6 +157,27 @@ def gemm_f64_blas(A_bits, B_bits, absolute: bool = False) -> np.ndarray:
         np.abs(a, out=a)
         np.abs(b, out=b)
     return a @ b.T
+
+
+def grouped_gemm_f64(A_bits, B_bits, k_offsets, absolute: bool = False, blas: bool = False) -> np.ndarray:
+    """Grouped GEMM over K slices: D[g] = sum over k_offsets[g] <= k < k_offsets[g+1] of a[:, k] b[:, k]^T.
+
+    The per-group K range is the dynamic domain of TS "Schedules" (Dynamic
+    Domain: the loop bound comes from an offsets array).  Each group is the
+    plain triple loop (or numpy's matmul with ``blas``) on its column slice;
+    an empty group is all zeros."""
+    A = _bits(A_bits)
+    B = _bits(B_bits)
+    off = [int(x) for x in k_offsets]
+    G = len(off) - 1
+    D = np.zeros((G, A.shape[0], B.shape[0]), dtype=np.float64)
+    for g in range(G):
+        k0, k1 = off[g], off[g + 1]
+        if k1 > k0:
+            a = np.ascontiguousarray(A[:, k0:k1])
+            b = np.ascontiguousarray(B[:, k0:k1])
+            D[g] = gemm_f64_blas(a, b, absolute) if blas else gemm_f64(a, b, absolute=absolute)
+    return D
 
 
 # ---------------------------------------------------------------------- copy

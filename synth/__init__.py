@@ -178,3 +178,29 @@ GEMM_RAGGED = _w(4, "gemm 8191x6143x4096 fp32-out ragged contended", 8191, 6143,
                  ("static", "clc"))
 COPY_N = 1 << 28
 COPY_SEED = SEED_BASE + 1
+
+
+@dataclass(frozen=True)
+class GroupedWorkload:
+    """A grouped GEMM whose groups differ in K (e.g. per-expert weight gradients)."""
+
+    name: str
+    M: int
+    N: int
+    groups: int
+    seed: int
+
+    def k_offsets(self) -> list:
+        # group sizes in 64-column blocks: 1 + floor(127 u^2) -- skewed towards small groups
+        z = splitmix64(self.seed, self.groups)
+        u = (z >> np.uint64(11)).astype(np.float64) * 2.0 ** -53
+        blocks = 1 + np.floor(127.0 * u * u).astype(np.int64)
+        return [0] + [int(x) for x in np.cumsum(blocks * 64)]
+
+    def inputs(self):
+        K = self.k_offsets()[-1]
+        return (uniform_pm1_bf16(self.seed + 1, (self.M, K)), uniform_pm1_bf16(self.seed + 2, (self.N, K)))
+
+
+GROUPED = GroupedWorkload("grouped gemm 16 groups 2048x2048, K per group 64..8192 (skewed)", 2048, 2048, 16,
+                          SEED_BASE + 5)

@@ -170,6 +170,35 @@ def test_gemm_k_zero_is_zero():
     assert np.array_equal(oracle.gemm_f64(A, B), np.zeros((4, 3)))
 
 
+def test_grouped_single_group_is_the_plain_gemm():
+    A = synth.uniform_pm1_bf16(51, (17, 128))
+    B = synth.uniform_pm1_bf16(52, (13, 128))
+    assert np.array_equal(oracle.grouped_gemm_f64(A, B, [0, 128])[0], oracle.gemm_f64(A, B))
+
+
+def test_grouped_groups_sum_to_the_full_product():
+    # linearity over disjoint K slices (integer inputs: every sum is exact)
+    A = synth.int_uniform_bf16(53, (19, 448))
+    B = synth.int_uniform_bf16(54, (11, 448))
+    off = [0, 64, 64, 256, 448]
+    D = oracle.grouped_gemm_f64(A, B, off)
+    assert np.array_equal(D.sum(axis=0), oracle.gemm_f64(A, B))
+    assert np.array_equal(D[1], np.zeros((19, 11)))  # the empty group
+
+
+def test_grouped_slices_match_integer_matmul():
+    A = synth.int_uniform_bf16(55, (9, 320))
+    B = synth.int_uniform_bf16(56, (7, 320))
+    off = [64, 128, 320]
+    ai = oracle.bf16_to_f64(A).astype(np.int64)
+    bi = oracle.bf16_to_f64(B).astype(np.int64)
+    D = oracle.grouped_gemm_f64(A, B, off)
+    for g in range(2):
+        k0, k1 = off[g], off[g + 1]
+        assert np.array_equal(D[g], (ai[:, k0:k1] @ bi[:, k0:k1].T).astype(np.float64))
+    assert np.array_equal(oracle.grouped_gemm_f64(A, B, off, blas=True), D)
+
+
 # ------------------------------------------------------------------- copy
 @pytest.mark.parametrize("n", [0, 1, 7, 8, 1000, 4097])
 def test_copy_is_identity(n):

@@ -79,6 +79,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ts_protocol_check.argtypes = [I32, P, I32, I32, P, P, P, ctypes.c_char_p, I64, ctypes.POINTER(I64),
                                       ctypes.c_char_p, I32]
     lib.ts_protocol_check.restype = I32
+    lib.ts_gemm_bf16_grouped.argtypes = [P, P, P, I64, I64, I64, P, I32, I32, ctypes.POINTER(GemmOpts), P]
+    lib.ts_gemm_grouped_launch_info.argtypes = [I64, I64, I64, P, I32, I32, ctypes.POINTER(GemmOpts),
+                                                ctypes.POINTER(LaunchInfo)]
     lib.ts_copy_i16.argtypes = [P, P, I64, P]
     lib.ts_spin.argtypes = [I32, I64, P, P]
     lib.ts_spin_wait_started.argtypes = [P, I32, ctypes.c_double]
@@ -90,7 +93,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ts_last_error_detail.argtypes = []
     lib.ts_last_error_detail.restype = ctypes.c_char_p
     for name in ("ts_gemm_bf16", "ts_gemm_bf16_ex", "ts_gemm_launch_info", "ts_gemm_bf16_checked_noalloc",
-                 "ts_gemm_protocol_info",
+                 "ts_gemm_protocol_info", "ts_gemm_bf16_grouped", "ts_gemm_grouped_launch_info",
                  "ts_copy_i16", "ts_spin",
                  "ts_spin_wait_started", "ts_sync_and_check"):
         getattr(lib, name).restype = ctypes.c_int
@@ -260,6 +263,48 @@ def ts_gemm_launch_info(M: int, N: int, K: int, out=TS_OUT_BF16, sched="static",
     """The launch ts_gemm_bf16_ex would make; ``workspace`` resolves as in that call."""
     ws = _resolve_workspace(M, N, K, out, sched, workspace, split_tail, **opts)
     return _launch_info_raw(M, N, K, out, sched, workspace=ws, split_tail=split_tail, **opts)
+
+
+def _offsets(k_offsets) -> "np.ndarray":
+    import numpy as np
+
+    off = np.ascontiguousarray(np.asarray(k_offsets, dtype=np.int64))
+    if off.ndim != 1 or off.size < 2:
+        raise ValueError("k_offsets must list groups + 1 offsets")
+    return off
+
+
+def ts_gemm_grouped_launch_info(M: int, N: int, k_offsets, out=TS_OUT_BF16, sched="static", **opts) -> dict:
+    off = _offsets(k_offsets)
+    o = _opts(**opts)
+    info = LaunchInfo()
+    _check(_lib.ts_gemm_grouped_launch_info(M, N, off.size - 1, off.ctypes.data, int(out), _sched(sched),
+                                            ctypes.byref(o), ctypes.byref(info)))
+    return {f: getattr(info, f) for f, _ in LaunchInfo._fields_}
+
+
+def ts_gemm_bf16_grouped(A: torch.Tensor, B: torch.Tensor, D: torch.Tensor, k_offsets, sched="static", tile="auto",
+                         max_workers=0, timeout_s=0.0, trace=None, raster_group=0, stream=None) -> None:
+    """D[g] = A[:, k_g:k_g+1] @ B[:, k_g:k_g+1].T for every group g (k_offsets: groups + 1 multiples of 64).
+
+    A [M, >=K] and B [N, >=K] bf16 with unit column stride; D [groups, M, N]
+    bf16 or fp32 whose groups are M * ldd elements apart."""
+    off = _offsets(k_offsets)
+    G = off.size - 1
+    lda = _matrix(A, "A", torch.bfloat16)
+    ldb = _matrix(B, "B", torch.bfloat16)
+    if D.dtype not in _OUT or not D.is_cuda or D.dim() != 3 or D.stride(2) != 1:
+        raise TypeError("D must be a [groups, M, N] bf16/fp32 CUDA tensor with unit column stride")
+    M, N = A.shape[0], B.shape[0]
+    if tuple(D.shape) != (G, M, N) or (G > 1 and D.stride(0) != M * D.stride(1)):
+        raise ValueError(f"D must be [{G}, {M}, {N}] with groups M rows apart")
+    if int(off[-1]) > min(A.shape[1], B.shape[1]):
+        raise ValueError("k_offsets reach past the columns of A or B")
+    o = _opts(tile, max_workers, lda if M > 1 else 0, ldb if N > 1 else 0, D.stride(1) if M > 1 else 0, timeout_s,
+              trace, raster_group)
+    _check(_lib.ts_gemm_bf16_grouped(ctypes.c_void_p(A.data_ptr()), ctypes.c_void_p(B.data_ptr()),
+                                     ctypes.c_void_p(D.data_ptr()), M, N, G, off.ctypes.data, _OUT[D.dtype],
+                                     _sched(sched), ctypes.byref(o), _stream_handle(stream)))
 
 
 def ts_gemm_protocol_info(tile="256x256", out=TS_OUT_BF16) -> dict:

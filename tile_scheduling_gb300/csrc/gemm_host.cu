@@ -66,6 +66,28 @@ ts_status make_map(CUtensorMap *m, const void *ptr, CUtensorMapDataType dt, int 
     return TS_OK;
 }
 
+// D as a 3-D tensor [depth][rows][cols] (depth = groups, 1 for a plain GEMM)
+// stored in boxes of box_rows x box_cols x 1 with the 128-byte swizzle; the
+// store clips at `rows` inside each group.
+ts_status make_map_d(CUtensorMap *m, const void *ptr, CUtensorMapDataType dt, int esize, int64_t depth, int64_t rows,
+                     int64_t cols, int64_t ld, int box_rows, int box_cols) {
+    ts_status err = TS_OK;
+    auto fn = encode_fn(&err);
+    if (!fn) return err;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                          static_cast<cuuint64_t>(depth)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld * esize), static_cast<cuuint64_t>(rows * ld * esize)};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, dt, 3, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(TS_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled failed (%d) for D of %lld x %lld x %lld, pitch %lld B",
+                    static_cast<int>(r), static_cast<long long>(depth), static_cast<long long>(rows),
+                    static_cast<long long>(cols), static_cast<long long>(ld * esize));
+    return TS_OK;
+}
+
 template <class T>
 __global__ void zero_fill_kernel(T *D, int64_t M, int64_t N, int64_t ldd) {
     const int64_t total = M * N;
@@ -104,7 +126,7 @@ constexpr int64_t kCounterRegionBytes = 8192;
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 ts_status plan_gemm(const void *D, int64_t M, int64_t N, int64_t K, int32_t out, int32_t sched,
-                    const ts_gemm_opts *o, Plan *pl) {
+                    const ts_gemm_opts *o, Plan *pl, int64_t groups = 0) {
     if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
         return fail(TS_ERR_INVALID_ARG, "sizes must be in [0, 2^31-1] (M=%lld N=%lld K=%lld)",
                     static_cast<long long>(M), static_cast<long long>(N), static_cast<long long>(K));
@@ -151,7 +173,7 @@ ts_status plan_gemm(const void *D, int64_t M, int64_t N, int64_t K, int32_t out,
     pl->tile_n = bn;
     pl->tiles_m = cdiv(M, pl->tile_m);
     pl->tiles_n = cdiv(N, pl->tile_n);
-    pl->num_tiles = pl->tiles_m * pl->tiles_n;
+    pl->num_tiles = pl->tiles_m * pl->tiles_n * (groups > 0 ? groups : 1);
     if (pl->num_tiles * cg > kMaxDim) return fail(TS_ERR_UNSUPPORTED, "too many output tiles");
     int resident = 0;
     cudaError_t e = pl->v->max_workers(&resident);
@@ -168,7 +190,7 @@ ts_status plan_gemm(const void *D, int64_t M, int64_t N, int64_t K, int32_t out,
     pl->split_ws_bytes = 0;
     pl->counter_bytes = 0;
     pl->split = false;
-    if (o->split_tail >= 0 && K > 0 && pl->num_tiles > W) {
+    if (o->split_tail >= 0 && groups == 0 && K > 0 && pl->num_tiles > W) {
         const int64_t r = pl->num_tiles % W;
         const int64_t s =
             r > 0 ? std::min<int64_t>(std::min<int64_t>(W / r, nk / kMinKBlocksPerPart), kMaxParts) : 0;
@@ -201,14 +223,14 @@ ts_status plan_gemm(const void *D, int64_t M, int64_t N, int64_t K, int32_t out,
 }  // namespace
 }  // namespace ts
 
-extern "C" {
-
-ts_status ts_gemm_launch_info(int64_t M, int64_t N, int64_t K, int32_t out_dtype, int32_t sched,
-                              const ts_gemm_opts *opts, ts_launch_info *info) {
+namespace ts {
+ts_status fill_info(int64_t M, int64_t N, int64_t K, int32_t out_dtype, int32_t sched, const ts_gemm_opts *opts,
+                    ts_launch_info *info, int64_t groups) {
     if (!info) return ts::fail(TS_ERR_INVALID_ARG, "info is NULL");
     ts::Plan pl;
     // alignment of D is unknown here: report the TMA-store epilogue when the pitch allows it
-    ts_status s = ts::plan_gemm(reinterpret_cast<const void *>(uintptr_t(256)), M, N, K, out_dtype, sched, opts, &pl);
+    ts_status s = ts::plan_gemm(reinterpret_cast<const void *>(uintptr_t(256)), M, N, K, out_dtype, sched, opts, &pl,
+                                groups);
     if (s != TS_OK) return s;
     info->tile_m = pl.tile_m;
     info->tile_n = pl.tile_n;
@@ -228,6 +250,14 @@ ts_status ts_gemm_launch_info(int64_t M, int64_t N, int64_t K, int32_t out_dtype
     info->workspace_bytes = pl.split_ws_bytes;
     return TS_OK;
 }
+}  // namespace ts
+
+extern "C" {
+
+ts_status ts_gemm_launch_info(int64_t M, int64_t N, int64_t K, int32_t out_dtype, int32_t sched,
+                              const ts_gemm_opts *opts, ts_launch_info *info) {
+    return ts::fill_info(M, N, K, out_dtype, sched, opts, info, 0);
+}
 
 ts_status ts_gemm_protocol_info(int32_t tile, int32_t out_dtype, ts_gemm_protocol *proto) {
     if (!proto) return ts::fail(TS_ERR_INVALID_ARG, "proto is NULL");
@@ -245,26 +275,52 @@ ts_status ts_gemm_protocol_info(int32_t tile, int32_t out_dtype, ts_gemm_protoco
     return TS_OK;
 }
 
-ts_status ts_gemm_bf16_ex(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K, int32_t out_dtype,
-                          int32_t sched, const ts_gemm_opts *opts, void *stream) {
-    using namespace ts;
+}  // extern "C"
+
+namespace ts {
+namespace {
+
+// Validate a grouped GEMM's K offsets (host array of groups + 1 entries).
+ts_status check_groups(int64_t groups, const int64_t *k_offsets) {
+    if (groups < 1) return fail(TS_ERR_INVALID_ARG, "groups = %lld must be >= 1", static_cast<long long>(groups));
+    if (groups > kMaxGroups)
+        return fail(TS_ERR_UNSUPPORTED, "%lld groups exceed the %d-group limit", static_cast<long long>(groups),
+                    kMaxGroups);
+    if (!k_offsets) return fail(TS_ERR_INVALID_ARG, "k_offsets is NULL");
+    for (int64_t g = 0; g <= groups; ++g) {
+        if (k_offsets[g] < 0 || k_offsets[g] % 64 || k_offsets[g] > kMaxDim)
+            return fail(TS_ERR_INVALID_ARG, "k_offsets[%lld] = %lld must be a multiple of 64 in [0, 2^31)",
+                        static_cast<long long>(g), static_cast<long long>(k_offsets[g]));
+        if (g > 0 && k_offsets[g] < k_offsets[g - 1])
+            return fail(TS_ERR_INVALID_ARG, "k_offsets must not decrease (index %lld)", static_cast<long long>(g));
+    }
+    return TS_OK;
+}
+
+// Shared launch path.  groups == 0: plain GEMM over K.  groups > 0: group g
+// multiplies columns [k_offsets[g], k_offsets[g + 1]) of A and B into D + g * M * ldd.
+ts_status gemm_launch(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K, int32_t out_dtype,
+                      int32_t sched, const ts_gemm_opts *opts, void *stream, int64_t groups,
+                      const int64_t *k_offsets) {
     Plan pl;
-    ts_status s = plan_gemm(D, M, N, K, out_dtype, sched, opts, &pl);
+    ts_status s = plan_gemm(D, M, N, K, out_dtype, sched, opts, &pl, groups);
     if (s != TS_OK) return s;
     if (M == 0 || N == 0) return TS_OK;
+    const int64_t depth = groups > 0 ? groups : 1;
     if (!D) return fail(TS_ERR_INVALID_ARG, "D is NULL");
     const int esize = out_dtype == TS_OUT_F32 ? 4 : 2;
     if (reinterpret_cast<uintptr_t>(D) % esize) return fail(TS_ERR_INVALID_ARG, "D is not aligned to its element size");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const int64_t dbytes = ((M - 1) * pl.ldd + N) * esize;
+    const int64_t dbytes = ((depth * M - 1) * pl.ldd + N) * esize;
 
     if (K == 0) {
-        const int64_t total = M * N;
+        // every group (or the single product) is an empty sum: D = 0
+        const int64_t total = depth * M * N;
         const int blocks = static_cast<int>(std::min<int64_t>(cdiv(total, 256), 4096));
         if (out_dtype == TS_OUT_F32)
-            zero_fill_kernel<float><<<blocks, 256, 0, st>>>(static_cast<float *>(D), M, N, pl.ldd);
+            zero_fill_kernel<float><<<blocks, 256, 0, st>>>(static_cast<float *>(D), depth * M, N, pl.ldd);
         else
-            zero_fill_kernel<uint16_t><<<blocks, 256, 0, st>>>(static_cast<uint16_t *>(D), M, N, pl.ldd);
+            zero_fill_kernel<uint16_t><<<blocks, 256, 0, st>>>(static_cast<uint16_t *>(D), depth * M, N, pl.ldd);
         cudaError_t e = cudaGetLastError();
         return e == cudaSuccess ? TS_OK : cuda_fail(e, "zero-fill launch");
     }
@@ -289,7 +345,7 @@ ts_status ts_gemm_bf16_ex(const void *A, const void *B, void *D, int64_t M, int6
     if (pl.tma_store) {
         const CUtensorMapDataType dt =
             out_dtype == TS_OUT_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-        if ((s = make_map(&L.d, D, dt, esize, M, N, pl.ldd, 32, 128 / esize)) != TS_OK) return s;
+        if ((s = make_map_d(&L.d, D, dt, esize, depth, M, N, pl.ldd, 32, 128 / esize)) != TS_OK) return s;
     }
     unsigned long long *status = device_status_word(&s);
     if (!status) return s;
@@ -322,12 +378,43 @@ ts_status ts_gemm_bf16_ex(const void *A, const void *B, void *D, int64_t M, int6
     p.drain_ns = kDrainNs;
     p.status = status;
     p.trace = reinterpret_cast<long long *>(o->trace);
+    p.groups = static_cast<int32_t>(groups);
+    p.tiles_per_group = static_cast<int32_t>(pl.tiles_m * pl.tiles_n);
+    p.group_stride = M * pl.ldd;
+    for (int64_t g = 0; groups > 0 && g <= groups; ++g) p.group_kb[g] = static_cast<int32_t>(k_offsets[g] / 64);
     L.grid = static_cast<int>(pl.grid);
     L.stream = st;
     cudaError_t e = pl.v->launch(L);
     if (e != cudaSuccess) return cuda_fail(e, "GEMM launch");
     return TS_OK;
 }
+
+}  // namespace
+}  // namespace ts
+
+extern "C" {
+
+ts_status ts_gemm_bf16_ex(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K, int32_t out_dtype,
+                          int32_t sched, const ts_gemm_opts *opts, void *stream) {
+    return ts::gemm_launch(A, B, D, M, N, K, out_dtype, sched, opts, stream, 0, nullptr);
+}
+
+ts_status ts_gemm_bf16_grouped(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t groups,
+                               const int64_t *k_offsets, int32_t out_dtype, int32_t sched, const ts_gemm_opts *opts,
+                               void *stream) {
+    ts_status s = ts::check_groups(groups, k_offsets);
+    if (s != TS_OK) return s;
+    return ts::gemm_launch(A, B, D, M, N, k_offsets[groups], out_dtype, sched, opts, stream, groups, k_offsets);
+}
+
+ts_status ts_gemm_grouped_launch_info(int64_t M, int64_t N, int64_t groups, const int64_t *k_offsets,
+                                      int32_t out_dtype, int32_t sched, const ts_gemm_opts *opts,
+                                      ts_launch_info *info) {
+    ts_status s = ts::check_groups(groups, k_offsets);
+    if (s != TS_OK) return s;
+    return ts::fill_info(M, N, k_offsets[groups], out_dtype, sched, opts, info, groups);
+}
+
 
 ts_status ts_gemm_bf16(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K, int32_t out_dtype,
                        int32_t sched, void *stream) {

@@ -185,15 +185,25 @@ struct Smem {
 
 // One work unit: a whole output tile, or one K-range of a split tail tile.
 struct Unit {
-    int32_t tile;      // output tile id (raster order)
+    int32_t tile;      // output tile id within its group (raster order)
     int32_t kb0, kb1;  // k-blocks [kb0, kb1)
     int32_t tail;      // index among the split tail tiles, or -1 for a whole tile
     int32_t part;      // K part of a split tile
+    int32_t group;     // group of a grouped GEMM (0 otherwise)
 };
 
 __device__ __forceinline__ Unit decode_unit(int32_t u, const GemmParams &p) {
     Unit w;
-    if (u < p.full_tiles) {
+    w.group = 0;
+    if (p.groups > 0) {
+        // dynamic domain: the k-block range comes from the group's offsets
+        w.group = u / p.tiles_per_group;
+        w.tile = u - w.group * p.tiles_per_group;
+        w.kb0 = p.group_kb[w.group];
+        w.kb1 = p.group_kb[w.group + 1];
+        w.tail = -1;
+        w.part = 0;
+    } else if (u < p.full_tiles) {
         w.tile = u;
         w.kb0 = 0;
         w.kb1 = p.num_k_blocks;
@@ -461,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // group).  A TMA store is used only for boxes whose columns lie inside
         // D: the store clips rows exactly but a ragged right edge only to
         // 16-byte granules, so a subtile that crosses N takes plain stores.
-        auto emit = [&](const uint32_t (&v)[RAW], int32_t row0, int32_t col) {
+        auto emit = [&](const uint32_t (&v)[RAW], int32_t row0, int32_t col, int32_t group) {
             if (row0 >= p.M || col >= p.N) return;
             uint32_t w[32];
             if constexpr (OUT == OUT_F32) {
@@ -482,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    tma_store_2d(&tmD, stg + buf * C::EPI_BUF, col, row0);
+                    tma_store_3d(&tmD, stg + buf * C::EPI_BUF, col, row0, group);
                     bulk_commit();
                 }
                 buf ^= 1u;
@@ -490,12 +500,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int32_t row = row0 + lane;
                 if (row < p.M) {
                     if constexpr (OUT == OUT_F32) {
-                        float *dst = static_cast<float *>(p.D) + static_cast<int64_t>(row) * p.ldd + col;
+                        float *dst = static_cast<float *>(p.D) + group * p.group_stride +
+                                     static_cast<int64_t>(row) * p.ldd + col;
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
                             if (col + j < p.N) dst[j] = __uint_as_float(w[j]);
                     } else {
-                        uint16_t *dst = static_cast<uint16_t *>(p.D) + static_cast<int64_t>(row) * p.ldd + col;
+                        uint16_t *dst = static_cast<uint16_t *>(p.D) + group * p.group_stride +
+                                        static_cast<int64_t>(row) * p.ldd + col;
 #pragma unroll
                         for (int j = 0; j < 64; ++j)
                             if (col + j < p.N) dst[j] = static_cast<uint16_t>(w[j >> 1] >> (16 * (j & 1)));
@@ -536,6 +548,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld_32x32b_x32(taddr + s * RAW + 32, hi);
                 }
                 tmem_ld_wait();
+                if (w.kb1 == w.kb0) {
+                    // a group with K = 0: the accumulator was never written, D is zero
+#pragma unroll
+                    for (int j = 0; j < RAW; ++j) v[j] = 0u;
+                }
                 if (s == C::NUM_SUB - 1) {
                     // accumulator fully read: hand it back to the MMA issuer
                     tc_fence_before();
@@ -554,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                make_float4(__uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
                                            __uint_as_float(v[4 * c + 2]), __uint_as_float(v[4 * c + 3])));
                 } else {
-                    emit(v, row0, col0 + s * C::SUB_COLS);
+                    emit(v, row0, col0 + s * C::SUB_COLS, w.group);
                 }
             }
             if (split) {
@@ -605,7 +622,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 v[ch * 32 + 4 * c + 3] = __float_as_uint(a.w);
                             }
                         }
-                        emit(v, row0, col0 + s * C::SUB_COLS);
+                        emit(v, row0, col0 + s * C::SUB_COLS, w.group);
                     }
                 }
             }

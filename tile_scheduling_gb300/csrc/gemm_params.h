@@ -28,6 +28,10 @@ constexpr int kStatusWords = 4;
 // of a 32-column chunk at once, so this bounds its registers.
 constexpr int kMaxParts = 4;
 
+// Most groups of a grouped GEMM: the group table travels in the kernel's
+// parameter block.
+constexpr int kMaxGroups = 256;
+
 // Work units: units [0, full_tiles) are whole tiles (unit u = tile u).  The
 // last split_tiles tiles are each split along K into `parts` units; unit
 // full_tiles + t * parts + p covers k-blocks [p * nk / parts, (p + 1) * nk / parts)
@@ -51,6 +55,13 @@ struct GemmParams {
     long long *trace;      // 4 int64 per work unit, or nullptr
     int32_t *counters;     // split_tiles * CG * 4 slab counters (zero between launches)
     float *partials;       // split_tiles * parts * CG * 4 slabs of 32 x BN fp32
+    // Grouped GEMM (groups > 0): unit u is tile u % tiles_per_group of group
+    // u / tiles_per_group, whose k-blocks are [group_kb[g], group_kb[g + 1]).
+    // D of group g starts group_stride elements after D of group g - 1.
+    int32_t groups;
+    int32_t tiles_per_group;
+    int64_t group_stride;
+    int32_t group_kb[kMaxGroups + 1];
 };
 
 }  // namespace ts
