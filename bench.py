@@ -361,6 +361,55 @@ def run_grouped(args, ws, rank, local):
                                             "l2": "256 MiB buffer written between launches"}}
 
 
+def run_causal(args, ws, rank, local):
+    """8192^3 bf16 GEMM with every output tile strictly above the diagonal skipped (a causal,
+    block-sparse output): static persistent vs CLC, counting only the computed tiles' flops."""
+    import torch
+
+    import tile_scheduling_gb300 as ts
+
+    torch.cuda.set_device(local)
+    w = synth.GEMM_8192
+    A_bits, B_bits = w.inputs()
+    A = torch.from_numpy(A_bits.view(np.int16)).view(torch.bfloat16).cuda()
+    B = torch.from_numpy(B_bits.view(np.int16)).view(torch.bfloat16).cuda()
+    D = torch.zeros((w.M, w.N), dtype=torch.bfloat16, device="cuda")
+    info = ts.ts_gemm_launch_info(w.M, w.N, w.K, ts.TS_OUT_BF16, "static", tile=args.tile, workspace=None)
+    tm, tn, TM, TN = info["tile_m"], info["tile_n"], info["tiles_m"], info["tiles_n"]
+    mb = np.arange(TM)[:, None]
+    nb = np.arange(TN)[None, :]
+    mask_np = (nb * tn > mb * tm + tm - 1).astype(np.uint8)
+    mask = torch.from_numpy(mask_np.reshape(-1)).cuda()
+    computed = int((mask_np == 0).sum())
+    flops = 2.0 * tm * tn * w.K * computed
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    times = {"static": [], "clc": []}
+    kw = dict(tile=args.tile, workspace=None, skip_tiles=mask)
+    for sched in times:
+        for _ in range(args.warmup):
+            ts.ts_gemm_bf16_ex(A, B, D, sched=sched, **kw)
+    for _ in range(args.steps):
+        for sched in times:
+            flush.zero_()
+            times[sched].append(_event_ms(lambda: ts.ts_gemm_bf16_ex(A, B, D, sched=sched, **kw), stream))
+    ts.ts_sync_and_check()
+    res = {}
+    for sched, v in times.items():
+        med = statistics.median(v)
+        res[sched] = {"ms_median": round(med, 4), "ms_min": round(min(v), 4),
+                      "tflops": round(flops / (med * 1e-3) / 1e12, 1)}
+    if rank != 0:
+        return None
+    return {"metric": "causal 8192^3 bf16 GEMM TFLOP/s (tiles above the diagonal skipped; computed tiles only)",
+            "unit": "TFLOP/s", "value": res["clc"]["tflops"], "static": res["static"], "clc": res["clc"],
+            "clc_speedup_over_static": round(res["static"]["ms_median"] / res["clc"]["ms_median"], 3),
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "dtype": "bf16",
+            "data": "synthetic", "config": {"workload": "causal " + w.name, "tile": args.tile,
+                                            "tiles_computed": computed, "tiles_skipped": int(mask_np.sum()),
+                                            "l2": "256 MiB buffer written between launches"}}
+
+
 def run_contended(args, ws, rank, local):
     """Ragged 8191x6143x4096 fp32-out GEMM while a spin kernel holds 32 SMs for half the solo GEMM time.
 
@@ -557,7 +606,7 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--workload", default="headline", choices=["headline", "gemm4096", "contended", "grouped"])
+    ap.add_argument("--workload", default="headline", choices=["headline", "gemm4096", "contended", "grouped", "causal"])
     ap.add_argument("--reps", type=int, default=10)
     ap.add_argument("--spin-ctas", type=int, default=32)
     args = ap.parse_args(argv)
@@ -584,6 +633,8 @@ def main(argv=None):
             line = run_contended(args, ws, rank, local)
         elif args.workload == "grouped":
             line = run_grouped(args, ws, rank, local)
+        elif args.workload == "causal":
+            line = run_causal(args, ws, rank, local)
         else:
             line = run_ours(args, ws, rank, local)
     finally:

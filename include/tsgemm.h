@@ -65,6 +65,12 @@ typedef struct {
                              partials and needs no initialisation.  Launches that may overlap on
                              the GPU need separate workspaces. */
     int64_t workspace_bytes;
+    const uint8_t *skip_tiles; /* device array or NULL: one byte per output tile, entry
+                             g * tiles_m * tiles_n + m_block * tiles_n + n_block (g = group, 0 for
+                             a plain GEMM; blocks of ts_launch_info.tile_m x tile_n).  A nonzero byte
+                             skips the tile: it is neither computed nor stored (D keeps its contents
+                             there), but the schedulers still hand it out (CUTLASS TS "Schedules",
+                             Skippable Tiles).  A launch with a skip mask does not split its tail. */
 } ts_gemm_opts;
 
 /* What ts_gemm_bf16_ex would launch for a problem (host-only query). */

@@ -190,7 +190,8 @@ ts_status plan_gemm(const void *D, int64_t M, int64_t N, int64_t K, int32_t out,
     pl->split_ws_bytes = 0;
     pl->counter_bytes = 0;
     pl->split = false;
-    if (o->split_tail >= 0 && groups == 0 && K > 0 && pl->num_tiles > W) {
+    // (not with a skip mask: the plan cannot see which tiles of the last wave will run)
+    if (o->split_tail >= 0 && groups == 0 && !o->skip_tiles && K > 0 && pl->num_tiles > W) {
         const int64_t r = pl->num_tiles % W;
         const int64_t s =
             r > 0 ? std::min<int64_t>(std::min<int64_t>(W / r, nk / kMinKBlocksPerPart), kMaxParts) : 0;
@@ -378,6 +379,7 @@ ts_status gemm_launch(const void *A, const void *B, void *D, int64_t M, int64_t 
     p.drain_ns = kDrainNs;
     p.status = status;
     p.trace = reinterpret_cast<long long *>(o->trace);
+    p.skip = o->skip_tiles;
     p.groups = static_cast<int32_t>(groups);
     p.tiles_per_group = static_cast<int32_t>(pl.tiles_m * pl.tiles_n);
     p.group_stride = M * pl.ldd;

@@ -190,6 +190,7 @@ struct Unit {
     int32_t tail;      // index among the split tail tiles, or -1 for a whole tile
     int32_t part;      // K part of a split tile
     int32_t group;     // group of a grouped GEMM (0 otherwise)
+    bool skip;         // the tile is skipped: no data work, only queue bookkeeping
 };
 
 __device__ __forceinline__ Unit decode_unit(int32_t u, const GemmParams &p) {
@@ -217,6 +218,16 @@ __device__ __forceinline__ Unit decode_unit(int32_t u, const GemmParams &p) {
         w.kb0 = static_cast<int32_t>(static_cast<int64_t>(w.part) * p.num_k_blocks / p.parts);
         w.kb1 = static_cast<int32_t>(static_cast<int64_t>(w.part + 1) * p.num_k_blocks / p.parts);
     }
+    // Skippable tiles (TS "Schedules", Skippable Tiles): every role still takes
+    // and advances past the unit, but a skipped tile loads, multiplies and
+    // stores nothing.
+    w.skip = false;
+    if (p.skip != nullptr) {
+        int32_t mb, nb;
+        raster(w.tile, p, mb, nb);
+        w.skip = p.skip[w.group * p.tiles_per_group + mb * p.tiles_n + nb] != 0;
+    }
+    if (w.skip) w.kb1 = w.kb0;
     return w;
 }
 
@@ -377,6 +388,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool alive = true;
             while (unit >= 0 && alive) {
                 const Unit w = decode_unit(unit, p);
+                if (w.skip) {  // no accumulator is used for a skipped tile
+                    unit = next_unit(sm, p, unit, clc_idx);
+                    continue;
+                }
                 if (!wait_phase(sm.tempty(acc), acc_phase ^ 1u, sm.abort_flag, p, WAIT_MMA_TMEM_EMPTY)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
@@ -529,6 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int32_t row0 = mb * C::TILE_M + static_cast<int32_t>(rank) * C::BM + 32 * q;
             const int32_t col0 = nb * BN;
             const bool split = w.tail >= 0;
+            if (!w.skip) {
             int ok = 1;
             if (lane == 0) ok = wait_phase(sm.tfull(acc), acc_phase, sm.abort_flag, p, WAIT_EPI_TMEM_FULL);
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -626,14 +642,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+            }  // !w.skip
             if (p.trace && rank == 0 && q == 0 && lane == 0) {
                 atomicAdd(reinterpret_cast<unsigned long long *>(&p.trace[4 * unit]), 1ull);
                 p.trace[4 * unit + 1] = worker;
                 p.trace[4 * unit + 3] = static_cast<long long>(globaltimer());
-            }
-            if (++acc == 2) {
-                acc = 0;
-                acc_phase ^= 1u;
             }
             int32_t nu = 0;
             if (lane == 0) nu = next_unit(sm, p, unit, clc_idx);

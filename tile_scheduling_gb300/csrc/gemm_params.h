@@ -58,6 +58,7 @@ struct GemmParams {
     // Grouped GEMM (groups > 0): unit u is tile u % tiles_per_group of group
     // u / tiles_per_group, whose k-blocks are [group_kb[g], group_kb[g + 1]).
     // D of group g starts group_stride elements after D of group g - 1.
+    const uint8_t *skip;   // per tile (all groups, unit order of whole tiles): nonzero = skip, or nullptr
     int32_t groups;
     int32_t tiles_per_group;
     int64_t group_stride;
