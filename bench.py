@@ -410,6 +410,46 @@ def run_causal(args, ws, rank, local):
                                             "l2": "256 MiB buffer written between launches"}}
 
 
+def run_fork(args, ws, rank, local):
+    """8192^3 bf16 GEMM with the Fork's second consumer (row sums of A) vs without, 1-CTA 128x256 tiles."""
+    import torch
+
+    import tile_scheduling_gb300 as ts
+
+    torch.cuda.set_device(local)
+    w = synth.GEMM_8192
+    A_bits, B_bits = w.inputs()
+    A = torch.from_numpy(A_bits.view(np.int16)).view(torch.bfloat16).cuda()
+    B = torch.from_numpy(B_bits.view(np.int16)).view(torch.bfloat16).cuda()
+    D = torch.empty((w.M, w.N), dtype=torch.bfloat16, device="cuda")
+    R = torch.empty((w.M,), dtype=torch.float32, device="cuda")
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    kw = dict(sched=args.sched, tile="128x256", workspace=None)
+    fns = {"plain": lambda: ts.ts_gemm_bf16_ex(A, B, D, **kw),
+           "fork_row_sums": lambda: ts.ts_gemm_bf16_ex(A, B, D, row_sums=R, **kw)}
+    for f in fns.values():
+        for _ in range(args.warmup):
+            f()
+    times = {k: [] for k in fns}
+    for _ in range(args.steps):
+        for k, f in fns.items():
+            flush.zero_()
+            times[k].append(_event_ms(f, stream))
+    ts.ts_sync_and_check()
+    flops = 2.0 * w.M * w.N * w.K
+    res = {k: {"ms_median": round(statistics.median(v), 4),
+               "tflops": round(flops / (statistics.median(v) * 1e-3) / 1e12, 1)} for k, v in times.items()}
+    if rank != 0:
+        return None
+    return {"metric": "8192^3 bf16 GEMM TFLOP/s with the Fork row-sum consumer vs without (128x256)",
+            "unit": "TFLOP/s", "value": res["fork_row_sums"]["tflops"], **res,
+            "fork_overhead": round(res["fork_row_sums"]["ms_median"] / res["plain"]["ms_median"] - 1, 4),
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "dtype": "bf16",
+            "data": "synthetic", "config": {"workload": w.name + " (128x256, " + args.sched + ")",
+                                            "l2": "256 MiB buffer written between launches"}}
+
+
 def run_contended(args, ws, rank, local):
     """Ragged 8191x6143x4096 fp32-out GEMM while a spin kernel holds 32 SMs for half the solo GEMM time.
 
@@ -606,7 +646,7 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--workload", default="headline", choices=["headline", "gemm4096", "contended", "grouped", "causal"])
+    ap.add_argument("--workload", default="headline", choices=["headline", "gemm4096", "contended", "grouped", "causal", "fork"])
     ap.add_argument("--reps", type=int, default=10)
     ap.add_argument("--spin-ctas", type=int, default=32)
     args = ap.parse_args(argv)
@@ -635,6 +675,8 @@ def main(argv=None):
             line = run_grouped(args, ws, rank, local)
         elif args.workload == "causal":
             line = run_causal(args, ws, rank, local)
+        elif args.workload == "fork":
+            line = run_fork(args, ws, rank, local)
         else:
             line = run_ours(args, ws, rank, local)
     finally:

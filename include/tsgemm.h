@@ -71,6 +71,13 @@ typedef struct {
                              skips the tile: it is neither computed nor stored (D keeps its contents
                              there), but the schedulers still hand it out (CUTLASS TS "Schedules",
                              Skippable Tiles).  A launch with a skip mask does not split its tail. */
+    float *row_sums;      /* device fp32 [groups][M] or NULL.  When given, a second consumer task
+                             reads every shared-memory ring stage beside the MMA (a Fork pipeline
+                             group: CUTLASS TS "Pipeline Groups", Fork) and writes
+                             row_sums[g][i] = sum over the group's K range of A[i][k], the
+                             correction term of zero-point-quantised products.  Rows whose first
+                             tile column is skipped are left untouched.  1-CTA tiles only (AUTO
+                             picks one; TS_TILE_256x256_2CTA is TS_ERR_UNSUPPORTED); no split tail. */
 } ts_gemm_opts;
 
 /* What ts_gemm_bf16_ex would launch for a problem (host-only query). */
@@ -108,6 +115,7 @@ typedef struct {
     int32_t clc_response_bytes;
     int32_t epilogue_warps;      /* epilogue warps per CTA */
     int32_t stage_bytes;         /* A + B bytes one CTA loads per stage */
+    int32_t aux_empty_arrivals;  /* arrivals on aux_empty[s] from the Fork row-sum task (row_sums given) */
 } ts_gemm_protocol;
 
 /* Fill *proto for the kernel variant of `tile` (TS_TILE_128x128, _128x256 or

@@ -18,6 +18,8 @@ Functions and the passages they follow:
   conversion the bf16-output epilogue applies to the fp32 accumulator.
 * ``grouped_gemm_f64``: the same sum per group over that group's K slice
   (TS "Schedules", Dynamic Domain: a per-tile loop bound from an offsets array).
+* ``row_sums_f64``: per-row sums of A over each group's K range, the second
+  output of the Fork pipeline group (TS "Pipeline Groups", Fork).
 * ``copy_i16``: dst[gid] = src[gid] for gid < n (TS "Resources", the int16
   copy example; TS "Schedules", the grid-stride domain).
 * ``static_schedule`` / ``static_owner``: worker w takes tiles w, w+W, ...
@@ -178,6 +180,21 @@ def grouped_gemm_f64(A_bits, B_bits, k_offsets, absolute: bool = False, blas: bo
             b = np.ascontiguousarray(B[:, k0:k1])
             D[g] = gemm_f64_blas(a, b, absolute) if blas else gemm_f64(a, b, absolute=absolute)
     return D
+
+
+def row_sums_f64(A_bits, k_offsets) -> np.ndarray:
+    """R[g][i] = sum over k_offsets[g] <= k < k_offsets[g+1] of a[i, k], by a plain loop.
+
+    The second output of the Fork pipeline group (TS "Pipeline Groups", Fork):
+    a second consumer reads the same A stages as the MMA."""
+    A = _bits(A_bits)
+    off = [int(x) for x in k_offsets]
+    a = bf16_to_f64(A)
+    R = np.zeros((len(off) - 1, A.shape[0]), dtype=np.float64)
+    for g in range(len(off) - 1):
+        for k in range(off[g], off[g + 1]):
+            R[g] += a[:, k]
+    return R
 
 
 # ---------------------------------------------------------------------- copy

@@ -199,6 +199,23 @@ def test_grouped_slices_match_integer_matmul():
     assert np.array_equal(oracle.grouped_gemm_f64(A, B, off, blas=True), D)
 
 
+def test_row_sums_equal_a_product_with_a_row_of_ones():
+    # sum_k a[i, k] = (A . 1^T)[i]: the row sums are the GEMM against a row of ones
+    A = synth.uniform_pm1_bf16(57, (23, 192))
+    ones = np.full((1, 192), 0x3F80, np.uint16)
+    R = oracle.row_sums_f64(A, [0, 192])
+    D = oracle.gemm_f64(A, ones)
+    assert np.all(np.abs(R[0] - D[:, 0]) <= 192 * 2.0 ** -52 * oracle.gemm_f64(A, ones, absolute=True)[:, 0])
+
+
+def test_row_sums_integer_groups_exact():
+    A = synth.int_uniform_bf16(58, (11, 256))
+    ai = oracle.bf16_to_f64(A).astype(np.int64)
+    R = oracle.row_sums_f64(A, [0, 64, 64, 256])
+    assert np.array_equal(R[0], ai[:, :64].sum(1)) and np.array_equal(R[2], ai[:, 64:].sum(1))
+    assert np.array_equal(R[1], np.zeros(11))
+
+
 # ------------------------------------------------------------------- copy
 @pytest.mark.parametrize("n", [0, 1, 7, 8, 1000, 4097])
 def test_copy_is_identity(n):

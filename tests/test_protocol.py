@@ -100,7 +100,7 @@ def test_clc_protocol_verified_cta_pair(units):
     assert r.ok, r.message
 
 
-@pytest.mark.parametrize("mutation", pc.MUTATIONS)
+@pytest.mark.parametrize("mutation", [m for m in pc.MUTATIONS if not m.startswith("fork")])
 @pytest.mark.parametrize("tile,sched,warps", [("128x256", "clc", None), ("256x256", "clc", 1),
                                               ("256x256", "static", 2)])
 def test_planted_mistakes_are_caught(mutation, tile, sched, warps):
@@ -109,3 +109,24 @@ def test_planted_mistakes_are_caught(mutation, tile, sched, warps):
         assert r.ok  # the static scheduler never touches the CLC barriers
     else:
         assert not r.ok and r.status == 1, (mutation, r)
+
+
+@pytest.mark.parametrize("sched", ["static", "clc"])
+@pytest.mark.parametrize("tile", ["128x128", "128x256"])
+def test_fork_protocol_verified(tile, sched):
+    # the ring's second consumer (row sums of A) beside the MMA issuer
+    r = pc.check_variant(tile, [2, 1, 2], sched, stages=2, fork=True)
+    assert r.ok, r.message
+
+
+@pytest.mark.parametrize("sched", ["static", "clc"])
+def test_fork_mistake_is_caught(sched):
+    r = pc.check_variant("128x256", [2, 1, 2], sched, stages=2, fork=True,
+                         mutate="fork_producer_ignores_second_consumer")
+    assert not r.ok and r.status == 1, r
+
+
+def test_fork_exports_its_arrivals(ts):
+    assert ts.ts_gemm_protocol_info("128x256", 0)["aux_empty_arrivals"] == 1
+    with pytest.raises(ValueError):
+        pc.build_program(ts.ts_gemm_protocol_info("256x256", 0), [1], fork=True)

@@ -46,7 +46,8 @@ class GemmOpts(ctypes.Structure):
     _fields_ = [("tile", ctypes.c_int32), ("max_workers", ctypes.c_int32), ("lda", ctypes.c_int64),
                 ("ldb", ctypes.c_int64), ("ldd", ctypes.c_int64), ("timeout_s", ctypes.c_double),
                 ("trace", ctypes.c_void_p), ("raster_group", ctypes.c_int32), ("split_tail", ctypes.c_int32),
-                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_int64), ("skip_tiles", ctypes.c_void_p)]
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_int64), ("skip_tiles", ctypes.c_void_p),
+                ("row_sums", ctypes.c_void_p)]
 
 
 class LaunchInfo(ctypes.Structure):
@@ -62,7 +63,7 @@ class GemmProtocol(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "cluster", "stages", "tx_bytes", "full_arrivals", "empty_arrivals", "accumulators", "tmem_full_arrivals",
         "tmem_empty_arrivals", "clc_slots", "clc_full_arrivals", "clc_empty_arrivals", "clc_response_bytes",
-        "epilogue_warps", "stage_bytes")]
+        "epilogue_warps", "stage_bytes", "aux_empty_arrivals")]
 
 
 def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
@@ -125,8 +126,12 @@ def _sched(s) -> int:
 
 
 def _opts(tile="auto", max_workers=0, lda=0, ldb=0, ldd=0, timeout_s=0.0, trace=None, raster_group=0,
-          split_tail=0, workspace=None, skip_tiles=None):
+          split_tail=0, workspace=None, skip_tiles=None, row_sums=None):
     o = GemmOpts()
+    if row_sums is not None:
+        if row_sums.dtype != torch.float32 or not row_sums.is_cuda or not row_sums.is_contiguous():
+            raise TypeError("row_sums must be a contiguous float32 CUDA tensor")
+        o.row_sums = row_sums.data_ptr()
     if skip_tiles is not None:
         if skip_tiles.dtype not in (torch.uint8, torch.bool) or not skip_tiles.is_cuda or not skip_tiles.is_contiguous():
             raise TypeError("skip_tiles must be a contiguous uint8/bool CUDA tensor (one entry per tile)")
@@ -191,7 +196,7 @@ def workspace_for(nbytes: int, device=None) -> torch.Tensor:
 
 def ts_gemm_bf16_ex(A: torch.Tensor, B: torch.Tensor, D: torch.Tensor, sched="static", tile="auto",
                     max_workers=0, timeout_s=0.0, trace=None, raster_group=0, workspace="auto", split_tail=0,
-                    skip_tiles=None, stream=None) -> None:
+                    skip_tiles=None, row_sums=None, stream=None) -> None:
     """D = A @ B.T for bf16 A [M, K] and B [N, K]; D [M, N] is bf16 or fp32.
 
     Rows may be strided (the row stride becomes lda / ldb / ldd).  ``workspace``
@@ -200,9 +205,11 @@ def ts_gemm_bf16_ex(A: torch.Tensor, B: torch.Tensor, D: torch.Tensor, sched="st
     ``stream`` (default: torch's current stream)."""
     M, N, K, lda, ldb, ldd = _gemm_args(A, B, D)
     lda, ldb, ldd = (lda if M > 1 else 0), (ldb if N > 1 else 0), (ldd if M > 1 else 0)
-    workspace = _resolve_workspace(M, N, K, _OUT[D.dtype], sched, workspace, split_tail, tile=tile,
+    workspace = _resolve_workspace(M, N, K, _OUT[D.dtype], sched, workspace,
+                                   -1 if (skip_tiles is not None or row_sums is not None) else split_tail, tile=tile,
                                    max_workers=max_workers, lda=lda, ldb=ldb, ldd=ldd)
-    o = _opts(tile, max_workers, lda, ldb, ldd, timeout_s, trace, raster_group, split_tail, workspace, skip_tiles)
+    o = _opts(tile, max_workers, lda, ldb, ldd, timeout_s, trace, raster_group, split_tail, workspace, skip_tiles,
+              row_sums)
     _check(_lib.ts_gemm_bf16_ex(ctypes.c_void_p(A.data_ptr()), ctypes.c_void_p(B.data_ptr()),
                                 ctypes.c_void_p(D.data_ptr()), M, N, K, _OUT[D.dtype], _sched(sched),
                                 ctypes.byref(o), _stream_handle(stream)))
@@ -289,7 +296,7 @@ def ts_gemm_grouped_launch_info(M: int, N: int, k_offsets, out=TS_OUT_BF16, sche
 
 def ts_gemm_bf16_grouped(A: torch.Tensor, B: torch.Tensor, D: torch.Tensor, k_offsets, sched="static", tile="auto",
                          max_workers=0, timeout_s=0.0, trace=None, raster_group=0, skip_tiles=None,
-                         stream=None) -> None:
+                         row_sums=None, stream=None) -> None:
     """D[g] = A[:, k_g:k_g+1] @ B[:, k_g:k_g+1].T for every group g (k_offsets: groups + 1 multiples of 64).
 
     A [M, >=K] and B [N, >=K] bf16 with unit column stride; D [groups, M, N]
@@ -306,7 +313,7 @@ def ts_gemm_bf16_grouped(A: torch.Tensor, B: torch.Tensor, D: torch.Tensor, k_of
     if int(off[-1]) > min(A.shape[1], B.shape[1]):
         raise ValueError("k_offsets reach past the columns of A or B")
     o = _opts(tile, max_workers, lda if M > 1 else 0, ldb if N > 1 else 0, D.stride(1) if M > 1 else 0, timeout_s,
-              trace, raster_group, skip_tiles=skip_tiles)
+              trace, raster_group, skip_tiles=skip_tiles, row_sums=row_sums)
     _check(_lib.ts_gemm_bf16_grouped(ctypes.c_void_p(A.data_ptr()), ctypes.c_void_p(B.data_ptr()),
                                      ctypes.c_void_p(D.data_ptr()), M, N, G, off.ctypes.data, _OUT[D.dtype],
                                      _sched(sched), ctypes.byref(o), _stream_handle(stream)))

@@ -151,12 +151,14 @@ ts_status plan_gemm(const void *D, int64_t M, int64_t N, int64_t K, int32_t out,
     const int sms = device_sms(dev);
     if (sms <= 0) return fail(TS_ERR_CUDA, "cannot query the SM count");
     int tile = o->tile;
+    if (o->row_sums && tile == TS_TILE_256x256_2CTA)
+        return fail(TS_ERR_UNSUPPORTED, "row sums (the Fork consumer) need a one-CTA tile");
     if (tile == TS_TILE_AUTO) {
         // Largest tile that still gives every SM work: the 2-CTA tile halves
         // each SM's share of B traffic, the 128x128 tile suits small outputs.
         const int64_t t256 = cdiv(M, 256) * cdiv(N, 256);
         const int64_t t128x256 = cdiv(M, 128) * cdiv(N, 256);
-        if (t256 * 2 >= sms)
+        if (t256 * 2 >= sms && !o->row_sums)
             tile = TS_TILE_256x256_2CTA;
         else if (t128x256 >= sms)
             tile = TS_TILE_128x256;
@@ -191,7 +193,7 @@ ts_status plan_gemm(const void *D, int64_t M, int64_t N, int64_t K, int32_t out,
     pl->counter_bytes = 0;
     pl->split = false;
     // (not with a skip mask: the plan cannot see which tiles of the last wave will run)
-    if (o->split_tail >= 0 && groups == 0 && !o->skip_tiles && K > 0 && pl->num_tiles > W) {
+    if (o->split_tail >= 0 && groups == 0 && !o->skip_tiles && !o->row_sums && K > 0 && pl->num_tiles > W) {
         const int64_t r = pl->num_tiles % W;
         const int64_t s =
             r > 0 ? std::min<int64_t>(std::min<int64_t>(W / r, nk / kMinKBlocksPerPart), kMaxParts) : 0;
@@ -380,6 +382,7 @@ ts_status gemm_launch(const void *A, const void *B, void *D, int64_t M, int64_t 
     p.status = status;
     p.trace = reinterpret_cast<long long *>(o->trace);
     p.skip = o->skip_tiles;
+    p.row_sums = o->row_sums;
     p.groups = static_cast<int32_t>(groups);
     p.tiles_per_group = static_cast<int32_t>(pl.tiles_m * pl.tiles_n);
     p.group_stride = M * pl.ldd;

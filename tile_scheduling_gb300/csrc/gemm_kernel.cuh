@@ -86,6 +86,7 @@ struct GemmCfg {
     static constexpr int ACCUMULATORS = 2;
     static constexpr int CLC_FULL_ARRIVALS = 1;  // this CTA's scheduler thread arms the slot
     static constexpr int CLC_RESPONSE_BYTES = 16;
+    static constexpr int AUX_EMPTY_ARRIVALS = 1;  // the Fork row-sum task (lane 0 of warp 3)
     // Consumers of one CLC response: producer, MMA, the epilogue warps and the
     // scheduler in the even CTA; producer, epilogue warps and scheduler in the odd one.
     static constexpr int CLC_CONSUMERS = (3 + EPI_WARPS) + (CG == 2 ? 2 + EPI_WARPS : 0);
@@ -100,7 +101,7 @@ struct GemmCfg {
     static_assert(STAGES >= 2, "ring too shallow");
     static_assert(SMEM_BYTES <= kSmemLimit, "shared memory budget");
     static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzle atoms must stay 1024-byte aligned");
-    static_assert(2 * STAGES * 8 + 5 * 8 + 2 * kMaxClcDepth * 8 + 16 * kMaxClcDepth + 8 <= BAR_BYTES,
+    static_assert(3 * STAGES * 8 + 5 * 8 + 2 * kMaxClcDepth * 8 + 16 * kMaxClcDepth + 8 <= BAR_BYTES,
                   "barrier region");
 };
 
@@ -180,6 +181,10 @@ struct Smem {
     __device__ __forceinline__ uint32_t clc_full(int r) const { return bars + 8u * (2 * C::STAGES + 5 + r); }
     __device__ __forceinline__ uint32_t clc_empty(int r) const {
         return bars + 8u * (2 * C::STAGES + 5 + kMaxClcDepth + r);
+    }
+    // Fork: the second consumer of ring stage s (the row-sum task) releases it here.
+    __device__ __forceinline__ uint32_t aux_empty(int s) const {
+        return bars + 8u * (2 * C::STAGES + 5 + 2 * kMaxClcDepth + s);
     }
 };
 
@@ -278,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     sm.epi = sm.b + C::STAGES * C::B_BYTES;
     sm.resp = sm.epi + C::EPI_BYTES;
     sm.bars = sm.resp + 16u * kMaxClcDepth;
-    const uint32_t tail = sm.bars + 8u * (2 * C::STAGES + 5 + 2 * kMaxClcDepth);
+    const uint32_t tail = sm.bars + 8u * (3 * C::STAGES + 5 + 2 * kMaxClcDepth);
     sm.tmem_slot = reinterpret_cast<uint32_t *>(gbase + (tail - base));
     sm.abort_flag = reinterpret_cast<volatile int *>(gbase + (tail - base) + 4);
 
@@ -286,6 +291,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = threadIdx.x & 31;
     const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;
     const int32_t worker = static_cast<int32_t>(blockIdx.x / CG);
+    // Fork pipeline group (CUTLASS TS "Pipeline Groups", Fork): each ring stage
+    // is filled once and read by two consumer tasks, the MMA issuer and the
+    // row-sum task on warp 3; each releases the stage on its own empty barrier
+    // and the producer refills it only after both.  One-CTA tiles only.
+    const bool fork = CG == 1 && p.row_sums != nullptr;
 
     // ------------------------------------------------------------ prologue
     if (warp == 0 && lane == 0) {
@@ -305,8 +315,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(sm.mma_done(), 1);
         for (int r = 0; r < kMaxClcDepth; ++r) {
             mbar_init(sm.clc_full(r), C::CLC_FULL_ARRIVALS);
-            mbar_init(sm.clc_empty(r), C::CLC_CONSUMERS);
+            // with the Fork row-sum task, warp 3 consumes every response too
+            mbar_init(sm.clc_empty(r), C::CLC_CONSUMERS + (fork ? 1 : 0));
         }
+        for (int s = 0; s < C::STAGES; ++s) mbar_init(sm.aux_empty(s), C::AUX_EMPTY_ARRIVALS);
         *sm.abort_flag = 0;
         fence_mbar_init();
     }
@@ -338,7 +350,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int32_t b_row = nb * BN + static_cast<int32_t>(rank) * C::B_ROWS;
                 if (p.trace && rank == 0) p.trace[4 * unit + 2] = static_cast<long long>(globaltimer());
                 for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
-                    if (!wait_phase(sm.empty(stage), phase ^ 1u, sm.abort_flag, p, WAIT_PRODUCER_EMPTY)) {
+                    if (!wait_phase(sm.empty(stage), phase ^ 1u, sm.abort_flag, p, WAIT_PRODUCER_EMPTY) ||
+                        (fork && !wait_phase(sm.aux_empty(stage), phase ^ 1u, sm.abort_flag, p, WAIT_PRODUCER_EMPTY))) {
                         alive = false;
                         break;
                     }
@@ -373,6 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             for (int i = 0; i < C::STAGES; ++i) {
                 if (!wait_drain(sm.empty(stage), phase ^ 1u, sm.abort_flag, p)) break;
+                if (fork && !wait_drain(sm.aux_empty(stage), phase ^ 1u, sm.abort_flag, p)) break;
                 if (++stage == C::STAGES) {
                     stage = 0;
                     phase ^= 1u;
@@ -471,6 +485,83 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (outstanding) wait_drain(sm.clc_full(out_r), out_ph, sm.abort_flag, p);
+        }
+        __syncwarp();
+    } else if (warp == 3) {
+        // ------------------------------------------- Fork consumer: row sums of A
+        // Reads every ring stage after the MMA issuer's full barrier; on the
+        // tiles of the first tile column (n block 0) it adds each row of the A
+        // tile (64 bf16 per row; lane L owns rows L, L+32, L+64, L+96) to a
+        // running fp32 sum over the unit's k-blocks and stores it at the end.
+        if (fork) {
+            int32_t unit = first_unit;
+            uint32_t clc_idx = 0, stage = 0, phase = 0;
+            bool alive = true;
+            while (unit >= 0 && alive) {
+                const Unit w = decode_unit(unit, p);
+                int32_t mb, nb;
+                raster(w.tile, p, mb, nb);
+                const bool active = nb == 0 && !w.skip;
+                // eight accumulators per row (one per chunk slot) keep the adds
+                // independent; they are combined in slot order at the end
+                float sum[4][8];
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) sum[r][c] = 0.f;
+                for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
+                    int ok = 1;
+                    if (lane == 0) ok = wait_phase(sm.full(stage), phase, sm.abort_flag, p, WAIT_MMA_FULL);
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (!ok) {
+                        alive = false;
+                        break;
+                    }
+                    if (active) {
+                        const uint32_t a_tile = sm.a + stage * C::A_BYTES;
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) {
+                            const uint32_t row = a_tile + static_cast<uint32_t>(lane + 32 * r) * 128u;
+#pragma unroll
+                            for (int c = 0; c < 8; ++c) {
+                                // The sum does not care about the order of a row's chunks;
+                                // reading slot c ^ (lane & 7) puts every 8 lanes on 8
+                                // different 16-byte bank groups (no bank conflicts).
+                                uint32_t x0, x1, x2, x3;
+                                asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                                             : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3)
+                                             : "r"(row + ((static_cast<uint32_t>(c) ^ (lane & 7u)) << 4)));
+                                const uint32_t xs[4] = {x0, x1, x2, x3};
+#pragma unroll
+                                for (int j = 0; j < 4; ++j) {
+                                    sum[r][c] += __uint_as_float(xs[j] << 16);
+                                    sum[r][c] += __uint_as_float(xs[j] & 0xffff0000u);
+                                }
+                            }
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(sm.aux_empty(stage));
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!alive) break;
+                if (active) {
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        float t = sum[r][0];
+#pragma unroll
+                        for (int c = 1; c < 8; ++c) t += sum[r][c];
+                        const int32_t row = mb * C::TILE_M + lane + 32 * r;
+                        if (row < p.M) p.row_sums[static_cast<int64_t>(w.group) * p.M + row] = t;
+                    }
+                }
+                int32_t nu = 0;
+                if (lane == 0) nu = next_unit(sm, p, unit, clc_idx);
+                unit = __shfl_sync(0xffffffffu, nu, 0);
+            }
         }
         __syncwarp();
     } else if (warp >= 4) {

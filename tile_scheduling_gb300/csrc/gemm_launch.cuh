@@ -39,7 +39,8 @@ struct GemmInstance {
                                 C::CLC_CONSUMERS,
                                 C::CLC_RESPONSE_BYTES,
                                 C::EPI_WARPS,
-                                C::A_BYTES + C::B_BYTES};
+                                C::A_BYTES + C::B_BYTES,
+                                C::AUX_EMPTY_ARRIVALS};
     }
 
     static cudaError_t launch(const GemmLaunch &L) {

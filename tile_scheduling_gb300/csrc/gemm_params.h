@@ -58,7 +58,8 @@ struct GemmParams {
     // Grouped GEMM (groups > 0): unit u is tile u % tiles_per_group of group
     // u / tiles_per_group, whose k-blocks are [group_kb[g], group_kb[g + 1]).
     // D of group g starts group_stride elements after D of group g - 1.
-    const uint8_t *skip;   // per tile (all groups, unit order of whole tiles): nonzero = skip, or nullptr
+    const uint8_t *skip;   // per tile, row-major by tile row and column per group: nonzero = skip, or nullptr
+    float *row_sums;       // Fork consumer output [groups][M]: sum over the K range of each row of A, or nullptr
     int32_t groups;
     int32_t tiles_per_group;
     int64_t group_stride;

@@ -37,7 +37,8 @@ from . import _lib
 
 OP_WAIT, OP_ARRIVE, OP_TMA, OP_MMA, OP_COMMIT, OP_TREAD, OP_CREQ, OP_CREAD = range(8)
 MUTATIONS = ("tmem_empty_count_low", "tmem_empty_count_high", "clc_empty_count_low", "tx_bytes_one_cta",
-             "producer_wait_parity", "epilogue_release_before_read", "mma_skip_stage_release")
+             "producer_wait_parity", "epilogue_release_before_read", "mma_skip_stage_release",
+             "fork_producer_ignores_second_consumer")
 
 
 def _tag(unit: int, kb: int) -> int:
@@ -62,7 +63,7 @@ class Program:
 
 
 def build_program(proto: dict, units: list, sched: str = "static", epilogue_warps: int | None = None,
-                  stages: int | None = None, mutate: str | None = None) -> Program:
+                  stages: int | None = None, mutate: str | None = None, fork: bool = False) -> Program:
     """The kernel's role loops for one worker.
 
     proto           ts_gemm_protocol_info() of the variant.
@@ -72,7 +73,13 @@ def build_program(proto: dict, units: list, sched: str = "static", epilogue_warp
     epilogue_warps  epilogue warps per CTA to model (default: the kernel's).
     stages          ring depth to model (default: the kernel's).
     mutate          plant one protocol mistake (MUTATIONS), for the checker's tests.
+    fork            add the Fork pipeline group's second consumer of the ring (the
+                    row-sum task): it reads every stage after the full barrier and
+                    releases it on its own empty barrier; the producer refills a
+                    stage only after both consumers released it (one-CTA tiles).
     """
+    if fork and proto["cluster"] != 1:
+        raise ValueError("the Fork consumer runs on one-CTA tiles only")
     if mutate is not None and mutate not in MUTATIONS:
         raise ValueError(f"unknown mutation {mutate}")
     cg = proto["cluster"]
@@ -88,8 +95,10 @@ def build_program(proto: dict, units: list, sched: str = "static", epilogue_warp
                                                           "tmem_empty_count_high": 1}.get(mutate, 0)
     tempty = [P.bar(f"tmem_empty[{a}]", tempty_n) for a in range(A)]
     clc_full = [[P.bar(f"clc_full[{c}][{r}]", proto["clc_full_arrivals"]) for r in range(R)] for c in range(cg)]
-    clc_empty_n = proto["clc_empty_arrivals"] - dropped - (1 if mutate == "clc_empty_count_low" else 0)
+    clc_empty_n = proto["clc_empty_arrivals"] - dropped - (1 if mutate == "clc_empty_count_low" else 0) \
+        + (1 if fork else 0)
     clc_empty = [P.bar(f"clc_empty[{r}]", clc_empty_n) for r in range(R)]
+    aux_empty = [P.bar(f"aux_empty[{s}]", proto["aux_empty_arrivals"]) for s in range(S)] if fork else []
     stage = [[P.buf(f"stage[{c}][{s}]") for s in range(S)] for c in range(cg)]
     accb = [P.buf(f"tmem[{a}]") for a in range(A)]
     slot = [[P.buf(f"clc_slot[{c}][{r}]") for r in range(R)] for c in range(cg)]
@@ -112,6 +121,8 @@ def build_program(proto: dict, units: list, sched: str = "static", epilogue_warp
         for u, nk in enumerate(units):
             for kb in range(nk):
                 ops.append(rec(OP_WAIT, empty[c][s], ph if mutate == "producer_wait_parity" else ph ^ 1))
+                if fork and mutate != "fork_producer_ignores_second_consumer":
+                    ops.append(rec(OP_WAIT, aux_empty[s], ph ^ 1))
                 if c == 0:
                     ops.append(rec(OP_ARRIVE, full[0][s], tx))
                 ops.append(rec(OP_TMA, stage[c][s], _tag(u, kb), full[0][s], proto["stage_bytes"]))
@@ -123,8 +134,10 @@ def build_program(proto: dict, units: list, sched: str = "static", epilogue_warp
             for i in range(1, min(issued, S) + 1):
                 b = issued - i
                 ops.append(rec(OP_WAIT, full[0][b % S], (b // S) & 1))
-        for _ in range(S):  # drain: the MMA released every stage
+        for _ in range(S):  # drain: the MMA (and the Fork consumer) released every stage
             ops.append(rec(OP_WAIT, empty[c][s], ph ^ 1))
+            if fork:
+                ops.append(rec(OP_WAIT, aux_empty[s], ph ^ 1))
             s, ph = adv(s, ph, S)
         P.roles.append((f"producer[{c}]", None, ops))
 
@@ -155,6 +168,17 @@ def build_program(proto: dict, units: list, sched: str = "static", epilogue_warp
                 if clc:
                     consume(ops, c, u)
             P.roles.append((f"epilogue[{c}][{w}]", f"epilogue[{c}]", ops))
+
+    if fork:  # the Fork pipeline group's second consumer of the ring
+        ops, s, ph = [], 0, 0
+        for u, nk in enumerate(units):
+            for kb in range(nk):
+                ops += [rec(OP_WAIT, full[0][s], ph), rec(OP_TREAD, stage[0][s], _tag(u, kb)),
+                        rec(OP_ARRIVE, aux_empty[s], 0)]
+                s, ph = adv(s, ph, S)
+            if clc:
+                consume(ops, 0, u)
+        P.roles.append(("rowsum", None, ops))
 
     if clc:  # CLC scheduler of each CTA; the even CTA's request fills every CTA's slot
         for c in range(cg):
