@@ -273,10 +273,18 @@ def run_ours(args, ws, rank, local):
     return line
 
 
-def _event_ms(fn, stream):
+def _event_ms(fn, stream, hide_host=True):
+    """Device time of fn's launches on `stream` (CUDA events).
+
+    hide_host: a short GPU sleep queued ahead of the start event keeps the device
+    busy while the host runs fn's Python and C setup, so that host overhead does
+    not fall inside the timed region (otherwise an idle GPU records the start
+    event at once and the gap until the launch is counted)."""
     import torch
 
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if hide_host:
+        torch.cuda._sleep(500_000)
     e0.record(stream)
     fn()
     e1.record(stream)
@@ -450,6 +458,54 @@ def run_fork(args, ws, rank, local):
                                             "l2": "256 MiB buffer written between launches"}}
 
 
+def run_rows(args, ws, rank, local):
+    """Jagged int16 copy, 8192 rows of 64..262144 elements (log-uniform): the static grid-stride work
+    queue vs the CLC one, plus an oversubscribed CLC launch (twice as many tiles as rows, the extra
+    half skipped).  Inputs (0.5 GiB each way) are larger than L2."""
+    import torch
+
+    import tile_scheduling_gb300 as ts
+
+    torch.cuda.set_device(local)
+    w = synth.ROWS
+    src_h, off_h = w.inputs()
+    src = torch.from_numpy(src_h).cuda()
+    dst = torch.empty_like(src)
+    off = torch.from_numpy(off_h).cuda()
+    stream = torch.cuda.current_stream()
+    nbytes = 4.0 * src.numel()  # 2 bytes read + 2 written per element
+    runs = {"static": dict(sched="static"), "clc": dict(sched="clc"),
+            "clc_oversubscribed_2x": dict(sched="clc", tiles=2 * w.rows)}
+    times = {k: [] for k in runs}
+    for k, kw in runs.items():
+        for _ in range(args.warmup):
+            ts.ts_copy_i16_rows(src, dst, off, **kw)
+    for _ in range(args.steps):  # alternate so clock drift hits every variant alike
+        for k, kw in runs.items():
+            times[k].append(_event_ms(lambda: ts.ts_copy_i16_rows(src, dst, off, **kw), stream))
+    ts.ts_sync_and_check()
+    if not torch.equal(dst, src):
+        raise RuntimeError("jagged copy result differs from its input")
+    if rank != 0:
+        return None
+    peaks = load_peaks()
+    res = {}
+    for k, v in times.items():
+        med = statistics.median(v)
+        res[k] = {"ms_median": round(med, 4), "ms_min": round(min(v), 4),
+                  "gbs": round(nbytes / (med * 1e-3) / 1e9, 1)}
+    best = res["clc"]["gbs"]
+    return {"metric": "jagged int16 row copy HBM GB/s (8192 rows, log-uniform lengths), static vs CLC work queue",
+            "unit": "GB/s", "value": best, **res,
+            "clc_speedup_over_static": round(res["static"]["ms_median"] / res["clc"]["ms_median"], 3),
+            "roofline": {"bound": "hbm", "achieved": best, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(best / peaks["hbm_gbs"], 4), "traffic": None,
+                         "peak_kind": f"{peaks['source']} HBM copy", "kernel": "rows_copy_kernel"},
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "dtype": "int16",
+            "data": "synthetic", "config": {"workload": w.name, "elements": int(src.numel()), "rows": w.rows,
+                                            "l2": "inputs larger than L2 (0.5 GiB each way); no flush"}}
+
+
 def run_contended(args, ws, rank, local):
     """Ragged 8191x6143x4096 fp32-out GEMM while a spin kernel holds 32 SMs for half the solo GEMM time.
 
@@ -487,7 +543,8 @@ def run_contended(args, ws, rank, local):
         torch.cuda.synchronize()
         ts.ts_spin(ctas, spin_ns, started, stream=side)
         ts.ts_spin_wait_started(started, ctas, 5.0)
-        ms = _event_ms(lambda: gemm(sched, trace), stream)
+        # no sleep ahead: the GEMM must start while the spin still holds its SMs
+        ms = _event_ms(lambda: gemm(sched, trace), stream, hide_host=False)
         torch.cuda.synchronize()
         return ms
 
@@ -670,7 +727,8 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--workload", default="headline", choices=["headline", "gemm4096", "contended", "grouped", "causal", "fork"])
+    ap.add_argument("--workload", default="headline", choices=["headline", "gemm4096", "contended", "grouped", "causal", "fork",
+                                                                   "rows"])
     ap.add_argument("--reps", type=int, default=10)
     ap.add_argument("--spin-ctas", type=int, default=32)
     args = ap.parse_args(argv)
@@ -699,6 +757,8 @@ def main(argv=None):
             line = run_grouped(args, ws, rank, local)
         elif args.workload == "causal":
             line = run_causal(args, ws, rank, local)
+        elif args.workload == "rows":
+            line = run_rows(args, ws, rank, local)
         elif args.workload == "fork":
             line = run_fork(args, ws, rank, local)
         else:

@@ -250,6 +250,61 @@ ts_status ts_gemm_bf16_checked_noalloc(const void *A, const void *B, void *D, in
  */
 ts_status ts_copy_i16(const int16_t *src, int16_t *dst, int64_t n, void *stream);
 
+/* Optional knobs for ts_copy_i16_rows; zero means "default" for every field. */
+typedef struct {
+    int64_t tiles;              /* work tiles launched, >= rows; 0 = rows.  Tiles t >= the row
+                                   count copy nothing but still take part in the work queue
+                                   (the oversubscribed copy queue). */
+    const int64_t *rows_device; /* device int64 or NULL: the row count, read once per CTA on the
+                                   device and clamped to [0, rows].  Lets one launch shape (tiles,
+                                   rows as capacities) serve a count that a previous kernel wrote. */
+    const uint8_t *skip_rows;   /* device array of `rows` bytes or NULL: nonzero = skip that row */
+    int32_t threads;            /* threads per CTA: 128, 256, 512 or 1024; 0 = 512 */
+    int32_t max_workers;        /* static scheduler: cap on persistent CTAs; 0 = all resident */
+    double timeout_s;           /* limit on one wait for a CLC response; 0 = 1 s */
+    int64_t *trace;             /* device int64 [2 * tiles] zeroed by the caller, or NULL: per tile t,
+                                   [2t] += 1 per visit, [2t+1] = blockIdx.x of the CTA that ran it */
+} ts_rows_opts;
+
+/*
+ * ts_copy_i16_rows -- copy the rows of a jagged int16 array through a work
+ * queue: for every row r < R that is not skipped,
+ *
+ *   dst[i] = src[i]   for offsets[r] <= i < offsets[r + 1]
+ *
+ * where R is `rows`, or *opts->rows_device clamped to [0, rows].  Work tile t
+ * is row t: its loop bound comes from the offsets array (CUTLASS TS
+ * "Schedules", Dynamic Domain: get_domain_size(tile) = offsets[t + 1] -
+ * offsets[t]); tiles past R and rows marked in skip_rows run no copy, while
+ * every tile still waits on, advances and releases the queue (TS "Schedules",
+ * Skippable Tiles, whose example is this oversubscribed copy).  sched picks
+ * the queue: TS_SCHED_STATIC, a grid-stride persistent loop over the resident
+ * CTAs, or TS_SCHED_CLC, one CTA per tile with Cluster Launch Control work
+ * stealing ("Cluster Launch Control": the request for the next tile is issued
+ * before the current row is copied).  Elements of dst outside the copied rows
+ * are never written.
+ *
+ *   src, dst  device int16 arrays of n elements, 2-byte aligned; src == dst is
+ *             allowed (each element is rewritten with itself); any other
+ *             overlap is TS_ERR_INVALID_ARG.  32-byte vectors are used when src
+ *             and dst share their offset modulo 32 bytes, 16-byte ones modulo
+ *             16, element-wise copies otherwise.
+ *   offsets   device int64 array of rows + 1 entries (read on the device).  A
+ *             row with offsets[r] < 0, offsets[r + 1] < offsets[r] or
+ *             offsets[r + 1] > n is not copied; the next ts_sync_and_check
+ *             returns TS_ERR_INVALID_ARG naming the first such row.
+ *   rows      row count (upper bound when rows_device is given), >= 0.
+ * A CLC response that does not arrive within timeout_s is reported as
+ * TS_ERR_TIMEOUT by ts_sync_and_check; the CTA then stops taking tiles.
+ */
+ts_status ts_copy_i16_rows(const int16_t *src, int16_t *dst, int64_t n, const int64_t *offsets, int64_t rows,
+                           int32_t sched, const ts_rows_opts *opts, void *stream);
+
+/* The launch ts_copy_i16_rows would make (host only): num_tiles = num_units =
+ * tiles, grid_ctas = workers = CTAs launched, resident = CTAs that fit at once. */
+ts_status ts_copy_rows_launch_info(int64_t n, int64_t rows, int32_t sched, const ts_rows_opts *opts,
+                                   ts_launch_info *info);
+
 /*
  * ts_spin -- occupy `ctas` SMs for `duration_ns` nanoseconds (measured with
  * %globaltimer), to make part of the GPU unavailable to a following kernel.

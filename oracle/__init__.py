@@ -1,4 +1,4 @@
-"""CPU oracle for the tile-scheduled GEMM and the int16 copy.
+"""CPU oracle for the tile-scheduled GEMM, the int16 copy and the jagged row copy.
 
 TEST INFRASTRUCTURE ONLY: imported by tests/, by the smoke check and by the
 benchmark's CPU-baseline leg, never by the product path.  It shares no code
@@ -22,6 +22,11 @@ Functions and the passages they follow:
   output of the Fork pipeline group (TS "Pipeline Groups", Fork).
 * ``copy_i16``: dst[gid] = src[gid] for gid < n (TS "Resources", the int16
   copy example; TS "Schedules", the grid-stride domain).
+* ``copy_rows_i16``: the jagged row copy -- for every row r below the row
+  count that the skip mask does not drop, dst[i] = src[i] for offsets[r] <= i
+  < offsets[r + 1]; every other element keeps its value (TS "Schedules",
+  Dynamic Domain: a per-tile loop bound from an offsets array; Skippable
+  Tiles: the oversubscribed copy whose skipped tiles copy nothing).
 * ``static_schedule`` / ``static_owner``: worker w takes tiles w, w+W, ...
   ("Cluster Launch Control", limits of the static persistent scheduler,
   worked example of 12 tiles on 4 workers).
@@ -76,6 +81,8 @@ def _load():
                                             ctypes.c_int, ctypes.c_int]
             lib.oracle_gemm_entries_f64.argtypes = [P, P, I64, I64, I64, P, P, I64, P, P, ctypes.c_int]
             lib.oracle_copy_i16.argtypes = [P, P, I64]
+            lib.oracle_copy_rows_i16.argtypes = [P, P, I64, P, I64, P]
+            lib.oracle_copy_rows_i16.restype = I64
             lib.oracle_static_owner.argtypes = [I64, I64, P]
             _lib = lib
     return _lib
@@ -203,6 +210,27 @@ def copy_i16(src) -> np.ndarray:
     d = np.empty_like(s)
     _load().oracle_copy_i16(_ptr(s), _ptr(d), s.size)
     return d
+
+
+def copy_rows_i16(src, dst, offsets, rows: int | None = None, skip=None) -> tuple[np.ndarray, int]:
+    """The jagged row copy applied to a copy of ``dst``; returns (result, first invalid row or -1)."""
+    s = np.ascontiguousarray(np.asarray(src, dtype=np.int16))
+    d = np.array(dst, dtype=np.int16, copy=True)
+    if d.shape != s.shape:
+        raise ValueError("src and dst differ in size")
+    off = np.ascontiguousarray(np.asarray(offsets, dtype=np.int64))
+    if rows is None:
+        rows = max(off.size - 1, 0)
+    if off.size < rows + 1:
+        raise ValueError("offsets needs rows + 1 entries")
+    sk = None
+    if skip is not None:
+        sk = np.ascontiguousarray(np.asarray(skip, dtype=np.uint8))
+        if sk.size < rows:
+            raise ValueError("skip needs one entry per row")
+    bad = _load().oracle_copy_rows_i16(_ptr(s), _ptr(d), s.size, _ptr(off), int(rows),
+                                       _ptr(sk) if sk is not None else None)
+    return d, int(bad)
 
 
 # ---------------------------------------------------------------- scheduling

@@ -1,5 +1,6 @@
 /*
- * Oracle for the tile-scheduled GEMM and the grid-stride int16 copy.
+ * Oracle for the tile-scheduled GEMM, the grid-stride int16 copy and the
+ * jagged row copy.
  *
  * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the
  * benchmark's CPU-baseline leg may load this library.  It shares no code with
@@ -21,6 +22,13 @@
  *
  * The copy follows TS "Resources", the int16 example (InputGmemResource.get_item /
  * OutputGmemResource.set_item): dst[gid] = src[gid] for every gid < n.
+ *
+ * The jagged row copy follows TS "Schedules": Dynamic Domain (work tile t runs
+ * its loop from offsets[t] to offsets[t + 1]) and Skippable Tiles (a per-tile
+ * predicate drops the copy of a tile; tiles past the row count are such tiles
+ * of the oversubscribed copy queue).  Whatever the queue, the result is: every
+ * row r < rows that is not skipped has dst[i] = src[i] for its i, and no
+ * other element of dst changes.
  *
  * The static persistent assignment follows "Cluster Launch Control", section
  * on the limits of the static persistent scheduler: with W workers, worker w
@@ -118,6 +126,25 @@ void oracle_gemm_entries_f64(const uint16_t *A, const uint16_t *B,
 /* dst[gid] = src[gid] for gid < n, one element at a time. */
 void oracle_copy_i16(const int16_t *src, int16_t *dst, int64_t n) {
     for (int64_t gid = 0; gid < n; ++gid) dst[gid] = src[gid];
+}
+
+/* For each row r < rows with skip == NULL or skip[r] == 0: dst[i] = src[i]
+ * for offsets[r] <= i < offsets[r + 1].  A row whose bounds are not
+ * 0 <= offsets[r] <= offsets[r + 1] <= n is left alone.  Returns the first
+ * such row, or -1 if every row examined was valid. */
+int64_t oracle_copy_rows_i16(const int16_t *src, int16_t *dst, int64_t n, const int64_t *offsets, int64_t rows,
+                             const uint8_t *skip) {
+    int64_t first_bad = -1;
+    for (int64_t r = 0; r < rows; ++r) {
+        if (skip && skip[r]) continue;
+        const int64_t b = offsets[r], e = offsets[r + 1];
+        if (b < 0 || e < b || e > n) {
+            if (first_bad < 0) first_bad = r;
+            continue;
+        }
+        for (int64_t i = b; i < e; ++i) dst[i] = src[i];
+    }
+    return first_bad;
 }
 
 /* owner[t] = the worker that the static grid-stride rule gives tile t. */

@@ -204,3 +204,29 @@ class GroupedWorkload:
 
 GROUPED = GroupedWorkload("grouped gemm 16 groups 2048x2048, K per group 64..8192 (skewed)", 2048, 2048, 16,
                           SEED_BASE + 5)
+
+
+@dataclass(frozen=True)
+class RowsWorkload:
+    """A jagged int16 array whose row lengths span several decades (log-uniform)."""
+
+    name: str
+    rows: int
+    min_len: int
+    max_len: int
+    seed: int
+
+    def offsets(self) -> np.ndarray:
+        # length = floor(min_len * (max_len / min_len) ** u), u uniform in [0, 1), in generator order
+        z = splitmix64(self.seed, self.rows)
+        u = (z >> np.uint64(11)).astype(np.float64) * 2.0 ** -53
+        lengths = np.floor(self.min_len * (self.max_len / self.min_len) ** u).astype(np.int64)
+        return np.concatenate([[0], np.cumsum(lengths)]).astype(np.int64)
+
+    def inputs(self):
+        off = self.offsets()
+        return int16_uniform(self.seed + 1, int(off[-1])), off
+
+
+ROWS = RowsWorkload("jagged int16 copy, 8192 rows of 64..262144 elements (log-uniform)", 8192, 64, 262144,
+                    SEED_BASE + 6)

@@ -72,3 +72,20 @@ def test_header_is_plain_c():
         r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), "-c", c,
                             "-o", os.path.join(d, "t.o")], capture_output=True, text=True)
         assert r.returncode == 0, r.stderr
+
+
+def test_row_copy_argument_errors_need_no_gpu(ts):
+    E = ts.TS_ERR_INVALID_ARG
+    assert ts.ts_copy_i16_rows_ptr(4096, 8192, -1, 64, 0, stream=0) == E  # n < 0
+    assert ts.ts_copy_i16_rows_ptr(4096, 8192, 8, 64, -2, stream=0) == E  # rows < 0
+    assert ts.ts_copy_i16_rows_ptr(4096, 8192, 8, 64, 1, sched=5, stream=0) == E
+    assert ts.ts_copy_i16_rows_ptr(4096, 8192, 8, 64, 4, tiles=3, stream=0) == E  # tiles below rows
+    assert "tiles" in ts.ts_last_error_detail()
+    assert ts.ts_copy_i16_rows_ptr(4096, 8192, 8, 64, 1, threads=100, stream=0) == E
+    assert ts.ts_copy_i16_rows_ptr(4096, 8192, 8, 0, 1, stream=0) == E  # offsets NULL
+    assert ts.ts_copy_i16_rows_ptr(0, 8192, 8, 64, 1, stream=0) == E  # src NULL
+    assert ts.ts_copy_i16_rows_ptr(4096, 4100, 8, 64, 1, stream=0) == E  # overlap
+    assert ts.ts_copy_i16_rows_ptr(4097, 8192, 8, 64, 1, stream=0) == E  # odd address
+    assert ts.ts_copy_i16_rows_ptr(4096, 8192, 8, 64, 1, timeout_s=-1.0, stream=0) == E
+    # an empty queue launches nothing
+    assert ts.ts_copy_i16_rows_ptr(0, 0, 0, 0, 0, stream=0) == ts.TS_OK

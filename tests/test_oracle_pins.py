@@ -223,6 +223,63 @@ def test_copy_is_identity(n):
     assert np.array_equal(oracle.copy_i16(src), src)
 
 
+def _golden_rows():
+    meta, cases = {}, []
+    with open(os.path.join(GOLDEN, "copy_rows_example.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, vals = line.split(":")
+            if key.startswith("case"):
+                _, rows, mode = key.split()
+                cases.append((int(rows), mode == "skip", np.array(vals.split(), dtype=np.int16)))
+            else:
+                meta[key] = np.array(vals.split(), dtype=np.int64)
+    return meta, cases
+
+
+def test_copy_rows_golden():
+    meta, cases = _golden_rows()
+    n = int(meta["n"][0])
+    for rows, use_skip, want in cases:
+        got, bad = oracle.copy_rows_i16(meta["src"].astype(np.int16), np.full(n, -1, np.int16), meta["offsets"],
+                                        rows, meta["skip"] if use_skip else None)
+        assert bad == -1
+        assert np.array_equal(got, want), (rows, use_skip, got)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_copy_rows_over_a_partition_is_the_plain_copy(seed):
+    # rows that tile [0, n) exactly, none skipped: the jagged copy is the whole copy
+    rng = np.random.default_rng(seed)
+    n = 5000
+    cuts = np.sort(rng.integers(0, n + 1, size=40))
+    offsets = np.concatenate([[0], cuts, [n]])
+    src = synth.int16_uniform(300 + seed, n)
+    got, bad = oracle.copy_rows_i16(src, np.zeros(n, np.int16), offsets)
+    assert bad == -1 and np.array_equal(got, oracle.copy_i16(src))
+
+
+def test_copy_rows_skipping_everything_changes_nothing():
+    src = synth.int16_uniform(7, 100)
+    dst0 = synth.int16_uniform(8, 100)
+    offsets = np.array([0, 10, 50, 100])
+    got, _ = oracle.copy_rows_i16(src, dst0, offsets, skip=np.ones(3, np.uint8))
+    assert np.array_equal(got, dst0)
+    got, _ = oracle.copy_rows_i16(src, dst0, offsets, rows=0)
+    assert np.array_equal(got, dst0)
+
+
+def test_copy_rows_reports_the_first_invalid_row():
+    src = np.arange(1, 11, dtype=np.int16)
+    # row 1 decreases, row 2 ends past n; row 0 is still copied
+    got, bad = oracle.copy_rows_i16(src, np.zeros(10, np.int16), [1, 3, 2, 11])
+    assert bad == 1 and np.array_equal(got, [0, 2, 3, 0, 0, 0, 0, 0, 0, 0])
+    assert oracle.copy_rows_i16(src, np.zeros(10, np.int16), [-1, 3])[1] == 0
+    assert oracle.copy_rows_i16(src, np.zeros(10, np.int16), [0, 10, 11])[1] == 1
+
+
 # ------------------------------------------------------------- scheduling
 def test_static_schedule_worked_example():
     want = {}
@@ -289,3 +346,20 @@ def test_planted_bad_rounding_fails_golden():
 
     mism = [tok for tok, v, bits, _ in _golden_bf16() if not math.isnan(v) and trunc(v) != bits]
     assert mism, "the golden cases must distinguish RNE from truncation"
+
+
+@pytest.mark.parametrize("wrong", ["inclusive_end", "ignores_skip", "ignores_row_count"])
+def test_planted_row_copy_mistakes_fail_golden(wrong):
+    meta, cases = _golden_rows()
+    src, off, skip = meta["src"].astype(np.int16), meta["offsets"], meta["skip"]
+
+    def variant(rows, use_skip):
+        d = np.full(src.size, -1, np.int16)
+        for r in range(off.size - 1 if wrong == "ignores_row_count" else rows):
+            if use_skip and skip[r] and wrong != "ignores_skip":
+                continue
+            e = off[r + 1] + (1 if wrong == "inclusive_end" else 0)
+            d[off[r]:min(e, src.size)] = src[off[r]:min(e, src.size)]
+        return d
+
+    assert any(not np.array_equal(variant(rows, use_skip), want) for rows, use_skip, want in cases)

@@ -59,6 +59,12 @@ class LaunchInfo(ctypes.Structure):
                 ("workspace_bytes", ctypes.c_int64)]
 
 
+class RowsOpts(ctypes.Structure):
+    _fields_ = [("tiles", ctypes.c_int64), ("rows_device", ctypes.c_void_p), ("skip_rows", ctypes.c_void_p),
+                ("threads", ctypes.c_int32), ("max_workers", ctypes.c_int32), ("timeout_s", ctypes.c_double),
+                ("trace", ctypes.c_void_p)]
+
+
 class GemmProtocol(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "cluster", "stages", "tx_bytes", "full_arrivals", "empty_arrivals", "accumulators", "tmem_full_arrivals",
@@ -84,6 +90,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ts_gemm_grouped_launch_info.argtypes = [I64, I64, I64, P, I32, I32, ctypes.POINTER(GemmOpts),
                                                 ctypes.POINTER(LaunchInfo)]
     lib.ts_copy_i16.argtypes = [P, P, I64, P]
+    lib.ts_copy_i16_rows.argtypes = [P, P, I64, P, I64, I32, ctypes.POINTER(RowsOpts), P]
+    lib.ts_copy_rows_launch_info.argtypes = [I64, I64, I32, ctypes.POINTER(RowsOpts), ctypes.POINTER(LaunchInfo)]
     lib.ts_spin.argtypes = [I32, I64, P, P]
     lib.ts_spin_wait_started.argtypes = [P, I32, ctypes.c_double]
     lib.ts_sync_and_check.argtypes = [P]
@@ -95,7 +103,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ts_last_error_detail.restype = ctypes.c_char_p
     for name in ("ts_gemm_bf16", "ts_gemm_bf16_ex", "ts_gemm_launch_info", "ts_gemm_bf16_checked_noalloc",
                  "ts_gemm_protocol_info", "ts_gemm_bf16_grouped", "ts_gemm_grouped_launch_info",
-                 "ts_copy_i16", "ts_spin",
+                 "ts_copy_i16", "ts_copy_i16_rows", "ts_copy_rows_launch_info", "ts_spin",
                  "ts_spin_wait_started", "ts_sync_and_check"):
         getattr(lib, name).restype = ctypes.c_int
     return lib
@@ -340,6 +348,66 @@ def ts_copy_i16(src: torch.Tensor, dst: torch.Tensor, stream=None) -> None:
 
 def ts_copy_i16_ptr(src: int, dst: int, n: int, stream=None) -> int:
     return _lib.ts_copy_i16(ctypes.c_void_p(src), ctypes.c_void_p(dst), n, _stream_handle(stream))
+
+
+def _rows_opts(tiles=0, rows_device=None, skip_rows=None, threads=0, max_workers=0, timeout_s=0.0, trace=None):
+    o = RowsOpts()
+    o.tiles = int(tiles)
+    o.threads = int(threads)
+    o.max_workers = int(max_workers)
+    o.timeout_s = float(timeout_s)
+    for name, t, dtype in (("rows_device", rows_device, torch.int64), ("skip_rows", skip_rows, torch.uint8),
+                           ("trace", trace, torch.int64)):
+        if t is None:
+            continue
+        if t.dtype != dtype or not t.is_cuda or not t.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous {dtype} CUDA tensor")
+        setattr(o, name, t.data_ptr())
+    return o
+
+
+def ts_copy_rows_launch_info(n: int, rows: int, sched="clc", **opts) -> dict:
+    o = _rows_opts(**{k: v for k, v in opts.items() if k in ("tiles", "threads", "max_workers")})
+    info = LaunchInfo()
+    _check(_lib.ts_copy_rows_launch_info(int(n), int(rows), _sched(sched), ctypes.byref(o), ctypes.byref(info)))
+    return {f: getattr(info, f) for f, _ in LaunchInfo._fields_}
+
+
+def ts_copy_i16_rows(src: torch.Tensor, dst: torch.Tensor, offsets: torch.Tensor, rows=None, sched="clc", tiles=0,
+                     rows_device=None, skip_rows=None, threads=0, max_workers=0, timeout_s=0.0, trace=None,
+                     stream=None) -> None:
+    """Copy rows [offsets[r], offsets[r+1]) of a jagged int16 array through a work queue.
+
+    src and dst: contiguous int16 CUDA tensors of equal size n; offsets: int64
+    CUDA tensor of rows + 1 entries (rows defaults to offsets.numel() - 1).
+    Tiles past the row count (tiles > rows, or rows_device below rows) and rows
+    marked in skip_rows copy nothing but still take part in the queue."""
+    for t, name in ((src, "src"), (dst, "dst")):
+        if t.dtype != torch.int16 or not t.is_cuda or not t.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous int16 CUDA tensor")
+    if src.numel() != dst.numel():
+        raise ValueError("src and dst differ in size")
+    if offsets.dtype != torch.int64 or not offsets.is_cuda or not offsets.is_contiguous():
+        raise TypeError("offsets must be a contiguous int64 CUDA tensor")
+    if rows is None:
+        rows = max(offsets.numel() - 1, 0)
+    if offsets.numel() < rows + 1:
+        raise ValueError("offsets needs rows + 1 entries")
+    if skip_rows is not None and skip_rows.numel() < rows:
+        raise ValueError("skip_rows needs one byte per row")
+    o = _rows_opts(tiles, rows_device, skip_rows, threads, max_workers, timeout_s, trace)
+    if trace is not None and trace.numel() < 2 * max(int(tiles), int(rows)):
+        raise ValueError("trace needs 2 * tiles entries")
+    _check(_lib.ts_copy_i16_rows(ctypes.c_void_p(src.data_ptr()), ctypes.c_void_p(dst.data_ptr()), src.numel(),
+                                 ctypes.c_void_p(offsets.data_ptr()), int(rows), _sched(sched), ctypes.byref(o),
+                                 _stream_handle(stream)))
+
+
+def ts_copy_i16_rows_ptr(src: int, dst: int, n: int, offsets: int, rows: int, sched=1, stream=None, **opts) -> int:
+    """Raw-pointer call of ts_copy_i16_rows; returns the status without raising."""
+    o = _rows_opts(**opts)
+    return _lib.ts_copy_i16_rows(ctypes.c_void_p(src), ctypes.c_void_p(dst), int(n), ctypes.c_void_p(offsets),
+                                 int(rows), _sched(sched), ctypes.byref(o), _stream_handle(stream))
 
 
 def ts_spin(ctas: int, duration_ns: int, started: torch.Tensor, stream=None) -> None:

@@ -16,12 +16,14 @@ enum : int32_t {
     WAIT_SCHED_CLC_EMPTY = 5,
     WAIT_CLC_FULL = 6,
     WAIT_DRAIN = 7,
+    WAIT_ROWS_CLC = 8,
 };
 
 // Device status word (library-owned, one per device):
-//   [0] first error code (0 = none, 1 = wait timeout)
-//   [1] (where << 32) | blockIdx.x of the first error
-//   [2] number of timed-out waits since the last check
+//   [0] first error code (0 = none, 1 = wait timeout, 2 = row bounds of the
+//       jagged copy outside [0, n])
+//   [1] code 1: (where << 32) | blockIdx.x;  code 2: the row index
+//   [2] number of errors since the last check
 constexpr int kStatusWords = 4;
 
 // Most K parts a split tail tile is cut into: the reduction loads every part

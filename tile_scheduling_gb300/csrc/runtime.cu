@@ -27,6 +27,7 @@ const char *wait_name(int where) {
         case WAIT_SCHED_CLC_EMPTY: return "CLC scheduler waiting for a free response slot";
         case WAIT_CLC_FULL: return "waiting for a CLC response";
         case WAIT_DRAIN: return "waiting for in-flight copies at exit";
+        case WAIT_ROWS_CLC: return "row copy waiting for a CLC response";
         default: return "unknown wait";
     }
 }
@@ -127,9 +128,13 @@ ts_status ts_sync_and_check(void *stream) {
     const unsigned long long zero[ts::kStatusWords] = {0, 0, 0, 0};
     e = cudaMemcpy(dev, zero, sizeof zero, cudaMemcpyHostToDevice);
     if (e != cudaSuccess) return ts::cuda_fail(e, "clearing the status word");
+    if (h[0] == 2)
+        return ts::fail(TS_ERR_INVALID_ARG,
+                        "row %llu of the jagged copy has bounds outside [0, n] or decreasing; %llu rows not copied",
+                        h[1], h[2]);
     const int where = static_cast<int>(h[1] >> 32);
     const unsigned block = static_cast<unsigned>(h[1] & 0xffffffffu);
-    return ts::fail(TS_ERR_TIMEOUT, "barrier wait timed out (%s) in block %u; %llu waits gave up",
+    return ts::fail(TS_ERR_TIMEOUT, "barrier wait timed out (%s) in block %u; %llu errors recorded",
                     ts::wait_name(where), block, h[2]);
 }
 
