@@ -273,18 +273,18 @@ def run_ours(args, ws, rank, local):
     return line
 
 
-def _event_ms(fn, stream, hide_host=True):
+def _event_ms(fn, stream, sleep_cycles=500_000):
     """Device time of fn's launches on `stream` (CUDA events).
 
-    hide_host: a short GPU sleep queued ahead of the start event keeps the device
-    busy while the host runs fn's Python and C setup, so that host overhead does
-    not fall inside the timed region (otherwise an idle GPU records the start
-    event at once and the gap until the launch is counted)."""
+    A short GPU sleep queued ahead of the start event keeps the device busy
+    while the host runs fn's Python and C setup, so that host overhead does not
+    fall inside the timed region (otherwise an idle GPU records the start event
+    at once and the gap until the launch is counted)."""
     import torch
 
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if hide_host:
-        torch.cuda._sleep(500_000)
+    if sleep_cycles:
+        torch.cuda._sleep(sleep_cycles)
     e0.record(stream)
     fn()
     e1.record(stream)
@@ -536,15 +536,17 @@ def run_contended(args, ws, rank, local):
         for _ in range(args.warmup):
             gemm(sched)
         solo[sched] = statistics.median([_event_ms(lambda: gemm(sched), stream) for _ in range(args.reps)])
-    spin_ns = int(0.5 * solo["static"] * 1e6)
+    # half the solo time from the GEMM's start, plus the ~30 us of sleep queued ahead of it
+    spin_ns = int(0.5 * solo["static"] * 1e6) + 30_000
 
     def contended(sched, trace=None):
         started.zero_()
         torch.cuda.synchronize()
         ts.ts_spin(ctas, spin_ns, started, stream=side)
         ts.ts_spin_wait_started(started, ctas, 5.0)
-        # no sleep ahead: the GEMM must start while the spin still holds its SMs
-        ms = _event_ms(lambda: gemm(sched, trace), stream, hide_host=False)
+        # a short sleep only (~30 us): it hides the host's launch work, and the GEMM
+        # still starts while the spin holds its SMs for most of its time
+        ms = _event_ms(lambda: gemm(sched, trace), stream, sleep_cycles=60_000)
         torch.cuda.synchronize()
         return ms
 

@@ -229,4 +229,4 @@ class RowsWorkload:
 
 
 ROWS = RowsWorkload("jagged int16 copy, 8192 rows of 64..262144 elements (log-uniform)", 8192, 64, 262144,
-                    SEED_BASE + 6)
+                    SEED_BASE + 8)
