@@ -46,7 +46,8 @@ TRAFFIC_PATH = os.path.join(ROOT, "profiles", "traffic.txt")
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_BF16_SUSTAINED = 1700.0
-KERNEL_SOURCES = {"gemm": ["gemm_kernel.cuh", "ptx.cuh", "gemm_params.h", "gemm_launch.cuh"], "copy": ["copy.cu"]}
+KERNEL_SOURCES = {"gemm": ["gemm_kernel.cuh", "ptx.cuh", "gemm_params.h", "gemm_launch.cuh"], "copy": ["copy.cu"],
+                  "rows": ["rows_copy.cu", "ptx.cuh", "gemm_params.h"]}
 
 
 # ------------------------------------------------------------------ helpers
@@ -499,7 +500,7 @@ def run_rows(args, ws, rank, local):
             "unit": "GB/s", "value": best, **res,
             "clc_speedup_over_static": round(res["static"]["ms_median"] / res["clc"]["ms_median"], 3),
             "roofline": {"bound": "hbm", "achieved": best, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": round(best / peaks["hbm_gbs"], 4), "traffic": None,
+                         "frac": round(best / peaks["hbm_gbs"], 4), "traffic": load_traffic("rows", "8192 rows log-uniform"),
                          "peak_kind": f"{peaks['source']} HBM copy", "kernel": "rows_copy_kernel"},
             "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "dtype": "int16",
             "data": "synthetic", "config": {"workload": w.name, "elements": int(src.numel()), "rows": w.rows,

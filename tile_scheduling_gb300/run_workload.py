@@ -1,6 +1,6 @@
 """Run one named workload a few times (for profilers such as ncu); prints nothing but a summary line.
 
-Usage: python -m tile_scheduling_gb300.run_workload {gemm256,gemm4096,gemm8192,ragged,copy}
+Usage: python -m tile_scheduling_gb300.run_workload {gemm256,gemm4096,gemm8192,ragged,copy,rows}
            [--launches N] [--sched static|clc] [--tile auto|128x128|128x256|256x256]
 """
 from __future__ import annotations
@@ -26,7 +26,7 @@ GEMMS = {"gemm256": synth.GEMM_256, "gemm4096": synth.GEMM_4096, "gemm8192": syn
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("workload", choices=sorted(GEMMS) + ["copy"])
+    ap.add_argument("workload", choices=sorted(GEMMS) + ["copy", "rows"])
     ap.add_argument("--launches", type=int, default=3)
     ap.add_argument("--sched", default=None, choices=["static", "clc"])
     ap.add_argument("--tile", default=None)
@@ -38,6 +38,17 @@ def main(argv=None):
             ts.ts_copy_i16(src, dst)
         ts.ts_sync_and_check()
         print(f"copy n={synth.COPY_N} x{a.launches} ok")
+        return 0
+    if a.workload == "rows":
+        src_h, off_h = synth.ROWS.inputs()
+        src = torch.from_numpy(src_h).cuda()
+        dst = torch.empty_like(src)
+        off = torch.from_numpy(off_h).cuda()
+        sched = a.sched or "clc"
+        for _ in range(a.launches):
+            ts.ts_copy_i16_rows(src, dst, off, sched=sched)
+        ts.ts_sync_and_check()
+        print(f"{synth.ROWS.name}: {sched} x{a.launches} ok")
         return 0
     w = GEMMS[a.workload]
     A_bits, B_bits = w.inputs()
