@@ -145,6 +145,32 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
     return wait_slow(bar, parity, p.timeout_ns, abort_flag, true, p, where);
 }
 
+// Bounded wait for roles whose waits last about a tile and whose wake-up is not
+// on the critical path (epilogue warps waiting for an accumulator, the CLC
+// scheduler waiting for a free slot): it sleeps between polls, leaving the
+// issue slots and shared-memory port of its SM sub-partition to the producer
+// and the MMA issuer.  Measured: 0.5-1 % faster at 8192^3 than polling.
+static __device__ __noinline__ bool wait_long_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                                   const GemmParams &p, int where) {
+    const uint64_t t0 = globaltimer();
+    for (;;) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer() - t0 > p.timeout_ns) {
+            report_timeout(p, where);
+            *abort_flag = 1;
+            return false;
+        }
+        __nanosleep(500);
+    }
+}
+
+__device__ __forceinline__ bool wait_long(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                          const GemmParams &p, int where) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_long_slow(bar, parity, abort_flag, p, where);
+}
+
 __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, volatile int *abort_flag,
                                            const GemmParams &p) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -462,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t r = idx % depth;
                 const uint32_t ph = (idx / depth) & 1u;
                 if (rank == 0) {
-                    if (!wait_phase(sm.clc_empty(r), ph ^ 1u, sm.abort_flag, p, WAIT_SCHED_CLC_EMPTY)) break;
+                    if (!wait_long(sm.clc_empty(r), ph ^ 1u, sm.abort_flag, p, WAIT_SCHED_CLC_EMPTY)) break;
                     fence_proxy_async_smem();
                     mbar_arrive_expect_tx(sm.clc_full(r), C::CLC_RESPONSE_BYTES);
                     if constexpr (CG == 1)
@@ -637,7 +663,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool split = w.tail >= 0;
             if (!w.skip) {
             int ok = 1;
-            if (lane == 0) ok = wait_phase(sm.tfull(acc), acc_phase, sm.abort_flag, p, WAIT_EPI_TMEM_FULL);
+            if (lane == 0) ok = wait_long(sm.tfull(acc), acc_phase, sm.abort_flag, p, WAIT_EPI_TMEM_FULL);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             tc_fence_after();
