@@ -216,6 +216,26 @@ ts_status ts_gemm_launch_info(int64_t M, int64_t N, int64_t K, int32_t out_dtype
                               const ts_gemm_opts *opts, ts_launch_info *info);
 
 /*
+ * ts_gemm_tile_coords -- the output tile that each tile id of the launch
+ * ts_gemm_bf16_ex would make covers (host only, no launch).  The kernel's
+ * raster walks `raster_group` tile rows down one column band before moving to
+ * the next band (a build choice for L2 reuse; the pages leave tile order
+ * open).  The host evaluates the very function the kernel runs.
+ *
+ *   M, N, K, out_dtype, sched, opts   as for ts_gemm_launch_info (opts->tile and
+ *                                     opts->raster_group matter)
+ *   first_tile, count   tile ids [first_tile, first_tile + count) within
+ *                       [0, tiles_m * tiles_n)
+ *   m_block, n_block    HOST int32 arrays of `count` entries, written with the
+ *                       tile row and tile column of each id
+ * Errors: TS_ERR_INVALID_ARG for a range outside the tile grid or NULL outputs
+ * (count > 0), plus the argument errors of ts_gemm_launch_info.
+ */
+ts_status ts_gemm_tile_coords(int64_t M, int64_t N, int64_t K, int32_t out_dtype, int32_t sched,
+                              const ts_gemm_opts *opts, int64_t first_tile, int64_t count, int32_t *m_block,
+                              int32_t *n_block);
+
+/*
  * ts_gemm_bf16_checked_noalloc -- ts_gemm_bf16 (default tile choice) plus a
  * check that the tile scheduler computed every output tile exactly once, for
  * callers that cannot allocate device memory.  No counterpart in the pages:

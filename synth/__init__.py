@@ -176,6 +176,9 @@ GEMM_8192 = _w(3, "gemm 8192x8192x8192 bf16-out 2-CTA 256x256 clc", 8192, 8192, 
                ("clc",))
 GEMM_RAGGED = _w(4, "gemm 8191x6143x4096 fp32-out ragged contended", 8191, 6143, 4096, "f32", "uniform", "128x256",
                  ("static", "clc"))
+# K = 64 is one k-block per tile: the 134 MB bf16 output dominates the traffic (HBM-bound GEMM).
+GEMM_SMALLK = _w(10, "gemm 8192x8192x64 bf16-out small-K (output-write bound)", 8192, 8192, 64, "bf16", "uniform",
+                 "256x256", ("static", "clc"))
 COPY_N = 1 << 28
 COPY_SEED = SEED_BASE + 1
 

@@ -23,3 +23,11 @@ def lib():
     import tile_scheduling_gb300 as ts
 
     return ts
+
+
+@pytest.fixture(scope="session")
+def ts():
+    """The binding for host-only calls (loads the built library; no GPU needed)."""
+    import tile_scheduling_gb300 as ts
+
+    return ts

@@ -15,13 +15,6 @@ def _declared():
     return sorted(set(re.findall(r"\b(ts_[a-z0-9_]+)\s*\(", src)))
 
 
-@pytest.fixture(scope="module")
-def ts():
-    import tile_scheduling_gb300 as ts
-
-    return ts
-
-
 def test_header_declares_the_api():
     names = _declared()
     for n in ("ts_gemm_bf16", "ts_gemm_bf16_ex", "ts_copy_i16", "ts_sync_and_check"):

@@ -54,6 +54,19 @@ def test_gemm_integer_bit_exact(lib, tile, sched, out):
     assert_bit_exact(D, oracle.gemm_f64(A, B), f"integer {tile} {sched}")
 
 
+@pytest.mark.parametrize("G", [1, 2, 3, 5, 8, 16, 64])
+@pytest.mark.parametrize("tile,sched", [("128x128", "clc"), ("128x256", "static"), ("256x256", "clc"),
+                                        ("256x256", "static")])
+def test_gemm_raster_groups_cover_every_tile(lib, G, tile, sched):
+    # tile rows not a multiple of the raster group, so the last group is shorter;
+    # every tile id must land on a distinct tile (NaN-filled D shows a missed one)
+    M, N, K = 1100, 1300, 128
+    A = synth.int_uniform_bf16(141 + G, (M, K))
+    B = synth.int_uniform_bf16(241 + G, (N, K))
+    D = _run(lib, A, B, torch.float32, sched=sched, tile=tile, raster_group=G)
+    assert_bit_exact(D, oracle.gemm_f64(A, B), f"raster group {G} {tile} {sched}")
+
+
 @pytest.mark.parametrize("tile", TILES)
 @pytest.mark.parametrize("sched", SCHEDS)
 def test_gemm_one_hot_selects_columns(lib, tile, sched):
@@ -206,6 +219,28 @@ def test_gemm_8192_bf16_2cta_clc_sampled_rows(lib):
     e, ea = oracle.gemm_entries_f64(A, B, ii, cols)
     got2 = oracle.bf16_to_f64(bf16_bits(D[torch.as_tensor(ii, device="cuda"), torch.as_tensor(cols, device="cuda")]))
     assert_within_bound(got2, e, ea, torch.bfloat16, "8192^3 sampled entries")
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("sched", SCHEDS)
+@pytest.mark.parametrize("tile", ["128x256", "256x256"])
+def test_gemm_small_k_sampled(lib, sched, tile):
+    # 8192x8192x64: one k-block per tile, the output-write-bound launch the bench times
+    w = synth.GEMM_SMALLK
+    A, B = w.inputs()
+    D = _run(lib, A, B, torch.bfloat16, sched=sched, tile=tile)
+    rng = np.random.default_rng(64)
+    rows = np.unique(np.concatenate([rng.integers(0, w.M, 128), [0, 127, 128, 255, 256, w.M - 1]]))
+    a = oracle.bf16_to_f64(A[rows])
+    b = oracle.bf16_to_f64(B)
+    assert_within_bound(oracle.bf16_to_f64(bf16_bits(D[torch.as_tensor(rows, device="cuda")])), a @ b.T,
+                        np.abs(a) @ np.abs(b).T, torch.bfloat16, f"8192x8192x64 {sched} {tile} sampled rows")
+    ii = rng.integers(0, w.M, 256)
+    jj = rng.integers(0, w.N, 256)
+    e, ea = oracle.gemm_entries_f64(A, B, ii, jj)
+    got = oracle.bf16_to_f64(bf16_bits(D[torch.as_tensor(ii, device="cuda"), torch.as_tensor(jj, device="cuda")]))
+    assert_within_bound(got, e, ea, torch.bfloat16, f"8192x8192x64 {sched} {tile} sampled entries")
+    assert not torch.isnan(D).any()  # every output tile was written
 
 
 @pytest.mark.slow

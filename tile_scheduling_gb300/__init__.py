@@ -82,6 +82,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ts_gemm_launch_info.argtypes = [I64, I64, I64, I32, I32, ctypes.POINTER(GemmOpts),
                                         ctypes.POINTER(LaunchInfo)]
     lib.ts_gemm_bf16_checked_noalloc.argtypes = [P, P, P, I64, I64, I64, I32, I32, P, P]
+    lib.ts_gemm_tile_coords.argtypes = [I64, I64, I64, I32, I32, ctypes.POINTER(GemmOpts), I64, I64, P, P]
     lib.ts_gemm_protocol_info.argtypes = [I32, I32, ctypes.POINTER(GemmProtocol)]
     lib.ts_protocol_check.argtypes = [I32, P, I32, I32, P, P, P, ctypes.c_char_p, I64, ctypes.POINTER(I64),
                                       ctypes.c_char_p, I32]
@@ -102,7 +103,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ts_last_error_detail.argtypes = []
     lib.ts_last_error_detail.restype = ctypes.c_char_p
     for name in ("ts_gemm_bf16", "ts_gemm_bf16_ex", "ts_gemm_launch_info", "ts_gemm_bf16_checked_noalloc",
-                 "ts_gemm_protocol_info", "ts_gemm_bf16_grouped", "ts_gemm_grouped_launch_info",
+                 "ts_gemm_tile_coords", "ts_gemm_protocol_info", "ts_gemm_bf16_grouped", "ts_gemm_grouped_launch_info",
                  "ts_copy_i16", "ts_copy_i16_rows", "ts_copy_rows_launch_info", "ts_spin",
                  "ts_spin_wait_started", "ts_sync_and_check"):
         getattr(lib, name).restype = ctypes.c_int
@@ -282,6 +283,28 @@ def ts_gemm_launch_info(M: int, N: int, K: int, out=TS_OUT_BF16, sched="static",
     """The launch ts_gemm_bf16_ex would make; ``workspace`` resolves as in that call."""
     ws = _resolve_workspace(M, N, K, out, sched, workspace, split_tail, **opts)
     return _launch_info_raw(M, N, K, out, sched, workspace=ws, split_tail=split_tail, **opts)
+
+
+def ts_gemm_tile_coords(M: int, N: int, K: int, out=TS_OUT_BF16, sched="static", first=0, count=None, tile="auto",
+                        raster_group=0):
+    """(m_block, n_block) int32 arrays: the output tile that each tile id of the launch covers."""
+    import numpy as np
+
+    o = _opts(tile=tile, raster_group=raster_group)
+    if count is None:
+        if o.tile == TS_TILE_AUTO:  # the automatic choice depends on the device
+            info = _launch_info_raw(M, N, K, out, sched, tile=tile, raster_group=raster_group)
+            tiles = info["tiles_m"] * info["tiles_n"]
+        else:
+            bm = 256 if o.tile == TS_TILE_256x256_2CTA else 128
+            bn = 128 if o.tile == TS_TILE_128x128 else 256
+            tiles = -(-max(M, 0) // bm) * -(-max(N, 0) // bn)
+        count = tiles - first
+    mb = np.zeros(max(count, 0), dtype=np.int32)
+    nb = np.zeros(max(count, 0), dtype=np.int32)
+    _check(_lib.ts_gemm_tile_coords(M, N, K, int(out), _sched(sched), ctypes.byref(o), first, count,
+                                    mb.ctypes.data, nb.ctypes.data))
+    return mb, nb
 
 
 def _offsets(k_offsets) -> "np.ndarray":

@@ -88,6 +88,19 @@ ts_status make_map_d(CUtensorMap *m, const void *ptr, CUtensorMapDataType dt, in
     return TS_OK;
 }
 
+// Multiplier and shift of FastDiv for divisor d (1 <= d < 2^31; an empty grid's
+// divisor 0 is taken as 1, it divides nothing).
+FastDiv fast_div_for(int64_t d) {
+    if (d < 1) d = 1;
+    int l = 0;
+    while ((int64_t{1} << l) < d) ++l;
+    FastDiv f;
+    f.s = 31 + l;
+    f.m = ((uint64_t{1} << f.s) + static_cast<uint64_t>(d) - 1) / static_cast<uint64_t>(d);
+    f.pad = 0;
+    return f;
+}
+
 template <class T>
 __global__ void zero_fill_kernel(T *D, int64_t M, int64_t N, int64_t ldd) {
     const int64_t total = M * N;
@@ -124,6 +137,18 @@ constexpr int64_t kMinKBlocksPerPart = 4;
 constexpr int64_t kCounterRegionBytes = 8192;
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// The raster's group size and division constants for a planned launch.
+void set_raster(GemmParams &p, const Plan &pl, const ts_gemm_opts *o) {
+    p.tiles_m = static_cast<int32_t>(pl.tiles_m);
+    p.tiles_n = static_cast<int32_t>(pl.tiles_n);
+    p.raster_group = o->raster_group > 0 ? o->raster_group : kDefaultRaster;
+    const int64_t G = p.raster_group;
+    const int64_t groups_m = cdiv(pl.tiles_m, G);
+    p.div_group_tiles = fast_div_for(G * pl.tiles_n);
+    p.div_group_rows = fast_div_for(G);
+    p.div_last_rows = fast_div_for(pl.tiles_m - (groups_m - 1) * G);
+}
 
 ts_status plan_gemm(const void *D, int64_t M, int64_t N, int64_t K, int32_t out, int32_t sched,
                     const ts_gemm_opts *o, Plan *pl, int64_t groups = 0) {
@@ -262,6 +287,54 @@ ts_status ts_gemm_launch_info(int64_t M, int64_t N, int64_t K, int32_t out_dtype
     return ts::fill_info(M, N, K, out_dtype, sched, opts, info, 0);
 }
 
+ts_status ts_gemm_tile_coords(int64_t M, int64_t N, int64_t K, int32_t out_dtype, int32_t sched,
+                              const ts_gemm_opts *opts, int64_t first_tile, int64_t count, int32_t *m_block,
+                              int32_t *n_block) {
+    ts::Plan pl;
+    std::memset(&pl, 0, sizeof pl);
+    const int32_t tile = opts ? opts->tile : TS_TILE_AUTO;
+    if (tile == TS_TILE_AUTO) {
+        // the automatic tile choice depends on the device's SM count
+        ts_status s = ts::plan_gemm(reinterpret_cast<const void *>(uintptr_t(256)), M, N, K, out_dtype, sched, opts,
+                                    &pl, 0);
+        if (s != TS_OK) return s;
+    } else {
+        // an explicit tile fixes the grid of tiles: no device is needed
+        if (M < 0 || N < 0 || K < 0 || M > ts::kMaxDim || N > ts::kMaxDim || K > ts::kMaxDim)
+            return ts::fail(TS_ERR_INVALID_ARG, "sizes must be in [0, 2^31-1]");
+        if (out_dtype != TS_OUT_BF16 && out_dtype != TS_OUT_F32)
+            return ts::fail(TS_ERR_INVALID_ARG, "out_dtype %d", out_dtype);
+        if (sched != TS_SCHED_STATIC && sched != TS_SCHED_CLC) return ts::fail(TS_ERR_INVALID_ARG, "sched %d", sched);
+        if (tile < TS_TILE_AUTO || tile > TS_TILE_256x256_2CTA) return ts::fail(TS_ERR_INVALID_ARG, "tile %d", tile);
+        if (opts->raster_group < 0) return ts::fail(TS_ERR_INVALID_ARG, "negative option");
+        const int64_t tile_m = tile == TS_TILE_256x256_2CTA ? 256 : 128;
+        const int64_t tile_n = tile == TS_TILE_128x128 ? 128 : 256;
+        pl.tiles_m = ts::cdiv(M, tile_m);
+        pl.tiles_n = ts::cdiv(N, tile_n);
+        if (pl.tiles_m * pl.tiles_n * (tile_m / 128) > ts::kMaxDim)
+            return ts::fail(TS_ERR_UNSUPPORTED, "too many output tiles");
+    }
+    const int64_t tiles = pl.tiles_m * pl.tiles_n;
+    if (first_tile < 0 || count < 0 || first_tile > tiles || count > tiles - first_tile)
+        return ts::fail(TS_ERR_INVALID_ARG, "tiles [%lld, %lld + %lld) outside [0, %lld)",
+                        static_cast<long long>(first_tile), static_cast<long long>(first_tile),
+                        static_cast<long long>(count), static_cast<long long>(tiles));
+    if (count > 0 && (!m_block || !n_block)) return ts::fail(TS_ERR_INVALID_ARG, "m_block or n_block is NULL");
+    ts_gemm_opts z;
+    std::memset(&z, 0, sizeof z);
+    ts::GemmParams p;
+    std::memset(&p, 0, sizeof p);
+    if (count == 0) return TS_OK;
+    ts::set_raster(p, pl, opts ? opts : &z);
+    for (int64_t t = 0; t < count; ++t) {
+        int32_t mb, nb;
+        ts::raster(static_cast<int32_t>(first_tile + t), p, mb, nb);
+        m_block[t] = mb;
+        n_block[t] = nb;
+    }
+    return TS_OK;
+}
+
 ts_status ts_gemm_protocol_info(int32_t tile, int32_t out_dtype, ts_gemm_protocol *proto) {
     if (!proto) return ts::fail(TS_ERR_INVALID_ARG, "proto is NULL");
     if (out_dtype != TS_OUT_BF16 && out_dtype != TS_OUT_F32) return ts::fail(TS_ERR_INVALID_ARG, "out_dtype %d", out_dtype);
@@ -369,7 +442,7 @@ ts_status gemm_launch(const void *A, const void *B, void *D, int64_t M, int64_t 
         p.counters = static_cast<int32_t *>(o->workspace);
         p.partials = reinterpret_cast<float *>(static_cast<char *>(o->workspace) + pl.counter_bytes);
     }
-    p.raster_group = o->raster_group > 0 ? o->raster_group : kDefaultRaster;
+    set_raster(p, pl, o);
     p.sched = sched;
     p.tma_store = pl.tma_store;
     p.clc_depth = 2;

@@ -177,19 +177,6 @@ __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, volati
     return wait_slow(bar, parity, p.drain_ns, abort_flag, false, p, WAIT_DRAIN);
 }
 
-// Tile id -> (m block, n block): consecutive ids walk `raster_group` tile rows
-// down a column band, so workers running at the same time share B tiles in L2.
-__device__ __forceinline__ void raster(int32_t tile, const GemmParams &p, int32_t &mb, int32_t &nb) {
-    const int32_t G = p.raster_group;
-    const int32_t per_group = G * p.tiles_n;
-    const int32_t g = tile / per_group;
-    const int32_t first_m = g * G;
-    const int32_t gsize = min(G, p.tiles_m - first_m);
-    const int32_t local = tile - g * per_group;
-    mb = first_m + local % gsize;
-    nb = local / gsize;
-}
-
 // Shared-memory map of one CTA.
 template <class C>
 struct Smem {

@@ -40,11 +40,26 @@ constexpr int kMaxGroups = 256;
 // of tile full_tiles + t.  Split units write fp32 partials to `workspace`; the
 // warp that finishes a 32-row slab last (per-slab counter) sums the parts in
 // order 0..parts-1 and stores D.
+// Division of a non-negative int32 by a divisor fixed at launch, as a
+// multiply-high and shift (Granlund and Montgomery, "Division by Invariant
+// Integers using Multiplication", 1994): for d >= 1, l = ceil(log2 d),
+// s = 31 + l and m = ceil(2^s / d), floor(n / d) = (n * m) >> s for every
+// 0 <= n < 2^31.  m < 2^32 always; the product is taken in 64 bits.
+struct FastDiv {
+    uint64_t m;
+    int32_t s;
+    int32_t pad;
+};
+
 struct GemmParams {
     int32_t M, N, K;
     int32_t tiles_m, tiles_n, num_tiles, num_k_blocks;
     int32_t num_units, full_tiles, split_tiles, parts;
     int32_t raster_group;  // >= 1
+    int32_t pad1;
+    // the raster's divisors: tiles per group of tile rows (raster_group * tiles_n),
+    // raster_group, and the height of the last (possibly shorter) group
+    FastDiv div_group_tiles, div_group_rows, div_last_rows;
     int32_t sched;         // SCHED_STATIC / SCHED_CLC
     int32_t tma_store;     // 1: TMA-store epilogue, 0: st.global epilogue
     int32_t clc_depth;     // response slots in flight (1 or 2)
@@ -67,5 +82,32 @@ struct GemmParams {
     int64_t group_stride;
     int32_t group_kb[kMaxGroups + 1];
 };
+
+#if defined(__CUDACC__)
+#define TS_HOST_DEVICE __host__ __device__ __forceinline__
+#else
+#define TS_HOST_DEVICE inline
+#endif
+
+TS_HOST_DEVICE int32_t fast_div(int32_t n, const FastDiv &d) {
+    return static_cast<int32_t>((static_cast<uint64_t>(static_cast<uint32_t>(n)) * d.m) >> d.s);
+}
+
+// Tile id -> (m block, n block).  Consecutive ids walk `raster_group` tile rows
+// down a column band, so workers running at the same time share B tiles in L2.
+// The divisions go through FastDiv: the epilogue warps decode every tile on
+// their own critical path, where the GPU's multi-instruction integer divide
+// cost ~270 cycles per tile.  The host evaluates the same function to report
+// the mapping (ts_gemm_tile_coords).
+TS_HOST_DEVICE void raster(int32_t tile, const GemmParams &p, int32_t &mb, int32_t &nb) {
+    const int32_t G = p.raster_group;
+    const int32_t g = fast_div(tile, p.div_group_tiles);
+    const int32_t first_m = g * G;
+    const bool last = first_m + G > p.tiles_m;  // the last group may hold fewer tile rows
+    const int32_t gsize = last ? p.tiles_m - first_m : G;
+    const int32_t local = tile - g * (G * p.tiles_n);
+    nb = fast_div(local, last ? p.div_last_rows : p.div_group_rows);
+    mb = first_m + (local - nb * gsize);
+}
 
 }  // namespace ts

@@ -54,8 +54,15 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 }
 
 // Arrive on a barrier given by its shared::cluster address (any CTA of the cluster).
+// The release is CTA-scoped (the instruction's default semantics).  Both callers
+// only hand back storage they have finished reading: a TMEM accumulator after
+// tcgen05.wait::ld and tcgen05.fence::before_thread_sync, or a CLC response slot
+// after its read and a proxy fence.  A cluster-scoped release would also wait
+// until all of the thread's earlier writes are visible to the whole cluster,
+// including the epilogue's staging writes; on the peer CTA of a 2-SM tile that
+// cost about 1.7k cycles per tile.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+    asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
 
 // One probe of phase `parity`; true once that phase has completed.

@@ -1,6 +1,6 @@
 """Run one named workload a few times (for profilers such as ncu); prints nothing but a summary line.
 
-Usage: python -m tile_scheduling_gb300.run_workload {gemm256,gemm4096,gemm8192,ragged,copy,rows}
+Usage: python -m tile_scheduling_gb300.run_workload {gemm256,gemm4096,gemm8192,ragged,smallk,copy,rows}
            [--launches N] [--sched static|clc] [--tile auto|128x128|128x256|256x256]
 """
 from __future__ import annotations
@@ -21,7 +21,7 @@ import synth  # noqa: E402
 import tile_scheduling_gb300 as ts  # noqa: E402
 
 GEMMS = {"gemm256": synth.GEMM_256, "gemm4096": synth.GEMM_4096, "gemm8192": synth.GEMM_8192,
-         "ragged": synth.GEMM_RAGGED}
+         "ragged": synth.GEMM_RAGGED, "smallk": synth.GEMM_SMALLK}
 
 
 def main(argv=None):
