@@ -257,7 +257,7 @@ def run_ours(args, ws, rank, local):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": workload, "M": M, "N": N, "K": K, "out": "bf16", "tile": args.tile,
                    "sched": args.sched, "tiles": info["num_tiles"], "grid_ctas": info["grid_ctas"],
-                   "stages": info["stages"], "copy_n": n_copy,
+                   "stages": info["stages"], "epi_warps": info["epi_warps"], "copy_n": n_copy,
                    "l2": "inputs larger than L2 (256 MiB GEMM operands, 1 GiB copy traffic); no flush",
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
         "gemm": {"tflops": round(gemm_tflops, 2), "ms_median": round(statistics.median(gemm_ms), 4),
@@ -561,6 +561,8 @@ def run_smallk(args, ws, rank, local):
             "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "dtype": "bf16",
             "data": "synthetic", "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "tile": h_tile,
                                             "sched": h_sched, "launches_per_sample": batch,
+                                            "epi_warps": ts.ts_gemm_launch_info(w.M, w.N, w.K, ts.TS_OUT_BF16, h_sched,
+                                                                                tile=h_tile)["epi_warps"],
                                             "l2": "output (134 MB) larger than L2; A and B (1 MiB each) stay resident; no flush"}}
 
 

@@ -78,6 +78,10 @@ typedef struct {
                              correction term of zero-point-quantised products.  Rows whose first
                              tile column is skipped are left untouched.  1-CTA tiles only (AUTO
                              picks one; TS_TILE_256x256_2CTA is TS_ERR_UNSUPPORTED); no split tail. */
+    int32_t epi_warps;    /* epilogue warps per CTA: 4 (one per TMEM lane quarter) or 8 (two per
+                             quarter, alternating subtiles: more latency hidden when the epilogue
+                             bounds the tile); 0 = 8 for a plain GEMM with K <= 512, else 4.
+                             Anything else is TS_ERR_INVALID_ARG.  Results do not depend on it. */
 } ts_gemm_opts;
 
 /* What ts_gemm_bf16_ex would launch for a problem (host-only query). */
@@ -95,6 +99,7 @@ typedef struct {
     int32_t split_parts;     /* K parts per split tile (1 if none) */
     int32_t resident;        /* workers (CTAs or 2-CTA clusters) that fit on the GPU at once */
     int64_t workspace_bytes; /* workspace a split tail needs (0 when no split would help) */
+    int32_t epi_warps;       /* epilogue warps per CTA (4 or 8; CTAs have 128 + 32 * epi_warps threads) */
 } ts_launch_info;
 
 /* The barrier protocol of one kernel variant: the numbers the kernel
@@ -119,9 +124,9 @@ typedef struct {
 } ts_gemm_protocol;
 
 /* Fill *proto for the kernel variant of `tile` (TS_TILE_128x128, _128x256 or
- * _256x256_2CTA; TS_TILE_AUTO is TS_ERR_INVALID_ARG) and `out_dtype`.  Host
- * only; needs no GPU. */
-ts_status ts_gemm_protocol_info(int32_t tile, int32_t out_dtype, ts_gemm_protocol *proto);
+ * _256x256_2CTA; TS_TILE_AUTO is TS_ERR_INVALID_ARG), `out_dtype` and
+ * `epi_warps` (4 or 8; 0 = 4).  Host only; needs no GPU. */
+ts_status ts_gemm_protocol_info(int32_t tile, int32_t out_dtype, int32_t epi_warps, ts_gemm_protocol *proto);
 
 /*
  * ts_protocol_check -- explore every interleaving of a small mbarrier program

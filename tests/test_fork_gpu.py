@@ -13,15 +13,16 @@ pytestmark = pytest.mark.gpu
 
 @pytest.mark.parametrize("tile", ["128x128", "128x256"])
 @pytest.mark.parametrize("sched", ["static", "clc"])
-def test_fork_integer_exact(lib, tile, sched):
+@pytest.mark.parametrize("ew", [4, 8])
+def test_fork_integer_exact(lib, tile, sched, ew):
     M, N, K = 700, 600, 640
     A = synth.int_uniform_bf16(801, (M, K))
     B = synth.int_uniform_bf16(802, (N, K))
     D = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
     R = torch.full((M,), float("nan"), dtype=torch.float32, device="cuda")
-    lib.ts_gemm_bf16_ex(to_device_bf16(A), to_device_bf16(B), D, sched=sched, tile=tile, row_sums=R)
+    lib.ts_gemm_bf16_ex(to_device_bf16(A), to_device_bf16(B), D, sched=sched, tile=tile, row_sums=R, epi_warps=ew)
     lib.ts_sync_and_check()
-    assert_bit_exact(D, oracle.gemm_f64(A, B), f"fork D {tile} {sched}")
+    assert_bit_exact(D, oracle.gemm_f64(A, B), f"fork D {tile} {sched} {ew}")
     assert np.array_equal(R.cpu().numpy().astype(np.float64), oracle.row_sums_f64(A, [0, K])[0])
 
 

@@ -46,12 +46,23 @@ def test_gemm_256_fp32_static_128x128(lib):
 @pytest.mark.parametrize("tile", TILES)
 @pytest.mark.parametrize("sched", SCHEDS)
 @pytest.mark.parametrize("out", OUTS)
-def test_gemm_integer_bit_exact(lib, tile, sched, out):
+@pytest.mark.parametrize("ew", [4, 8])
+def test_gemm_integer_bit_exact(lib, tile, sched, out, ew):
     M, N, K = 600, 520, 328  # ragged in M, N and K
     A = synth.int_uniform_bf16(101, (M, K))
     B = synth.int_uniform_bf16(102, (N, K))
-    D = _run(lib, A, B, out, sched=sched, tile=tile)
-    assert_bit_exact(D, oracle.gemm_f64(A, B), f"integer {tile} {sched}")
+    D = _run(lib, A, B, out, sched=sched, tile=tile, epi_warps=ew)
+    assert_bit_exact(D, oracle.gemm_f64(A, B), f"integer {tile} {sched} {ew} epilogue warps")
+
+
+def test_gemm_epilogue_warps_automatic_choice(lib):
+    # eight epilogue warps for a short K loop, four for a long one or a grouped GEMM
+    assert lib.ts_gemm_launch_info(4096, 4096, 512, lib.TS_OUT_BF16, "clc")["epi_warps"] == 8
+    assert lib.ts_gemm_launch_info(4096, 4096, 576, lib.TS_OUT_BF16, "clc")["epi_warps"] == 4
+    assert lib.ts_gemm_launch_info(4096, 4096, 64, lib.TS_OUT_BF16, "clc", epi_warps=4)["epi_warps"] == 4
+    assert lib.ts_gemm_grouped_launch_info(512, 512, [0, 64, 128])["epi_warps"] == 4
+    with pytest.raises(lib.TsError):
+        lib.ts_gemm_launch_info(4096, 4096, 64, lib.TS_OUT_BF16, "clc", epi_warps=2)
 
 
 @pytest.mark.parametrize("G", [1, 2, 3, 5, 8, 16, 64])
@@ -224,11 +235,12 @@ def test_gemm_8192_bf16_2cta_clc_sampled_rows(lib):
 @pytest.mark.slow
 @pytest.mark.parametrize("sched", SCHEDS)
 @pytest.mark.parametrize("tile", ["128x256", "256x256"])
-def test_gemm_small_k_sampled(lib, sched, tile):
+@pytest.mark.parametrize("ew", [4, 8])
+def test_gemm_small_k_sampled(lib, sched, tile, ew):
     # 8192x8192x64: one k-block per tile, the output-write-bound launch the bench times
     w = synth.GEMM_SMALLK
     A, B = w.inputs()
-    D = _run(lib, A, B, torch.bfloat16, sched=sched, tile=tile)
+    D = _run(lib, A, B, torch.bfloat16, sched=sched, tile=tile, epi_warps=ew)
     rng = np.random.default_rng(64)
     rows = np.unique(np.concatenate([rng.integers(0, w.M, 128), [0, 127, 128, 255, 256, w.M - 1]]))
     a = oracle.bf16_to_f64(A[rows])

@@ -24,11 +24,12 @@ def _run(lib, A_bits, B_bits, off, out, **kw):
 @pytest.mark.parametrize("tile", TILES)
 @pytest.mark.parametrize("sched", ["static", "clc"])
 @pytest.mark.parametrize("out", [torch.float32, torch.bfloat16])
-def test_grouped_integer_bit_exact(lib, tile, sched, out):
+@pytest.mark.parametrize("ew", [4, 8])
+def test_grouped_integer_bit_exact(lib, tile, sched, out, ew):
     M, N = 300, 520
     A = synth.int_uniform_bf16(601, (M, 1024))
     B = synth.int_uniform_bf16(602, (N, 1024))
-    D = _run(lib, A, B, OFFSETS, out, sched=sched, tile=tile)
+    D = _run(lib, A, B, OFFSETS, out, sched=sched, tile=tile, epi_warps=ew)
     ref = oracle.grouped_gemm_f64(A, B, OFFSETS, blas=True)
     for g in range(len(OFFSETS) - 1):
         assert_bit_exact(D[g], ref[g], f"group {g} {tile} {sched}")

@@ -6,6 +6,8 @@ compiled variant and both schedulers; every planted protocol mistake must be
 caught; and the engine's mbarrier semantics are pinned on tiny hand-written
 programs.
 """
+import itertools
+
 import pytest
 
 from tile_scheduling_gb300 import protocol as pc
@@ -62,16 +64,16 @@ def test_engine_reports_over_arrival():
 
 # ------------------------------------------------------------ kernel protocol
 def test_exported_counts_match_the_role_structure(ts):
-    for tile in ("128x128", "128x256", "256x256"):
-        for out in (ts.TS_OUT_BF16, ts.TS_OUT_F32):
-            p = ts.ts_gemm_protocol_info(tile, out)
-            cg, e = p["cluster"], p["epilogue_warps"]
-            assert p["tx_bytes"] == p["stage_bytes"] * cg
-            assert p["tmem_empty_arrivals"] == e * cg
-            # producer, MMA, scheduler and epilogue warps of the even CTA; producer,
-            # scheduler and epilogue warps of the odd CTA
-            assert p["clc_empty_arrivals"] == (3 + e) + (2 + e if cg == 2 else 0)
-            assert p["full_arrivals"] == p["empty_arrivals"] == p["tmem_full_arrivals"] == 1
+    for tile, out, ew in itertools.product(("128x128", "128x256", "256x256"), (ts.TS_OUT_BF16, ts.TS_OUT_F32), (4, 8)):
+        p = ts.ts_gemm_protocol_info(tile, out, ew)
+        cg, e = p["cluster"], p["epilogue_warps"]
+        assert e == ew
+        assert p["tx_bytes"] == p["stage_bytes"] * cg
+        assert p["tmem_empty_arrivals"] == e * cg
+        # producer, MMA, scheduler and epilogue warps of the even CTA; producer,
+        # scheduler and epilogue warps of the odd CTA
+        assert p["clc_empty_arrivals"] == (3 + e) + (2 + e if cg == 2 else 0)
+        assert p["full_arrivals"] == p["empty_arrivals"] == p["tmem_full_arrivals"] == 1
 
 
 @pytest.mark.parametrize("tile", ["128x128", "128x256", "256x256"])
@@ -130,3 +132,28 @@ def test_fork_exports_its_arrivals(ts):
     assert ts.ts_gemm_protocol_info("128x256", 0)["aux_empty_arrivals"] == 1
     with pytest.raises(ValueError):
         pc.build_program(ts.ts_gemm_protocol_info("256x256", 0), [1], fork=True)
+
+
+def test_protocol_info_epilogue_warp_choices(ts):
+    assert ts.ts_gemm_protocol_info("128x256", 0)["epilogue_warps"] == 4  # 0 = the four-warp variant
+    with pytest.raises(ts.TsError):
+        ts.ts_gemm_protocol_info("128x256", 0, 6)
+
+
+# Eight epilogue warps: two per TMEM lane quarter, each releasing the
+# accumulator after its own subtiles.  Each warp still runs one read and one
+# release per unit, so the model is the same with twice the arrivals expected;
+# models of fewer warps count the rest as arrived.
+@pytest.mark.parametrize("tile,sched,warps,units", [("128x256", "clc", 2, [2, 1]), ("128x128", "static", 3, [1, 2]),
+                                                    ("256x256", "clc", 1, [1, 2]), ("256x256", "static", 2, [2, 1])])
+def test_eight_warp_protocol_verified(tile, sched, warps, units):
+    r = pc.check_variant(tile, units, sched, stages=2, variant_epi_warps=8, epilogue_warps=warps)
+    assert r.ok, r.message
+
+
+@pytest.mark.parametrize("mutation", ["epilogue_release_before_read", "tmem_empty_count_low"])
+def test_eight_warp_planted_mistakes_are_caught(mutation):
+    assert mutation in pc.MUTATIONS
+    r = pc.check_variant("256x256", [2, 1, 2], "clc", stages=2, variant_epi_warps=8, epilogue_warps=1,
+                         mutate=mutation)
+    assert not r.ok and r.status == 1, (mutation, r)

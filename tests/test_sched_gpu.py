@@ -31,11 +31,13 @@ def _traced(lib, A_bits, B_bits, out, tile, sched, **kw):
 
 @pytest.mark.parametrize("tile", ["128x128", "128x256", "256x256"])
 @pytest.mark.parametrize("max_workers", [0, 7, 1])
-def test_static_owner_follows_grid_stride_rule(lib, tile, max_workers):
+@pytest.mark.parametrize("ew", [4, 8])
+def test_static_owner_follows_grid_stride_rule(lib, tile, max_workers, ew):
     M, N, K = 1500, 1300, 128
     A = synth.int_uniform_bf16(301, (M, K))
     B = synth.int_uniform_bf16(302, (N, K))
-    info, tr, D = _traced(lib, A, B, torch.float32, tile, "static", max_workers=max_workers)
+    info, tr, D = _traced(lib, A, B, torch.float32, tile, "static", max_workers=max_workers, epi_warps=ew)
+    assert info["epi_warps"] == ew
     if max_workers:
         assert info["workers"] == min(max_workers, info["num_units"])
     assert np.all(tr[:, 0] == 1), "a work unit was not visited exactly once"
@@ -45,11 +47,12 @@ def test_static_owner_follows_grid_stride_rule(lib, tile, max_workers):
 
 
 @pytest.mark.parametrize("tile", ["128x128", "128x256", "256x256"])
-def test_clc_covers_every_tile_once(lib, tile):
+@pytest.mark.parametrize("ew", [4, 8])
+def test_clc_covers_every_tile_once(lib, tile, ew):
     M, N, K = 4000, 3000, 64  # many more tiles than resident workers
     A = synth.int_uniform_bf16(311, (M, K))
     B = synth.int_uniform_bf16(312, (N, K))
-    info, tr, D = _traced(lib, A, B, torch.bfloat16, tile, "clc")
+    info, tr, D = _traced(lib, A, B, torch.bfloat16, tile, "clc", epi_warps=ew)
     assert info["grid_ctas"] == info["num_units"] * info["cluster"]
     ok, why = oracle.clc_coverage_ok(tr[:, 0], tr[:, 1])
     assert ok, why

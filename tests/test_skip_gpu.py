@@ -27,7 +27,8 @@ def _causal(tiles_m, tiles_n, tm, tn):
 @pytest.mark.parametrize("tile", ["128x128", "128x256", "256x256"])
 @pytest.mark.parametrize("sched", ["static", "clc"])
 @pytest.mark.parametrize("out", [torch.float32, torch.bfloat16])
-def test_skipped_tiles_untouched_others_exact(lib, tile, sched, out):
+@pytest.mark.parametrize("ew", [4, 8])
+def test_skipped_tiles_untouched_others_exact(lib, tile, sched, out, ew):
     M, N, K = 1500, 1400, 320
     A = synth.int_uniform_bf16(701, (M, K))
     B = synth.int_uniform_bf16(702, (N, K))
@@ -38,7 +39,7 @@ def test_skipped_tiles_untouched_others_exact(lib, tile, sched, out):
     trace = torch.zeros(4 * info["num_units"], dtype=torch.int64, device="cuda")
     D = torch.full((M, N), SENTINEL, dtype=out, device="cuda")
     lib.ts_gemm_bf16_ex(to_device_bf16(A), to_device_bf16(B), D, sched=sched, tile=tile, workspace=None,
-                        trace=trace, skip_tiles=torch.from_numpy(mask.reshape(-1)).cuda())
+                        trace=trace, skip_tiles=torch.from_numpy(mask.reshape(-1)).cuda(), epi_warps=ew)
     lib.ts_sync_and_check()
     skipped = _mask_rows_cols(mask, info["tile_m"], info["tile_n"], M, N).astype(bool)
     ref = oracle.gemm_f64(A, B)

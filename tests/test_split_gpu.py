@@ -26,7 +26,8 @@ def _info(lib, M, N, K, out, sched, tile, ws):
 
 @pytest.mark.parametrize("tile,M,N,K", CASES)
 @pytest.mark.parametrize("sched", ["static", "clc"])
-def test_split_tail_integer_bit_exact_and_workspace_rearmed(lib, tile, M, N, K, sched):
+@pytest.mark.parametrize("ew", [4, 8])
+def test_split_tail_integer_bit_exact_and_workspace_rearmed(lib, tile, M, N, K, sched, ew):
     A = synth.int_uniform_bf16(801, (M, K))
     B = synth.int_uniform_bf16(802, (N, K))
     need = _info(lib, M, N, K, lib.TS_OUT_F32, sched, tile, None)["workspace_bytes"]
@@ -37,9 +38,10 @@ def test_split_tail_integer_bit_exact_and_workspace_rearmed(lib, tile, M, N, K, 
     assert info["num_units"] == info["num_tiles"] + info["split_tiles"] * (info["split_parts"] - 1)
     trace = torch.zeros(4 * info["num_units"], dtype=torch.int64, device="cuda")
     D = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
-    lib.ts_gemm_bf16_ex(to_device_bf16(A), to_device_bf16(B), D, sched=sched, tile=tile, workspace=ws, trace=trace)
+    lib.ts_gemm_bf16_ex(to_device_bf16(A), to_device_bf16(B), D, sched=sched, tile=tile, workspace=ws, trace=trace,
+                        epi_warps=ew)
     lib.ts_sync_and_check()
-    assert_bit_exact(D, oracle.gemm_f64_blas(A, B), f"split {tile} {sched}")
+    assert_bit_exact(D, oracle.gemm_f64_blas(A, B), f"split {tile} {sched} {ew} epilogue warps")
     tr = trace.view(-1, 4).cpu().numpy()
     if sched == "static":
         assert np.all(tr[:, 0] == 1)
@@ -53,7 +55,8 @@ def test_split_tail_integer_bit_exact_and_workspace_rearmed(lib, tile, M, N, K, 
 
 @pytest.mark.parametrize("tile,M,N,K", CASES)
 @pytest.mark.parametrize("out", [torch.float32, torch.bfloat16])
-def test_split_tail_random_within_bound_and_deterministic(lib, tile, M, N, K, out):
+@pytest.mark.parametrize("ew", [4, 8])
+def test_split_tail_random_within_bound_and_deterministic(lib, tile, M, N, K, out, ew):
     A = synth.uniform_pm1_bf16(811, (M, K))
     B = synth.uniform_pm1_bf16(812, (N, K))
     ref = oracle.gemm_f64_blas(A, B)
@@ -62,7 +65,7 @@ def test_split_tail_random_within_bound_and_deterministic(lib, tile, M, N, K, ou
     results = []
     for sched in ("clc", "static", "clc"):
         D = torch.full((M, N), float("nan"), dtype=out, device="cuda")
-        lib.ts_gemm_bf16_ex(Ad, Bd, D, sched=sched, tile=tile)  # cached workspace
+        lib.ts_gemm_bf16_ex(Ad, Bd, D, sched=sched, tile=tile, epi_warps=ew)  # cached workspace
         lib.ts_sync_and_check()
         assert_within_bound(as_f64(D), ref, S, out, f"split {tile} {sched} {out}")
         results.append(bf16_bits(D) if out == torch.bfloat16 else D.cpu().numpy())

@@ -1,4 +1,5 @@
-// GEMM variant: BN = 128, 1-CTA worker, bf16 output.
+// GEMM variant: BN = 128, 1-CTA worker, bf16 output; 4 and 8 epilogue warps.
 #include "gemm_launch.cuh"
 
-TS_GEMM_VARIANT(variant_128_1_bf16, 128, 1, OUT_BF16)
+TS_GEMM_VARIANT(variant_128_1_bf16_e4, 128, 1, OUT_BF16, 4)
+TS_GEMM_VARIANT(variant_128_1_bf16_e8, 128, 1, OUT_BF16, 8)

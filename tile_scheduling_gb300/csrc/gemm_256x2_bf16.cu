@@ -1,4 +1,5 @@
-// GEMM variant: BN = 256, 2-CTA worker, bf16 output.
+// GEMM variant: BN = 256, 2-CTA worker, bf16 output; 4 and 8 epilogue warps.
 #include "gemm_launch.cuh"
 
-TS_GEMM_VARIANT(variant_256_2_bf16, 256, 2, OUT_BF16)
+TS_GEMM_VARIANT(variant_256_2_bf16_e4, 256, 2, OUT_BF16, 4)
+TS_GEMM_VARIANT(variant_256_2_bf16_e8, 256, 2, OUT_BF16, 8)

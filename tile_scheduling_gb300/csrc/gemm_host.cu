@@ -12,14 +12,17 @@
 
 namespace ts {
 
-extern const GemmVariant variant_128_1_bf16, variant_128_1_f32, variant_256_1_bf16, variant_256_1_f32,
-    variant_256_2_bf16, variant_256_2_f32;
+extern const GemmVariant variant_128_1_bf16_e4, variant_128_1_f32_e4, variant_256_1_bf16_e4, variant_256_1_f32_e4,
+    variant_256_2_bf16_e4, variant_256_2_f32_e4, variant_128_1_bf16_e8, variant_128_1_f32_e8, variant_256_1_bf16_e8,
+    variant_256_1_f32_e8, variant_256_2_bf16_e8, variant_256_2_f32_e8;
 
-const GemmVariant *find_variant(int bn, int cg, int out) {
-    static const GemmVariant *const all[] = {&variant_128_1_bf16, &variant_128_1_f32, &variant_256_1_bf16,
-                                             &variant_256_1_f32,  &variant_256_2_bf16, &variant_256_2_f32};
+const GemmVariant *find_variant(int bn, int cg, int out, int epi_warps) {
+    static const GemmVariant *const all[] = {
+        &variant_128_1_bf16_e4, &variant_128_1_f32_e4, &variant_256_1_bf16_e4, &variant_256_1_f32_e4,
+        &variant_256_2_bf16_e4, &variant_256_2_f32_e4, &variant_128_1_bf16_e8, &variant_128_1_f32_e8,
+        &variant_256_1_bf16_e8, &variant_256_1_f32_e8, &variant_256_2_bf16_e8, &variant_256_2_f32_e8};
     for (const GemmVariant *v : all)
-        if (v->bn == bn && v->cg == cg && v->out == out) return v;
+        if (v->bn == bn && v->cg == cg && v->out == out && v->epi_warps == epi_warps) return v;
     return nullptr;
 }
 
@@ -135,6 +138,7 @@ constexpr int64_t kMinKBlocksPerPart = 4;
 // so a workspace reused across problem shapes never has partial data where a
 // later shape keeps its counters (which every launch leaves at zero).
 constexpr int64_t kCounterRegionBytes = 8192;
+constexpr int64_t kShortK = 512;  // K at or below which the automatic choice is eight epilogue warps
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -163,6 +167,8 @@ ts_status plan_gemm(const void *D, int64_t M, int64_t N, int64_t K, int32_t out,
     if (o->tile < TS_TILE_AUTO || o->tile > TS_TILE_256x256_2CTA) return fail(TS_ERR_INVALID_ARG, "tile %d", o->tile);
     if (o->max_workers < 0 || o->raster_group < 0 || o->timeout_s < 0)
         return fail(TS_ERR_INVALID_ARG, "negative option");
+    if (o->epi_warps != 0 && o->epi_warps != 4 && o->epi_warps != 8)
+        return fail(TS_ERR_INVALID_ARG, "epi_warps = %d (0, 4 or 8)", o->epi_warps);
     pl->lda = o->lda ? o->lda : K;
     pl->ldb = o->ldb ? o->ldb : K;
     pl->ldd = o->ldd ? o->ldd : N;
@@ -193,7 +199,12 @@ ts_status plan_gemm(const void *D, int64_t M, int64_t N, int64_t K, int32_t out,
     int bn = 256, cg = 1;
     if (tile == TS_TILE_128x128) bn = 128;
     if (tile == TS_TILE_256x256_2CTA) cg = 2;
-    pl->v = find_variant(bn, cg, out);
+    // Epilogue warps: with a short K loop the epilogue bounds every tile and
+    // eight warps hide more of its latencies; with a long one the epilogue
+    // hides under the mainloop and four leave the SM's issue slots to it.
+    int epi_warps = o->epi_warps;
+    if (epi_warps == 0) epi_warps = groups == 0 && K <= kShortK ? 8 : 4;
+    pl->v = find_variant(bn, cg, out, epi_warps);
     if (!pl->v) return fail(TS_ERR_UNSUPPORTED, "no compiled variant for tile %d", tile);
     pl->cg = cg;
     pl->tile_m = 128 * cg;
@@ -222,7 +233,7 @@ ts_status plan_gemm(const void *D, int64_t M, int64_t N, int64_t K, int32_t out,
         const int64_t r = pl->num_tiles % W;
         const int64_t s =
             r > 0 ? std::min<int64_t>(std::min<int64_t>(W / r, nk / kMinKBlocksPerPart), kMaxParts) : 0;
-        const int64_t counters = r * cg * 4 * static_cast<int64_t>(sizeof(int32_t));
+        const int64_t counters = r * cg * 8 * static_cast<int64_t>(sizeof(int32_t));
         if (r > 0 && s >= 2 && counters <= kCounterRegionBytes) {
             pl->counter_bytes = kCounterRegionBytes;
             pl->split_ws_bytes = pl->counter_bytes + r * s * cg * 4 * 32 * static_cast<int64_t>(bn) * 4;
@@ -276,6 +287,7 @@ ts_status fill_info(int64_t M, int64_t N, int64_t K, int32_t out_dtype, int32_t 
     info->split_parts = static_cast<int32_t>(pl.parts);
     info->resident = static_cast<int32_t>(pl.resident);
     info->workspace_bytes = pl.split_ws_bytes;
+    info->epi_warps = pl.v->epi_warps;
     return TS_OK;
 }
 }  // namespace ts
@@ -335,9 +347,11 @@ ts_status ts_gemm_tile_coords(int64_t M, int64_t N, int64_t K, int32_t out_dtype
     return TS_OK;
 }
 
-ts_status ts_gemm_protocol_info(int32_t tile, int32_t out_dtype, ts_gemm_protocol *proto) {
+ts_status ts_gemm_protocol_info(int32_t tile, int32_t out_dtype, int32_t epi_warps, ts_gemm_protocol *proto) {
     if (!proto) return ts::fail(TS_ERR_INVALID_ARG, "proto is NULL");
     if (out_dtype != TS_OUT_BF16 && out_dtype != TS_OUT_F32) return ts::fail(TS_ERR_INVALID_ARG, "out_dtype %d", out_dtype);
+    if (epi_warps == 0) epi_warps = 4;
+    if (epi_warps != 4 && epi_warps != 8) return ts::fail(TS_ERR_INVALID_ARG, "epi_warps = %d (0, 4 or 8)", epi_warps);
     int bn, cg;
     switch (tile) {
         case TS_TILE_128x128: bn = 128, cg = 1; break;
@@ -345,7 +359,7 @@ ts_status ts_gemm_protocol_info(int32_t tile, int32_t out_dtype, ts_gemm_protoco
         case TS_TILE_256x256_2CTA: bn = 256, cg = 2; break;
         default: return ts::fail(TS_ERR_INVALID_ARG, "tile %d (an explicit tile is required)", tile);
     }
-    const ts::GemmVariant *v = ts::find_variant(bn, cg, out_dtype);
+    const ts::GemmVariant *v = ts::find_variant(bn, cg, out_dtype, epi_warps);
     if (!v) return ts::fail(TS_ERR_UNSUPPORTED, "no compiled variant for tile %d", tile);
     *proto = v->protocol;
     return TS_OK;

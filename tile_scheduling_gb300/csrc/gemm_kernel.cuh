@@ -6,7 +6,7 @@
 // 2 * S barriers: one producer thread arrives with the summed transaction
 // bytes of both loads, the single MMA consumer waits and releases once).
 //
-// Warp roles (256 threads, one CTA per SM):
+// Warp roles (256 or 384 threads, one CTA per SM):
 //   warp 0      TMA producer: per k-block, acquire an empty stage, arm the
 //               full barrier with A+B bytes, issue the two tile loads
 //               (TS "Introduction", Load-A skeleton: compute_coords, acquire,
@@ -19,12 +19,14 @@
 //               next tile while the current one is computed ("Cluster Launch
 //               Control", overlap loop; TS "Schedules", dynamic persistent
 //               shape with a dedicated scheduler task).
-//   warp 3      barrier initialisation, then idle.
-//   warps 4-7   epilogue: TMEM -> registers (tcgen05.ld, 32 columns per load)
-//               -> fp32 or bf16 -> swizzled shared staging -> TMA store, one
-//               subtile after another (TS "Resources", subtile epilogue:
-//               load_subtile / store at column coordc_n + subtile_idx * 32,
-//               bracketed by tmem_c.wait() / release()).
+//   warp 3      barrier initialisation, then idle (or the Fork row-sum task).
+//   warps 4..   epilogue, 4 or 8 warps: TMEM -> registers (tcgen05.ld, 32
+//               columns per load) -> fp32 or bf16 -> swizzled shared staging ->
+//               TMA store, one subtile after another (TS "Resources", subtile
+//               epilogue: load_subtile / store at column coordc_n +
+//               subtile_idx * 32, bracketed by tmem_c.wait() / release()).
+//               With 8, two warps share each TMEM lane quarter and alternate
+//               subtiles.
 //
 // Every role walks the same tile sequence and advances at the same tile
 // boundary (TS "Schedules", Persistent Scheduling).  Static mode: worker w of
@@ -51,13 +53,18 @@
 
 namespace ts {
 
-constexpr int kThreads = 256;
+constexpr int kRoleWarps = 4;       // producer, MMA issuer, CLC scheduler, Fork row-sum task
 constexpr int kSmemLimit = 232448;  // 227 KB: largest opt-in dynamic shared memory per CTA
 constexpr int kMaxClcDepth = 2;
 
-template <int BN_, int CG_, int OUT_>
+// EW_ epilogue warps: 4 (one per TMEM lane quarter) or 8 (two per quarter,
+// splitting the columns).  Eight hide more of the epilogue's instruction
+// latencies when the K loop is short and the epilogue bounds the tile.
+template <int BN_, int CG_, int OUT_, int EW_>
 struct GemmCfg {
     static constexpr int BN = BN_, CG = CG_, OUT = OUT_;
+    static constexpr int EPI_WARPS = EW_;
+    static constexpr int THREADS = 32 * (kRoleWarps + EPI_WARPS);
     static constexpr int BM = 128;              // accumulator rows per CTA = TMEM lanes
     static constexpr int TILE_M = BM * CG;      // output rows per worker
     static constexpr int BK = 64;               // bf16 per 128-byte swizzle row
@@ -71,14 +78,16 @@ struct GemmCfg {
     static constexpr int SUB_COLS = 128 / OUT_BYTES;   // store subtile: 128 bytes of a row
     static constexpr int NUM_SUB = BN / SUB_COLS;
     static constexpr int EPI_BUF = 32 * 128;           // one warp: 32 rows x 128 bytes
-    static constexpr int EPI_BYTES = 4 * 2 * EPI_BUF;  // 4 warps, double-buffered
+    // staging buffers per epilogue warp: 32 KB in all either way, so the ring
+    // keeps its depth (with eight warps the two warps of a quarter alternate)
+    static constexpr int EPI_BUFS = EPI_WARPS == 4 ? 2 : 1;
+    static constexpr int EPI_BYTES = EPI_WARPS * EPI_BUFS * EPI_BUF;
     static constexpr int TMEM_COLS = 2 * BN;           // two accumulators
     static constexpr int BAR_BYTES = 256;
     static constexpr int STAGES = (kSmemLimit - 1024 - EPI_BYTES - BAR_BYTES) / STAGE_BYTES;
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
     // Barrier arrival counts (one place: the kernel initialises its barriers
     // with these, and the host-side protocol checker models them).
-    static constexpr int EPI_WARPS = 4;
     static constexpr int FULL_ARRIVALS = 1;   // the even CTA's producer (arrive.expect_tx)
     static constexpr int EMPTY_ARRIVALS = 1;  // one tcgen05.commit per stage use
     static constexpr int TFULL_ARRIVALS = 1;  // one tcgen05.commit per accumulator use
@@ -98,6 +107,8 @@ struct GemmCfg {
 
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N");
     static_assert(CG == 1 || CG == 2, "cluster size");
+    static_assert(EPI_WARPS == 4 || EPI_WARPS == 8, "epilogue warps");
+    static_assert(NUM_SUB % (EPI_WARPS / 4) == 0, "subtiles split evenly between a quarter's warps");
     static_assert(STAGES >= 2, "ring too shallow");
     static_assert(SMEM_BYTES <= kSmemLimit, "shared memory budget");
     static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzle atoms must stay 1024-byte aligned");
@@ -279,11 +290,11 @@ __device__ __forceinline__ int32_t next_unit(const Smem<C> &sm, const GemmParams
     return clc_consume(sm, p, clc_idx);
 }
 
-template <int BN, int CG, int OUT>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int BN, int CG, int OUT, int EW>
+__global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
     gemm_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmD, const __grid_constant__ GemmParams p) {
-    using C = GemmCfg<BN, CG, OUT>;
+    using C = GemmCfg<BN, CG, OUT, EW>;
     constexpr int RAW = C::SUB_COLS;  // fp32 accumulator words per lane per store subtile
     extern __shared__ __align__(1024) uint8_t smem_raw[];
 
@@ -579,9 +590,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp >= 4) {
         // --------------------------------------------------------- epilogue
-        static_assert(C::EPI_WARPS == 4 && kThreads == 256, "warps 4-7 are the epilogue warpgroup");
-        const int q = warp - 4;  // TMEM lane quarter this warp may access
-        const uint32_t stg = sm.epi + static_cast<uint32_t>(q) * 2u * C::EPI_BUF;
+        // Warps 4 .. 4 + EW - 1.  A warp may access TMEM lanes 32 * (warp % 4) onwards:
+        // warp 4 + j takes lane quarter q = j % 4 and, with eight warps, the
+        // subtiles s = h, h + 2, ... (h = j / 4) of that quarter's rows.
+        constexpr int HALVES = C::EPI_WARPS / 4;
+        const int q = (warp - kRoleWarps) & 3;
+        const int h = (warp - kRoleWarps) >> 2;
+        const uint32_t stg = sm.epi + static_cast<uint32_t>(warp - kRoleWarps) * C::EPI_BUFS * C::EPI_BUF;
         int32_t unit = first_unit;
         uint32_t clc_idx = 0, acc = 0, acc_phase = 0, buf = 0;
 
@@ -601,7 +616,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j = 0; j < 32; ++j) w[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
             }
             if (p.tma_store && col + C::SUB_COLS <= p.N) {
-                if (lane == 0) bulk_wait_read<1>();  // the store that used this buffer has read it
+                if (lane == 0) bulk_wait_read<C::EPI_BUFS - 1>();  // the store that used this buffer has read it
                 __syncwarp();
                 const uint32_t row_addr = stg + buf * C::EPI_BUF + static_cast<uint32_t>(lane) * 128u;
 #pragma unroll
@@ -614,7 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_store_3d(&tmD, stg + buf * C::EPI_BUF, col, row0, group);
                     bulk_commit();
                 }
-                buf ^= 1u;
+                buf = buf + 1u == C::EPI_BUFS ? 0u : buf + 1u;
             } else {
                 const int32_t row = row0 + lane;
                 if (row < p.M) {
@@ -657,7 +672,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + acc * BN;
             float4 *const mine = split ? slab_of(w, w.part) : nullptr;
 #pragma unroll 1
-            for (int s = 0; s < C::NUM_SUB; ++s) {
+            for (int s = h; s < C::NUM_SUB; s += HALVES) {
                 uint32_t v[RAW];
                 if constexpr (RAW == 32) {
                     tmem_ld_32x32b_x32(taddr + s * 32, v);
@@ -673,8 +688,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int j = 0; j < RAW; ++j) v[j] = 0u;
                 }
-                if (s == C::NUM_SUB - 1) {
-                    // accumulator fully read: hand it back to the MMA issuer
+                if (s + HALVES >= C::NUM_SUB) {
+                    // this warp's part of the accumulator is read: hand it back to the MMA issuer
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) {
@@ -695,13 +710,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (split) {
-                // The last of the `parts` warps to finish this slab sums the
-                // partials in part order and stores D; it also re-arms the counter.
+                // The last of the `parts` warps to finish this slab (its subtiles of
+                // it, with eight warps) sums the partials in part order and stores
+                // D; it also re-arms the counter.
                 __threadfence();
                 __syncwarp();
                 int last = 0;
                 if (lane == 0) {
-                    int32_t *cnt = p.counters + (w.tail * CG + static_cast<int32_t>(rank)) * 4 + q;
+                    int32_t *cnt =
+                        p.counters + ((w.tail * CG + static_cast<int32_t>(rank)) * 4 + q) * HALVES + h;
                     last = atomicAdd(cnt, 1) == p.parts - 1;
                     if (last) atomicExch(cnt, 0);
                 }
@@ -709,23 +726,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (last) {
                     __threadfence();
 #pragma unroll 1
-                    for (int s = 0; s < C::NUM_SUB; ++s) {
+                    for (int s = h; s < C::NUM_SUB; s += HALVES) {
                         uint32_t v[RAW];
-                        // 32 columns at a time: every part's 8 float4 per lane are in
-                        // flight together, then summed in part order 0, 1, ...
+                        // F4 float4 (4 * F4 columns) at a time: every part's F4 float4
+                        // per lane are in flight together, then summed in part order
+                        // 0, 1, ...  Eight epilogue warps leave half the registers.
+                        constexpr int F4 = C::EPI_WARPS == 4 ? 8 : 4;
 #pragma unroll
-                        for (int ch = 0; ch < RAW / 32; ++ch) {
-                            float4 x[kMaxParts][8];
+                        for (int ch = 0; ch < RAW / (4 * F4); ++ch) {
+                            float4 x[kMaxParts][F4];
 #pragma unroll
                             for (int pp = 0; pp < kMaxParts; ++pp) {
                                 if (pp < p.parts) {
-                                    const float4 *src = slab_of(w, pp) + (s * (RAW / 4) + ch * 8) * 32 + lane;
+                                    const float4 *src = slab_of(w, pp) + (s * (RAW / 4) + ch * F4) * 32 + lane;
 #pragma unroll
-                                    for (int c = 0; c < 8; ++c) x[pp][c] = __ldcg(src + c * 32);
+                                    for (int c = 0; c < F4; ++c) x[pp][c] = __ldcg(src + c * 32);
                                 }
                             }
 #pragma unroll
-                            for (int c = 0; c < 8; ++c) {
+                            for (int c = 0; c < F4; ++c) {
                                 float4 a = x[0][c];
 #pragma unroll
                                 for (int pp = 1; pp < kMaxParts; ++pp) {
@@ -736,10 +755,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         a.w += x[pp][c].w;
                                     }
                                 }
-                                v[ch * 32 + 4 * c] = __float_as_uint(a.x);
-                                v[ch * 32 + 4 * c + 1] = __float_as_uint(a.y);
-                                v[ch * 32 + 4 * c + 2] = __float_as_uint(a.z);
-                                v[ch * 32 + 4 * c + 3] = __float_as_uint(a.w);
+                                v[ch * 4 * F4 + 4 * c] = __float_as_uint(a.x);
+                                v[ch * 4 * F4 + 4 * c + 1] = __float_as_uint(a.y);
+                                v[ch * 4 * F4 + 4 * c + 2] = __float_as_uint(a.z);
+                                v[ch * 4 * F4 + 4 * c + 3] = __float_as_uint(a.w);
                             }
                         }
                         emit(v, row0, col0 + s * C::SUB_COLS, w.group);
@@ -751,7 +770,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 acc_phase ^= 1u;
             }
             }  // !w.skip
-            if (p.trace && rank == 0 && q == 0 && lane == 0) {
+            if (p.trace && rank == 0 && q == 0 && h == 0 && lane == 0) {
                 atomicAdd(reinterpret_cast<unsigned long long *>(&p.trace[4 * unit]), 1ull);
                 p.trace[4 * unit + 1] = worker;
                 p.trace[4 * unit + 3] = static_cast<long long>(globaltimer());

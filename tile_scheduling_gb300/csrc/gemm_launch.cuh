@@ -9,9 +9,9 @@
 
 namespace ts {
 
-template <int BN, int CG, int OUT>
+template <int BN, int CG, int OUT, int EW>
 struct GemmInstance {
-    using C = GemmCfg<BN, CG, OUT>;
+    using C = GemmCfg<BN, CG, OUT, EW>;
 
     // cudaFuncSetAttribute once per device (bit per device ordinal).
     static cudaError_t prepare() {
@@ -19,7 +19,7 @@ struct GemmInstance {
         const int dev = current_device();
         const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
         if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
-        cudaError_t e = cudaFuncSetAttribute(gemm_ws_kernel<BN, CG, OUT>,
+        cudaError_t e = cudaFuncSetAttribute(gemm_ws_kernel<BN, CG, OUT, EW>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
         if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
         return e;
@@ -48,7 +48,7 @@ struct GemmInstance {
         if (e != cudaSuccess) return e;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(static_cast<unsigned>(L.grid), 1, 1);
-        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.blockDim = dim3(C::THREADS, 1, 1);
         cfg.dynamicSmemBytes = C::SMEM_BYTES;
         cfg.stream = L.stream;
         cudaLaunchAttribute attr[1];
@@ -60,7 +60,7 @@ struct GemmInstance {
             cfg.attrs = attr;
             cfg.numAttrs = 1;
         }
-        return cudaLaunchKernelEx(&cfg, gemm_ws_kernel<BN, CG, OUT>, L.a, L.b, L.d, L.p);
+        return cudaLaunchKernelEx(&cfg, gemm_ws_kernel<BN, CG, OUT, EW>, L.a, L.b, L.d, L.p);
     }
 
     static cudaError_t max_workers(int *out) {
@@ -68,7 +68,7 @@ struct GemmInstance {
         if (e != cudaSuccess) return e;
         if (CG == 1) {
             int per_sm = 0;
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemm_ws_kernel<BN, CG, OUT>, kThreads,
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemm_ws_kernel<BN, CG, OUT, EW>, C::THREADS,
                                                               C::SMEM_BYTES);
             if (e != cudaSuccess) return e;
             *out = per_sm * device_sms(current_device());
@@ -76,7 +76,7 @@ struct GemmInstance {
         }
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(2 * 1024, 1, 1);
-        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.blockDim = dim3(C::THREADS, 1, 1);
         cfg.dynamicSmemBytes = C::SMEM_BYTES;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -86,7 +86,7 @@ struct GemmInstance {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int clusters = 0;
-        e = cudaOccupancyMaxActiveClusters(&clusters, reinterpret_cast<const void *>(gemm_ws_kernel<BN, CG, OUT>),
+        e = cudaOccupancyMaxActiveClusters(&clusters, reinterpret_cast<const void *>(gemm_ws_kernel<BN, CG, OUT, EW>),
                                            &cfg);
         if (e != cudaSuccess) return e;
         *out = clusters;
@@ -96,15 +96,16 @@ struct GemmInstance {
 
 }  // namespace ts
 
-#define TS_GEMM_VARIANT(NAME, BN, CG, OUT)                                                                 \
+#define TS_GEMM_VARIANT(NAME, BN, CG, OUT, EW)                                                             \
     namespace ts {                                                                                         \
     extern const GemmVariant NAME;                                                                         \
     const GemmVariant NAME = {BN,                                                                          \
                               CG,                                                                          \
                               OUT,                                                                         \
-                              GemmCfg<BN, CG, OUT>::STAGES,                                                \
-                              GemmCfg<BN, CG, OUT>::SMEM_BYTES,                                            \
-                              GemmInstance<BN, CG, OUT>::protocol(),                                       \
-                              &GemmInstance<BN, CG, OUT>::launch,                                          \
-                              &GemmInstance<BN, CG, OUT>::max_workers};                                    \
+                              EW,                                                                          \
+                              GemmCfg<BN, CG, OUT, EW>::STAGES,                                            \
+                              GemmCfg<BN, CG, OUT, EW>::SMEM_BYTES,                                        \
+                              GemmInstance<BN, CG, OUT, EW>::protocol(),                                   \
+                              &GemmInstance<BN, CG, OUT, EW>::launch,                                      \
+                              &GemmInstance<BN, CG, OUT, EW>::max_workers};                                \
     }

@@ -70,7 +70,7 @@ struct GemmParams {
     uint64_t drain_ns;     // limit for waiting on copies still in flight at exit
     unsigned long long *status;
     long long *trace;      // 4 int64 per work unit, or nullptr
-    int32_t *counters;     // split_tiles * CG * 4 slab counters (zero between launches)
+    int32_t *counters;     // split_tiles * CG * 8 slab counters (zero between launches)
     float *partials;       // split_tiles * parts * CG * 4 slabs of 32 x BN fp32
     // Grouped GEMM (groups > 0): unit u is tile u % tiles_per_group of group
     // u / tiles_per_group, whose k-blocks are [group_kb[g], group_kb[g + 1]).

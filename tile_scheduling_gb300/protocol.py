@@ -230,8 +230,9 @@ def check(P: Program, max_states: int = 20_000_000) -> Result:
 
 
 def check_variant(tile: str, units: list, sched: str = "static", out: int = 0, max_states: int = 20_000_000,
-                  **kw) -> Result:
-    """Check the protocol of a compiled kernel variant on a unit sequence."""
+                  variant_epi_warps: int = 4, **kw) -> Result:
+    """Check the protocol of a compiled kernel variant (tile, output type and
+    epilogue warp count) on a unit sequence."""
     from . import ts_gemm_protocol_info
 
-    return check(build_program(ts_gemm_protocol_info(tile, out), units, sched, **kw), max_states)
+    return check(build_program(ts_gemm_protocol_info(tile, out, variant_epi_warps), units, sched, **kw), max_states)
