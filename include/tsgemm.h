@@ -28,7 +28,7 @@ extern "C" {
 typedef enum {
     TS_OK = 0,
     TS_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad enum, overlapping copy */
-    TS_ERR_UNSUPPORTED = 2, /* legal request this build cannot run (TMA alignment, size limits) */
+    TS_ERR_UNSUPPORTED = 2, /* legal request the library cannot run (TMA alignment, size limits) */
     TS_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed; detail has the CUDA message */
     TS_ERR_TIMEOUT = 4      /* a kernel gave up on a barrier wait (reported by ts_sync_and_check) */
 } ts_status;
