@@ -8,6 +8,11 @@
 #include "gemm_kernel.cuh"
 
 namespace ts {
+// Internal linkage: each variant translation unit has its own instance, and
+// the per-device "prepared" flag below is not merged with a same-named one in
+// another copy of this library loaded into the process (function-local
+// statics of templates otherwise become process-unique symbols).
+namespace {
 
 template <int BN, int CG, int OUT, int EW>
 struct GemmInstance {
@@ -94,6 +99,7 @@ struct GemmInstance {
     }
 };
 
+}  // namespace
 }  // namespace ts
 
 #define TS_GEMM_VARIANT(NAME, BN, CG, OUT, EW)                                                             \
