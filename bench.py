@@ -259,7 +259,9 @@ def run_ours(args, ws, rank, local):
                    "sched": args.sched, "tiles": info["num_tiles"], "grid_ctas": info["grid_ctas"],
                    "stages": info["stages"], "epi_warps": info["epi_warps"], "copy_n": n_copy,
                    "l2": "inputs larger than L2 (256 MiB GEMM operands, 1 GiB copy traffic); no flush",
-                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+                   "seeds": {"A": hex(w.seed_a), "B": hex(w.seed_b), "copy": hex(synth.COPY_SEED)},
+                   "gpu": torch.cuda.get_device_name(local), "sms": torch.cuda.get_device_properties(local).multi_processor_count},
         "gemm": {"tflops": round(gemm_tflops, 2), "ms_median": round(statistics.median(gemm_ms), 4),
                  "ms_min": round(min(gemm_ms), 4)},
         "copy": {"gbs": round(copy_gbs, 1), "ms_median": round(statistics.median(copy_ms), 4),
