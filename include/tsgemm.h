@@ -289,6 +289,16 @@ typedef struct {
     double timeout_s;           /* limit on one wait for a CLC response; 0 = 1 s */
     int64_t *trace;             /* device int64 [2 * tiles] zeroed by the caller, or NULL: per tile t,
                                    [2t] += 1 per visit, [2t+1] = blockIdx.x of the CTA that ran it */
+    int64_t chunk;              /* 0: work tile t is row t (the Dynamic Domain form below).  > 0: each row
+                                   is cut into pieces of at most `chunk` elements and every piece is a work
+                                   tile, in row order, so a long row no longer runs on one CTA at the end
+                                   of the queue.  A planning kernel (one CTA, same stream) reads the
+                                   offsets first.  tiles defaults to, and may not be below,
+                                   rows + ceil(n / chunk); tiles past the last piece are skipped. */
+    void *workspace;            /* chunk > 0: device scratch of ts_launch_info.workspace_bytes bytes,
+                                   256-byte aligned, no initialisation; launches that may overlap on the
+                                   GPU need separate workspaces */
+    int64_t workspace_bytes;
 } ts_rows_opts;
 
 /*
@@ -320,13 +330,17 @@ typedef struct {
  *             returns TS_ERR_INVALID_ARG naming the first such row.
  *   rows      row count (upper bound when rows_device is given), >= 0.
  * A CLC response that does not arrive within timeout_s is reported as
- * TS_ERR_TIMEOUT by ts_sync_and_check; the CTA then stops taking tiles.
+ * TS_ERR_TIMEOUT by ts_sync_and_check; the CTA then stops taking tiles.  In
+ * chunked mode, rows that overlap can need more pieces than `tiles`: the rows
+ * whose pieces do not fit are reported as TS_ERR_INVALID_ARG by
+ * ts_sync_and_check (the pieces that fit are copied).
  */
 ts_status ts_copy_i16_rows(const int16_t *src, int16_t *dst, int64_t n, const int64_t *offsets, int64_t rows,
                            int32_t sched, const ts_rows_opts *opts, void *stream);
 
 /* The launch ts_copy_i16_rows would make (host only): num_tiles = num_units =
- * tiles, grid_ctas = workers = CTAs launched, resident = CTAs that fit at once. */
+ * tiles, grid_ctas = workers = CTAs launched, resident = CTAs that fit at once,
+ * workspace_bytes = the workspace chunked mode needs (0 otherwise). */
 ts_status ts_copy_rows_launch_info(int64_t n, int64_t rows, int32_t sched, const ts_rows_opts *opts,
                                    ts_launch_info *info);
 

@@ -82,5 +82,9 @@ def test_row_copy_argument_errors_need_no_gpu(ts):
     assert ts.ts_copy_i16_rows_ptr(4096, 4100, 8, 64, 1, stream=0) == E  # overlap
     assert ts.ts_copy_i16_rows_ptr(4097, 8192, 8, 64, 1, stream=0) == E  # odd address
     assert ts.ts_copy_i16_rows_ptr(4096, 8192, 8, 64, 1, timeout_s=-1.0, stream=0) == E
+    assert ts.ts_copy_i16_rows_ptr(4096, 8192, 8, 64, 1, chunk=-1, stream=0) == E
+    # chunked: tiles may not be below rows + ceil(n / chunk) = 2 + 3
+    assert ts.ts_copy_i16_rows_ptr(4096, 8192, 9, 64, 2, chunk=4, tiles=4, stream=0) == E
+    assert "ceil(n / chunk)" in ts.ts_last_error_detail()
     # an empty queue launches nothing
     assert ts.ts_copy_i16_rows_ptr(0, 0, 0, 0, 0, stream=0) == ts.TS_OK

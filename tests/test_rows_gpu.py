@@ -172,3 +172,123 @@ def test_rows_full_workload_bit_exact(lib, sched):
     idx = np.random.default_rng(1).integers(0, n, 1 << 16)
     assert bad == -1 and np.array_equal(dst[torch.as_tensor(idx, device="cuda")].cpu().numpy(), want[idx])
     assert torch.equal(trace.view(-1, 2)[:, 0].cpu(), torch.ones(synth.ROWS.rows, dtype=torch.int64))
+
+
+# ------------------------------------------------------------ chunked mode
+# Rows cut into work tiles of at most `chunk` elements (a planning kernel maps
+# tiles to rows); the result is the same row copy.
+
+
+@pytest.mark.parametrize("sched", ["static", "clc"])
+@pytest.mark.parametrize("chunk", [1, 7, 16, 100, 4096, 1 << 20])
+def test_rows_chunked_random_jagged(lib, sched, chunk):
+    offsets, n = _jagged(91 + chunk, 200 if chunk > 1 else 40, 3000 if chunk > 1 else 300)
+    src = synth.int16_uniform(92, n)
+    dst0 = synth.int16_uniform(93, n)
+    got = _run(lib, src, dst0, offsets, sched, chunk=chunk)
+    want, bad = oracle.copy_rows_i16(src, dst0, offsets)
+    assert bad == -1 and np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("sched", ["static", "clc"])
+@pytest.mark.parametrize("src_off,dst_off", [(0, 0), (8, 0), (3, 3), (1, 6)])
+def test_rows_chunked_vector_paths(lib, sched, src_off, dst_off):
+    offsets, n = _jagged(95, 120, 5000, lead=3, trail=9)
+    src = synth.int16_uniform(96, n)
+    dst0 = synth.int16_uniform(97, n)
+    got = _run(lib, src, dst0, offsets, sched, src_off=src_off, dst_off=dst_off, chunk=33)
+    want, _ = oracle.copy_rows_i16(src, dst0, offsets)
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("sched", ["static", "clc"])
+def test_rows_chunked_tiles_visited_once_and_extra_tiles_skipped(lib, sched):
+    offsets, n = _jagged(101, 150, 2000)
+    rows = offsets.size - 1
+    chunk = 250
+    info = lib.ts_copy_rows_launch_info(n, rows, sched, chunk=chunk)
+    tiles = info["num_tiles"]
+    assert tiles == rows + -(-n // chunk) and info["workspace_bytes"] > 0
+    pieces = int(sum(-(-(int(offsets[r + 1]) - int(offsets[r])) // chunk) for r in range(rows)))
+    assert pieces < tiles  # some tiles are past the last piece
+    src = synth.int16_uniform(102, n)
+    dst0 = synth.int16_uniform(103, n)
+    trace = torch.zeros(2 * tiles, dtype=torch.int64, device="cuda")
+    got = _run(lib, src, dst0, offsets, sched, chunk=chunk, trace=trace)
+    want, _ = oracle.copy_rows_i16(src, dst0, offsets)
+    assert np.array_equal(got, want)
+    tr = trace.view(tiles, 2).cpu().numpy()
+    if sched == "static":
+        assert np.array_equal(tr[:, 0], np.ones(tiles))
+        assert np.array_equal(tr[:, 1], oracle.static_owner(tiles, info["grid_ctas"]))
+    else:
+        ok, why = oracle.clc_coverage_ok(tr[:, 0], tr[:, 1])
+        assert ok, why
+
+
+@pytest.mark.parametrize("sched", ["static", "clc"])
+@pytest.mark.parametrize("count", [0, 1, 77, 200])
+def test_rows_chunked_skip_mask_and_device_count(lib, sched, count):
+    offsets, n = _jagged(111, 200, 1500)
+    src = synth.int16_uniform(112, n)
+    dst0 = synth.int16_uniform(113, n)
+    skip = (synth.splitmix64(114, 200) % np.uint64(4) == 0).astype(np.uint8)
+    rd = torch.tensor([count], dtype=torch.int64, device="cuda")
+    got = _run(lib, src, dst0, offsets, sched, chunk=64, rows_device=rd, skip_rows=torch.from_numpy(skip).cuda())
+    want, _ = oracle.copy_rows_i16(src, dst0, offsets, rows=count, skip=skip)
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("sched", ["static", "clc"])
+def test_rows_chunked_bad_bounds_reported(lib, sched):
+    n = 1000
+    offsets = np.array([0, 100, 300, 600, 1200], dtype=np.int64)  # row 3 runs past n
+    src = synth.int16_uniform(121, n)
+    dst0 = synth.int16_uniform(122, n)
+    sbuf = torch.from_numpy(src).cuda()
+    dbuf = torch.from_numpy(dst0.copy()).cuda()
+    lib.ts_copy_i16_rows(sbuf, dbuf, torch.from_numpy(offsets).cuda(), sched=sched, chunk=64)
+    with pytest.raises(lib.TsError) as ei:
+        lib.ts_sync_and_check()
+    assert ei.value.status == lib.TS_ERR_INVALID_ARG and "bounds" in ei.value.detail
+    want, first_bad = oracle.copy_rows_i16(src, dst0, offsets)
+    assert first_bad == 3 and np.array_equal(dbuf.cpu().numpy(), want)
+
+
+def test_rows_chunked_overlapping_rows_need_more_tiles(lib):
+    # rows 0 and 3 are both [0, n) (row 2, which runs backwards, is skipped):
+    # 20 pieces, above the default budget of rows + ceil(n / chunk) = 14 tiles
+    n, chunk = 1000, 100
+    src = torch.from_numpy(synth.int16_uniform(131, n)).cuda()
+    off = torch.tensor([0, n, n, 0, n], dtype=torch.int64, device="cuda")
+    skip = torch.tensor([0, 0, 1, 0], dtype=torch.uint8, device="cuda")
+    dst = torch.zeros(n, dtype=torch.int16, device="cuda")
+    lib.ts_copy_i16_rows(src, dst, off, sched="clc", chunk=chunk, skip_rows=skip)
+    with pytest.raises(lib.TsError) as ei:
+        lib.ts_sync_and_check()
+    assert ei.value.status == lib.TS_ERR_INVALID_ARG and "pieces" in ei.value.detail
+    # with enough tiles every piece is copied (twice, for the overlap)
+    dst = torch.zeros(n, dtype=torch.int16, device="cuda")
+    lib.ts_copy_i16_rows(src, dst, off, sched="clc", chunk=chunk, skip_rows=skip, tiles=20)
+    lib.ts_sync_and_check()
+    assert torch.equal(dst, src)
+
+
+def test_rows_chunked_needs_a_workspace(lib):
+    src = torch.zeros(100, dtype=torch.int16, device="cuda")
+    dst = torch.zeros(100, dtype=torch.int16, device="cuda")
+    off = torch.tensor([0, 100], dtype=torch.int64, device="cuda")
+    assert lib.ts_copy_i16_rows_ptr(src.data_ptr(), dst.data_ptr(), 100, off.data_ptr(), 1,
+                                    chunk=10) == lib.TS_ERR_INVALID_ARG
+    assert "workspace" in lib.ts_last_error_detail()
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("sched", ["static", "clc"])
+def test_rows_full_workload_chunked_bit_exact(lib, sched):
+    src_h, offsets = synth.ROWS.inputs()
+    src = torch.from_numpy(src_h).cuda()
+    dst = torch.zeros_like(src)
+    lib.ts_copy_i16_rows(src, dst, torch.from_numpy(offsets).cuda(), sched=sched, chunk=32768)
+    lib.ts_sync_and_check()
+    assert torch.equal(dst, src)  # the rows tile [0, n)

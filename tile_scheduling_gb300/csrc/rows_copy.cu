@@ -16,6 +16,15 @@
 // thread, and a ragged tail.  Row bounds are read on the device and checked
 // against [0, n] before any access; a row that fails the check is reported in
 // the status word and not copied.
+//
+// Chunked mode (not on the pages): rows are cut into pieces of at most `chunk`
+// elements and every piece is a work tile, so that a long row is not left to
+// one CTA at the end of the queue.  A planning kernel (one CTA) scans the
+// piece counts and writes, per row, its first tile (base) and, per tile, its
+// row (map); the copy kernel then finds tile t's piece with two loads.  The
+// launch's tile count is an upper bound on the pieces (rows + ceil(n / chunk)
+// for rows that do not overlap); tiles past the last piece are skipped like
+// the oversubscribed tiles above.
 #include <algorithm>
 #include <cstring>
 
@@ -41,6 +50,9 @@ struct RowsParams {
     int64_t tiles;               // work tiles (>= rows)
     int32_t sched;
     int32_t pad0;
+    int64_t chunk;               // elements per piece, or 0: one tile per row
+    int64_t *base;               // chunked: rows + 1 entries, first tile of each row (base[rows] = pieces)
+    int32_t *map;                // chunked: tiles entries, the row of each tile
     uint64_t timeout_ns;
     uint64_t drain_ns;
     unsigned long long *status;
@@ -127,6 +139,72 @@ __device__ __noinline__ bool rows_wait(uint32_t bar, uint32_t parity, uint64_t l
     }
 }
 
+constexpr int kPlanThreads = 1024;
+
+// Chunked mode, first kernel: piece counts of the rows, their running sum
+// (base) and the tile -> row map.  One CTA walks the rows 1024 at a time with
+// a block-wide inclusive scan; a row with bad bounds or marked in skip_rows
+// gets no pieces (bad bounds are reported, as in the per-row mode).  Pieces
+// that would not fit in the launch's tiles are not mapped, and reported.
+__global__ void __launch_bounds__(kPlanThreads) rows_plan_kernel(const __grid_constant__ RowsParams p) {
+    __shared__ int64_t warp_sum[kPlanThreads / 32];
+    __shared__ int64_t carry_s;
+    int64_t rows = p.rows;
+    if (p.rows_device) {
+        const int64_t r = *p.rows_device;
+        rows = r < 0 ? 0 : (r < p.rows ? r : p.rows);
+    }
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    if (tid == 0) carry_s = 0;
+    __syncthreads();
+    for (int64_t r0 = 0; r0 < rows; r0 += kPlanThreads) {
+        const int64_t r = r0 + tid;
+        int64_t pieces = 0, b = 0;
+        if (r < rows && !(p.skip && p.skip[r])) {
+            b = p.offsets[r];
+            const int64_t e = p.offsets[r + 1];
+            if (b >= 0 && b <= e && e <= p.n)
+                pieces = (e - b + p.chunk - 1) / p.chunk;
+            else
+                rows_report(p, 2ull, static_cast<unsigned long long>(r));
+        }
+        // block-wide inclusive scan of the piece counts
+        int64_t x = pieces;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int64_t y = __shfl_up_sync(0xffffffffu, x, d);
+            if (lane >= d) x += y;
+        }
+        if (lane == 31) warp_sum[wid] = x;
+        __syncthreads();
+        if (wid == 0) {
+            int64_t w = lane < kPlanThreads / 32 ? warp_sum[lane] : 0;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int64_t y = __shfl_up_sync(0xffffffffu, w, d);
+                if (lane >= d) w += y;
+            }
+            if (lane < kPlanThreads / 32) warp_sum[lane] = w;  // inclusive warp totals
+        }
+        __syncthreads();
+        const int64_t carry = carry_s;
+        const int64_t first = carry + (wid > 0 ? warp_sum[wid - 1] : 0) + x - pieces;
+        if (r < rows) p.base[r] = first;
+        for (int64_t j = 0; j < pieces; ++j) {
+            const int64_t t = first + j;
+            if (t >= p.tiles) {
+                rows_report(p, 3ull, static_cast<unsigned long long>(r));
+                break;
+            }
+            p.map[t] = static_cast<int32_t>(r);
+        }
+        __syncthreads();  // every thread has read carry_s and warp_sum
+        if (tid == kPlanThreads - 1) carry_s = carry + warp_sum[kPlanThreads / 32 - 1];
+        __syncthreads();
+    }
+    if (tid == 0) p.base[rows] = carry_s;
+}
+
 template <int VEC>
 __global__ void __launch_bounds__(kRowsMaxThreads) rows_copy_kernel(const __grid_constant__ RowsParams p) {
     __shared__ __align__(16) uint8_t resp[16];
@@ -145,6 +223,12 @@ __global__ void __launch_bounds__(kRowsMaxThreads) rows_copy_kernel(const __grid
         const int64_t r = *p.rows_device;
         rows = r < 0 ? 0 : (r < p.rows ? r : p.rows);
     }
+    // chunked: the planning kernel's piece count, clamped to the tiles it could map
+    int64_t pieces = 0;
+    if (p.chunk > 0) {
+        pieces = p.base[rows];
+        if (pieces > p.tiles) pieces = p.tiles;
+    }
     __syncthreads();
 
     int64_t tile = blockIdx.x;
@@ -156,7 +240,15 @@ __global__ void __launch_bounds__(kRowsMaxThreads) rows_copy_kernel(const __grid
             clc_try_cancel(resp_a, bar_a);
         }
         // skippable region: the row copy only; the queue bookkeeping below runs for every tile
-        if (tile < rows && !(p.skip && p.skip[tile])) {
+        if (p.chunk > 0) {
+            if (tile < pieces) {
+                const int64_t r = p.map[tile];
+                const int64_t b0 = p.offsets[r], e0 = p.offsets[r + 1];
+                const int64_t b = b0 + (tile - p.base[r]) * p.chunk;
+                const int64_t e = b + p.chunk < e0 ? b + p.chunk : e0;
+                if (b >= 0 && b <= e && e <= p.n) copy_row<VEC>(p.src, p.dst, b, e);  // checked by the plan too
+            }
+        } else if (tile < rows && !(p.skip && p.skip[tile])) {
             const int64_t b = p.offsets[tile], e = p.offsets[tile + 1];
             if (b >= 0 && b <= e && e <= p.n)
                 copy_row<VEC>(p.src, p.dst, b, e);
@@ -195,6 +287,7 @@ struct RowsPlan {
     int vec;
     int threads;
     int64_t tiles, grid, resident;
+    int64_t chunk, base_bytes, workspace_bytes;  // chunked mode: workspace = base[rows + 1], then map[tiles]
 };
 
 ts_status plan_rows(const int16_t *src, const int16_t *dst, int64_t n, const int64_t *offsets, int64_t rows,
@@ -205,12 +298,22 @@ ts_status plan_rows(const int16_t *src, const int16_t *dst, int64_t n, const int
     if (n < 0 || rows < 0) return fail(TS_ERR_INVALID_ARG, "negative size (n=%lld rows=%lld)",
                                        static_cast<long long>(n), static_cast<long long>(rows));
     if (sched != TS_SCHED_STATIC && sched != TS_SCHED_CLC) return fail(TS_ERR_INVALID_ARG, "sched %d", sched);
-    if (o->tiles < 0 || o->max_workers < 0 || o->timeout_s < 0) return fail(TS_ERR_INVALID_ARG, "negative option");
-    pl->tiles = o->tiles ? o->tiles : rows;
-    if (pl->tiles < rows)
-        return fail(TS_ERR_INVALID_ARG, "tiles = %lld is below rows = %lld", static_cast<long long>(pl->tiles),
-                    static_cast<long long>(rows));
+    if (o->tiles < 0 || o->max_workers < 0 || o->timeout_s < 0 || o->chunk < 0 || o->workspace_bytes < 0)
+        return fail(TS_ERR_INVALID_ARG, "negative option");
+    // chunked: enough tiles for the pieces of rows that do not overlap
+    const int64_t min_tiles = o->chunk > 0 ? rows + (n + o->chunk - 1) / o->chunk : rows;
+    pl->tiles = o->tiles ? o->tiles : min_tiles;
+    if (pl->tiles < min_tiles)
+        return fail(TS_ERR_INVALID_ARG, "tiles = %lld is below %lld (%s)", static_cast<long long>(pl->tiles),
+                    static_cast<long long>(min_tiles), o->chunk > 0 ? "rows + ceil(n / chunk)" : "rows");
     if (pl->tiles > kRowsMaxTiles) return fail(TS_ERR_UNSUPPORTED, "more than 2^31 - 1 work tiles");
+    pl->chunk = o->chunk;
+    pl->base_bytes = 0;
+    pl->workspace_bytes = 0;
+    if (o->chunk > 0) {
+        pl->base_bytes = ((rows + 1) * 8 + 255) / 256 * 256;
+        pl->workspace_bytes = pl->base_bytes + pl->tiles * 4;
+    }
     if (rows > 0 && !offsets) return fail(TS_ERR_INVALID_ARG, "offsets is NULL");
     if (n > 0 && (!src || !dst)) return fail(TS_ERR_INVALID_ARG, "src or dst is NULL");
     const uintptr_t s = reinterpret_cast<uintptr_t>(src), d = reinterpret_cast<uintptr_t>(dst);
@@ -272,12 +375,26 @@ ts_status ts_copy_i16_rows(const int16_t *src, int16_t *dst, int64_t n, const in
     p.skip = opts ? opts->skip_rows : nullptr;
     p.tiles = pl.tiles;
     p.sched = sched;
+    p.chunk = pl.chunk;
+    if (pl.chunk > 0) {
+        if (!opts->workspace || opts->workspace_bytes < pl.workspace_bytes ||
+            reinterpret_cast<uintptr_t>(opts->workspace) % 256 != 0)
+            return fail(TS_ERR_INVALID_ARG, "chunked copy needs a 256-byte aligned workspace of %lld bytes",
+                        static_cast<long long>(pl.workspace_bytes));
+        p.base = static_cast<int64_t *>(opts->workspace);
+        p.map = reinterpret_cast<int32_t *>(static_cast<char *>(opts->workspace) + pl.base_bytes);
+    }
     p.timeout_ns = (opts && opts->timeout_s > 0) ? static_cast<uint64_t>(opts->timeout_s * 1e9) : kRowsDefaultTimeoutNs;
     if (p.timeout_ns == 0) p.timeout_ns = 1;
     p.drain_ns = kRowsDrainNs;
     p.status = status;
     p.trace = opts ? reinterpret_cast<long long *>(opts->trace) : nullptr;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (pl.chunk > 0) {
+        rows_plan_kernel<<<1, kPlanThreads, 0, st>>>(p);
+        const cudaError_t pe = cudaGetLastError();
+        if (pe != cudaSuccess) return cuda_fail(pe, "row copy planning launch");
+    }
     cudaError_t e = pl.vec == 32   ? launch_rows<32>(p, pl.grid, pl.threads, st)
                     : pl.vec == 16 ? launch_rows<16>(p, pl.grid, pl.threads, st)
                                    : launch_rows<2>(p, pl.grid, pl.threads, st);
@@ -302,6 +419,7 @@ ts_status ts_copy_rows_launch_info(int64_t n, int64_t rows, int32_t sched, const
     info->grid_ctas = pl.grid;
     info->workers = pl.grid;
     info->resident = static_cast<int32_t>(pl.resident);
+    info->workspace_bytes = pl.workspace_bytes;
     return TS_OK;
 }
 

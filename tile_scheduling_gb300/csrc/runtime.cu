@@ -132,6 +132,11 @@ ts_status ts_sync_and_check(void *stream) {
         return ts::fail(TS_ERR_INVALID_ARG,
                         "row %llu of the jagged copy has bounds outside [0, n] or decreasing; %llu rows not copied",
                         h[1], h[2]);
+    if (h[0] == 3)
+        return ts::fail(TS_ERR_INVALID_ARG,
+                        "row %llu of the chunked copy has pieces past the launch's work tiles (overlapping rows "
+                        "need a larger tiles); %llu rows not fully copied",
+                        h[1], h[2]);
     const int where = static_cast<int>(h[1] >> 32);
     const unsigned block = static_cast<unsigned>(h[1] & 0xffffffffu);
     return ts::fail(TS_ERR_TIMEOUT, "barrier wait timed out (%s) in block %u; %llu errors recorded",
