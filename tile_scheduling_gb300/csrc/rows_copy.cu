@@ -140,12 +140,15 @@ __device__ __noinline__ bool rows_wait(uint32_t bar, uint32_t parity, uint64_t l
 }
 
 constexpr int kPlanThreads = 1024;
+constexpr int kPlanRows = 8;  // consecutive rows per planning thread: 8192 rows per pass
 
 // Chunked mode, first kernel: piece counts of the rows, their running sum
-// (base) and the tile -> row map.  One CTA walks the rows 1024 at a time with
-// a block-wide inclusive scan; a row with bad bounds or marked in skip_rows
-// gets no pieces (bad bounds are reported, as in the per-row mode).  Pieces
-// that would not fit in the launch's tiles are not mapped, and reported.
+// (base) and the tile -> row map.  One CTA walks the rows 8192 at a time: each
+// thread takes 8 consecutive rows (all their offsets loaded at once), and a
+// block-wide exclusive scan of the threads' piece totals places them.  A row
+// with bad bounds or marked in skip_rows gets no pieces (bad bounds are
+// reported, as in the per-row mode).  Pieces that would not fit in the
+// launch's tiles are not mapped, and reported.
 __global__ void __launch_bounds__(kPlanThreads) rows_plan_kernel(const __grid_constant__ RowsParams p) {
     __shared__ int64_t warp_sum[kPlanThreads / 32];
     __shared__ int64_t carry_s;
@@ -157,19 +160,28 @@ __global__ void __launch_bounds__(kPlanThreads) rows_plan_kernel(const __grid_co
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     if (tid == 0) carry_s = 0;
     __syncthreads();
-    for (int64_t r0 = 0; r0 < rows; r0 += kPlanThreads) {
-        const int64_t r = r0 + tid;
-        int64_t pieces = 0, b = 0;
-        if (r < rows && !(p.skip && p.skip[r])) {
-            b = p.offsets[r];
-            const int64_t e = p.offsets[r + 1];
-            if (b >= 0 && b <= e && e <= p.n)
-                pieces = (e - b + p.chunk - 1) / p.chunk;
-            else
-                rows_report(p, 2ull, static_cast<unsigned long long>(r));
+    for (int64_t r0 = 0; r0 < rows; r0 += kPlanThreads * kPlanRows) {
+        const int64_t rt = r0 + static_cast<int64_t>(tid) * kPlanRows;  // this thread's first row
+        int64_t off[kPlanRows + 1];
+#pragma unroll
+        for (int j = 0; j <= kPlanRows; ++j) off[j] = rt + j <= rows ? p.offsets[rt + j] : 0;
+        int64_t cnt[kPlanRows];
+        int64_t total = 0;
+#pragma unroll
+        for (int j = 0; j < kPlanRows; ++j) {
+            const int64_t r = rt + j;
+            cnt[j] = 0;
+            if (r < rows && !(p.skip && p.skip[r])) {
+                const int64_t b = off[j], e = off[j + 1];
+                if (b >= 0 && b <= e && e <= p.n)
+                    cnt[j] = (e - b + p.chunk - 1) / p.chunk;
+                else
+                    rows_report(p, 2ull, static_cast<unsigned long long>(r));
+            }
+            total += cnt[j];
         }
-        // block-wide inclusive scan of the piece counts
-        int64_t x = pieces;
+        // block-wide inclusive scan of the thread totals
+        int64_t x = total;
 #pragma unroll
         for (int d = 1; d < 32; d <<= 1) {
             const int64_t y = __shfl_up_sync(0xffffffffu, x, d);
@@ -188,15 +200,21 @@ __global__ void __launch_bounds__(kPlanThreads) rows_plan_kernel(const __grid_co
         }
         __syncthreads();
         const int64_t carry = carry_s;
-        const int64_t first = carry + (wid > 0 ? warp_sum[wid - 1] : 0) + x - pieces;
-        if (r < rows) p.base[r] = first;
-        for (int64_t j = 0; j < pieces; ++j) {
-            const int64_t t = first + j;
-            if (t >= p.tiles) {
-                rows_report(p, 3ull, static_cast<unsigned long long>(r));
-                break;
+        int64_t first = carry + (wid > 0 ? warp_sum[wid - 1] : 0) + x - total;
+#pragma unroll
+        for (int j = 0; j < kPlanRows; ++j) {
+            const int64_t r = rt + j;
+            if (r >= rows) break;
+            p.base[r] = first;
+            for (int64_t k = 0; k < cnt[j]; ++k) {
+                const int64_t t = first + k;
+                if (t >= p.tiles) {
+                    rows_report(p, 3ull, static_cast<unsigned long long>(r));
+                    break;
+                }
+                p.map[t] = static_cast<int32_t>(r);
             }
-            p.map[t] = static_cast<int32_t>(r);
+            first += cnt[j];
         }
         __syncthreads();  // every thread has read carry_s and warp_sum
         if (tid == kPlanThreads - 1) carry_s = carry + warp_sum[kPlanThreads / 32 - 1];
