@@ -357,6 +357,15 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
         __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(sm.tmem_slot);
+    // Launched as a programmatic dependent of the previous kernel in the
+    // stream: everything above touches only this CTA's shared memory, TMEM and
+    // the kernel parameters, so it overlaps that kernel's tail; no global
+    // memory is read or written before its writes are visible.  The next
+    // kernel may then be scheduled right away: it cannot occupy an SM before
+    // this grid's CTA there has exited (a CTA takes all of an SM's shared
+    // memory), and it waits here in turn.
+    grid_dep_wait();
+    grid_dep_launch();
 
     const int32_t first_unit = worker < p.num_units ? worker : -1;
 

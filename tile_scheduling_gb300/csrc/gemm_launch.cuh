@@ -56,14 +56,20 @@ struct GemmInstance {
         cfg.blockDim = dim3(C::THREADS, 1, 1);
         cfg.dynamicSmemBytes = C::SMEM_BYTES;
         cfg.stream = L.stream;
-        cudaLaunchAttribute attr[1];
+        // Programmatic stream serialization: the kernel's prologue may overlap the
+        // previous kernel in the stream; the kernel waits for it (griddepcontrol)
+        // before its first global memory access.
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
         if (CG == 2) {
-            attr[0].id = cudaLaunchAttributeClusterDimension;
-            attr[0].val.clusterDim.x = 2;
-            attr[0].val.clusterDim.y = 1;
-            attr[0].val.clusterDim.z = 1;
-            cfg.attrs = attr;
-            cfg.numAttrs = 1;
+            attr[1].id = cudaLaunchAttributeClusterDimension;
+            attr[1].val.clusterDim.x = 2;
+            attr[1].val.clusterDim.y = 1;
+            attr[1].val.clusterDim.z = 1;
+            cfg.numAttrs = 2;
         }
         return cudaLaunchKernelEx(&cfg, gemm_ws_kernel<BN, CG, OUT, EW>, L.a, L.b, L.d, L.p);
     }

@@ -115,6 +115,16 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap *m, uint32_t src,
                  : "memory");
 }
 
+// Programmatic dependent launch: wait until the grid this one depends on (the
+// previous kernel in the stream, when this grid was launched with programmatic
+// stream serialization) has completed and its writes are visible; a no-op for
+// a grid launched without it.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Let the next kernel in the stream (if launched as a programmatic dependent)
+// be scheduled before this grid completes; it still waits in grid_dep_wait.
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 // Wait until at most N committed store groups still read shared memory.
