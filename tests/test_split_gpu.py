@@ -6,6 +6,8 @@ slab counter.  Integer inputs must stay bit-exact, random inputs within the
 bound, the result must not depend on which part finished last, and the
 workspace must come back zeroed.
 """
+import functools
+
 import numpy as np
 import pytest
 import torch
@@ -16,20 +18,34 @@ from parity import as_f64, assert_bit_exact, assert_within_bound, bf16_bits, to_
 
 pytestmark = pytest.mark.gpu
 
-# (tile, M, N, K): each leaves a partial last wave on a 152-SM GB300
-CASES = [("128x256", 4096, 4096, 1024), ("256x256", 4096, 5120, 1024), ("128x128", 2600, 2900, 640)]
+# (tile, M, N, K): each leaves a partial last wave on a 152-SM GB300, with
+# K long enough for parts of at least 32 k-blocks
+CASES = [("128x256", 2048, 2560, 4096), ("256x256", 2560, 2560, 4096), ("128x128", 1664, 1664, 4096)]
 
 
 def _info(lib, M, N, K, out, sched, tile, ws):
     return lib.ts_gemm_launch_info(M, N, K, out, sched, tile=tile, workspace=ws)
 
 
+@functools.lru_cache(maxsize=None)
+def _integer_case(M, N, K):
+    A = synth.int_uniform_bf16(801, (M, K))
+    B = synth.int_uniform_bf16(802, (N, K))
+    return A, B, oracle.gemm_f64_blas(A, B)
+
+
+@functools.lru_cache(maxsize=None)
+def _random_case(M, N, K):
+    A = synth.uniform_pm1_bf16(811, (M, K))
+    B = synth.uniform_pm1_bf16(812, (N, K))
+    return A, B, oracle.gemm_f64_blas(A, B), oracle.gemm_f64_blas(A, B, absolute=True)
+
+
 @pytest.mark.parametrize("tile,M,N,K", CASES)
 @pytest.mark.parametrize("sched", ["static", "clc"])
 @pytest.mark.parametrize("ew", [4, 8])
 def test_split_tail_integer_bit_exact_and_workspace_rearmed(lib, tile, M, N, K, sched, ew):
-    A = synth.int_uniform_bf16(801, (M, K))
-    B = synth.int_uniform_bf16(802, (N, K))
+    A, B, ref = _integer_case(M, N, K)
     need = _info(lib, M, N, K, lib.TS_OUT_F32, sched, tile, None)["workspace_bytes"]
     assert need > 0, "case must leave a partial last wave"
     ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
@@ -41,7 +57,7 @@ def test_split_tail_integer_bit_exact_and_workspace_rearmed(lib, tile, M, N, K, 
     lib.ts_gemm_bf16_ex(to_device_bf16(A), to_device_bf16(B), D, sched=sched, tile=tile, workspace=ws, trace=trace,
                         epi_warps=ew)
     lib.ts_sync_and_check()
-    assert_bit_exact(D, oracle.gemm_f64_blas(A, B), f"split {tile} {sched} {ew} epilogue warps")
+    assert_bit_exact(D, ref, f"split {tile} {sched} {ew} epilogue warps")
     tr = trace.view(-1, 4).cpu().numpy()
     if sched == "static":
         assert np.all(tr[:, 0] == 1)
@@ -57,10 +73,7 @@ def test_split_tail_integer_bit_exact_and_workspace_rearmed(lib, tile, M, N, K, 
 @pytest.mark.parametrize("out", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("ew", [4, 8])
 def test_split_tail_random_within_bound_and_deterministic(lib, tile, M, N, K, out, ew):
-    A = synth.uniform_pm1_bf16(811, (M, K))
-    B = synth.uniform_pm1_bf16(812, (N, K))
-    ref = oracle.gemm_f64_blas(A, B)
-    S = oracle.gemm_f64_blas(A, B, absolute=True)
+    A, B, ref, S = _random_case(M, N, K)
     Ad, Bd = to_device_bf16(A), to_device_bf16(B)
     results = []
     for sched in ("clc", "static", "clc"):
@@ -79,13 +92,15 @@ def test_split_tail_random_within_bound_and_deterministic(lib, tile, M, N, K, ou
 
 
 def test_split_needs_enough_k(lib):
-    # 4 k-blocks cannot be split into parts of at least 4 k-blocks
-    info = lib.ts_gemm_launch_info(4096, 4096, 256, lib.TS_OUT_BF16, "static", tile="128x256")
+    # 32 k-blocks cannot be split into parts of at least 32 k-blocks
+    info = lib.ts_gemm_launch_info(2048, 2560, 2048, lib.TS_OUT_BF16, "static", tile="128x256")
     assert info["split_tiles"] == 0 and info["workspace_bytes"] == 0
+    info = lib.ts_gemm_launch_info(2048, 2560, 4096, lib.TS_OUT_BF16, "static", tile="128x256")
+    assert info["split_tiles"] > 0 and info["split_parts"] == 2
 
 
 def test_split_disabled_by_option(lib):
     ws = torch.zeros(64 << 20, dtype=torch.uint8, device="cuda")
-    info = lib.ts_gemm_launch_info(4096, 4096, 1024, lib.TS_OUT_BF16, "static", tile="128x256", workspace=ws,
+    info = lib.ts_gemm_launch_info(2048, 2560, 4096, lib.TS_OUT_BF16, "static", tile="128x256", workspace=ws,
                                    split_tail=-1)
     assert info["split_tiles"] == 0 and info["num_units"] == info["num_tiles"]

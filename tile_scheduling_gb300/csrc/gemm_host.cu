@@ -133,7 +133,10 @@ struct Plan {
     bool split;                       // applied (workspace given and large enough)
 };
 
-constexpr int64_t kMinKBlocksPerPart = 4;
+// A split part writes and re-reads an fp32 partial of its tile, a fixed cost
+// that only pays off against long parts: with 4 k-blocks per part the split
+// made 8192^2 x 512 10 % slower, and it broke even around 32 (K = 2048 per part).
+constexpr int64_t kMinKBlocksPerPart = 32;
 // The workspace starts with a fixed counter region; partials always follow it,
 // so a workspace reused across problem shapes never has partial data where a
 // later shape keeps its counters (which every launch leaves at zero).
