@@ -80,7 +80,7 @@ typedef struct {
                              picks one; TS_TILE_256x256_2CTA is TS_ERR_UNSUPPORTED); no split tail. */
     int32_t epi_warps;    /* epilogue warps per CTA: 4 (one per TMEM lane quarter) or 8 (two per
                              quarter, alternating subtiles: more latency hidden when the epilogue
-                             bounds the tile); 0 = 8 for a plain GEMM with K <= 512, else 4.
+                             bounds the tile); 0 = 8 for a plain GEMM with K <= 256, else 4.
                              Anything else is TS_ERR_INVALID_ARG.  Results do not depend on it. */
 } ts_gemm_opts;
 

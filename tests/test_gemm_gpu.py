@@ -57,8 +57,8 @@ def test_gemm_integer_bit_exact(lib, tile, sched, out, ew):
 
 def test_gemm_epilogue_warps_automatic_choice(lib):
     # eight epilogue warps for a short K loop, four for a long one or a grouped GEMM
-    assert lib.ts_gemm_launch_info(4096, 4096, 512, lib.TS_OUT_BF16, "clc")["epi_warps"] == 8
-    assert lib.ts_gemm_launch_info(4096, 4096, 576, lib.TS_OUT_BF16, "clc")["epi_warps"] == 4
+    assert lib.ts_gemm_launch_info(4096, 4096, 256, lib.TS_OUT_BF16, "clc")["epi_warps"] == 8
+    assert lib.ts_gemm_launch_info(4096, 4096, 320, lib.TS_OUT_BF16, "clc")["epi_warps"] == 4
     assert lib.ts_gemm_launch_info(4096, 4096, 64, lib.TS_OUT_BF16, "clc", epi_warps=4)["epi_warps"] == 4
     assert lib.ts_gemm_grouped_launch_info(512, 512, [0, 64, 128])["epi_warps"] == 4
     with pytest.raises(lib.TsError):
