@@ -1,0 +1,72 @@
+"""Stream order across back-to-back launches (GEMMs are programmatic dependents).
+
+Each GEMM launch may start its prologue while the previous kernel in the
+stream is still running, and waits (griddepcontrol) before touching global
+memory.  These chains would read stale data or lose writes if it did not:
+every case is integer-valued so the results are exact.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from parity import assert_bit_exact, bf16_bits, to_device_bf16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("tile,sched", [("128x256", "static"), ("256x256", "clc"), ("128x128", "clc")])
+def test_gemm_chain_reads_the_previous_output(lib, tile, sched):
+    # D1 = A B^T (bf16, exact small integers), then D2 = D1 C^T, D3 = D2 E^T, launched back to back
+    M, K = 1024, 128
+    A = synth.int_uniform_bf16(901, (M, K))
+    B = synth.one_hot_rows_bf16(K, K, np.random.default_rng(1).permutation(K))  # D1 = a column permutation of A
+    C = synth.one_hot_rows_bf16(K, K, np.random.default_rng(2).permutation(K))
+    E = synth.int_uniform_bf16(903, (256, K))
+    d_a, d_b, d_c, d_e = (to_device_bf16(x) for x in (A, B, C, E))
+    D1 = torch.full((M, K), float("nan"), dtype=torch.bfloat16, device="cuda")
+    D2 = torch.full((M, K), float("nan"), dtype=torch.bfloat16, device="cuda")
+    D3 = torch.full((M, 256), float("nan"), dtype=torch.float32, device="cuda")
+    for _ in range(3):  # repeated so that later launches overlap earlier ones' tails
+        lib.ts_gemm_bf16_ex(d_a, d_b, D1, sched=sched, tile=tile)
+        lib.ts_gemm_bf16_ex(D1, d_c, D2, sched=sched, tile=tile)
+        lib.ts_gemm_bf16_ex(D2, d_e, D3, sched=sched, tile=tile)
+    lib.ts_sync_and_check()
+    d1 = oracle.gemm_f64(A, B)
+    assert np.array_equal(bf16_bits(D1), oracle.bf16_rne(d1))
+    d2_bits = oracle.bf16_rne(oracle.gemm_f64(oracle.bf16_rne(d1), C))
+    assert np.array_equal(bf16_bits(D2), d2_bits)
+    assert_bit_exact(D3, oracle.gemm_f64(d2_bits, E), f"chain {tile} {sched}")
+
+
+def test_gemm_overwrites_in_stream_order(lib):
+    # two GEMMs write the same D back to back: the second one's values remain
+    M, N, K = 2048, 2048, 64
+    A1, A2 = synth.int_uniform_bf16(911, (M, K)), synth.int_uniform_bf16(912, (M, K))
+    B = synth.int_uniform_bf16(913, (N, K))
+    d_a1, d_a2, d_b = to_device_bf16(A1), to_device_bf16(A2), to_device_bf16(B)
+    D = torch.zeros((M, N), dtype=torch.float32, device="cuda")
+    for _ in range(4):
+        lib.ts_gemm_bf16_ex(d_a1, d_b, D, sched="clc")
+        lib.ts_gemm_bf16_ex(d_a2, d_b, D, sched="static")
+    lib.ts_sync_and_check()
+    assert_bit_exact(D, oracle.gemm_f64(A2, B), "write after write")
+
+
+def test_copy_then_gemm_then_copy(lib):
+    # the GEMM reads what the copy kernel just wrote; the next copy reads the GEMM's output
+    M, N, K = 512, 768, 192
+    A = synth.int_uniform_bf16(921, (M, K))
+    B = synth.int_uniform_bf16(922, (N, K))
+    src = to_device_bf16(A).view(torch.int16).reshape(-1)
+    a_copy = torch.zeros_like(src)
+    D = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    out = torch.zeros(M * N, dtype=torch.int16, device="cuda")
+    lib.ts_copy_i16(src, a_copy)
+    lib.ts_gemm_bf16_ex(a_copy.view(torch.bfloat16).view(M, K), to_device_bf16(B), D, sched="clc")
+    lib.ts_copy_i16(D.view(torch.int16).reshape(-1), out)
+    lib.ts_sync_and_check()
+    want = oracle.bf16_rne(oracle.gemm_f64(A, B))
+    assert np.array_equal(bf16_bits(D), want)
+    assert np.array_equal(out.cpu().numpy().view(np.uint16).reshape(M, N), want)
