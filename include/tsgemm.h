@@ -82,6 +82,13 @@ typedef struct {
                              quarter, alternating subtiles: more latency hidden when the epilogue
                              bounds the tile); 0 = 8 for a plain GEMM with K <= 256, else 4.
                              Anything else is TS_ERR_INVALID_ARG.  Results do not depend on it. */
+    int32_t merge;        /* the ring's barrier layout (CUTLASS TS "Pipeline Groups"): 0 = FusedMerge,
+                             one producer thread loads A and B onto one full barrier per stage
+                             (2 * S mbarriers); 1 = Merge, separate producer warps for A and for B,
+                             each with its own full barrier per stage, sharing the empty barrier
+                             (3 * S).  Merge uses four epilogue warps (epi_warps = 8 is
+                             TS_ERR_UNSUPPORTED) and cannot run with row_sums (both need warp 3:
+                             TS_ERR_UNSUPPORTED).  Results do not depend on it. */
 } ts_gemm_opts;
 
 /* What ts_gemm_bf16_ex would launch for a problem (host-only query). */
@@ -100,6 +107,7 @@ typedef struct {
     int32_t resident;        /* workers (CTAs or 2-CTA clusters) that fit on the GPU at once */
     int64_t workspace_bytes; /* workspace a split tail needs (0 when no split would help) */
     int32_t epi_warps;       /* epilogue warps per CTA (4 or 8; CTAs have 128 + 32 * epi_warps threads) */
+    int32_t merge;           /* 1: Merge barrier layout (A and B producers apart), 0: FusedMerge */
 } ts_launch_info;
 
 /* The barrier protocol of one kernel variant: the numbers the kernel
@@ -121,12 +129,17 @@ typedef struct {
     int32_t epilogue_warps;      /* epilogue warps per CTA */
     int32_t stage_bytes;         /* A + B bytes one CTA loads per stage */
     int32_t aux_empty_arrivals;  /* arrivals on aux_empty[s] from the Fork row-sum task (row_sums given) */
+    int32_t merge;               /* 1: Merge layout, A on full[s] (a_stage_bytes * cluster) and B on
+                                    full_b[s] ((stage_bytes - a_stage_bytes) * cluster), one producer each */
+    int32_t a_stage_bytes;       /* A bytes one CTA loads per stage */
 } ts_gemm_protocol;
 
 /* Fill *proto for the kernel variant of `tile` (TS_TILE_128x128, _128x256 or
- * _256x256_2CTA; TS_TILE_AUTO is TS_ERR_INVALID_ARG), `out_dtype` and
- * `epi_warps` (4 or 8; 0 = 4).  Host only; needs no GPU. */
-ts_status ts_gemm_protocol_info(int32_t tile, int32_t out_dtype, int32_t epi_warps, ts_gemm_protocol *proto);
+ * _256x256_2CTA; TS_TILE_AUTO is TS_ERR_INVALID_ARG), `out_dtype`, `epi_warps`
+ * (4 or 8; 0 = 4) and `merge` (0 or 1; Merge variants have 4 epilogue warps).
+ * Host only; needs no GPU. */
+ts_status ts_gemm_protocol_info(int32_t tile, int32_t out_dtype, int32_t epi_warps, int32_t merge,
+                                ts_gemm_protocol *proto);
 
 /*
  * ts_protocol_check -- explore every interleaving of a small mbarrier program

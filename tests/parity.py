@@ -54,3 +54,9 @@ def assert_bit_exact(D: torch.Tensor, ref: np.ndarray, what=""):
     if not np.array_equal(got, want):
         bad = np.argwhere(got != want)[:5]
         raise AssertionError(f"{what}: {int((got != want).sum())} mismatches; first {bad.tolist()}")
+
+
+# Kernel layouts the parametrised GPU tests run: (epilogue warps, barrier
+# layout), 0 = FusedMerge (A and B on one full barrier per stage), 1 = Merge
+# (separate producers and full barriers for A and B; four epilogue warps).
+LAYOUTS = [(4, 0), (8, 0), (4, 1)]

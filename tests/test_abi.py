@@ -49,6 +49,15 @@ def test_argument_errors_need_no_gpu(ts):
     assert ts.ts_gemm_bf16_ptr(0, 0, 0, 4, 4, 8, ts.TS_OUT_F32, stream=0, lda=4) == ts.TS_ERR_INVALID_ARG
     assert ts.ts_gemm_bf16_ptr(0, 0, 0, 4, 4, 8, ts.TS_OUT_F32, stream=0, epi_warps=6) == ts.TS_ERR_INVALID_ARG
     assert "epi_warps" in ts.ts_last_error_detail()
+    assert ts.ts_gemm_bf16_ptr(0, 0, 0, 4, 4, 8, ts.TS_OUT_F32, stream=0, merge=2) == ts.TS_ERR_INVALID_ARG
+    assert "merge" in ts.ts_last_error_detail()
+    # the Merge layout's B producer and the Fork row-sum task would both need warp 3
+    o = ts._opts(merge=1)
+    o.row_sums = 4096
+    assert ts._lib.ts_gemm_bf16_ex(None, None, None, 4, 4, 8, ts.TS_OUT_F32, 0, ctypes.byref(o),
+                                   None) == ts.TS_ERR_UNSUPPORTED
+    assert ts.ts_gemm_bf16_ptr(0, 0, 0, 4, 4, 8, ts.TS_OUT_F32, stream=0, merge=1,
+                               epi_warps=8) == ts.TS_ERR_UNSUPPORTED
     assert ts.ts_copy_i16_ptr(0, 0, -3, stream=0) == ts.TS_ERR_INVALID_ARG
     assert ts.ts_copy_i16_ptr(0, 0, 0, stream=0) == ts.TS_OK
     assert ts.ts_copy_i16_ptr(4096, 4100, 8, stream=0) == ts.TS_ERR_INVALID_ARG  # overlap

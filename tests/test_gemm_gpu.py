@@ -12,7 +12,7 @@ import torch
 
 import oracle
 import synth
-from parity import as_f64, assert_bit_exact, assert_within_bound, bf16_bits, to_device_bf16
+from parity import as_f64, assert_bit_exact, assert_within_bound, bf16_bits, to_device_bf16, LAYOUTS
 
 pytestmark = pytest.mark.gpu
 
@@ -46,13 +46,13 @@ def test_gemm_256_fp32_static_128x128(lib):
 @pytest.mark.parametrize("tile", TILES)
 @pytest.mark.parametrize("sched", SCHEDS)
 @pytest.mark.parametrize("out", OUTS)
-@pytest.mark.parametrize("ew", [4, 8])
-def test_gemm_integer_bit_exact(lib, tile, sched, out, ew):
+@pytest.mark.parametrize("ew,merge", LAYOUTS)
+def test_gemm_integer_bit_exact(lib, tile, sched, out, ew, merge):
     M, N, K = 600, 520, 328  # ragged in M, N and K
     A = synth.int_uniform_bf16(101, (M, K))
     B = synth.int_uniform_bf16(102, (N, K))
-    D = _run(lib, A, B, out, sched=sched, tile=tile, epi_warps=ew)
-    assert_bit_exact(D, oracle.gemm_f64(A, B), f"integer {tile} {sched} {ew} epilogue warps")
+    D = _run(lib, A, B, out, sched=sched, tile=tile, epi_warps=ew, merge=merge)
+    assert_bit_exact(D, oracle.gemm_f64(A, B), f"integer {tile} {sched} {ew} epilogue warps, merge {merge}")
 
 
 def test_gemm_epilogue_warps_automatic_choice(lib):
@@ -61,6 +61,9 @@ def test_gemm_epilogue_warps_automatic_choice(lib):
     assert lib.ts_gemm_launch_info(4096, 4096, 320, lib.TS_OUT_BF16, "clc")["epi_warps"] == 4
     assert lib.ts_gemm_launch_info(4096, 4096, 64, lib.TS_OUT_BF16, "clc", epi_warps=4)["epi_warps"] == 4
     assert lib.ts_gemm_grouped_launch_info(512, 512, [0, 64, 128])["epi_warps"] == 4
+    # the Merge layout is built with four
+    info = lib.ts_gemm_launch_info(4096, 4096, 64, lib.TS_OUT_BF16, "clc", merge=1)
+    assert info["epi_warps"] == 4 and info["merge"] == 1
     with pytest.raises(lib.TsError):
         lib.ts_gemm_launch_info(4096, 4096, 64, lib.TS_OUT_BF16, "clc", epi_warps=2)
 
@@ -212,10 +215,11 @@ def test_gemm_4096_bf16_128x256(lib, sched):
 
 
 @pytest.mark.slow
-def test_gemm_8192_bf16_2cta_clc_sampled_rows(lib):
+@pytest.mark.parametrize("merge", [0, 1])
+def test_gemm_8192_bf16_2cta_clc_sampled_rows(lib, merge):
     w = synth.GEMM_8192
     A, B = w.inputs()
-    D = _run(lib, A, B, torch.bfloat16, sched="clc", tile="256x256")
+    D = _run(lib, A, B, torch.bfloat16, sched="clc", tile="256x256", merge=merge)
     rng = np.random.default_rng(8192)
     rows = np.unique(np.concatenate([rng.integers(0, w.M, 96), [0, 255, 256, w.M - 1]]))
     a = oracle.bf16_to_f64(A[rows])

@@ -5,7 +5,7 @@ import torch
 
 import oracle
 import synth
-from parity import as_f64, assert_bit_exact, assert_within_bound, to_device_bf16
+from parity import as_f64, assert_bit_exact, assert_within_bound, to_device_bf16, LAYOUTS
 
 pytestmark = pytest.mark.gpu
 
@@ -24,12 +24,12 @@ def _run(lib, A_bits, B_bits, off, out, **kw):
 @pytest.mark.parametrize("tile", TILES)
 @pytest.mark.parametrize("sched", ["static", "clc"])
 @pytest.mark.parametrize("out", [torch.float32, torch.bfloat16])
-@pytest.mark.parametrize("ew", [4, 8])
-def test_grouped_integer_bit_exact(lib, tile, sched, out, ew):
+@pytest.mark.parametrize("ew,merge", LAYOUTS)
+def test_grouped_integer_bit_exact(lib, tile, sched, out, ew, merge):
     M, N = 300, 520
     A = synth.int_uniform_bf16(601, (M, 1024))
     B = synth.int_uniform_bf16(602, (N, 1024))
-    D = _run(lib, A, B, OFFSETS, out, sched=sched, tile=tile, epi_warps=ew)
+    D = _run(lib, A, B, OFFSETS, out, sched=sched, tile=tile, epi_warps=ew, merge=merge)
     ref = oracle.grouped_gemm_f64(A, B, OFFSETS, blas=True)
     for g in range(len(OFFSETS) - 1):
         assert_bit_exact(D[g], ref[g], f"group {g} {tile} {sched}")

@@ -102,7 +102,7 @@ def test_clc_protocol_verified_cta_pair(units):
     assert r.ok, r.message
 
 
-@pytest.mark.parametrize("mutation", [m for m in pc.MUTATIONS if not m.startswith("fork")])
+@pytest.mark.parametrize("mutation", [m for m in pc.MUTATIONS if not m.startswith(("fork", "merge"))])
 @pytest.mark.parametrize("tile,sched,warps", [("128x256", "clc", None), ("256x256", "clc", 1),
                                               ("256x256", "static", 2)])
 def test_planted_mistakes_are_caught(mutation, tile, sched, warps):
@@ -157,3 +157,44 @@ def test_eight_warp_planted_mistakes_are_caught(mutation):
     r = pc.check_variant("256x256", [2, 1, 2], "clc", stages=2, variant_epi_warps=8, epilogue_warps=1,
                          mutate=mutation)
     assert not r.ok and r.status == 1, (mutation, r)
+
+
+# Merge barrier layout ("Pipeline Groups", Merge): A and B loaded by two
+# producer warps onto their own full barriers, one shared empty barrier, the
+# MMA waiting on both.
+def test_merge_exports_its_layout(ts):
+    for tile, out in itertools.product(("128x128", "128x256", "256x256"), (ts.TS_OUT_BF16, ts.TS_OUT_F32)):
+        fused, p = ts.ts_gemm_protocol_info(tile, out, 4, 0), ts.ts_gemm_protocol_info(tile, out, 4, 1)
+        cg, e = p["cluster"], p["epilogue_warps"]
+        assert fused["merge"] == 0 and p["merge"] == 1 and e == 4
+        assert p["a_stage_bytes"] == 128 * 64 * 2  # 128 rows of A, one 128-byte swizzle row each
+        assert p["stage_bytes"] == fused["stage_bytes"] and p["stages"] == fused["stages"]
+        # the B producer of each CTA consumes every CLC response too
+        assert p["clc_empty_arrivals"] == fused["clc_empty_arrivals"] + cg
+    with pytest.raises(ts.TsError):
+        ts.ts_gemm_protocol_info("128x256", 0, 8, 1)  # Merge is built with four epilogue warps
+    with pytest.raises(ts.TsError):
+        ts.ts_gemm_protocol_info("128x256", 0, 4, 2)
+    with pytest.raises(ValueError):
+        pc.build_program(ts.ts_gemm_protocol_info("128x256", 0, 4, 1), [1], fork=True)
+
+
+@pytest.mark.parametrize("tile,sched,warps,units", [("128x128", "static", None, [2, 1, 2]),
+                                                    ("128x256", "clc", None, [2, 1, 2]),
+                                                    ("128x128", "clc", 2, [1, 3]),
+                                                    ("256x256", "static", 2, [2, 1, 2]),
+                                                    ("256x256", "clc", 1, [1]),
+                                                    ("256x256", "clc", 1, [3])])
+def test_merge_protocol_verified(tile, sched, warps, units):
+    r = pc.check_variant(tile, units, sched, stages=2, variant_merge=1, epilogue_warps=warps)
+    assert r.ok, r.message
+
+
+@pytest.mark.parametrize("mutation", [m for m in pc.MUTATIONS if not m.startswith("fork")])
+@pytest.mark.parametrize("tile,sched,warps", [("128x256", "clc", 2), ("256x256", "static", 1)])
+def test_merge_planted_mistakes_are_caught(mutation, tile, sched, warps):
+    r = pc.check_variant(tile, [2, 1, 2], sched, stages=2, variant_merge=1, epilogue_warps=warps, mutate=mutation)
+    if mutation == "clc_empty_count_low" and sched == "static":
+        assert r.ok
+    else:
+        assert not r.ok and r.status == 1, (mutation, r)

@@ -12,7 +12,7 @@ import torch
 
 import oracle
 import synth
-from parity import assert_bit_exact, to_device_bf16
+from parity import assert_bit_exact, to_device_bf16, LAYOUTS
 
 pytestmark = pytest.mark.gpu
 
@@ -31,12 +31,13 @@ def _traced(lib, A_bits, B_bits, out, tile, sched, **kw):
 
 @pytest.mark.parametrize("tile", ["128x128", "128x256", "256x256"])
 @pytest.mark.parametrize("max_workers", [0, 7, 1])
-@pytest.mark.parametrize("ew", [4, 8])
-def test_static_owner_follows_grid_stride_rule(lib, tile, max_workers, ew):
+@pytest.mark.parametrize("ew,merge", LAYOUTS)
+def test_static_owner_follows_grid_stride_rule(lib, tile, max_workers, ew, merge):
     M, N, K = 1500, 1300, 128
     A = synth.int_uniform_bf16(301, (M, K))
     B = synth.int_uniform_bf16(302, (N, K))
-    info, tr, D = _traced(lib, A, B, torch.float32, tile, "static", max_workers=max_workers, epi_warps=ew)
+    info, tr, D = _traced(lib, A, B, torch.float32, tile, "static", max_workers=max_workers, epi_warps=ew,
+                          merge=merge)
     assert info["epi_warps"] == ew
     if max_workers:
         assert info["workers"] == min(max_workers, info["num_units"])
@@ -47,12 +48,12 @@ def test_static_owner_follows_grid_stride_rule(lib, tile, max_workers, ew):
 
 
 @pytest.mark.parametrize("tile", ["128x128", "128x256", "256x256"])
-@pytest.mark.parametrize("ew", [4, 8])
-def test_clc_covers_every_tile_once(lib, tile, ew):
+@pytest.mark.parametrize("ew,merge", LAYOUTS)
+def test_clc_covers_every_tile_once(lib, tile, ew, merge):
     M, N, K = 4000, 3000, 64  # many more tiles than resident workers
     A = synth.int_uniform_bf16(311, (M, K))
     B = synth.int_uniform_bf16(312, (N, K))
-    info, tr, D = _traced(lib, A, B, torch.bfloat16, tile, "clc", epi_warps=ew)
+    info, tr, D = _traced(lib, A, B, torch.bfloat16, tile, "clc", epi_warps=ew, merge=merge)
     assert info["grid_ctas"] == info["num_units"] * info["cluster"]
     ok, why = oracle.clc_coverage_ok(tr[:, 0], tr[:, 1])
     assert ok, why

@@ -6,7 +6,7 @@ import torch
 
 import oracle
 import synth
-from parity import assert_bit_exact, to_device_bf16
+from parity import assert_bit_exact, to_device_bf16, LAYOUTS
 
 pytestmark = pytest.mark.gpu
 
@@ -27,8 +27,8 @@ def _causal(tiles_m, tiles_n, tm, tn):
 @pytest.mark.parametrize("tile", ["128x128", "128x256", "256x256"])
 @pytest.mark.parametrize("sched", ["static", "clc"])
 @pytest.mark.parametrize("out", [torch.float32, torch.bfloat16])
-@pytest.mark.parametrize("ew", [4, 8])
-def test_skipped_tiles_untouched_others_exact(lib, tile, sched, out, ew):
+@pytest.mark.parametrize("ew,merge", LAYOUTS)
+def test_skipped_tiles_untouched_others_exact(lib, tile, sched, out, ew, merge):
     M, N, K = 1500, 1400, 320
     A = synth.int_uniform_bf16(701, (M, K))
     B = synth.int_uniform_bf16(702, (N, K))
@@ -39,7 +39,7 @@ def test_skipped_tiles_untouched_others_exact(lib, tile, sched, out, ew):
     trace = torch.zeros(4 * info["num_units"], dtype=torch.int64, device="cuda")
     D = torch.full((M, N), SENTINEL, dtype=out, device="cuda")
     lib.ts_gemm_bf16_ex(to_device_bf16(A), to_device_bf16(B), D, sched=sched, tile=tile, workspace=None,
-                        trace=trace, skip_tiles=torch.from_numpy(mask.reshape(-1)).cuda(), epi_warps=ew)
+                        trace=trace, skip_tiles=torch.from_numpy(mask.reshape(-1)).cuda(), epi_warps=ew, merge=merge)
     lib.ts_sync_and_check()
     skipped = _mask_rows_cols(mask, info["tile_m"], info["tile_n"], M, N).astype(bool)
     ref = oracle.gemm_f64(A, B)

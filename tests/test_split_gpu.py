@@ -14,7 +14,7 @@ import torch
 
 import oracle
 import synth
-from parity import as_f64, assert_bit_exact, assert_within_bound, bf16_bits, to_device_bf16
+from parity import as_f64, assert_bit_exact, assert_within_bound, bf16_bits, to_device_bf16, LAYOUTS
 
 pytestmark = pytest.mark.gpu
 
@@ -43,8 +43,8 @@ def _random_case(M, N, K):
 
 @pytest.mark.parametrize("tile,M,N,K", CASES)
 @pytest.mark.parametrize("sched", ["static", "clc"])
-@pytest.mark.parametrize("ew", [4, 8])
-def test_split_tail_integer_bit_exact_and_workspace_rearmed(lib, tile, M, N, K, sched, ew):
+@pytest.mark.parametrize("ew,merge", LAYOUTS)
+def test_split_tail_integer_bit_exact_and_workspace_rearmed(lib, tile, M, N, K, sched, ew, merge):
     A, B, ref = _integer_case(M, N, K)
     need = _info(lib, M, N, K, lib.TS_OUT_F32, sched, tile, None)["workspace_bytes"]
     assert need > 0, "case must leave a partial last wave"
@@ -55,7 +55,7 @@ def test_split_tail_integer_bit_exact_and_workspace_rearmed(lib, tile, M, N, K, 
     trace = torch.zeros(4 * info["num_units"], dtype=torch.int64, device="cuda")
     D = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
     lib.ts_gemm_bf16_ex(to_device_bf16(A), to_device_bf16(B), D, sched=sched, tile=tile, workspace=ws, trace=trace,
-                        epi_warps=ew)
+                        epi_warps=ew, merge=merge)
     lib.ts_sync_and_check()
     assert_bit_exact(D, ref, f"split {tile} {sched} {ew} epilogue warps")
     tr = trace.view(-1, 4).cpu().numpy()
@@ -71,14 +71,14 @@ def test_split_tail_integer_bit_exact_and_workspace_rearmed(lib, tile, M, N, K, 
 
 @pytest.mark.parametrize("tile,M,N,K", CASES)
 @pytest.mark.parametrize("out", [torch.float32, torch.bfloat16])
-@pytest.mark.parametrize("ew", [4, 8])
-def test_split_tail_random_within_bound_and_deterministic(lib, tile, M, N, K, out, ew):
+@pytest.mark.parametrize("ew,merge", LAYOUTS)
+def test_split_tail_random_within_bound_and_deterministic(lib, tile, M, N, K, out, ew, merge):
     A, B, ref, S = _random_case(M, N, K)
     Ad, Bd = to_device_bf16(A), to_device_bf16(B)
     results = []
     for sched in ("clc", "static", "clc"):
         D = torch.full((M, N), float("nan"), dtype=out, device="cuda")
-        lib.ts_gemm_bf16_ex(Ad, Bd, D, sched=sched, tile=tile, epi_warps=ew)  # cached workspace
+        lib.ts_gemm_bf16_ex(Ad, Bd, D, sched=sched, tile=tile, epi_warps=ew, merge=merge)  # cached workspace
         lib.ts_sync_and_check()
         assert_within_bound(as_f64(D), ref, S, out, f"split {tile} {sched} {out}")
         results.append(bf16_bits(D) if out == torch.bfloat16 else D.cpu().numpy())

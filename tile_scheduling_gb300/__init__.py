@@ -47,7 +47,7 @@ class GemmOpts(ctypes.Structure):
                 ("ldb", ctypes.c_int64), ("ldd", ctypes.c_int64), ("timeout_s", ctypes.c_double),
                 ("trace", ctypes.c_void_p), ("raster_group", ctypes.c_int32), ("split_tail", ctypes.c_int32),
                 ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_int64), ("skip_tiles", ctypes.c_void_p),
-                ("row_sums", ctypes.c_void_p), ("epi_warps", ctypes.c_int32)]
+                ("row_sums", ctypes.c_void_p), ("epi_warps", ctypes.c_int32), ("merge", ctypes.c_int32)]
 
 
 class LaunchInfo(ctypes.Structure):
@@ -56,7 +56,7 @@ class LaunchInfo(ctypes.Structure):
                 ("num_tiles", ctypes.c_int64), ("grid_ctas", ctypes.c_int64), ("workers", ctypes.c_int64),
                 ("smem_bytes", ctypes.c_int32), ("tma_store", ctypes.c_int32), ("num_units", ctypes.c_int64),
                 ("split_tiles", ctypes.c_int64), ("split_parts", ctypes.c_int32), ("resident", ctypes.c_int32),
-                ("workspace_bytes", ctypes.c_int64), ("epi_warps", ctypes.c_int32)]
+                ("workspace_bytes", ctypes.c_int64), ("epi_warps", ctypes.c_int32), ("merge", ctypes.c_int32)]
 
 
 class RowsOpts(ctypes.Structure):
@@ -70,7 +70,7 @@ class GemmProtocol(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "cluster", "stages", "tx_bytes", "full_arrivals", "empty_arrivals", "accumulators", "tmem_full_arrivals",
         "tmem_empty_arrivals", "clc_slots", "clc_full_arrivals", "clc_empty_arrivals", "clc_response_bytes",
-        "epilogue_warps", "stage_bytes", "aux_empty_arrivals")]
+        "epilogue_warps", "stage_bytes", "aux_empty_arrivals", "merge", "a_stage_bytes")]
 
 
 def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
@@ -84,7 +84,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                         ctypes.POINTER(LaunchInfo)]
     lib.ts_gemm_bf16_checked_noalloc.argtypes = [P, P, P, I64, I64, I64, I32, I32, P, P]
     lib.ts_gemm_tile_coords.argtypes = [I64, I64, I64, I32, I32, ctypes.POINTER(GemmOpts), I64, I64, P, P]
-    lib.ts_gemm_protocol_info.argtypes = [I32, I32, I32, ctypes.POINTER(GemmProtocol)]
+    lib.ts_gemm_protocol_info.argtypes = [I32, I32, I32, I32, ctypes.POINTER(GemmProtocol)]
     lib.ts_protocol_check.argtypes = [I32, P, I32, I32, P, P, P, ctypes.c_char_p, I64, ctypes.POINTER(I64),
                                       ctypes.c_char_p, I32]
     lib.ts_protocol_check.restype = I32
@@ -136,9 +136,10 @@ def _sched(s) -> int:
 
 
 def _opts(tile="auto", max_workers=0, lda=0, ldb=0, ldd=0, timeout_s=0.0, trace=None, raster_group=0,
-          split_tail=0, workspace=None, skip_tiles=None, row_sums=None, epi_warps=0):
+          split_tail=0, workspace=None, skip_tiles=None, row_sums=None, epi_warps=0, merge=0):
     o = GemmOpts()
     o.epi_warps = int(epi_warps)
+    o.merge = int(merge)
     if row_sums is not None:
         if row_sums.dtype != torch.float32 or not row_sums.is_cuda or not row_sums.is_contiguous():
             raise TypeError("row_sums must be a contiguous float32 CUDA tensor")
@@ -207,21 +208,22 @@ def workspace_for(nbytes: int, device=None) -> torch.Tensor:
 
 def ts_gemm_bf16_ex(A: torch.Tensor, B: torch.Tensor, D: torch.Tensor, sched="static", tile="auto",
                     max_workers=0, timeout_s=0.0, trace=None, raster_group=0, workspace="auto", split_tail=0,
-                    skip_tiles=None, row_sums=None, epi_warps=0, stream=None) -> None:
+                    skip_tiles=None, row_sums=None, epi_warps=0, merge=0, stream=None) -> None:
     """D = A @ B.T for bf16 A [M, K] and B [N, K]; D [M, N] is bf16 or fp32.
 
     Rows may be strided (the row stride becomes lda / ldb / ldd).  ``workspace``
     ("auto": a cached zero-filled buffer; None: no split tail; or a CUDA tensor)
     lets the last partial wave of tiles be split along K.  ``epi_warps``: 4, 8
-    or 0 (automatic).  Asynchronous on ``stream`` (default: torch's current
-    stream)."""
+    or 0 (automatic); ``merge``: 1 for the Merge barrier layout (A and B from
+    separate producer warps).  Asynchronous on ``stream`` (default: torch's
+    current stream)."""
     M, N, K, lda, ldb, ldd = _gemm_args(A, B, D)
     lda, ldb, ldd = (lda if M > 1 else 0), (ldb if N > 1 else 0), (ldd if M > 1 else 0)
     workspace = _resolve_workspace(M, N, K, _OUT[D.dtype], sched, workspace,
                                    -1 if (skip_tiles is not None or row_sums is not None) else split_tail, tile=tile,
                                    max_workers=max_workers, lda=lda, ldb=ldb, ldd=ldd)
     o = _opts(tile, max_workers, lda, ldb, ldd, timeout_s, trace, raster_group, split_tail, workspace, skip_tiles,
-              row_sums, epi_warps)
+              row_sums, epi_warps, merge)
     _check(_lib.ts_gemm_bf16_ex(ctypes.c_void_p(A.data_ptr()), ctypes.c_void_p(B.data_ptr()),
                                 ctypes.c_void_p(D.data_ptr()), M, N, K, _OUT[D.dtype], _sched(sched),
                                 ctypes.byref(o), _stream_handle(stream)))
@@ -330,7 +332,7 @@ def ts_gemm_grouped_launch_info(M: int, N: int, k_offsets, out=TS_OUT_BF16, sche
 
 def ts_gemm_bf16_grouped(A: torch.Tensor, B: torch.Tensor, D: torch.Tensor, k_offsets, sched="static", tile="auto",
                          max_workers=0, timeout_s=0.0, trace=None, raster_group=0, skip_tiles=None,
-                         row_sums=None, epi_warps=0, stream=None) -> None:
+                         row_sums=None, epi_warps=0, merge=0, stream=None) -> None:
     """D[g] = A[:, k_g:k_g+1] @ B[:, k_g:k_g+1].T for every group g (k_offsets: groups + 1 multiples of 64).
 
     A [M, >=K] and B [N, >=K] bf16 with unit column stride; D [groups, M, N]
@@ -347,17 +349,17 @@ def ts_gemm_bf16_grouped(A: torch.Tensor, B: torch.Tensor, D: torch.Tensor, k_of
     if int(off[-1]) > min(A.shape[1], B.shape[1]):
         raise ValueError("k_offsets reach past the columns of A or B")
     o = _opts(tile, max_workers, lda if M > 1 else 0, ldb if N > 1 else 0, D.stride(1) if M > 1 else 0, timeout_s,
-              trace, raster_group, skip_tiles=skip_tiles, row_sums=row_sums, epi_warps=epi_warps)
+              trace, raster_group, skip_tiles=skip_tiles, row_sums=row_sums, epi_warps=epi_warps, merge=merge)
     _check(_lib.ts_gemm_bf16_grouped(ctypes.c_void_p(A.data_ptr()), ctypes.c_void_p(B.data_ptr()),
                                      ctypes.c_void_p(D.data_ptr()), M, N, G, off.ctypes.data, _OUT[D.dtype],
                                      _sched(sched), ctypes.byref(o), _stream_handle(stream)))
 
 
-def ts_gemm_protocol_info(tile="256x256", out=TS_OUT_BF16, epi_warps=0) -> dict:
+def ts_gemm_protocol_info(tile="256x256", out=TS_OUT_BF16, epi_warps=0, merge=0) -> dict:
     """Barrier layout and arrival counts of a kernel variant (no GPU needed)."""
     proto = GemmProtocol()
     _check(_lib.ts_gemm_protocol_info(_TILE[tile] if isinstance(tile, str) else int(tile), int(out), int(epi_warps),
-                                      ctypes.byref(proto)))
+                                      int(merge), ctypes.byref(proto)))
     return {f: getattr(proto, f) for f, _ in GemmProtocol._fields_}
 
 

@@ -30,13 +30,13 @@ struct GemmLaunch {
 };
 
 struct GemmVariant {
-    int bn, cg, out, epi_warps, stages, smem_bytes;
+    int bn, cg, out, epi_warps, merge, stages, smem_bytes;
     ts_gemm_protocol protocol;  // barrier layout and arrival counts of this variant
     cudaError_t (*launch)(const GemmLaunch &);
     // Workers (CTAs, or 2-CTA clusters) that can be resident at once.
     cudaError_t (*max_workers)(int *);
 };
 
-const GemmVariant *find_variant(int bn, int cg, int out, int epi_warps);
+const GemmVariant *find_variant(int bn, int cg, int out, int epi_warps, int merge);
 
 }  // namespace ts

@@ -14,15 +14,18 @@ namespace ts {
 
 extern const GemmVariant variant_128_1_bf16_e4, variant_128_1_f32_e4, variant_256_1_bf16_e4, variant_256_1_f32_e4,
     variant_256_2_bf16_e4, variant_256_2_f32_e4, variant_128_1_bf16_e8, variant_128_1_f32_e8, variant_256_1_bf16_e8,
-    variant_256_1_f32_e8, variant_256_2_bf16_e8, variant_256_2_f32_e8;
+    variant_256_1_f32_e8, variant_256_2_bf16_e8, variant_256_2_f32_e8, variant_128_1_bf16_e4m, variant_128_1_f32_e4m,
+    variant_256_1_bf16_e4m, variant_256_1_f32_e4m, variant_256_2_bf16_e4m, variant_256_2_f32_e4m;
 
-const GemmVariant *find_variant(int bn, int cg, int out, int epi_warps) {
+const GemmVariant *find_variant(int bn, int cg, int out, int epi_warps, int merge) {
     static const GemmVariant *const all[] = {
-        &variant_128_1_bf16_e4, &variant_128_1_f32_e4, &variant_256_1_bf16_e4, &variant_256_1_f32_e4,
-        &variant_256_2_bf16_e4, &variant_256_2_f32_e4, &variant_128_1_bf16_e8, &variant_128_1_f32_e8,
-        &variant_256_1_bf16_e8, &variant_256_1_f32_e8, &variant_256_2_bf16_e8, &variant_256_2_f32_e8};
+        &variant_128_1_bf16_e4,  &variant_128_1_f32_e4,  &variant_256_1_bf16_e4,  &variant_256_1_f32_e4,
+        &variant_256_2_bf16_e4,  &variant_256_2_f32_e4,  &variant_128_1_bf16_e8,  &variant_128_1_f32_e8,
+        &variant_256_1_bf16_e8,  &variant_256_1_f32_e8,  &variant_256_2_bf16_e8,  &variant_256_2_f32_e8,
+        &variant_128_1_bf16_e4m, &variant_128_1_f32_e4m, &variant_256_1_bf16_e4m, &variant_256_1_f32_e4m,
+        &variant_256_2_bf16_e4m, &variant_256_2_f32_e4m};
     for (const GemmVariant *v : all)
-        if (v->bn == bn && v->cg == cg && v->out == out && v->epi_warps == epi_warps) return v;
+        if (v->bn == bn && v->cg == cg && v->out == out && v->epi_warps == epi_warps && v->merge == merge) return v;
     return nullptr;
 }
 
@@ -176,6 +179,11 @@ ts_status plan_gemm(const void *D, int64_t M, int64_t N, int64_t K, int32_t out,
         return fail(TS_ERR_INVALID_ARG, "negative option");
     if (o->epi_warps != 0 && o->epi_warps != 4 && o->epi_warps != 8)
         return fail(TS_ERR_INVALID_ARG, "epi_warps = %d (0, 4 or 8)", o->epi_warps);
+    if (o->merge != 0 && o->merge != 1) return fail(TS_ERR_INVALID_ARG, "merge = %d (0 or 1)", o->merge);
+    if (o->merge && o->row_sums)
+        return fail(TS_ERR_UNSUPPORTED, "the Merge layout's B producer and the Fork consumer both need warp 3");
+    if (o->merge && o->epi_warps == 8)
+        return fail(TS_ERR_UNSUPPORTED, "the Merge layout is built with four epilogue warps");
     pl->lda = o->lda ? o->lda : K;
     pl->ldb = o->ldb ? o->ldb : K;
     pl->ldd = o->ldd ? o->ldd : N;
@@ -210,8 +218,8 @@ ts_status plan_gemm(const void *D, int64_t M, int64_t N, int64_t K, int32_t out,
     // eight warps hide more of its latencies; with a long one the epilogue
     // hides under the mainloop and four leave the SM's issue slots to it.
     int epi_warps = o->epi_warps;
-    if (epi_warps == 0) epi_warps = groups == 0 && K <= kShortK ? 8 : 4;
-    pl->v = find_variant(bn, cg, out, epi_warps);
+    if (epi_warps == 0) epi_warps = !o->merge && groups == 0 && K <= kShortK ? 8 : 4;
+    pl->v = find_variant(bn, cg, out, epi_warps, o->merge);
     if (!pl->v) return fail(TS_ERR_UNSUPPORTED, "no compiled variant for tile %d", tile);
     pl->cg = cg;
     pl->tile_m = 128 * cg;
@@ -295,6 +303,7 @@ ts_status fill_info(int64_t M, int64_t N, int64_t K, int32_t out_dtype, int32_t 
     info->resident = static_cast<int32_t>(pl.resident);
     info->workspace_bytes = pl.split_ws_bytes;
     info->epi_warps = pl.v->epi_warps;
+    info->merge = pl.v->merge;
     return TS_OK;
 }
 }  // namespace ts
@@ -354,11 +363,13 @@ ts_status ts_gemm_tile_coords(int64_t M, int64_t N, int64_t K, int32_t out_dtype
     return TS_OK;
 }
 
-ts_status ts_gemm_protocol_info(int32_t tile, int32_t out_dtype, int32_t epi_warps, ts_gemm_protocol *proto) {
+ts_status ts_gemm_protocol_info(int32_t tile, int32_t out_dtype, int32_t epi_warps, int32_t merge,
+                                ts_gemm_protocol *proto) {
     if (!proto) return ts::fail(TS_ERR_INVALID_ARG, "proto is NULL");
     if (out_dtype != TS_OUT_BF16 && out_dtype != TS_OUT_F32) return ts::fail(TS_ERR_INVALID_ARG, "out_dtype %d", out_dtype);
     if (epi_warps == 0) epi_warps = 4;
     if (epi_warps != 4 && epi_warps != 8) return ts::fail(TS_ERR_INVALID_ARG, "epi_warps = %d (0, 4 or 8)", epi_warps);
+    if (merge != 0 && merge != 1) return ts::fail(TS_ERR_INVALID_ARG, "merge = %d (0 or 1)", merge);
     int bn, cg;
     switch (tile) {
         case TS_TILE_128x128: bn = 128, cg = 1; break;
@@ -366,7 +377,7 @@ ts_status ts_gemm_protocol_info(int32_t tile, int32_t out_dtype, int32_t epi_war
         case TS_TILE_256x256_2CTA: bn = 256, cg = 2; break;
         default: return ts::fail(TS_ERR_INVALID_ARG, "tile %d (an explicit tile is required)", tile);
     }
-    const ts::GemmVariant *v = ts::find_variant(bn, cg, out_dtype, epi_warps);
+    const ts::GemmVariant *v = ts::find_variant(bn, cg, out_dtype, epi_warps, merge);
     if (!v) return ts::fail(TS_ERR_UNSUPPORTED, "no compiled variant for tile %d", tile);
     *proto = v->protocol;
     return TS_OK;

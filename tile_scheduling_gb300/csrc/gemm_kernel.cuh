@@ -60,10 +60,16 @@ constexpr int kMaxClcDepth = 2;
 // EW_ epilogue warps: 4 (one per TMEM lane quarter) or 8 (two per quarter,
 // splitting the columns).  Eight hide more of the epilogue's instruction
 // latencies when the K loop is short and the epilogue bounds the tile.
-template <int BN_, int CG_, int OUT_, int EW_>
+// MG_ selects the ring's barrier layout ("Pipeline Groups"): 0 is FusedMerge
+// (one producer thread loads A and B onto one full barrier per stage, 2 * S
+// barriers); 1 is Merge (a producer for A on warp 0 and one for B on warp 3,
+// each with its own full barrier per stage, sharing the empty barrier:
+// 3 * S barriers).
+template <int BN_, int CG_, int OUT_, int EW_, int MG_ = 0>
 struct GemmCfg {
     static constexpr int BN = BN_, CG = CG_, OUT = OUT_;
     static constexpr int EPI_WARPS = EW_;
+    static constexpr int MERGE = MG_;
     static constexpr int THREADS = 32 * (kRoleWarps + EPI_WARPS);
     static constexpr int BM = 128;              // accumulator rows per CTA = TMEM lanes
     static constexpr int TILE_M = BM * CG;      // output rows per worker
@@ -74,6 +80,8 @@ struct GemmCfg {
     static constexpr int B_BYTES = B_ROWS * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int TX_BYTES = STAGE_BYTES * CG;  // bytes landing on the even CTA's full barrier
+    static constexpr int TX_A_BYTES = A_BYTES * CG;     // Merge: on the A full barrier
+    static constexpr int TX_B_BYTES = B_BYTES * CG;     // Merge: on the B full barrier
     static constexpr int OUT_BYTES = OUT == OUT_F32 ? 4 : 2;
     static constexpr int SUB_COLS = 128 / OUT_BYTES;   // store subtile: 128 bytes of a row
     static constexpr int NUM_SUB = BN / SUB_COLS;
@@ -88,7 +96,7 @@ struct GemmCfg {
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
     // Barrier arrival counts (one place: the kernel initialises its barriers
     // with these, and the host-side protocol checker models them).
-    static constexpr int FULL_ARRIVALS = 1;   // the even CTA's producer (arrive.expect_tx)
+    static constexpr int FULL_ARRIVALS = 1;   // the even CTA's producer of that barrier (arrive.expect_tx)
     static constexpr int EMPTY_ARRIVALS = 1;  // one tcgen05.commit per stage use
     static constexpr int TFULL_ARRIVALS = 1;  // one tcgen05.commit per accumulator use
     static constexpr int TEMPTY_ARRIVALS = EPI_WARPS * CG;  // every epilogue warp of the CTA pair
@@ -96,9 +104,9 @@ struct GemmCfg {
     static constexpr int CLC_FULL_ARRIVALS = 1;  // this CTA's scheduler thread arms the slot
     static constexpr int CLC_RESPONSE_BYTES = 16;
     static constexpr int AUX_EMPTY_ARRIVALS = 1;  // the Fork row-sum task (lane 0 of warp 3)
-    // Consumers of one CLC response: producer, MMA, the epilogue warps and the
-    // scheduler in the even CTA; producer, epilogue warps and scheduler in the odd one.
-    static constexpr int CLC_CONSUMERS = (3 + EPI_WARPS) + (CG == 2 ? 2 + EPI_WARPS : 0);
+    // Consumers of one CLC response: producer(s), MMA, the epilogue warps and the
+    // scheduler in the even CTA; producer(s), epilogue warps and scheduler in the odd one.
+    static constexpr int CLC_CONSUMERS = (3 + MERGE + EPI_WARPS) + (CG == 2 ? 2 + MERGE + EPI_WARPS : 0);
     // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B bf16
     // (bits 7-9 = 1, 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at
     // bits 17-22, M >> 4 at bits 24-28.
@@ -108,6 +116,7 @@ struct GemmCfg {
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N");
     static_assert(CG == 1 || CG == 2, "cluster size");
     static_assert(EPI_WARPS == 4 || EPI_WARPS == 8, "epilogue warps");
+    static_assert(MERGE == 0 || MERGE == 1, "barrier layout");
     static_assert(NUM_SUB % (EPI_WARPS / 4) == 0, "subtiles split evenly between a quarter's warps");
     static_assert(STAGES >= 2, "ring too shallow");
     static_assert(SMEM_BYTES <= kSmemLimit, "shared memory budget");
@@ -210,6 +219,9 @@ struct Smem {
     __device__ __forceinline__ uint32_t aux_empty(int s) const {
         return bars + 8u * (2 * C::STAGES + 5 + 2 * kMaxClcDepth + s);
     }
+    // Merge: B's full barrier of stage s (full(s) then tracks A alone).  The
+    // Fork consumer and Merge never run together, so they share the slots.
+    __device__ __forceinline__ uint32_t full_b(int s) const { return aux_empty(s); }
 };
 
 // One work unit: a whole output tile, or one K-range of a split tail tile.
@@ -290,11 +302,11 @@ __device__ __forceinline__ int32_t next_unit(const Smem<C> &sm, const GemmParams
     return clc_consume(sm, p, clc_idx);
 }
 
-template <int BN, int CG, int OUT, int EW>
+template <int BN, int CG, int OUT, int EW, int MG>
 __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
     gemm_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmD, const __grid_constant__ GemmParams p) {
-    using C = GemmCfg<BN, CG, OUT, EW>;
+    using C = GemmCfg<BN, CG, OUT, EW, MG>;
     constexpr int RAW = C::SUB_COLS;  // fp32 accumulator words per lane per store subtile
     extern __shared__ __align__(1024) uint8_t smem_raw[];
 
@@ -319,7 +331,7 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
     // is filled once and read by two consumer tasks, the MMA issuer and the
     // row-sum task on warp 3; each releases the stage on its own empty barrier
     // and the producer refills it only after both.  One-CTA tiles only.
-    const bool fork = CG == 1 && p.row_sums != nullptr;
+    const bool fork = !MG && CG == 1 && p.row_sums != nullptr;
 
     // ------------------------------------------------------------ prologue
     if (warp == 0 && lane == 0) {
@@ -339,10 +351,12 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
         mbar_init(sm.mma_done(), 1);
         for (int r = 0; r < kMaxClcDepth; ++r) {
             mbar_init(sm.clc_full(r), C::CLC_FULL_ARRIVALS);
-            // with the Fork row-sum task, warp 3 consumes every response too
+            // with the Fork row-sum task, warp 3 consumes every response too (with
+            // Merge, its B producer is counted in CLC_CONSUMERS)
             mbar_init(sm.clc_empty(r), C::CLC_CONSUMERS + (fork ? 1 : 0));
         }
-        for (int s = 0; s < C::STAGES; ++s) mbar_init(sm.aux_empty(s), C::AUX_EMPTY_ARRIVALS);
+        // Fork: the row-sum task's empty barriers; Merge: B's full barriers (one arrival each)
+        for (int s = 0; s < C::STAGES; ++s) mbar_init(sm.aux_empty(s), MG ? C::FULL_ARRIVALS : C::AUX_EMPTY_ARRIVALS);
         *sm.abort_flag = 0;
         fence_mbar_init();
     }
@@ -369,62 +383,76 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
 
     const int32_t first_unit = worker < p.num_units ? worker : -1;
 
-    if (warp == 0) {
-        // ------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            int32_t unit = first_unit;
-            uint32_t clc_idx = 0, stage = 0, phase = 0, issued = 0;
-            bool alive = true;
-            while (unit >= 0 && alive) {
-                const Unit w = decode_unit(unit, p);
-                int32_t mb, nb;
-                raster(w.tile, p, mb, nb);
-                const int32_t a_row = mb * C::TILE_M + static_cast<int32_t>(rank) * C::BM;
-                const int32_t b_row = nb * BN + static_cast<int32_t>(rank) * C::B_ROWS;
-                if (p.trace && rank == 0) p.trace[4 * unit + 2] = static_cast<long long>(globaltimer());
-                for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
-                    if (!wait_phase(sm.empty(stage), phase ^ 1u, sm.abort_flag, p, WAIT_PRODUCER_EMPTY) ||
-                        (fork && !wait_phase(sm.aux_empty(stage), phase ^ 1u, sm.abort_flag, p, WAIT_PRODUCER_EMPTY))) {
-                        alive = false;
-                        break;
-                    }
-                    if (rank == 0) mbar_arrive_expect_tx(sm.full(stage), C::TX_BYTES);
-                    const uint32_t da = sm.a + stage * C::A_BYTES;
-                    const uint32_t db = sm.b + stage * C::B_BYTES;
-                    if constexpr (CG == 1) {
-                        tma_load_2d(da, &tmA, sm.full(stage), kb * C::BK, a_row);
-                        tma_load_2d(db, &tmB, sm.full(stage), kb * C::BK, b_row);
-                    } else {
-                        const uint32_t fb = mapa(sm.full(stage), 0);
-                        tma_load_2d_pair(da, &tmA, fb, kb * C::BK, a_row);
-                        tma_load_2d_pair(db, &tmB, fb, kb * C::BK, b_row);
-                    }
-                    ++issued;
-                    if (++stage == C::STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
+    // TMA producer loop of one thread: per k-block, acquire the stage's empty
+    // barrier (and the Fork consumer's), arm full_bar(stage) with `tx` bytes
+    // (the even CTA), issue the A and/or B tile loads, which complete on the
+    // even CTA's barrier.  FusedMerge: warp 0 loads both onto full(s).  Merge:
+    // warp 0 loads A onto full(s) and warp 3 loads B onto full_b(s).
+    auto produce = [&](const bool load_a, const bool load_b, const bool b_bar, const uint32_t tx) {
+        auto full_bar = [&](uint32_t st) { return b_bar ? sm.full_b(st) : sm.full(st); };
+        int32_t unit = first_unit;
+        uint32_t clc_idx = 0, stage = 0, phase = 0, issued = 0;
+        bool alive = true;
+        while (unit >= 0 && alive) {
+            const Unit w = decode_unit(unit, p);
+            int32_t mb, nb;
+            raster(w.tile, p, mb, nb);
+            const int32_t a_row = mb * C::TILE_M + static_cast<int32_t>(rank) * C::BM;
+            const int32_t b_row = nb * BN + static_cast<int32_t>(rank) * C::B_ROWS;
+            if (p.trace && rank == 0 && load_a) p.trace[4 * unit + 2] = static_cast<long long>(globaltimer());
+            for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
+                if (!wait_phase(sm.empty(stage), phase ^ 1u, sm.abort_flag, p, WAIT_PRODUCER_EMPTY) ||
+                    (fork && !wait_phase(sm.aux_empty(stage), phase ^ 1u, sm.abort_flag, p, WAIT_PRODUCER_EMPTY))) {
+                    alive = false;
+                    break;
                 }
-                if (!alive) break;
-                unit = next_unit(sm, p, unit, clc_idx);
-            }
-            // Drain: every issued load has landed (even CTA's full barriers) and
-            // the MMA has released every stage.
-            if (rank == 0) {
-                const uint32_t n = issued < C::STAGES ? issued : C::STAGES;
-                for (uint32_t i = 1; i <= n; ++i) {
-                    const uint32_t b = issued - i;
-                    wait_drain(sm.full(b % C::STAGES), (b / C::STAGES) & 1u, sm.abort_flag, p);
+                const uint32_t fb = full_bar(stage);
+                if (rank == 0) mbar_arrive_expect_tx(fb, tx);
+                const uint32_t da = sm.a + stage * C::A_BYTES;
+                const uint32_t db = sm.b + stage * C::B_BYTES;
+                if constexpr (CG == 1) {
+                    if (load_a) tma_load_2d(da, &tmA, fb, kb * C::BK, a_row);
+                    if (load_b) tma_load_2d(db, &tmB, fb, kb * C::BK, b_row);
+                } else {
+                    const uint32_t fb0 = mapa(fb, 0);
+                    if (load_a) tma_load_2d_pair(da, &tmA, fb0, kb * C::BK, a_row);
+                    if (load_b) tma_load_2d_pair(db, &tmB, fb0, kb * C::BK, b_row);
                 }
-            }
-            for (int i = 0; i < C::STAGES; ++i) {
-                if (!wait_drain(sm.empty(stage), phase ^ 1u, sm.abort_flag, p)) break;
-                if (fork && !wait_drain(sm.aux_empty(stage), phase ^ 1u, sm.abort_flag, p)) break;
+                ++issued;
                 if (++stage == C::STAGES) {
                     stage = 0;
                     phase ^= 1u;
                 }
             }
+            if (!alive) break;
+            unit = next_unit(sm, p, unit, clc_idx);
+        }
+        // Drain: every issued load has landed (even CTA's full barriers) and
+        // the MMA has released every stage.
+        if (rank == 0) {
+            const uint32_t n = issued < C::STAGES ? issued : C::STAGES;
+            for (uint32_t i = 1; i <= n; ++i) {
+                const uint32_t b = issued - i;
+                wait_drain(full_bar(b % C::STAGES), (b / C::STAGES) & 1u, sm.abort_flag, p);
+            }
+        }
+        for (int i = 0; i < C::STAGES; ++i) {
+            if (!wait_drain(sm.empty(stage), phase ^ 1u, sm.abort_flag, p)) break;
+            if (fork && !wait_drain(sm.aux_empty(stage), phase ^ 1u, sm.abort_flag, p)) break;
+            if (++stage == C::STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    };
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            if constexpr (MG)
+                produce(true, false, false, C::TX_A_BYTES);
+            else
+                produce(true, true, false, C::TX_BYTES);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -443,7 +471,8 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
                 for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
-                    if (!wait_phase(sm.full(stage), phase, sm.abort_flag, p, WAIT_MMA_FULL)) {
+                    if (!wait_phase(sm.full(stage), phase, sm.abort_flag, p, WAIT_MMA_FULL) ||
+                        (MG && !wait_phase(sm.full_b(stage), phase, sm.abort_flag, p, WAIT_MMA_FULL))) {
                         alive = false;
                         break;
                     }
@@ -519,6 +548,10 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
             }
             if (outstanding) wait_drain(sm.clc_full(out_r), out_ph, sm.abort_flag, p);
         }
+        __syncwarp();
+    } else if (warp == 3 && MG) {
+        // ------------------------------------------------- Merge: TMA producer of B
+        if (lane == 0) produce(false, true, true, C::TX_B_BYTES);
         __syncwarp();
     } else if (warp == 3) {
         // ------------------------------------------- Fork consumer: row sums of A

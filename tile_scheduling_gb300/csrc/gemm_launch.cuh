@@ -14,9 +14,9 @@ namespace ts {
 // statics of templates otherwise become process-unique symbols).
 namespace {
 
-template <int BN, int CG, int OUT, int EW>
+template <int BN, int CG, int OUT, int EW, int MG>
 struct GemmInstance {
-    using C = GemmCfg<BN, CG, OUT, EW>;
+    using C = GemmCfg<BN, CG, OUT, EW, MG>;
 
     // cudaFuncSetAttribute once per device (bit per device ordinal).
     static cudaError_t prepare() {
@@ -24,7 +24,7 @@ struct GemmInstance {
         const int dev = current_device();
         const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
         if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
-        cudaError_t e = cudaFuncSetAttribute(gemm_ws_kernel<BN, CG, OUT, EW>,
+        cudaError_t e = cudaFuncSetAttribute(gemm_ws_kernel<BN, CG, OUT, EW, MG>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
         if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
         return e;
@@ -45,7 +45,9 @@ struct GemmInstance {
                                 C::CLC_RESPONSE_BYTES,
                                 C::EPI_WARPS,
                                 C::A_BYTES + C::B_BYTES,
-                                C::AUX_EMPTY_ARRIVALS};
+                                C::AUX_EMPTY_ARRIVALS,
+                                C::MERGE,
+                                C::A_BYTES};
     }
 
     static cudaError_t launch(const GemmLaunch &L) {
@@ -71,7 +73,7 @@ struct GemmInstance {
             attr[1].val.clusterDim.z = 1;
             cfg.numAttrs = 2;
         }
-        return cudaLaunchKernelEx(&cfg, gemm_ws_kernel<BN, CG, OUT, EW>, L.a, L.b, L.d, L.p);
+        return cudaLaunchKernelEx(&cfg, gemm_ws_kernel<BN, CG, OUT, EW, MG>, L.a, L.b, L.d, L.p);
     }
 
     static cudaError_t max_workers(int *out) {
@@ -79,7 +81,7 @@ struct GemmInstance {
         if (e != cudaSuccess) return e;
         if (CG == 1) {
             int per_sm = 0;
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemm_ws_kernel<BN, CG, OUT, EW>, C::THREADS,
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemm_ws_kernel<BN, CG, OUT, EW, MG>, C::THREADS,
                                                               C::SMEM_BYTES);
             if (e != cudaSuccess) return e;
             *out = per_sm * device_sms(current_device());
@@ -97,7 +99,7 @@ struct GemmInstance {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int clusters = 0;
-        e = cudaOccupancyMaxActiveClusters(&clusters, reinterpret_cast<const void *>(gemm_ws_kernel<BN, CG, OUT, EW>),
+        e = cudaOccupancyMaxActiveClusters(&clusters, reinterpret_cast<const void *>(gemm_ws_kernel<BN, CG, OUT, EW, MG>),
                                            &cfg);
         if (e != cudaSuccess) return e;
         *out = clusters;
@@ -108,16 +110,17 @@ struct GemmInstance {
 }  // namespace
 }  // namespace ts
 
-#define TS_GEMM_VARIANT(NAME, BN, CG, OUT, EW)                                                             \
+#define TS_GEMM_VARIANT(NAME, BN, CG, OUT, EW, MG)                                                         \
     namespace ts {                                                                                         \
     extern const GemmVariant NAME;                                                                         \
     const GemmVariant NAME = {BN,                                                                          \
                               CG,                                                                          \
                               OUT,                                                                         \
                               EW,                                                                          \
-                              GemmCfg<BN, CG, OUT, EW>::STAGES,                                            \
-                              GemmCfg<BN, CG, OUT, EW>::SMEM_BYTES,                                        \
-                              GemmInstance<BN, CG, OUT, EW>::protocol(),                                   \
-                              &GemmInstance<BN, CG, OUT, EW>::launch,                                      \
-                              &GemmInstance<BN, CG, OUT, EW>::max_workers};                                \
+                              MG,                                                                          \
+                              GemmCfg<BN, CG, OUT, EW, MG>::STAGES,                                        \
+                              GemmCfg<BN, CG, OUT, EW, MG>::SMEM_BYTES,                                    \
+                              GemmInstance<BN, CG, OUT, EW, MG>::protocol(),                               \
+                              &GemmInstance<BN, CG, OUT, EW, MG>::launch,                                  \
+                              &GemmInstance<BN, CG, OUT, EW, MG>::max_workers};                            \
     }

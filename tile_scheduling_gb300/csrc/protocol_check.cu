@@ -16,8 +16,10 @@
 // int32 wide:
 //   WAIT   bar parity            ARRIVE bar tx_bytes (expect-tx, then arrive)
 //   TMA    buf tag bar bytes     -> async: buf := tag, then complete-tx(bar)
-//   MMA    sbuf0 sbuf1 acc tag   -> in-order queue: sbufs must hold tag; a tag
-//                                   with k-block > 0 must find tag - 1 in acc
+//   MMA    sbuf0 sbuf1 acc tag sbuf2 sbuf3
+//                                -> in-order queue: the (up to four) sbufs must
+//                                   hold tag; a tag with k-block > 0 must find
+//                                   tag - 1 in acc
 //   COMMIT bar0 bar1             -> in-order queue: one arrival on each bar
 //   TREAD  buf tag               buf must hold tag
 //   CREQ   slot0 slot1 seq bar0 bar1 bytes  -> async: slots := seq, complete-tx
@@ -203,7 +205,7 @@ struct Checker {
                 const int nq = s[m.o_mq];
                 for (int q = 0; q < nq; ++q) {
                     const int32_t *mo = op(s[m.o_mq + 1 + q]);
-                    if (mo[0] == OP_MMA && (mo[1] == o[1] || mo[2] == o[1])) {
+                    if (mo[0] == OP_MMA && (mo[1] == o[1] || mo[2] == o[1] || mo[5] == o[1] || mo[6] == o[1])) {
                         char b[256];
                         snprintf(b, sizeof b, "copy of tag %d overwrote %s before the queued MMA of tag %d read it",
                                  o[2], m.buf_name[o[1]].c_str(), mo[4]);
@@ -231,7 +233,7 @@ struct Checker {
             const int32_t *o = op(s[m.o_mq + 1]);
             if (o[0] == OP_MMA) {
                 const int tag = o[4];
-                for (int j = 1; j <= 2; ++j) {
+                for (const int j : {1, 2, 5, 6}) {
                     if (o[j] >= 0 && s[m.o_buf + o[j]] != tag) {
                         char b[256];
                         snprintf(b, sizeof b, "MMA of tag %d read %s holding tag %d", tag, m.buf_name[o[j]].c_str(),

@@ -15,7 +15,8 @@ responses) and reports
 
 * a deadlock: no role can move and nothing is in flight, before every role
   has finished;
-* a race: an MMA reads a ring stage that does not hold the k-block it expects
+* a race: an MMA reads a ring stage (or, in the Merge layout, either half of
+  it) that does not hold the k-block it expects
   (overwritten early or not yet landed) or accumulates onto the wrong partial
   sum, an epilogue reads an accumulator that is not the finished tile, or a
   CLC response slot is refilled before every role read it.
@@ -38,7 +39,7 @@ from . import _lib
 OP_WAIT, OP_ARRIVE, OP_TMA, OP_MMA, OP_COMMIT, OP_TREAD, OP_CREQ, OP_CREAD = range(8)
 MUTATIONS = ("tmem_empty_count_low", "tmem_empty_count_high", "clc_empty_count_low", "tx_bytes_one_cta",
              "producer_wait_parity", "epilogue_release_before_read", "mma_skip_stage_release",
-             "fork_producer_ignores_second_consumer")
+             "fork_producer_ignores_second_consumer", "merge_mma_skips_b_wait")
 
 
 def _tag(unit: int, kb: int) -> int:
@@ -77,9 +78,19 @@ def build_program(proto: dict, units: list, sched: str = "static", epilogue_warp
                     row-sum task): it reads every stage after the full barrier and
                     releases it on its own empty barrier; the producer refills a
                     stage only after both consumers released it (one-CTA tiles).
+
+    A variant with proto["merge"] = 1 has the Merge layout of the "Pipeline
+    Groups" page: two producers per CTA, one loading A onto full[s] and one
+    loading B onto full_b[s], both waiting on the shared empty[s]; the MMA
+    waits on both full barriers, and every producer consumes each CLC response.
     """
+    merge = bool(proto.get("merge", 0))
     if fork and proto["cluster"] != 1:
         raise ValueError("the Fork consumer runs on one-CTA tiles only")
+    if fork and merge:
+        raise ValueError("the Merge layout has no Fork consumer")
+    if mutate == "merge_mma_skips_b_wait" and not merge:
+        raise ValueError("merge_mma_skips_b_wait needs a Merge variant")
     if mutate is not None and mutate not in MUTATIONS:
         raise ValueError(f"unknown mutation {mutate}")
     cg = proto["cluster"]
@@ -89,6 +100,7 @@ def build_program(proto: dict, units: list, sched: str = "static", epilogue_warp
     A, R = proto["accumulators"], proto["clc_slots"]
     P = Program()
     full = [[P.bar(f"full[{c}][{s}]", proto["full_arrivals"]) for s in range(S)] for c in range(cg)]
+    full_b = [P.bar(f"full_b[{s}]", proto["full_arrivals"]) for s in range(S)] if merge else []
     empty = [[P.bar(f"empty[{c}][{s}]", proto["empty_arrivals"]) for s in range(S)] for c in range(cg)]
     tfull = [[P.bar(f"tmem_full[{c}][{a}]", proto["tmem_full_arrivals"]) for a in range(A)] for c in range(cg)]
     tempty_n = proto["tmem_empty_arrivals"] - dropped + {"tmem_empty_count_low": -1,
@@ -99,10 +111,13 @@ def build_program(proto: dict, units: list, sched: str = "static", epilogue_warp
         + (1 if fork else 0)
     clc_empty = [P.bar(f"clc_empty[{r}]", clc_empty_n) for r in range(R)]
     aux_empty = [P.bar(f"aux_empty[{s}]", proto["aux_empty_arrivals"]) for s in range(S)] if fork else []
-    stage = [[P.buf(f"stage[{c}][{s}]") for s in range(S)] for c in range(cg)]
+    stage = [[P.buf(f"stage[{c}][{s}]") for s in range(S)] for c in range(cg)]  # A (and B unless Merge)
+    stage_b = [[P.buf(f"stage_b[{c}][{s}]") for s in range(S)] for c in range(cg)] if merge else []
     accb = [P.buf(f"tmem[{a}]") for a in range(A)]
     slot = [[P.buf(f"clc_slot[{c}][{r}]") for r in range(R)] for c in range(cg)]
-    tx = proto["tx_bytes"] - (proto["stage_bytes"] if mutate == "tx_bytes_one_cta" else 0)
+    a_bytes = proto["a_stage_bytes"] if merge else proto["stage_bytes"]  # per CTA, onto full[s]
+    b_bytes = proto["stage_bytes"] - a_bytes  # per CTA, onto full_b[s] (Merge)
+    tx = (proto["tx_bytes"] if not merge else a_bytes * cg) - (a_bytes if mutate == "tx_bytes_one_cta" else 0)
     clc = sched == "clc"
 
     def rec(*v):
@@ -116,37 +131,46 @@ def build_program(proto: dict, units: list, sched: str = "static", epilogue_warp
     def adv(i, ph, n):
         return (0, ph ^ 1) if i + 1 == n else (i + 1, ph)
 
-    for c in range(cg):  # producer of each CTA
-        ops, s, ph, issued = [], 0, 0, 0
-        for u, nk in enumerate(units):
-            for kb in range(nk):
-                ops.append(rec(OP_WAIT, empty[c][s], ph if mutate == "producer_wait_parity" else ph ^ 1))
-                if fork and mutate != "fork_producer_ignores_second_consumer":
+    # producers of each CTA: one (A and B onto full[s]), or with Merge one for A
+    # onto full[s] and one for B onto full_b[s]
+    lines = [("producer", full, stage, a_bytes, tx)]
+    if merge:
+        lines = [("producer_a", full, stage, a_bytes, tx), ("producer_b", [full_b], stage_b, b_bytes, b_bytes * cg)]
+    for name, fbar, sbuf, nbytes, arm in lines:
+        for c in range(cg):
+            ops, s, ph, issued = [], 0, 0, 0
+            for u, nk in enumerate(units):
+                for kb in range(nk):
+                    ops.append(rec(OP_WAIT, empty[c][s], ph if mutate == "producer_wait_parity" else ph ^ 1))
+                    if fork and mutate != "fork_producer_ignores_second_consumer":
+                        ops.append(rec(OP_WAIT, aux_empty[s], ph ^ 1))
+                    if c == 0:
+                        ops.append(rec(OP_ARRIVE, fbar[0][s], arm))
+                    ops.append(rec(OP_TMA, sbuf[c][s], _tag(u, kb), fbar[0][s], nbytes))
+                    issued += 1
+                    s, ph = adv(s, ph, S)
+                if clc:
+                    consume(ops, c, u)
+            if c == 0:  # drain: the last issued loads landed
+                for i in range(1, min(issued, S) + 1):
+                    b = issued - i
+                    ops.append(rec(OP_WAIT, fbar[0][b % S], (b // S) & 1))
+            for _ in range(S):  # drain: the MMA (and the Fork consumer) released every stage
+                ops.append(rec(OP_WAIT, empty[c][s], ph ^ 1))
+                if fork:
                     ops.append(rec(OP_WAIT, aux_empty[s], ph ^ 1))
-                if c == 0:
-                    ops.append(rec(OP_ARRIVE, full[0][s], tx))
-                ops.append(rec(OP_TMA, stage[c][s], _tag(u, kb), full[0][s], proto["stage_bytes"]))
-                issued += 1
                 s, ph = adv(s, ph, S)
-            if clc:
-                consume(ops, c, u)
-        if c == 0:  # drain: the last issued loads landed
-            for i in range(1, min(issued, S) + 1):
-                b = issued - i
-                ops.append(rec(OP_WAIT, full[0][b % S], (b // S) & 1))
-        for _ in range(S):  # drain: the MMA (and the Fork consumer) released every stage
-            ops.append(rec(OP_WAIT, empty[c][s], ph ^ 1))
-            if fork:
-                ops.append(rec(OP_WAIT, aux_empty[s], ph ^ 1))
-            s, ph = adv(s, ph, S)
-        P.roles.append((f"producer[{c}]", None, ops))
+            P.roles.append((f"{name}[{c}]", None, ops))
 
     ops, s, ph, a, aph = [], 0, 0, 0, 0  # MMA issuer of the even CTA
     for u, nk in enumerate(units):
         ops.append(rec(OP_WAIT, tempty[a], aph ^ 1))
         for kb in range(nk):
             ops.append(rec(OP_WAIT, full[0][s], ph))
-            ops.append(rec(OP_MMA, stage[0][s], stage[1][s] if cg == 2 else -1, accb[a], _tag(u, kb)))
+            if merge and mutate != "merge_mma_skips_b_wait":
+                ops.append(rec(OP_WAIT, full_b[s], ph))
+            sb = [stage_b[0][s], stage_b[1][s] if cg == 2 else -1] if merge else [-1, -1]
+            ops.append(rec(OP_MMA, stage[0][s], stage[1][s] if cg == 2 else -1, accb[a], _tag(u, kb), *sb))
             if not (mutate == "mma_skip_stage_release" and u == 0 and kb == 0):
                 ops.append(rec(OP_COMMIT, empty[0][s], empty[1][s] if cg == 2 else -1))
             s, ph = adv(s, ph, S)
@@ -230,9 +254,10 @@ def check(P: Program, max_states: int = 20_000_000) -> Result:
 
 
 def check_variant(tile: str, units: list, sched: str = "static", out: int = 0, max_states: int = 20_000_000,
-                  variant_epi_warps: int = 4, **kw) -> Result:
-    """Check the protocol of a compiled kernel variant (tile, output type and
-    epilogue warp count) on a unit sequence."""
+                  variant_epi_warps: int = 4, variant_merge: int = 0, **kw) -> Result:
+    """Check the protocol of a compiled kernel variant (tile, output type,
+    epilogue warp count and barrier layout) on a unit sequence."""
     from . import ts_gemm_protocol_info
 
-    return check(build_program(ts_gemm_protocol_info(tile, out, variant_epi_warps), units, sched, **kw), max_states)
+    proto = ts_gemm_protocol_info(tile, out, variant_epi_warps, variant_merge)
+    return check(build_program(proto, units, sched, **kw), max_states)
