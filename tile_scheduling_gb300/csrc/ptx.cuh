@@ -103,15 +103,21 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap *m, uint32_t src, int32_t x, int32_t y) {
-    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(m),
-                 "r"(src), "r"(x), "r"(y)
-                 : "memory");
+// L2 policy that marks lines as the first to evict (fraction 1.0): for data
+// this kernel writes once and never reads back.
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
 }
 
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap *m, uint32_t src, int32_t x, int32_t y, int32_t z) {
-    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(m),
-                 "r"(src), "r"(x), "r"(y), "r"(z)
+// 3-D tiled store from this CTA's shared memory into a bulk group, with an L2
+// cache-policy operand.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *m, uint32_t src, int32_t x, int32_t y, int32_t z,
+                                             uint64_t pol) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group.L2::cache_hint [%0, {%2, %3, %4}], [%1], "
+                 "%5;" ::"l"(m),
+                 "r"(src), "r"(x), "r"(y), "r"(z), "l"(pol)
                  : "memory");
 }
 
