@@ -283,8 +283,10 @@ ts_status ts_gemm_bf16_checked_noalloc(const void *A, const void *B, void *D, in
  *   src, dst  device int16 arrays of n elements.  src == dst is a no-op;
  *             any other overlap is TS_ERR_INVALID_ARG.
  *   n         element count >= 0.
- * 16-byte vectors are used when src and dst share their offset modulo 16
- * bytes; other alignments take an element-wise path with the same result.
+ * 32-byte vectors are used when src and dst share their offset modulo 32
+ * bytes, 16-byte vectors when they share it modulo 16 (elements before the
+ * first aligned one and after the last whole vector one by one); other
+ * alignments take an element-wise path with the same result.
  */
 ts_status ts_copy_i16(const int16_t *src, int16_t *dst, int64_t n, void *stream);
 

@@ -23,6 +23,23 @@ def test_copy_sizes_and_alignments(lib, n, src_off, dst_off):
     assert np.all(d[:dst_off] == -1) and np.all(d[dst_off + n:] == -1)
 
 
+# Sizes of many rounds of the grid-stride loop, with a partial last round and
+# a head and tail of single elements (odd offsets and sizes), on the 32-byte,
+# 16-byte and element-wise paths.
+@pytest.mark.parametrize("n,src_off,dst_off", [((1 << 23) + 3, 3, 3), (5 * (1 << 22) + 11, 0, 8),
+                                               (3 * (1 << 21) + 1, 1, 5), (1 << 24, 0, 0)])
+def test_copy_many_chunks_per_cta(lib, n, src_off, dst_off):
+    src_h = synth.int16_uniform(900 + n, n)
+    sbuf = torch.zeros(n + 16, dtype=torch.int16, device="cuda")
+    dbuf = torch.full((n + 16,), -1, dtype=torch.int16, device="cuda")
+    sbuf[src_off:src_off + n] = torch.from_numpy(src_h).cuda()
+    lib.ts_copy_i16(sbuf[src_off:src_off + n], dbuf[dst_off:dst_off + n])
+    lib.ts_sync_and_check()
+    d = dbuf.cpu().numpy()
+    assert np.array_equal(d[dst_off:dst_off + n], oracle.copy_i16(src_h))
+    assert np.all(d[:dst_off] == -1) and np.all(d[dst_off + n:] == -1)
+
+
 @pytest.mark.slow
 def test_copy_full_size_bit_exact(lib):
     n = synth.COPY_N
