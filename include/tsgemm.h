@@ -78,16 +78,19 @@ typedef struct {
                              correction term of zero-point-quantised products.  Rows whose first
                              tile column is skipped are left untouched.  1-CTA tiles only (AUTO
                              picks one; TS_TILE_256x256_2CTA is TS_ERR_UNSUPPORTED); no split tail. */
-    int32_t epi_warps;    /* epilogue warps per CTA: 4 (one per TMEM lane quarter) or 8 (two per
-                             quarter, alternating subtiles: more latency hidden when the epilogue
-                             bounds the tile); 0 = 8 for a plain GEMM with K <= 256, else 4.
-                             Anything else is TS_ERR_INVALID_ARG.  Results do not depend on it. */
+    int32_t epi_warps;    /* epilogue warps per CTA: 4 (one per TMEM lane quarter), 8 or 16 (two or
+                             four per quarter, taking its subtiles in turn: more latency hidden
+                             when the epilogue bounds the tile); 0 = automatic: for a plain GEMM
+                             16 with K <= 128 on a 256-column tile, 8 with K <= 256, else 4.
+                             16 needs a 256-column tile (else TS_ERR_UNSUPPORTED) and never
+                             splits the tail.  Anything else is TS_ERR_INVALID_ARG.  Results do
+                             not depend on it. */
     int32_t merge;        /* the ring's barrier layout (CUTLASS TS "Pipeline Groups"): 0 = FusedMerge,
                              one producer thread loads A and B onto one full barrier per stage
                              (2 * S mbarriers); 1 = Merge, separate producer warps for A and for B,
                              each with its own full barrier per stage, sharing the empty barrier
-                             (3 * S).  Merge uses four epilogue warps (epi_warps = 8 is
-                             TS_ERR_UNSUPPORTED) and cannot run with row_sums (both need warp 3:
+                             (3 * S).  Merge uses four epilogue warps (epi_warps = 8 or 16
+                             is TS_ERR_UNSUPPORTED) and cannot run with row_sums (both need warp 3:
                              TS_ERR_UNSUPPORTED).  Results do not depend on it. */
 } ts_gemm_opts;
 
@@ -106,7 +109,7 @@ typedef struct {
     int32_t split_parts;     /* K parts per split tile (1 if none) */
     int32_t resident;        /* workers (CTAs or 2-CTA clusters) that fit on the GPU at once */
     int64_t workspace_bytes; /* workspace a split tail needs (0 when no split would help) */
-    int32_t epi_warps;       /* epilogue warps per CTA (4 or 8; CTAs have 128 + 32 * epi_warps threads) */
+    int32_t epi_warps;       /* epilogue warps per CTA (4, 8 or 16; CTAs have 128 + 32 * epi_warps threads) */
     int32_t merge;           /* 1: Merge barrier layout (A and B producers apart), 0: FusedMerge */
 } ts_launch_info;
 
@@ -136,7 +139,8 @@ typedef struct {
 
 /* Fill *proto for the kernel variant of `tile` (TS_TILE_128x128, _128x256 or
  * _256x256_2CTA; TS_TILE_AUTO is TS_ERR_INVALID_ARG), `out_dtype`, `epi_warps`
- * (4 or 8; 0 = 4) and `merge` (0 or 1; Merge variants have 4 epilogue warps).
+ * (4, 8 or 16; 0 = 4; 16 for 256-column tiles only) and `merge` (0 or 1; Merge
+ * variants have 4 epilogue warps).
  * Host only; needs no GPU. */
 ts_status ts_gemm_protocol_info(int32_t tile, int32_t out_dtype, int32_t epi_warps, int32_t merge,
                                 ts_gemm_protocol *proto);

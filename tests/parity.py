@@ -60,3 +60,9 @@ def assert_bit_exact(D: torch.Tensor, ref: np.ndarray, what=""):
 # layout), 0 = FusedMerge (A and B on one full barrier per stage), 1 = Merge
 # (separate producers and full barriers for A and B; four epilogue warps).
 LAYOUTS = [(4, 0), (8, 0), (4, 1)]
+
+
+def tile_layouts(tiles):
+    """(tile, epilogue warps, barrier layout) cases: every layout on every tile,
+    and sixteen epilogue warps on the 256-column tiles (the only ones built)."""
+    return [(t, ew, mg) for t in tiles for ew, mg in LAYOUTS + ([(16, 0)] if t != "128x128" else [])]

@@ -11,9 +11,8 @@ from parity import assert_bit_exact, as_f64, assert_within_bound, to_device_bf16
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("tile", ["128x128", "128x256"])
+@pytest.mark.parametrize("tile,ew", [("128x128", 4), ("128x128", 8), ("128x256", 4), ("128x256", 8), ("128x256", 16)])
 @pytest.mark.parametrize("sched", ["static", "clc"])
-@pytest.mark.parametrize("ew", [4, 8])
 def test_fork_integer_exact(lib, tile, sched, ew):
     M, N, K = 700, 600, 640
     A = synth.int_uniform_bf16(801, (M, K))

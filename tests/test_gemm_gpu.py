@@ -12,7 +12,7 @@ import torch
 
 import oracle
 import synth
-from parity import as_f64, assert_bit_exact, assert_within_bound, bf16_bits, to_device_bf16, LAYOUTS
+from parity import as_f64, assert_bit_exact, assert_within_bound, bf16_bits, tile_layouts, to_device_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -43,10 +43,9 @@ def test_gemm_256_fp32_static_128x128(lib):
 
 
 # ------------------------------------------------------ exact-value cases
-@pytest.mark.parametrize("tile", TILES)
+@pytest.mark.parametrize("tile,ew,merge", tile_layouts(TILES))
 @pytest.mark.parametrize("sched", SCHEDS)
 @pytest.mark.parametrize("out", OUTS)
-@pytest.mark.parametrize("ew,merge", LAYOUTS)
 def test_gemm_integer_bit_exact(lib, tile, sched, out, ew, merge):
     M, N, K = 600, 520, 328  # ragged in M, N and K
     A = synth.int_uniform_bf16(101, (M, K))
@@ -56,8 +55,14 @@ def test_gemm_integer_bit_exact(lib, tile, sched, out, ew, merge):
 
 
 def test_gemm_epilogue_warps_automatic_choice(lib):
-    # eight epilogue warps for a short K loop, four for a long one or a grouped GEMM
-    assert lib.ts_gemm_launch_info(4096, 4096, 256, lib.TS_OUT_BF16, "clc")["epi_warps"] == 8
+    # sixteen epilogue warps for the shortest K loops on 256-column tiles, eight
+    # for short ones, four for a long one or a grouped GEMM
+    for K, ew in ((64, 16), (128, 16), (192, 8), (256, 8)):
+        assert lib.ts_gemm_launch_info(4096, 4096, K, lib.TS_OUT_BF16, "clc")["epi_warps"] == ew
+        assert lib.ts_gemm_launch_info(4096, 4096, K, lib.TS_OUT_BF16, "static", tile="128x256")["epi_warps"] == ew
+    assert lib.ts_gemm_launch_info(4096, 4096, 64, lib.TS_OUT_BF16, "clc", tile="128x128")["epi_warps"] == 8
+    with pytest.raises(lib.TsError):
+        lib.ts_gemm_launch_info(4096, 4096, 64, lib.TS_OUT_BF16, "clc", tile="128x128", epi_warps=16)
     assert lib.ts_gemm_launch_info(4096, 4096, 320, lib.TS_OUT_BF16, "clc")["epi_warps"] == 4
     assert lib.ts_gemm_launch_info(4096, 4096, 64, lib.TS_OUT_BF16, "clc", epi_warps=4)["epi_warps"] == 4
     assert lib.ts_gemm_grouped_launch_info(512, 512, [0, 64, 128])["epi_warps"] == 4
@@ -239,7 +244,7 @@ def test_gemm_8192_bf16_2cta_clc_sampled_rows(lib, merge):
 @pytest.mark.slow
 @pytest.mark.parametrize("sched", SCHEDS)
 @pytest.mark.parametrize("tile", ["128x256", "256x256"])
-@pytest.mark.parametrize("ew", [4, 8])
+@pytest.mark.parametrize("ew", [4, 8, 16])
 def test_gemm_small_k_sampled(lib, sched, tile, ew):
     # 8192x8192x64: one k-block per tile, the output-write-bound launch the bench times
     w = synth.GEMM_SMALLK

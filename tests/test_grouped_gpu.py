@@ -5,7 +5,7 @@ import torch
 
 import oracle
 import synth
-from parity import as_f64, assert_bit_exact, assert_within_bound, to_device_bf16, LAYOUTS
+from parity import as_f64, assert_bit_exact, assert_within_bound, to_device_bf16, tile_layouts
 
 pytestmark = pytest.mark.gpu
 
@@ -21,10 +21,9 @@ def _run(lib, A_bits, B_bits, off, out, **kw):
     return D
 
 
-@pytest.mark.parametrize("tile", TILES)
+@pytest.mark.parametrize("tile,ew,merge", tile_layouts(TILES))
 @pytest.mark.parametrize("sched", ["static", "clc"])
 @pytest.mark.parametrize("out", [torch.float32, torch.bfloat16])
-@pytest.mark.parametrize("ew,merge", LAYOUTS)
 def test_grouped_integer_bit_exact(lib, tile, sched, out, ew, merge):
     M, N = 300, 520
     A = synth.int_uniform_bf16(601, (M, 1024))

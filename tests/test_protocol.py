@@ -138,6 +138,15 @@ def test_protocol_info_epilogue_warp_choices(ts):
     assert ts.ts_gemm_protocol_info("128x256", 0)["epilogue_warps"] == 4  # 0 = the four-warp variant
     with pytest.raises(ts.TsError):
         ts.ts_gemm_protocol_info("128x256", 0, 6)
+    with pytest.raises(ts.TsError):
+        ts.ts_gemm_protocol_info("128x128", 0, 16)  # sixteen only on 256-column tiles
+    for tile, out in itertools.product(("128x256", "256x256"), (ts.TS_OUT_BF16, ts.TS_OUT_F32)):
+        p, p8 = ts.ts_gemm_protocol_info(tile, out, 16), ts.ts_gemm_protocol_info(tile, out, 8)
+        cg = p["cluster"]
+        assert p["epilogue_warps"] == 16 and p["tmem_empty_arrivals"] == 16 * cg
+        assert p["clc_empty_arrivals"] == p8["clc_empty_arrivals"] + 8 * cg
+        # 64 KB of staging instead of 32 KB: one stage fewer
+        assert p["stages"] == p8["stages"] - 1
 
 
 # Eight epilogue warps: two per TMEM lane quarter, each releasing the
@@ -198,3 +207,19 @@ def test_merge_planted_mistakes_are_caught(mutation, tile, sched, warps):
         assert r.ok
     else:
         assert not r.ok and r.status == 1, (mutation, r)
+
+
+# Sixteen epilogue warps: four per TMEM lane quarter, each releasing the
+# accumulator after its own subtiles; the model keeps a few of them.
+@pytest.mark.parametrize("tile,sched,warps,units", [("128x256", "clc", 2, [2, 1]), ("128x256", "static", 3, [1, 2, 1]),
+                                                    ("256x256", "clc", 1, [1, 2]), ("256x256", "static", 2, [2, 1])])
+def test_sixteen_warp_protocol_verified(tile, sched, warps, units):
+    r = pc.check_variant(tile, units, sched, stages=2, variant_epi_warps=16, epilogue_warps=warps)
+    assert r.ok, r.message
+
+
+@pytest.mark.parametrize("mutation", ["epilogue_release_before_read", "tmem_empty_count_high", "clc_empty_count_low"])
+def test_sixteen_warp_planted_mistakes_are_caught(mutation):
+    r = pc.check_variant("256x256", [2, 1, 2], "clc", stages=2, variant_epi_warps=16, epilogue_warps=1,
+                         mutate=mutation)
+    assert not r.ok and r.status == 1, (mutation, r)

@@ -12,7 +12,7 @@ import torch
 
 import oracle
 import synth
-from parity import assert_bit_exact, to_device_bf16, LAYOUTS
+from parity import assert_bit_exact, to_device_bf16, tile_layouts
 
 pytestmark = pytest.mark.gpu
 
@@ -29,9 +29,8 @@ def _traced(lib, A_bits, B_bits, out, tile, sched, **kw):
     return info, trace.view(-1, 4).cpu().numpy(), D
 
 
-@pytest.mark.parametrize("tile", ["128x128", "128x256", "256x256"])
+@pytest.mark.parametrize("tile,ew,merge", tile_layouts(["128x128", "128x256", "256x256"]))
 @pytest.mark.parametrize("max_workers", [0, 7, 1])
-@pytest.mark.parametrize("ew,merge", LAYOUTS)
 def test_static_owner_follows_grid_stride_rule(lib, tile, max_workers, ew, merge):
     M, N, K = 1500, 1300, 128
     A = synth.int_uniform_bf16(301, (M, K))
@@ -47,8 +46,7 @@ def test_static_owner_follows_grid_stride_rule(lib, tile, max_workers, ew, merge
     assert_bit_exact(D, oracle.gemm_f64(A, B), f"static {tile}")
 
 
-@pytest.mark.parametrize("tile", ["128x128", "128x256", "256x256"])
-@pytest.mark.parametrize("ew,merge", LAYOUTS)
+@pytest.mark.parametrize("tile,ew,merge", tile_layouts(["128x128", "128x256", "256x256"]))
 def test_clc_covers_every_tile_once(lib, tile, ew, merge):
     M, N, K = 4000, 3000, 64  # many more tiles than resident workers
     A = synth.int_uniform_bf16(311, (M, K))

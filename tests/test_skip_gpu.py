@@ -6,7 +6,7 @@ import torch
 
 import oracle
 import synth
-from parity import assert_bit_exact, to_device_bf16, LAYOUTS
+from parity import assert_bit_exact, to_device_bf16, tile_layouts
 
 pytestmark = pytest.mark.gpu
 
@@ -24,10 +24,9 @@ def _causal(tiles_m, tiles_n, tm, tn):
     return (nb * tn > mb * tm + tm - 1).astype(np.uint8)  # tiles entirely above the diagonal
 
 
-@pytest.mark.parametrize("tile", ["128x128", "128x256", "256x256"])
+@pytest.mark.parametrize("tile,ew,merge", tile_layouts(["128x128", "128x256", "256x256"]))
 @pytest.mark.parametrize("sched", ["static", "clc"])
 @pytest.mark.parametrize("out", [torch.float32, torch.bfloat16])
-@pytest.mark.parametrize("ew,merge", LAYOUTS)
 def test_skipped_tiles_untouched_others_exact(lib, tile, sched, out, ew, merge):
     M, N, K = 1500, 1400, 320
     A = synth.int_uniform_bf16(701, (M, K))

@@ -91,6 +91,20 @@ def test_split_tail_random_within_bound_and_deterministic(lib, tile, M, N, K, ou
     assert_within_bound(as_f64(D), ref, S, out, f"unsplit {tile} {out}")
 
 
+@pytest.mark.parametrize("tile,M,N,K", CASES[:2])
+def test_sixteen_epilogue_warps_do_not_split(lib, tile, M, N, K):
+    # the 16-warp variants have no reduction path: the plan keeps whole tiles
+    A, B, ref = _integer_case(M, N, K)
+    need = _info(lib, M, N, K, lib.TS_OUT_F32, "clc", tile, None)["workspace_bytes"]
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    info = lib.ts_gemm_launch_info(M, N, K, lib.TS_OUT_F32, "clc", tile=tile, workspace=ws, epi_warps=16)
+    assert info["split_tiles"] == 0 and info["num_units"] == info["num_tiles"] and info["epi_warps"] == 16
+    D = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    lib.ts_gemm_bf16_ex(to_device_bf16(A), to_device_bf16(B), D, sched="clc", tile=tile, workspace=ws, epi_warps=16)
+    lib.ts_sync_and_check()
+    assert_bit_exact(D, ref, f"{tile} 16 epilogue warps, whole tiles")
+
+
 def test_split_needs_enough_k(lib):
     # 32 k-blocks cannot be split into parts of at least 32 k-blocks
     info = lib.ts_gemm_launch_info(2048, 2560, 2048, lib.TS_OUT_BF16, "static", tile="128x256")

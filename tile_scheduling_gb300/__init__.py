@@ -213,8 +213,8 @@ def ts_gemm_bf16_ex(A: torch.Tensor, B: torch.Tensor, D: torch.Tensor, sched="st
 
     Rows may be strided (the row stride becomes lda / ldb / ldd).  ``workspace``
     ("auto": a cached zero-filled buffer; None: no split tail; or a CUDA tensor)
-    lets the last partial wave of tiles be split along K.  ``epi_warps``: 4, 8
-    or 0 (automatic); ``merge``: 1 for the Merge barrier layout (A and B from
+    lets the last partial wave of tiles be split along K.  ``epi_warps``: 4, 8,
+    16 (256-column tiles) or 0 (automatic); ``merge``: 1 for the Merge barrier layout (A and B from
     separate producer warps).  Asynchronous on ``stream`` (default: torch's
     current stream)."""
     M, N, K, lda, ldb, ldd = _gemm_args(A, B, D)

@@ -8,7 +8,7 @@
 // once).  The MG = 1 variants take the Merge layout instead: A and B have a
 // producer and a full barrier each and share the empty barrier (3 * S).
 //
-// Warp roles (256 or 384 threads, one CTA per SM):
+// Warp roles (256, 384 or 640 threads, one CTA per SM):
 //   warp 0      TMA producer: per k-block, acquire an empty stage, arm the
 //               full barrier with A+B bytes, issue the two tile loads
 //               (TS "Introduction", Load-A skeleton: compute_coords, acquire,
@@ -23,13 +23,13 @@
 //               shape with a dedicated scheduler task).
 //   warp 3      barrier initialisation, then idle, the Fork row-sum task or
 //               (Merge) the TMA producer of B.
-//   warps 4..   epilogue, 4 or 8 warps: TMEM -> registers (tcgen05.ld, 32
+//   warps 4..   epilogue, 4, 8 or 16 warps: TMEM -> registers (tcgen05.ld, 32
 //               columns per load) -> fp32 or bf16 -> swizzled shared staging ->
 //               TMA store, one subtile after another (TS "Resources", subtile
 //               epilogue: load_subtile / store at column coordc_n +
 //               subtile_idx * 32, bracketed by tmem_c.wait() / release()).
-//               With 8, two warps share each TMEM lane quarter and alternate
-//               subtiles.
+//               With 8 (16), two (four) warps share each TMEM lane quarter
+//               and take its subtiles in turn.
 //
 // Every role walks the same tile sequence and advances at the same tile
 // boundary (TS "Schedules", Persistent Scheduling).  Static mode: worker w of
@@ -60,9 +60,12 @@ constexpr int kRoleWarps = 4;       // producer, MMA issuer, CLC scheduler, Fork
 constexpr int kSmemLimit = 232448;  // 227 KB: largest opt-in dynamic shared memory per CTA
 constexpr int kMaxClcDepth = 2;
 
-// EW_ epilogue warps: 4 (one per TMEM lane quarter) or 8 (two per quarter,
-// splitting the columns).  Eight hide more of the epilogue's instruction
-// latencies when the K loop is short and the epilogue bounds the tile.
+// EW_ epilogue warps: 4 (one per TMEM lane quarter), 8 or 16 (two or four per
+// quarter, splitting the columns).  More warps hide more of the epilogue's
+// instruction latencies when the K loop is short and the epilogue bounds the
+// tile.  Sixteen are built for 256-column tiles only (each warp then stores
+// one 128-byte-wide subtile per tile with bf16 output) and without the split
+// tail's reduction, which does not fit their 96 registers per thread.
 // MG_ selects the ring's barrier layout ("Pipeline Groups"): 0 is FusedMerge
 // (one producer thread loads A and B onto one full barrier per stage, 2 * S
 // barriers); 1 is Merge (a producer for A on warp 0 and one for B on warp 3,
@@ -89,9 +92,11 @@ struct GemmCfg {
     static constexpr int SUB_COLS = 128 / OUT_BYTES;   // store subtile: 128 bytes of a row
     static constexpr int NUM_SUB = BN / SUB_COLS;
     static constexpr int EPI_BUF = 32 * 128;           // one warp: 32 rows x 128 bytes
-    // staging buffers per epilogue warp: 32 KB in all either way, so the ring
-    // keeps its depth (with eight warps the two warps of a quarter alternate)
+    // staging buffers per epilogue warp: 32 KB in all with 4 or 8 warps, so
+    // the ring keeps its depth (the warps of a quarter alternate); 64 KB with
+    // 16, which costs the ring one stage (only short K loops use them)
     static constexpr int EPI_BUFS = EPI_WARPS == 4 ? 2 : 1;
+    static constexpr bool SPLIT = EPI_WARPS != 16;  // the split tail's reduction is compiled in
     static constexpr int EPI_BYTES = EPI_WARPS * EPI_BUFS * EPI_BUF;
     static constexpr int TMEM_COLS = 2 * BN;           // two accumulators
     static constexpr int BAR_BYTES = 256;
@@ -118,7 +123,7 @@ struct GemmCfg {
 
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N");
     static_assert(CG == 1 || CG == 2, "cluster size");
-    static_assert(EPI_WARPS == 4 || EPI_WARPS == 8, "epilogue warps");
+    static_assert(EPI_WARPS == 4 || EPI_WARPS == 8 || EPI_WARPS == 16, "epilogue warps");
     static_assert(MERGE == 0 || MERGE == 1, "barrier layout");
     static_assert(NUM_SUB % (EPI_WARPS / 4) == 0, "subtiles split evenly between a quarter's warps");
     static_assert(STAGES >= 2, "ring too shallow");
@@ -636,8 +641,8 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
     } else if (warp >= 4) {
         // --------------------------------------------------------- epilogue
         // Warps 4 .. 4 + EW - 1.  A warp may access TMEM lanes 32 * (warp % 4) onwards:
-        // warp 4 + j takes lane quarter q = j % 4 and, with eight warps, the
-        // subtiles s = h, h + 2, ... (h = j / 4) of that quarter's rows.
+        // warp 4 + j takes lane quarter q = j % 4 and, with 8 or 16 warps, the
+        // subtiles s = h, h + EW / 4, ... (h = j / 4) of that quarter's rows.
         constexpr int HALVES = C::EPI_WARPS / 4;
         const int q = (warp - kRoleWarps) & 3;
         const int h = (warp - kRoleWarps) >> 2;
@@ -712,7 +717,7 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
             raster(w.tile, p, mb, nb);
             const int32_t row0 = mb * C::TILE_M + static_cast<int32_t>(rank) * C::BM + 32 * q;
             const int32_t col0 = nb * BN;
-            const bool split = w.tail >= 0;
+            const bool split = C::SPLIT && w.tail >= 0;  // the host plans no split for 16 warps
             if (!w.skip) {
             int ok = 1;
             if (lane == 0) ok = wait_long(sm.tfull(acc), acc_phase, sm.abort_flag, p, WAIT_EPI_TMEM_FULL);
