@@ -479,13 +479,15 @@ def run_rows(args, ws, rank, local):
     nbytes = 4.0 * src.numel()  # 2 bytes read + 2 written per element
     runs = {"static": dict(sched="static"), "clc": dict(sched="clc"),
             "clc_oversubscribed_2x": dict(sched="clc", tiles=2 * w.rows)}
-    # chunked mode: rows cut into work tiles of at most `chunk` elements (a planning kernel maps tiles to rows)
+    # chunked mode: rows cut into work tiles of at most `chunk` elements (a planning kernel maps tiles to
+    # rows); packed mode: the rows laid end to end, every tile `chunk` of their elements
     for sched in ("clc", "static"):
-        for chunk in (16384, 32768, 65536):
-            need = ts.ts_copy_rows_launch_info(src.numel(), w.rows, sched, chunk=chunk)["workspace_bytes"]
-            runs[f"{sched}_chunk_{chunk // 1024}k"] = dict(sched=sched, chunk=chunk,
-                                                          workspace=torch.empty(need, dtype=torch.uint8,
-                                                                                device="cuda"))
+        for pack in (0, 1):
+            for chunk in (16384, 32768, 65536):
+                need = ts.ts_copy_rows_launch_info(src.numel(), w.rows, sched, chunk=chunk,
+                                                   pack=pack)["workspace_bytes"]
+                runs[f"{sched}_{'packed' if pack else 'chunk'}_{chunk // 1024}k"] = dict(
+                    sched=sched, chunk=chunk, pack=pack, workspace=torch.empty(need, dtype=torch.uint8, device="cuda"))
     times = {k: [] for k in runs}
     for k, kw in runs.items():
         for _ in range(args.warmup):
@@ -507,16 +509,19 @@ def run_rows(args, ws, rank, local):
     head = max(res, key=lambda k: res[k]["gbs"])  # the fastest configuration, named in config
     best = res[head]["gbs"]
     chunk = runs[head].get("chunk", 0)
+    pack = runs[head].get("pack", 0)
     return {"metric": "jagged int16 row copy HBM GB/s (8192 rows, log-uniform lengths), static vs CLC work queue",
             "unit": "GB/s", "value": best, **res,
             "clc_speedup_over_static": round(res["static"]["ms_median"] / res["clc"]["ms_median"], 3),
             "roofline": {"bound": "hbm", "achieved": best, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": round(best / peaks["hbm_gbs"], 4),
-                         "traffic": load_traffic("rows", f"8192 rows log-uniform {runs[head]['sched']} chunk {chunk}"),
+                         "traffic": load_traffic("rows", f"8192 rows log-uniform {runs[head]['sched']} "
+                                                         f"{'packed' if pack else 'chunk'} {chunk}"),
                          "peak_kind": f"{peaks['source']} HBM copy", "kernel": "rows_copy_kernel"},
             "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "dtype": "int16",
             "data": "synthetic", "config": {"workload": w.name, "elements": int(src.numel()), "rows": w.rows,
                                             "reported": head, "sched": runs[head]["sched"], "chunk": chunk,
+                                            "pack": pack,
                                             "l2": "inputs larger than L2 (0.5 GiB each way); no flush"}}
 
 

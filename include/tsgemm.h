@@ -311,13 +311,20 @@ typedef struct {
     int64_t chunk;              /* 0: work tile t is row t (the Dynamic Domain form below).  > 0: each row
                                    is cut into pieces of at most `chunk` elements and every piece is a work
                                    tile, in row order, so a long row no longer runs on one CTA at the end
-                                   of the queue.  A planning kernel (one CTA, same stream) reads the
-                                   offsets first.  tiles defaults to, and may not be below,
+                                   of the queue.  Two planning kernels (same stream, CTAs of 1024
+                                   rows) read the offsets first.  tiles defaults to, and may not be below,
                                    rows + ceil(n / chunk); tiles past the last piece are skipped. */
     void *workspace;            /* chunk > 0: device scratch of ts_launch_info.workspace_bytes bytes,
                                    256-byte aligned, no initialisation; launches that may overlap on the
                                    GPU need separate workspaces */
     int64_t workspace_bytes;
+    int32_t pack;               /* 1 (needs 1 <= chunk <= 2^30): the copied rows are laid end to end and
+                                   work tile t copies their elements [t * chunk, (t + 1) * chunk), so
+                                   short rows share a tile and long ones span several; every tile but
+                                   the last moves chunk elements.  tiles defaults to, and may not be
+                                   below, ceil(n / chunk).  0: chunk pieces per row as above.  Other
+                                   values are TS_ERR_INVALID_ARG.  Results do not depend on it. */
+    int32_t reserved;           /* must be 0 */
 } ts_rows_opts;
 
 /*

@@ -6,6 +6,8 @@ triple-loop oracle span several tiles and a ragged tail; the full-size
 workloads are checked against the oracle's BLAS route (whole output) or on
 sampled rows.
 """
+import functools
+
 import numpy as np
 import pytest
 import torch
@@ -105,6 +107,27 @@ def test_gemm_identity_returns_a(lib, tile):
     B = synth.one_hot_rows_bf16(K, K, np.arange(K))
     D = _run(lib, A, B, torch.float32, sched="static", tile=tile)
     assert np.array_equal(as_f64(D), oracle.bf16_to_f64(A))
+
+
+# Extreme aspect ratios: a K loop of 1024 k-blocks (every ring barrier wraps
+# its phase over a hundred times inside one tile), a single tile row 2048
+# tiles wide, and a single tile column 8193 tiles tall whose D pitch (3
+# elements) rules out TMA stores.  Integer entries keep every partial sum exact.
+@functools.lru_cache(maxsize=None)
+def _aspect_case(M, N, K):
+    A = synth.int_uniform_bf16(141, (M, K))
+    B = synth.int_uniform_bf16(142, (N, K))
+    return A, B, oracle.gemm_f64(A, B)
+
+
+@pytest.mark.parametrize("M,N,K", [(2, 300, 1 << 16), (1, 1 << 18, 64), ((1 << 20) + 7, 3, 64)])
+@pytest.mark.parametrize("tile", TILES)
+@pytest.mark.parametrize("sched", SCHEDS)
+def test_gemm_extreme_aspect_integer(lib, M, N, K, tile, sched):
+    A, B, ref = _aspect_case(M, N, K)
+    for out in OUTS:
+        D = _run(lib, A, B, out, sched=sched, tile=tile)
+        assert_bit_exact(D, ref, f"{M}x{N}x{K} {tile} {sched} {out}")
 
 
 # ---------------------------------------------------------- random inputs

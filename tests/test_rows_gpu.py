@@ -292,3 +292,128 @@ def test_rows_full_workload_chunked_bit_exact(lib, sched):
     lib.ts_copy_i16_rows(src, dst, torch.from_numpy(offsets).cuda(), sched=sched, chunk=32768)
     lib.ts_sync_and_check()
     assert torch.equal(dst, src)  # the rows tile [0, n)
+
+
+# ------------------------------------------------------------- packed mode
+# The copied rows laid end to end, every work tile `chunk` of their elements:
+# short rows share a tile (in batches of one row per thread), long rows span
+# several; the result is the same row copy.
+
+
+@pytest.mark.parametrize("sched", ["static", "clc"])
+@pytest.mark.parametrize("chunk", [1, 7, 16, 100, 4096, 1 << 20])
+@pytest.mark.parametrize("threads", [128, 512])
+def test_rows_packed_random_jagged(lib, sched, chunk, threads):
+    offsets, n = _jagged(141 + chunk, 200 if chunk > 1 else 40, 3000 if chunk > 1 else 300)
+    src = synth.int16_uniform(142, n)
+    dst0 = synth.int16_uniform(143, n)
+    got = _run(lib, src, dst0, offsets, sched, chunk=chunk, pack=1, threads=threads)
+    want, bad = oracle.copy_rows_i16(src, dst0, offsets)
+    assert bad == -1 and np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("sched", ["static", "clc"])
+@pytest.mark.parametrize("threads", [128, 1024])
+def test_rows_packed_many_tiny_rows_per_tile(lib, sched, threads):
+    # 6000 rows of 0-5 elements: a 4096-element tile holds well over a batch of rows
+    offsets, n = _jagged(151, 6000, 5)
+    src = synth.int16_uniform(152, n)
+    dst0 = synth.int16_uniform(153, n)
+    got = _run(lib, src, dst0, offsets, sched, chunk=4096, pack=1, threads=threads)
+    want, _ = oracle.copy_rows_i16(src, dst0, offsets)
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("sched", ["static", "clc"])
+@pytest.mark.parametrize("src_off,dst_off", [(0, 0), (8, 0), (3, 3), (1, 6)])
+def test_rows_packed_vector_paths(lib, sched, src_off, dst_off):
+    offsets, n = _jagged(155, 300, 700, lead=3, trail=9)
+    src = synth.int16_uniform(156, n)
+    dst0 = synth.int16_uniform(157, n)
+    got = _run(lib, src, dst0, offsets, sched, src_off=src_off, dst_off=dst_off, chunk=1000, pack=1)
+    want, _ = oracle.copy_rows_i16(src, dst0, offsets)
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("sched", ["static", "clc"])
+def test_rows_packed_tiles_visited_once_and_extra_tiles_skipped(lib, sched):
+    offsets, n = _jagged(161, 150, 2000, lead=700, trail=900)
+    rows = offsets.size - 1
+    chunk = 250
+    info = lib.ts_copy_rows_launch_info(n, rows, sched, chunk=chunk, pack=1)
+    tiles = info["num_tiles"]
+    assert tiles == -(-n // chunk) and info["workspace_bytes"] > 0
+    total = int(offsets[-1] - offsets[0])
+    assert -(-total // chunk) < tiles  # some tiles are past the last packed element
+    src = synth.int16_uniform(162, n)
+    dst0 = synth.int16_uniform(163, n)
+    trace = torch.zeros(2 * tiles, dtype=torch.int64, device="cuda")
+    got = _run(lib, src, dst0, offsets, sched, chunk=chunk, pack=1, trace=trace)
+    want, _ = oracle.copy_rows_i16(src, dst0, offsets)
+    assert np.array_equal(got, want)
+    tr = trace.view(tiles, 2).cpu().numpy()
+    if sched == "static":
+        assert np.array_equal(tr[:, 0], np.ones(tiles))
+        assert np.array_equal(tr[:, 1], oracle.static_owner(tiles, info["grid_ctas"]))
+    else:
+        ok, why = oracle.clc_coverage_ok(tr[:, 0], tr[:, 1])
+        assert ok, why
+
+
+@pytest.mark.parametrize("sched", ["static", "clc"])
+@pytest.mark.parametrize("count", [0, 1, 77, 200])
+def test_rows_packed_skip_mask_and_device_count(lib, sched, count):
+    offsets, n = _jagged(171, 200, 1500)
+    src = synth.int16_uniform(172, n)
+    dst0 = synth.int16_uniform(173, n)
+    skip = (synth.splitmix64(174, 200) % np.uint64(4) == 0).astype(np.uint8)
+    rd = torch.tensor([count], dtype=torch.int64, device="cuda")
+    got = _run(lib, src, dst0, offsets, sched, chunk=300, pack=1, rows_device=rd,
+               skip_rows=torch.from_numpy(skip).cuda())
+    want, _ = oracle.copy_rows_i16(src, dst0, offsets, rows=count, skip=skip)
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("sched", ["static", "clc"])
+def test_rows_packed_bad_bounds_reported(lib, sched):
+    n = 1000
+    offsets = np.array([0, 100, 300, 600, 1200], dtype=np.int64)  # row 3 runs past n
+    src = synth.int16_uniform(181, n)
+    dst0 = synth.int16_uniform(182, n)
+    sbuf = torch.from_numpy(src).cuda()
+    dbuf = torch.from_numpy(dst0.copy()).cuda()
+    lib.ts_copy_i16_rows(sbuf, dbuf, torch.from_numpy(offsets).cuda(), sched=sched, chunk=64, pack=1)
+    with pytest.raises(lib.TsError) as ei:
+        lib.ts_sync_and_check()
+    assert ei.value.status == lib.TS_ERR_INVALID_ARG and "bounds" in ei.value.detail
+    want, first_bad = oracle.copy_rows_i16(src, dst0, offsets)
+    assert first_bad == 3 and np.array_equal(dbuf.cpu().numpy(), want)
+
+
+def test_rows_packed_overlapping_rows_need_more_tiles(lib):
+    # rows 0 and 3 are both [0, n) (row 2, which runs backwards, is skipped):
+    # 2n packed elements need 20 tiles, above the default ceil(n / chunk) = 10
+    n, chunk = 1000, 100
+    src = torch.from_numpy(synth.int16_uniform(191, n)).cuda()
+    off = torch.tensor([0, n, n, 0, n], dtype=torch.int64, device="cuda")
+    skip = torch.tensor([0, 0, 1, 0], dtype=torch.uint8, device="cuda")
+    dst = torch.zeros(n, dtype=torch.int16, device="cuda")
+    lib.ts_copy_i16_rows(src, dst, off, sched="clc", chunk=chunk, pack=1, skip_rows=skip)
+    with pytest.raises(lib.TsError) as ei:
+        lib.ts_sync_and_check()
+    assert ei.value.status == lib.TS_ERR_INVALID_ARG and "pieces" in ei.value.detail
+    dst = torch.zeros(n, dtype=torch.int16, device="cuda")
+    lib.ts_copy_i16_rows(src, dst, off, sched="clc", chunk=chunk, pack=1, skip_rows=skip, tiles=20)
+    lib.ts_sync_and_check()
+    assert torch.equal(dst, src)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("sched", ["static", "clc"])
+def test_rows_full_workload_packed_bit_exact(lib, sched):
+    src_h, offsets = synth.ROWS.inputs()
+    src = torch.from_numpy(src_h).cuda()
+    dst = torch.zeros_like(src)
+    lib.ts_copy_i16_rows(src, dst, torch.from_numpy(offsets).cuda(), sched=sched, chunk=32768, pack=1)
+    lib.ts_sync_and_check()
+    assert torch.equal(dst, src)  # the rows tile [0, n)

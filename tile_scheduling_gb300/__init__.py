@@ -63,7 +63,7 @@ class RowsOpts(ctypes.Structure):
     _fields_ = [("tiles", ctypes.c_int64), ("rows_device", ctypes.c_void_p), ("skip_rows", ctypes.c_void_p),
                 ("threads", ctypes.c_int32), ("max_workers", ctypes.c_int32), ("timeout_s", ctypes.c_double),
                 ("trace", ctypes.c_void_p), ("chunk", ctypes.c_int64), ("workspace", ctypes.c_void_p),
-                ("workspace_bytes", ctypes.c_int64)]
+                ("workspace_bytes", ctypes.c_int64), ("pack", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 class GemmProtocol(ctypes.Structure):
@@ -379,10 +379,11 @@ def ts_copy_i16_ptr(src: int, dst: int, n: int, stream=None) -> int:
 
 
 def _rows_opts(tiles=0, rows_device=None, skip_rows=None, threads=0, max_workers=0, timeout_s=0.0, trace=None,
-               chunk=0, workspace=None):
+               chunk=0, workspace=None, pack=0):
     o = RowsOpts()
     o.tiles = int(tiles)
     o.chunk = int(chunk)
+    o.pack = int(pack)
     if workspace is not None:
         if not workspace.is_cuda or not workspace.is_contiguous():
             raise TypeError("workspace must be a contiguous CUDA tensor")
@@ -402,7 +403,7 @@ def _rows_opts(tiles=0, rows_device=None, skip_rows=None, threads=0, max_workers
 
 
 def ts_copy_rows_launch_info(n: int, rows: int, sched="clc", **opts) -> dict:
-    o = _rows_opts(**{k: v for k, v in opts.items() if k in ("tiles", "threads", "max_workers", "chunk")})
+    o = _rows_opts(**{k: v for k, v in opts.items() if k in ("tiles", "threads", "max_workers", "chunk", "pack")})
     info = LaunchInfo()
     _check(_lib.ts_copy_rows_launch_info(int(n), int(rows), _sched(sched), ctypes.byref(o), ctypes.byref(info)))
     return {f: getattr(info, f) for f, _ in LaunchInfo._fields_}
@@ -410,15 +411,16 @@ def ts_copy_rows_launch_info(n: int, rows: int, sched="clc", **opts) -> dict:
 
 def ts_copy_i16_rows(src: torch.Tensor, dst: torch.Tensor, offsets: torch.Tensor, rows=None, sched="clc", tiles=0,
                      rows_device=None, skip_rows=None, threads=0, max_workers=0, timeout_s=0.0, trace=None,
-                     chunk=0, workspace=None, stream=None) -> None:
+                     chunk=0, workspace=None, pack=0, stream=None) -> None:
     """Copy rows [offsets[r], offsets[r+1]) of a jagged int16 array through a work queue.
 
     src and dst: contiguous int16 CUDA tensors of equal size n; offsets: int64
     CUDA tensor of rows + 1 entries (rows defaults to offsets.numel() - 1).
     Tiles past the row count (tiles > rows, or rows_device below rows) and rows
     marked in skip_rows copy nothing but still take part in the queue.
-    chunk > 0 cuts rows into work tiles of at most chunk elements; its
-    workspace is allocated here unless one is passed."""
+    chunk > 0 cuts rows into work tiles of at most chunk elements; with
+    pack=1 the rows are laid end to end and every tile copies chunk of their
+    elements.  The planning workspace is allocated here unless one is passed."""
     for t, name in ((src, "src"), (dst, "dst")):
         if t.dtype != torch.int16 or not t.is_cuda or not t.is_contiguous():
             raise TypeError(f"{name} must be a contiguous int16 CUDA tensor")
@@ -433,10 +435,11 @@ def ts_copy_i16_rows(src: torch.Tensor, dst: torch.Tensor, offsets: torch.Tensor
     if skip_rows is not None and skip_rows.numel() < rows:
         raise ValueError("skip_rows needs one byte per row")
     if chunk and workspace is None:
-        need = ts_copy_rows_launch_info(src.numel(), rows, sched, tiles=tiles, chunk=chunk)["workspace_bytes"]
+        need = ts_copy_rows_launch_info(src.numel(), rows, sched, tiles=tiles, chunk=chunk,
+                                        pack=pack)["workspace_bytes"]
         workspace = torch.empty(need, dtype=torch.uint8, device=src.device)
-    o = _rows_opts(tiles, rows_device, skip_rows, threads, max_workers, timeout_s, trace, chunk, workspace)
-    min_tiles = int(rows) + (-(-src.numel() // int(chunk)) if chunk else 0)
+    o = _rows_opts(tiles, rows_device, skip_rows, threads, max_workers, timeout_s, trace, chunk, workspace, pack)
+    min_tiles = (0 if pack else int(rows)) + (-(-src.numel() // int(chunk)) if chunk else 0)
     if trace is not None and trace.numel() < 2 * max(int(tiles), min_tiles):
         raise ValueError("trace needs 2 * tiles entries")
     _check(_lib.ts_copy_i16_rows(ctypes.c_void_p(src.data_ptr()), ctypes.c_void_p(dst.data_ptr()), src.numel(),

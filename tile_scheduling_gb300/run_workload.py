@@ -31,6 +31,7 @@ def main(argv=None):
     ap.add_argument("--sched", default=None, choices=["static", "clc"])
     ap.add_argument("--tile", default=None)
     ap.add_argument("--chunk", type=int, default=0, help="rows: elements per work tile (0: one tile per row)")
+    ap.add_argument("--pack", type=int, default=0, choices=[0, 1], help="rows: lay the rows end to end (with --chunk)")
     a = ap.parse_args(argv)
     if a.workload == "copy":
         src = torch.from_numpy(synth.int16_uniform(synth.COPY_SEED, synth.COPY_N)).cuda()
@@ -48,12 +49,13 @@ def main(argv=None):
         sched = a.sched or "clc"
         ws = None
         if a.chunk:
-            need = ts.ts_copy_rows_launch_info(src.numel(), synth.ROWS.rows, sched, chunk=a.chunk)["workspace_bytes"]
+            need = ts.ts_copy_rows_launch_info(src.numel(), synth.ROWS.rows, sched, chunk=a.chunk,
+                                               pack=a.pack)["workspace_bytes"]
             ws = torch.empty(need, dtype=torch.uint8, device="cuda")
         for _ in range(a.launches):
-            ts.ts_copy_i16_rows(src, dst, off, sched=sched, chunk=a.chunk, workspace=ws)
+            ts.ts_copy_i16_rows(src, dst, off, sched=sched, chunk=a.chunk, workspace=ws, pack=a.pack)
         ts.ts_sync_and_check()
-        print(f"{synth.ROWS.name}: {sched} chunk {a.chunk} x{a.launches} ok")
+        print(f"{synth.ROWS.name}: {sched} chunk {a.chunk} pack {a.pack} x{a.launches} ok")
         return 0
     w = GEMMS[a.workload]
     A_bits, B_bits = w.inputs()
