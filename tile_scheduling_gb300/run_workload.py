@@ -32,6 +32,7 @@ def main(argv=None):
     ap.add_argument("--tile", default=None)
     ap.add_argument("--chunk", type=int, default=0, help="rows: elements per work tile (0: one tile per row)")
     ap.add_argument("--pack", type=int, default=0, choices=[0, 1], help="rows: lay the rows end to end (with --chunk)")
+    ap.add_argument("--merge", type=int, default=0, choices=[0, 1], help="GEMM: the Merge barrier layout")
     a = ap.parse_args(argv)
     if a.workload == "copy":
         src = torch.from_numpy(synth.int16_uniform(synth.COPY_SEED, synth.COPY_N)).cuda()
@@ -66,9 +67,9 @@ def main(argv=None):
     sched = a.sched or w.sched[-1]
     tile = a.tile or w.tile
     for _ in range(a.launches):
-        ts.ts_gemm_bf16_ex(A, B, D, sched=sched, tile=tile)
+        ts.ts_gemm_bf16_ex(A, B, D, sched=sched, tile=tile, merge=a.merge)
     ts.ts_sync_and_check()
-    print(f"{w.name}: {sched} {tile} x{a.launches} ok")
+    print(f"{w.name}: {sched} {tile} merge {a.merge} x{a.launches} ok")
     return 0
 
 
