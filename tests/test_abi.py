@@ -95,5 +95,13 @@ def test_row_copy_argument_errors_need_no_gpu(ts):
     # chunked: tiles may not be below rows + ceil(n / chunk) = 2 + 3
     assert ts.ts_copy_i16_rows_ptr(4096, 8192, 9, 64, 2, chunk=4, tiles=4, stream=0) == E
     assert "ceil(n / chunk)" in ts.ts_last_error_detail()
+    # packed: a chunk in [1, 2^30] is required, pack is 0 or 1, and tiles may not be
+    # below ceil(n / chunk) = 3 (the rows do not count)
+    assert ts.ts_copy_i16_rows_ptr(4096, 8192, 9, 64, 2, pack=1, stream=0) == E
+    assert "pack" in ts.ts_last_error_detail()
+    assert ts.ts_copy_i16_rows_ptr(4096, 8192, 9, 64, 2, chunk=(1 << 30) + 1, pack=1, stream=0) == E
+    assert ts.ts_copy_i16_rows_ptr(4096, 8192, 9, 64, 2, chunk=4, pack=2, stream=0) == E
+    assert ts.ts_copy_i16_rows_ptr(4096, 8192, 9, 64, 2, chunk=4, pack=1, tiles=2, stream=0) == E
+    assert "ceil(n / chunk)" in ts.ts_last_error_detail()
     # an empty queue launches nothing
     assert ts.ts_copy_i16_rows_ptr(0, 0, 0, 0, 0, stream=0) == ts.TS_OK
