@@ -296,9 +296,10 @@ ts_status ts_copy_i16(const int16_t *src, int16_t *dst, int64_t n, void *stream)
 
 /* Optional knobs for ts_copy_i16_rows; zero means "default" for every field. */
 typedef struct {
-    int64_t tiles;              /* work tiles launched, >= rows; 0 = rows.  Tiles t >= the row
-                                   count copy nothing but still take part in the work queue
-                                   (the oversubscribed copy queue). */
+    int64_t tiles;              /* work tiles launched; 0 = the mode's minimum (rows; with a chunk,
+                                   see chunk and pack), which it may not be below.  Tiles t >= the
+                                   row count (or past the last piece) copy nothing but still take
+                                   part in the work queue (the oversubscribed copy queue). */
     const int64_t *rows_device; /* device int64 or NULL: the row count, read once per CTA on the
                                    device and clamped to [0, rows].  Lets one launch shape (tiles,
                                    rows as capacities) serve a count that a previous kernel wrote. */
@@ -357,16 +358,19 @@ typedef struct {
  *   rows      row count (upper bound when rows_device is given), >= 0.
  * A CLC response that does not arrive within timeout_s is reported as
  * TS_ERR_TIMEOUT by ts_sync_and_check; the CTA then stops taking tiles.  In
- * chunked mode, rows that overlap can need more pieces than `tiles`: the rows
- * whose pieces do not fit are reported as TS_ERR_INVALID_ARG by
- * ts_sync_and_check (the pieces that fit are copied).
+ * chunked or packed mode, rows that overlap can need more tiles than `tiles`:
+ * the rows whose pieces do not fit are reported as TS_ERR_INVALID_ARG by
+ * ts_sync_and_check (the pieces that fit are copied).  The planning kernels
+ * and the copy kernel are launched as programmatic dependents of the kernel
+ * before them in the stream: each may be scheduled during that kernel's tail
+ * and reads no memory before its writes are visible.
  */
 ts_status ts_copy_i16_rows(const int16_t *src, int16_t *dst, int64_t n, const int64_t *offsets, int64_t rows,
                            int32_t sched, const ts_rows_opts *opts, void *stream);
 
 /* The launch ts_copy_i16_rows would make (host only): num_tiles = num_units =
  * tiles, grid_ctas = workers = CTAs launched, resident = CTAs that fit at once,
- * workspace_bytes = the workspace chunked mode needs (0 otherwise). */
+ * workspace_bytes = the workspace chunked and packed modes need (0 otherwise). */
 ts_status ts_copy_rows_launch_info(int64_t n, int64_t rows, int32_t sched, const ts_rows_opts *opts,
                                    ts_launch_info *info);
 
