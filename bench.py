@@ -663,62 +663,54 @@ def run_contended(args, ws, rank, local):
 
 
 def run_e2e(args, ts, A_bits, B_bits, M, N, K, ws):
-    """The GEMM through the public call with host buffers, copies inside the timed region.
+    """The GEMM through the public call on host buffers, copies inside the timed region.
 
-    Every step copies its A and B from pinned host memory, runs the GEMM and reads D
-    back to pinned host memory.  Steps are double-buffered over three streams, so the
-    copy-in of step i+1 and the copy-out of step i-1 overlap the GEMM of step i."""
+    Every step is one ts_gemm_bf16_host call: it copies A and B from pinned host memory into
+    device buffers, runs the GEMM and copies D back to pinned host memory, all on one stream.
+    Consecutive steps go round-robin to three streams, each with its own device buffers, so one
+    step's copies overlap the others' GEMMs and copies."""
     import torch
 
+    nbuf = 3
     A_h = torch.from_numpy(A_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
     B_h = torch.from_numpy(B_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
-    D_h = [torch.empty((M, N), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
-    A = [torch.empty((M, K), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
-    B = [torch.empty((N, K), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
-    D = [torch.empty((M, N), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
-    s_in, s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
-    ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("in", "comp", "out")}
-    used = [False, False]
+    D_h = [torch.empty((M, N), dtype=torch.bfloat16).pin_memory() for _ in range(nbuf)]
+    A = [torch.empty((M, K), dtype=torch.bfloat16, device="cuda") for _ in range(nbuf)]
+    B = [torch.empty((N, K), dtype=torch.bfloat16, device="cuda") for _ in range(nbuf)]
+    D = [torch.empty((M, N), dtype=torch.bfloat16, device="cuda") for _ in range(nbuf)]
+    streams = [torch.cuda.Stream() for _ in range(nbuf)]
+    # calls on different streams overlap, so each stream gets its own split-tail workspace (zeroed)
+    need = ts.ts_gemm_launch_info(M, N, K, ts.TS_OUT_BF16, args.sched, tile=args.tile,
+                                  workspace=None)["workspace_bytes"]
+    wsp = [torch.zeros(max(need, 256), dtype=torch.uint8, device="cuda") for _ in range(nbuf)]
 
     def step(i):
-        b = i % 2
-        if used[b]:
-            s_in.wait_event(ev["comp"][b])   # the GEMM two steps back has read A[b], B[b]
-            s_comp.wait_event(ev["out"][b])  # and its D[b] has been read back
-        with torch.cuda.stream(s_in):
-            A[b].copy_(A_h, non_blocking=True)
-            B[b].copy_(B_h, non_blocking=True)
-            ev["in"][b].record(s_in)
-        s_comp.wait_event(ev["in"][b])
-        ts.ts_gemm_bf16_ex(A[b], B[b], D[b], sched=args.sched, tile=args.tile, stream=s_comp)
-        ev["comp"][b].record(s_comp)
-        s_out.wait_event(ev["comp"][b])
-        with torch.cuda.stream(s_out):
-            D_h[b].copy_(D[b], non_blocking=True)
-            ev["out"][b].record(s_out)
-        used[b] = True
+        b = i % nbuf
+        ts.ts_gemm_bf16_host(A_h, B_h, D_h[b], A[b], B[b], D[b], sched=args.sched, tile=args.tile,
+                             workspace=wsp[b], stream=streams[b])
 
-    for i in range(2):
+    for i in range(nbuf):
         step(i)
     torch.cuda.synchronize()
     steps = max(3, min(args.steps, args.e2e_steps))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(s_in)
-    s_comp.wait_event(e0)
-    s_out.wait_event(e0)
+    e0.record(streams[0])
+    for st in streams[1:]:
+        st.wait_event(e0)
     for i in range(steps):
         step(i)
-    s_in.wait_stream(s_comp)
-    s_in.wait_stream(s_out)
-    e1.record(s_in)
+    for st in streams[1:]:
+        streams[0].wait_stream(st)
+    e1.record(streams[0])
     torch.cuda.synchronize()
     ms = reduce_times([e0.elapsed_time(e1)], "max")[0]
     ts.ts_sync_and_check()
     flops = 2.0 * M * N * K
     return {"value": round(ws * flops * steps / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
             "h2d_bytes_per_step": int(A_h.numel() * 2 + B_h.numel() * 2), "d2h_bytes_per_step": int(D_h[0].numel() * 2),
-            "steps": steps, "ms_per_step": round(ms / steps, 4),
-            "pipelining": "double-buffered: copy-in, GEMM and copy-out of consecutive steps overlap on 3 streams"}
+            "steps": steps, "ms_per_step": round(ms / steps, 4), "call": "ts_gemm_bf16_host",
+            "pipelining": f"one call per step (copy in, GEMM, copy out on one stream); steps round-robin over "
+                          f"{nbuf} streams and buffer sets"}
 
 
 # -------------------------------------------------------- CPU oracle arm

@@ -203,6 +203,27 @@ ts_status ts_gemm_bf16_ex(const void *A, const void *B, void *D, int64_t M, int6
                           int32_t out_dtype, int32_t sched, const ts_gemm_opts *opts, void *stream);
 
 /*
+ * ts_gemm_bf16_host -- ts_gemm_bf16_ex on operands in host memory: copies A and
+ * B from host memory into the caller's device buffers, runs the GEMM on them
+ * and copies D back to host memory, all queued on `stream` in that order.
+ *
+ *   A_host, B_host, D_host  host arrays laid out as the device ones (row pitches
+ *                           lda, ldb, ldd of opts, or packed rows); page-locked
+ *                           memory makes the copies asynchronous, pageable memory
+ *                           makes the calling thread wait for them
+ *   A_dev, B_dev, D_dev     device buffers the caller owns, as for ts_gemm_bf16_ex
+ * NULL buffers and the problem's sizes and options (as ts_gemm_launch_info
+ * checks them) are rejected before anything is copied; the device pointers'
+ * alignment and overlap are checked by the GEMM call, after A and B have been
+ * queued for copying (D is then not copied back).  Results and the other
+ * arguments are as for ts_gemm_bf16_ex.  The host buffers must stay valid
+ * until the stream reaches the copies.
+ */
+ts_status ts_gemm_bf16_host(const void *A_host, const void *B_host, void *D_host, void *A_dev, void *B_dev,
+                            void *D_dev, int64_t M, int64_t N, int64_t K, int32_t out_dtype, int32_t sched,
+                            const ts_gemm_opts *opts, void *stream);
+
+/*
  * ts_gemm_bf16_grouped -- a grouped GEMM whose groups differ in K:
  *
  *   D[g][i][j] = sum_{k_offsets[g] <= k < k_offsets[g+1]} A[i][k] * B[j][k],   0 <= g < groups

@@ -49,6 +49,8 @@ def test_argument_errors_need_no_gpu(ts):
     assert ts.ts_gemm_bf16_ptr(0, 0, 0, 4, 4, 8, ts.TS_OUT_F32, stream=0, lda=4) == ts.TS_ERR_INVALID_ARG
     assert ts.ts_gemm_bf16_ptr(0, 0, 0, 4, 4, 8, ts.TS_OUT_F32, stream=0, epi_warps=6) == ts.TS_ERR_INVALID_ARG
     assert "epi_warps" in ts.ts_last_error_detail()
+    assert ts._lib.ts_gemm_bf16_host(None, None, None, None, None, None, 4, 4, 8, ts.TS_OUT_F32, 0, None,
+                                     None) == ts.TS_ERR_INVALID_ARG  # NULL buffers, before any CUDA call
     assert ts.ts_gemm_bf16_ptr(0, 0, 0, 4, 4, 8, ts.TS_OUT_F32, stream=0, merge=2) == ts.TS_ERR_INVALID_ARG
     assert "merge" in ts.ts_last_error_detail()
     # the Merge layout's B producer and the Fork row-sum task would both need warp 3

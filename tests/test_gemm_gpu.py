@@ -130,6 +130,40 @@ def test_gemm_extreme_aspect_integer(lib, M, N, K, tile, sched):
         assert_bit_exact(D, ref, f"{M}x{N}x{K} {tile} {sched} {out}")
 
 
+# Host buffers: the copies in, the GEMM and the copy out in one call.
+@pytest.mark.parametrize("pinned", [True, False])
+@pytest.mark.parametrize("M,N,K", [(600, 520, 328), (1, 300, 64), (257, 1, 72), (300, 260, 0)])
+@pytest.mark.parametrize("out", OUTS)
+def test_gemm_host_buffers_integer_exact(lib, pinned, M, N, K, out):
+    A_bits = synth.int_uniform_bf16(151, (M, K))
+    B_bits = synth.int_uniform_bf16(152, (N, K))
+    A_h = torch.from_numpy(A_bits.view(np.int16)).view(torch.bfloat16)
+    B_h = torch.from_numpy(B_bits.view(np.int16)).view(torch.bfloat16)
+    D_h = torch.full((M, N), float("nan"), dtype=out)
+    if pinned:
+        A_h, B_h, D_h = A_h.pin_memory(), B_h.pin_memory(), D_h.pin_memory()
+    A = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
+    B = torch.empty((N, K), dtype=torch.bfloat16, device="cuda")
+    D = torch.empty((M, N), dtype=out, device="cuda")
+    lib.ts_gemm_bf16_host(A_h, B_h, D_h, A, B, D, sched="clc")
+    torch.cuda.synchronize()
+    lib.ts_sync_and_check()
+    assert_bit_exact(D_h, oracle.gemm_f64(A_bits, B_bits), f"host buffers {M}x{N}x{K} {out} pinned={pinned}")
+
+
+def test_gemm_host_buffers_checks_before_copying(lib):
+    A_h = torch.ones((64, 64), dtype=torch.bfloat16)
+    B_h = torch.ones((64, 64), dtype=torch.bfloat16)
+    D_h = torch.full((64, 64), 7.0, dtype=torch.float32)
+    A = torch.zeros((64, 64), dtype=torch.bfloat16, device="cuda")
+    B = torch.zeros((64, 64), dtype=torch.bfloat16, device="cuda")
+    D = torch.zeros((64, 64), dtype=torch.float32, device="cuda")
+    with pytest.raises(lib.TsError):
+        lib.ts_gemm_bf16_host(A_h, B_h, D_h, A, B, D, tile="128x128", epi_warps=16)  # no such variant
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(A) == 0 and torch.all(D_h == 7.0)  # nothing was copied either way
+
+
 # ---------------------------------------------------------- random inputs
 @pytest.mark.parametrize("M,N,K", [(1, 1, 8), (127, 129, 64), (129, 127, 72), (255, 255, 200), (1, 255, 8),
                                    (255, 1, 136), (384, 640, 1024)])

@@ -80,6 +80,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     P, I32, I64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
     lib.ts_gemm_bf16.argtypes = [P, P, P, I64, I64, I64, I32, I32, P]
     lib.ts_gemm_bf16_ex.argtypes = [P, P, P, I64, I64, I64, I32, I32, ctypes.POINTER(GemmOpts), P]
+    lib.ts_gemm_bf16_host.argtypes = [P, P, P, P, P, P, I64, I64, I64, I32, I32, ctypes.POINTER(GemmOpts), P]
     lib.ts_gemm_launch_info.argtypes = [I64, I64, I64, I32, I32, ctypes.POINTER(GemmOpts),
                                         ctypes.POINTER(LaunchInfo)]
     lib.ts_gemm_bf16_checked_noalloc.argtypes = [P, P, P, I64, I64, I64, I32, I32, P, P]
@@ -227,6 +228,26 @@ def ts_gemm_bf16_ex(A: torch.Tensor, B: torch.Tensor, D: torch.Tensor, sched="st
     _check(_lib.ts_gemm_bf16_ex(ctypes.c_void_p(A.data_ptr()), ctypes.c_void_p(B.data_ptr()),
                                 ctypes.c_void_p(D.data_ptr()), M, N, K, _OUT[D.dtype], _sched(sched),
                                 ctypes.byref(o), _stream_handle(stream)))
+
+
+def ts_gemm_bf16_host(A_host: torch.Tensor, B_host: torch.Tensor, D_host: torch.Tensor, A: torch.Tensor,
+                      B: torch.Tensor, D: torch.Tensor, sched="static", tile="auto", workspace="auto", epi_warps=0,
+                      stream=None) -> None:
+    """D_host = A_host @ B_host.T through the device buffers A, B, D: the copies in, the GEMM and the
+    copy out are queued on ``stream`` (page-locked host tensors keep them asynchronous).  All six
+    tensors are contiguous, each host tensor shaped and typed as its device one."""
+    for h, d, name in ((A_host, A, "A"), (B_host, B, "B"), (D_host, D, "D")):
+        if h.is_cuda or not h.is_contiguous() or not d.is_contiguous():
+            raise TypeError(f"{name}_host must be a contiguous host tensor and {name} a contiguous CUDA tensor")
+        if h.shape != d.shape or h.dtype != d.dtype:
+            raise ValueError(f"{name}_host and {name} differ in shape or dtype")
+    M, N, K, _, _, _ = _gemm_args(A, B, D)
+    workspace = _resolve_workspace(M, N, K, _OUT[D.dtype], sched, workspace, 0, tile=tile)
+    o = _opts(tile=tile, workspace=workspace, epi_warps=epi_warps)
+    _check(_lib.ts_gemm_bf16_host(ctypes.c_void_p(A_host.data_ptr()), ctypes.c_void_p(B_host.data_ptr()),
+                                  ctypes.c_void_p(D_host.data_ptr()), ctypes.c_void_p(A.data_ptr()),
+                                  ctypes.c_void_p(B.data_ptr()), ctypes.c_void_p(D.data_ptr()), M, N, K,
+                                  _OUT[D.dtype], _sched(sched), ctypes.byref(o), _stream_handle(stream)))
 
 
 def ts_gemm_bf16(A: torch.Tensor, B: torch.Tensor, D: torch.Tensor, sched="static", stream=None) -> None:

@@ -545,4 +545,34 @@ ts_status ts_gemm_bf16(const void *A, const void *B, void *D, int64_t M, int64_t
     return ts_gemm_bf16_ex(A, B, D, M, N, K, out_dtype, sched, nullptr, stream);
 }
 
+ts_status ts_gemm_bf16_host(const void *A_host, const void *B_host, void *D_host, void *A_dev, void *B_dev,
+                            void *D_dev, int64_t M, int64_t N, int64_t K, int32_t out_dtype, int32_t sched,
+                            const ts_gemm_opts *opts, void *stream) {
+    using namespace ts;
+    if (M < 0 || N < 0 || K < 0) return ts_gemm_bf16_ex(A_dev, B_dev, D_dev, M, N, K, out_dtype, sched, opts, stream);
+    const int64_t lda = opts && opts->lda ? opts->lda : K, ldb = opts && opts->ldb ? opts->ldb : K;
+    const int64_t ldd = opts && opts->ldd ? opts->ldd : N;
+    const int64_t esize = out_dtype == TS_OUT_F32 ? 4 : 2;
+    // the bytes the device buffers span: every row at its pitch, the last one to its end
+    const int64_t a_bytes = M > 0 && K > 0 ? ((M - 1) * lda + K) * 2 : 0;
+    const int64_t b_bytes = N > 0 && K > 0 ? ((N - 1) * ldb + K) * 2 : 0;
+    const int64_t d_bytes = M > 0 && N > 0 ? ((M - 1) * ldd + N) * esize : 0;
+    if ((a_bytes && (!A_host || !A_dev)) || (b_bytes && (!B_host || !B_dev)) || (d_bytes && (!D_host || !D_dev)))
+        return fail(TS_ERR_INVALID_ARG, "a host or device buffer is NULL");
+    // sizes and options are checked before anything is copied
+    ts_launch_info info;
+    ts_status s = ts_gemm_launch_info(M, N, K, out_dtype, sched, opts, &info);
+    if (s != TS_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaSuccess;
+    if (a_bytes) e = cudaMemcpyAsync(A_dev, A_host, static_cast<size_t>(a_bytes), cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess && b_bytes)
+        e = cudaMemcpyAsync(B_dev, B_host, static_cast<size_t>(b_bytes), cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return cuda_fail(e, "copy of A or B to the device");
+    s = ts_gemm_bf16_ex(A_dev, B_dev, D_dev, M, N, K, out_dtype, sched, opts, stream);
+    if (s != TS_OK) return s;
+    if (d_bytes) e = cudaMemcpyAsync(D_host, D_dev, static_cast<size_t>(d_bytes), cudaMemcpyDeviceToHost, st);
+    return e == cudaSuccess ? TS_OK : cuda_fail(e, "copy of D to the host");
+}
+
 }  // extern "C"
