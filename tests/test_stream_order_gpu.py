@@ -70,3 +70,72 @@ def test_copy_then_gemm_then_copy(lib):
     want = oracle.bf16_rne(oracle.gemm_f64(A, B))
     assert np.array_equal(bf16_bits(D), want)
     assert np.array_equal(out.cpu().numpy().view(np.uint16).reshape(M, N), want)
+
+
+@pytest.mark.parametrize("pack", [0, 1])
+def test_row_copy_between_gemms_with_offsets_written_just_before(lib, pack):
+    # GEMM -> (a kernel writes the offsets) -> planned row copy of the GEMM's output -> GEMM on the copy:
+    # the planning kernels and the copy are programmatic dependents and must see every earlier write
+    M, N, K = 512, 512, 128
+    A = synth.int_uniform_bf16(931, (M, K))
+    B = synth.int_uniform_bf16(932, (N, K))
+    E = synth.int_uniform_bf16(933, (256, N))
+    D = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    D2 = torch.zeros((M, N), dtype=torch.bfloat16, device="cuda")
+    D3 = torch.full((M, 256), float("nan"), dtype=torch.float32, device="cuda")
+    lengths = (synth.splitmix64(934, M) % np.uint64(2 * N)).astype(np.int64)
+    bounds = np.minimum(np.concatenate([[0], np.cumsum(lengths)]), M * N).astype(np.int64)
+    bounds[-1] = M * N  # the rows cover the whole output
+    off = torch.zeros(M + 1, dtype=torch.int64, device="cuda")
+    ws = torch.empty(lib.ts_copy_rows_launch_info(M * N, M, "clc", chunk=4096, pack=pack)["workspace_bytes"],
+                     dtype=torch.uint8, device="cuda")
+    for _ in range(3):
+        off.zero_()
+        lib.ts_gemm_bf16_ex(to_device_bf16(A), to_device_bf16(B), D, sched="clc")
+        off.copy_(torch.from_numpy(bounds).cuda(non_blocking=False))
+        lib.ts_copy_i16_rows(D.view(torch.int16).reshape(-1), D2.view(torch.int16).reshape(-1), off, sched="clc",
+                             chunk=4096, pack=pack, workspace=ws)
+        lib.ts_gemm_bf16_ex(D2, to_device_bf16(E), D3, sched="static")
+    lib.ts_sync_and_check()
+    d_bits = oracle.bf16_rne(oracle.gemm_f64(A, B))
+    assert np.array_equal(bf16_bits(D2), d_bits)
+    assert_bit_exact(D3, oracle.gemm_f64(d_bits, E), f"row copy between GEMMs, pack {pack}")
+
+
+def test_cuda_graph_replay(lib):
+    # a GEMM, a copy and a planned row copy captured once and replayed with new inputs
+    M, N, K = 512, 768, 192
+    B = synth.int_uniform_bf16(941, (N, K))
+    d_b = to_device_bf16(B)
+    A_in = torch.zeros((M, K), dtype=torch.bfloat16, device="cuda")
+    D = torch.zeros((M, N), dtype=torch.bfloat16, device="cuda")
+    out = torch.zeros(M * N, dtype=torch.int16, device="cuda")
+    rows_out = torch.zeros(M * N, dtype=torch.int16, device="cuda")
+    off = torch.from_numpy(np.arange(0, M * N + 1, N, dtype=np.int64)).cuda()
+    ws = torch.empty(lib.ts_copy_rows_launch_info(M * N, M, "clc", chunk=1000)["workspace_bytes"], dtype=torch.uint8,
+                     device="cuda")
+    gemm_ws = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
+
+    def step():
+        lib.ts_gemm_bf16_ex(A_in, d_b, D, sched="clc", workspace=gemm_ws)
+        lib.ts_copy_i16(D.view(torch.int16).reshape(-1), out)
+        lib.ts_copy_i16_rows(out, rows_out, off, sched="clc", chunk=1000, workspace=ws)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()  # first calls outside the capture: per-device set-up
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for r in range(3):
+        A = synth.int_uniform_bf16(950 + r, (M, K))
+        A_in.copy_(to_device_bf16(A))
+        g.replay()
+        torch.cuda.synchronize()
+        lib.ts_sync_and_check()
+        want = oracle.bf16_rne(oracle.gemm_f64(A, B))
+        assert np.array_equal(bf16_bits(D), want), f"replay {r}: GEMM"
+        assert np.array_equal(rows_out.cpu().numpy().view(np.uint16).reshape(M, N), want), f"replay {r}: copies"
