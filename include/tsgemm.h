@@ -310,8 +310,9 @@ ts_status ts_gemm_bf16_checked_noalloc(const void *A, const void *B, void *D, in
  *   n         element count >= 0.
  * 32-byte vectors are used when src and dst share their offset modulo 32
  * bytes, 16-byte vectors when they share it modulo 16 (elements before the
- * first aligned one and after the last whole vector one by one); other
- * alignments take an element-wise path with the same result.
+ * first aligned one and after the last whole vector one by one); otherwise
+ * every aligned 16-byte dst vector is assembled from two aligned 16-byte
+ * source vectors inside src.  Every path gives the same result.
  */
 ts_status ts_copy_i16(const int16_t *src, int16_t *dst, int64_t n, void *stream);
 

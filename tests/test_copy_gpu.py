@@ -40,6 +40,27 @@ def test_copy_many_chunks_per_cta(lib, n, src_off, dst_off):
     assert np.all(d[:dst_off] == -1) and np.all(d[dst_off + n:] == -1)
 
 
+# Every pair of element offsets within a 16-byte vector: the 32- and 16-byte
+# vector paths, and for offsets that differ modulo 8 elements the shifted path
+# (aligned destination vectors joined from two source vectors), all seven shifts.
+@pytest.mark.parametrize("n", [37, 4096 + 5, (1 << 20) + 3])
+def test_copy_every_relative_alignment(lib, n):
+    src_h = synth.int16_uniform(1300 + n, n)
+    sbuf = torch.zeros(n + 16, dtype=torch.int16, device="cuda")
+    dbuf = torch.full((n + 16,), -1, dtype=torch.int16, device="cuda")
+    want = oracle.copy_i16(src_h)
+    for src_off in range(8):
+        sbuf.zero_()
+        sbuf[src_off:src_off + n] = torch.from_numpy(src_h).cuda()
+        for dst_off in range(8):
+            dbuf.fill_(-1)
+            lib.ts_copy_i16(sbuf[src_off:src_off + n], dbuf[dst_off:dst_off + n])
+            lib.ts_sync_and_check()
+            d = dbuf.cpu().numpy()
+            assert np.array_equal(d[dst_off:dst_off + n], want), (src_off, dst_off)
+            assert np.all(d[:dst_off] == -1) and np.all(d[dst_off + n:] == -1), (src_off, dst_off)
+
+
 @pytest.mark.slow
 def test_copy_full_size_bit_exact(lib):
     n = synth.COPY_N

@@ -9,8 +9,10 @@
 // this streams at ~97 % of the copy bandwidth, ahead of deeper unrolling,
 // 16-byte vectors or fuller occupancy.  The ragged head (until src is 32-byte
 // aligned) and tail are copied element by element with the same guard.  When
-// src and dst differ in their offset modulo 32 bytes, 16-byte vectors (same
-// offset modulo 16) or single elements are used instead.
+// src and dst differ in their offset modulo 32 bytes, 16-byte vectors are used
+// (same offset modulo 16); when they differ modulo 16, each aligned 16-byte
+// dst vector is joined from two aligned source vectors with funnel shifts
+// (measured: 4614 GB/s at n = 2^27 against 1909 element by element).
 #include <algorithm>
 
 #include "common.h"
@@ -80,6 +82,44 @@ __global__ void __launch_bounds__(kCopyThreads) copy_i16_vec_kernel(const int16_
     if (gid < n - tail0) dst[tail0 + gid] = src[tail0 + gid];
 }
 
+// src and dst that differ in their offset modulo 16 bytes (by DELTA bytes,
+// even, once dst is aligned): every aligned 16-byte vector k of dst is bytes
+// DELTA .. DELTA + 15 of the aligned source vectors k and k + 1, joined with
+// funnel shifts.  Vectors [k0, k1) are copied so (both source vectors inside
+// src, the dst vector inside dst); the `head` elements before and the elements
+// from `tail0` on are copied one by one.
+template <int DELTA>
+__device__ __forceinline__ int4 join16(const int4 &a, const int4 &b) {
+    const uint32_t w[8] = {static_cast<uint32_t>(a.x), static_cast<uint32_t>(a.y), static_cast<uint32_t>(a.z),
+                           static_cast<uint32_t>(a.w), static_cast<uint32_t>(b.x), static_cast<uint32_t>(b.y),
+                           static_cast<uint32_t>(b.z), static_cast<uint32_t>(b.w)};
+    constexpr int q = DELTA / 4, r = DELTA % 4;  // whole words, then 0 or 2 bytes
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o[i] = r == 0 ? w[q + i] : __funnelshift_r(w[q + i], w[q + i + 1], 8 * r);
+    return make_int4(static_cast<int>(o[0]), static_cast<int>(o[1]), static_cast<int>(o[2]), static_cast<int>(o[3]));
+}
+
+template <int DELTA>
+__global__ void __launch_bounds__(kCopyThreads) copy_i16_shift_kernel(const int16_t *__restrict__ src,
+                                                                      int16_t *__restrict__ dst, int64_t n,
+                                                                      const int4 *__restrict__ sv,
+                                                                      int4 *__restrict__ dv, int64_t k0, int64_t k1,
+                                                                      int64_t head, int64_t tail0) {
+    const int64_t gid = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+    const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    int64_t k = k0 + gid;
+    for (; k + step < k1; k += 2 * step) {  // two vectors in flight per thread
+        const int4 a0 = __ldcs(sv + k), b0 = __ldcs(sv + k + 1);
+        const int4 a1 = __ldcs(sv + k + step), b1 = __ldcs(sv + k + step + 1);
+        __stcs(dv + k, join16<DELTA>(a0, b0));
+        __stcs(dv + k + step, join16<DELTA>(a1, b1));
+    }
+    for (; k < k1; k += step) __stcs(dv + k, join16<DELTA>(__ldcs(sv + k), __ldcs(sv + k + 1)));
+    if (gid < head) dst[gid] = src[gid];
+    if (gid < n - tail0) dst[tail0 + gid] = src[tail0 + gid];
+}
+
 __global__ void __launch_bounds__(kCopyThreads) copy_i16_scalar_kernel(const int16_t *__restrict__ src,
                                                                        int16_t *__restrict__ dst, int64_t n) {
     const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -112,7 +152,38 @@ extern "C" ts_status ts_copy_i16(const int16_t *src, int16_t *dst, int64_t n, vo
         const int64_t head = std::min<int64_t>(n, static_cast<int64_t>(((16 - s % 16) % 16) / 2));
         copy_i16_vec_kernel<16><<<grid, kCopyThreads, 0, st>>>(src, dst, head, (n - head) / 8, n);
     } else {
-        copy_i16_scalar_kernel<<<grid, kCopyThreads, 0, st>>>(src, dst, n);
+        // dst's first aligned vector, and the aligned source vectors around it
+        const int64_t hd = std::min<int64_t>(n, static_cast<int64_t>(((16 - d % 16) % 16) / 2));
+        const uintptr_t d0 = d + 2 * hd, s0 = s + 2 * hd;
+        const int delta = static_cast<int>(s0 % 16);  // even, 2 .. 14
+        const uintptr_t sb = s0 - delta;              // aligned source vector j starts at sb + 16 j
+        const int64_t k0 = sb >= s ? 0 : 1;           // source vector k0 starts inside src
+        // source vector k + 1 ends inside src, dst vector k inside dst
+        const int64_t k1 = std::min<int64_t>(static_cast<int64_t>((s + bytes - sb) / 16) - 1,
+                                             static_cast<int64_t>((d + bytes - d0) / 16));
+        if (k1 - k0 < 1) {
+            copy_i16_scalar_kernel<<<grid, kCopyThreads, 0, st>>>(src, dst, n);
+        } else {
+            const int4 *sv = reinterpret_cast<const int4 *>(sb);
+            int4 *dv = reinterpret_cast<int4 *>(d0);
+            const int64_t head = hd + 8 * k0, tail0 = hd + 8 * k1;
+            switch (delta) {
+#define TS_SHIFT_CASE(D)                                                                                    \
+    case D:                                                                                                 \
+        copy_i16_shift_kernel<D><<<grid, kCopyThreads, 0, st>>>(src, dst, n, sv, dv, k0, k1, head, tail0); \
+        break;
+                TS_SHIFT_CASE(2)
+                TS_SHIFT_CASE(4)
+                TS_SHIFT_CASE(6)
+                TS_SHIFT_CASE(8)
+                TS_SHIFT_CASE(10)
+                TS_SHIFT_CASE(12)
+                TS_SHIFT_CASE(14)
+#undef TS_SHIFT_CASE
+                default:
+                    copy_i16_scalar_kernel<<<grid, kCopyThreads, 0, st>>>(src, dst, n);
+            }
+        }
     }
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? TS_OK : cuda_fail(e, "copy launch");
