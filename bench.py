@@ -46,8 +46,8 @@ TRAFFIC_PATH = os.path.join(ROOT, "profiles", "traffic.txt")
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_BF16_SUSTAINED = 1700.0
-KERNEL_SOURCES = {"gemm": ["gemm_kernel.cuh", "ptx.cuh", "gemm_params.h", "gemm_launch.cuh"], "copy": ["copy.cu"],
-                  "rows": ["rows_copy.cu", "ptx.cuh", "gemm_params.h"]}
+KERNEL_SOURCES = {"gemm": ["gemm_kernel.cuh", "ptx.cuh", "gemm_params.h", "gemm_launch.cuh"],
+                  "copy": ["copy.cu", "shift.cuh"], "rows": ["rows_copy.cu", "ptx.cuh", "gemm_params.h", "shift.cuh"]}
 
 
 # ------------------------------------------------------------------ helpers

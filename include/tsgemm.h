@@ -372,7 +372,8 @@ typedef struct {
  *             allowed (each element is rewritten with itself); any other
  *             overlap is TS_ERR_INVALID_ARG.  32-byte vectors are used when src
  *             and dst share their offset modulo 32 bytes, 16-byte ones modulo
- *             16, element-wise copies otherwise.
+ *             16; otherwise aligned 16-byte dst vectors joined from two source
+ *             vectors inside src (packed mode: element-wise copies).
  *   offsets   device int64 array of rows + 1 entries (read on the device).  A
  *             row with offsets[r] < 0, offsets[r + 1] < offsets[r] or
  *             offsets[r + 1] > n is not copied; the next ts_sync_and_check

@@ -417,3 +417,19 @@ def test_rows_full_workload_packed_bit_exact(lib, sched):
     lib.ts_copy_i16_rows(src, dst, torch.from_numpy(offsets).cuda(), sched=sched, chunk=32768, pack=1)
     lib.ts_sync_and_check()
     assert torch.equal(dst, src)  # the rows tile [0, n)
+
+
+# Every shift between src and dst within a 16-byte vector, whole rows and
+# chunked pieces: rows whose src and dst differ modulo 16 bytes join each dst
+# vector from two source vectors (which may lie outside the row, never outside
+# src).
+@pytest.mark.parametrize("sched", ["static", "clc"])
+@pytest.mark.parametrize("chunk", [0, 333])
+@pytest.mark.parametrize("dst_off", range(8))
+def test_rows_every_relative_alignment(lib, sched, chunk, dst_off):
+    offsets, n = _jagged(1601, 90, 1200, lead=1, trail=2)
+    src = synth.int16_uniform(1602, n)
+    dst0 = synth.int16_uniform(1603, n)
+    got = _run(lib, src, dst0, offsets, sched, src_off=3, dst_off=dst_off, chunk=chunk)
+    want, _ = oracle.copy_rows_i16(src, dst0, offsets)
+    assert np.array_equal(got, want)

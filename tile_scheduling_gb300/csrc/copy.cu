@@ -16,6 +16,7 @@
 #include <algorithm>
 
 #include "common.h"
+#include "shift.cuh"
 
 namespace ts {
 namespace {
@@ -88,18 +89,6 @@ __global__ void __launch_bounds__(kCopyThreads) copy_i16_vec_kernel(const int16_
 // funnel shifts.  Vectors [k0, k1) are copied so (both source vectors inside
 // src, the dst vector inside dst); the `head` elements before and the elements
 // from `tail0` on are copied one by one.
-template <int DELTA>
-__device__ __forceinline__ int4 join16(const int4 &a, const int4 &b) {
-    const uint32_t w[8] = {static_cast<uint32_t>(a.x), static_cast<uint32_t>(a.y), static_cast<uint32_t>(a.z),
-                           static_cast<uint32_t>(a.w), static_cast<uint32_t>(b.x), static_cast<uint32_t>(b.y),
-                           static_cast<uint32_t>(b.z), static_cast<uint32_t>(b.w)};
-    constexpr int q = DELTA / 4, r = DELTA % 4;  // whole words, then 0 or 2 bytes
-    uint32_t o[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) o[i] = r == 0 ? w[q + i] : __funnelshift_r(w[q + i], w[q + i + 1], 8 * r);
-    return make_int4(static_cast<int>(o[0]), static_cast<int>(o[1]), static_cast<int>(o[2]), static_cast<int>(o[3]));
-}
-
 template <int DELTA>
 __global__ void __launch_bounds__(kCopyThreads) copy_i16_shift_kernel(const int16_t *__restrict__ src,
                                                                       int16_t *__restrict__ dst, int64_t n,

@@ -13,7 +13,8 @@
 //
 // A row is copied by the whole CTA: a ragged head until src + begin reaches
 // the vector alignment, 32-byte (or 16-byte) vectors with two in flight per
-// thread, and a ragged tail.  Row bounds are read on the device and checked
+// thread, and a ragged tail; when src and dst differ modulo 16 bytes, aligned
+// dst vectors joined from two source vectors.  Row bounds are read on the device and checked
 // against [0, n] before any access; a row that fails the check is reported in
 // the status word and not copied.
 //
@@ -44,6 +45,7 @@
 
 #include "common.h"
 #include "ptx.cuh"
+#include "shift.cuh"
 
 namespace ts {
 namespace {
@@ -53,6 +55,36 @@ constexpr int64_t kRowsMaxTiles = 0x7fffffffLL;  // grid x limit
 constexpr uint64_t kRowsDefaultTimeoutNs = 1000ull * 1000 * 1000;
 constexpr uint64_t kRowsDrainNs = 200ull * 1000 * 1000;
 constexpr int64_t kRowsMaxPackChunk = int64_t(1) << 30;  // a packed tile's vector counts stay in int32
+
+// dst[i] = src[i] for b <= i < e when src and dst differ in their offset
+// modulo 16 bytes by DELTA (once dst is aligned), by every thread of the CTA:
+// each aligned 16-byte vector k of the row's dst is joined from the aligned
+// source vectors k and k + 1.  A source vector may lie outside the row but
+// never outside src[0, n); the elements not covered by such vectors (at most
+// 15 at the head, a few at the tail) are copied one by one.
+template <int DELTA>
+__device__ __forceinline__ void copy_row_shift(const int16_t *__restrict__ src, int16_t *__restrict__ dst, int64_t n,
+                                               int64_t b, int64_t e) {
+    const int64_t tid = threadIdx.x, T = blockDim.x;
+    const uintptr_t da = reinterpret_cast<uintptr_t>(dst + b), sa = reinterpret_cast<uintptr_t>(src + b);
+    int64_t hd = static_cast<int64_t>(((16 - da % 16) % 16) / 2);
+    if (hd > e - b) hd = e - b;
+    const uintptr_t d0 = da + 2 * hd, sb = sa + 2 * hd - DELTA;
+    const uintptr_t s_lo = reinterpret_cast<uintptr_t>(src), s_hi = s_lo + 2 * static_cast<uintptr_t>(n);
+    const int64_t k0 = sb >= s_lo ? 0 : 1;
+    int64_t k1 = static_cast<int64_t>((s_hi - sb) / 16) - 1;
+    const int64_t kd = static_cast<int64_t>((da + 2 * static_cast<uintptr_t>(e - b) - d0) / 16);
+    if (kd < k1) k1 = kd;
+    if (hd == e - b || k1 - k0 < 1) {  // no whole vector: element by element
+        for (int64_t i = b + tid; i < e; i += T) dst[i] = src[i];
+        return;
+    }
+    const int4 *sv = reinterpret_cast<const int4 *>(sb);
+    int4 *dv = reinterpret_cast<int4 *>(d0);
+    for (int64_t k = k0 + tid; k < k1; k += T) __stcs(dv + k, join16<DELTA>(__ldcs(sv + k), __ldcs(sv + k + 1)));
+    for (int64_t i = b + tid; i < b + hd + 8 * k0; i += T) dst[i] = src[i];
+    for (int64_t i = b + hd + 8 * k1 + tid; i < e; i += T) dst[i] = src[i];
+}
 
 // Division by the chunk size, a launch constant, with a multiply-high (the
 // round-up method of Granlund and Montgomery, "Division by invariant integers
@@ -175,6 +207,18 @@ __device__ __forceinline__ void copy_row(const int16_t *__restrict__ src, int16_
 __device__ __forceinline__ void rows_report(const RowsParams &p, unsigned long long code, unsigned long long info) {
     if (atomicCAS(&p.status[0], 0ull, code) == 0ull) atomicExch(&p.status[1], info);
     atomicAdd(&p.status[2], 1ull);
+}
+
+
+// Row copy by vector class: VEC 32, 16 (src and dst share their offset modulo
+// VEC bytes) or 2 (element-wise), or -DELTA (they differ modulo 16 bytes by
+// DELTA: vectors joined from two source vectors).
+template <int VEC>
+__device__ __forceinline__ void row_copy(const RowsParams &p, int64_t b, int64_t e) {
+    if constexpr (VEC < 0)
+        copy_row_shift<-VEC>(p.src, p.dst, p.n, b, e);
+    else
+        copy_row<VEC>(p.src, p.dst, b, e);
 }
 
 // Bounded phase wait on a CTA-local mbarrier.
@@ -427,7 +471,8 @@ __global__ void __launch_bounds__(kRowsMaxThreads, 2) rows_copy_kernel(const __g
                 const int64_t r = p.map[tile];
                 const int64_t r_end = tile + 1 < pieces ? p.map[tile + 1] + 1 : rows;
                 const int64_t v0 = tile * p.chunk, v1 = v0 + p.chunk < total ? v0 + p.chunk : total;
-                copy_packed<VEC>(p, v0, v1, r, r_end, *reinterpret_cast<PackTables *>(dyn_smem));
+                // (packed tiles take element-wise copies when src and dst differ modulo 16)
+                copy_packed<(VEC < 0 ? 2 : VEC)>(p, v0, v1, r, r_end, *reinterpret_cast<PackTables *>(dyn_smem));
             }
         } else if (p.chunk > 0) {
             if (tile < pieces) {
@@ -435,12 +480,12 @@ __global__ void __launch_bounds__(kRowsMaxThreads, 2) rows_copy_kernel(const __g
                 const int64_t b0 = p.offsets[r], e0 = p.offsets[r + 1];
                 const int64_t b = b0 + (tile - p.base[r]) * p.chunk;
                 const int64_t e = b + p.chunk < e0 ? b + p.chunk : e0;
-                if (b >= 0 && b <= e && e <= p.n) copy_row<VEC>(p.src, p.dst, b, e);  // checked by the plan too
+                if (b >= 0 && b <= e && e <= p.n) row_copy<VEC>(p, b, e);  // checked by the plan too
             }
         } else if (tile < rows && !(p.skip && p.skip[tile])) {
             const int64_t b = p.offsets[tile], e = p.offsets[tile + 1];
             if (b >= 0 && b <= e && e <= p.n)
-                copy_row<VEC>(p.src, p.dst, b, e);
+                row_copy<VEC>(p, b, e);
             else if (threadIdx.x == 0)
                 rows_report(p, 2ull, static_cast<unsigned long long>(tile));
         }
@@ -525,7 +570,8 @@ ts_status plan_rows(const int16_t *src, const int16_t *dst, int64_t n, const int
     pl->threads = o->threads ? o->threads : 512;
     if (pl->threads != 128 && pl->threads != 256 && pl->threads != 512 && pl->threads != 1024)
         return fail(TS_ERR_INVALID_ARG, "threads = %d (128, 256, 512 or 1024)", pl->threads);
-    pl->vec = (s % 32) == (d % 32) ? 32 : (s % 16) == (d % 16) ? 16 : 2;
+    // 32- or 16-byte vectors, or -DELTA: vectors joined across a DELTA-byte shift (src and dst differ modulo 16)
+    pl->vec = (s % 32) == (d % 32) ? 32 : (s % 16) == (d % 16) ? 16 : -static_cast<int>((s - d) & 15u);
     pl->grid = 0;
     pl->resident = 0;
     if (pl->tiles == 0) return TS_OK;  // an empty queue: nothing to launch
@@ -622,9 +668,19 @@ ts_status ts_copy_i16_rows(const int16_t *src, int16_t *dst, int64_t n, const in
         if (pe == cudaSuccess) pe = launch_dependent(rows_plan_write_kernel, pl.plan_ctas, kPlanThreads, 0, st, p);
         if (pe != cudaSuccess) return cuda_fail(pe, "row copy planning launch");
     }
-    cudaError_t e = pl.vec == 32   ? launch_rows<32>(p, pl.grid, pl.threads, pl.smem, st)
-                    : pl.vec == 16 ? launch_rows<16>(p, pl.grid, pl.threads, pl.smem, st)
-                                   : launch_rows<2>(p, pl.grid, pl.threads, pl.smem, st);
+    cudaError_t e = cudaSuccess;
+    switch (pl.vec) {
+        case 32: e = launch_rows<32>(p, pl.grid, pl.threads, pl.smem, st); break;
+        case 16: e = launch_rows<16>(p, pl.grid, pl.threads, pl.smem, st); break;
+        case -2: e = launch_rows<-2>(p, pl.grid, pl.threads, pl.smem, st); break;
+        case -4: e = launch_rows<-4>(p, pl.grid, pl.threads, pl.smem, st); break;
+        case -6: e = launch_rows<-6>(p, pl.grid, pl.threads, pl.smem, st); break;
+        case -8: e = launch_rows<-8>(p, pl.grid, pl.threads, pl.smem, st); break;
+        case -10: e = launch_rows<-10>(p, pl.grid, pl.threads, pl.smem, st); break;
+        case -12: e = launch_rows<-12>(p, pl.grid, pl.threads, pl.smem, st); break;
+        case -14: e = launch_rows<-14>(p, pl.grid, pl.threads, pl.smem, st); break;
+        default: e = launch_rows<2>(p, pl.grid, pl.threads, pl.smem, st);
+    }
     return e == cudaSuccess ? TS_OK : cuda_fail(e, "row copy launch");
 }
 
