@@ -13,6 +13,17 @@ launches, summed over ranks).  The copy's HBM GB/s is reported beside it.
 host->device copy of A and B from pinned memory, the GEMM, and the
 device->host read of D are all inside the timed region.
 
+After the headline, the same line reports the other workloads, each timed in a
+region of its own: ``gemm4096`` (4096^3 bf16-out, the automatic tile and the
+128x256 tile, static persistent vs CLC, launches back to back over four
+rotating buffer sets so that no launch finds its operands in L2),
+``contended`` (the ragged 8191x6143x4096 fp32-out GEMM while a spin kernel
+holds 32 SMs for half the solo time: >= 10 alternating static/CLC pairs, the
+median times and each scheduler's launch tail from a traced run) and
+``smallk`` (8192x8192x64 bf16-out, output-write bound, in HBM GB/s).  Clocks
+are sampled in process through read-only NVML queries every 2 ms during every
+timed region.
+
 ``--impl reference`` times the CPU oracle (the plain fp64 triple loop) on the
 host cores instead, on a bounded sample of the same workload (one row of D per
 step); it is a deliberately slow baseline, not a competitor.
@@ -146,6 +157,122 @@ class ClockSampler:
                 "samples": len(sms)}
 
 
+class NvmlLib:
+    """Read-only NVML queries through the driver's libnvidia-ml (ctypes): SM clock, its maximum,
+    power draw and the active clock-event reasons.  Nothing here changes a setting."""
+
+    # nvmlClocksEventReasons bits
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
+    CLOCK_SM = 1
+
+    def __init__(self, path: str = "libnvidia-ml.so.1"):
+        import ctypes
+
+        self.ct = ctypes
+        self.lib = ctypes.CDLL(path)
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit_v2 failed")
+        self._reasons = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def handle(self, uuid: str | None, pci_bus_id: str | None, index: int):
+        ct = self.ct
+        h = ct.c_void_p()
+        if uuid and self.lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ct.byref(h)) == 0:
+            return h
+        if pci_bus_id and self.lib.nvmlDeviceGetHandleByPciBusId_v2(pci_bus_id.encode(), ct.byref(h)) == 0:
+            return h
+        if self.lib.nvmlDeviceGetHandleByIndex_v2(ct.c_uint(index), ct.byref(h)) == 0:
+            return h
+        raise OSError("no NVML handle for the device")
+
+    def sample(self, h):
+        """(sm_mhz, sm_max_mhz, power_w or None, reason bits)."""
+        ct = self.ct
+        clk, mx, mw, rs = ct.c_uint(), ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(h, self.CLOCK_SM, ct.byref(clk)) != 0:
+            raise OSError("nvmlDeviceGetClockInfo failed")
+        if self.lib.nvmlDeviceGetMaxClockInfo(h, self.CLOCK_SM, ct.byref(mx)) != 0:
+            raise OSError("nvmlDeviceGetMaxClockInfo failed")
+        power = float(mw.value) / 1e3 if self.lib.nvmlDeviceGetPowerUsage(h, ct.byref(mw)) == 0 else None
+        bits = int(rs.value) if self._reasons(h, ct.byref(rs)) == 0 else 0
+        return float(clk.value), float(mx.value), power, bits
+
+
+class NvmlClockSampler:
+    """Samples the GPU's SM clock and clock-event reasons every `period_s` from a host thread, in
+    process, through read-only NVML queries, so that even a timed region of a few milliseconds gets
+    several samples.  `regions` collects (name, t0, t1) of the timed regions; `summary(name)` reduces
+    the samples that fall inside one region (or all regions)."""
+
+    def __init__(self, device: int = 0, period_s: float = 0.002, nvml=None):
+        self.period = period_s
+        self.samples = []  # (time, sm_mhz, sm_max_mhz, power_w, reason bits)
+        self.regions = []
+        self._stop = threading.Event()
+        self._t = None
+        self.error = None
+        try:
+            self.nvml = nvml if nvml is not None else NvmlLib()
+            uuid = pci = None
+            try:
+                import torch
+
+                prop = torch.cuda.get_device_properties(device)
+                u = str(getattr(prop, "uuid", "") or "")
+                uuid = (u if u.startswith("GPU-") else f"GPU-{u}") if u else None
+                if hasattr(prop, "pci_bus_id"):
+                    pci = f"{prop.pci_domain_id:08x}:{prop.pci_bus_id:02x}:{prop.pci_device_id:02x}.0"
+            except Exception:  # noqa: BLE001 - a fake NVML needs no torch device
+                pass
+            self.h = self.nvml.handle(uuid, pci, device)
+        except (OSError, AttributeError) as e:
+            self.nvml = None
+            self.error = str(e)
+
+    def start(self):
+        if self.nvml is None:
+            return
+        self._t = threading.Thread(target=self._run, daemon=True)
+        self._t.start()
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                self.samples.append((time.time(), *self.nvml.sample(self.h)))
+            except OSError as e:
+                self.error = str(e)
+                return
+            self._stop.wait(self.period)
+
+    def stop(self):
+        self._stop.set()
+        if self._t:
+            self._t.join(timeout=5)
+
+    def region(self, name: str, t0: float, t1: float):
+        self.regions.append((name, t0, t1))
+
+    def summary(self, name: str | None = None):
+        spans = [(a, b) for n, a, b in self.regions if name is None or n == name]
+        sel = [s for s in self.samples if any(a <= s[0] <= b for a, b in spans)]
+        out = {"source": "nvml, in process", "period_ms": round(self.period * 1e3, 2), "samples": len(sel)}
+        if self.error:
+            out["error"] = self.error
+        if not sel:
+            out.update(sm_mhz=None, sm_max_mhz=None, reasons=[])
+            return out
+        reasons = set()
+        for s in sel:
+            reasons.update(n for bit, n in NvmlLib.REASONS.items() if s[4] & bit)
+        powers = [s[3] for s in sel if s[3] is not None]
+        out.update(sm_mhz=statistics.median(s[1] for s in sel), sm_min_mhz=min(s[1] for s in sel),
+                   sm_max_mhz=max(s[2] for s in sel), reasons=sorted(reasons),
+                   power_w_max=round(max(powers), 1) if powers else None)
+        return out
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -204,9 +331,13 @@ def run_ours(args, ws, rank, local):
 
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     outer0, outer1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(local)
+    sampler = NvmlClockSampler(local)
+    smi = None
+    if sampler.nvml is None:  # no NVML in this process: fall back to nvidia-smi polling
+        smi = ClockSampler(local)
+        smi.start()
+        time.sleep(0.3)
     sampler.start()
-    time.sleep(0.3)
     if ws > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -217,9 +348,10 @@ def run_ours(args, ws, rank, local):
     outer1.record(stream)
     torch.cuda.synchronize()
     t1 = time.time()
+    sampler.region("headline", t0, t1)
     if ws > 1:
         dist.barrier()
-    clocks = sampler.stop(t0, t1)
+    clocks = sampler.summary("headline") if smi is None else smi.stop(t0, t1)
     ts.ts_sync_and_check()
 
     gemm_ms = [e[0].elapsed_time(e[1]) for e in events]
@@ -235,21 +367,35 @@ def run_ours(args, ws, rank, local):
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, ts, A_bits, B_bits, M, N, K, ws)
+    del A, B, D, src, dst
+    torch.cuda.empty_cache()
 
+    # the other GEMM workloads, each in its own timed region (rank 0 reports its own numbers)
+    extra = {}
+    if not args.no_configs:
+        extra["gemm4096"] = measure_gemm4096(ts, sampler, reps=args.config_reps)
+        extra["contended"] = measure_contended(ts, sampler, reps=max(10, args.reps), ctas=args.spin_ctas,
+                                               tile=args.contended_tile, warmup=args.warmup)
+        extra["smallk"] = measure_smallk(ts, sampler, samples=args.config_reps, warmup=args.warmup)
+    sampler.stop()
     if rank != 0:
         return None
     peaks = load_peaks()
     per_launch_s = gemm_sum * 1e-3 / args.steps
     achieved = flops / per_launch_s / 1e12
     workload = f"gemm_bf16 {M}x{N}x{K} bf16-out {args.tile} {args.sched} + copy_i16 n=2^28"
-    roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops_sustained"],
-            "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops_sustained"], 4),
+    roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
+            "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
             "traffic": load_traffic("gemm", f"{M}x{N}x{K} {args.tile} {args.sched}"),
-            "peak_kind": f"{peaks['source']} bf16 sustained (kernel timed inside a long step)",
-            "frac_of_burst_peak": round(achieved / peaks["bf16_tflops"], 4), "kernel": "gemm_ws_kernel"}
+            "peak_kind": f"{peaks['source']} bf16 burst: the GEMM is timed in a region of "
+                         f"{total / 1e3:.3f} s, far shorter than the seconds-long loop of the sustained figure",
+            "frac_of_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4),
+            "peak_sustained": peaks["bf16_tflops_sustained"], "kernel": "gemm_ws_kernel",
+            "algorithmic_flops_per_launch": flops}
     copy_roof = {"bound": "hbm", "achieved": round(copy_gbs / ws, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                  "frac": round(copy_gbs / ws / peaks["hbm_gbs"], 4), "traffic": load_traffic("copy", "n=2^28"),
-                 "peak_kind": f"{peaks['source']} HBM copy", "kernel": "copy_i16_vec_kernel"}
+                 "peak_kind": f"{peaks['source']} HBM copy", "kernel": "copy_i16_vec_kernel",
+                 "algorithmic_bytes_per_launch": copy_bytes}
     line = {
         "metric": "bf16 GEMM TFLOP/s at 8192^3 (2-CTA 256x256, CLC); int16 copy HBM GB/s",
         "value": round(gemm_tflops, 2), "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
@@ -270,6 +416,7 @@ def run_ours(args, ws, rank, local):
         "clocks": clocks,
         "gpu_launches": 2 * args.steps,
         "e2e": e2e,
+        **extra,
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args)
@@ -295,40 +442,101 @@ def _event_ms(fn, stream, sleep_cycles=500_000):
     return e0.elapsed_time(e1)
 
 
+def _dev_bf16(bits):
+    import torch
+
+    return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def _batched_ms(fns, reps, batch, stream, sampler=None, region=None, sleep_cycles=2_000_000):
+    """Per-launch device time of each fn(i) in `fns`: `reps` samples, each `batch` calls queued back to
+    back (i = 0, 1, ...) between two CUDA events on `stream`, behind a GPU sleep that covers the host's
+    submission work; the configurations alternate so that clock drift reaches all of them alike.
+    Returns {name: [ms per launch, one per sample]}."""
+    import torch
+
+    out = {k: [] for k in fns}
+    for _ in range(reps):
+        for k, f in fns.items():
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda._sleep(sleep_cycles)
+            e0.record(stream)
+            t0 = time.time()
+            for i in range(batch):
+                f(i)
+            e1.record(stream)
+            e1.synchronize()
+            if sampler is not None:
+                sampler.region(region or k, t0, time.time())
+            out[k].append(e0.elapsed_time(e1) / batch)
+    return out
+
+
+def measure_gemm4096(ts, sampler, reps=5, batch=20, nset=4):
+    """4096^3 bf16-out GEMM, uniform [-1, 1] inputs: the automatic tile choice and the 128x256 tile, each
+    under the static persistent and the CLC scheduler.  The launches of a sample run back to back over
+    `nset` input/output buffer sets used in turn (4 x 96 MiB, larger than L2), so no launch finds its
+    operands in L2 from the launch before."""
+    import torch
+
+    w = synth.GEMM_4096
+    A_bits, B_bits = w.inputs()
+    As = [_dev_bf16(A_bits) for _ in range(nset)]
+    Bs = [_dev_bf16(B_bits) for _ in range(nset)]
+    Ds = [torch.empty((w.M, w.N), dtype=torch.bfloat16, device="cuda") for _ in range(nset)]
+    stream = torch.cuda.current_stream()
+    runs = {}
+    for tile in ("auto", "128x256"):
+        for sched in ("static", "clc"):
+            runs[f"{tile} {sched}"] = (lambda i, tile=tile, sched=sched:
+                                       ts.ts_gemm_bf16_ex(As[i % nset], Bs[i % nset], Ds[i % nset], sched=sched,
+                                                          tile=tile))
+    for f in runs.values():
+        for i in range(2 * nset):
+            f(i)
+    torch.cuda.synchronize()
+    ts.ts_sync_and_check()
+    times = _batched_ms(runs, reps, batch, stream, sampler, "gemm4096")
+    ts.ts_sync_and_check()
+    peaks = load_peaks()
+    flops = 2.0 * w.M * w.N * w.K
+    res = {}
+    for k, v in times.items():
+        tile, sched = k.split()
+        med = statistics.median(v)
+        info = ts.ts_gemm_launch_info(w.M, w.N, w.K, ts.TS_OUT_BF16, sched, tile=tile)
+        tf = flops / (med * 1e-3) / 1e12
+        res[k] = {"tile": f"{info['tile_m']}x{info['tile_n']}" + (" 2-CTA" if info["cluster"] == 2 else ""),
+                  "sched": sched, "us_median": round(med * 1e3, 2), "us_min": round(min(v) * 1e3, 2),
+                  "tflops": round(tf, 1), "frac_of_burst": round(tf / peaks["bf16_tflops"], 4),
+                  "split_tail": f"{info['split_tiles']} tiles x {info['split_parts']} parts",
+                  "stages": info["stages"], "epi_warps": info["epi_warps"]}
+    best_auto = max(("auto static", "auto clc"), key=lambda k: res[k]["tflops"])
+    return {"metric": "bf16 GEMM TFLOP/s, 4096^3 bf16-out, static vs CLC, automatic tile and 128x256",
+            "unit": "TFLOP/s", "value": res[best_auto]["tflops"], "frac_of_burst": res[best_auto]["frac_of_burst"],
+            "reported": best_auto, "runs": res, "peak": peaks["bf16_tflops"],
+            "peak_kind": f"{peaks['source']} bf16 burst", "samples": reps, "launches_per_sample": batch,
+            "gpu_launches": reps * batch * len(runs),
+            "clocks": sampler.summary("gemm4096") if sampler is not None else None,
+            "config": {"workload": w.name, "l2": f"{nset} buffer sets of A, B, D used in turn ({nset} x 96 MiB, "
+                                                  "larger than L2); launches back to back"}}
+
+
 def run_gemm4096(args, ws, rank, local):
-    """4096^3 bf16-out GEMM with 128x256 tiles: static persistent vs CLC (medians over --steps launches)."""
+    """4096^3 bf16-out GEMM, static persistent vs CLC, automatic tile and 128x256."""
     import torch
 
     import tile_scheduling_gb300 as ts
 
     torch.cuda.set_device(local)
-    w = synth.GEMM_4096
-    A_bits, B_bits = w.inputs()
-    A = torch.from_numpy(A_bits.view(np.int16)).view(torch.bfloat16).cuda()
-    B = torch.from_numpy(B_bits.view(np.int16)).view(torch.bfloat16).cuda()
-    D = torch.empty((w.M, w.N), dtype=torch.bfloat16, device="cuda")
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")  # > L2: inputs would otherwise stay resident
-    stream = torch.cuda.current_stream()
-    res = {}
-    for sched in ("static", "clc"):
-        for _ in range(args.warmup):
-            ts.ts_gemm_bf16_ex(A, B, D, sched=sched, tile="128x256")
-        ms = []
-        for _ in range(args.steps):
-            flush.zero_()
-            ms.append(_event_ms(lambda: ts.ts_gemm_bf16_ex(A, B, D, sched=sched, tile="128x256"), stream))
-        ts.ts_sync_and_check()
-        med = statistics.median(ms)
-        res[sched] = {"ms_median": round(med, 4), "ms_min": round(min(ms), 4),
-                      "tflops": round(2.0 * w.M * w.N * w.K / (med * 1e-3) / 1e12, 1)}
+    sampler = NvmlClockSampler(local)
+    sampler.start()
+    line = measure_gemm4096(ts, sampler, reps=args.steps)
+    sampler.stop()
     if rank != 0:
         return None
-    peaks = load_peaks()
-    return {"metric": "bf16 GEMM TFLOP/s, 4096^3 bf16-out, 128x256 tiles, static vs CLC", "unit": "TFLOP/s",
-            "value": res["clc"]["tflops"], "static": res["static"], "clc": res["clc"], "n_gpus": ws,
-            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "dtype": "bf16",
-            "data": "synthetic", "config": {"workload": w.name, "l2": "256 MiB buffer written between launches"},
-            "peak_bf16_tflops_burst": peaks["bf16_tflops"], "peak_source": peaks["source"]}
+    return {**line, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+            "dtype": "bf16", "data": "synthetic"}
 
 
 def run_grouped(args, ws, rank, local):
@@ -525,95 +733,93 @@ def run_rows(args, ws, rank, local):
                                             "l2": "inputs larger than L2 (0.5 GiB each way); no flush"}}
 
 
-def run_smallk(args, ws, rank, local):
+def measure_smallk(ts, sampler, samples=20, warmup=5, batch=25):
     """8192x8192x64 bf16-out GEMM: one k-block per tile, so the 134 MB output write bounds it (HBM GB/s).
-    Both schedulers on the 2-CTA 256x256 tile and on the 1-CTA 128x256 tile, launches alternated."""
+    Both schedulers on the 2-CTA 256x256 tile and on the 1-CTA 128x256 tile, samples alternated; a
+    sample is `batch` launches back to back (a launch takes ~25 us, close to the event timer's grain)."""
     import torch
 
-    import tile_scheduling_gb300 as ts
-
-    torch.cuda.set_device(local)
     w = synth.GEMM_SMALLK
     A_bits, B_bits = w.inputs()
-    A = torch.from_numpy(A_bits.view(np.int16)).view(torch.bfloat16).cuda()
-    B = torch.from_numpy(B_bits.view(np.int16)).view(torch.bfloat16).cuda()
+    A, B = _dev_bf16(A_bits), _dev_bf16(B_bits)
     D = torch.empty((w.M, w.N), dtype=torch.bfloat16, device="cuda")
     stream = torch.cuda.current_stream()
     nbytes = 2.0 * (w.M * w.K + w.N * w.K) + 2.0 * w.M * w.N  # A and B read once, D written once
-    runs = {f"{sched} {tile}": dict(sched=sched, tile=tile) for tile in ("256x256", "128x256") for sched in ("clc", "static")}
-    times = {k: [] for k in runs}
-    for kw in runs.values():
-        for _ in range(args.warmup):
-            ts.ts_gemm_bf16_ex(A, B, D, **kw)
-    # A launch takes ~40 us, close to the event timer's resolution: each sample
-    # times `batch` launches queued back to back behind a GPU sleep long enough
-    # to cover their host-side submission.
-    batch = 25
-
-    def launches(kw):
-        for _ in range(batch):
-            ts.ts_gemm_bf16_ex(A, B, D, **kw)
-
-    for _ in range(args.steps):  # alternate so clock drift hits every variant alike
-        for k, kw in runs.items():
-            times[k].append(_event_ms(lambda: launches(kw), stream, sleep_cycles=4_000_000) / batch)
+    runs = {f"{sched} {tile}": (lambda i, sched=sched, tile=tile: ts.ts_gemm_bf16_ex(A, B, D, sched=sched, tile=tile))
+            for tile in ("256x256", "128x256") for sched in ("clc", "static")}
+    for f in runs.values():
+        for i in range(warmup):
+            f(i)
+    torch.cuda.synchronize()
+    times = _batched_ms(runs, samples, batch, stream, sampler, "smallk", sleep_cycles=4_000_000)
     ts.ts_sync_and_check()
-    if rank != 0:
-        return None
     peaks = load_peaks()
     res = {}
     for k, v in times.items():
         med = statistics.median(v)
-        res[k] = {"ms_median": round(med, 4), "ms_min": round(min(v), 4), "gbs": round(nbytes / (med * 1e-3) / 1e9, 1),
+        res[k] = {"us_median": round(med * 1e3, 2), "us_min": round(min(v) * 1e3, 2),
+                  "gbs": round(nbytes / (med * 1e-3) / 1e9, 1),
+                  "frac_of_hbm": round(nbytes / (med * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
                   "tflops": round(2.0 * w.M * w.N * w.K / (med * 1e-3) / 1e12, 1)}
-    head = max(res, key=lambda k: res[k]["gbs"])  # the line reports the fastest configuration, named in config
+    head = max(res, key=lambda k: res[k]["gbs"])  # the fastest configuration, named in config
     h_sched, h_tile = head.split()
     best = res[head]["gbs"]
     return {"metric": "small-K bf16 GEMM HBM GB/s (8192x8192x64, bf16 out)", "unit": "GB/s", "value": best,
-            "runs": res,
+            "frac_of_hbm": round(best / peaks["hbm_gbs"], 4), "runs": res,
             "roofline": {"bound": "hbm", "achieved": best, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": round(best / peaks["hbm_gbs"], 4),
                          "traffic": load_traffic("gemm", f"{w.M}x{w.N}x{w.K} {h_tile} {h_sched}"),
                          "peak_kind": f"{peaks['source']} HBM copy", "kernel": "gemm_ws_kernel",
-                         "algorithmic_bytes": int(nbytes)},
-            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "dtype": "bf16",
-            "data": "synthetic", "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "tile": h_tile,
-                                            "sched": h_sched, "launches_per_sample": batch,
-                                            "epi_warps": ts.ts_gemm_launch_info(w.M, w.N, w.K, ts.TS_OUT_BF16, h_sched,
-                                                                                tile=h_tile)["epi_warps"],
-                                            "l2": "output (134 MB) larger than L2; A and B (1 MiB each) stay resident; no flush"}}
+                         "algorithmic_bytes_per_launch": int(nbytes)},
+            "samples": samples, "launches_per_sample": batch, "gpu_launches": samples * batch * len(runs),
+            "clocks": sampler.summary("smallk") if sampler is not None else None,
+            "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "tile": h_tile, "sched": h_sched,
+                       "epi_warps": ts.ts_gemm_launch_info(w.M, w.N, w.K, ts.TS_OUT_BF16, h_sched,
+                                                           tile=h_tile)["epi_warps"],
+                       "l2": "output (134 MB) larger than L2; A and B (1 MiB each) stay resident; no flush"}}
 
 
-def run_contended(args, ws, rank, local):
-    """Ragged 8191x6143x4096 fp32-out GEMM while a spin kernel holds 32 SMs for half the solo GEMM time.
-
-    Static persistent vs CLC, alternating, --reps pairs; a traced run per scheduler gives the tail
-    (last worker's finish minus the median worker's finish)."""
+def run_smallk(args, ws, rank, local):
+    """8192x8192x64 bf16-out GEMM in HBM GB/s."""
     import torch
 
     import tile_scheduling_gb300 as ts
 
     torch.cuda.set_device(local)
+    sampler = NvmlClockSampler(local)
+    sampler.start()
+    line = measure_smallk(ts, sampler, samples=args.steps, warmup=args.warmup)
+    sampler.stop()
+    if rank != 0:
+        return None
+    return {**line, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+            "dtype": "bf16", "data": "synthetic"}
+
+
+def measure_contended(ts, sampler, reps=10, ctas=32, tile="256x256", warmup=5):
+    """Ragged 8191x6143x4096 fp32-out GEMM while a spin kernel on a second stream holds `ctas` SMs for
+    half the solo static GEMM time.  Static persistent vs CLC in `reps` alternating pairs (a fresh spin
+    per run); a traced run per scheduler gives the tail (the last worker's finish minus the median
+    worker's finish)."""
+    import torch
+
     w = synth.GEMM_RAGGED
     A_bits, B_bits = w.inputs()
-    A = torch.from_numpy(A_bits.view(np.int16)).view(torch.bfloat16).cuda()
-    B = torch.from_numpy(B_bits.view(np.int16)).view(torch.bfloat16).cuda()
+    A, B = _dev_bf16(A_bits), _dev_bf16(B_bits)
     Dbuf = torch.empty((w.M, 6144), dtype=torch.float32, device="cuda")
     D = Dbuf[:, :w.N]  # 6144-element pitch: TMA stores, masked at N = 6143
     stream = torch.cuda.current_stream()
     side = torch.cuda.Stream()
     started = torch.zeros(1, dtype=torch.int32).pin_memory()
-    ctas = args.spin_ctas
-    tile = args.tile
 
     def gemm(sched, trace=None):
         ts.ts_gemm_bf16_ex(A, B, D, sched=sched, tile=tile, trace=trace)
 
     solo = {}
     for sched in ("static", "clc"):
-        for _ in range(args.warmup):
+        for _ in range(warmup):
             gemm(sched)
-        solo[sched] = statistics.median([_event_ms(lambda: gemm(sched), stream) for _ in range(args.reps)])
+        solo[sched] = statistics.median([_event_ms(lambda: gemm(sched), stream) for _ in range(reps)])
     # half the solo time from the GEMM's start, plus the ~30 us of sleep queued ahead of it
     spin_ns = int(0.5 * solo["static"] * 1e6) + 30_000
 
@@ -624,12 +830,15 @@ def run_contended(args, ws, rank, local):
         ts.ts_spin_wait_started(started, ctas, 5.0)
         # a short sleep only (~30 us): it hides the host's launch work, and the GEMM
         # still starts while the spin holds its SMs for most of its time
+        t0 = time.time()
         ms = _event_ms(lambda: gemm(sched, trace), stream, sleep_cycles=60_000)
+        if sampler is not None:
+            sampler.region("contended", t0, time.time())
         torch.cuda.synchronize()
         return ms
 
     times = {"static": [], "clc": []}
-    for _ in range(args.reps):
+    for _ in range(reps):
         for sched in ("static", "clc"):
             times[sched].append(contended(sched))
     tails = {}
@@ -646,8 +855,6 @@ def run_contended(args, ws, rank, local):
         tails[sched] = {"workers_ran": len(fin), "tail_us": round((f.max() - np.median(f)) / 1e3, 1),
                         "span_us": round((f.max() - t0) / 1e3, 1), "visits_ok": bool(np.all(tr[:, 0] == 1))}
     ts.ts_sync_and_check()
-    if rank != 0:
-        return None
     flops = 2.0 * w.M * w.N * w.K
     out = {}
     for sched in ("static", "clc"):
@@ -658,8 +865,27 @@ def run_contended(args, ws, rank, local):
     return {"metric": "ragged 8191x6143x4096 fp32-out GEMM TFLOP/s with 32 SMs held for half the solo time",
             "unit": "TFLOP/s", "value": out["clc"]["tflops"], "static": out["static"], "clc": out["clc"],
             "clc_speedup_over_static": round(out["static"]["ms_median"] / out["clc"]["ms_median"], 3),
-            "n_gpus": ws, "reps": args.reps, "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": w.name, "tile": tile, "spin_ctas": ctas, "spin_ns": spin_ns, "ldd": 6144}}
+            "clc_tail_shorter": bool(out["clc"]["tail_us"] < out["static"]["tail_us"]),
+            "pairs": reps, "gpu_launches": 2 * reps + 2,
+            "clocks": sampler.summary("contended") if sampler is not None else None,
+            "config": {"workload": w.name, "tile": tile, "spin_ctas": ctas, "spin_ns": spin_ns, "ldd": 6144,
+                       "l2": "inputs larger than L2 (A 67 MB, B 50 MB, D 201 MB); one launch per timed region"}}
+
+
+def run_contended(args, ws, rank, local):
+    """Ragged 8191x6143x4096 fp32-out GEMM with 32 SMs held: static persistent vs CLC."""
+    import torch
+
+    import tile_scheduling_gb300 as ts
+
+    torch.cuda.set_device(local)
+    sampler = NvmlClockSampler(local)
+    sampler.start()
+    line = measure_contended(ts, sampler, reps=args.reps, ctas=args.spin_ctas, tile=args.tile, warmup=args.warmup)
+    sampler.stop()
+    if rank != 0:
+        return None
+    return {**line, "n_gpus": ws, "higher_is_better": True, "dtype": "bf16", "data": "synthetic"}
 
 
 def run_e2e(args, ts, A_bits, B_bits, M, N, K, ws):
@@ -801,8 +1027,13 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--workload", default="headline", choices=["headline", "gemm4096", "contended", "grouped", "causal", "fork",
                                                                    "rows", "smallk"])
-    ap.add_argument("--reps", type=int, default=10)
+    ap.add_argument("--reps", type=int, default=10, help="static/CLC pairs of the contended workload (>= 10)")
     ap.add_argument("--spin-ctas", type=int, default=32)
+    ap.add_argument("--no-configs", action="store_true",
+                    help="headline only: skip the 4096^3, contended and small-K measurements")
+    ap.add_argument("--config-reps", type=int, default=7,
+                    help="samples per configuration of the 4096^3 and small-K measurements")
+    ap.add_argument("--contended-tile", default="256x256", choices=["128x128", "128x256", "256x256", "auto"])
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

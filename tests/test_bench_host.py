@@ -77,3 +77,72 @@ def test_reference_arm_other_ranks_exit_quietly():
                        env=env)
     assert r.returncode == 0, r.stderr
     assert r.stdout.strip() == ""
+
+
+class _FakeNvml:
+    """Stands in for the driver's NVML: a scripted sequence of (sm MHz, max MHz, watts, reason bits)."""
+
+    def __init__(self, seq):
+        self.seq = list(seq)
+        self.i = 0
+        self.handles = []
+
+    def handle(self, uuid, pci, index):
+        self.handles.append((uuid, pci, index))
+        return "h"
+
+    def sample(self, h):
+        assert h == "h"
+        s = self.seq[min(self.i, len(self.seq) - 1)]
+        self.i += 1
+        return s
+
+
+def test_nvml_sampler_summarises_only_samples_inside_a_region():
+    sys.path.insert(0, ROOT)
+    import bench
+
+    smp = bench.NvmlClockSampler(device=3, period_s=0.001, nvml=_FakeNvml([(2070.0, 2070.0, 500.0, 0x4)]))
+    assert smp.error is None
+    # samples placed by hand: two inside the region, one before and one after it
+    smp.samples = [(0.5, 1000.0, 2070.0, 100.0, 0x8), (1.0, 1800.0, 2070.0, 900.0, 0x4),
+                   (1.5, 1900.0, 2070.0, 950.0, 0x0), (2.5, 1200.0, 2070.0, 300.0, 0x40)]
+    smp.region("a", 0.9, 2.0)
+    s = smp.summary("a")
+    assert s["samples"] == 2 and s["sm_mhz"] == 1850.0 and s["sm_min_mhz"] == 1800.0
+    assert s["reasons"] == ["sw_power_cap"] and s["power_w_max"] == 950.0 and s["sm_max_mhz"] == 2070.0
+    assert smp.summary("missing")["samples"] == 0 and smp.summary("missing")["sm_mhz"] is None
+
+
+def test_nvml_sampler_thread_collects_and_decodes_reason_bits():
+    sys.path.insert(0, ROOT)
+    import time
+
+    import bench
+
+    fake = _FakeNvml([(1500.0, 2070.0, 1400.0, 0x8 | 0x20 | 0x40 | 0x4)])
+    smp = bench.NvmlClockSampler(period_s=0.001, nvml=fake)
+    t0 = time.time()
+    smp.start()
+    time.sleep(0.05)
+    smp.stop()
+    smp.region("r", t0, time.time())
+    s = smp.summary("r")
+    assert s["samples"] >= 5
+    assert s["reasons"] == ["hw_slowdown", "hw_thermal_slowdown", "sw_power_cap", "sw_thermal_slowdown"]
+    assert fake.handles and fake.handles[0][2] == 0
+
+
+def test_nvml_sampler_without_nvml_reports_the_error():
+    sys.path.insert(0, ROOT)
+    import bench
+
+    class Broken:
+        def handle(self, *a):
+            raise OSError("no device")
+
+    smp = bench.NvmlClockSampler(nvml=Broken())
+    smp.start()
+    smp.stop()
+    assert smp.nvml is None and "no device" in smp.error
+    assert smp.summary()["samples"] == 0

@@ -284,10 +284,8 @@ def test_gemm_8192_bf16_2cta_clc_sampled_rows(lib, merge):
     D = _run(lib, A, B, torch.bfloat16, sched="clc", tile="256x256", merge=merge)
     rng = np.random.default_rng(8192)
     rows = np.unique(np.concatenate([rng.integers(0, w.M, 96), [0, 255, 256, w.M - 1]]))
-    a = oracle.bf16_to_f64(A[rows])
-    b = oracle.bf16_to_f64(B)
-    ref = a @ b.T
-    S = np.abs(a) @ np.abs(b).T
+    ref = oracle.gemm_f64_blas(A[rows], B)
+    S = oracle.gemm_f64_blas(A[rows], B, absolute=True)
     got = oracle.bf16_to_f64(bf16_bits(D[torch.as_tensor(rows, device="cuda")]))
     assert_within_bound(got, ref, S, torch.bfloat16, "8192^3 sampled rows")
     # every tile column/row block is exercised by the sampled rows' full width; add sampled columns too
@@ -309,10 +307,9 @@ def test_gemm_small_k_sampled(lib, sched, tile, ew):
     D = _run(lib, A, B, torch.bfloat16, sched=sched, tile=tile, epi_warps=ew)
     rng = np.random.default_rng(64)
     rows = np.unique(np.concatenate([rng.integers(0, w.M, 128), [0, 127, 128, 255, 256, w.M - 1]]))
-    a = oracle.bf16_to_f64(A[rows])
-    b = oracle.bf16_to_f64(B)
-    assert_within_bound(oracle.bf16_to_f64(bf16_bits(D[torch.as_tensor(rows, device="cuda")])), a @ b.T,
-                        np.abs(a) @ np.abs(b).T, torch.bfloat16, f"8192x8192x64 {sched} {tile} sampled rows")
+    assert_within_bound(oracle.bf16_to_f64(bf16_bits(D[torch.as_tensor(rows, device="cuda")])),
+                        oracle.gemm_f64_blas(A[rows], B), oracle.gemm_f64_blas(A[rows], B, absolute=True),
+                        torch.bfloat16, f"8192x8192x64 {sched} {tile} sampled rows")
     ii = rng.integers(0, w.M, 256)
     jj = rng.integers(0, w.N, 256)
     e, ea = oracle.gemm_entries_f64(A, B, ii, jj)
