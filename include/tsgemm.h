@@ -167,6 +167,25 @@ int32_t ts_protocol_check(int32_t nbars, const int32_t *bar_expected, int32_t nb
                           const char *names, int64_t max_states, int64_t *states_out, char *msg, int32_t msg_len);
 
 /*
+ * ts_protocol_check_ex -- ts_protocol_check with global counters (host only).
+ * The split tiles of the GEMM hand their fp32 partials over through a per-slab
+ * counter in global memory: each part stores its partial, fences, and adds one
+ * to the counter; the part that draws the last ticket re-arms the counter and
+ * sums every part.  The programs model that with store, fence and ticket
+ * records (see protocol_check.cu).
+ *
+ *   ncounters            counters (all start at 0)
+ *   counter_reductions   per counter, how often its last ticket must be drawn
+ * Every other argument and the return value are those of ts_protocol_check; a
+ * run that ends with a counter not back at 0, or drawn last a different number
+ * of times, is a violation (1).
+ */
+int32_t ts_protocol_check_ex(int32_t nbars, const int32_t *bar_expected, int32_t nbufs, int32_t nroles,
+                             const int32_t *role_group, const int32_t *role_offsets, const int32_t *ops,
+                             int32_t ncounters, const int32_t *counter_reductions, const char *names,
+                             int64_t max_states, int64_t *states_out, char *msg, int32_t msg_len);
+
+/*
  * ts_gemm_bf16 -- D = A * B^T with bf16 inputs and fp32 accumulation.
  *
  * Definition: D[i][j] = sum_{k<K} A[i][k] * B[j][k] (CUTLASS TS "Pipeline

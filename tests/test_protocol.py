@@ -102,7 +102,8 @@ def test_clc_protocol_verified_cta_pair(units):
     assert r.ok, r.message
 
 
-@pytest.mark.parametrize("mutation", [m for m in pc.MUTATIONS if not m.startswith(("fork", "merge"))])
+@pytest.mark.parametrize("mutation", [m for m in pc.MUTATIONS
+                                      if not m.startswith(("fork", "merge")) and m not in pc.ZERO_K_MUTATIONS])
 @pytest.mark.parametrize("tile,sched,warps", [("128x256", "clc", None), ("256x256", "clc", 1),
                                               ("256x256", "static", 2)])
 def test_planted_mistakes_are_caught(mutation, tile, sched, warps):
@@ -199,7 +200,7 @@ def test_merge_protocol_verified(tile, sched, warps, units):
     assert r.ok, r.message
 
 
-@pytest.mark.parametrize("mutation", [m for m in pc.MUTATIONS if not m.startswith("fork")])
+@pytest.mark.parametrize("mutation", [m for m in pc.MUTATIONS if not m.startswith("fork") and m not in pc.ZERO_K_MUTATIONS])
 @pytest.mark.parametrize("tile,sched,warps", [("128x256", "clc", 2), ("256x256", "static", 1)])
 def test_merge_planted_mistakes_are_caught(mutation, tile, sched, warps):
     r = pc.check_variant(tile, [2, 1, 2], sched, stages=2, variant_merge=1, epilogue_warps=warps, mutate=mutation)
@@ -223,3 +224,92 @@ def test_sixteen_warp_planted_mistakes_are_caught(mutation):
     r = pc.check_variant("256x256", [2, 1, 2], "clc", stages=2, variant_epi_warps=16, epilogue_warps=1,
                          mutate=mutation)
     assert not r.ok and r.status == 1, (mutation, r)
+
+
+# --------------------------------------------- units with no k-blocks (skip, K = 0)
+# A skipped tile (TS "Schedules", Skippable Tiles) is taken from the queue by every
+# role but loads nothing and takes no accumulator; a K = 0 group of a grouped GEMM
+# takes an accumulator that the MMA commits with no MMA issued and the epilogue
+# reads (discarding it) and releases.
+MIXED = [[2, pc.SKIP, 0, 2], [0, 1, pc.SKIP, 1], [pc.SKIP, pc.SKIP, 1, 0, 1], [0, 0, 1], [pc.SKIP, 0, pc.SKIP]]
+
+
+@pytest.mark.parametrize("units", MIXED)
+@pytest.mark.parametrize("tile", ["128x128", "128x256", "256x256"])
+@pytest.mark.parametrize("sched", ["static", "clc"])
+def test_units_without_k_blocks_verified_on_every_tile(tile, units, sched):
+    r = pc.check_variant(tile, units, sched, stages=2, epilogue_warps=1)
+    assert r.ok, r.message
+
+
+@pytest.mark.parametrize("units", MIXED[:2])
+@pytest.mark.parametrize("ew", [2, 4])
+def test_units_without_k_blocks_verified_with_more_epilogue_warps(units, ew):
+    r = pc.check_variant("128x256", units, "clc", stages=2, epilogue_warps=min(ew, 4), variant_epi_warps=ew * 2
+                         if ew == 4 else 4)
+    assert r.ok, r.message
+
+
+@pytest.mark.parametrize("units", MIXED[:2])
+def test_units_without_k_blocks_verified_fork_and_merge(units):
+    assert pc.check_variant("128x256", units, "clc", stages=2, fork=True).ok
+    assert pc.check_variant("256x256", units, "static", stages=2, epilogue_warps=1, variant_merge=1).ok
+
+
+ZERO_K_CASES = {"mma_takes_skipped_accumulator": [1, pc.SKIP, 1, 1], "epilogue_waits_skipped_tile": [1, pc.SKIP, 1],
+                "zero_k_mma_no_commit": [1, 0, 1], "zero_k_epilogue_no_release": [0, 1, 1]}
+
+
+@pytest.mark.parametrize("mutation", pc.ZERO_K_MUTATIONS)
+@pytest.mark.parametrize("tile", ["128x128", "128x256", "256x256"])
+@pytest.mark.parametrize("sched", ["static", "clc"])
+def test_zero_k_mistakes_are_caught(mutation, tile, sched):
+    r = pc.check_variant(tile, ZERO_K_CASES[mutation], sched, stages=2, epilogue_warps=1, mutate=mutation)
+    assert not r.ok and r.status == 1, (mutation, r)
+    # the same sequence without the mistake is clean
+    assert pc.check_variant(tile, ZERO_K_CASES[mutation], sched, stages=2, epilogue_warps=1).ok
+
+
+# ------------------------------------------- the split tiles' counter handoff
+@pytest.mark.parametrize("parts", [2, 3, 4])
+@pytest.mark.parametrize("launches", [1, 2, 3])
+def test_split_handoff_verified(parts, launches):
+    r = pc.check(pc.build_split_program(parts, launches))
+    assert r.ok, r.message
+
+
+@pytest.mark.parametrize("mutation", pc.SPLIT_MUTATIONS)
+@pytest.mark.parametrize("parts", [2, 3, 4])
+def test_split_handoff_mistakes_are_caught(mutation, parts):
+    r = pc.check(pc.build_split_program(parts, 2, mutate=mutation))
+    assert not r.ok and r.status == 1, (mutation, r)
+
+
+def test_engine_ticket_counts_reductions_and_rearm():
+    # two roles draw tickets 0 and 1 of a counter whose last ticket is 1; the last re-arms
+    P = pc.Program()
+    c = P.counter(1)
+    P.buf("x0")
+    P.roles.append(("a", None, [[OP.OP_TICKET, c, 1, 0, 0, 0, 1, -1]]))
+    P.roles.append(("b", None, [[OP.OP_TICKET, c, 1, 0, 0, 0, 1, -1]]))
+    assert pc.check(P).ok
+    P.counters[0] = 2  # expected two reductions: only one happens
+    r = pc.check(P)
+    assert not r.ok and "after 1 reductions" in r.message
+
+
+def test_engine_fence_waits_for_own_stores_only():
+    # b's fence does not wait for a's store, so b may read x0 before it lands
+    P = pc.Program()
+    P.buf("x0")
+    P.roles.append(("a", None, [[OP.OP_GWRITE, 0, 5, -1, -1, -1, -1, -1], [OP.OP_FENCE] + [-1] * 7]))
+    P.roles.append(("b", None, [[OP.OP_FENCE] + [-1] * 7, [OP.OP_TICKET, -1, -1, -1, -1, -1, -1, -1]]))
+    P.roles[1] = ("b", None, [[OP.OP_FENCE] + [-1] * 7])
+    assert pc.check(P).ok
+    c = P.counter(1)
+    P.roles[0] = ("a", None, [[OP.OP_GWRITE, 0, 5, -1, -1, -1, -1, -1], [OP.OP_FENCE] + [-1] * 7,
+                              [OP.OP_TICKET, c, 0, 0, 1, 5, 1, -1]])
+    assert pc.check(P).ok  # a's own fence orders its store before its ticket's read
+    P.roles[0] = ("a", None, [[OP.OP_GWRITE, 0, 5, -1, -1, -1, -1, -1], [OP.OP_TICKET, c, 0, 0, 1, 5, 1, -1]])
+    r = pc.check(P)
+    assert not r.ok and "holding tag -1" in r.message

@@ -89,6 +89,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ts_protocol_check.argtypes = [I32, P, I32, I32, P, P, P, ctypes.c_char_p, I64, ctypes.POINTER(I64),
                                       ctypes.c_char_p, I32]
     lib.ts_protocol_check.restype = I32
+    lib.ts_protocol_check_ex.argtypes = [I32, P, I32, I32, P, P, P, I32, P, ctypes.c_char_p, I64, ctypes.POINTER(I64),
+                                         ctypes.c_char_p, I32]
+    lib.ts_protocol_check_ex.restype = I32
     lib.ts_gemm_bf16_grouped.argtypes = [P, P, P, I64, I64, I64, P, I32, I32, ctypes.POINTER(GemmOpts), P]
     lib.ts_gemm_grouped_launch_info.argtypes = [I64, I64, I64, P, I32, I32, ctypes.POINTER(GemmOpts),
                                                 ctypes.POINTER(LaunchInfo)]
@@ -488,6 +491,14 @@ def ts_spin_wait_started(started: torch.Tensor, expected: int, timeout_s: float 
 
 def ts_protocol_check(program, max_states: int = 20_000_000):
     """Explore a barrier-protocol program (see tile_scheduling_gb300.protocol)."""
+    from .protocol import check
+
+    return check(program, max_states)
+
+
+def ts_protocol_check_ex(program, max_states: int = 20_000_000):
+    """Explore a barrier-protocol program with global counters (the split tiles' handoff); the
+    program's counters and their expected reductions travel with it."""
     from .protocol import check
 
     return check(program, max_states)

@@ -24,10 +24,22 @@
 //   TREAD  buf tag               buf must hold tag
 //   CREQ   slot0 slot1 seq bar0 bar1 bytes  -> async: slots := seq, complete-tx
 //   CREAD  buf seq               buf must hold seq
+//   GWRITE buf tag               -> async: buf := tag (a global-memory store,
+//                                   visible to other roles once it lands)
+//   FENCE                        blocks while a GWRITE of this role is in flight
+//   TICKET ctr last buf0 nbufs tag0 rearm
+//                                fetch-and-add on counter ctr; the role that
+//                                draws `last` re-arms the counter to 0 (if rearm)
+//                                and reads bufs buf0 .. buf0 + nbufs - 1, which
+//                                must hold tag0, tag0 + 1, ...
+//   TREADB buf limit             buf must hold a tag below limit (a read whose
+//                                data is discarded: only a later writer races it)
 // (negative operands mean "none"; tags are unit * 1024 + k-block.)  A role step
-// runs one wait or arrive plus the ops after it that only enqueue work or, after
-// a wait, only check a buffer: their effects become visible later, through the
-// queue or the async completions, which are explored separately.
+// runs one wait, fence, arrive or ticket plus the ops after it that only enqueue
+// work or, after a wait, only check a buffer: their effects become visible
+// later, through the queue or the async completions, which are explored
+// separately.  Counters start at 0; when every role has finished, each must be
+// back at 0 and have been drawn `last` exactly its expected number of times.
 #include <algorithm>
 #include <cstdio>
 #include <cstring>
@@ -39,17 +51,30 @@
 namespace ts {
 namespace {
 
-enum : int32_t { OP_WAIT = 0, OP_ARRIVE, OP_TMA, OP_MMA, OP_COMMIT, OP_TREAD, OP_CREQ, OP_CREAD };
+enum : int32_t {
+    OP_WAIT = 0,
+    OP_ARRIVE,
+    OP_TMA,
+    OP_MMA,
+    OP_COMMIT,
+    OP_TREAD,
+    OP_CREQ,
+    OP_CREAD,
+    OP_GWRITE,
+    OP_FENCE,
+    OP_TICKET,
+    OP_TREADB
+};
 constexpr int kRec = 8;
 constexpr int kMaxQueue = 32;
 constexpr int kMaxAsync = 32;
 
 struct Model {
-    int nbars, nbufs, nroles;
-    const int32_t *expected, *group, *off, *ops;
+    int nbars, nbufs, nroles, nctrs;
+    const int32_t *expected, *group, *off, *ops, *ctr_expected;
     std::vector<std::string> role_name, bar_name, buf_name;
     // state layout offsets
-    int o_pc, o_bar, o_buf, o_mq, o_asy, len;
+    int o_pc, o_bar, o_buf, o_mq, o_asy, o_ctr, len;
 };
 
 struct Checker {
@@ -152,10 +177,44 @@ struct Checker {
             while (pc < end) {
                 const int32_t *o = op(m.off[i] + pc);
                 const int kind = o[0];
-                if ((kind == OP_WAIT || kind == OP_ARRIVE) && !first) break;
-                if ((kind == OP_TREAD || kind == OP_CREAD) && arrived) break;
+                if ((kind == OP_WAIT || kind == OP_ARRIVE || kind == OP_FENCE || kind == OP_TICKET) && !first) break;
+                if ((kind == OP_TREAD || kind == OP_CREAD || kind == OP_TREADB) && arrived) break;
                 if (kind == OP_WAIT) {
                     if (t[m.o_bar + 3 * o[1]] % 2 == o[2]) break;
+                } else if (kind == OP_FENCE) {
+                    bool pending = false;
+                    for (int k = 0; k < t[m.o_asy]; ++k) {
+                        const int idx = t[m.o_asy + 1 + k];
+                        pending |= idx >= m.off[i] && idx < m.off[i + 1];
+                    }
+                    if (pending) break;
+                } else if (kind == OP_TICKET) {
+                    const int c = o[1];
+                    const int drawn = t[m.o_ctr + 2 * c];
+                    t[m.o_ctr + 2 * c] = drawn + 1;
+                    if (drawn == o[2]) {
+                        if (o[6]) t[m.o_ctr + 2 * c] = 0;
+                        t[m.o_ctr + 2 * c + 1] += 1;
+                        for (int k = 0; k < o[4]; ++k) {
+                            if (t[m.o_buf + o[3] + k] != o[5] + k) {
+                                char b[256];
+                                snprintf(b, sizeof b, "%s: reduction read %s holding tag %d, expected %d",
+                                         m.role_name[i].c_str(), m.buf_name[o[3] + k].c_str(),
+                                         t[m.o_buf + o[3] + k], o[5] + k);
+                                return violation(b);
+                            }
+                        }
+                    }
+                    arrived = true;
+                } else if (kind == OP_GWRITE) {
+                    if (!push_list(t, m.o_asy, kMaxAsync, m.off[i] + pc)) return violation("too many copies in flight");
+                } else if (kind == OP_TREADB) {
+                    if (t[m.o_buf + o[1]] >= o[2]) {
+                        char b[256];
+                        snprintf(b, sizeof b, "%s: read of %s found tag %d, written after the read began",
+                                 m.role_name[i].c_str(), m.buf_name[o[1]].c_str(), t[m.o_buf + o[1]]);
+                        return violation(b);
+                    }
                 } else if (kind == OP_ARRIVE) {
                     if (!arrive(t, o[1], o[2]))
                         return violation(m.role_name[i] + ": more arrivals than " + m.bar_name[o[1]] +
@@ -201,7 +260,9 @@ struct Checker {
             t[m.o_asy + na] = -1;
             t[m.o_asy] = na - 1;
             const int32_t *o = op(idx);
-            if (o[0] == OP_TMA) {
+            if (o[0] == OP_GWRITE) {
+                t[m.o_buf + o[1]] = o[2];
+            } else if (o[0] == OP_TMA) {
                 const int nq = s[m.o_mq];
                 for (int q = 0; q < nq; ++q) {
                     const int32_t *mo = op(s[m.o_mq + 1 + q]);
@@ -286,7 +347,18 @@ struct Checker {
                     msg = "deadlock: " + blocked;
                     return 1;
                 }
-                continue;  // every role finished, nothing in flight
+                // every role finished, nothing in flight: every counter re-armed and
+                // drawn last as often as expected
+                for (int c = 0; c < m.nctrs; ++c) {
+                    if (s[m.o_ctr + 2 * c] != 0 || s[m.o_ctr + 2 * c + 1] != m.ctr_expected[c]) {
+                        char b[256];
+                        snprintf(b, sizeof b, "counter %d ends at %d after %d reductions (expected 0 after %d)", c,
+                                 s[m.o_ctr + 2 * c], s[m.o_ctr + 2 * c + 1], m.ctr_expected[c]);
+                        msg = b;
+                        return 1;
+                    }
+                }
+                continue;
             }
             for (auto &t : succ) {
                 canon(t);
@@ -322,15 +394,17 @@ std::vector<std::string> split_lines(const char *s) {
 }  // namespace
 }  // namespace ts
 
-extern "C" int32_t ts_protocol_check(int32_t nbars, const int32_t *bar_expected, int32_t nbufs, int32_t nroles,
-                                     const int32_t *role_group, const int32_t *role_offsets, const int32_t *ops,
-                                     const char *names, int64_t max_states, int64_t *states_out, char *msg,
-                                     int32_t msg_len) {
+extern "C" int32_t ts_protocol_check_ex(int32_t nbars, const int32_t *bar_expected, int32_t nbufs, int32_t nroles,
+                                        const int32_t *role_group, const int32_t *role_offsets, const int32_t *ops,
+                                        int32_t ncounters, const int32_t *counter_reductions, const char *names,
+                                        int64_t max_states, int64_t *states_out, char *msg, int32_t msg_len) {
     using namespace ts;
     if (nbars < 0 || nbufs < 0 || nroles <= 0 || !bar_expected || !role_group || !role_offsets || !ops ||
-        max_states <= 0 || !msg || msg_len <= 0)
+        ncounters < 0 || (ncounters > 0 && !counter_reductions) || max_states <= 0 || !msg || msg_len <= 0)
         return -1;
     Model m;
+    m.nctrs = ncounters;
+    m.ctr_expected = counter_reductions;
     m.nbars = nbars;
     m.nbufs = nbufs;
     m.nroles = nroles;
@@ -348,10 +422,19 @@ extern "C" int32_t ts_protocol_check(int32_t nbars, const int32_t *bar_expected,
     m.o_buf = m.o_bar + 3 * nbars;
     m.o_mq = m.o_buf + nbufs;
     m.o_asy = m.o_mq + 1 + kMaxQueue;
-    m.len = m.o_asy + 1 + kMaxAsync;
+    m.o_ctr = m.o_asy + 1 + kMaxAsync;
+    m.len = m.o_ctr + 2 * ncounters;
     Checker c(m, max_states);
     const int rc = c.run();
     if (states_out) *states_out = c.states;
     snprintf(msg, static_cast<size_t>(msg_len), "%s", c.msg.c_str());
     return rc;
+}
+
+extern "C" int32_t ts_protocol_check(int32_t nbars, const int32_t *bar_expected, int32_t nbufs, int32_t nroles,
+                                     const int32_t *role_group, const int32_t *role_offsets, const int32_t *ops,
+                                     const char *names, int64_t max_states, int64_t *states_out, char *msg,
+                                     int32_t msg_len) {
+    return ts_protocol_check_ex(nbars, bar_expected, nbufs, nroles, role_group, role_offsets, ops, 0, nullptr, names,
+                                max_states, states_out, msg, msg_len);
 }

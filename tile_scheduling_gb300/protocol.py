@@ -18,14 +18,23 @@ responses) and reports
 * a race: an MMA reads a ring stage (or, in the Merge layout, either half of
   it) that does not hold the k-block it expects
   (overwritten early or not yet landed) or accumulates onto the wrong partial
-  sum, an epilogue reads an accumulator that is not the finished tile, or a
+  sum, an epilogue reads an accumulator that is not the finished tile (or,
+  for a unit with no k-blocks, one that a later unit already writes), or a
   CLC response slot is refilled before every role read it.
 
 A model is one worker (a CTA, or a CTA pair) over a short sequence of work
-units.  Epilogue warps run identical, independent programs, so a model may
-keep fewer of them than the kernel has; the barriers they arrive on then
-expect exactly the removed warps' arrivals fewer, so a miscount in the
-kernel's constants still shows.
+units.  A unit has k-blocks (a whole tile or one K part of a split tile),
+none (a group with K = 0 of a grouped GEMM: the MMA takes an accumulator and
+commits it with no MMA issued, the epilogue reads and releases it), or is
+skipped (TS "Schedules", Skippable Tiles: every role takes the unit from the
+queue, but no load is issued and no accumulator is taken).  A second model,
+build_split_program, covers the one protocol that crosses workers: the split
+tiles' partials handed over through a per-slab counter in global memory.
+
+Epilogue warps run identical, independent programs, so a model may keep fewer
+of them than the kernel has; the barriers they arrive on then expect exactly
+the removed warps' arrivals fewer, so a miscount in the kernel's constants
+still shows.
 """
 from __future__ import annotations
 
@@ -36,10 +45,16 @@ import numpy as np
 
 from . import _lib
 
-OP_WAIT, OP_ARRIVE, OP_TMA, OP_MMA, OP_COMMIT, OP_TREAD, OP_CREQ, OP_CREAD = range(8)
+OP_WAIT, OP_ARRIVE, OP_TMA, OP_MMA, OP_COMMIT, OP_TREAD, OP_CREQ, OP_CREAD, OP_GWRITE, OP_FENCE, OP_TICKET, \
+    OP_TREADB = range(12)
+SKIP = -1  # a skipped tile in a unit sequence
+# mistakes that show only on units with no k-blocks (a skipped tile or a K = 0 group)
+ZERO_K_MUTATIONS = ("mma_takes_skipped_accumulator", "epilogue_waits_skipped_tile", "zero_k_mma_no_commit",
+                    "zero_k_epilogue_no_release")
 MUTATIONS = ("tmem_empty_count_low", "tmem_empty_count_high", "clc_empty_count_low", "tx_bytes_one_cta",
              "producer_wait_parity", "epilogue_release_before_read", "mma_skip_stage_release",
-             "fork_producer_ignores_second_consumer", "merge_mma_skips_b_wait")
+             "fork_producer_ignores_second_consumer", "merge_mma_skips_b_wait") + ZERO_K_MUTATIONS
+SPLIT_MUTATIONS = ("split_no_fence", "split_no_rearm", "split_last_early")
 
 
 def _tag(unit: int, kb: int) -> int:
@@ -52,6 +67,7 @@ class Program:
     bar_names: list = field(default_factory=list)
     bufs: list = field(default_factory=list)
     roles: list = field(default_factory=list)  # (name, group or None, [op records])
+    counters: list = field(default_factory=list)  # expected reductions of each global counter
 
     def bar(self, name: str, count: int) -> int:
         self.bars.append(int(count))
@@ -62,13 +78,18 @@ class Program:
         self.bufs.append(name)
         return len(self.bufs) - 1
 
+    def counter(self, reductions: int) -> int:
+        self.counters.append(int(reductions))
+        return len(self.counters) - 1
+
 
 def build_program(proto: dict, units: list, sched: str = "static", epilogue_warps: int | None = None,
                   stages: int | None = None, mutate: str | None = None, fork: bool = False) -> Program:
     """The kernel's role loops for one worker.
 
     proto           ts_gemm_protocol_info() of the variant.
-    units           k-blocks of each work unit the worker processes, in order.
+    units           k-blocks of each work unit the worker processes, in order:
+                    n > 0 k-blocks, 0 (a K = 0 group) or SKIP (a skipped tile).
     sched           "static", or "clc": after each unit every role consumes one
                     response; the first len(units) - 1 name a unit, the last fails.
     epilogue_warps  epilogue warps per CTA to model (default: the kernel's).
@@ -93,6 +114,8 @@ def build_program(proto: dict, units: list, sched: str = "static", epilogue_warp
         raise ValueError("merge_mma_skips_b_wait needs a Merge variant")
     if mutate is not None and mutate not in MUTATIONS:
         raise ValueError(f"unknown mutation {mutate}")
+    if any(nk != SKIP and nk < 0 for nk in units):
+        raise ValueError("a unit has n >= 0 k-blocks or is SKIP")
     cg = proto["cluster"]
     S = stages or proto["stages"]
     E = proto["epilogue_warps"] if epilogue_warps is None else epilogue_warps
@@ -140,7 +163,7 @@ def build_program(proto: dict, units: list, sched: str = "static", epilogue_warp
         for c in range(cg):
             ops, s, ph, issued = [], 0, 0, 0
             for u, nk in enumerate(units):
-                for kb in range(nk):
+                for kb in range(max(nk, 0)):  # a skipped tile or a K = 0 group loads nothing
                     ops.append(rec(OP_WAIT, empty[c][s], ph if mutate == "producer_wait_parity" else ph ^ 1))
                     if fork and mutate != "fork_producer_ignores_second_consumer":
                         ops.append(rec(OP_WAIT, aux_empty[s], ph ^ 1))
@@ -164,8 +187,12 @@ def build_program(proto: dict, units: list, sched: str = "static", epilogue_warp
 
     ops, s, ph, a, aph = [], 0, 0, 0, 0  # MMA issuer of the even CTA
     for u, nk in enumerate(units):
+        if nk == SKIP and mutate != "mma_takes_skipped_accumulator":
+            if clc:  # a skipped tile takes no accumulator; the queue still advances
+                consume(ops, 0, u)
+            continue
         ops.append(rec(OP_WAIT, tempty[a], aph ^ 1))
-        for kb in range(nk):
+        for kb in range(max(nk, 0)):
             ops.append(rec(OP_WAIT, full[0][s], ph))
             if merge and mutate != "merge_mma_skips_b_wait":
                 ops.append(rec(OP_WAIT, full_b[s], ph))
@@ -174,7 +201,9 @@ def build_program(proto: dict, units: list, sched: str = "static", epilogue_warp
             if not (mutate == "mma_skip_stage_release" and u == 0 and kb == 0):
                 ops.append(rec(OP_COMMIT, empty[0][s], empty[1][s] if cg == 2 else -1))
             s, ph = adv(s, ph, S)
-        ops.append(rec(OP_COMMIT, tfull[0][a], tfull[1][a] if cg == 2 else -1))
+        if not (mutate == "zero_k_mma_no_commit" and nk == 0):
+            # with no k-block the commit completes at once: the epilogue finds an empty sum
+            ops.append(rec(OP_COMMIT, tfull[0][a], tfull[1][a] if cg == 2 else -1))
         a, aph = adv(a, aph, A)
         if clc:
             consume(ops, 0, u)
@@ -184,10 +213,23 @@ def build_program(proto: dict, units: list, sched: str = "static", epilogue_warp
         for w in range(E):
             ops, a, aph = [], 0, 0
             for u, nk in enumerate(units):
+                if nk == SKIP and mutate != "epilogue_waits_skipped_tile":
+                    if clc:  # a skipped tile stores nothing and takes no accumulator
+                        consume(ops, c, u)
+                    continue
                 ops.append(rec(OP_WAIT, tfull[c][a], aph))
-                read = rec(OP_TREAD, accb[a], _tag(u, nk - 1))
+                if nk > 0:
+                    read = rec(OP_TREAD, accb[a], _tag(u, nk - 1))
+                else:
+                    # K = 0 (or a skipped tile under the mutation): the accumulator's old
+                    # contents are read and discarded (zeros are stored); only a later
+                    # unit's MMA writing it during the read would be a race
+                    read = rec(OP_TREADB, accb[a], _tag(u, 0))
                 release = rec(OP_ARRIVE, tempty[a], 0)
-                ops += [release, read] if mutate == "epilogue_release_before_read" else [read, release]
+                if mutate == "zero_k_epilogue_no_release" and nk == 0:
+                    ops.append(read)
+                else:
+                    ops += [release, read] if mutate == "epilogue_release_before_read" else [read, release]
                 a, aph = adv(a, aph, A)
                 if clc:
                     consume(ops, c, u)
@@ -196,7 +238,7 @@ def build_program(proto: dict, units: list, sched: str = "static", epilogue_warp
     if fork:  # the Fork pipeline group's second consumer of the ring
         ops, s, ph = [], 0, 0
         for u, nk in enumerate(units):
-            for kb in range(nk):
+            for kb in range(max(nk, 0)):
                 ops += [rec(OP_WAIT, full[0][s], ph), rec(OP_TREAD, stage[0][s], _tag(u, kb)),
                         rec(OP_ARRIVE, aux_empty[s], 0)]
                 s, ph = adv(s, ph, S)
@@ -242,12 +284,13 @@ def check(P: Program, max_states: int = 20_000_000) -> Result:
     bars = np.ascontiguousarray(np.array(P.bars, dtype=np.int32))
     grp = np.ascontiguousarray(np.array(role_group, dtype=np.int32))
     off = np.ascontiguousarray(np.array(offsets, dtype=np.int32))
+    ctrs = np.ascontiguousarray(np.array(P.counters if P.counters else [0], dtype=np.int32))
     names = "\n".join([n for n, _, _ in P.roles] + P.bar_names + P.bufs).encode()
     msg = ctypes.create_string_buffer(512)
     states = ctypes.c_int64(0)
-    rc = _lib.ts_protocol_check(len(P.bars), bars.ctypes.data, len(P.bufs), len(P.roles), grp.ctypes.data,
-                                off.ctypes.data, ops.ctypes.data, names, int(max_states), ctypes.byref(states), msg,
-                                len(msg))
+    rc = _lib.ts_protocol_check_ex(len(P.bars), bars.ctypes.data, len(P.bufs), len(P.roles), grp.ctypes.data,
+                                   off.ctypes.data, ops.ctypes.data, len(P.counters), ctrs.ctypes.data, names,
+                                   int(max_states), ctypes.byref(states), msg, len(msg))
     if rc < 0:
         raise ValueError("ts_protocol_check rejected the program")
     return Result(rc == 0, rc, int(states.value), msg.value.decode())
@@ -261,3 +304,41 @@ def check_variant(tile: str, units: list, sched: str = "static", out: int = 0, m
 
     proto = ts_gemm_protocol_info(tile, out, variant_epi_warps, variant_merge)
     return check(build_program(proto, units, sched, **kw), max_states)
+
+
+def build_split_program(parts: int, launches: int = 2, mutate: str | None = None) -> Program:
+    """The split tiles' handoff of one 32-row slab, across the workers of its K parts.
+
+    Part p (a different worker each) stores its fp32 partial of the slab, fences
+    (__threadfence), and adds one to the slab's counter in global memory; the part
+    that draws ticket parts - 1 re-arms the counter to 0 and sums the partials of
+    every part (gemm_kernel.cuh, the split epilogue).  Nothing waits on another
+    worker.  `launches` kernel launches run back to back on the same workspace
+    (a barrier stands for the launch boundary), so a counter left armed shows as
+    a launch with no reduction.  Checked: every reduction reads each part's
+    partial of its own launch, and each launch reduces exactly once.
+
+    mutate: "split_no_fence" (the ticket may overtake the partial's store),
+    "split_no_rearm" (the counter is left at `parts`), "split_last_early" (the
+    part that draws ticket parts - 2 reduces)."""
+    if parts < 2:
+        raise ValueError("a split tile has at least two parts")
+    if mutate is not None and mutate not in SPLIT_MUTATIONS:
+        raise ValueError(f"unknown mutation {mutate}")
+    P = Program()
+    ctr = P.counter(launches)
+    partial = [P.buf(f"partial[{p}]") for p in range(parts)]
+    boundary = P.bar("launch_boundary", parts)
+    last = parts - (2 if mutate == "split_last_early" else 1)
+    rearm = 0 if mutate == "split_no_rearm" else 1
+    for p in range(parts):
+        ops = []
+        for L in range(launches):
+            ops.append([OP_GWRITE, partial[p], L * 1024 + p, -1, -1, -1, -1, -1])
+            if mutate != "split_no_fence":
+                ops.append([OP_FENCE, -1, -1, -1, -1, -1, -1, -1])
+            ops.append([OP_TICKET, ctr, last, partial[0], parts, L * 1024, rearm, -1])
+            ops.append([OP_ARRIVE, boundary, 0, -1, -1, -1, -1, -1])
+            ops.append([OP_WAIT, boundary, L & 1, -1, -1, -1, -1, -1])
+        P.roles.append((f"part[{p}]", None, ops))
+    return P
