@@ -175,6 +175,7 @@ class NvmlLib:
             raise OSError("nvmlInit_v2 failed")
         self._reasons = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
             self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        self._max = {}  # the maximum SM clock is fixed; its query takes ~1.5 ms, so it is asked once
 
     def handle(self, uuid: str | None, pci_bus_id: str | None, index: int):
         ct = self.ct
@@ -190,14 +191,18 @@ class NvmlLib:
     def sample(self, h):
         """(sm_mhz, sm_max_mhz, power_w or None, reason bits)."""
         ct = self.ct
-        clk, mx, mw, rs = ct.c_uint(), ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        clk, mw, rs = ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
         if self.lib.nvmlDeviceGetClockInfo(h, self.CLOCK_SM, ct.byref(clk)) != 0:
             raise OSError("nvmlDeviceGetClockInfo failed")
-        if self.lib.nvmlDeviceGetMaxClockInfo(h, self.CLOCK_SM, ct.byref(mx)) != 0:
-            raise OSError("nvmlDeviceGetMaxClockInfo failed")
+        key = h.value
+        if key not in self._max:
+            mx = ct.c_uint()
+            if self.lib.nvmlDeviceGetMaxClockInfo(h, self.CLOCK_SM, ct.byref(mx)) != 0:
+                raise OSError("nvmlDeviceGetMaxClockInfo failed")
+            self._max[key] = float(mx.value)
         power = float(mw.value) / 1e3 if self.lib.nvmlDeviceGetPowerUsage(h, ct.byref(mw)) == 0 else None
         bits = int(rs.value) if self._reasons(h, ct.byref(rs)) == 0 else 0
-        return float(clk.value), float(mx.value), power, bits
+        return float(clk.value), self._max[key], power, bits
 
 
 class NvmlClockSampler:
@@ -234,6 +239,10 @@ class NvmlClockSampler:
     def start(self):
         if self.nvml is None:
             return
+        # the launching thread holds the interpreter for up to the switch interval
+        # (5 ms by default) at a time: shorten it so the sampler keeps its period
+        self._switch = sys.getswitchinterval()
+        sys.setswitchinterval(min(self._switch, self.period / 4))
         self._t = threading.Thread(target=self._run, daemon=True)
         self._t.start()
 
@@ -250,6 +259,7 @@ class NvmlClockSampler:
         self._stop.set()
         if self._t:
             self._t.join(timeout=5)
+            sys.setswitchinterval(self._switch)
 
     def region(self, name: str, t0: float, t1: float):
         self.regions.append((name, t0, t1))

@@ -1,8 +1,10 @@
-"""The split tail: the last, partial wave of tiles split along K across idle workers.
+"""Split tiles: the tiles that would leave the last wave partly empty, split along K.
 
-Each part writes an fp32 partial to the workspace; the warp that finishes a
-32-row slab last sums the parts in part order and stores D, then re-arms the
-slab counter.  Integer inputs must stay bit-exact, random inputs within the
+Their parts are the first work units, so that the partial writes and the
+reduction run in the epilogue while the mainloop already computes the next
+tiles.  Each part writes an fp32 partial to the workspace; the warp that
+finishes a 32-row slab last sums the parts in part order and stores D, then
+re-arms the slab counter.  Integer inputs must stay bit-exact, random inputs within the
 bound, the result must not depend on which part finished last, and the
 workspace must come back zeroed.
 """
@@ -118,3 +120,30 @@ def test_split_disabled_by_option(lib):
     info = lib.ts_gemm_launch_info(2048, 2560, 4096, lib.TS_OUT_BF16, "static", tile="128x256", workspace=ws,
                                    split_tail=-1)
     assert info["split_tiles"] == 0 and info["num_units"] == info["num_tiles"]
+
+
+@pytest.mark.parametrize("sched", ["static", "clc"])
+def test_split_parts_are_the_first_units(lib, sched):
+    # units 0 .. split_tiles * parts - 1 are the K parts of tiles 0 .. split_tiles - 1
+    M, N, K = 2560, 2560, 4096
+    A, B, ref = _integer_case(M, N, K)
+    need = _info(lib, M, N, K, lib.TS_OUT_F32, sched, "256x256", None)["workspace_bytes"]
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    info = _info(lib, M, N, K, lib.TS_OUT_F32, sched, "256x256", ws)
+    S, P = info["split_tiles"], info["split_parts"]
+    assert S > 0
+    trace = torch.zeros(4 * info["num_units"], dtype=torch.int64, device="cuda")
+    D = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    lib.ts_gemm_bf16_ex(to_device_bf16(A), to_device_bf16(B), D, sched=sched, tile="256x256", workspace=ws,
+                        trace=trace)
+    lib.ts_sync_and_check()
+    assert_bit_exact(D, ref, f"split-first {sched}")
+    tr = trace.view(-1, 4).cpu().numpy()
+    if sched == "static":
+        # every split part runs as the first unit of its worker
+        owner = tr[:, 1]
+        assert len(set(owner[:S * P].tolist())) == S * P
+        first = {}
+        for u in range(info["num_units"]):
+            first.setdefault(int(owner[u]), u)
+        assert all(first[int(owner[u])] == u for u in range(S * P))

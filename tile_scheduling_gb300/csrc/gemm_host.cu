@@ -244,8 +244,10 @@ ts_status plan_gemm(const void *D, int64_t M, int64_t N, int64_t K, int32_t out,
     if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
     if (resident <= 0) return fail(TS_ERR_UNSUPPORTED, "kernel cannot be resident on this device");
     pl->resident = resident;
-    // Split tail: when the tiles do not fill the last wave of W workers, the
-    // r = tiles mod W leftover tiles are split along K into s = W / r parts.
+    // Split wave: when the tiles do not fill the last wave of W workers, r =
+    // tiles mod W tiles are split along K into s = W / r parts, and those parts
+    // are scheduled first, so that their partial writes and reduction overlap
+    // the next tiles' mainloops rather than trail the launch.
     int64_t W = resident;
     if (sched == TS_SCHED_STATIC && o->max_workers > 0) W = std::min<int64_t>(W, o->max_workers);
     const int64_t nk = cdiv(K, 64);

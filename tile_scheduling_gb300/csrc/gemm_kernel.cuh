@@ -96,7 +96,7 @@ struct GemmCfg {
     // the ring keeps its depth (the warps of a quarter alternate); 64 KB with
     // 16, which costs the ring one stage (only short K loops use them)
     static constexpr int EPI_BUFS = EPI_WARPS == 4 ? 2 : 1;
-    static constexpr bool SPLIT = EPI_WARPS != 16;  // the split tail's reduction is compiled in
+    static constexpr bool SPLIT = EPI_WARPS != 16;  // the split tiles' reduction is compiled in
     static constexpr int EPI_BYTES = EPI_WARPS * EPI_BUFS * EPI_BUF;
     static constexpr int TMEM_COLS = 2 * BN;           // two accumulators
     static constexpr int BAR_BYTES = 256;
@@ -232,11 +232,11 @@ struct Smem {
     __device__ __forceinline__ uint32_t full_b(int s) const { return aux_empty(s); }
 };
 
-// One work unit: a whole output tile, or one K-range of a split tail tile.
+// One work unit: a whole output tile, or one K-range of a split tile.
 struct Unit {
     int32_t tile;      // output tile id within its group (raster order)
     int32_t kb0, kb1;  // k-blocks [kb0, kb1)
-    int32_t tail;      // index among the split tail tiles, or -1 for a whole tile
+    int32_t tail;      // index among the split tiles, or -1 for a whole tile
     int32_t part;      // K part of a split tile
     int32_t group;     // group of a grouped GEMM (0 otherwise)
     bool skip;         // the tile is skipped: no data work, only queue bookkeeping
@@ -253,19 +253,19 @@ __device__ __forceinline__ Unit decode_unit(int32_t u, const GemmParams &p) {
         w.kb1 = p.group_kb[w.group + 1];
         w.tail = -1;
         w.part = 0;
-    } else if (u < p.full_tiles) {
-        w.tile = u;
+    } else if (u < p.split_tiles * p.parts) {
+        // a K part of a split tile (those units come first)
+        w.tail = u / p.parts;
+        w.part = u - w.tail * p.parts;
+        w.tile = w.tail;
+        w.kb0 = static_cast<int32_t>(static_cast<int64_t>(w.part) * p.num_k_blocks / p.parts);
+        w.kb1 = static_cast<int32_t>(static_cast<int64_t>(w.part + 1) * p.num_k_blocks / p.parts);
+    } else {
+        w.tile = u - p.split_tiles * (p.parts - 1);
         w.kb0 = 0;
         w.kb1 = p.num_k_blocks;
         w.tail = -1;
         w.part = 0;
-    } else {
-        const int32_t v = u - p.full_tiles;
-        w.tail = v / p.parts;
-        w.part = v - w.tail * p.parts;
-        w.tile = p.full_tiles + w.tail;
-        w.kb0 = static_cast<int32_t>(static_cast<int64_t>(w.part) * p.num_k_blocks / p.parts);
-        w.kb1 = static_cast<int32_t>(static_cast<int64_t>(w.part + 1) * p.num_k_blocks / p.parts);
     }
     // Skippable tiles (TS "Schedules", Skippable Tiles): every role still takes
     // and advances past the unit, but a skipped tile loads, multiplies and
@@ -715,6 +715,13 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
             const Unit w = decode_unit(unit, p);
             int32_t mb, nb;
             raster(w.tile, p, mb, nb);
+            // The next unit is taken as soon as this warp has handed the accumulator
+            // back, before its stores (and a split unit's partial write and reduction):
+            // the epilogue is the last consumer of each CLC response, so taking it early
+            // frees the slot for the scheduler's next request sooner.  Measured at
+            // 4096^3, 2-CTA CLC with split tiles: 80.7 -> 76.2 us.
+            int32_t nu = 0;
+            bool taken = false;
             const int32_t row0 = mb * C::TILE_M + static_cast<int32_t>(rank) * C::BM + 32 * q;
             const int32_t col0 = nb * BN;
             const bool split = C::SPLIT && w.tail >= 0;  // the host plans no split for 16 warps
@@ -753,6 +760,8 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
                         else
                             mbar_arrive_cluster(mapa(sm.tempty(acc), 0));
                     }
+                    if (lane == 0) nu = next_unit(sm, p, unit, clc_idx);
+                    taken = true;
                 }
                 if (split) {
 #pragma unroll
@@ -830,8 +839,7 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
                 p.trace[4 * unit + 1] = worker;
                 p.trace[4 * unit + 3] = static_cast<long long>(globaltimer());
             }
-            int32_t nu = 0;
-            if (lane == 0) nu = next_unit(sm, p, unit, clc_idx);
+            if (!taken && lane == 0) nu = next_unit(sm, p, unit, clc_idx);  // a skipped tile
             unit = __shfl_sync(0xffffffffu, nu, 0);
         }
         if (lane == 0) bulk_wait<0>();

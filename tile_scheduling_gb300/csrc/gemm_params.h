@@ -34,12 +34,17 @@ constexpr int kMaxParts = 4;
 // parameter block.
 constexpr int kMaxGroups = 256;
 
-// Work units: units [0, full_tiles) are whole tiles (unit u = tile u).  The
-// last split_tiles tiles are each split along K into `parts` units; unit
-// full_tiles + t * parts + p covers k-blocks [p * nk / parts, (p + 1) * nk / parts)
-// of tile full_tiles + t.  Split units write fp32 partials to `workspace`; the
-// warp that finishes a 32-row slab last (per-slab counter) sums the parts in
-// order 0..parts-1 and stores D.
+// Work units: when the tiles would leave the last wave of workers partly
+// empty, split_tiles tiles (tiles 0 .. split_tiles - 1 of the raster) are each
+// split along K into `parts` units, and those units come first: unit
+// t * parts + p (t < split_tiles) covers k-blocks [p * nk / parts,
+// (p + 1) * nk / parts) of tile t.  Units split_tiles * parts onwards are the
+// whole tiles split_tiles, split_tiles + 1, ... (full_tiles of them).  Split
+// units write fp32 partials to `workspace`; the warp that finishes a 32-row
+// slab last (per-slab counter) sums the parts in order 0..parts-1 and stores
+// D.  Scheduled first, a split tile's partial write and reduction run in the
+// epilogue while the mainloop already computes the worker's next tile, instead
+// of after the last wave.
 // Division of a non-negative int32 by a divisor fixed at launch, as a
 // multiply-high and shift (Granlund and Montgomery, "Division by Invariant
 // Integers using Multiplication", 1994): for d >= 1, l = ceil(log2 d),
