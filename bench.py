@@ -211,7 +211,7 @@ class NvmlClockSampler:
     several samples.  `regions` collects (name, t0, t1) of the timed regions; `summary(name)` reduces
     the samples that fall inside one region (or all regions)."""
 
-    def __init__(self, device: int = 0, period_s: float = 0.002, nvml=None):
+    def __init__(self, device: int = 0, period_s: float = 0.001, nvml=None):
         self.period = period_s
         self.samples = []  # (time, sm_mhz, sm_max_mhz, power_w, reason bits)
         self.regions = []

@@ -281,8 +281,9 @@ ts_status ts_gemm_launch_info(int64_t M, int64_t N, int64_t K, int32_t out_dtype
  * ts_gemm_tile_coords -- the output tile that each tile id of the launch
  * ts_gemm_bf16_ex would make covers (host only, no launch).  The kernel's
  * raster walks `raster_group` tile rows down one column band before moving to
- * the next band (a build choice for L2 reuse; the pages leave tile order
- * open).  The host evaluates the very function the kernel runs.
+ * the next band, the bands of odd groups from the right (a build choice for L2
+ * reuse; the pages leave tile order open).  The host evaluates the very
+ * function the kernel runs.
  *
  *   M, N, K, out_dtype, sched, opts   as for ts_gemm_launch_info (opts->tile and
  *                                     opts->raster_group matter)
@@ -307,8 +308,11 @@ ts_status ts_gemm_tile_coords(int64_t M, int64_t N, int64_t K, int32_t out_dtype
  * (room for 65536 output tiles, 2 MiB per device, held until the process
  * exits) instead of caller memory.  The call allocates nothing.  Its first call
  * on a device looks the array's address up and should precede any stream
- * capture.  All calls on a device share the one array: calls that overlap on
- * the GPU race and must be serialised by the caller.
+ * capture; the address is kept for the life of the process, so a
+ * cudaDeviceReset after that first call is not supported (the array may move
+ * when the module is loaded again).  All calls on a device share the one
+ * array: calls that overlap on the GPU race and must be serialised by the
+ * caller.
  *
  *   A, B, D, M, N, K, out_dtype, sched   as for ts_gemm_bf16
  *   bad_tiles  device int32, written asynchronously on `stream` with the number

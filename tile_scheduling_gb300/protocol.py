@@ -218,6 +218,8 @@ def build_program(proto: dict, units: list, sched: str = "static", epilogue_warp
                         consume(ops, c, u)
                     continue
                 ops.append(rec(OP_WAIT, tfull[c][a], aph))
+                if clc:  # the next response is taken as soon as the accumulator is held
+                    consume(ops, c, u)
                 if nk > 0:
                     read = rec(OP_TREAD, accb[a], _tag(u, nk - 1))
                 else:
@@ -231,8 +233,6 @@ def build_program(proto: dict, units: list, sched: str = "static", epilogue_warp
                 else:
                     ops += [release, read] if mutate == "epilogue_release_before_read" else [read, release]
                 a, aph = adv(a, aph, A)
-                if clc:
-                    consume(ops, c, u)
             P.roles.append((f"epilogue[{c}][{w}]", f"epilogue[{c}]", ops))
 
     if fork:  # the Fork pipeline group's second consumer of the ring
