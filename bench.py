@@ -21,7 +21,7 @@ rotating buffer sets so that no launch finds its operands in L2),
 holds 32 SMs for half the solo time: >= 10 alternating static/CLC pairs, the
 median times and each scheduler's launch tail from a traced run) and
 ``smallk`` (8192x8192x64 bf16-out, output-write bound, in HBM GB/s).  Clocks
-are sampled in process through read-only NVML queries every 2 ms during every
+are sampled in process through read-only NVML queries every 1 ms during every
 timed region.
 
 ``--impl reference`` times the CPU oracle (the plain fp64 triple loop) on the

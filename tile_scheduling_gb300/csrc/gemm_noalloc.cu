@@ -13,7 +13,9 @@
 // loads the library holds it (2 MiB) until the process exits.  Its device
 // address is looked up once per device, on the first call made with that
 // device current; that first call should therefore come before any stream
-// capture.  Every call shares the one array per device: calls that overlap on
+// capture.  The address is kept for the life of the process: a cudaDeviceReset
+// after the first call (which may load the module, and the array, elsewhere)
+// is not supported.  Every call shares the one array per device: calls that overlap on
 // the GPU (two streams, or two host threads) race on it, so serialise them.
 // Each call clears the part it uses before the GEMM runs.
 #include <algorithm>
