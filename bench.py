@@ -520,7 +520,8 @@ def measure_gemm4096(ts, sampler, reps=5, batch=20, nset=4):
                   "sched": sched, "us_median": round(med * 1e3, 2), "us_min": round(min(v) * 1e3, 2),
                   "tflops": round(tf, 1), "frac_of_burst": round(tf / peaks["bf16_tflops"], 4),
                   "split_tail": f"{info['split_tiles']} tiles x {info['split_parts']} parts",
-                  "stages": info["stages"], "epi_warps": info["epi_warps"]}
+                  "stages": info["stages"], "epi_warps": info["epi_warps"],
+                  "traffic": load_traffic("gemm", f"{w.M}x{w.N}x{w.K} {tile} {sched}")}
     best_auto = max(("auto static", "auto clc"), key=lambda k: res[k]["tflops"])
     return {"metric": "bf16 GEMM TFLOP/s, 4096^3 bf16-out, static vs CLC, automatic tile and 128x256",
             "unit": "TFLOP/s", "value": res[best_auto]["tflops"], "frac_of_burst": res[best_auto]["frac_of_burst"],
