@@ -102,6 +102,14 @@ def test_clc_protocol_verified_cta_pair(units):
     assert r.ok, r.message
 
 
+@pytest.mark.slow
+def test_clc_protocol_verified_cta_pair_two_epilogue_warps_per_cta():
+    # two epilogue warps per CTA of the pair, interleaved with each other and with the odd
+    # CTA's: ~9.6 million states, about 40 s
+    r = pc.check_variant("256x256", [1, 1], "clc", stages=2, epilogue_warps=2, max_states=30_000_000)
+    assert r.ok, r.message
+
+
 @pytest.mark.parametrize("mutation", [m for m in pc.MUTATIONS
                                       if not m.startswith(("fork", "merge")) and m not in pc.ZERO_K_MUTATIONS])
 @pytest.mark.parametrize("tile,sched,warps", [("128x256", "clc", None), ("256x256", "clc", 1),
