@@ -321,3 +321,30 @@ def test_engine_fence_waits_for_own_stores_only():
     P.roles[0] = ("a", None, [[OP.OP_GWRITE, 0, 5, -1, -1, -1, -1, -1], [OP.OP_TICKET, c, 0, 0, 1, 5, 1, -1]])
     r = pc.check(P)
     assert not r.ok and "holding tag -1" in r.message
+
+
+# ------------------------------------------------- lazy CLC requests (long K loops)
+# The scheduler's request k waits until the producer has nearly loaded unit k (a barrier
+# the producer arrives on once per unit, `lazy_lead` k-blocks before the unit's end), so
+# a worker claims its next unit shortly before it needs it.
+@pytest.mark.parametrize("tile,warps,units", [("128x256", None, [2, 1, 2]), ("128x128", None, [1, pc.SKIP, 0, 1]),
+                                              ("256x256", 1, [3, 1]), ("256x256", 1, [1, pc.SKIP, 0, 1])])
+def test_lazy_clc_protocol_verified(tile, warps, units):
+    r = pc.check_variant(tile, units, "clc", stages=2, epilogue_warps=warps, lazy=True)
+    assert r.ok, r.message
+    # the signal at the first k-block of every unit (a lead as long as the unit)
+    r = pc.check_variant(tile, units, "clc", stages=2, epilogue_warps=warps, lazy=True, lazy_lead=8)
+    assert r.ok, r.message
+
+
+def test_lazy_clc_protocol_verified_fork_and_merge():
+    assert pc.check_variant("128x256", [2, 1], "clc", stages=2, lazy=True, fork=True).ok
+    assert pc.check_variant("128x256", [2, 1], "clc", stages=2, epilogue_warps=2, lazy=True, variant_merge=1).ok
+
+
+@pytest.mark.parametrize("tile,warps", [("128x256", None), ("256x256", 1)])
+def test_lazy_wait_one_unit_late_is_caught(tile, warps):
+    # waiting for the producer to begin the *next* unit deadlocks: that unit needs this request
+    r = pc.check_variant(tile, [2, 1, 2], "clc", stages=2, epilogue_warps=warps, lazy=True,
+                         mutate="lazy_wait_one_unit_late")
+    assert not r.ok and "deadlock" in r.message

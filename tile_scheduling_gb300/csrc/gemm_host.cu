@@ -155,6 +155,11 @@ constexpr int64_t kShortK = 256;
 // Measured on 8192^2 x K, bf16 out, against eight: 5-9 % faster at K = 64,
 // -1 to +5 % at 128, 2-15 % slower from 256 on.
 constexpr int64_t kTinyK = 128;
+// K loops of at least this many k-blocks take lazy CLC requests: the producer
+// needs the next unit only after loading the current one (>= 32 k-blocks, some
+// 8 us), far longer than a request takes.  Shorter loops keep two requests in
+// flight: with one k-block per tile the producer runs several tiles ahead.
+constexpr int64_t kLazyClcKBlocks = 32;
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -494,6 +499,7 @@ ts_status gemm_launch(const void *A, const void *B, void *D, int64_t M, int64_t 
     p.sched = sched;
     p.tma_store = pl.tma_store;
     p.clc_depth = 2;
+    p.clc_lazy = (groups == 0 && p.num_k_blocks >= kLazyClcKBlocks) ? 1 : 0;
     p.D = D;
     p.ldd = pl.ldd;
     const double tmo = o->timeout_s > 0 ? o->timeout_s : kDefaultTimeoutS;

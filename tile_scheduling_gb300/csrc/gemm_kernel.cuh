@@ -59,6 +59,11 @@ namespace ts {
 constexpr int kRoleWarps = 4;       // producer, MMA issuer, CLC scheduler, Fork task or B producer
 constexpr int kSmemLimit = 232448;  // 227 KB: largest opt-in dynamic shared memory per CTA
 constexpr int kMaxClcDepth = 2;
+// Lazy CLC requests: the producer signals that its unit is nearly loaded this
+// many k-blocks before the end of the unit (some 4 us of MMA on the pair tile,
+// plus the ring's lead), so the request for the worker's next unit is issued
+// shortly before that unit is needed rather than when the current one begins.
+constexpr int kLazyLeadKBlocks = 16;
 
 // EW_ epilogue warps: 4 (one per TMEM lane quarter), 8 or 16 (two or four per
 // quarter, splitting the columns).  More warps hide more of the epilogue's
@@ -129,7 +134,7 @@ struct GemmCfg {
     static_assert(STAGES >= 2, "ring too shallow");
     static_assert(SMEM_BYTES <= kSmemLimit, "shared memory budget");
     static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzle atoms must stay 1024-byte aligned");
-    static_assert(3 * STAGES * 8 + 5 * 8 + 2 * kMaxClcDepth * 8 + 16 * kMaxClcDepth + 8 + 4 * EPI_WARPS <= BAR_BYTES,
+    static_assert(3 * STAGES * 8 + 6 * 8 + 2 * kMaxClcDepth * 8 + 16 * kMaxClcDepth + 8 + 4 * EPI_WARPS <= BAR_BYTES,
                   "barrier region");
 };
 
@@ -231,6 +236,13 @@ struct Smem {
     // Merge: B's full barrier of stage s (full(s) then tracks A alone).  The
     // Fork consumer and Merge never run together, so they share the slots.
     __device__ __forceinline__ uint32_t full_b(int s) const { return aux_empty(s); }
+    // The producer arrives here once per work unit, when at most
+    // kLazyLeadKBlocks of the unit's k-blocks remain to be loaded (at once for a
+    // shorter or empty unit): phase j completes when it reaches that point of its
+    // j-th unit (lazy CLC requests wait on it).
+    __device__ __forceinline__ uint32_t prod_began() const {
+        return bars + 8u * (3 * C::STAGES + 5 + 2 * kMaxClcDepth);
+    }
 };
 
 // One work unit: a whole output tile, or one K-range of a split tile.
@@ -328,7 +340,7 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
     sm.epi = sm.b + C::STAGES * C::B_BYTES;
     sm.resp = sm.epi + C::EPI_BYTES;
     sm.bars = sm.resp + 16u * kMaxClcDepth;
-    const uint32_t tail = sm.bars + 8u * (3 * C::STAGES + 5 + 2 * kMaxClcDepth);
+    const uint32_t tail = sm.bars + 8u * (3 * C::STAGES + 6 + 2 * kMaxClcDepth);
     sm.tmem_slot = reinterpret_cast<uint32_t *>(gbase + (tail - base));
     sm.abort_flag = reinterpret_cast<volatile int *>(gbase + (tail - base) + 4);
     sm.next_slot = reinterpret_cast<int32_t *>(gbase + (tail - base) + 8);
@@ -367,6 +379,7 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
         }
         // Fork: the row-sum task's empty barriers; Merge: B's full barriers (one arrival each)
         for (int s = 0; s < C::STAGES; ++s) mbar_init(sm.aux_empty(s), MG ? C::FULL_ARRIVALS : C::AUX_EMPTY_ARRIVALS);
+        mbar_init(sm.prod_began(), 1);
         *sm.abort_flag = 0;
         fence_mbar_init();
     }
@@ -405,12 +418,16 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
         bool alive = true;
         while (unit >= 0 && alive) {
             const Unit w = decode_unit(unit, p);
+            // the k-block at which the unit counts as nearly loaded (lazy CLC requests wait for it)
+            const int32_t near_end = w.kb1 - w.kb0 > kLazyLeadKBlocks ? w.kb1 - kLazyLeadKBlocks : w.kb0;
+            if (load_a && w.kb1 <= w.kb0) mbar_arrive(sm.prod_began());
             int32_t mb, nb;
             raster(w.tile, p, mb, nb);
             const int32_t a_row = mb * C::TILE_M + static_cast<int32_t>(rank) * C::BM;
             const int32_t b_row = nb * BN + static_cast<int32_t>(rank) * C::B_ROWS;
             if (p.trace && rank == 0 && load_a) p.trace[4 * unit + 2] = static_cast<long long>(globaltimer());
             for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
+                if (load_a && kb == near_end) mbar_arrive(sm.prod_began());
                 if (!wait_phase(sm.empty(stage), phase ^ 1u, sm.abort_flag, p, WAIT_PRODUCER_EMPTY) ||
                     (fork && !wait_phase(sm.aux_empty(stage), phase ^ 1u, sm.abort_flag, p, WAIT_PRODUCER_EMPTY))) {
                     alive = false;
@@ -535,6 +552,13 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
                 const uint32_t ph = (idx / depth) & 1u;
                 if (rank == 0) {
                     if (!wait_long(sm.clc_empty(r), ph ^ 1u, sm.abort_flag, p, WAIT_SCHED_CLC_EMPTY)) break;
+                    // Lazy requests (long K loops): request idx names the unit after this
+                    // worker's unit idx, so it waits until the producer has all but the last
+                    // kLazyLeadKBlocks of unit idx loaded (completion idx + 1 of prod_began).
+                    // A worker then claims its next unit shortly before it needs it, not
+                    // when its current unit begins, so the units left late in the launch go
+                    // to the workers that finish first.
+                    if (p.clc_lazy && !wait_long(sm.prod_began(), idx & 1u, sm.abort_flag, p, WAIT_SCHED_PRODUCER)) break;
                     fence_proxy_async_smem();
                     mbar_arrive_expect_tx(sm.clc_full(r), C::CLC_RESPONSE_BYTES);
                     if constexpr (CG == 1)

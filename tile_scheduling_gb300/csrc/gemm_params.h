@@ -17,6 +17,7 @@ enum : int32_t {
     WAIT_CLC_FULL = 6,
     WAIT_DRAIN = 7,
     WAIT_ROWS_CLC = 8,
+    WAIT_SCHED_PRODUCER = 9,
 };
 
 // Device status word (library-owned, one per device):
@@ -68,7 +69,7 @@ struct GemmParams {
     int32_t sched;         // SCHED_STATIC / SCHED_CLC
     int32_t tma_store;     // 1: TMA-store epilogue, 0: st.global epilogue
     int32_t clc_depth;     // response slots in flight (1 or 2)
-    int32_t pad0;
+    int32_t clc_lazy;      // 1: the request for the unit after unit j waits until the producer began unit j
     void *D;               // used by the st.global epilogue
     int64_t ldd;           // elements
     uint64_t timeout_ns;   // per-wait limit

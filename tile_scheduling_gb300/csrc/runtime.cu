@@ -28,6 +28,7 @@ const char *wait_name(int where) {
         case WAIT_CLC_FULL: return "waiting for a CLC response";
         case WAIT_DRAIN: return "waiting for in-flight copies at exit";
         case WAIT_ROWS_CLC: return "row copy waiting for a CLC response";
+        case WAIT_SCHED_PRODUCER: return "CLC scheduler waiting for the producer to begin its unit";
         default: return "unknown wait";
     }
 }

@@ -55,6 +55,7 @@ MUTATIONS = ("tmem_empty_count_low", "tmem_empty_count_high", "clc_empty_count_l
              "producer_wait_parity", "epilogue_release_before_read", "mma_skip_stage_release",
              "fork_producer_ignores_second_consumer", "merge_mma_skips_b_wait") + ZERO_K_MUTATIONS
 SPLIT_MUTATIONS = ("split_no_fence", "split_no_rearm", "split_last_early")
+LAZY_MUTATIONS = ("lazy_wait_one_unit_late",)
 
 
 def _tag(unit: int, kb: int) -> int:
@@ -84,7 +85,8 @@ class Program:
 
 
 def build_program(proto: dict, units: list, sched: str = "static", epilogue_warps: int | None = None,
-                  stages: int | None = None, mutate: str | None = None, fork: bool = False) -> Program:
+                  stages: int | None = None, mutate: str | None = None, fork: bool = False,
+                  lazy: bool = False, lazy_lead: int = 1) -> Program:
     """The kernel's role loops for one worker.
 
     proto           ts_gemm_protocol_info() of the variant.
@@ -99,6 +101,12 @@ def build_program(proto: dict, units: list, sched: str = "static", epilogue_warp
                     row-sum task): it reads every stage after the full barrier and
                     releases it on its own empty barrier; the producer refills a
                     stage only after both consumers released it (one-CTA tiles).
+    lazy            lazy CLC requests (long K loops): the (A) producer of the even
+                    CTA arrives on a barrier once per unit, when at most
+                    `lazy_lead` of its k-blocks remain to be loaded (the kernel's
+                    lead is 16; at once for a shorter or empty unit), and the
+                    scheduler's request k waits for that point of unit k
+                    (completion k + 1) before it is issued.
 
     A variant with proto["merge"] = 1 has the Merge layout of the "Pipeline
     Groups" page: two producers per CTA, one loading A onto full[s] and one
@@ -112,8 +120,10 @@ def build_program(proto: dict, units: list, sched: str = "static", epilogue_warp
         raise ValueError("the Merge layout has no Fork consumer")
     if mutate == "merge_mma_skips_b_wait" and not merge:
         raise ValueError("merge_mma_skips_b_wait needs a Merge variant")
-    if mutate is not None and mutate not in MUTATIONS:
+    if mutate is not None and mutate not in MUTATIONS + LAZY_MUTATIONS:
         raise ValueError(f"unknown mutation {mutate}")
+    if mutate in LAZY_MUTATIONS and not lazy:
+        raise ValueError(f"{mutate} needs lazy requests")
     if any(nk != SKIP and nk < 0 for nk in units):
         raise ValueError("a unit has n >= 0 k-blocks or is SKIP")
     cg = proto["cluster"]
@@ -134,6 +144,8 @@ def build_program(proto: dict, units: list, sched: str = "static", epilogue_warp
         + (1 if fork else 0)
     clc_empty = [P.bar(f"clc_empty[{r}]", clc_empty_n) for r in range(R)]
     aux_empty = [P.bar(f"aux_empty[{s}]", proto["aux_empty_arrivals"]) for s in range(S)] if fork else []
+    clc = sched == "clc"
+    began = P.bar("prod_began", 1) if (lazy and clc) else -1
     stage = [[P.buf(f"stage[{c}][{s}]") for s in range(S)] for c in range(cg)]  # A (and B unless Merge)
     stage_b = [[P.buf(f"stage_b[{c}][{s}]") for s in range(S)] for c in range(cg)] if merge else []
     accb = [P.buf(f"tmem[{a}]") for a in range(A)]
@@ -141,7 +153,6 @@ def build_program(proto: dict, units: list, sched: str = "static", epilogue_warp
     a_bytes = proto["a_stage_bytes"] if merge else proto["stage_bytes"]  # per CTA, onto full[s]
     b_bytes = proto["stage_bytes"] - a_bytes  # per CTA, onto full_b[s] (Merge)
     tx = (proto["tx_bytes"] if not merge else a_bytes * cg) - (a_bytes if mutate == "tx_bytes_one_cta" else 0)
-    clc = sched == "clc"
 
     def rec(*v):
         v = list(v) + [-1] * (8 - len(v))
@@ -162,8 +173,14 @@ def build_program(proto: dict, units: list, sched: str = "static", epilogue_warp
     for name, fbar, sbuf, nbytes, arm in lines:
         for c in range(cg):
             ops, s, ph, issued = [], 0, 0, 0
+            signals = began >= 0 and c == 0 and name in ("producer", "producer_a")
             for u, nk in enumerate(units):
+                near_end = nk - lazy_lead if nk > lazy_lead else 0
+                if signals and nk <= 0:
+                    ops.append(rec(OP_ARRIVE, began, 0))  # an empty unit counts as loaded at once
                 for kb in range(max(nk, 0)):  # a skipped tile or a K = 0 group loads nothing
+                    if signals and kb == near_end:
+                        ops.append(rec(OP_ARRIVE, began, 0))  # unit u nearly loaded
                     ops.append(rec(OP_WAIT, empty[c][s], ph if mutate == "producer_wait_parity" else ph ^ 1))
                     if fork and mutate != "fork_producer_ignores_second_consumer":
                         ops.append(rec(OP_WAIT, aux_empty[s], ph ^ 1))
@@ -252,8 +269,10 @@ def build_program(proto: dict, units: list, sched: str = "static", epilogue_warp
             for k in range(len(units)):
                 r, ph2 = k % R, (k // R) & 1
                 if c == 0:
-                    ops += [rec(OP_WAIT, clc_empty[r], ph2 ^ 1),
-                            rec(OP_ARRIVE, clc_full[0][r], proto["clc_response_bytes"]),
+                    ops.append(rec(OP_WAIT, clc_empty[r], ph2 ^ 1))
+                    if began >= 0:  # request k waits until the producer began unit k
+                        ops.append(rec(OP_WAIT, began, (k + (1 if mutate == "lazy_wait_one_unit_late" else 0)) & 1))
+                    ops += [rec(OP_ARRIVE, clc_full[0][r], proto["clc_response_bytes"]),
                             rec(OP_CREQ, slot[0][r], slot[1][r] if cg == 2 else -1, k, clc_full[0][r],
                                 clc_full[1][r] if cg == 2 else -1, proto["clc_response_bytes"])]
                 else:
