@@ -916,7 +916,7 @@ def run_e2e(args, ts, A_bits, B_bits, M, N, K, ws):
     B = [torch.empty((N, K), dtype=torch.bfloat16, device="cuda") for _ in range(nbuf)]
     D = [torch.empty((M, N), dtype=torch.bfloat16, device="cuda") for _ in range(nbuf)]
     streams = [torch.cuda.Stream() for _ in range(nbuf)]
-    # calls on different streams overlap, so each stream gets its own split-tail workspace (zeroed)
+    # calls on different streams overlap, so each stream gets its own split-tile workspace (zeroed)
     need = ts.ts_gemm_launch_info(M, N, K, ts.TS_OUT_BF16, args.sched, tile=args.tile,
                                   workspace=None)["workspace_bytes"]
     wsp = [torch.zeros(max(need, 256), dtype=torch.uint8, device="cuda") for _ in range(nbuf)]

@@ -58,7 +58,7 @@ typedef struct {
     int32_t raster_group; /* tile raster: consecutive tile ids walk this many tile rows; 0 = 8 */
     int32_t split_tail;   /* 0: split the last, partial wave of tiles along K when `workspace` is
                              large enough; -1: never split */
-    void *workspace;      /* device scratch for the split tail (ts_launch_info.workspace_bytes),
+    void *workspace;      /* device scratch for the split tiles (ts_launch_info.workspace_bytes),
                              256-byte aligned.  Its first 8 KiB hold per-slab counters: zero them
                              before the first use; every normal launch leaves them zero again
                              (after TS_ERR_TIMEOUT zero them once more).  The rest holds fp32
@@ -77,7 +77,7 @@ typedef struct {
                              row_sums[g][i] = sum over the group's K range of A[i][k], the
                              correction term of zero-point-quantised products.  Rows whose first
                              tile column is skipped are left untouched.  1-CTA tiles only (AUTO
-                             picks one; TS_TILE_256x256_2CTA is TS_ERR_UNSUPPORTED); no split tail. */
+                             picks one; TS_TILE_256x256_2CTA is TS_ERR_UNSUPPORTED); no split tiles. */
     int32_t epi_warps;    /* epilogue warps per CTA: 4 (one per TMEM lane quarter), 8 or 16 (two or
                              four per quarter, taking its subtiles in turn: more latency hidden
                              when the epilogue bounds the tile); 0 = automatic: for a plain GEMM
@@ -105,10 +105,10 @@ typedef struct {
     int32_t smem_bytes;      /* dynamic shared memory per CTA */
     int32_t tma_store;       /* 1 if D is written through TMA stores, 0 for the st.global epilogue */
     int64_t num_units;       /* work units scheduled: whole tiles plus the K parts of split tiles */
-    int64_t split_tiles;     /* tiles of the last wave split along K (0 if none) */
+    int64_t split_tiles;     /* tiles split along K, scheduled first (0 if none) */
     int32_t split_parts;     /* K parts per split tile (1 if none) */
     int32_t resident;        /* workers (CTAs or 2-CTA clusters) that fit on the GPU at once */
-    int64_t workspace_bytes; /* workspace a split tail needs (0 when no split would help) */
+    int64_t workspace_bytes; /* workspace the split tiles need (0 when no split would help) */
     int32_t epi_warps;       /* epilogue warps per CTA (4, 8 or 16; CTAs have 128 + 32 * epi_warps threads) */
     int32_t merge;           /* 1: Merge barrier layout (A and B producers apart), 0: FusedMerge */
 } ts_launch_info;
@@ -261,7 +261,7 @@ ts_status ts_gemm_bf16_host(const void *A_host, const void *B_host, void *D_host
  *              may be empty: its D is zero)
  *   groups     1 .. 256
  * opts as for ts_gemm_bf16_ex (tile, max_workers, lda/ldb/ldd, timeout_s, trace
- * with 4 * num_units entries); the split tail is not used.  Work units are the
+ * with 4 * num_units entries); no tiles are split.  Work units are the
  * tiles of group 0, then of group 1, ...
  */
 ts_status ts_gemm_bf16_grouped(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t groups,

@@ -6,7 +6,7 @@ accumulation is exact in any order and the bf16 output is the round to nearest
 even of the exact value; the oracle's float64 BLAS route is exact on the same
 inputs for the same reason.  Every element of D is compared, not a sample.
 The workloads: 4096^3 (128x256 tile and the automatic choice, static and CLC),
-8192^3 on the 2-CTA 256x256 tile under CLC with the split tail planned and
+8192^3 on the 2-CTA 256x256 tile under CLC with the split tiles planned and
 applied, the ragged 8191 x 6143 x 4096 fp32 GEMM at pitches 6144 (TMA stores)
 and 6143 (plain stores) alone and with 32 SMs held by the spin kernel, and the
 small-K 8192 x 8192 x 64 GEMM.

@@ -216,8 +216,8 @@ def ts_gemm_bf16_ex(A: torch.Tensor, B: torch.Tensor, D: torch.Tensor, sched="st
     """D = A @ B.T for bf16 A [M, K] and B [N, K]; D [M, N] is bf16 or fp32.
 
     Rows may be strided (the row stride becomes lda / ldb / ldd).  ``workspace``
-    ("auto": a cached zero-filled buffer; None: no split tail; or a CUDA tensor)
-    lets the last partial wave of tiles be split along K.  ``epi_warps``: 4, 8,
+    ("auto": a cached zero-filled buffer; None: no split tiles; or a CUDA tensor)
+    lets the tiles that would leave the last wave partly empty be split along K.  ``epi_warps``: 4, 8,
     16 (256-column tiles) or 0 (automatic); ``merge``: 1 for the Merge barrier layout (A and B from
     separate producer warps).  Asynchronous on ``stream`` (default: torch's
     current stream)."""
@@ -507,7 +507,7 @@ def ts_protocol_check_ex(program, max_states: int = 20_000_000):
 def ts_sync_and_check(stream=None) -> None:
     """Synchronise and raise TsError for a device-side timeout (or CUDA error).
 
-    After a timeout the cached split-tail workspaces may hold partial counters,
+    After a timeout the cached split-tile workspaces may hold partial counters,
     so they are zeroed again before the error is raised."""
     st = _lib.ts_sync_and_check(_stream_handle(stream))
     if st == TS_ERR_TIMEOUT:

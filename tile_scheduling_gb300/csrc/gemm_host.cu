@@ -131,7 +131,7 @@ struct Plan {
     int64_t lda, ldb, ldd;
     int tma_store;
     int64_t resident;                 // workers that fit at once
-    int64_t split_tiles, parts;       // split tail (0, 1 when not split)
+    int64_t split_tiles, parts;       // split tiles and their K parts (0, 1 when not split)
     int64_t num_units;
     int64_t split_ws_bytes;           // workspace the split would need (0: no split helps)
     int64_t counter_bytes;            // counter region at the start of the workspace
