@@ -27,7 +27,7 @@ enum : int32_t {
 //   [2] number of errors since the last check
 constexpr int kStatusWords = 4;
 
-// Most K parts a split tile is cut into: the reduction loads every part
+// Most K parts a split tail tile is cut into: the reduction loads every part
 // of a 32-column chunk at once, so this bounds its registers.
 constexpr int kMaxParts = 4;
 
