@@ -98,3 +98,33 @@ def test_spin_rejects_bad_arguments(lib):
         lib.ts_spin(1, -5, started)
     with pytest.raises(TypeError):
         lib.ts_spin(1, 1000, torch.zeros(1, dtype=torch.int32))
+
+
+@pytest.mark.parametrize("tile,ew,merge", tile_layouts(["128x256", "256x256"]))
+@pytest.mark.parametrize("held", [0, 32])
+def test_lazy_clc_claims_balance_few_long_units(lib, tile, ew, merge, held):
+    # 2560 x 2560 x 8192: few units per worker and long K loops, so the scheduler's requests
+    # wait until the producer has nearly loaded its unit.  Every unit once, every running
+    # worker starts on its own block's unit, the result bit-exact, with and without SMs held;
+    # no worker ends up with two more whole tiles than another.
+    M, N, K = 2560, 2560, 8192
+    A = synth.int_uniform_bf16(331, (M, K))
+    B = synth.int_uniform_bf16(332, (N, K))
+    started = torch.zeros(1, dtype=torch.int32).pin_memory()
+    if held:
+        side = torch.cuda.Stream()
+        lib.ts_spin(held, 100_000, started, stream=side)
+        lib.ts_spin_wait_started(started, held, 5.0)
+    info, tr, D = _traced(lib, A, B, torch.float32, tile, "clc", epi_warps=ew, merge=merge)
+    torch.cuda.synchronize()
+    ok, why = oracle.clc_coverage_ok(tr[:, 0], tr[:, 1])
+    assert ok, why
+    assert_bit_exact(D, oracle.gemm_f64_blas(A, B), f"lazy CLC {tile} held {held}")
+    if not held:
+        kb = 128  # k-blocks of a whole tile
+        work = {}
+        for u in range(info["num_units"]):
+            w = int(tr[u, 1])
+            part = u < info["split_tiles"] * info["split_parts"]
+            work[w] = work.get(w, 0) + (kb // info["split_parts"] if part else kb)
+        assert max(work.values()) - min(work.values()) <= kb + kb // max(info["split_parts"], 1)

@@ -53,6 +53,28 @@ def test_skipped_tiles_untouched_others_exact(lib, tile, sched, out, ew, merge):
         assert ok, why
 
 
+@pytest.mark.parametrize("tile,ew,merge", tile_layouts(["128x256", "256x256"]))
+def test_skipped_tiles_with_lazy_clc_requests(lib, tile, ew, merge):
+    # K = 2048 (32 k-blocks): CLC requests wait for the producer to near the end of its unit; a
+    # skipped tile has no k-block, so its producer signals at once and the queue keeps moving
+    M, N, K = 2048, 1792, 2048
+    A = synth.int_uniform_bf16(721, (M, K))
+    B = synth.int_uniform_bf16(722, (N, K))
+    info = lib.ts_gemm_launch_info(M, N, K, lib.TS_OUT_F32, "clc", tile=tile, workspace=None)
+    mask = _causal(info["tiles_m"], info["tiles_n"], info["tile_m"], info["tile_n"])
+    trace = torch.zeros(4 * info["num_units"], dtype=torch.int64, device="cuda")
+    D = torch.full((M, N), SENTINEL, dtype=torch.float32, device="cuda")
+    lib.ts_gemm_bf16_ex(to_device_bf16(A), to_device_bf16(B), D, sched="clc", tile=tile, workspace=None,
+                        trace=trace, skip_tiles=torch.from_numpy(mask.reshape(-1)).cuda(), epi_warps=ew, merge=merge)
+    lib.ts_sync_and_check()
+    skipped = _mask_rows_cols(mask, info["tile_m"], info["tile_n"], M, N).astype(bool)
+    ref = oracle.gemm_f64_blas(A, B)
+    ref[skipped] = SENTINEL
+    assert_bit_exact(D, ref, f"skip + lazy CLC {tile}")
+    ok, why = oracle.clc_coverage_ok(trace.view(-1, 4)[:, 0].cpu().numpy(), trace.view(-1, 4)[:, 1].cpu().numpy())
+    assert ok, why
+
+
 def test_every_tile_skipped_leaves_d_alone(lib):
     M, N, K = 512, 512, 128
     A = to_device_bf16(synth.int_uniform_bf16(711, (M, K)))
