@@ -194,8 +194,11 @@ int32_t ts_protocol_check_ex(int32_t nbars, const int32_t *bar_expected, int32_t
  * Tiles are assigned by the static grid-stride rule (TS "Schedules",
  * Scheduling Shapes; "Cluster Launch Control", static persistent scheduler)
  * or by Cluster Launch Control work stealing ("Cluster Launch Control", one
- * CLC request and the overlap loop).  The scheduler changes which CTA computes
- * a tile, never the result.
+ * CLC request and the overlap loop).  Under CLC each worker keeps up to two
+ * requests in flight; with K loops of at least 32 k-blocks a request waits
+ * until the worker's current unit is nearly loaded (16 k-blocks left), so the
+ * last units go to the workers that finish first.  The scheduler changes which
+ * CTA computes a tile, never the result.
  *
  *   A     device, bf16 [M][K] row-major (K contiguous), 16-byte aligned
  *   B     device, bf16 [N][K] row-major (K contiguous), 16-byte aligned
