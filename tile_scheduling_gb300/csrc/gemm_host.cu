@@ -500,6 +500,11 @@ ts_status gemm_launch(const void *A, const void *B, void *D, int64_t M, int64_t 
     p.tma_store = pl.tma_store;
     p.clc_depth = 2;
     p.clc_lazy = (groups == 0 && p.num_k_blocks >= kLazyClcKBlocks) ? 1 : 0;
+    // Units of odd waves walk their K range downwards (see GemmParams::k_alt).  The
+    // wave length is the number of workers that fit at once, whatever the scheduler
+    // or the static cap, so a unit's summation order is a function of the plan alone.
+    p.k_alt = 1;
+    p.div_wave = fast_div_for(pl.resident);
     p.D = D;
     p.ldd = pl.ldd;
     const double tmo = o->timeout_s > 0 ? o->timeout_s : kDefaultTimeoutS;

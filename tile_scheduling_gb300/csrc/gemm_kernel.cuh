@@ -406,8 +406,9 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
 
     const int32_t first_unit = worker < p.num_units ? worker : -1;
 
-    // TMA producer loop of one thread: per k-block, acquire the stage's empty
-    // barrier (and the Fork consumer's), arm full_bar(stage) with `tx` bytes
+    // TMA producer loop of one thread: per k-block of the unit (upwards, or
+    // downwards in the units of odd waves: GemmParams::k_alt), acquire the stage's
+    // empty barrier (and the Fork consumer's), arm full_bar(stage) with `tx` bytes
     // (the even CTA), issue the A and/or B tile loads, which complete on the
     // even CTA's barrier.  FusedMerge: warp 0 loads both onto full(s).  Merge:
     // warp 0 loads A onto full(s) and warp 3 loads B onto full_b(s).
@@ -418,16 +419,19 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
         bool alive = true;
         while (unit >= 0 && alive) {
             const Unit w = decode_unit(unit, p);
-            // the k-block at which the unit counts as nearly loaded (lazy CLC requests wait for it)
-            const int32_t near_end = w.kb1 - w.kb0 > kLazyLeadKBlocks ? w.kb1 - kLazyLeadKBlocks : w.kb0;
-            if (load_a && w.kb1 <= w.kb0) mbar_arrive(sm.prod_began());
+            const int32_t nkb = w.kb1 - w.kb0;
+            // the load at which the unit counts as nearly loaded (lazy CLC requests wait for it)
+            const int32_t near_end = nkb > kLazyLeadKBlocks ? nkb - kLazyLeadKBlocks : 0;
+            const bool rev = p.k_alt && (fast_div(unit, p.div_wave) & 1);
+            if (load_a && nkb <= 0) mbar_arrive(sm.prod_began());
             int32_t mb, nb;
             raster(w.tile, p, mb, nb);
             const int32_t a_row = mb * C::TILE_M + static_cast<int32_t>(rank) * C::BM;
             const int32_t b_row = nb * BN + static_cast<int32_t>(rank) * C::B_ROWS;
             if (p.trace && rank == 0 && load_a) p.trace[4 * unit + 2] = static_cast<long long>(globaltimer());
-            for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
-                if (load_a && kb == near_end) mbar_arrive(sm.prod_began());
+            for (int32_t i = 0; i < nkb; ++i) {
+                const int32_t kb = rev ? w.kb1 - 1 - i : w.kb0 + i;
+                if (load_a && i == near_end) mbar_arrive(sm.prod_began());
                 if (!wait_phase(sm.empty(stage), phase ^ 1u, sm.abort_flag, p, WAIT_PRODUCER_EMPTY) ||
                     (fork && !wait_phase(sm.aux_empty(stage), phase ^ 1u, sm.abort_flag, p, WAIT_PRODUCER_EMPTY))) {
                     alive = false;
