@@ -12,7 +12,7 @@ import torch
 
 import oracle
 import synth
-from parity import assert_bit_exact, to_device_bf16, tile_layouts
+from parity import as_f64, assert_bit_exact, assert_within_bound, to_device_bf16, tile_layouts
 
 pytestmark = pytest.mark.gpu
 
@@ -128,3 +128,28 @@ def test_lazy_clc_claims_balance_few_long_units(lib, tile, ew, merge, held):
             part = u < info["split_tiles"] * info["split_parts"]
             work[w] = work.get(w, 0) + (kb // info["split_parts"] if part else kb)
         assert max(work.values()) - min(work.values()) <= kb + kb // max(info["split_parts"], 1)
+
+
+@pytest.mark.parametrize("tile,M,N", [("128x128", 2048, 2048), ("128x256", 2048, 4096), ("256x256", 4096, 2048)])
+def test_random_results_identical_across_schedulers_and_caps(lib, tile, M, N):
+    # More units than fit at once, so the second wave's units walk their K range
+    # downwards.  Which way a unit walks depends only on its index and the plan's
+    # resident worker count, so on non-integer inputs (where the summation order
+    # shows in the fp32 result) static, CLC and a capped static grid agree bit for
+    # bit, and each lies within the error bound of the oracle's product.
+    K = 512
+    A = synth.uniform_pm1_bf16(341, (M, K))
+    B = synth.uniform_pm1_bf16(342, (N, K))
+    Ad, Bd = to_device_bf16(A), to_device_bf16(B)
+    info = lib.ts_gemm_launch_info(M, N, K, lib.TS_OUT_F32, "static", tile=tile)
+    assert info["num_units"] > info["resident"] and info["split_tiles"] == 0
+    outs = []
+    for sched, cap in (("static", 0), ("clc", 0), ("static", 7)):
+        D = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+        lib.ts_gemm_bf16_ex(Ad, Bd, D, sched=sched, tile=tile, max_workers=cap)
+        lib.ts_sync_and_check()
+        outs.append(D)
+    for D, what in zip(outs[1:], ("clc", "static capped at 7 workers")):
+        assert torch.equal(outs[0], D), f"{tile}: {what} differs from static"
+    assert_within_bound(as_f64(outs[0]), oracle.gemm_f64_blas(A, B), oracle.gemm_f64_blas(A, B, absolute=True),
+                        torch.float32, f"random {tile}")
