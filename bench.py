@@ -352,6 +352,9 @@ def run_ours(args, ws, rank, local):
         dist.barrier()
     torch.cuda.synchronize()
     t0 = time.time()
+    # a GPU sleep ahead of the region keeps the device busy while the host queues the
+    # first steps, so the first GEMM's events do not count the host's submission time
+    torch.cuda._sleep(4_000_000)
     outer0.record(stream)
     for i in range(args.steps):
         step(events[i])
@@ -496,11 +499,13 @@ def measure_gemm4096(ts, sampler, reps=5, batch=20, nset=4):
     Ds = [torch.empty((w.M, w.N), dtype=torch.bfloat16, device="cuda") for _ in range(nset)]
     stream = torch.cuda.current_stream()
     runs = {}
-    for tile in ("auto", "128x256"):
-        for sched in ("static", "clc"):
-            runs[f"{tile} {sched}"] = (lambda i, tile=tile, sched=sched:
-                                       ts.ts_gemm_bf16_ex(As[i % nset], Bs[i % nset], Ds[i % nset], sched=sched,
-                                                          tile=tile))
+    for ready in (0, 1):
+        for tile in ("auto", "128x256"):
+            for sched in ("static", "clc"):
+                runs[f"{tile} {sched}" + (" inputs_ready" if ready else "")] = (
+                    lambda i, tile=tile, sched=sched, ready=ready:
+                    ts.ts_gemm_bf16_ex(As[i % nset], Bs[i % nset], Ds[i % nset], sched=sched, tile=tile,
+                                       inputs_ready=ready))
     for f in runs.values():
         for i in range(2 * nset):
             f(i)
@@ -512,20 +517,32 @@ def measure_gemm4096(ts, sampler, reps=5, batch=20, nset=4):
     flops = 2.0 * w.M * w.N * w.K
     res = {}
     for k, v in times.items():
-        tile, sched = k.split()
+        tile, sched = k.split()[:2]
+        ready = k.endswith("inputs_ready")
         med = statistics.median(v)
         info = ts.ts_gemm_launch_info(w.M, w.N, w.K, ts.TS_OUT_BF16, sched, tile=tile)
         tf = flops / (med * 1e-3) / 1e12
         res[k] = {"tile": f"{info['tile_m']}x{info['tile_n']}" + (" 2-CTA" if info["cluster"] == 2 else ""),
-                  "sched": sched, "us_median": round(med * 1e3, 2), "us_min": round(min(v) * 1e3, 2),
-                  "tflops": round(tf, 1), "frac_of_burst": round(tf / peaks["bf16_tflops"], 4),
+                  "sched": sched, "inputs_ready": int(ready), "us_median": round(med * 1e3, 2),
+                  "us_min": round(min(v) * 1e3, 2), "tflops": round(tf, 1),
+                  "frac_of_burst": round(tf / peaks["bf16_tflops"], 4),
                   "split_tail": f"{info['split_tiles']} tiles x {info['split_parts']} parts",
                   "stages": info["stages"], "epi_warps": info["epi_warps"],
+                  # DRAM bytes of one launch: the captures ran the default mode, whose work is the same
                   "traffic": load_traffic("gemm", f"{w.M}x{w.N}x{w.K} {tile} {sched}")}
-    best_auto = max(("auto static", "auto clc"), key=lambda k: res[k]["tflops"])
+    autos = [k for k in res if k.startswith("auto")]
+    best_auto = max(autos, key=lambda k: res[k]["tflops"])
+    best_default = max(("auto static", "auto clc"), key=lambda k: res[k]["tflops"])
     return {"metric": "bf16 GEMM TFLOP/s, 4096^3 bf16-out, static vs CLC, automatic tile and 128x256",
             "unit": "TFLOP/s", "value": res[best_auto]["tflops"], "frac_of_burst": res[best_auto]["frac_of_burst"],
-            "reported": best_auto, "runs": res, "peak": peaks["bf16_tflops"],
+            "reported": best_auto,
+            "value_default_mode": res[best_default]["tflops"],
+            "frac_of_burst_default_mode": res[best_default]["frac_of_burst"],
+            "reported_default_mode": best_default,
+            "inputs_ready": "runs marked inputs_ready pass that option (A and B were final before the previous "
+                            "launch began, which holds here: nothing writes them), so their loads overlap the "
+                            "previous launch's tail; the other runs wait for the previous launch first",
+            "runs": res, "peak": peaks["bf16_tflops"],
             "peak_kind": f"{peaks['source']} bf16 burst", "samples": reps, "launches_per_sample": batch,
             "gpu_launches": reps * batch * len(runs),
             "clocks": sampler.summary("gemm4096") if sampler is not None else None,
@@ -756,8 +773,10 @@ def measure_smallk(ts, sampler, samples=20, warmup=5, batch=25):
     D = torch.empty((w.M, w.N), dtype=torch.bfloat16, device="cuda")
     stream = torch.cuda.current_stream()
     nbytes = 2.0 * (w.M * w.K + w.N * w.K) + 2.0 * w.M * w.N  # A and B read once, D written once
-    runs = {f"{sched} {tile}": (lambda i, sched=sched, tile=tile: ts.ts_gemm_bf16_ex(A, B, D, sched=sched, tile=tile))
-            for tile in ("256x256", "128x256") for sched in ("clc", "static")}
+    runs = {f"{sched} {tile}" + (" inputs_ready" if ready else ""):
+            (lambda i, sched=sched, tile=tile, ready=ready:
+             ts.ts_gemm_bf16_ex(A, B, D, sched=sched, tile=tile, inputs_ready=ready))
+            for ready in (0, 1) for tile in ("256x256", "128x256") for sched in ("clc", "static")}
     for f in runs.values():
         for i in range(warmup):
             f(i)
@@ -768,15 +787,22 @@ def measure_smallk(ts, sampler, samples=20, warmup=5, batch=25):
     res = {}
     for k, v in times.items():
         med = statistics.median(v)
-        res[k] = {"us_median": round(med * 1e3, 2), "us_min": round(min(v) * 1e3, 2),
-                  "gbs": round(nbytes / (med * 1e-3) / 1e9, 1),
+        res[k] = {"inputs_ready": int(k.endswith("inputs_ready")), "us_median": round(med * 1e3, 2),
+                  "us_min": round(min(v) * 1e3, 2), "gbs": round(nbytes / (med * 1e-3) / 1e9, 1),
                   "frac_of_hbm": round(nbytes / (med * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
                   "tflops": round(2.0 * w.M * w.N * w.K / (med * 1e-3) / 1e12, 1)}
     head = max(res, key=lambda k: res[k]["gbs"])  # the fastest configuration, named in config
-    h_sched, h_tile = head.split()
+    h_sched, h_tile = head.split()[:2]
     best = res[head]["gbs"]
+    head_default = max((k for k in res if not res[k]["inputs_ready"]), key=lambda k: res[k]["gbs"])
     return {"metric": "small-K bf16 GEMM HBM GB/s (8192x8192x64, bf16 out)", "unit": "GB/s", "value": best,
-            "frac_of_hbm": round(best / peaks["hbm_gbs"], 4), "runs": res,
+            "frac_of_hbm": round(best / peaks["hbm_gbs"], 4), "reported": head,
+            "value_default_mode": res[head_default]["gbs"], "frac_of_hbm_default_mode": res[head_default]["frac_of_hbm"],
+            "reported_default_mode": head_default,
+            "inputs_ready": "runs marked inputs_ready pass that option (A and B were final before the previous "
+                            "launch began, which holds here: nothing writes them), so their loads and MMAs "
+                            "overlap the previous launch's tail; the other runs wait for the previous launch first",
+            "runs": res,
             "roofline": {"bound": "hbm", "achieved": best, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": round(best / peaks["hbm_gbs"], 4),
                          "traffic": load_traffic("gemm", f"{w.M}x{w.N}x{w.K} {h_tile} {h_sched}"),
@@ -785,6 +811,7 @@ def measure_smallk(ts, sampler, samples=20, warmup=5, batch=25):
             "samples": samples, "launches_per_sample": batch, "gpu_launches": samples * batch * len(runs),
             "clocks": sampler.summary("smallk") if sampler is not None else None,
             "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "tile": h_tile, "sched": h_sched,
+                       "inputs_ready": res[head]["inputs_ready"],
                        "epi_warps": ts.ts_gemm_launch_info(w.M, w.N, w.K, ts.TS_OUT_BF16, h_sched,
                                                            tile=h_tile)["epi_warps"],
                        "l2": "output (134 MB) larger than L2; A and B (1 MiB each) stay resident; no flush"}}

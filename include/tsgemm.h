@@ -92,6 +92,20 @@ typedef struct {
                              (3 * S).  Merge uses four epilogue warps (epi_warps = 8 or 16
                              is TS_ERR_UNSUPPORTED) and cannot run with row_sums (both need warp 3:
                              TS_ERR_UNSUPPORTED).  Results do not depend on it. */
+    int32_t inputs_ready; /* 1: the caller guarantees that A, B and skip_tiles held their final contents
+                             before the kernel preceding this call in the stream began (none of them
+                             is written by that kernel, nor by anything that kernel may run
+                             alongside).  Every GEMM launch is a programmatic dependent of the
+                             previous kernel; its dependent-launch barrier is one resource of the
+                             kernel's dependency graph (CUTLASS TS "Introduction", Core Terms: a PDL
+                             barrier).  By default (0) every task waits on it before touching global
+                             memory.  With 1 the epilogue (which writes D, the split tiles' workspace
+                             and the trace) waits on it first, and every other task runs its first
+                             work unit ahead of it and waits on it before its second (the Fork task
+                             before its first row_sums store, the producer before its first trace
+                             write), so the first tiles' loads and MMAs overlap the previous kernel's
+                             tail.  Results do not depend on it when the guarantee holds; when it
+                             does not, they are undefined.  Anything else is TS_ERR_INVALID_ARG. */
 } ts_gemm_opts;
 
 /* What ts_gemm_bf16_ex would launch for a problem (host-only query). */

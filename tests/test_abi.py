@@ -53,6 +53,8 @@ def test_argument_errors_need_no_gpu(ts):
                                      None) == ts.TS_ERR_INVALID_ARG  # NULL buffers, before any CUDA call
     assert ts.ts_gemm_bf16_ptr(0, 0, 0, 4, 4, 8, ts.TS_OUT_F32, stream=0, merge=2) == ts.TS_ERR_INVALID_ARG
     assert "merge" in ts.ts_last_error_detail()
+    assert ts.ts_gemm_bf16_ptr(0, 0, 0, 4, 4, 8, ts.TS_OUT_F32, stream=0, inputs_ready=2) == ts.TS_ERR_INVALID_ARG
+    assert "inputs_ready" in ts.ts_last_error_detail()
     # the Merge layout's B producer and the Fork row-sum task would both need warp 3
     o = ts._opts(merge=1)
     o.row_sums = 4096

@@ -348,3 +348,40 @@ def test_lazy_wait_one_unit_late_is_caught(tile, warps):
     r = pc.check_variant(tile, [2, 1, 2], "clc", stages=2, epilogue_warps=warps, lazy=True,
                          mutate="lazy_wait_one_unit_late")
     assert not r.ok and "deadlock" in r.message
+
+
+# ------------------------------------------------ the dependent-launch barrier (inputs_ready)
+# The barrier is released as late as possible in these models (once every role that waits on it
+# has reached its wait), so a role whose first unit needs the epilogue deadlocks.
+@pytest.mark.parametrize("tile,sched,kw", [
+    ("128x256", "static", {}),
+    ("128x256", "clc", {}),
+    ("128x256", "clc", {"lazy": True}),
+    ("128x128", "static", {"fork": True}),
+    ("256x256", "static", {"variant_merge": 1, "epilogue_warps": 1, "stages": 2}),
+])
+@pytest.mark.parametrize("units", [[2, 2, 2], [pc.SKIP, 0, 2, 1]])
+def test_early_loads_protocol_verified(tile, sched, kw, units):
+    r = pc.check_variant(tile, units, sched, early=True, **kw)
+    assert r.ok, r.message
+
+
+def test_early_loads_protocol_verified_cta_pair_clc():
+    r = pc.check_variant("256x256", [pc.SKIP, 0, 2, 1], "clc", early=True, stages=2, epilogue_warps=1)
+    assert r.ok, r.message
+
+
+@pytest.mark.parametrize("mutation", pc.EARLY_MUTATIONS)
+@pytest.mark.parametrize("tile,sched,kw", [("128x256", "clc", {"stages": 2}),
+                                           ("128x256", "clc", {"stages": 2, "lazy": True}),
+                                           ("256x256", "static", {"stages": 2, "epilogue_warps": 1})])
+def test_early_loads_mistakes_are_caught(mutation, tile, sched, kw):
+    if mutation == "scheduler_dep_wait_late" and sched == "static":
+        pytest.skip("the static scheduler has no scheduler role")
+    r = pc.check_variant(tile, [2, 2, 2, 2], sched, early=True, mutate=mutation, **kw)
+    assert not r.ok and "deadlock" in r.message and "dependent_launch" in r.message, r.message
+
+
+def test_early_mutations_need_early():
+    with pytest.raises(ValueError):
+        pc.check_variant("128x256", [2, 2, 2], "clc", mutate="mma_dep_wait_late")

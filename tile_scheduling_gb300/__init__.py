@@ -47,7 +47,8 @@ class GemmOpts(ctypes.Structure):
                 ("ldb", ctypes.c_int64), ("ldd", ctypes.c_int64), ("timeout_s", ctypes.c_double),
                 ("trace", ctypes.c_void_p), ("raster_group", ctypes.c_int32), ("split_tail", ctypes.c_int32),
                 ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_int64), ("skip_tiles", ctypes.c_void_p),
-                ("row_sums", ctypes.c_void_p), ("epi_warps", ctypes.c_int32), ("merge", ctypes.c_int32)]
+                ("row_sums", ctypes.c_void_p), ("epi_warps", ctypes.c_int32), ("merge", ctypes.c_int32),
+                ("inputs_ready", ctypes.c_int32)]
 
 
 class LaunchInfo(ctypes.Structure):
@@ -140,10 +141,11 @@ def _sched(s) -> int:
 
 
 def _opts(tile="auto", max_workers=0, lda=0, ldb=0, ldd=0, timeout_s=0.0, trace=None, raster_group=0,
-          split_tail=0, workspace=None, skip_tiles=None, row_sums=None, epi_warps=0, merge=0):
+          split_tail=0, workspace=None, skip_tiles=None, row_sums=None, epi_warps=0, merge=0, inputs_ready=0):
     o = GemmOpts()
     o.epi_warps = int(epi_warps)
     o.merge = int(merge)
+    o.inputs_ready = int(inputs_ready)
     if row_sums is not None:
         if row_sums.dtype != torch.float32 or not row_sums.is_cuda or not row_sums.is_contiguous():
             raise TypeError("row_sums must be a contiguous float32 CUDA tensor")
@@ -212,22 +214,23 @@ def workspace_for(nbytes: int, device=None) -> torch.Tensor:
 
 def ts_gemm_bf16_ex(A: torch.Tensor, B: torch.Tensor, D: torch.Tensor, sched="static", tile="auto",
                     max_workers=0, timeout_s=0.0, trace=None, raster_group=0, workspace="auto", split_tail=0,
-                    skip_tiles=None, row_sums=None, epi_warps=0, merge=0, stream=None) -> None:
+                    skip_tiles=None, row_sums=None, epi_warps=0, merge=0, inputs_ready=0, stream=None) -> None:
     """D = A @ B.T for bf16 A [M, K] and B [N, K]; D [M, N] is bf16 or fp32.
 
     Rows may be strided (the row stride becomes lda / ldb / ldd).  ``workspace``
     ("auto": a cached zero-filled buffer; None: no split tiles; or a CUDA tensor)
     lets the tiles that would leave the last wave partly empty be split along K.  ``epi_warps``: 4, 8,
     16 (256-column tiles) or 0 (automatic); ``merge``: 1 for the Merge barrier layout (A and B from
-    separate producer warps).  Asynchronous on ``stream`` (default: torch's
-    current stream)."""
+    separate producer warps); ``inputs_ready``: 1 when A, B and skip_tiles were final before the
+    previous kernel in the stream began (their loads then overlap that kernel's tail).  Asynchronous on
+    ``stream`` (default: torch's current stream)."""
     M, N, K, lda, ldb, ldd = _gemm_args(A, B, D)
     lda, ldb, ldd = (lda if M > 1 else 0), (ldb if N > 1 else 0), (ldd if M > 1 else 0)
     workspace = _resolve_workspace(M, N, K, _OUT[D.dtype], sched, workspace,
                                    -1 if (skip_tiles is not None or row_sums is not None) else split_tail, tile=tile,
                                    max_workers=max_workers, lda=lda, ldb=ldb, ldd=ldd)
     o = _opts(tile, max_workers, lda, ldb, ldd, timeout_s, trace, raster_group, split_tail, workspace, skip_tiles,
-              row_sums, epi_warps, merge)
+              row_sums, epi_warps, merge, inputs_ready)
     _check(_lib.ts_gemm_bf16_ex(ctypes.c_void_p(A.data_ptr()), ctypes.c_void_p(B.data_ptr()),
                                 ctypes.c_void_p(D.data_ptr()), M, N, K, _OUT[D.dtype], _sched(sched),
                                 ctypes.byref(o), _stream_handle(stream)))
@@ -356,7 +359,7 @@ def ts_gemm_grouped_launch_info(M: int, N: int, k_offsets, out=TS_OUT_BF16, sche
 
 def ts_gemm_bf16_grouped(A: torch.Tensor, B: torch.Tensor, D: torch.Tensor, k_offsets, sched="static", tile="auto",
                          max_workers=0, timeout_s=0.0, trace=None, raster_group=0, skip_tiles=None,
-                         row_sums=None, epi_warps=0, merge=0, stream=None) -> None:
+                         row_sums=None, epi_warps=0, merge=0, inputs_ready=0, stream=None) -> None:
     """D[g] = A[:, k_g:k_g+1] @ B[:, k_g:k_g+1].T for every group g (k_offsets: groups + 1 multiples of 64).
 
     A [M, >=K] and B [N, >=K] bf16 with unit column stride; D [groups, M, N]
@@ -373,7 +376,8 @@ def ts_gemm_bf16_grouped(A: torch.Tensor, B: torch.Tensor, D: torch.Tensor, k_of
     if int(off[-1]) > min(A.shape[1], B.shape[1]):
         raise ValueError("k_offsets reach past the columns of A or B")
     o = _opts(tile, max_workers, lda if M > 1 else 0, ldb if N > 1 else 0, D.stride(1) if M > 1 else 0, timeout_s,
-              trace, raster_group, skip_tiles=skip_tiles, row_sums=row_sums, epi_warps=epi_warps, merge=merge)
+              trace, raster_group, skip_tiles=skip_tiles, row_sums=row_sums, epi_warps=epi_warps, merge=merge,
+              inputs_ready=inputs_ready)
     _check(_lib.ts_gemm_bf16_grouped(ctypes.c_void_p(A.data_ptr()), ctypes.c_void_p(B.data_ptr()),
                                      ctypes.c_void_p(D.data_ptr()), M, N, G, off.ctypes.data, _OUT[D.dtype],
                                      _sched(sched), ctypes.byref(o), _stream_handle(stream)))

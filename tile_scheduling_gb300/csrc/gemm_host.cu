@@ -191,6 +191,8 @@ ts_status plan_gemm(const void *D, int64_t M, int64_t N, int64_t K, int32_t out,
     if (o->epi_warps != 0 && o->epi_warps != 4 && o->epi_warps != 8 && o->epi_warps != 16)
         return fail(TS_ERR_INVALID_ARG, "epi_warps = %d (0, 4, 8 or 16)", o->epi_warps);
     if (o->merge != 0 && o->merge != 1) return fail(TS_ERR_INVALID_ARG, "merge = %d (0 or 1)", o->merge);
+    if (o->inputs_ready != 0 && o->inputs_ready != 1)
+        return fail(TS_ERR_INVALID_ARG, "inputs_ready = %d (0 or 1)", o->inputs_ready);
     if (o->merge && o->row_sums)
         return fail(TS_ERR_UNSUPPORTED, "the Merge layout's B producer and the Fork consumer both need warp 3");
     if (o->merge && o->epi_warps > 4)
@@ -505,6 +507,7 @@ ts_status gemm_launch(const void *A, const void *B, void *D, int64_t M, int64_t 
     // or the static cap, so a unit's summation order is a function of the plan alone.
     p.k_alt = 1;
     p.div_wave = fast_div_for(pl.resident);
+    p.inputs_ready = o->inputs_ready;
     p.D = D;
     p.ldd = pl.ldd;
     const double tmo = o->timeout_s > 0 ? o->timeout_s : kDefaultTimeoutS;

@@ -396,13 +396,34 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(sm.tmem_slot);
     // Launched as a programmatic dependent of the previous kernel in the
     // stream: everything above touches only this CTA's shared memory, TMEM and
-    // the kernel parameters, so it overlaps that kernel's tail; no global
-    // memory is read or written before its writes are visible.  The next
-    // kernel may then be scheduled right away: it cannot occupy an SM before
-    // this grid's CTA there has exited (a CTA takes all of an SM's shared
-    // memory), and it waits here in turn.
-    grid_dep_wait();
-    grid_dep_launch();
+    // the kernel parameters, so it overlaps that kernel's tail.  The
+    // dependent-launch barrier (the previous kernel's completion, its writes
+    // visible) is a resource of its own (CUTLASS TS "Introduction", Core Terms:
+    // a PDL barrier).  By default every role waits on it here, before any global
+    // memory access.  With inputs_ready the caller states that A, B and the skip
+    // mask were final before the previous kernel began: the epilogue, which
+    // writes D (and the split partials, counters and trace), waits on it first;
+    // every other role runs its first work unit ahead of it and waits on it
+    // before its second (the producer before its first trace write, the Fork
+    // task before its first row-sum store).  No wait of a role's first unit
+    // depends on the epilogue (the ring drains into the first accumulator, the
+    // first CLC response slots are free), so every bounded wait that could last
+    // as long as the previous kernel starts after the barrier.  The first
+    // units' loads and MMAs then overlap the previous kernel's tail.  The next
+    // kernel is allowed to launch only after this barrier: it cannot occupy an
+    // SM before this grid's CTA there has exited (a CTA takes all of an SM's
+    // shared memory), and it waits on its own barrier in turn.
+    if (!p.inputs_ready) {
+        grid_dep_wait();
+        grid_dep_launch();
+    }
+    // A role's wait on the barrier after its first unit (inputs_ready only).
+    auto dep_wait_once = [&](bool &waited) {
+        if (p.inputs_ready && !waited) {
+            grid_dep_wait();
+            waited = true;
+        }
+    };
 
     const int32_t first_unit = worker < p.num_units ? worker : -1;
 
@@ -416,7 +437,8 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
         auto full_bar = [&](uint32_t st) { return b_bar ? sm.full_b(st) : sm.full(st); };
         int32_t unit = first_unit;
         uint32_t clc_idx = 0, stage = 0, phase = 0, issued = 0;
-        bool alive = true;
+        bool alive = true, waited = false;
+        if (p.trace) dep_wait_once(waited);  // the trace is written below
         while (unit >= 0 && alive) {
             const Unit w = decode_unit(unit, p);
             const int32_t nkb = w.kb1 - w.kb0;
@@ -456,8 +478,10 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
                 }
             }
             if (!alive) break;
+            dep_wait_once(waited);
             unit = next_unit(sm, p, unit, clc_idx);
         }
+        dep_wait_once(waited);
         // Drain: every issued load has landed (even CTA's full barriers) and
         // the MMA has released every stage.
         if (rank == 0) {
@@ -491,10 +515,11 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
         if (lane == 0 && rank == 0) {
             int32_t unit = first_unit;
             uint32_t clc_idx = 0, stage = 0, phase = 0, acc = 0, acc_phase = 0;
-            bool alive = true;
+            bool alive = true, waited = false;
             while (unit >= 0 && alive) {
                 const Unit w = decode_unit(unit, p);
                 if (w.skip) {  // no accumulator is used for a skipped tile
+                    dep_wait_once(waited);
                     unit = next_unit(sm, p, unit, clc_idx);
                     continue;
                 }
@@ -534,8 +559,10 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
                     acc = 0;
                     acc_phase ^= 1u;
                 }
+                dep_wait_once(waited);
                 unit = next_unit(sm, p, unit, clc_idx);
             }
+            dep_wait_once(waited);
             // Every MMA issued by this thread has completed before TMEM is freed.
             if constexpr (CG == 1)
                 mma_commit(sm.mma_done());
@@ -548,7 +575,7 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
         // ------------------------------------------------- CLC scheduler
         if (lane == 0 && p.sched == SCHED_CLC && first_unit >= 0) {
             uint32_t idx = 0;
-            bool outstanding = false;
+            bool outstanding = false, waited = false;
             uint32_t out_r = 0, out_ph = 0;
             const uint32_t depth = static_cast<uint32_t>(p.clc_depth);
             for (;;) {
@@ -583,7 +610,9 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
                     if (*sm.abort_flag && rank == 0) outstanding = true;
                     break;
                 }
+                dep_wait_once(waited);
             }
+            dep_wait_once(waited);
             if (outstanding) wait_drain(sm.clc_full(out_r), out_ph, sm.abort_flag, p);
         }
         __syncwarp();
@@ -600,7 +629,7 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
         if (fork) {
             int32_t unit = first_unit;
             uint32_t clc_idx = 0, stage = 0, phase = 0;
-            bool alive = true;
+            bool alive = true, waited = false;
             while (unit >= 0 && alive) {
                 const Unit w = decode_unit(unit, p);
                 int32_t mb, nb;
@@ -652,6 +681,7 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
                     }
                 }
                 if (!alive) break;
+                dep_wait_once(waited);  // before the first row-sum store
                 if (active) {
 #pragma unroll
                     for (int r = 0; r < 4; ++r) {
@@ -666,6 +696,7 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
                 if (lane == 0) nu = next_unit(sm, p, unit, clc_idx);
                 unit = __shfl_sync(0xffffffffu, nu, 0);
             }
+            dep_wait_once(waited);
         }
         __syncwarp();
     } else if (warp >= 4) {
@@ -673,6 +704,10 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
         // Warps 4 .. 4 + EW - 1.  A warp may access TMEM lanes 32 * (warp % 4) onwards:
         // warp 4 + j takes lane quarter q = j % 4 and, with 8 or 16 warps, the
         // subtiles s = h, h + EW / 4, ... (h = j / 4) of that quarter's rows.
+        if (p.inputs_ready) {  // D and this task's other outputs wait for the previous kernel
+            grid_dep_wait();
+            grid_dep_launch();
+        }
         constexpr int HALVES = C::EPI_WARPS / 4;
         const int q = (warp - kRoleWarps) & 3;
         const int h = (warp - kRoleWarps) >> 2;

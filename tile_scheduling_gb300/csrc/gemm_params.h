@@ -81,6 +81,8 @@ struct GemmParams {
     int32_t tma_store;     // 1: TMA-store epilogue, 0: st.global epilogue
     int32_t clc_depth;     // response slots in flight (1 or 2)
     int32_t clc_lazy;      // 1: the request for the unit after unit j waits until the producer began unit j
+    int32_t inputs_ready;  // 1: A, B and skip were final before the previous kernel began (loads skip its barrier)
+    int32_t pad2;
     void *D;               // used by the st.global epilogue
     int64_t ldd;           // elements
     uint64_t timeout_ns;   // per-wait limit

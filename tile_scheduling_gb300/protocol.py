@@ -56,6 +56,9 @@ MUTATIONS = ("tmem_empty_count_low", "tmem_empty_count_high", "clc_empty_count_l
              "fork_producer_ignores_second_consumer", "merge_mma_skips_b_wait") + ZERO_K_MUTATIONS
 SPLIT_MUTATIONS = ("split_no_fence", "split_no_rearm", "split_last_early")
 LAZY_MUTATIONS = ("lazy_wait_one_unit_late",)
+# mistakes in where a role waits on the dependent-launch barrier (inputs_ready): after its third
+# unit instead of its first
+EARLY_MUTATIONS = ("mma_dep_wait_late", "producer_dep_wait_late", "scheduler_dep_wait_late")
 
 
 def _tag(unit: int, kb: int) -> int:
@@ -86,7 +89,7 @@ class Program:
 
 def build_program(proto: dict, units: list, sched: str = "static", epilogue_warps: int | None = None,
                   stages: int | None = None, mutate: str | None = None, fork: bool = False,
-                  lazy: bool = False, lazy_lead: int = 1) -> Program:
+                  lazy: bool = False, lazy_lead: int = 1, early: bool = False) -> Program:
     """The kernel's role loops for one worker.
 
     proto           ts_gemm_protocol_info() of the variant.
@@ -107,6 +110,15 @@ def build_program(proto: dict, units: list, sched: str = "static", epilogue_warp
                     lead is 16; at once for a shorter or empty unit), and the
                     scheduler's request k waits for that point of unit k
                     (completion k + 1) before it is issued.
+    early           inputs_ready: the dependent-launch barrier (the previous
+                    kernel's completion; TS "Introduction", Core Terms: a PDL
+                    barrier) gates the epilogue from its start, and every other
+                    role waits on it after its first unit.  The model releases
+                    the barrier as late as it can: a "previous kernel" role
+                    arrives on it only once every other role has reached its
+                    wait, so a role whose first unit needs the epilogue (a wait
+                    that would last as long as the previous kernel, and could
+                    run into its time limit) shows as a deadlock.
 
     A variant with proto["merge"] = 1 has the Merge layout of the "Pipeline
     Groups" page: two producers per CTA, one loading A onto full[s] and one
@@ -120,10 +132,12 @@ def build_program(proto: dict, units: list, sched: str = "static", epilogue_warp
         raise ValueError("the Merge layout has no Fork consumer")
     if mutate == "merge_mma_skips_b_wait" and not merge:
         raise ValueError("merge_mma_skips_b_wait needs a Merge variant")
-    if mutate is not None and mutate not in MUTATIONS + LAZY_MUTATIONS:
+    if mutate is not None and mutate not in MUTATIONS + LAZY_MUTATIONS + EARLY_MUTATIONS:
         raise ValueError(f"unknown mutation {mutate}")
     if mutate in LAZY_MUTATIONS and not lazy:
         raise ValueError(f"{mutate} needs lazy requests")
+    if mutate in EARLY_MUTATIONS and not early:
+        raise ValueError(f"{mutate} needs early (inputs_ready)")
     if any(nk != SKIP and nk < 0 for nk in units):
         raise ValueError("a unit has n >= 0 k-blocks or is SKIP")
     cg = proto["cluster"]
@@ -146,6 +160,16 @@ def build_program(proto: dict, units: list, sched: str = "static", epilogue_warp
     aux_empty = [P.bar(f"aux_empty[{s}]", proto["aux_empty_arrivals"]) for s in range(S)] if fork else []
     clc = sched == "clc"
     began = P.bar("prod_began", 1) if (lazy and clc) else -1
+    if early:
+        n_prod = (2 if merge else 1) * cg
+        gate = P.bar("roles_at_dependency_wait", n_prod + 1 + (1 if fork else 0) + (cg if clc else 0))
+        pdl = P.bar("dependent_launch", 1)
+
+    def dep_wait(ops, u, late):
+        # a role's wait on the dependent-launch barrier after unit u (its first; the third under
+        # the role's mutation)
+        if early and u == (2 if late else 0):
+            ops += [rec(OP_ARRIVE, gate, 0), rec(OP_WAIT, pdl, 0)]
     stage = [[P.buf(f"stage[{c}][{s}]") for s in range(S)] for c in range(cg)]  # A (and B unless Merge)
     stage_b = [[P.buf(f"stage_b[{c}][{s}]") for s in range(S)] for c in range(cg)] if merge else []
     accb = [P.buf(f"tmem[{a}]") for a in range(A)]
@@ -189,8 +213,11 @@ def build_program(proto: dict, units: list, sched: str = "static", epilogue_warp
                     ops.append(rec(OP_TMA, sbuf[c][s], _tag(u, kb), fbar[0][s], nbytes))
                     issued += 1
                     s, ph = adv(s, ph, S)
+                dep_wait(ops, u, mutate == "producer_dep_wait_late")
                 if clc:
                     consume(ops, c, u)
+            if early and len(units) <= (2 if mutate == "producer_dep_wait_late" else 0):
+                ops += [rec(OP_ARRIVE, gate, 0), rec(OP_WAIT, pdl, 0)]
             if c == 0:  # drain: the last issued loads landed
                 for i in range(1, min(issued, S) + 1):
                     b = issued - i
@@ -203,8 +230,10 @@ def build_program(proto: dict, units: list, sched: str = "static", epilogue_warp
             P.roles.append((f"{name}[{c}]", None, ops))
 
     ops, s, ph, a, aph = [], 0, 0, 0, 0  # MMA issuer of the even CTA
+    mma_late = mutate == "mma_dep_wait_late"
     for u, nk in enumerate(units):
         if nk == SKIP and mutate != "mma_takes_skipped_accumulator":
+            dep_wait(ops, u, mma_late)
             if clc:  # a skipped tile takes no accumulator; the queue still advances
                 consume(ops, 0, u)
             continue
@@ -222,13 +251,18 @@ def build_program(proto: dict, units: list, sched: str = "static", epilogue_warp
             # with no k-block the commit completes at once: the epilogue finds an empty sum
             ops.append(rec(OP_COMMIT, tfull[0][a], tfull[1][a] if cg == 2 else -1))
         a, aph = adv(a, aph, A)
+        dep_wait(ops, u, mma_late)
         if clc:
             consume(ops, 0, u)
+    if early and len(units) <= (2 if mma_late else 0):
+        ops += [rec(OP_ARRIVE, gate, 0), rec(OP_WAIT, pdl, 0)]
     P.roles.append(("mma", None, ops))
 
     for c in range(cg):  # epilogue warps of each CTA: one symmetry group per CTA
         for w in range(E):
             ops, a, aph = [], 0, 0
+            if early:  # D is written only after the previous kernel completed
+                ops.append(rec(OP_WAIT, pdl, 0))
             for u, nk in enumerate(units):
                 if nk == SKIP and mutate != "epilogue_waits_skipped_tile":
                     if clc:  # a skipped tile stores nothing and takes no accumulator
@@ -259,6 +293,7 @@ def build_program(proto: dict, units: list, sched: str = "static", epilogue_warp
                 ops += [rec(OP_WAIT, full[0][s], ph), rec(OP_TREAD, stage[0][s], _tag(u, kb)),
                         rec(OP_ARRIVE, aux_empty[s], 0)]
                 s, ph = adv(s, ph, S)
+            dep_wait(ops, u, False)  # before the unit's row-sum store
             if clc:
                 consume(ops, 0, u)
         P.roles.append(("rowsum", None, ops))
@@ -278,7 +313,12 @@ def build_program(proto: dict, units: list, sched: str = "static", epilogue_warp
                 else:
                     ops.append(rec(OP_ARRIVE, clc_full[c][r], proto["clc_response_bytes"]))
                 consume(ops, c, k)
+                dep_wait(ops, k, mutate == "scheduler_dep_wait_late")
+            if early and len(units) <= (2 if mutate == "scheduler_dep_wait_late" else 0):
+                ops += [rec(OP_ARRIVE, gate, 0), rec(OP_WAIT, pdl, 0)]
             P.roles.append((f"scheduler[{c}]", None, ops))
+    if early:  # the previous kernel completes once every role that may has run ahead of it
+        P.roles.append(("previous_kernel", None, [rec(OP_WAIT, gate, 0), rec(OP_ARRIVE, pdl, 0)]))
     return P
 
 
