@@ -111,3 +111,22 @@ def test_grouped_workload_sampled(lib):
             got = as_f64(D[int(g)][torch.as_tensor(rows, device="cuda")])
             assert_within_bound(got, oracle.gemm_f64_blas(a, b), oracle.gemm_f64_blas(a, b, absolute=True),
                                 torch.bfloat16, f"grouped workload g{g}")
+
+
+@pytest.mark.parametrize("tile,sched", [("128x256", "clc"), ("256x256", "static")])
+def test_grouped_inputs_ready_back_to_back(lib, tile, sched):
+    # grouped launches back to back into one D with inputs_ready (A and B never written): the
+    # groups' first units run ahead of the previous launch, every D write waits for it
+    M, N = 300, 520
+    A = synth.int_uniform_bf16(603, (M, 1024))
+    B = synth.int_uniform_bf16(604, (N, 1024))
+    Ad, Bd = to_device_bf16(A), to_device_bf16(B)
+    G = len(OFFSETS) - 1
+    D = torch.full((G, M, N), float("nan"), dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    for _ in range(4):
+        lib.ts_gemm_bf16_grouped(Ad, Bd, D, OFFSETS, sched=sched, tile=tile, inputs_ready=1)
+    lib.ts_sync_and_check()
+    ref = oracle.grouped_gemm_f64(A, B, OFFSETS, blas=True)
+    for g in range(G):
+        assert_bit_exact(D[g], ref[g], f"group {g} {tile} {sched} inputs_ready")
