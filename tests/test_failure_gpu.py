@@ -20,13 +20,18 @@ pytestmark = pytest.mark.gpu
 
 @pytest.mark.parametrize("tile,sched", [("128x256", "static"), ("128x128", "clc"), ("256x256", "clc"),
                                         ("256x256", "static")])
-def test_wait_timeout_reported_then_context_still_works(lib, tile, sched):
+@pytest.mark.parametrize("ready", [0, 1])
+def test_wait_timeout_reported_then_context_still_works(lib, tile, sched, ready):
+    # ready = 1: the timed-out launch follows a normal one with inputs_ready, so its roles time
+    # out in their first unit, ahead of the dependent-launch barrier, and still leave cleanly
     M, N, K = 2048, 2048, 4096
     A_bits = synth.int_uniform_bf16(701, (M, K))
     B_bits = synth.int_uniform_bf16(702, (N, K))
     A, B = to_device_bf16(A_bits), to_device_bf16(B_bits)
     D = torch.zeros((M, N), dtype=torch.float32, device="cuda")
-    lib.ts_gemm_bf16_ex(A, B, D, sched=sched, tile=tile, timeout_s=1e-6)
+    if ready:
+        lib.ts_gemm_bf16_ex(A, B, D, sched=sched, tile=tile)
+    lib.ts_gemm_bf16_ex(A, B, D, sched=sched, tile=tile, timeout_s=1e-6, inputs_ready=ready)
     with pytest.raises(lib.TsError) as e:
         lib.ts_sync_and_check()
     assert e.value.status == lib.TS_ERR_TIMEOUT
