@@ -62,11 +62,37 @@ KERNEL_SOURCES = {"gemm": ["gemm_kernel.cuh", "ptx.cuh", "gemm_params.h", "gemm_
 
 
 # ------------------------------------------------------------------ helpers
+def _code_only(src: str) -> str:
+    """C/C++ source without its comments and with whitespace runs collapsed (string and character
+    literals kept as they are), so that a comment edit does not change a kernel's hash."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            i = src.find("\n", i)
+            i = n if i < 0 else i
+        elif src.startswith("/*", i):
+            i = src.find("*/", i + 2)
+            i = n if i < 0 else i + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_hash(kernel: str) -> str:
+    """Hash of a kernel's sources, code only: the key of the DRAM-traffic captures in profiles/."""
     h = hashlib.sha256()
     for f in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(ROOT, "tile_scheduling_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "tile_scheduling_gb300", "csrc", f), encoding="utf-8") as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

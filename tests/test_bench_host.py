@@ -146,3 +146,13 @@ def test_nvml_sampler_without_nvml_reports_the_error():
     smp.stop()
     assert smp.nvml is None and "no device" in smp.error
     assert smp.summary()["samples"] == 0
+
+
+def test_kernel_source_hash_ignores_comments_but_not_code():
+    import bench
+
+    src = 'int a = 1; // note\n/* block\n comment */ const char *s = "// kept"; char c = \'/\';\n'
+    code = bench._code_only(src)
+    assert code == 'int a = 1; const char *s = "// kept"; char c = \'/\';'
+    assert bench._code_only(src.replace("note", "another note")) == code
+    assert bench._code_only(src.replace("a = 1", "a = 2")) != code

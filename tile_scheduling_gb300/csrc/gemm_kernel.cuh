@@ -37,6 +37,13 @@
 // scheduler).  CLC mode: the grid covers all tiles, block (cluster) i starts
 // on tile i and then takes the coordinates of launches it cancels.
 //
+// A work unit's k-blocks are loaded upwards, or downwards in the units of odd
+// waves (GemmParams::k_alt), so each wave starts on operand panels the wave
+// before it left in L2.  The previous kernel in the stream is waited for
+// before any global memory access, or, with inputs_ready, by the epilogue
+// first and by every other role after its first unit (the dependent-launch
+// barrier as a resource of its own: see the comment at the wait).
+//
 // Two accumulators of BN fp32 columns live in TMEM, so the epilogue of one
 // tile overlaps the mainloop of the next.  With CG = 2 a CTA pair computes a
 // 256 x BN tile with cta_group::2 MMAs issued by the even CTA: each CTA loads
