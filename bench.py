@@ -843,6 +843,62 @@ def measure_smallk(ts, sampler, samples=20, warmup=5, batch=25):
                        "l2": "output (134 MB) larger than L2; A and B (1 MiB each) stay resident; no flush"}}
 
 
+def run_ingress(args, ws, rank, local):
+    """How fast one SM takes in operands: the 8192^3 GEMM under the static scheduler with a cap on the
+    persistent workers, 1-CTA 128x256 and 2-CTA 256x256 tiles, no split tiles.  From the kernel's
+    per-unit trace, each worker's tile period (the median gap between the ends of its consecutive
+    tiles) gives the tensor rate per SM; the clock samples of each run are reported beside it.  If
+    the rate of the 1-CTA tile were bound by something the SMs share (L2, the crossbar), it would
+    rise as fewer SMs run; if it is bound per SM, it rises only as much as the clock does."""
+    import torch
+
+    import tile_scheduling_gb300 as ts
+
+    torch.cuda.set_device(local)
+    sampler = NvmlClockSampler(local)
+    sampler.start()
+    w = synth.GEMM_8192
+    A_bits, B_bits = w.inputs()
+    A, B = _dev_bf16(A_bits), _dev_bf16(B_bits)
+    D = torch.empty((w.M, w.N), dtype=torch.bfloat16, device="cuda")
+    sms = ts.ts_num_sms()
+    runs = {}
+    for tile, cg, counts in (("128x256", 1, (sms, 3 * sms // 4, sms // 2, sms // 4, sms // 8)),
+                             ("256x256", 2, (sms // 2, 3 * sms // 8, sms // 4, sms // 8))):
+        for workers in counts:
+            kw = dict(sched="static", tile=tile, max_workers=workers, workspace=None)
+            info = ts.ts_gemm_launch_info(w.M, w.N, w.K, ts.TS_OUT_BF16, **kw)
+            trace = torch.zeros(4 * info["num_units"], dtype=torch.int64, device="cuda")
+            for _ in range(max(1, args.warmup // 3)):
+                ts.ts_gemm_bf16_ex(A, B, D, **kw)
+            torch.cuda.synchronize()
+            t0 = time.time()
+            ts.ts_gemm_bf16_ex(A, B, D, trace=trace, **kw)
+            torch.cuda.synchronize()
+            sampler.region(f"{tile} {workers}", t0, time.time())
+            ts.ts_sync_and_check()
+            tr = trace.view(-1, 4).cpu().numpy()
+            ends = {}
+            for u in range(info["num_units"]):
+                ends.setdefault(int(tr[u, 1]), []).append(int(tr[u, 3]))
+            gaps = [g for e in ends.values() for g in np.diff(np.sort(np.array(e))).tolist()]
+            period_us = statistics.median(gaps) / 1e3
+            tile_flops = 2.0 * info["tile_m"] * info["tile_n"] * w.K
+            clk = sampler.summary(f"{tile} {workers}")
+            runs[f"{tile} x{workers}"] = {
+                "tile": tile, "workers": workers, "sms": workers * cg, "tile_period_us": round(period_us, 2),
+                "tflops_per_sm": round(tile_flops / cg / (period_us * 1e-6) / 1e12, 2),
+                "sm_mhz": clk.get("sm_mhz"), "reasons": clk.get("reasons")}
+    sampler.stop()
+    if rank != 0:
+        return None
+    return {"metric": "operand ingress per SM: tensor TFLOP/s per SM of the 8192^3 GEMM vs the SMs in use",
+            "unit": "TFLOP/s per SM", "value": runs[f"128x256 x{sms}"]["tflops_per_sm"], "runs": runs,
+            "n_gpus": ws, "steps": 1, "warmup": args.warmup, "higher_is_better": True, "dtype": "bf16",
+            "data": "synthetic", "config": {"workload": w.name + " static, capped workers, no split tiles",
+                                            "flop_per_sm_cycle": 8192}}
+
+
 def run_smallk(args, ws, rank, local):
     """8192x8192x64 bf16-out GEMM in HBM GB/s."""
     import torch
@@ -1090,7 +1146,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--workload", default="headline", choices=["headline", "gemm4096", "contended", "grouped", "causal", "fork",
-                                                                   "rows", "smallk"])
+                                                                   "rows", "smallk", "ingress"])
     ap.add_argument("--reps", type=int, default=10, help="static/CLC pairs of the contended workload (>= 10)")
     ap.add_argument("--spin-ctas", type=int, default=32)
     ap.add_argument("--no-configs", action="store_true",
@@ -1130,6 +1186,8 @@ def main(argv=None):
             line = run_fork(args, ws, rank, local)
         elif args.workload == "smallk":
             line = run_smallk(args, ws, rank, local)
+        elif args.workload == "ingress":
+            line = run_ingress(args, ws, rank, local)
         else:
             line = run_ours(args, ws, rank, local)
     finally:
