@@ -33,7 +33,11 @@ typedef enum {
     TS_ERR_TIMEOUT = 4      /* a kernel gave up on a barrier wait (reported by ts_sync_and_check) */
 } ts_status;
 
-typedef enum { TS_SCHED_STATIC = 0, TS_SCHED_CLC = 1 } ts_sched;
+/* Scheduling shapes (CUTLASS TS "Schedules", Scheduling Shapes): static persistent (a grid of
+ * resident workers, tile i of worker w = w + i * workers), dynamic persistent (Cluster Launch
+ * Control: one CTA or cluster per tile, running workers take over pending ones), and -- GEMM only --
+ * non-persistent (one CTA or cluster per tile, each computing its own tile and exiting). */
+typedef enum { TS_SCHED_STATIC = 0, TS_SCHED_CLC = 1, TS_SCHED_NONPERSISTENT = 2 } ts_sched;
 typedef enum { TS_OUT_BF16 = 0, TS_OUT_F32 = 1 } ts_out_dtype;
 
 typedef enum {
@@ -206,9 +210,11 @@ int32_t ts_protocol_check_ex(int32_t nbars, const int32_t *bar_expected, int32_t
  * Groups", Overview: the GEMM mainloop resource graph gmem_ab -> smem_a,
  * smem_b -> tmem_c -> gmem_d; TS "Resources", per-work-tile scale_d reset).
  * Tiles are assigned by the static grid-stride rule (TS "Schedules",
- * Scheduling Shapes; "Cluster Launch Control", static persistent scheduler)
- * or by Cluster Launch Control work stealing ("Cluster Launch Control", one
- * CLC request and the overlap loop).  Under CLC each worker keeps up to two
+ * Scheduling Shapes; "Cluster Launch Control", static persistent scheduler),
+ * by Cluster Launch Control work stealing ("Cluster Launch Control", one
+ * CLC request and the overlap loop), or not at all (TS_SCHED_NONPERSISTENT:
+ * the launch grid maps one CTA or cluster to each work unit, which computes
+ * that unit and exits; the pages' non-persistent shape).  Under CLC each worker keeps up to two
  * requests in flight; with K loops of at least 32 k-blocks a request waits
  * until the worker's current unit is nearly loaded (16 k-blocks left), so the
  * last units go to the workers that finish first.  The scheduler changes which

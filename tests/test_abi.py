@@ -45,6 +45,7 @@ def test_argument_errors_need_no_gpu(ts):
     assert ts.ts_gemm_bf16_ptr(0, 0, 0, 4, 4, 1 << 31, ts.TS_OUT_F32, stream=0) == ts.TS_ERR_INVALID_ARG
     assert ts.ts_gemm_bf16_ptr(0, 0, 0, 4, 4, 4, 7, stream=0) == ts.TS_ERR_INVALID_ARG
     assert ts.ts_gemm_bf16_ptr(0, 0, 0, 4, 4, 4, ts.TS_OUT_F32, sched=5, stream=0) == ts.TS_ERR_INVALID_ARG
+    assert ts.ts_gemm_bf16_ptr(0, 0, 0, 4, 4, 4, ts.TS_OUT_F32, sched=3, stream=0) == ts.TS_ERR_INVALID_ARG
     assert ts.ts_gemm_bf16_ptr(0, 0, 0, 4, 4, 4, ts.TS_OUT_F32, stream=0, tile=9) == ts.TS_ERR_INVALID_ARG
     assert ts.ts_gemm_bf16_ptr(0, 0, 0, 4, 4, 8, ts.TS_OUT_F32, stream=0, lda=4) == ts.TS_ERR_INVALID_ARG
     assert ts.ts_gemm_bf16_ptr(0, 0, 0, 4, 4, 8, ts.TS_OUT_F32, stream=0, epi_warps=6) == ts.TS_ERR_INVALID_ARG

@@ -7,7 +7,8 @@ dependency mode, and multiplies integer-valued matrices in [-4, 4], whose
 products are exact in fp32 and in the oracle's float64.  Every element of D
 is compared, and nothing outside D (a sentinel band of the buffer) may change.
 A few cases have K >= 4096 and more tiles than fit at once, so that the plan
-splits tiles along K.
+splits tiles along K.  The scheduler is static persistent, CLC or
+non-persistent.
 """
 import numpy as np
 import pytest
@@ -42,7 +43,7 @@ def _cases():
             ew = int(rng.choice([0, 4, 8])) if big else int(rng.choice([0, 4, 8, 16]))
             if ew == 16 and tile not in ("128x256", "256x256"):
                 tile = str(rng.choice(["128x256", "256x256"]))
-        sched = str(rng.choice(["static", "clc"]))
+        sched = str(rng.choice(["static", "clc", "nonpersistent"]))
         cap = int(rng.choice([0, 0, 1, 7, 100])) if sched == "static" and not big else 0
         raster = int(rng.choice([0, 1, 3, 16]))
         ready = int(rng.random() < 0.5)
@@ -83,4 +84,4 @@ def test_sweep_covers_split_tiles_and_both_modes(lib):
                                        tile=tile, epi_warps=ew, merge=merge, max_workers=cap)
         split += info["split_tiles"] > 0
     assert split >= 1
-    assert {c[11] for c in cases} == {0, 1} and {c[6] for c in cases} == {"static", "clc"}
+    assert {c[11] for c in cases} == {0, 1} and {c[6] for c in cases} == {"static", "clc", "nonpersistent"}

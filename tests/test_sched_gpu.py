@@ -153,3 +153,29 @@ def test_random_results_identical_across_schedulers_and_caps(lib, tile, M, N):
         assert torch.equal(outs[0], D), f"{tile}: {what} differs from static"
     assert_within_bound(as_f64(outs[0]), oracle.gemm_f64_blas(A, B), oracle.gemm_f64_blas(A, B, absolute=True),
                         torch.float32, f"random {tile}")
+
+
+@pytest.mark.parametrize("tile,ew,merge", tile_layouts(["128x128", "128x256", "256x256"]))
+@pytest.mark.parametrize("ready", [0, 1])
+def test_nonpersistent_each_block_computes_its_own_unit(lib, tile, ew, merge, ready):
+    # the pages' non-persistent scheduling shape: one CTA (cluster) per unit, no queue
+    M, N, K = 1500, 1300, 192
+    A = synth.int_uniform_bf16(351, (M, K))
+    B = synth.int_uniform_bf16(352, (N, K))
+    info, tr, D = _traced(lib, A, B, torch.float32, tile, "nonpersistent", epi_warps=ew, merge=merge,
+                          inputs_ready=ready)
+    assert info["workers"] == info["num_units"] and info["grid_ctas"] == info["num_units"] * info["cluster"]
+    assert np.all(tr[:, 0] == 1), "a work unit was not visited exactly once"
+    assert np.array_equal(tr[:, 1], np.arange(info["num_units"])), "a block computed another block's unit"
+    assert_bit_exact(D, oracle.gemm_f64(A, B), f"non-persistent {tile}")
+
+
+@pytest.mark.parametrize("tile", ["128x256", "256x256"])
+def test_nonpersistent_with_split_tiles(lib, tile):
+    M, N, K = 2560, 2560, 4096
+    A = synth.int_uniform_bf16(361, (M, K))
+    B = synth.int_uniform_bf16(362, (N, K))
+    info, tr, D = _traced(lib, A, B, torch.float32, tile, "nonpersistent")
+    assert info["split_tiles"] > 0
+    assert np.all(tr[:, 0] == 1) and np.array_equal(tr[:, 1], np.arange(info["num_units"]))
+    assert_bit_exact(D, oracle.gemm_f64_blas(A, B), f"non-persistent split {tile}")

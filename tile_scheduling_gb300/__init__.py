@@ -20,11 +20,11 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_lib", "libtsgemm.so")
 
 TS_OK, TS_ERR_INVALID_ARG, TS_ERR_UNSUPPORTED, TS_ERR_CUDA, TS_ERR_TIMEOUT = range(5)
-TS_SCHED_STATIC, TS_SCHED_CLC = 0, 1
+TS_SCHED_STATIC, TS_SCHED_CLC, TS_SCHED_NONPERSISTENT = 0, 1, 2
 TS_OUT_BF16, TS_OUT_F32 = 0, 1
 TS_TILE_AUTO, TS_TILE_128x128, TS_TILE_128x256, TS_TILE_256x256_2CTA = range(4)
 
-_SCHED = {"static": TS_SCHED_STATIC, "clc": TS_SCHED_CLC}
+_SCHED = {"static": TS_SCHED_STATIC, "clc": TS_SCHED_CLC, "nonpersistent": TS_SCHED_NONPERSISTENT}
 _TILE = {"auto": TS_TILE_AUTO, "128x128": TS_TILE_128x128, "128x256": TS_TILE_128x256,
          "256x256": TS_TILE_256x256_2CTA}
 _OUT = {torch.bfloat16: TS_OUT_BF16, torch.float32: TS_OUT_F32}

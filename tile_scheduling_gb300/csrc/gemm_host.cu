@@ -181,7 +181,8 @@ ts_status plan_gemm(const void *D, int64_t M, int64_t N, int64_t K, int32_t out,
         return fail(TS_ERR_INVALID_ARG, "sizes must be in [0, 2^31-1] (M=%lld N=%lld K=%lld)",
                     static_cast<long long>(M), static_cast<long long>(N), static_cast<long long>(K));
     if (out != TS_OUT_BF16 && out != TS_OUT_F32) return fail(TS_ERR_INVALID_ARG, "out_dtype %d", out);
-    if (sched != TS_SCHED_STATIC && sched != TS_SCHED_CLC) return fail(TS_ERR_INVALID_ARG, "sched %d", sched);
+    if (sched != TS_SCHED_STATIC && sched != TS_SCHED_CLC && sched != TS_SCHED_NONPERSISTENT)
+        return fail(TS_ERR_INVALID_ARG, "sched %d", sched);
     ts_gemm_opts z;
     std::memset(&z, 0, sizeof z);
     if (!o) o = &z;
@@ -284,7 +285,7 @@ ts_status plan_gemm(const void *D, int64_t M, int64_t N, int64_t K, int32_t out,
     }
     pl->num_units = pl->num_tiles - pl->split_tiles + pl->split_tiles * pl->parts;
     if (pl->num_units * cg > kMaxDim) return fail(TS_ERR_UNSUPPORTED, "too many work units");
-    if (sched == TS_SCHED_CLC) {
+    if (sched != TS_SCHED_STATIC) {  // CLC and non-persistent: one CTA (cluster) per unit
         pl->workers = pl->num_units;
     } else {
         int64_t w = std::min<int64_t>(pl->num_units, W);
@@ -354,7 +355,8 @@ ts_status ts_gemm_tile_coords(int64_t M, int64_t N, int64_t K, int32_t out_dtype
             return ts::fail(TS_ERR_INVALID_ARG, "sizes must be in [0, 2^31-1]");
         if (out_dtype != TS_OUT_BF16 && out_dtype != TS_OUT_F32)
             return ts::fail(TS_ERR_INVALID_ARG, "out_dtype %d", out_dtype);
-        if (sched != TS_SCHED_STATIC && sched != TS_SCHED_CLC) return ts::fail(TS_ERR_INVALID_ARG, "sched %d", sched);
+        if (sched != TS_SCHED_STATIC && sched != TS_SCHED_CLC && sched != TS_SCHED_NONPERSISTENT)
+            return ts::fail(TS_ERR_INVALID_ARG, "sched %d", sched);
         if (tile < TS_TILE_AUTO || tile > TS_TILE_256x256_2CTA) return ts::fail(TS_ERR_INVALID_ARG, "tile %d", tile);
         if (opts->raster_group < 0) return ts::fail(TS_ERR_INVALID_ARG, "negative option");
         const int64_t tile_m = tile == TS_TILE_256x256_2CTA ? 256 : 128;

@@ -36,6 +36,8 @@
 // W takes tiles w, w + W, ... ("Cluster Launch Control", static persistent
 // scheduler).  CLC mode: the grid covers all tiles, block (cluster) i starts
 // on tile i and then takes the coordinates of launches it cancels.
+// Non-persistent mode: the grid covers all tiles and block (cluster) i
+// computes tile i alone (TS "Schedules", Scheduling Shapes).
 //
 // A work unit's k-blocks are loaded upwards, or downwards in the units of odd
 // waves (GemmParams::k_alt), so each wave starts on operand panels the wave
@@ -327,6 +329,7 @@ __device__ __forceinline__ int32_t next_unit(const Smem<C> &sm, const GemmParams
         const int32_t u = unit + static_cast<int32_t>(gridDim.x / C::CG);
         return u < p.num_units ? u : -1;
     }
+    if (p.sched == SCHED_NONPERSISTENT) return -1;  // one unit per CTA (cluster)
     return clc_consume(sm, p, clc_idx);
 }
 

@@ -4,7 +4,7 @@
 
 namespace ts {
 
-enum : int32_t { SCHED_STATIC = 0, SCHED_CLC = 1 };
+enum : int32_t { SCHED_STATIC = 0, SCHED_CLC = 1, SCHED_NONPERSISTENT = 2 };
 enum : int32_t { OUT_BF16 = 0, OUT_F32 = 1 };
 
 // Where a bounded wait gave up (reported in the status word).
@@ -77,7 +77,7 @@ struct GemmParams {
     // raster_group, and the height of the last (possibly shorter) group
     FastDiv div_group_tiles, div_group_rows, div_last_rows;
     FastDiv div_wave;      // the workers that fit on the GPU at once (a wave of units)
-    int32_t sched;         // SCHED_STATIC / SCHED_CLC
+    int32_t sched;         // SCHED_STATIC / SCHED_CLC / SCHED_NONPERSISTENT
     int32_t tma_store;     // 1: TMA-store epilogue, 0: st.global epilogue
     int32_t clc_depth;     // response slots in flight (1 or 2)
     int32_t clc_lazy;      // 1: the request for the unit after unit j waits until the producer began unit j
