@@ -85,3 +85,41 @@ def test_sweep_covers_split_tiles_and_both_modes(lib):
         split += info["split_tiles"] > 0
     assert split >= 1
     assert {c[11] for c in cases} == {0, 1} and {c[6] for c in cases} == {"static", "clc", "nonpersistent"}
+
+
+def _grouped_cases():
+    rng = np.random.default_rng(SEED + 1)
+    out = []
+    for i in range(24):
+        G = int(rng.integers(1, 17))
+        widths = [int(64 * rng.choice([0, 1, 2, 5, 16, 40])) for _ in range(G)]
+        base = int(64 * rng.integers(0, 3))
+        off = [base + int(x) for x in np.concatenate([[0], np.cumsum(widths)])]
+        M, N = (int(x) for x in rng.integers(1, 1200, 2))
+        out_t = str(rng.choice(["f32", "bf16"]))
+        tile = str(rng.choice(["auto", "128x128", "128x256", "256x256"]))
+        merge = int(rng.random() < 0.2)
+        ew = 0 if merge else int(rng.choice([0, 4, 8]))
+        sched = str(rng.choice(["static", "clc", "nonpersistent"]))
+        ready = int(rng.random() < 0.5)
+        out.append((i, tuple(off), M, N, out_t, tile, sched, ew, merge, ready))
+    return out
+
+
+@pytest.mark.parametrize("case", _grouped_cases(), ids=lambda c: "grouped%02d_g%d_%dx%d_%s_%s_%s_ew%d_mg%d_ready%d" % (
+    c[0], len(c[1]) - 1, c[2], c[3], c[4], c[5], c[6], c[7], c[8], c[9]))
+def test_random_grouped_bit_exact(lib, case):
+    # groups of 0 to 2560 columns (empty groups included), offsets not starting at 0
+    i, off, M, N, out_t, tile, sched, ew, merge, ready = case
+    Kt = max(off[-1], 8)
+    A = synth.int_uniform_bf16(SEED + 100 + 2 * i, (M, Kt))
+    B = synth.int_uniform_bf16(SEED + 101 + 2 * i, (N, Kt))
+    dt = torch.float32 if out_t == "f32" else torch.bfloat16
+    G = len(off) - 1
+    D = torch.full((G, M, N), float("nan"), dtype=dt, device="cuda")
+    lib.ts_gemm_bf16_grouped(to_device_bf16(A), to_device_bf16(B), D, list(off), sched=sched, tile=tile, epi_warps=ew,
+                             merge=merge, inputs_ready=ready)
+    lib.ts_sync_and_check()
+    ref = oracle.grouped_gemm_f64(A, B, list(off), blas=True)
+    for g in range(G):
+        assert_bit_exact(D[g], ref[g], f"case {case} group {g}")
