@@ -742,7 +742,7 @@ def run_rows(args, ws, rank, local):
     off = torch.from_numpy(off_h).cuda()
     stream = torch.cuda.current_stream()
     nbytes = 4.0 * src.numel()  # 2 bytes read + 2 written per element
-    runs = {"static": dict(sched="static"), "clc": dict(sched="clc"),
+    runs = {"static": dict(sched="static"), "clc": dict(sched="clc"), "nonpersistent": dict(sched="nonpersistent"),
             "clc_oversubscribed_2x": dict(sched="clc", tiles=2 * w.rows)}
     # chunked mode: rows cut into work tiles of at most `chunk` elements (a planning kernel maps tiles to
     # rows); packed mode: the rows laid end to end, every tile `chunk` of their elements
@@ -753,6 +753,9 @@ def run_rows(args, ws, rank, local):
                                                    pack=pack)["workspace_bytes"]
                 runs[f"{sched}_{'packed' if pack else 'chunk'}_{chunk // 1024}k"] = dict(
                     sched=sched, chunk=chunk, pack=pack, workspace=torch.empty(need, dtype=torch.uint8, device="cuda"))
+    need = ts.ts_copy_rows_launch_info(src.numel(), w.rows, "nonpersistent", chunk=32768)["workspace_bytes"]
+    runs["nonpersistent_chunk_32k"] = dict(sched="nonpersistent", chunk=32768,
+                                           workspace=torch.empty(need, dtype=torch.uint8, device="cuda"))
     times = {k: [] for k in runs}
     for k, kw in runs.items():
         for _ in range(args.warmup):
@@ -775,7 +778,8 @@ def run_rows(args, ws, rank, local):
     best = res[head]["gbs"]
     chunk = runs[head].get("chunk", 0)
     pack = runs[head].get("pack", 0)
-    return {"metric": "jagged int16 row copy HBM GB/s (8192 rows, log-uniform lengths), static vs CLC work queue",
+    return {"metric": "jagged int16 row copy HBM GB/s (8192 rows, log-uniform lengths), static vs CLC work queue "
+                      "(and non-persistent)",
             "unit": "GB/s", "value": best, **res,
             "clc_speedup_over_static": round(res["static"]["ms_median"] / res["clc"]["ms_median"], 3),
             "roofline": {"bound": "hbm", "achieved": best, "peak": peaks["hbm_gbs"], "unit": "GB/s",

@@ -409,10 +409,11 @@ typedef struct {
  * every tile still waits on, advances and releases the queue (TS "Schedules",
  * Skippable Tiles, whose example is this oversubscribed copy).  sched picks
  * the queue: TS_SCHED_STATIC, a grid-stride persistent loop over the resident
- * CTAs, or TS_SCHED_CLC, one CTA per tile with Cluster Launch Control work
+ * CTAs, TS_SCHED_CLC, one CTA per tile with Cluster Launch Control work
  * stealing ("Cluster Launch Control": the request for the next tile is issued
- * before the current row is copied).  Elements of dst outside the copied rows
- * are never written.
+ * before the current row is copied), or TS_SCHED_NONPERSISTENT, one CTA per
+ * tile and no queue.  Elements of dst outside the copied rows are never
+ * written.
  *
  *   src, dst  device int16 arrays of n elements, 2-byte aligned; src == dst is
  *             allowed (each element is rewritten with itself); any other

@@ -39,7 +39,7 @@ def _run(lib, src_h, dst0_h, offsets_h, sched, rows=None, src_off=0, dst_off=0, 
     return d[dst_off:dst_off + n]
 
 
-@pytest.mark.parametrize("sched", ["static", "clc"])
+@pytest.mark.parametrize("sched", ["static", "clc", "nonpersistent"])
 @pytest.mark.parametrize("threads", [128, 512, 1024])
 def test_rows_random_jagged(lib, sched, threads):
     offsets, n = _jagged(11 + threads, 300, 5000)
@@ -50,7 +50,7 @@ def test_rows_random_jagged(lib, sched, threads):
     assert bad == -1 and np.array_equal(got, want)
 
 
-@pytest.mark.parametrize("sched", ["static", "clc"])
+@pytest.mark.parametrize("sched", ["static", "clc", "nonpersistent"])
 @pytest.mark.parametrize("src_off,dst_off", [(0, 0), (16, 0), (8, 0), (3, 3), (1, 6), (0, 1)])
 def test_rows_vector_paths(lib, sched, src_off, dst_off):
     # shared offset mod 32 bytes (16 elements): 32-byte vectors; mod 16: 16-byte; otherwise element-wise
@@ -62,7 +62,7 @@ def test_rows_vector_paths(lib, sched, src_off, dst_off):
     assert np.array_equal(got, want)
 
 
-@pytest.mark.parametrize("sched", ["static", "clc"])
+@pytest.mark.parametrize("sched", ["static", "clc", "nonpersistent"])
 def test_rows_oversubscribed_tiles_are_skipped_and_counted(lib, sched):
     offsets, n = _jagged(31, 200, 2000)
     rows = offsets.size - 1
@@ -78,12 +78,14 @@ def test_rows_oversubscribed_tiles_are_skipped_and_counted(lib, sched):
     if sched == "static":
         assert np.array_equal(tr[:, 0], np.ones(tiles))
         assert np.array_equal(tr[:, 1], oracle.static_owner(tiles, info["grid_ctas"]))
+    elif sched == "nonpersistent":  # one CTA per tile, each on its own tile
+        assert np.array_equal(tr[:, 0], np.ones(tiles)) and np.array_equal(tr[:, 1], np.arange(tiles))
     else:
         ok, why = oracle.clc_coverage_ok(tr[:, 0], tr[:, 1])
         assert ok, why
 
 
-@pytest.mark.parametrize("sched", ["static", "clc"])
+@pytest.mark.parametrize("sched", ["static", "clc", "nonpersistent"])
 @pytest.mark.parametrize("count", [0, 1, 57, 200, 10_000])
 def test_rows_count_read_on_the_device(lib, sched, count):
     offsets, n = _jagged(41, 200, 1500)
@@ -95,7 +97,7 @@ def test_rows_count_read_on_the_device(lib, sched, count):
     assert np.array_equal(got, want)
 
 
-@pytest.mark.parametrize("sched", ["static", "clc"])
+@pytest.mark.parametrize("sched", ["static", "clc", "nonpersistent"])
 def test_rows_skip_mask(lib, sched):
     offsets, n = _jagged(51, 250, 1200)
     src = synth.int16_uniform(52, n)
@@ -106,7 +108,7 @@ def test_rows_skip_mask(lib, sched):
     assert np.array_equal(got, want)
 
 
-@pytest.mark.parametrize("sched", ["static", "clc"])
+@pytest.mark.parametrize("sched", ["static", "clc", "nonpersistent"])
 def test_rows_empty_queue_and_all_skipped(lib, sched):
     src = synth.int16_uniform(61, 100)
     dst0 = synth.int16_uniform(62, 100)
@@ -118,7 +120,7 @@ def test_rows_empty_queue_and_all_skipped(lib, sched):
     assert torch.equal(trace.view(50, 2)[:, 0].cpu(), torch.ones(50, dtype=torch.int64))
 
 
-@pytest.mark.parametrize("sched", ["static", "clc"])
+@pytest.mark.parametrize("sched", ["static", "clc", "nonpersistent"])
 @pytest.mark.parametrize("bad", ["decreasing", "past_n", "negative"])
 def test_rows_bad_bounds_are_reported_not_copied(lib, sched, bad):
     n = 1000
@@ -158,7 +160,7 @@ def test_rows_same_buffer_rewrites_itself(lib):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("sched", ["static", "clc"])
+@pytest.mark.parametrize("sched", ["static", "clc", "nonpersistent"])
 def test_rows_full_workload_bit_exact(lib, sched):
     src_h, offsets = synth.ROWS.inputs()
     n = src_h.size
@@ -179,7 +181,7 @@ def test_rows_full_workload_bit_exact(lib, sched):
 # tiles to rows); the result is the same row copy.
 
 
-@pytest.mark.parametrize("sched", ["static", "clc"])
+@pytest.mark.parametrize("sched", ["static", "clc", "nonpersistent"])
 @pytest.mark.parametrize("chunk", [1, 7, 16, 100, 4096, 1 << 20])
 def test_rows_chunked_random_jagged(lib, sched, chunk):
     offsets, n = _jagged(91 + chunk, 200 if chunk > 1 else 40, 3000 if chunk > 1 else 300)
@@ -190,7 +192,7 @@ def test_rows_chunked_random_jagged(lib, sched, chunk):
     assert bad == -1 and np.array_equal(got, want)
 
 
-@pytest.mark.parametrize("sched", ["static", "clc"])
+@pytest.mark.parametrize("sched", ["static", "clc", "nonpersistent"])
 @pytest.mark.parametrize("src_off,dst_off", [(0, 0), (8, 0), (3, 3), (1, 6)])
 def test_rows_chunked_vector_paths(lib, sched, src_off, dst_off):
     offsets, n = _jagged(95, 120, 5000, lead=3, trail=9)
@@ -201,7 +203,7 @@ def test_rows_chunked_vector_paths(lib, sched, src_off, dst_off):
     assert np.array_equal(got, want)
 
 
-@pytest.mark.parametrize("sched", ["static", "clc"])
+@pytest.mark.parametrize("sched", ["static", "clc", "nonpersistent"])
 def test_rows_chunked_tiles_visited_once_and_extra_tiles_skipped(lib, sched):
     offsets, n = _jagged(101, 150, 2000)
     rows = offsets.size - 1
@@ -221,12 +223,14 @@ def test_rows_chunked_tiles_visited_once_and_extra_tiles_skipped(lib, sched):
     if sched == "static":
         assert np.array_equal(tr[:, 0], np.ones(tiles))
         assert np.array_equal(tr[:, 1], oracle.static_owner(tiles, info["grid_ctas"]))
+    elif sched == "nonpersistent":  # one CTA per tile, each on its own tile
+        assert np.array_equal(tr[:, 0], np.ones(tiles)) and np.array_equal(tr[:, 1], np.arange(tiles))
     else:
         ok, why = oracle.clc_coverage_ok(tr[:, 0], tr[:, 1])
         assert ok, why
 
 
-@pytest.mark.parametrize("sched", ["static", "clc"])
+@pytest.mark.parametrize("sched", ["static", "clc", "nonpersistent"])
 @pytest.mark.parametrize("count", [0, 1, 77, 200])
 def test_rows_chunked_skip_mask_and_device_count(lib, sched, count):
     offsets, n = _jagged(111, 200, 1500)
@@ -239,7 +243,7 @@ def test_rows_chunked_skip_mask_and_device_count(lib, sched, count):
     assert np.array_equal(got, want)
 
 
-@pytest.mark.parametrize("sched", ["static", "clc"])
+@pytest.mark.parametrize("sched", ["static", "clc", "nonpersistent"])
 def test_rows_chunked_bad_bounds_reported(lib, sched):
     n = 1000
     offsets = np.array([0, 100, 300, 600, 1200], dtype=np.int64)  # row 3 runs past n
@@ -284,7 +288,7 @@ def test_rows_chunked_needs_a_workspace(lib):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("sched", ["static", "clc"])
+@pytest.mark.parametrize("sched", ["static", "clc", "nonpersistent"])
 def test_rows_full_workload_chunked_bit_exact(lib, sched):
     src_h, offsets = synth.ROWS.inputs()
     src = torch.from_numpy(src_h).cuda()
@@ -300,7 +304,7 @@ def test_rows_full_workload_chunked_bit_exact(lib, sched):
 # several; the result is the same row copy.
 
 
-@pytest.mark.parametrize("sched", ["static", "clc"])
+@pytest.mark.parametrize("sched", ["static", "clc", "nonpersistent"])
 @pytest.mark.parametrize("chunk", [1, 7, 16, 100, 4096, 1 << 20])
 @pytest.mark.parametrize("threads", [128, 512])
 def test_rows_packed_random_jagged(lib, sched, chunk, threads):
@@ -312,7 +316,7 @@ def test_rows_packed_random_jagged(lib, sched, chunk, threads):
     assert bad == -1 and np.array_equal(got, want)
 
 
-@pytest.mark.parametrize("sched", ["static", "clc"])
+@pytest.mark.parametrize("sched", ["static", "clc", "nonpersistent"])
 @pytest.mark.parametrize("threads", [128, 1024])
 def test_rows_packed_many_tiny_rows_per_tile(lib, sched, threads):
     # 6000 rows of 0-5 elements: a 4096-element tile holds well over a batch of rows
@@ -324,7 +328,7 @@ def test_rows_packed_many_tiny_rows_per_tile(lib, sched, threads):
     assert np.array_equal(got, want)
 
 
-@pytest.mark.parametrize("sched", ["static", "clc"])
+@pytest.mark.parametrize("sched", ["static", "clc", "nonpersistent"])
 @pytest.mark.parametrize("src_off,dst_off", [(0, 0), (8, 0), (3, 3), (1, 6)])
 def test_rows_packed_vector_paths(lib, sched, src_off, dst_off):
     offsets, n = _jagged(155, 300, 700, lead=3, trail=9)
@@ -335,7 +339,7 @@ def test_rows_packed_vector_paths(lib, sched, src_off, dst_off):
     assert np.array_equal(got, want)
 
 
-@pytest.mark.parametrize("sched", ["static", "clc"])
+@pytest.mark.parametrize("sched", ["static", "clc", "nonpersistent"])
 def test_rows_packed_tiles_visited_once_and_extra_tiles_skipped(lib, sched):
     offsets, n = _jagged(161, 150, 2000, lead=700, trail=900)
     rows = offsets.size - 1
@@ -355,12 +359,14 @@ def test_rows_packed_tiles_visited_once_and_extra_tiles_skipped(lib, sched):
     if sched == "static":
         assert np.array_equal(tr[:, 0], np.ones(tiles))
         assert np.array_equal(tr[:, 1], oracle.static_owner(tiles, info["grid_ctas"]))
+    elif sched == "nonpersistent":  # one CTA per tile, each on its own tile
+        assert np.array_equal(tr[:, 0], np.ones(tiles)) and np.array_equal(tr[:, 1], np.arange(tiles))
     else:
         ok, why = oracle.clc_coverage_ok(tr[:, 0], tr[:, 1])
         assert ok, why
 
 
-@pytest.mark.parametrize("sched", ["static", "clc"])
+@pytest.mark.parametrize("sched", ["static", "clc", "nonpersistent"])
 @pytest.mark.parametrize("count", [0, 1, 77, 200])
 def test_rows_packed_skip_mask_and_device_count(lib, sched, count):
     offsets, n = _jagged(171, 200, 1500)
@@ -374,7 +380,7 @@ def test_rows_packed_skip_mask_and_device_count(lib, sched, count):
     assert np.array_equal(got, want)
 
 
-@pytest.mark.parametrize("sched", ["static", "clc"])
+@pytest.mark.parametrize("sched", ["static", "clc", "nonpersistent"])
 def test_rows_packed_bad_bounds_reported(lib, sched):
     n = 1000
     offsets = np.array([0, 100, 300, 600, 1200], dtype=np.int64)  # row 3 runs past n
@@ -409,7 +415,7 @@ def test_rows_packed_overlapping_rows_need_more_tiles(lib):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("sched", ["static", "clc"])
+@pytest.mark.parametrize("sched", ["static", "clc", "nonpersistent"])
 def test_rows_full_workload_packed_bit_exact(lib, sched):
     src_h, offsets = synth.ROWS.inputs()
     src = torch.from_numpy(src_h).cuda()
@@ -423,7 +429,7 @@ def test_rows_full_workload_packed_bit_exact(lib, sched):
 # chunked pieces: rows whose src and dst differ modulo 16 bytes join each dst
 # vector from two source vectors (which may lie outside the row, never outside
 # src).
-@pytest.mark.parametrize("sched", ["static", "clc"])
+@pytest.mark.parametrize("sched", ["static", "clc", "nonpersistent"])
 @pytest.mark.parametrize("chunk", [0, 333])
 @pytest.mark.parametrize("dst_off", range(8))
 def test_rows_every_relative_alignment(lib, sched, chunk, dst_off):

@@ -7,7 +7,8 @@
 // part in the queue's wait / advance / release).  The work-tile loop runs on
 // either scheduler of "Cluster Launch Control": a static grid-stride
 // persistent loop (tile = blockIdx.x + i * gridDim.x), or one CTA per tile
-// whose running CTAs cancel pending ones.  The CLC request for the next tile
+// whose running CTAs cancel pending ones; or, non-persistent, one CTA per
+// tile that copies its own tile and exits.  The CLC request for the next tile
 // is issued before the current row is copied, so its latency hides under the
 // copy (the overlap loop of that page).
 //
@@ -493,6 +494,7 @@ __global__ void __launch_bounds__(kRowsMaxThreads, 2) rows_copy_kernel(const __g
             atomicAdd(reinterpret_cast<unsigned long long *>(&p.trace[2 * tile]), 1ull);
             p.trace[2 * tile + 1] = blockIdx.x;
         }
+        if (p.sched == SCHED_NONPERSISTENT) break;  // one tile per CTA, no queue
         if (!clc) {
             tile += gridDim.x;
             continue;
@@ -534,7 +536,8 @@ ts_status plan_rows(const int16_t *src, const int16_t *dst, int64_t n, const int
     if (!o) o = &z;
     if (n < 0 || rows < 0) return fail(TS_ERR_INVALID_ARG, "negative size (n=%lld rows=%lld)",
                                        static_cast<long long>(n), static_cast<long long>(rows));
-    if (sched != TS_SCHED_STATIC && sched != TS_SCHED_CLC) return fail(TS_ERR_INVALID_ARG, "sched %d", sched);
+    if (sched != TS_SCHED_STATIC && sched != TS_SCHED_CLC && sched != TS_SCHED_NONPERSISTENT)
+        return fail(TS_ERR_INVALID_ARG, "sched %d", sched);
     if (o->tiles < 0 || o->max_workers < 0 || o->timeout_s < 0 || o->chunk < 0 || o->workspace_bytes < 0)
         return fail(TS_ERR_INVALID_ARG, "negative option");
     if (o->pack != 0 && o->pack != 1) return fail(TS_ERR_INVALID_ARG, "pack = %d (0 or 1)", o->pack);
@@ -586,7 +589,7 @@ ts_status plan_rows(const int16_t *src, const int16_t *dst, int64_t n, const int
     if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
     if (per_sm <= 0) return fail(TS_ERR_UNSUPPORTED, "row copy kernel cannot be resident");
     pl->resident = static_cast<int64_t>(per_sm) * sms;
-    if (sched == TS_SCHED_CLC) {
+    if (sched != TS_SCHED_STATIC) {  // CLC and non-persistent: one CTA per tile
         pl->grid = pl->tiles;
     } else {
         int64_t w = pl->resident;
