@@ -18,7 +18,7 @@ from parity import as_f64, assert_bit_exact, assert_within_bound, to_device_bf16
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("sched", ["static", "clc"])
+@pytest.mark.parametrize("sched", ["static", "clc", "nonpersistent"])
 def test_no_alloc_entry_point_matches_existing_entry_point(lib, sched):
     M, N, K = 1000, 1200, 320
     A_bits = synth.uniform_pm1_bf16(901, (M, K))
