@@ -385,3 +385,12 @@ def test_early_loads_mistakes_are_caught(mutation, tile, sched, kw):
 def test_early_mutations_need_early():
     with pytest.raises(ValueError):
         pc.check_variant("128x256", [2, 2, 2], "clc", mutate="mma_dep_wait_late")
+
+
+@pytest.mark.parametrize("tile", ["128x128", "128x256", "256x256"])
+@pytest.mark.parametrize("early", [False, True])
+def test_nonpersistent_shape_protocol_verified(tile, early):
+    # the non-persistent shape: one unit per CTA (pair), no queue -- the static model on one unit,
+    # with and without inputs_ready
+    r = pc.check_variant(tile, [3], "static", stages=2, early=early)
+    assert r.ok, r.message
