@@ -1,7 +1,7 @@
 """Run one named workload a few times (for profilers such as ncu); prints nothing but a summary line.
 
 Usage: python -m tile_scheduling_gb300.run_workload {gemm256,gemm4096,gemm8192,ragged,smallk,copy,rows}
-           [--launches N] [--sched static|clc] [--tile auto|128x128|128x256|256x256]
+           [--launches N] [--sched static|clc|nonpersistent] [--tile auto|128x128|128x256|256x256]
 """
 from __future__ import annotations
 
@@ -28,7 +28,7 @@ def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("workload", choices=sorted(GEMMS) + ["copy", "rows"])
     ap.add_argument("--launches", type=int, default=3)
-    ap.add_argument("--sched", default=None, choices=["static", "clc"])
+    ap.add_argument("--sched", default=None, choices=["static", "clc", "nonpersistent"])
     ap.add_argument("--tile", default=None)
     ap.add_argument("--chunk", type=int, default=0, help="rows: elements per work tile (0: one tile per row)")
     ap.add_argument("--pack", type=int, default=0, choices=[0, 1], help="rows: lay the rows end to end (with --chunk)")
