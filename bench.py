@@ -423,11 +423,20 @@ def run_ours(args, ws, rank, local):
     per_launch_s = gemm_sum * 1e-3 / args.steps
     achieved = flops / per_launch_s / 1e12
     workload = f"gemm_bf16 {M}x{N}x{K} bf16-out {args.tile} {args.sched} + copy_i16 n=2^28"
-    roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
-            "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
+    # The burst figure is the peak for a GEMM timed in a short region; a region long enough to reach the
+    # power cap (half a second or more, or the cap seen in the clock samples) takes the sustained one.
+    capped = "sw_power_cap" in (clocks or {}).get("reasons", [])
+    sustained = total / 1e3 >= 0.5 or capped
+    peak = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
+    kind = (f"{peaks['source']} bf16 sustained: the GEMM is timed in a region of {total / 1e3:.3f} s"
+            + (" under the power cap" if capped else "") if sustained else
+            f"{peaks['source']} bf16 burst: the GEMM is timed in a region of {total / 1e3:.3f} s, far shorter "
+            "than the seconds-long loop of the sustained figure")
+    roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
+            "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
             "traffic": load_traffic("gemm", f"{M}x{N}x{K} {args.tile} {args.sched}"),
-            "peak_kind": f"{peaks['source']} bf16 burst: the GEMM is timed in a region of "
-                         f"{total / 1e3:.3f} s, far shorter than the seconds-long loop of the sustained figure",
+            "peak_kind": kind,
+            "frac_of_burst": round(achieved / peaks["bf16_tflops"], 4), "peak_burst": peaks["bf16_tflops"],
             "frac_of_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4),
             "peak_sustained": peaks["bf16_tflops_sustained"], "kernel": "gemm_ws_kernel",
             "algorithmic_flops_per_launch": flops}
