@@ -11,7 +11,8 @@ traffic), so no L2 flush is inserted between steps.
 launches, summed over ranks).  The copy's HBM GB/s is reported beside it.
 ``e2e`` times the same GEMM through the public call with host buffers: the
 host->device copy of A and B from pinned memory, the GEMM, and the
-device->host read of D are all inside the timed region.
+device->host read of D are all inside the timed region; its ``roofline`` sets
+the host traffic of a step against the same copies timed alone, with no GEMM.
 
 After the headline, the same line reports the other workloads, each timed in a
 region of its own: ``gemm4096`` (4096^3 bf16-out, the automatic tile and the
@@ -1069,11 +1070,57 @@ def run_e2e(args, ts, A_bits, B_bits, M, N, K, ws):
     ms = reduce_times([e0.elapsed_time(e1)], "max")[0]
     ts.ts_sync_and_check()
     flops = 2.0 * M * N * K
+    h2d = int(A_h.numel() * 2 + B_h.numel() * 2)
+    d2h = int(D_h[0].numel() * 2)
+    link = measure_host_link(A_h, B_h, D_h[0], A[0], B[0], D[0], streams[0], streams[1])
+    host_gbs = (h2d + d2h) * steps / (ms * 1e-3) / 1e9
     return {"value": round(ws * flops * steps / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
-            "h2d_bytes_per_step": int(A_h.numel() * 2 + B_h.numel() * 2), "d2h_bytes_per_step": int(D_h[0].numel() * 2),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": steps, "ms_per_step": round(ms / steps, 4), "call": "ts_gemm_bf16_host",
             "pipelining": f"one call per step (copy in, GEMM, copy out on one stream); steps round-robin over "
-                          f"{nbuf} streams and buffer sets"}
+                          f"{nbuf} streams and buffer sets",
+            "roofline": {"bound": "host link", "achieved": round(host_gbs, 1), "peak": link["both_gbs"],
+                         "unit": "GB/s", "frac": round(host_gbs / link["both_gbs"], 4),
+                         "peak_kind": "measured here: the step's copies alone (A and B in on one stream, D out on "
+                                      "another, at once), no GEMM",
+                         "link": link}}
+
+
+def measure_host_link(A_h, B_h, D_h, A, B, D, s_in, s_out, reps=5):
+    """Host link rates on this machine for the end-to-end step's own copies, with no GEMM running:
+    A and B in, D out, and both directions at once on two streams (median of `reps`)."""
+    import torch
+
+    h2d = (A_h.numel() + B_h.numel()) * A_h.element_size()
+    d2h = D_h.numel() * D_h.element_size()
+
+    def copy_in():
+        with torch.cuda.stream(s_in):
+            A.copy_(A_h, non_blocking=True)
+            B.copy_(B_h, non_blocking=True)
+
+    def copy_out():
+        with torch.cuda.stream(s_out):
+            D_h.copy_(D, non_blocking=True)
+
+    def timed(*fns):
+        out = []
+        for _ in range(reps + 1):
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s_in)
+            s_out.wait_event(e0)
+            for fn in fns:
+                fn()
+            s_in.wait_stream(s_out)
+            e1.record(s_in)
+            torch.cuda.synchronize()
+            out.append(e0.elapsed_time(e1))
+        return statistics.median(out[1:])
+
+    t_in, t_out, t_both = timed(copy_in), timed(copy_out), timed(copy_in, copy_out)
+    return {"h2d_gbs": round(h2d / t_in / 1e6, 1), "d2h_gbs": round(d2h / t_out / 1e6, 1),
+            "both_gbs": round((h2d + d2h) / t_both / 1e6, 1), "ms_step_copies_alone": round(t_both, 4)}
 
 
 # -------------------------------------------------------- CPU oracle arm
