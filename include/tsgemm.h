@@ -284,12 +284,33 @@ ts_status ts_gemm_bf16_host(const void *A_host, const void *B_host, void *D_host
  *              may be empty: its D is zero)
  *   groups     1 .. 256
  * opts as for ts_gemm_bf16_ex (tile, max_workers, lda/ldb/ldd, timeout_s, trace
- * with 4 * num_units entries); no tiles are split.  Work units are the
- * tiles of group 0, then of group 1, ...
+ * with 4 * num_units entries); no tiles are split.  Work units are the tiles
+ * of one group after another, the groups in the order ts_gemm_grouped_order
+ * gives: longest K range first, so that the short units are the ones left for
+ * the end of the launch (the LPT rule; results do not depend on the order).
  */
 ts_status ts_gemm_bf16_grouped(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t groups,
                                const int64_t *k_offsets, int32_t out_dtype, int32_t sched, const ts_gemm_opts *opts,
                                void *stream);
+
+/*
+ * ts_gemm_grouped_order -- the order in which ts_gemm_bf16_grouped schedules the
+ * groups (host only, no launch): work unit u of the launch is tile
+ * u % (tiles_m * tiles_n) of group order[u / (tiles_m * tiles_n)].  Groups are
+ * taken by K range (k_offsets[g + 1] - k_offsets[g]), longest first; equal
+ * ranges keep their index order.  Handing out the longest units first is
+ * Graham's LPT rule for list scheduling, which bounds how far apart the workers
+ * finish by the length of the shortest units rather than the longest; it helps
+ * the static round-robin deal and CLC work stealing alike (CUTLASS TS
+ * "Schedules", Dynamic Domain leaves the order of the units open).
+ *
+ *   groups, k_offsets   as for ts_gemm_bf16_grouped
+ *   order               HOST int32 array of `groups` entries, written with a
+ *                       permutation of 0 .. groups - 1
+ * Errors: those of ts_gemm_bf16_grouped's offset checks; TS_ERR_INVALID_ARG for
+ * a NULL order.
+ */
+ts_status ts_gemm_grouped_order(int64_t groups, const int64_t *k_offsets, int32_t *order);
 
 /* The launch ts_gemm_bf16_grouped would make (host only). */
 ts_status ts_gemm_grouped_launch_info(int64_t M, int64_t N, int64_t groups, const int64_t *k_offsets,

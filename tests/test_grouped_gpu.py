@@ -130,3 +130,26 @@ def test_grouped_inputs_ready_back_to_back(lib, tile, sched):
     ref = oracle.grouped_gemm_f64(A, B, OFFSETS, blas=True)
     for g in range(G):
         assert_bit_exact(D[g], ref[g], f"group {g} {tile} {sched} inputs_ready")
+
+
+def test_grouped_units_follow_the_longest_first_order(lib):
+    # One static worker runs the units one after another in unit order.  Groups of 1, 64 and 1
+    # k-blocks: the 64-block group is scheduled first, so the first four units (its 2 x 2 tiles)
+    # are the long ones, and the gaps between consecutive unit ends show it.
+    M, N = 256, 256
+    off = [0, 64, 4160, 4224]
+    assert list(lib.ts_gemm_grouped_order(off)) == [1, 0, 2]
+    A = synth.int_uniform_bf16(631, (M, off[-1]))
+    B = synth.int_uniform_bf16(632, (N, off[-1]))
+    info = lib.ts_gemm_grouped_launch_info(M, N, off, lib.TS_OUT_F32, "static", tile="128x128", max_workers=1)
+    assert info["workers"] == 1 and info["num_units"] == 12
+    trace = torch.zeros(4 * info["num_units"], dtype=torch.int64, device="cuda")
+    D = _run(lib, A, B, off, torch.float32, sched="static", tile="128x128", max_workers=1, trace=trace)
+    ref = oracle.grouped_gemm_f64(A, B, off, blas=True)
+    for g in range(3):
+        assert_bit_exact(D[g], ref[g], f"group {g}")
+    tr = trace.view(-1, 4).cpu().numpy()
+    assert np.all(tr[:, 0] == 1) and np.all(tr[:, 1] == 0)
+    gaps = np.diff(tr[:, 3]).astype(np.float64)  # gaps[i]: end of unit i + 1 after the end of unit i
+    long_gaps, short_gaps = gaps[0:3], gaps[4:11]
+    assert long_gaps.mean() > 3 * short_gaps.mean(), (long_gaps, short_gaps)

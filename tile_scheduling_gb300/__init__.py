@@ -96,6 +96,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ts_gemm_bf16_grouped.argtypes = [P, P, P, I64, I64, I64, P, I32, I32, ctypes.POINTER(GemmOpts), P]
     lib.ts_gemm_grouped_launch_info.argtypes = [I64, I64, I64, P, I32, I32, ctypes.POINTER(GemmOpts),
                                                 ctypes.POINTER(LaunchInfo)]
+    lib.ts_gemm_grouped_order.argtypes = [I64, P, P]
     lib.ts_copy_i16.argtypes = [P, P, I64, P]
     lib.ts_copy_i16_rows.argtypes = [P, P, I64, P, I64, I32, ctypes.POINTER(RowsOpts), P]
     lib.ts_copy_rows_launch_info.argtypes = [I64, I64, I32, ctypes.POINTER(RowsOpts), ctypes.POINTER(LaunchInfo)]
@@ -110,7 +111,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ts_last_error_detail.restype = ctypes.c_char_p
     for name in ("ts_gemm_bf16", "ts_gemm_bf16_ex", "ts_gemm_launch_info", "ts_gemm_bf16_checked_noalloc",
                  "ts_gemm_tile_coords", "ts_gemm_protocol_info", "ts_gemm_bf16_grouped", "ts_gemm_grouped_launch_info",
-                 "ts_copy_i16", "ts_copy_i16_rows", "ts_copy_rows_launch_info", "ts_spin",
+                 "ts_gemm_grouped_order", "ts_copy_i16", "ts_copy_i16_rows", "ts_copy_rows_launch_info", "ts_spin",
                  "ts_spin_wait_started", "ts_sync_and_check"):
         getattr(lib, name).restype = ctypes.c_int
     return lib
@@ -355,6 +356,16 @@ def ts_gemm_grouped_launch_info(M: int, N: int, k_offsets, out=TS_OUT_BF16, sche
     _check(_lib.ts_gemm_grouped_launch_info(M, N, off.size - 1, off.ctypes.data, int(out), _sched(sched),
                                             ctypes.byref(o), ctypes.byref(info)))
     return {f: getattr(info, f) for f, _ in LaunchInfo._fields_}
+
+
+def ts_gemm_grouped_order(k_offsets) -> "np.ndarray":
+    """The order in which ts_gemm_bf16_grouped schedules the groups (longest K range first)."""
+    import numpy as np
+
+    off = _offsets(k_offsets)
+    order = np.zeros(off.size - 1, dtype=np.int32)
+    _check(_lib.ts_gemm_grouped_order(off.size - 1, off.ctypes.data, order.ctypes.data))
+    return order
 
 
 def ts_gemm_bf16_grouped(A: torch.Tensor, B: torch.Tensor, D: torch.Tensor, k_offsets, sched="static", tile="auto",

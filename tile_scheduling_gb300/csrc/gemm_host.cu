@@ -430,6 +430,17 @@ ts_status check_groups(int64_t groups, const int64_t *k_offsets) {
     return TS_OK;
 }
 
+// The order in which a grouped GEMM's groups are scheduled (GemmParams::group_order):
+// by K range, longest first; equal ranges keep their index order.
+void group_order(int64_t groups, const int64_t *k_offsets, uint8_t *order) {
+    int32_t idx[kMaxGroups];
+    for (int32_t g = 0; g < groups; ++g) idx[g] = g;
+    std::stable_sort(idx, idx + groups, [&](int32_t x, int32_t y) {
+        return k_offsets[x + 1] - k_offsets[x] > k_offsets[y + 1] - k_offsets[y];
+    });
+    for (int64_t i = 0; i < groups; ++i) order[i] = static_cast<uint8_t>(idx[i]);
+}
+
 // Shared launch path.  groups == 0: plain GEMM over K.  groups > 0: group g
 // multiplies columns [k_offsets[g], k_offsets[g + 1]) of A and B into D + g * M * ldd.
 ts_status gemm_launch(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K, int32_t out_dtype,
@@ -524,6 +535,7 @@ ts_status gemm_launch(const void *A, const void *B, void *D, int64_t M, int64_t 
     p.tiles_per_group = static_cast<int32_t>(pl.tiles_m * pl.tiles_n);
     p.group_stride = M * pl.ldd;
     for (int64_t g = 0; groups > 0 && g <= groups; ++g) p.group_kb[g] = static_cast<int32_t>(k_offsets[g] / 64);
+    group_order(groups, k_offsets, p.group_order);
     L.grid = static_cast<int>(pl.grid);
     L.stream = st;
     cudaError_t e = pl.v->launch(L);
@@ -547,6 +559,16 @@ ts_status ts_gemm_bf16_grouped(const void *A, const void *B, void *D, int64_t M,
     ts_status s = ts::check_groups(groups, k_offsets);
     if (s != TS_OK) return s;
     return ts::gemm_launch(A, B, D, M, N, k_offsets[groups], out_dtype, sched, opts, stream, groups, k_offsets);
+}
+
+ts_status ts_gemm_grouped_order(int64_t groups, const int64_t *k_offsets, int32_t *order) {
+    ts_status s = ts::check_groups(groups, k_offsets);
+    if (s != TS_OK) return s;
+    if (!order) return ts::fail(TS_ERR_INVALID_ARG, "order is NULL");
+    uint8_t o[ts::kMaxGroups];
+    ts::group_order(groups, k_offsets, o);
+    for (int64_t i = 0; i < groups; ++i) order[i] = o[i];
+    return TS_OK;
 }
 
 ts_status ts_gemm_grouped_launch_info(int64_t M, int64_t N, int64_t groups, const int64_t *k_offsets,

@@ -268,9 +268,11 @@ __device__ __forceinline__ Unit decode_unit(int32_t u, const GemmParams &p) {
     Unit w;
     w.group = 0;
     if (p.groups > 0) {
-        // dynamic domain: the k-block range comes from the group's offsets
-        w.group = u / p.tiles_per_group;
-        w.tile = u - w.group * p.tiles_per_group;
+        // dynamic domain: the k-block range comes from the group's offsets; the
+        // groups are scheduled longest first (GemmParams::group_order)
+        const int32_t slot = u / p.tiles_per_group;
+        w.group = p.group_order[slot];
+        w.tile = u - slot * p.tiles_per_group;
         w.kb0 = p.group_kb[w.group];
         w.kb1 = p.group_kb[w.group + 1];
         w.tail = -1;

@@ -92,14 +92,21 @@ struct GemmParams {
     int32_t *counters;     // split_tiles * CG * 8 slab counters (zero between launches)
     float *partials;       // split_tiles * parts * CG * 4 slabs of 32 x BN fp32
     // Grouped GEMM (groups > 0): unit u is tile u % tiles_per_group of group
-    // u / tiles_per_group, whose k-blocks are [group_kb[g], group_kb[g + 1]).
-    // D of group g starts group_stride elements after D of group g - 1.
+    // group_order[u / tiles_per_group], whose k-blocks are [group_kb[g],
+    // group_kb[g + 1]).  D of group g starts group_stride elements after D of
+    // group g - 1.
     const uint8_t *skip;   // per tile, row-major by tile row and column per group: nonzero = skip, or nullptr
     float *row_sums;       // Fork consumer output [groups][M]: sum over the K range of each row of A, or nullptr
     int32_t groups;
     int32_t tiles_per_group;
     int64_t group_stride;
     int32_t group_kb[kMaxGroups + 1];
+    // The groups in the order their tiles are scheduled: longest K range first
+    // (ties by group index).  Handing out the longest units first is Graham's
+    // LPT rule ("Bounds on Multiprocessing Timing Anomalies", 1969): the units
+    // left for the end of the launch are the short ones, so the workers finish
+    // closer together, under a static round-robin deal and under CLC alike.
+    uint8_t group_order[kMaxGroups];
 };
 
 #if defined(__CUDACC__)
