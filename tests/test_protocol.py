@@ -105,7 +105,7 @@ def test_clc_protocol_verified_cta_pair(units):
 @pytest.mark.slow
 def test_clc_protocol_verified_cta_pair_two_epilogue_warps_per_cta():
     # two epilogue warps per CTA of the pair, interleaved with each other and with the odd
-    # CTA's: ~9.6 million states, about 40 s
+    # CTA's: ~9.6 million states, about 10 s
     r = pc.check_variant("256x256", [1, 1], "clc", stages=2, epilogue_warps=2, max_states=30_000_000)
     assert r.ok, r.message
 

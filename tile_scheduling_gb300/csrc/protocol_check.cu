@@ -41,6 +41,7 @@
 // separately.  Counters start at 0; when every role has finished, each must be
 // back at 0 and have been drawn `last` exactly its expected number of times.
 #include <algorithm>
+#include <cstdint>
 #include <cstdio>
 #include <cstring>
 #include <string>
@@ -79,43 +80,77 @@ struct Model {
 
 struct Checker {
     const Model &m;
-    std::vector<uint64_t> table;
+    std::vector<uint64_t> table;  // open addressing, load factor at most one half; grows by doubling
     uint64_t mask;
     int64_t states = 0, max_states;
     std::string msg;
 
     Checker(const Model &mm, int64_t maxs) : m(mm), max_states(maxs) {
-        uint64_t cap = 1024;
-        while (cap < static_cast<uint64_t>(2 * maxs + 2)) cap <<= 1;
-        table.assign(cap, 0);
-        mask = cap - 1;
+        table.assign(uint64_t(1) << 16, 0);
+        mask = table.size() - 1;
     }
 
-    static uint64_t hash(const std::vector<int32_t> &s) {
-        uint64_t h = 0x9E3779B97F4A7C15ull;
-        for (int32_t v : s) {
-            h ^= static_cast<uint32_t>(v);
-            h *= 0x100000001B3ull;
-            h ^= h >> 29;
+    // Hash of the live words of a state: the unused tails of the tcgen05 queue
+    // and of the in-flight list always hold -1, so they are left out.  Four
+    // independent lanes (words 4j, 4j + 1, 4j + 2 and 4j + 3 of each part) keep
+    // the multiplies from forming one long dependency chain.
+    uint64_t hash(const int32_t *s) const {
+        uint64_t h[4] = {0x9E3779B97F4A7C15ull, 0xC2B2AE3D27D4EB4Full, 0x165667B19E3779F9ull, 0x27D4EB2F165667C5ull};
+        auto step = [](uint64_t &x, int32_t v) {
+            x = (x ^ static_cast<uint32_t>(v)) * 0x100000001B3ull;
+            x ^= x >> 29;
+        };
+        auto mix = [&](const int32_t *p, int n) {
+            int k = 0;
+            for (; k + 3 < n; k += 4) {
+                step(h[0], p[k]);
+                step(h[1], p[k + 1]);
+                step(h[2], p[k + 2]);
+                step(h[3], p[k + 3]);
+            }
+            for (int j = 0; k < n; ++k, ++j) step(h[j], p[k]);
+            step(h[3], n);
+        };
+        mix(s, m.o_mq + 1 + s[m.o_mq]);  // pcs, barriers, buffers, the queue's length and entries
+        mix(s + m.o_asy, 1 + s[m.o_asy]);
+        mix(s + m.o_ctr, m.len - m.o_ctr);
+        uint64_t x = h[0];
+        for (int j = 1; j < 4; ++j) {
+            x ^= (h[j] ^ (h[j] >> 31)) * (0x9E3779B97F4A7C15ull + 2 * static_cast<uint64_t>(j));
+            x ^= x >> 32;
         }
-        return h ? h : 1;
+        return x ? x : 1;
     }
 
-    bool insert(const std::vector<int32_t> &s) {  // true if new
-        uint64_t h = hash(s);
+    void grow() {
+        std::vector<uint64_t> old(table.size() * 2, 0);
+        old.swap(table);
+        mask = table.size() - 1;
+        for (uint64_t h : old) {
+            if (!h) continue;
+            uint64_t i = h & mask;
+            while (table[i]) i = (i + 1) & mask;
+            table[i] = h;
+        }
+    }
+
+    void prefetch(uint64_t h) const { __builtin_prefetch(&table[h & mask]); }
+
+    bool insert(uint64_t h) {  // true if new
         for (uint64_t i = h & mask;; i = (i + 1) & mask) {
             if (table[i] == h) return false;
             if (table[i] == 0) {
                 table[i] = h;
                 ++states;
+                if (2 * static_cast<uint64_t>(states) > table.size()) grow();
                 return true;
             }
         }
     }
 
-    void canon(std::vector<int32_t> &s) const {
+    void canon(int32_t *s) const {
         // copies in flight form a set: keep them sorted
-        std::sort(s.begin() + m.o_asy + 1, s.begin() + m.o_asy + 1 + s[m.o_asy]);
+        std::sort(s + m.o_asy + 1, s + m.o_asy + 1 + s[m.o_asy]);
         // roles of one symmetry group run identical programs: keep their pcs sorted
         for (int i = 0; i < m.nroles; ++i) {
             if (m.group[i] < 0) continue;
@@ -127,8 +162,8 @@ struct Checker {
     const int32_t *op(int idx) const { return m.ops + static_cast<int64_t>(idx) * kRec; }
 
     // returns false on over-arrival
-    bool arrive(std::vector<int32_t> &s, int b, int tx) const {
-        int32_t *bs = &s[m.o_bar + 3 * b];
+    bool arrive(int32_t *s, int b, int tx) const {
+        int32_t *bs = s + m.o_bar + 3 * b;
         bs[1] -= 1;
         bs[2] += tx;
         if (bs[1] < 0) return false;
@@ -138,15 +173,15 @@ struct Checker {
         }
         return true;
     }
-    void complete_tx(std::vector<int32_t> &s, int b, int bytes) const {
-        int32_t *bs = &s[m.o_bar + 3 * b];
+    void complete_tx(int32_t *s, int b, int bytes) const {
+        int32_t *bs = s + m.o_bar + 3 * b;
         bs[2] -= bytes;
         if (bs[1] == 0 && bs[2] == 0) {
             bs[0] += 1;
             bs[1] = m.expected[b];
         }
     }
-    bool push_list(std::vector<int32_t> &s, int o, int cap, int v) const {
+    static bool push_list(int32_t *s, int o, int cap, int v) {
         int32_t &n = s[o];
         if (n >= cap) return false;
         s[o + 1 + n] = v;
@@ -159,20 +194,48 @@ struct Checker {
         return false;
     }
 
-    // Successors of `s`; false if a violation was found (msg set).
-    bool expand(const std::vector<int32_t> &s, std::vector<std::vector<int32_t>> &out, bool &any) {
+    // True if role i's next op cannot run in state s (a wait on an incomplete
+    // phase, or a fence behind one of its own stores in flight).
+    bool blocked_at(const int32_t *s, int i, const int32_t *o) const {
+        if (o[0] == OP_WAIT) return s[m.o_bar + 3 * o[1]] % 2 == o[2];
+        if (o[0] == OP_FENCE) {
+            for (int k = 0; k < s[m.o_asy]; ++k) {
+                const int idx = s[m.o_asy + 1 + k];
+                if (idx >= m.off[i] && idx < m.off[i + 1]) return true;
+            }
+        }
+        return false;
+    }
+
+    // Successors of `s`, appended to `out` (m.len words each); false if a
+    // violation was found (msg set).
+    bool expand(const int32_t *s, std::vector<int32_t> &out, bool &any) {
         any = false;
-        std::vector<std::pair<int, int>> tried;  // (group, pc)
+        std::pair<int, int> tried[64];  // (group, pc) of the symmetric roles tried
+        int ntried = 0;
+        std::vector<std::pair<int, int>> tried_more;
+        auto start = [&]() -> int32_t * {  // a new successor, a copy of s
+            const size_t base = out.size();
+            out.resize(base + m.len);
+            std::memcpy(&out[base], s, sizeof(int32_t) * m.len);
+            return &out[base];
+        };
         for (int i = 0; i < m.nroles; ++i) {
             int pc = s[m.o_pc + i];
             const int end = m.off[i + 1] - m.off[i];
             if (pc >= end) continue;
             if (m.group[i] >= 0) {
                 std::pair<int, int> key(m.group[i], pc);
-                if (std::find(tried.begin(), tried.end(), key) != tried.end()) continue;
-                tried.push_back(key);
+                if (std::find(tried, tried + ntried, key) != tried + ntried ||
+                    std::find(tried_more.begin(), tried_more.end(), key) != tried_more.end())
+                    continue;
+                if (ntried < 64)
+                    tried[ntried++] = key;
+                else
+                    tried_more.push_back(key);
             }
-            std::vector<int32_t> t = s;
+            if (blocked_at(s, i, op(m.off[i] + pc))) continue;  // blocked at its first op
+            int32_t *t = start();
             bool first = true, arrived = false;
             while (pc < end) {
                 const int32_t *o = op(m.off[i] + pc);
@@ -182,12 +245,7 @@ struct Checker {
                 if (kind == OP_WAIT) {
                     if (t[m.o_bar + 3 * o[1]] % 2 == o[2]) break;
                 } else if (kind == OP_FENCE) {
-                    bool pending = false;
-                    for (int k = 0; k < t[m.o_asy]; ++k) {
-                        const int idx = t[m.o_asy + 1 + k];
-                        pending |= idx >= m.off[i] && idx < m.off[i + 1];
-                    }
-                    if (pending) break;
+                    if (blocked_at(t, i, o)) break;
                 } else if (kind == OP_TICKET) {
                     const int c = o[1];
                     const int drawn = t[m.o_ctr + 2 * c];
@@ -242,9 +300,7 @@ struct Checker {
                 ++pc;
                 first = false;
             }
-            if (first) continue;  // blocked at its first op
             t[m.o_pc + i] = pc;
-            out.push_back(std::move(t));
             any = true;
         }
         // asynchronous copies and CLC responses complete in any order
@@ -254,7 +310,7 @@ struct Checker {
             bool dup = false;
             for (int j = 0; j < k; ++j) dup |= s[m.o_asy + 1 + j] == idx;
             if (dup) continue;
-            std::vector<int32_t> t = s;
+            int32_t *t = start();
             // remove entry k
             for (int j = k; j < na - 1; ++j) t[m.o_asy + 1 + j] = t[m.o_asy + 2 + j];
             t[m.o_asy + na] = -1;
@@ -281,13 +337,12 @@ struct Checker {
                 for (int j = 4; j <= 5; ++j)
                     if (o[j] >= 0) complete_tx(t, o[j], o[6]);
             }
-            out.push_back(std::move(t));
             any = true;
         }
         // the tcgen05 queue executes in order
         const int nq = s[m.o_mq];
         if (nq > 0) {
-            std::vector<int32_t> t = s;
+            int32_t *t = start();
             for (int j = 0; j < nq - 1; ++j) t[m.o_mq + 1 + j] = t[m.o_mq + 2 + j];
             t[m.o_mq + nq] = -1;
             t[m.o_mq] = nq - 1;
@@ -314,23 +369,26 @@ struct Checker {
                     if (o[j] >= 0 && !arrive(t, o[j], 0))
                         return violation("commit: more arrivals than " + m.bar_name[o[j]] + " expects in a phase");
             }
-            out.push_back(std::move(t));
             any = true;
         }
         return true;
     }
 
     int run() {
-        std::vector<int32_t> s0(m.len, 0);
+        const int L = m.len;
+        std::vector<int32_t> s0(L, 0);
         for (int b = 0; b < m.nbars; ++b) s0[m.o_bar + 3 * b + 1] = m.expected[b];
         for (int x = 0; x < m.nbufs; ++x) s0[m.o_buf + x] = -1;
         for (int k = 0; k < kMaxQueue; ++k) s0[m.o_mq + 1 + k] = -1;
         for (int k = 0; k < kMaxAsync; ++k) s0[m.o_asy + 1 + k] = -1;
-        insert(s0);
-        std::vector<std::vector<int32_t>> stack{s0}, succ;
+        insert(hash(s0.data()));
+        // depth-first: the stack holds states end to end, L words each
+        std::vector<int32_t> stack(s0), succ, cur(L);
+        std::vector<uint64_t> hs;
         while (!stack.empty()) {
-            std::vector<int32_t> s = std::move(stack.back());
-            stack.pop_back();
+            std::memcpy(cur.data(), &stack[stack.size() - L], sizeof(int32_t) * L);
+            stack.resize(stack.size() - L);
+            const int32_t *s = cur.data();
             succ.clear();
             bool any = false;
             if (!expand(s, succ, any)) return 1;
@@ -360,14 +418,21 @@ struct Checker {
                 }
                 continue;
             }
-            for (auto &t : succ) {
-                canon(t);
-                if (insert(t)) {
+            // hash every successor first and prefetch its table slot, so the
+            // (mostly cache-missing) probes of one state's successors overlap
+            hs.clear();
+            for (size_t at = 0; at < succ.size(); at += L) {
+                canon(&succ[at]);
+                hs.push_back(hash(&succ[at]));
+                prefetch(hs.back());
+            }
+            for (size_t k = 0; k < hs.size(); ++k) {
+                if (insert(hs[k])) {
                     if (states > max_states) {
                         msg = "state limit reached";
                         return 2;
                     }
-                    stack.push_back(std::move(t));
+                    stack.insert(stack.end(), &succ[k * L], &succ[k * L] + L);
                 }
             }
         }
