@@ -35,8 +35,9 @@ typedef enum {
 
 /* Scheduling shapes (CUTLASS TS "Schedules", Scheduling Shapes): static persistent (a grid of
  * resident workers, tile i of worker w = w + i * workers), dynamic persistent (Cluster Launch
- * Control: one CTA or cluster per tile, running workers take over pending ones), and -- GEMM only --
- * non-persistent (one CTA or cluster per tile, each computing its own tile and exiting). */
+ * Control: one CTA or cluster per tile, running workers take over pending ones), and
+ * non-persistent (one CTA or cluster per tile, each computing its own tile and exiting).  The GEMM
+ * and the jagged row copy take all three. */
 typedef enum { TS_SCHED_STATIC = 0, TS_SCHED_CLC = 1, TS_SCHED_NONPERSISTENT = 2 } ts_sched;
 typedef enum { TS_OUT_BF16 = 0, TS_OUT_F32 = 1 } ts_out_dtype;
 
@@ -119,7 +120,7 @@ typedef struct {
     int32_t stages;          /* shared-memory ring depth */
     int64_t tiles_m, tiles_n, num_tiles;
     int64_t grid_ctas;       /* CTAs launched */
-    int64_t workers;         /* static: persistent workers launched; CLC: num_units */
+    int64_t workers;         /* static: persistent workers launched; CLC and non-persistent: num_units */
     int32_t smem_bytes;      /* dynamic shared memory per CTA */
     int32_t tma_store;       /* 1 if D is written through TMA stores, 0 for the st.global epilogue */
     int64_t num_units;       /* work units scheduled: whole tiles plus the K parts of split tiles */
