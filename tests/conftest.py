@@ -8,9 +8,24 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 
+def pytest_addoption(parser):
+    parser.addoption("--exhaustive", action="store_true", default=False,
+                     help="also run the exhaustive protocol searches (minutes of host work each)")
+
+
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
     config.addinivalue_line("markers", "slow: full-size workload (seconds of host work)")
+    config.addinivalue_line("markers", "exhaustive: a state-space search of minutes, run with --exhaustive")
+
+
+def pytest_collection_modifyitems(config, items):
+    if config.getoption("--exhaustive"):
+        return
+    skip = pytest.mark.skip(reason="exhaustive search: run with --exhaustive")
+    for item in items:
+        if "exhaustive" in item.keywords:
+            item.add_marker(skip)
 
 
 @pytest.fixture(scope="session")

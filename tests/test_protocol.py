@@ -110,6 +110,14 @@ def test_clc_protocol_verified_cta_pair_two_epilogue_warps_per_cta():
     assert r.ok, r.message
 
 
+@pytest.mark.exhaustive
+def test_clc_protocol_verified_cta_pair_three_epilogue_warps_per_cta():
+    # three epilogue warps per CTA of the pair: ~1.2e8 states, about 5 minutes and 4 GB of host
+    # memory (run with --exhaustive)
+    r = pc.check_variant("256x256", [1, 1], "clc", stages=2, epilogue_warps=3, max_states=150_000_000)
+    assert r.ok, r.message
+
+
 @pytest.mark.parametrize("mutation", [m for m in pc.MUTATIONS
                                       if not m.startswith(("fork", "merge")) and m not in pc.ZERO_K_MUTATIONS])
 @pytest.mark.parametrize("tile,sched,warps", [("128x256", "clc", None), ("256x256", "clc", 1),
