@@ -1158,7 +1158,7 @@ def cpu_baseline(args):
     threads = oracle.default_threads()
     w = synth.GEMM_8192
     probe_rate, _ = _oracle_sample_rate(2, threads)
-    rows = int(max(2, min(1024, args.cpu_seconds * probe_rate / (2.0 * w.N * w.K))))
+    rows = int(max(2, min(4096, args.cpu_seconds * probe_rate / (2.0 * w.N * w.K))))
     rate, dt = _oracle_sample_rate(rows, threads)
     return {"value": round(rate / 1e12, 8), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
             "sample": f"{rows} full rows of D ({rows * w.N} entries, K={w.K}) of the {w.M}x{w.N}x{w.K} workload, "
