@@ -535,7 +535,7 @@ ts_status gemm_launch(const void *A, const void *B, void *D, int64_t M, int64_t 
     p.tiles_per_group = static_cast<int32_t>(pl.tiles_m * pl.tiles_n);
     p.group_stride = M * pl.ldd;
     for (int64_t g = 0; groups > 0 && g <= groups; ++g) p.group_kb[g] = static_cast<int32_t>(k_offsets[g] / 64);
-    group_order(groups, k_offsets, p.group_order);
+    if (groups > 0) group_order(groups, k_offsets, p.group_order);
     L.grid = static_cast<int>(pl.grid);
     L.stream = st;
     cudaError_t e = pl.v->launch(L);
