@@ -59,7 +59,9 @@ typedef struct {
     int64_t *trace;       /* device buffer of 4 * num_units int64 (ts_launch_info), zeroed by the
                              caller, or NULL.  Per work unit u: [4u] += 1 per visit,
                              [4u+1] = worker index, [4u+2] = %globaltimer when the producer
-                             started the unit, [4u+3] = %globaltimer when the epilogue finished it. */
+                             started the unit, [4u+3] = %globaltimer when the epilogue finished it
+                             (for a skipped tile no data passes between the two, so [4u+3] may
+                             precede [4u+2]). */
     int32_t raster_group; /* tile raster: consecutive tile ids walk this many tile rows; 0 = 8 */
     int32_t split_tail;   /* 0: split the last, partial wave of tiles along K when `workspace` is
                              large enough; -1: never split */

@@ -234,7 +234,12 @@ def test_inputs_ready_with_split_tiles_row_sums_skip_and_trace(lib, sched):
     want[keep] = -1.0
     assert np.array_equal(Dk.cpu().numpy(), want)
     tr = trace.view(-1, 4).cpu().numpy()
-    assert np.all(tr[:, 0] == 1) and np.all(tr[:, 3] >= tr[:, 2])
+    assert np.all(tr[:, 0] == 1)
+    # a computed tile's epilogue ends after its producer began it; a skipped tile moves no data
+    # between the two, so its stamps are not ordered
+    mb, nb = lib.ts_gemm_tile_coords(Ms, N, Ks, lib.TS_OUT_F32, sched, tile="128x256")
+    computed = skip.cpu().numpy()[mb * tiles_n + nb] == 0
+    assert computed.any() and np.all(tr[computed, 3] >= tr[computed, 2])
 
 
 def test_inputs_ready_waits_do_not_time_out_behind_a_long_kernel(lib):
