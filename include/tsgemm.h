@@ -113,6 +113,21 @@ typedef struct {
                              write), so the first tiles' loads and MMAs overlap the previous kernel's
                              tail.  Results do not depend on it when the guarantee holds; when it
                              does not, they are undefined.  Anything else is TS_ERR_INVALID_ARG. */
+    int32_t *protocol_log; /* device int32 buffer or NULL: a test instrument.  When given, the launch
+                             runs the protocol-logging build of its kernel, in which every role's
+                             thread records its barrier operations in program order (waits with
+                             their parity, arrivals, TMA loads, MMA k-blocks, tcgen05 commits, CLC
+                             requests, the dependent-launch wait, and the units the producer
+                             begins), so that a host-side model of the role loops can be compared
+                             with them.  Layout: per CTA c and role r (0 producer, 1 MMA issuer,
+                             2 CLC scheduler, 3 warp 3, 4 + j epilogue warp j; 20 roles), a block of
+                             protocol_log_cap + 1 words at (c * 20 + r) * (protocol_log_cap + 1):
+                             the count of events, then the first protocol_log_cap events; the
+                             caller zeroes the buffer.  Built for three shapes only: tile 128x128
+                             (FusedMerge or Merge) and the 2-CTA 256x256 tile, fp32 output, four
+                             epilogue warps (others: TS_ERR_UNSUPPORTED).  Results are those of the
+                             normal build. */
+    int32_t protocol_log_cap; /* events per CTA and role (>= 1 when protocol_log is given) */
 } ts_gemm_opts;
 
 /* What ts_gemm_bf16_ex would launch for a problem (host-only query). */
@@ -132,6 +147,9 @@ typedef struct {
     int64_t workspace_bytes; /* workspace the split tiles need (0 when no split would help) */
     int32_t epi_warps;       /* epilogue warps per CTA (4, 8 or 16; CTAs have 128 + 32 * epi_warps threads) */
     int32_t merge;           /* 1: Merge barrier layout (A and B producers apart), 0: FusedMerge */
+    int32_t clc_lazy;        /* 1: CLC requests wait until the producer has nearly loaded its unit
+                                (K loops of 32 k-blocks or more under CLC) */
+    int32_t reserved;
 } ts_launch_info;
 
 /* The barrier protocol of one kernel variant: the numbers the kernel

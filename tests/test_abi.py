@@ -110,3 +110,32 @@ def test_row_copy_argument_errors_need_no_gpu(ts):
     assert "ceil(n / chunk)" in ts.ts_last_error_detail()
     # an empty queue launches nothing
     assert ts.ts_copy_i16_rows_ptr(0, 0, 0, 0, 0, stream=0) == ts.TS_OK
+
+
+def test_binding_structs_match_the_header_layout(ts):
+    # the ctypes mirrors of the option and info structs have the C layout (size and every offset)
+    import subprocess
+    import tempfile
+
+    structs = {"ts_gemm_opts": ts.GemmOpts, "ts_launch_info": ts.LaunchInfo, "ts_rows_opts": ts.RowsOpts,
+               "ts_gemm_protocol": ts.GemmProtocol}
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "tsgemm.h"', 'int main(void) {']
+    for cname, cls in structs.items():
+        lines.append(f'printf("{cname} size %zu\\n", sizeof({cname}));')
+        for f, _ in cls._fields_:
+            lines.append(f'printf("{cname} {f} %zu\\n", offsetof({cname}, {f}));')
+    lines += ["return 0;", "}"]
+    with tempfile.TemporaryDirectory() as d:
+        c = os.path.join(d, "layout.c")
+        with open(c, "w") as fh:
+            fh.write("\n".join(lines))
+        exe = os.path.join(d, "layout")
+        r = subprocess.run(["gcc", "-std=c99", "-I", os.path.join(ROOT, "include"), c, "-o", exe],
+                           capture_output=True, text=True)
+        assert r.returncode == 0, r.stderr
+        out = subprocess.run([exe], capture_output=True, text=True, check=True).stdout.split("\n")
+    got = {tuple(line.split()[:2]): int(line.split()[2]) for line in out if line}
+    for cname, cls in structs.items():
+        assert got[(cname, "size")] == ctypes.sizeof(cls), cname
+        for f, _ in cls._fields_:
+            assert got[(cname, f)] == getattr(cls, f).offset, f"{cname}.{f}"

@@ -23,6 +23,7 @@ TS_OK, TS_ERR_INVALID_ARG, TS_ERR_UNSUPPORTED, TS_ERR_CUDA, TS_ERR_TIMEOUT = ran
 TS_SCHED_STATIC, TS_SCHED_CLC, TS_SCHED_NONPERSISTENT = 0, 1, 2
 TS_OUT_BF16, TS_OUT_F32 = 0, 1
 TS_TILE_AUTO, TS_TILE_128x128, TS_TILE_128x256, TS_TILE_256x256_2CTA = range(4)
+PROTOCOL_LOG_ROLES = 20  # roles per CTA in a protocol log (ts_gemm_opts.protocol_log)
 
 _SCHED = {"static": TS_SCHED_STATIC, "clc": TS_SCHED_CLC, "nonpersistent": TS_SCHED_NONPERSISTENT}
 _TILE = {"auto": TS_TILE_AUTO, "128x128": TS_TILE_128x128, "128x256": TS_TILE_128x256,
@@ -48,7 +49,8 @@ class GemmOpts(ctypes.Structure):
                 ("trace", ctypes.c_void_p), ("raster_group", ctypes.c_int32), ("split_tail", ctypes.c_int32),
                 ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_int64), ("skip_tiles", ctypes.c_void_p),
                 ("row_sums", ctypes.c_void_p), ("epi_warps", ctypes.c_int32), ("merge", ctypes.c_int32),
-                ("inputs_ready", ctypes.c_int32)]
+                ("inputs_ready", ctypes.c_int32), ("protocol_log", ctypes.c_void_p),
+                ("protocol_log_cap", ctypes.c_int32)]
 
 
 class LaunchInfo(ctypes.Structure):
@@ -57,7 +59,8 @@ class LaunchInfo(ctypes.Structure):
                 ("num_tiles", ctypes.c_int64), ("grid_ctas", ctypes.c_int64), ("workers", ctypes.c_int64),
                 ("smem_bytes", ctypes.c_int32), ("tma_store", ctypes.c_int32), ("num_units", ctypes.c_int64),
                 ("split_tiles", ctypes.c_int64), ("split_parts", ctypes.c_int32), ("resident", ctypes.c_int32),
-                ("workspace_bytes", ctypes.c_int64), ("epi_warps", ctypes.c_int32), ("merge", ctypes.c_int32)]
+                ("workspace_bytes", ctypes.c_int64), ("epi_warps", ctypes.c_int32), ("merge", ctypes.c_int32),
+                ("clc_lazy", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 class RowsOpts(ctypes.Structure):
@@ -142,11 +145,18 @@ def _sched(s) -> int:
 
 
 def _opts(tile="auto", max_workers=0, lda=0, ldb=0, ldd=0, timeout_s=0.0, trace=None, raster_group=0,
-          split_tail=0, workspace=None, skip_tiles=None, row_sums=None, epi_warps=0, merge=0, inputs_ready=0):
+          split_tail=0, workspace=None, skip_tiles=None, row_sums=None, epi_warps=0, merge=0, inputs_ready=0,
+          protocol_log=None):
     o = GemmOpts()
     o.epi_warps = int(epi_warps)
     o.merge = int(merge)
     o.inputs_ready = int(inputs_ready)
+    if protocol_log is not None:
+        if protocol_log.dtype != torch.int32 or not protocol_log.is_cuda or protocol_log.dim() != 3 or \
+                not protocol_log.is_contiguous() or protocol_log.shape[1] != PROTOCOL_LOG_ROLES:
+            raise TypeError(f"protocol_log must be a contiguous int32 CUDA tensor [CTAs][{PROTOCOL_LOG_ROLES}][cap + 1]")
+        o.protocol_log = protocol_log.data_ptr()
+        o.protocol_log_cap = protocol_log.shape[2] - 1
     if row_sums is not None:
         if row_sums.dtype != torch.float32 or not row_sums.is_cuda or not row_sums.is_contiguous():
             raise TypeError("row_sums must be a contiguous float32 CUDA tensor")
@@ -215,7 +225,8 @@ def workspace_for(nbytes: int, device=None) -> torch.Tensor:
 
 def ts_gemm_bf16_ex(A: torch.Tensor, B: torch.Tensor, D: torch.Tensor, sched="static", tile="auto",
                     max_workers=0, timeout_s=0.0, trace=None, raster_group=0, workspace="auto", split_tail=0,
-                    skip_tiles=None, row_sums=None, epi_warps=0, merge=0, inputs_ready=0, stream=None) -> None:
+                    skip_tiles=None, row_sums=None, epi_warps=0, merge=0, inputs_ready=0, protocol_log=None,
+                    stream=None) -> None:
     """D = A @ B.T for bf16 A [M, K] and B [N, K]; D [M, N] is bf16 or fp32.
 
     Rows may be strided (the row stride becomes lda / ldb / ldd).  ``workspace``
@@ -223,15 +234,17 @@ def ts_gemm_bf16_ex(A: torch.Tensor, B: torch.Tensor, D: torch.Tensor, sched="st
     lets the tiles that would leave the last wave partly empty be split along K.  ``epi_warps``: 4, 8,
     16 (256-column tiles) or 0 (automatic); ``merge``: 1 for the Merge barrier layout (A and B from
     separate producer warps); ``inputs_ready``: 1 when A, B and skip_tiles were final before the
-    previous kernel in the stream began (their loads then overlap that kernel's tail).  Asynchronous on
-    ``stream`` (default: torch's current stream)."""
+    previous kernel in the stream began (their loads then overlap that kernel's tail);
+    ``protocol_log``: a zeroed int32 CUDA tensor [CTAs][PROTOCOL_LOG_ROLES][cap + 1] that the
+    protocol-logging build fills with every role's barrier operations (a test instrument).
+    Asynchronous on ``stream`` (default: torch's current stream)."""
     M, N, K, lda, ldb, ldd = _gemm_args(A, B, D)
     lda, ldb, ldd = (lda if M > 1 else 0), (ldb if N > 1 else 0), (ldd if M > 1 else 0)
     workspace = _resolve_workspace(M, N, K, _OUT[D.dtype], sched, workspace,
                                    -1 if (skip_tiles is not None or row_sums is not None) else split_tail, tile=tile,
                                    max_workers=max_workers, lda=lda, ldb=ldb, ldd=ldd)
     o = _opts(tile, max_workers, lda, ldb, ldd, timeout_s, trace, raster_group, split_tail, workspace, skip_tiles,
-              row_sums, epi_warps, merge, inputs_ready)
+              row_sums, epi_warps, merge, inputs_ready, protocol_log)
     _check(_lib.ts_gemm_bf16_ex(ctypes.c_void_p(A.data_ptr()), ctypes.c_void_p(B.data_ptr()),
                                 ctypes.c_void_p(D.data_ptr()), M, N, K, _OUT[D.dtype], _sched(sched),
                                 ctypes.byref(o), _stream_handle(stream)))
@@ -370,7 +383,8 @@ def ts_gemm_grouped_order(k_offsets) -> "np.ndarray":
 
 def ts_gemm_bf16_grouped(A: torch.Tensor, B: torch.Tensor, D: torch.Tensor, k_offsets, sched="static", tile="auto",
                          max_workers=0, timeout_s=0.0, trace=None, raster_group=0, skip_tiles=None,
-                         row_sums=None, epi_warps=0, merge=0, inputs_ready=0, stream=None) -> None:
+                         row_sums=None, epi_warps=0, merge=0, inputs_ready=0, protocol_log=None,
+                         stream=None) -> None:
     """D[g] = A[:, k_g:k_g+1] @ B[:, k_g:k_g+1].T for every group g (k_offsets: groups + 1 multiples of 64).
 
     A [M, >=K] and B [N, >=K] bf16 with unit column stride; D [groups, M, N]
@@ -388,7 +402,7 @@ def ts_gemm_bf16_grouped(A: torch.Tensor, B: torch.Tensor, D: torch.Tensor, k_of
         raise ValueError("k_offsets reach past the columns of A or B")
     o = _opts(tile, max_workers, lda if M > 1 else 0, ldb if N > 1 else 0, D.stride(1) if M > 1 else 0, timeout_s,
               trace, raster_group, skip_tiles=skip_tiles, row_sums=row_sums, epi_warps=epi_warps, merge=merge,
-              inputs_ready=inputs_ready)
+              inputs_ready=inputs_ready, protocol_log=protocol_log)
     _check(_lib.ts_gemm_bf16_grouped(ctypes.c_void_p(A.data_ptr()), ctypes.c_void_p(B.data_ptr()),
                                      ctypes.c_void_p(D.data_ptr()), M, N, G, off.ctypes.data, _OUT[D.dtype],
                                      _sched(sched), ctypes.byref(o), _stream_handle(stream)))

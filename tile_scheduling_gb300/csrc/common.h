@@ -30,13 +30,14 @@ struct GemmLaunch {
 };
 
 struct GemmVariant {
-    int bn, cg, out, epi_warps, merge, stages, smem_bytes;
+    int bn, cg, out, epi_warps, merge, log, stages, smem_bytes;
     ts_gemm_protocol protocol;  // barrier layout and arrival counts of this variant
     cudaError_t (*launch)(const GemmLaunch &);
     // Workers (CTAs, or 2-CTA clusters) that can be resident at once.
     cudaError_t (*max_workers)(int *);
 };
 
-const GemmVariant *find_variant(int bn, int cg, int out, int epi_warps, int merge);
+// log = 1: the protocol-logging instantiation (a test instrument; few shapes have one).
+const GemmVariant *find_variant(int bn, int cg, int out, int epi_warps, int merge, int log = 0);
 
 }  // namespace ts

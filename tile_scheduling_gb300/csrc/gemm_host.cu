@@ -16,18 +16,22 @@ extern const GemmVariant variant_128_1_bf16_e4, variant_128_1_f32_e4, variant_25
     variant_256_2_bf16_e4, variant_256_2_f32_e4, variant_128_1_bf16_e8, variant_128_1_f32_e8, variant_256_1_bf16_e8,
     variant_256_1_f32_e8, variant_256_2_bf16_e8, variant_256_2_f32_e8, variant_128_1_bf16_e4m, variant_128_1_f32_e4m,
     variant_256_1_bf16_e4m, variant_256_1_f32_e4m, variant_256_2_bf16_e4m, variant_256_2_f32_e4m,
-    variant_256_1_bf16_e16, variant_256_1_f32_e16, variant_256_2_bf16_e16, variant_256_2_f32_e16;
+    variant_256_1_bf16_e16, variant_256_1_f32_e16, variant_256_2_bf16_e16, variant_256_2_f32_e16,
+    variant_128_1_f32_e4_log, variant_128_1_f32_e4m_log, variant_256_2_f32_e4_log;
 
-const GemmVariant *find_variant(int bn, int cg, int out, int epi_warps, int merge) {
+const GemmVariant *find_variant(int bn, int cg, int out, int epi_warps, int merge, int log) {
     static const GemmVariant *const all[] = {
-        &variant_128_1_bf16_e4,  &variant_128_1_f32_e4,  &variant_256_1_bf16_e4,  &variant_256_1_f32_e4,
-        &variant_256_2_bf16_e4,  &variant_256_2_f32_e4,  &variant_128_1_bf16_e8,  &variant_128_1_f32_e8,
-        &variant_256_1_bf16_e8,  &variant_256_1_f32_e8,  &variant_256_2_bf16_e8,  &variant_256_2_f32_e8,
-        &variant_128_1_bf16_e4m, &variant_128_1_f32_e4m, &variant_256_1_bf16_e4m, &variant_256_1_f32_e4m,
-        &variant_256_2_bf16_e4m, &variant_256_2_f32_e4m, &variant_256_1_bf16_e16, &variant_256_1_f32_e16,
-        &variant_256_2_bf16_e16, &variant_256_2_f32_e16};
+        &variant_128_1_bf16_e4,     &variant_128_1_f32_e4,      &variant_256_1_bf16_e4,  &variant_256_1_f32_e4,
+        &variant_256_2_bf16_e4,     &variant_256_2_f32_e4,      &variant_128_1_bf16_e8,  &variant_128_1_f32_e8,
+        &variant_256_1_bf16_e8,     &variant_256_1_f32_e8,      &variant_256_2_bf16_e8,  &variant_256_2_f32_e8,
+        &variant_128_1_bf16_e4m,    &variant_128_1_f32_e4m,     &variant_256_1_bf16_e4m, &variant_256_1_f32_e4m,
+        &variant_256_2_bf16_e4m,    &variant_256_2_f32_e4m,     &variant_256_1_bf16_e16, &variant_256_1_f32_e16,
+        &variant_256_2_bf16_e16,    &variant_256_2_f32_e16,     &variant_128_1_f32_e4_log,
+        &variant_128_1_f32_e4m_log, &variant_256_2_f32_e4_log};
     for (const GemmVariant *v : all)
-        if (v->bn == bn && v->cg == cg && v->out == out && v->epi_warps == epi_warps && v->merge == merge) return v;
+        if (v->bn == bn && v->cg == cg && v->out == out && v->epi_warps == epi_warps && v->merge == merge &&
+            v->log == log)
+            return v;
     return nullptr;
 }
 
@@ -238,7 +242,11 @@ ts_status plan_gemm(const void *D, int64_t M, int64_t N, int64_t K, int32_t out,
     }
     if (epi_warps == 16 && bn != 256)
         return fail(TS_ERR_UNSUPPORTED, "sixteen epilogue warps are built for 256-column tiles only");
-    pl->v = find_variant(bn, cg, out, epi_warps, o->merge);
+    if (o->protocol_log && o->protocol_log_cap < 1)
+        return fail(TS_ERR_INVALID_ARG, "protocol_log_cap = %d (>= 1 with a protocol log)", o->protocol_log_cap);
+    const int log = o->protocol_log ? 1 : 0;
+    pl->v = find_variant(bn, cg, out, epi_warps, o->merge, log);
+    if (!pl->v && log) return fail(TS_ERR_UNSUPPORTED, "no protocol-logging build of tile %d with these options", tile);
     if (!pl->v) return fail(TS_ERR_UNSUPPORTED, "no compiled variant for tile %d", tile);
     pl->cg = cg;
     pl->tile_m = 128 * cg;
@@ -304,6 +312,7 @@ namespace ts {
 ts_status fill_info(int64_t M, int64_t N, int64_t K, int32_t out_dtype, int32_t sched, const ts_gemm_opts *opts,
                     ts_launch_info *info, int64_t groups) {
     if (!info) return ts::fail(TS_ERR_INVALID_ARG, "info is NULL");
+    std::memset(info, 0, sizeof *info);
     ts::Plan pl;
     // alignment of D is unknown here: report the TMA-store epilogue when the pitch allows it
     ts_status s = ts::plan_gemm(reinterpret_cast<const void *>(uintptr_t(256)), M, N, K, out_dtype, sched, opts, &pl,
@@ -327,6 +336,7 @@ ts_status fill_info(int64_t M, int64_t N, int64_t K, int32_t out_dtype, int32_t 
     info->workspace_bytes = pl.split_ws_bytes;
     info->epi_warps = pl.v->epi_warps;
     info->merge = pl.v->merge;
+    info->clc_lazy = (sched == TS_SCHED_CLC && groups == 0 && cdiv(K, 64) >= kLazyClcKBlocks) ? 1 : 0;
     return TS_OK;
 }
 }  // namespace ts
@@ -514,7 +524,7 @@ ts_status gemm_launch(const void *A, const void *B, void *D, int64_t M, int64_t 
     p.sched = sched;
     p.tma_store = pl.tma_store;
     p.clc_depth = 2;
-    p.clc_lazy = (groups == 0 && p.num_k_blocks >= kLazyClcKBlocks) ? 1 : 0;
+    p.clc_lazy = (groups == 0 && p.num_k_blocks >= kLazyClcKBlocks) ? 1 : 0;  // (ts_launch_info.clc_lazy)
     // Units of odd waves walk their K range downwards (see GemmParams::k_alt).  The
     // wave length is the number of workers that fit at once, whatever the scheduler
     // or the static cap, so a unit's summation order is a function of the plan alone.
@@ -531,6 +541,8 @@ ts_status gemm_launch(const void *A, const void *B, void *D, int64_t M, int64_t 
     p.trace = reinterpret_cast<long long *>(o->trace);
     p.skip = o->skip_tiles;
     p.row_sums = o->row_sums;
+    p.plog = o->protocol_log;
+    p.plog_cap = o->protocol_log_cap;
     p.groups = static_cast<int32_t>(groups);
     p.tiles_per_group = static_cast<int32_t>(pl.tiles_m * pl.tiles_n);
     p.group_stride = M * pl.ldd;

@@ -84,12 +84,15 @@ constexpr int kLazyLeadKBlocks = 16;
 // (one producer thread loads A and B onto one full barrier per stage, 2 * S
 // barriers); 1 is Merge (a producer for A on warp 0 and one for B on warp 3,
 // each with its own full barrier per stage, sharing the empty barrier:
-// 3 * S barriers).
-template <int BN_, int CG_, int OUT_, int EW_, int MG_ = 0>
+// 3 * S barriers).  LOG_ = 1 compiles in the protocol log (a test instrument:
+// every role records its barrier operations; see PLog); the product variants
+// have LOG_ = 0, where every logging call compiles to nothing.
+template <int BN_, int CG_, int OUT_, int EW_, int MG_ = 0, int LOG_ = 0>
 struct GemmCfg {
     static constexpr int BN = BN_, CG = CG_, OUT = OUT_;
     static constexpr int EPI_WARPS = EW_;
     static constexpr int MERGE = MG_;
+    static constexpr bool LOG = LOG_ != 0;
     static constexpr int THREADS = 32 * (kRoleWarps + EPI_WARPS);
     static constexpr int BM = 128;              // accumulator rows per CTA = TMEM lanes
     static constexpr int TILE_M = BM * CG;      // output rows per worker
@@ -219,6 +222,69 @@ __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, volati
     return wait_slow(bar, parity, p.drain_ns, abort_flag, false, p, WAIT_DRAIN);
 }
 
+// Protocol log: the barrier operations of each role's thread, in program
+// order, so that a host-side model of the role loops can be compared with what
+// the kernel does.  Event word: op | family << 4 | index << 8 | parity << 16
+// (for PL_UNIT: op | skip << 4 | k-blocks << 8).  Roles: 0 the (A) producer,
+// 1 the MMA issuer, 2 the CLC scheduler, 3 warp 3 (Merge B producer or Fork
+// task), 4 + j epilogue warp j (lane 0).  Per CTA and role the log holds a
+// count (events recorded, which may exceed the capacity) and `cap` words.
+enum PlogOp : int32_t {
+    PL_WAIT = 1,    // mbarrier wait on (family, index) with the given parity
+    PL_ARRIVE = 2,  // arrive (with expect-tx where the op arms transaction bytes)
+    PL_TMA = 3,     // a TMA load completing on (family, index)
+    PL_MMA = 4,     // the MMAs of one k-block, reading ring stage `index`
+    PL_COMMIT = 5,  // tcgen05.commit arriving on (family, index)
+    PL_CREQ = 6,    // a CLC request into response slot `index`
+    PL_PDL = 7,     // the wait on the dependent-launch barrier
+    PL_UNIT = 8,    // the producer begins a unit
+    PL_TLOAD = 9,   // this warp's reads of accumulator `index` are complete
+    PL_CREAD = 10,  // CLC response slot `index` read
+    PL_SREAD = 11   // ring stage `index` read by the Fork task
+};
+enum PlogFamily : int32_t {
+    PF_FULL = 0, PF_EMPTY = 1, PF_TFULL = 2, PF_TEMPTY = 3, PF_CLC_FULL = 4, PF_CLC_EMPTY = 5,
+    PF_AUX = 6,  // the Fork task's empty barrier, or Merge's full barrier of B
+    PF_BEGAN = 7, PF_MMA_DONE = 8, PF_NONE = 15
+};
+constexpr int kPlogRoles = kRoleWarps + 16;
+
+template <bool ON>
+struct PLog {
+    int32_t *buf = nullptr;
+    int32_t cap = 0, n = 0;
+    __device__ __forceinline__ void open(const GemmParams &p, int role) {
+        if constexpr (ON) {
+            if (p.plog) {
+                buf = p.plog + (static_cast<int64_t>(blockIdx.x) * kPlogRoles + role) * (p.plog_cap + 1);
+                cap = p.plog_cap;
+            }
+        }
+    }
+    __device__ __forceinline__ void put(int32_t op, int32_t family, uint32_t index, uint32_t parity) {
+        if constexpr (ON) {
+            if (buf) {
+                if (n < cap) buf[1 + n] = op | (family << 4) | static_cast<int32_t>(index << 8) |
+                                          static_cast<int32_t>((parity & 1u) << 16);
+                ++n;
+            }
+        }
+    }
+    __device__ __forceinline__ void unit(bool skip, int32_t nkb) {
+        if constexpr (ON) {
+            if (buf) {
+                if (n < cap) buf[1 + n] = PL_UNIT | ((skip ? 1 : 0) << 4) | (nkb << 8);
+                ++n;
+            }
+        }
+    }
+    __device__ __forceinline__ void close() {
+        if constexpr (ON) {
+            if (buf) buf[0] = n;
+        }
+    }
+};
+
 // Shared-memory map of one CTA.
 template <class C>
 struct Smem {
@@ -308,15 +374,19 @@ __device__ __forceinline__ Unit decode_unit(int32_t u, const GemmParams &p) {
 // next work unit, or -1 when the cancel failed (no pending launch left) or the
 // kernel is aborting.
 template <class C>
-__device__ __forceinline__ int32_t clc_consume(const Smem<C> &sm, const GemmParams &p, uint32_t &idx) {
+__device__ __forceinline__ int32_t clc_consume(const Smem<C> &sm, const GemmParams &p, uint32_t &idx,
+                                               PLog<C::LOG> &lg) {
     const uint32_t depth = static_cast<uint32_t>(p.clc_depth);
     const uint32_t r = idx % depth;
     const uint32_t ph = (idx / depth) & 1u;
     ++idx;
+    lg.put(PL_WAIT, PF_CLC_FULL, r, ph);
     if (!wait_phase(sm.clc_full(r), ph, sm.abort_flag, p, WAIT_CLC_FULL)) return -1;
     uint32_t x = 0;
     const bool ok = clc_query(sm.resp + 16u * r, x);
+    lg.put(PL_CREAD, PF_CLC_FULL, r, 0);
     fence_proxy_async_smem();  // our generic read of the slot before the next async write into it
+    lg.put(PL_ARRIVE, PF_CLC_EMPTY, r, 0);
     if constexpr (C::CG == 1)
         mbar_arrive(sm.clc_empty(r));
     else
@@ -326,20 +396,21 @@ __device__ __forceinline__ int32_t clc_consume(const Smem<C> &sm, const GemmPara
 
 template <class C>
 __device__ __forceinline__ int32_t next_unit(const Smem<C> &sm, const GemmParams &p, int32_t unit,
-                                             uint32_t &clc_idx) {
+                                             uint32_t &clc_idx, PLog<C::LOG> &lg) {
     if (p.sched == SCHED_STATIC) {
         const int32_t u = unit + static_cast<int32_t>(gridDim.x / C::CG);
         return u < p.num_units ? u : -1;
     }
     if (p.sched == SCHED_NONPERSISTENT) return -1;  // one unit per CTA (cluster)
-    return clc_consume(sm, p, clc_idx);
+    return clc_consume(sm, p, clc_idx, lg);
 }
 
-template <int BN, int CG, int OUT, int EW, int MG>
+template <int BN, int CG, int OUT, int EW, int MG, int LOG = 0>
 __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
     gemm_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmD, const __grid_constant__ GemmParams p) {
-    using C = GemmCfg<BN, CG, OUT, EW, MG>;
+    using C = GemmCfg<BN, CG, OUT, EW, MG, LOG>;
+    using Log = PLog<C::LOG>;
     constexpr int RAW = C::SUB_COLS;  // fp32 accumulator words per lane per store subtile
     extern __shared__ __align__(1024) uint8_t smem_raw[];
 
@@ -430,8 +501,9 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
         grid_dep_launch();
     }
     // A role's wait on the barrier after its first unit (inputs_ready only).
-    auto dep_wait_once = [&](bool &waited) {
+    auto dep_wait_once = [&](bool &waited, Log &lg) {
         if (p.inputs_ready && !waited) {
+            lg.put(PL_PDL, PF_NONE, 0, 0);
             grid_dep_wait();
             waited = true;
         }
@@ -447,17 +519,24 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
     // warp 0 loads A onto full(s) and warp 3 loads B onto full_b(s).
     auto produce = [&](const bool load_a, const bool load_b, const bool b_bar, const uint32_t tx) {
         auto full_bar = [&](uint32_t st) { return b_bar ? sm.full_b(st) : sm.full(st); };
+        const int32_t full_fam = b_bar ? PF_AUX : PF_FULL;
+        Log lg;
+        lg.open(p, load_a ? 0 : 3);
         int32_t unit = first_unit;
         uint32_t clc_idx = 0, stage = 0, phase = 0, issued = 0;
         bool alive = true, waited = false;
-        if (p.trace) dep_wait_once(waited);  // the trace is written below
+        if (p.trace) dep_wait_once(waited, lg);  // the trace is written below
         while (unit >= 0 && alive) {
             const Unit w = decode_unit(unit, p);
             const int32_t nkb = w.kb1 - w.kb0;
+            lg.unit(w.skip, nkb);
             // the load at which the unit counts as nearly loaded (lazy CLC requests wait for it)
             const int32_t near_end = nkb > kLazyLeadKBlocks ? nkb - kLazyLeadKBlocks : 0;
             const bool rev = p.k_alt && (fast_div(unit, p.div_wave) & 1);
-            if (load_a && nkb <= 0) mbar_arrive(sm.prod_began());
+            if (load_a && nkb <= 0) {
+                lg.put(PL_ARRIVE, PF_BEGAN, 0, 0);
+                mbar_arrive(sm.prod_began());
+            }
             int32_t mb, nb;
             raster(w.tile, p, mb, nb);
             const int32_t a_row = mb * C::TILE_M + static_cast<int32_t>(rank) * C::BM;
@@ -465,14 +544,27 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
             if (p.trace && rank == 0 && load_a) p.trace[4 * unit + 2] = static_cast<long long>(globaltimer());
             for (int32_t i = 0; i < nkb; ++i) {
                 const int32_t kb = rev ? w.kb1 - 1 - i : w.kb0 + i;
-                if (load_a && i == near_end) mbar_arrive(sm.prod_began());
-                if (!wait_phase(sm.empty(stage), phase ^ 1u, sm.abort_flag, p, WAIT_PRODUCER_EMPTY) ||
-                    (fork && !wait_phase(sm.aux_empty(stage), phase ^ 1u, sm.abort_flag, p, WAIT_PRODUCER_EMPTY))) {
+                if (load_a && i == near_end) {
+                    lg.put(PL_ARRIVE, PF_BEGAN, 0, 0);
+                    mbar_arrive(sm.prod_began());
+                }
+                lg.put(PL_WAIT, PF_EMPTY, stage, phase ^ 1u);
+                if (!wait_phase(sm.empty(stage), phase ^ 1u, sm.abort_flag, p, WAIT_PRODUCER_EMPTY)) {
                     alive = false;
                     break;
                 }
+                if (fork) {
+                    lg.put(PL_WAIT, PF_AUX, stage, phase ^ 1u);
+                    if (!wait_phase(sm.aux_empty(stage), phase ^ 1u, sm.abort_flag, p, WAIT_PRODUCER_EMPTY)) {
+                        alive = false;
+                        break;
+                    }
+                }
                 const uint32_t fb = full_bar(stage);
-                if (rank == 0) mbar_arrive_expect_tx(fb, tx);
+                if (rank == 0) {
+                    lg.put(PL_ARRIVE, full_fam, stage, 0);
+                    mbar_arrive_expect_tx(fb, tx);
+                }
                 const uint32_t da = sm.a + stage * C::A_BYTES;
                 const uint32_t db = sm.b + stage * C::B_BYTES;
                 if constexpr (CG == 1) {
@@ -483,6 +575,7 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
                     if (load_a) tma_load_2d_pair(da, &tmA, fb0, kb * C::BK, a_row);
                     if (load_b) tma_load_2d_pair(db, &tmB, fb0, kb * C::BK, b_row);
                 }
+                lg.put(PL_TMA, full_fam, stage, 0);  // this producer's loads of the stage
                 ++issued;
                 if (++stage == C::STAGES) {
                     stage = 0;
@@ -490,27 +583,33 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
                 }
             }
             if (!alive) break;
-            dep_wait_once(waited);
-            unit = next_unit(sm, p, unit, clc_idx);
+            dep_wait_once(waited, lg);
+            unit = next_unit(sm, p, unit, clc_idx, lg);
         }
-        dep_wait_once(waited);
+        dep_wait_once(waited, lg);
         // Drain: every issued load has landed (even CTA's full barriers) and
         // the MMA has released every stage.
         if (rank == 0) {
             const uint32_t n = issued < C::STAGES ? issued : C::STAGES;
             for (uint32_t i = 1; i <= n; ++i) {
                 const uint32_t b = issued - i;
+                lg.put(PL_WAIT, full_fam, b % C::STAGES, (b / C::STAGES) & 1u);
                 wait_drain(full_bar(b % C::STAGES), (b / C::STAGES) & 1u, sm.abort_flag, p);
             }
         }
         for (int i = 0; i < C::STAGES; ++i) {
+            lg.put(PL_WAIT, PF_EMPTY, stage, phase ^ 1u);
             if (!wait_drain(sm.empty(stage), phase ^ 1u, sm.abort_flag, p)) break;
-            if (fork && !wait_drain(sm.aux_empty(stage), phase ^ 1u, sm.abort_flag, p)) break;
+            if (fork) {
+                lg.put(PL_WAIT, PF_AUX, stage, phase ^ 1u);
+                if (!wait_drain(sm.aux_empty(stage), phase ^ 1u, sm.abort_flag, p)) break;
+            }
             if (++stage == C::STAGES) {
                 stage = 0;
                 phase ^= 1u;
             }
         }
+        lg.close();
     };
 
     if (warp == 0) {
@@ -525,24 +624,34 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
         if (lane == 0 && rank == 0) {
+            Log lg;
+            lg.open(p, 1);
             int32_t unit = first_unit;
             uint32_t clc_idx = 0, stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool alive = true, waited = false;
             while (unit >= 0 && alive) {
                 const Unit w = decode_unit(unit, p);
                 if (w.skip) {  // no accumulator is used for a skipped tile
-                    dep_wait_once(waited);
-                    unit = next_unit(sm, p, unit, clc_idx);
+                    dep_wait_once(waited, lg);
+                    unit = next_unit(sm, p, unit, clc_idx, lg);
                     continue;
                 }
+                lg.put(PL_WAIT, PF_TEMPTY, acc, acc_phase ^ 1u);
                 if (!wait_phase(sm.tempty(acc), acc_phase ^ 1u, sm.abort_flag, p, WAIT_MMA_TMEM_EMPTY)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
                 for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
-                    if (!wait_phase(sm.full(stage), phase, sm.abort_flag, p, WAIT_MMA_FULL) ||
-                        (MG && !wait_phase(sm.full_b(stage), phase, sm.abort_flag, p, WAIT_MMA_FULL))) {
+                    lg.put(PL_WAIT, PF_FULL, stage, phase);
+                    if (!wait_phase(sm.full(stage), phase, sm.abort_flag, p, WAIT_MMA_FULL)) {
                         alive = false;
                         break;
+                    }
+                    if constexpr (MG) {
+                        lg.put(PL_WAIT, PF_AUX, stage, phase);
+                        if (!wait_phase(sm.full_b(stage), phase, sm.abort_flag, p, WAIT_MMA_FULL)) {
+                            alive = false;
+                            break;
+                        }
                     }
                     tc_fence_after();
                     const uint64_t da = sw128_kmajor_desc(sm.a + stage * C::A_BYTES);
@@ -553,6 +662,8 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
                         // the first MMA of a unit overwrites the accumulator
                         mma_bf16<CG>(d_tmem, da + 2u * kk, db + 2u * kk, C::IDESC, (kb != w.kb0) || (kk != 0));
                     }
+                    lg.put(PL_MMA, PF_FULL, stage, 0);
+                    lg.put(PL_COMMIT, PF_EMPTY, stage, 0);
                     if constexpr (CG == 1)
                         mma_commit(sm.empty(stage));
                     else
@@ -563,6 +674,7 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
                     }
                 }
                 if (!alive) break;
+                lg.put(PL_COMMIT, PF_TFULL, acc, 0);
                 if constexpr (CG == 1)
                     mma_commit(sm.tfull(acc));
                 else
@@ -571,21 +683,26 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
                     acc = 0;
                     acc_phase ^= 1u;
                 }
-                dep_wait_once(waited);
-                unit = next_unit(sm, p, unit, clc_idx);
+                dep_wait_once(waited, lg);
+                unit = next_unit(sm, p, unit, clc_idx, lg);
             }
-            dep_wait_once(waited);
+            dep_wait_once(waited, lg);
             // Every MMA issued by this thread has completed before TMEM is freed.
+            lg.put(PL_COMMIT, PF_MMA_DONE, 0, 0);
             if constexpr (CG == 1)
                 mma_commit(sm.mma_done());
             else
                 mma_commit_pair(sm.mma_done(), 0x1);
+            lg.put(PL_WAIT, PF_MMA_DONE, 0, 0);
             wait_drain(sm.mma_done(), 0, sm.abort_flag, p);
+            lg.close();
         }
         __syncwarp();
     } else if (warp == 2) {
         // ------------------------------------------------- CLC scheduler
         if (lane == 0 && p.sched == SCHED_CLC && first_unit >= 0) {
+            Log lg;
+            lg.open(p, 2);
             uint32_t idx = 0;
             bool outstanding = false, waited = false;
             uint32_t out_r = 0, out_ph = 0;
@@ -594,6 +711,7 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
                 const uint32_t r = idx % depth;
                 const uint32_t ph = (idx / depth) & 1u;
                 if (rank == 0) {
+                    lg.put(PL_WAIT, PF_CLC_EMPTY, r, ph ^ 1u);
                     if (!wait_long(sm.clc_empty(r), ph ^ 1u, sm.abort_flag, p, WAIT_SCHED_CLC_EMPTY)) break;
                     // Lazy requests (long K loops): request idx names the unit after this
                     // worker's unit idx, so it waits until the producer has all but the last
@@ -601,9 +719,14 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
                     // A worker then claims its next unit shortly before it needs it, not
                     // when its current unit begins, so the units left late in the launch go
                     // to the workers that finish first.
-                    if (p.clc_lazy && !wait_long(sm.prod_began(), idx & 1u, sm.abort_flag, p, WAIT_SCHED_PRODUCER)) break;
+                    if (p.clc_lazy) {
+                        lg.put(PL_WAIT, PF_BEGAN, 0, idx & 1u);
+                        if (!wait_long(sm.prod_began(), idx & 1u, sm.abort_flag, p, WAIT_SCHED_PRODUCER)) break;
+                    }
                     fence_proxy_async_smem();
+                    lg.put(PL_ARRIVE, PF_CLC_FULL, r, 0);
                     mbar_arrive_expect_tx(sm.clc_full(r), C::CLC_RESPONSE_BYTES);
+                    lg.put(PL_CREQ, PF_CLC_FULL, r, 0);
                     if constexpr (CG == 1)
                         clc_try_cancel(sm.resp + 16u * r, sm.clc_full(r));
                     else
@@ -613,19 +736,21 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
                     out_ph = ph;
                 } else {
                     // the even CTA's request multicasts its response here: arm our barrier for it
+                    lg.put(PL_ARRIVE, PF_CLC_FULL, r, 0);
                     mbar_arrive_expect_tx(sm.clc_full(r), C::CLC_RESPONSE_BYTES);
                 }
-                const int32_t t = clc_consume(sm, p, idx);
+                const int32_t t = clc_consume(sm, p, idx, lg);
                 outstanding = false;
                 if (t < 0) {
                     // a failed wait leaves the request possibly in flight
                     if (*sm.abort_flag && rank == 0) outstanding = true;
                     break;
                 }
-                dep_wait_once(waited);
+                dep_wait_once(waited, lg);
             }
-            dep_wait_once(waited);
+            dep_wait_once(waited, lg);
             if (outstanding) wait_drain(sm.clc_full(out_r), out_ph, sm.abort_flag, p);
+            lg.close();
         }
         __syncwarp();
     } else if (warp == 3 && MG) {
@@ -639,6 +764,8 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
         // tile (64 bf16 per row; lane L owns rows L, L+32, L+64, L+96) to a
         // running fp32 sum over the unit's k-blocks and stores it at the end.
         if (fork) {
+            Log lg;
+            if (lane == 0) lg.open(p, 3);
             int32_t unit = first_unit;
             uint32_t clc_idx = 0, stage = 0, phase = 0;
             bool alive = true, waited = false;
@@ -656,6 +783,7 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
                     for (int c = 0; c < 8; ++c) sum[r][c] = 0.f;
                 for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
                     int ok = 1;
+                    lg.put(PL_WAIT, PF_FULL, stage, phase);
                     if (lane == 0) ok = wait_phase(sm.full(stage), phase, sm.abort_flag, p, WAIT_MMA_FULL);
                     ok = __shfl_sync(0xffffffffu, ok, 0);
                     if (!ok) {
@@ -685,7 +813,9 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
                             }
                         }
                     }
+                    lg.put(PL_SREAD, PF_FULL, stage, 0);
                     __syncwarp();
+                    lg.put(PL_ARRIVE, PF_AUX, stage, 0);
                     if (lane == 0) mbar_arrive(sm.aux_empty(stage));
                     if (++stage == C::STAGES) {
                         stage = 0;
@@ -693,7 +823,7 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
                     }
                 }
                 if (!alive) break;
-                dep_wait_once(waited);  // before the first row-sum store
+                dep_wait_once(waited, lg);  // before the first row-sum store
                 if (active) {
 #pragma unroll
                     for (int r = 0; r < 4; ++r) {
@@ -705,10 +835,11 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
                     }
                 }
                 int32_t nu = 0;
-                if (lane == 0) nu = next_unit(sm, p, unit, clc_idx);
+                if (lane == 0) nu = next_unit(sm, p, unit, clc_idx, lg);
                 unit = __shfl_sync(0xffffffffu, nu, 0);
             }
-            dep_wait_once(waited);
+            dep_wait_once(waited, lg);
+            lg.close();
         }
         __syncwarp();
     } else if (warp >= 4) {
@@ -716,7 +847,10 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
         // Warps 4 .. 4 + EW - 1.  A warp may access TMEM lanes 32 * (warp % 4) onwards:
         // warp 4 + j takes lane quarter q = j % 4 and, with 8 or 16 warps, the
         // subtiles s = h, h + EW / 4, ... (h = j / 4) of that quarter's rows.
+        Log lg;
+        if (lane == 0) lg.open(p, warp);
         if (p.inputs_ready) {  // D and this task's other outputs wait for the previous kernel
+            lg.put(PL_PDL, PF_NONE, 0, 0);
             grid_dep_wait();
             grid_dep_launch();
         }
@@ -805,11 +939,12 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
             const bool split = C::SPLIT && w.tail >= 0;  // the host plans no split for 16 warps
             if (!w.skip) {
             int ok = 1;
+            lg.put(PL_WAIT, PF_TFULL, acc, acc_phase);
             if (lane == 0) ok = wait_long(sm.tfull(acc), acc_phase, sm.abort_flag, p, WAIT_EPI_TMEM_FULL);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             tc_fence_after();
-            if (lane == 0) sm.next_slot[warp - kRoleWarps] = next_unit(sm, p, unit, clc_idx);
+            if (lane == 0) sm.next_slot[warp - kRoleWarps] = next_unit(sm, p, unit, clc_idx, lg);
             taken = true;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + acc * BN;
             float4 *const mine = split ? slab_of(w, w.part) : nullptr;
@@ -834,6 +969,8 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
                     // this warp's part of the accumulator is read: hand it back to the MMA issuer
                     tc_fence_before();
                     __syncwarp();
+                    lg.put(PL_TLOAD, PF_TFULL, acc, 0);
+                    lg.put(PL_ARRIVE, PF_TEMPTY, acc, 0);
                     if (lane == 0) {
                         if constexpr (CG == 1)
                             mbar_arrive(sm.tempty(acc));
@@ -918,10 +1055,11 @@ __global__ void __launch_bounds__(32 * (kRoleWarps + EW), 1)
                 p.trace[4 * unit + 3] = static_cast<long long>(globaltimer());
             }
             int32_t nu = 0;
-            if (lane == 0) nu = taken ? sm.next_slot[warp - kRoleWarps] : next_unit(sm, p, unit, clc_idx);  // a skipped tile
+            if (lane == 0) nu = taken ? sm.next_slot[warp - kRoleWarps] : next_unit(sm, p, unit, clc_idx, lg);  // a skipped tile
             unit = __shfl_sync(0xffffffffu, nu, 0);
         }
         if (lane == 0) bulk_wait<0>();
+        lg.close();
         __syncwarp();
     }
 

@@ -14,9 +14,9 @@ namespace ts {
 // statics of templates otherwise become process-unique symbols).
 namespace {
 
-template <int BN, int CG, int OUT, int EW, int MG>
+template <int BN, int CG, int OUT, int EW, int MG, int LOG>
 struct GemmInstance {
-    using C = GemmCfg<BN, CG, OUT, EW, MG>;
+    using C = GemmCfg<BN, CG, OUT, EW, MG, LOG>;
 
     // cudaFuncSetAttribute once per device (bit per device ordinal).
     static cudaError_t prepare() {
@@ -24,7 +24,7 @@ struct GemmInstance {
         const int dev = current_device();
         const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
         if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
-        cudaError_t e = cudaFuncSetAttribute(gemm_ws_kernel<BN, CG, OUT, EW, MG>,
+        cudaError_t e = cudaFuncSetAttribute(gemm_ws_kernel<BN, CG, OUT, EW, MG, LOG>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
         if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
         return e;
@@ -73,7 +73,7 @@ struct GemmInstance {
             attr[1].val.clusterDim.z = 1;
             cfg.numAttrs = 2;
         }
-        return cudaLaunchKernelEx(&cfg, gemm_ws_kernel<BN, CG, OUT, EW, MG>, L.a, L.b, L.d, L.p);
+        return cudaLaunchKernelEx(&cfg, gemm_ws_kernel<BN, CG, OUT, EW, MG, LOG>, L.a, L.b, L.d, L.p);
     }
 
     static cudaError_t max_workers(int *out) {
@@ -81,7 +81,7 @@ struct GemmInstance {
         if (e != cudaSuccess) return e;
         if (CG == 1) {
             int per_sm = 0;
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemm_ws_kernel<BN, CG, OUT, EW, MG>, C::THREADS,
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemm_ws_kernel<BN, CG, OUT, EW, MG, LOG>, C::THREADS,
                                                               C::SMEM_BYTES);
             if (e != cudaSuccess) return e;
             *out = per_sm * device_sms(current_device());
@@ -99,7 +99,7 @@ struct GemmInstance {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int clusters = 0;
-        e = cudaOccupancyMaxActiveClusters(&clusters, reinterpret_cast<const void *>(gemm_ws_kernel<BN, CG, OUT, EW, MG>),
+        e = cudaOccupancyMaxActiveClusters(&clusters, reinterpret_cast<const void *>(gemm_ws_kernel<BN, CG, OUT, EW, MG, LOG>),
                                            &cfg);
         if (e != cudaSuccess) return e;
         *out = clusters;
@@ -110,7 +110,7 @@ struct GemmInstance {
 }  // namespace
 }  // namespace ts
 
-#define TS_GEMM_VARIANT(NAME, BN, CG, OUT, EW, MG)                                                         \
+#define TS_GEMM_VARIANT_LOG(NAME, BN, CG, OUT, EW, MG, LOG)                                                \
     namespace ts {                                                                                         \
     extern const GemmVariant NAME;                                                                         \
     const GemmVariant NAME = {BN,                                                                          \
@@ -118,9 +118,12 @@ struct GemmInstance {
                               OUT,                                                                         \
                               EW,                                                                          \
                               MG,                                                                          \
-                              GemmCfg<BN, CG, OUT, EW, MG>::STAGES,                                        \
-                              GemmCfg<BN, CG, OUT, EW, MG>::SMEM_BYTES,                                    \
-                              GemmInstance<BN, CG, OUT, EW, MG>::protocol(),                               \
-                              &GemmInstance<BN, CG, OUT, EW, MG>::launch,                                  \
-                              &GemmInstance<BN, CG, OUT, EW, MG>::max_workers};                            \
+                              LOG,                                                                         \
+                              GemmCfg<BN, CG, OUT, EW, MG, LOG>::STAGES,                                   \
+                              GemmCfg<BN, CG, OUT, EW, MG, LOG>::SMEM_BYTES,                               \
+                              GemmInstance<BN, CG, OUT, EW, MG, LOG>::protocol(),                          \
+                              &GemmInstance<BN, CG, OUT, EW, MG, LOG>::launch,                             \
+                              &GemmInstance<BN, CG, OUT, EW, MG, LOG>::max_workers};                       \
     }
+// A product variant; TS_GEMM_VARIANT_LOG with LOG = 1 instantiates the protocol-logging kernel.
+#define TS_GEMM_VARIANT(NAME, BN, CG, OUT, EW, MG) TS_GEMM_VARIANT_LOG(NAME, BN, CG, OUT, EW, MG, 0)

@@ -97,6 +97,11 @@ struct GemmParams {
     // group g - 1.
     const uint8_t *skip;   // per tile, row-major by tile row and column per group: nonzero = skip, or nullptr
     float *row_sums;       // Fork consumer output [groups][M]: sum over the K range of each row of A, or nullptr
+    // Protocol log (the logged instantiation only): per CTA and role, a count
+    // followed by plog_cap event words (PlogOp in gemm_kernel.cuh), or nullptr.
+    int32_t *plog;
+    int32_t plog_cap;
+    int32_t pad3;
     int32_t groups;
     int32_t tiles_per_group;
     int64_t group_stride;

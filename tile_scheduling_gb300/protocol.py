@@ -401,3 +401,156 @@ def build_split_program(parts: int, launches: int = 2, mutate: str | None = None
             ops.append([OP_WAIT, boundary, L & 1, -1, -1, -1, -1, -1])
         P.roles.append((f"part[{p}]", None, ops))
     return P
+
+
+# ------------------------------------------------------------ protocol log
+# The logging build of the kernel (ts_gemm_opts.protocol_log) records every role's barrier
+# operations in program order.  These functions turn a model program and a kernel log into the
+# same event vocabulary, so that each modelled role can be compared with what the kernel did.
+PL_WAIT, PL_ARRIVE, PL_TMA, PL_MMA, PL_COMMIT, PL_CREQ, PL_PDL, PL_UNIT, PL_TLOAD, PL_CREAD, PL_SREAD = range(1, 12)
+PF_FULL, PF_EMPTY, PF_TFULL, PF_TEMPTY, PF_CLC_FULL, PF_CLC_EMPTY, PF_AUX, PF_BEGAN, PF_MMA_DONE = range(9)
+PF_NONE = 15
+_FAMILY = {"full": PF_FULL, "empty": PF_EMPTY, "tmem_full": PF_TFULL, "tmem_empty": PF_TEMPTY,
+           "clc_full": PF_CLC_FULL, "clc_empty": PF_CLC_EMPTY, "aux_empty": PF_AUX, "full_b": PF_AUX,
+           "prod_began": PF_BEGAN}
+_OP_NAME = {PL_WAIT: "wait", PL_ARRIVE: "arrive", PL_TMA: "tma", PL_MMA: "mma", PL_COMMIT: "commit",
+            PL_CREQ: "clc_request", PL_PDL: "dependent_launch_wait", PL_TLOAD: "accumulator_read",
+            PL_CREAD: "response_read", PL_SREAD: "stage_read"}
+_FAM_NAME = {v: k for k, v in _FAMILY.items() if k != "full_b"}
+_FAM_NAME.update({PF_MMA_DONE: "mma_done", PF_NONE: "-"})
+LOG_ROLES = 20  # roles per CTA in the log: 0 producer, 1 MMA, 2 scheduler, 3 warp 3, 4 + j epilogue warp j
+
+
+def encode_event(op: int, family: int = PF_NONE, index: int = 0, parity: int = 0) -> int:
+    """The kernel's event word (PLog::put)."""
+    return op | (family << 4) | (index << 8) | ((parity & 1) << 16)
+
+
+def describe(ev) -> str:
+    op, fam, idx, par = ev
+    s = f"{_OP_NAME.get(op, op)} {_FAM_NAME.get(fam, fam)}[{idx}]"
+    return s + (f" parity {par}" if op == PL_WAIT else "")
+
+
+def decode_log(block) -> tuple[list, list]:
+    """One role's log block (count, then events) -> (events, units).
+
+    events: (op, family, index, parity) tuples in program order; units: the units the producer
+    began, SKIP or their k-block counts.  Raises if the events overflowed the block."""
+    block = np.asarray(block, dtype=np.int64)
+    n = int(block[0])
+    if n > block.size - 1:
+        raise ValueError(f"the log holds {block.size - 1} events of {n}: give it more room")
+    events, units = [], []
+    for w in block[1:1 + n]:
+        w = int(w)
+        op = w & 0xF
+        if op == PL_UNIT:
+            units.append(SKIP if (w >> 4) & 1 else w >> 8)
+            continue
+        events.append((op, (w >> 4) & 0xF, (w >> 8) & 0xFF, (w >> 16) & 1 if op == PL_WAIT else 0))
+    return events, units
+
+
+def _bar(name: str):
+    """Model barrier name -> (family, index); None for the model's own gate barrier."""
+    base = name.split("[")[0]
+    if base == "roles_at_dependency_wait":
+        return None
+    if base == "dependent_launch":
+        return "pdl"
+    idx = int(name.rstrip("]").split("[")[-1]) if "[" in name else 0
+    return _FAMILY[base], idx
+
+
+def _buf_index(name: str) -> int:
+    return int(name.rstrip("]").split("[")[-1])
+
+
+def model_events(P: Program, role: str) -> list:
+    """The modelled role's operations in the log's vocabulary: barrier operations, and the reads
+    of accumulators, CLC responses and (by the Fork task) ring stages.  The gate on which the model
+    holds back the previous kernel is the model's own."""
+    ops = next(o for n, _, o in P.roles if n == role)
+    out = []
+    for o in ops:
+        kind = o[0]
+        if kind == OP_WAIT:
+            b = _bar(P.bar_names[o[1]])
+            if b == "pdl":
+                out.append((PL_PDL, PF_NONE, 0, 0))
+            elif b is not None:
+                out.append((PL_WAIT, b[0], b[1], o[2] & 1))
+        elif kind == OP_ARRIVE:
+            b = _bar(P.bar_names[o[1]])
+            if b is not None and b != "pdl":
+                out.append((PL_ARRIVE, b[0], b[1], 0))
+        elif kind == OP_TMA:
+            b = _bar(P.bar_names[o[3]])
+            out.append((PL_TMA, b[0], b[1], 0))
+        elif kind == OP_MMA:
+            out.append((PL_MMA, PF_FULL, _buf_index(P.bufs[o[1]]), 0))
+        elif kind == OP_COMMIT:
+            b = _bar(P.bar_names[o[1]])
+            out.append((PL_COMMIT, b[0], b[1], 0))
+        elif kind == OP_CREQ:
+            b = _bar(P.bar_names[o[4]])
+            out.append((PL_CREQ, b[0], b[1], 0))
+        elif kind in (OP_TREAD, OP_TREADB):
+            name = P.bufs[o[1]]
+            if name.startswith("tmem"):
+                out.append((PL_TLOAD, PF_TFULL, _buf_index(name), 0))
+            elif name.startswith("stage"):
+                out.append((PL_SREAD, PF_FULL, _buf_index(name), 0))
+        elif kind == OP_CREAD:
+            out.append((PL_CREAD, PF_CLC_FULL, _buf_index(P.bufs[o[1]]), 0))
+    return out
+
+
+def kernel_events(events: list, lazy_signals: bool) -> list:
+    """A role's logged events as the model states them: the MMA issuer's final commit and wait on
+    its own completion barrier (before TMEM is freed) are not modelled, and the producers' arrivals
+    on prod_began are modelled only where the scheduler waits on them (lazy CLC requests, the
+    even CTA's producer); the kernel makes them on every unit."""
+    return [e for e in events if e[1] != PF_MMA_DONE and not (e[1] == PF_BEGAN and e[0] == PL_ARRIVE and
+                                                              not lazy_signals)]
+
+
+def log_role(model_role: str) -> tuple[int, int]:
+    """Model role name -> (CTA within the worker, log role)."""
+    base = model_role.split("[")[0]
+    idx = [int(x) for x in model_role.replace("]", "").split("[")[1:]]
+    if base in ("producer", "producer_a"):
+        return idx[0], 0
+    if base == "producer_b":
+        return idx[0], 3
+    if base == "mma":
+        return 0, 1
+    if base == "scheduler":
+        return idx[0], 2
+    if base == "rowsum":
+        return 0, 3
+    if base == "epilogue":
+        return idx[0], 4 + idx[1]
+    raise ValueError(f"no log role for {model_role}")
+
+
+def compare_with_log(P: Program, log_blocks, worker_ctas: list, lazy: bool) -> list:
+    """Compare every modelled role with the kernel's log of one worker.
+
+    log_blocks[c][r]: the log block of CTA worker_ctas[c] and role r.  Returns a list of
+    mismatch descriptions (empty when every role did exactly what the model says)."""
+    problems = []
+    for name, _, _ in P.roles:
+        if name == "previous_kernel":
+            continue
+        c, r = log_role(name)
+        got, _ = decode_log(log_blocks[worker_ctas[c]][r])
+        got = kernel_events(got, lazy and c == 0 and r == 0)
+        want = model_events(P, name)
+        if got != want:
+            k = next((i for i, (g, w) in enumerate(zip(got, want)) if g != w), min(len(got), len(want)))
+            problems.append(f"{name} (CTA {worker_ctas[c]}, log role {r}): event {k}: kernel "
+                            f"{describe(got[k]) if k < len(got) else 'ends'}, model "
+                            f"{describe(want[k]) if k < len(want) else 'ends'} ({len(got)} / {len(want)} events)")
+    return problems
