@@ -111,6 +111,15 @@ def test_clc_protocol_verified_cta_pair_two_epilogue_warps_per_cta():
 
 
 @pytest.mark.exhaustive
+def test_merge_protocol_verified_cta_pair_two_units():
+    # the Merge layout on the CTA pair under CLC, two one-k-block units: ~4.1e7 states, about a
+    # minute (run with --exhaustive)
+    r = pc.check_variant("256x256", [1, 1], "clc", stages=2, epilogue_warps=1, variant_merge=1,
+                         max_states=100_000_000)
+    assert r.ok, r.message
+
+
+@pytest.mark.exhaustive
 def test_clc_protocol_verified_cta_pair_three_epilogue_warps_per_cta():
     # three epilogue warps per CTA of the pair: ~1.2e8 states, about 5 minutes and 4 GB of host
     # memory (run with --exhaustive)
