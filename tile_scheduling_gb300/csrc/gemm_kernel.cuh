@@ -56,6 +56,11 @@
 // the wait in the device status word, raises a CTA-local abort flag, lets
 // every role leave its loop, waits (with its own limit) for copies and MMAs
 // still in flight, frees TMEM and returns.
+//
+// A logging instantiation (LOG = 1; a test instrument) has every role record
+// its barrier operations in program order (PLog), for comparison with the
+// host-side model of these role loops; in the product instantiations every
+// logging call compiles to nothing.
 #pragma once
 #include <cuda.h>
 #include <cuda_runtime.h>
