@@ -123,10 +123,11 @@ typedef struct {
                              2 CLC scheduler, 3 warp 3, 4 + j epilogue warp j; 20 roles), a block of
                              protocol_log_cap + 1 words at (c * 20 + r) * (protocol_log_cap + 1):
                              the count of events, then the first protocol_log_cap events; the
-                             caller zeroes the buffer.  Built for three shapes only: tile 128x128
-                             (FusedMerge or Merge) and the 2-CTA 256x256 tile, fp32 output, four
-                             epilogue warps (others: TS_ERR_UNSUPPORTED).  Results are those of the
-                             normal build. */
+                             caller zeroes the buffer.  Built for fp32 output on five shapes only:
+                             tile 128x128 with four epilogue warps (FusedMerge or Merge) or eight,
+                             tile 128x256 with sixteen, and the 2-CTA 256x256 tile with four
+                             (others: TS_ERR_UNSUPPORTED).  Results are those of the normal
+                             build. */
     int32_t protocol_log_cap; /* events per CTA and role (>= 1 when protocol_log is given) */
 } ts_gemm_opts;
 

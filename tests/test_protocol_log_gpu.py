@@ -25,18 +25,18 @@ CAP = 2048
 
 
 def _logged(lib, M, N, K, sched, tile, merge=0, max_workers=0, fork=False, skip=None, inputs_ready=0, offsets=None,
-            seed=0x910):
+            seed=0x910, ew=4):
     Kt = offsets[-1] if offsets is not None else K
     A = synth.int_uniform_bf16(seed, (M, max(Kt, 8)))
     B = synth.int_uniform_bf16(seed + 1, (N, max(Kt, 8)))
     Ad, Bd = to_device_bf16(A), to_device_bf16(B)
-    kw = dict(sched=sched, tile=tile, merge=merge, max_workers=max_workers, epi_warps=4, inputs_ready=inputs_ready)
+    kw = dict(sched=sched, tile=tile, merge=merge, max_workers=max_workers, epi_warps=ew, inputs_ready=inputs_ready)
     if offsets is not None:
         info = lib.ts_gemm_grouped_launch_info(M, N, offsets, lib.TS_OUT_F32, sched, tile=tile, merge=merge,
-                                               max_workers=max_workers, epi_warps=4)
+                                               max_workers=max_workers, epi_warps=ew)
     else:
         info = lib.ts_gemm_launch_info(M, N, K, lib.TS_OUT_F32, sched, tile=tile, merge=merge,
-                                       max_workers=max_workers, epi_warps=4,
+                                       max_workers=max_workers, epi_warps=ew,
                                        split_tail=-1 if (fork or skip is not None) else 0)
     log = torch.zeros((info["grid_ctas"], pc.LOG_ROLES, CAP + 1), dtype=torch.int32, device="cuda")
     R = torch.full((M,), float("nan"), dtype=torch.float32, device="cuda") if fork else None
@@ -66,8 +66,8 @@ def _logged(lib, M, N, K, sched, tile, merge=0, max_workers=0, fork=False, skip=
     return info, log.cpu().numpy()
 
 
-def _check_workers(lib, info, log, tile, sched, merge=0, fork=False, early=False, mutate=None):
-    proto = lib.ts_gemm_protocol_info(tile, lib.TS_OUT_F32, 4, merge)
+def _check_workers(lib, info, log, tile, sched, merge=0, fork=False, early=False, mutate=None, ew=4):
+    proto = lib.ts_gemm_protocol_info(tile, lib.TS_OUT_F32, ew, merge)
     cg = proto["cluster"]
     lazy = bool(info["clc_lazy"])
     ran, problems = 0, []
@@ -111,6 +111,19 @@ def test_kernel_operations_follow_the_model(lib, case, ready):
     assert ran >= 1 and not problems, "\n".join(problems[:5])
     if sched == "clc":
         assert ran < info["grid_ctas"] // info["cluster"], "some worker should have taken over another's launch"
+
+
+@pytest.mark.parametrize("ready", [0, 1])
+@pytest.mark.parametrize("sched", ["static", "clc"])
+@pytest.mark.parametrize("tile,ew,K", [("128x128", 8, 256), ("128x256", 16, 64), ("128x256", 16, 128)])
+def test_more_epilogue_warps_follow_the_model(lib, tile, ew, K, sched, ready):
+    # eight warps (two per TMEM lane quarter) and sixteen (four), the short-K epilogues
+    M, N = 2048, 4096
+    info, log = _logged(lib, M, N, K, sched, tile, max_workers=16 if sched == "static" else 0, inputs_ready=ready,
+                        ew=ew)
+    assert info["epi_warps"] == ew
+    ran, problems = _check_workers(lib, info, log, tile, sched, early=bool(ready), ew=ew)
+    assert ran >= 1 and not problems, "\n".join(problems[:5])
 
 
 @pytest.mark.parametrize("sched", ["static", "clc"])

@@ -17,7 +17,8 @@ extern const GemmVariant variant_128_1_bf16_e4, variant_128_1_f32_e4, variant_25
     variant_256_1_f32_e8, variant_256_2_bf16_e8, variant_256_2_f32_e8, variant_128_1_bf16_e4m, variant_128_1_f32_e4m,
     variant_256_1_bf16_e4m, variant_256_1_f32_e4m, variant_256_2_bf16_e4m, variant_256_2_f32_e4m,
     variant_256_1_bf16_e16, variant_256_1_f32_e16, variant_256_2_bf16_e16, variant_256_2_f32_e16,
-    variant_128_1_f32_e4_log, variant_128_1_f32_e4m_log, variant_256_2_f32_e4_log;
+    variant_128_1_f32_e4_log, variant_128_1_f32_e4m_log, variant_128_1_f32_e8_log, variant_256_1_f32_e16_log,
+    variant_256_2_f32_e4_log;
 
 const GemmVariant *find_variant(int bn, int cg, int out, int epi_warps, int merge, int log) {
     static const GemmVariant *const all[] = {
@@ -27,7 +28,8 @@ const GemmVariant *find_variant(int bn, int cg, int out, int epi_warps, int merg
         &variant_128_1_bf16_e4m,    &variant_128_1_f32_e4m,     &variant_256_1_bf16_e4m, &variant_256_1_f32_e4m,
         &variant_256_2_bf16_e4m,    &variant_256_2_f32_e4m,     &variant_256_1_bf16_e16, &variant_256_1_f32_e16,
         &variant_256_2_bf16_e16,    &variant_256_2_f32_e16,     &variant_128_1_f32_e4_log,
-        &variant_128_1_f32_e4m_log, &variant_256_2_f32_e4_log};
+        &variant_128_1_f32_e4m_log, &variant_128_1_f32_e8_log,  &variant_256_1_f32_e16_log,
+        &variant_256_2_f32_e4_log};
     for (const GemmVariant *v : all)
         if (v->bn == bn && v->cg == cg && v->out == out && v->epi_warps == epi_warps && v->merge == merge &&
             v->log == log)
