@@ -147,3 +147,26 @@ def test_split_parts_are_the_first_units(lib, sched):
         for u in range(info["num_units"]):
             first.setdefault(int(owner[u]), u)
         assert all(first[int(owner[u])] == u for u in range(S * P))
+
+
+def test_automatic_workspaces_are_per_stream(lib):
+    # split-tile launches on two streams at once, each with the binding's automatic workspace: the
+    # streams get workspaces of their own, and both results are exact
+    tile, M, N, K = "256x256", 2560, 2560, 4096
+    A, B, ref = _integer_case(M, N, K)
+    Ad, Bd = to_device_bf16(A), to_device_bf16(B)
+    assert _info(lib, M, N, K, lib.TS_OUT_F32, "clc", tile, "auto")["split_tiles"] > 0
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    need = _info(lib, M, N, K, lib.TS_OUT_F32, "clc", tile, None)["workspace_bytes"]
+    assert lib.workspace_for(need, stream=s1).data_ptr() != lib.workspace_for(need, stream=s2).data_ptr()
+    assert lib.workspace_for(need, stream=s1.cuda_stream).data_ptr() == lib.workspace_for(need, stream=s1).data_ptr()
+    D1 = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    D2 = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    for _ in range(3):
+        lib.ts_gemm_bf16_ex(Ad, Bd, D1, sched="clc", tile=tile, stream=s1)
+        lib.ts_gemm_bf16_ex(Ad, Bd, D2, sched="static", tile=tile, stream=s2)
+    torch.cuda.synchronize()
+    lib.ts_sync_and_check()
+    assert_bit_exact(D1, ref, "stream 1")
+    assert_bit_exact(D2, ref, "stream 2")

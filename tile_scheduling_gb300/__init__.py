@@ -209,17 +209,26 @@ def _gemm_args(A, B, D):
 _WORKSPACES: dict = {}
 
 
-def workspace_for(nbytes: int, device=None) -> torch.Tensor:
-    """A zero-filled device workspace of at least ``nbytes``, cached per device.
+def workspace_for(nbytes: int, device=None, stream=None) -> torch.Tensor:
+    """A zero-filled device workspace of at least ``nbytes``, cached per device and stream.
 
     The kernel leaves the workspace zeroed after every normal launch, so one
-    buffer serves every call on a device (calls on different streams that may
-    overlap need buffers of their own)."""
+    buffer serves every call on a stream; calls on different streams, which may
+    overlap on the GPU, get buffers of their own.  A buffer is allocated and
+    zeroed on the stream it serves, so the zeroing is ordered before the
+    launches that use it (``stream``: a torch stream or a raw handle; default
+    the current stream)."""
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
-    ws = _WORKSPACES.get(dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    elif not isinstance(stream, torch.cuda.Stream):
+        stream = torch.cuda.ExternalStream(int(stream), device=dev)
+    key = (dev, stream.cuda_stream)
+    ws = _WORKSPACES.get(key)
     if ws is None or ws.numel() < nbytes:
-        ws = torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=dev)
-        _WORKSPACES[dev] = ws
+        with torch.cuda.stream(stream):
+            ws = torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=dev)
+        _WORKSPACES[key] = ws
     return ws
 
 
@@ -242,7 +251,7 @@ def ts_gemm_bf16_ex(A: torch.Tensor, B: torch.Tensor, D: torch.Tensor, sched="st
     lda, ldb, ldd = (lda if M > 1 else 0), (ldb if N > 1 else 0), (ldd if M > 1 else 0)
     workspace = _resolve_workspace(M, N, K, _OUT[D.dtype], sched, workspace,
                                    -1 if (skip_tiles is not None or row_sums is not None) else split_tail, tile=tile,
-                                   max_workers=max_workers, lda=lda, ldb=ldb, ldd=ldd)
+                                   max_workers=max_workers, lda=lda, ldb=ldb, ldd=ldd, stream=stream)
     o = _opts(tile, max_workers, lda, ldb, ldd, timeout_s, trace, raster_group, split_tail, workspace, skip_tiles,
               row_sums, epi_warps, merge, inputs_ready, protocol_log)
     _check(_lib.ts_gemm_bf16_ex(ctypes.c_void_p(A.data_ptr()), ctypes.c_void_p(B.data_ptr()),
@@ -262,7 +271,7 @@ def ts_gemm_bf16_host(A_host: torch.Tensor, B_host: torch.Tensor, D_host: torch.
         if h.shape != d.shape or h.dtype != d.dtype:
             raise ValueError(f"{name}_host and {name} differ in shape or dtype")
     M, N, K, _, _, _ = _gemm_args(A, B, D)
-    workspace = _resolve_workspace(M, N, K, _OUT[D.dtype], sched, workspace, 0, tile=tile)
+    workspace = _resolve_workspace(M, N, K, _OUT[D.dtype], sched, workspace, 0, tile=tile, stream=stream)
     o = _opts(tile=tile, workspace=workspace, epi_warps=epi_warps)
     _check(_lib.ts_gemm_bf16_host(ctypes.c_void_p(A_host.data_ptr()), ctypes.c_void_p(B_host.data_ptr()),
                                   ctypes.c_void_p(D_host.data_ptr()), ctypes.c_void_p(A.data_ptr()),
@@ -315,13 +324,13 @@ def _launch_info_raw(M: int, N: int, K: int, out, sched, **opts) -> dict:
     return {f: getattr(info, f) for f, _ in LaunchInfo._fields_}
 
 
-def _resolve_workspace(M, N, K, out, sched, workspace, split_tail, **opts):
+def _resolve_workspace(M, N, K, out, sched, workspace, split_tail, stream=None, **opts):
     if not isinstance(workspace, str):
         return workspace
     if split_tail < 0:
         return None
     need = _launch_info_raw(M, N, K, out, sched, split_tail=split_tail, **opts)["workspace_bytes"]
-    return workspace_for(need) if need > 0 else None
+    return workspace_for(need, stream=stream) if need > 0 else None
 
 
 def ts_gemm_launch_info(M: int, N: int, K: int, out=TS_OUT_BF16, sched="static", workspace="auto", split_tail=0,
