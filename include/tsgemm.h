@@ -6,7 +6,8 @@
  * C ABI: plain pointers and sizes only.  Every device pointer is owned by
  * the caller; the library never allocates device memory on these paths.  The
  * only library-owned device state is a small per-device status word that
- * records a timed-out barrier wait (see ts_sync_and_check).
+ * records a timed-out barrier wait (see ts_sync_and_check) and the statically
+ * sized scratch array of ts_gemm_bf16_checked_noalloc, both module globals.
  *
  * Streams are passed as `void *` holding a cudaStream_t (NULL = the legacy
  * default stream).  Every compute call is asynchronous on that stream and
