@@ -21,7 +21,9 @@ rotating buffer sets so that no launch finds its operands in L2),
 ``contended`` (the ragged 8191x6143x4096 fp32-out GEMM while a spin kernel
 holds 32 SMs for half the solo time: >= 10 alternating static/CLC pairs, the
 median times and each scheduler's launch tail from a traced run) and
-``smallk`` (8192x8192x64 bf16-out, output-write bound, in HBM GB/s).  Clocks
+``smallk`` (8192x8192x64 bf16-out, output-write bound, in HBM GB/s) and
+``grouped`` (16 groups of 2048x2048 whose K ranges from 64 to 8192, the groups
+scheduled longest K first, static persistent vs CLC).  Clocks
 are sampled in process through read-only NVML queries every 1 ms during every
 timed region.
 
@@ -417,6 +419,7 @@ def run_ours(args, ws, rank, local):
         extra["contended"] = measure_contended(ts, sampler, reps=max(10, args.reps), ctas=args.spin_ctas,
                                                tile=args.contended_tile, warmup=args.warmup)
         extra["smallk"] = measure_smallk(ts, sampler, samples=args.config_reps, warmup=args.warmup)
+        extra["grouped"] = measure_grouped(ts, sampler, reps=args.config_reps)
     sampler.stop()
     if rank != 0:
         return None
@@ -519,6 +522,41 @@ def _batched_ms(fns, reps, batch, stream, sampler=None, region=None, sleep_cycle
                 sampler.region(region or k, t0, time.time())
             out[k].append(e0.elapsed_time(e1) / batch)
     return out
+
+
+def measure_grouped(ts, sampler, reps=7, batch=5):
+    """The grouped GEMM whose 16 groups of 2048 x 2048 differ in K (64 .. 8192, skewed), the groups
+    scheduled longest K first, under the static persistent and the CLC scheduler (samples alternated).
+    Each launch reads 624 MB of A and B, more than L2 holds, so no launch finds its operands there."""
+    import torch
+
+    w = synth.GROUPED
+    off = w.k_offsets()
+    A_bits, B_bits = w.inputs()
+    A, B = _dev_bf16(A_bits), _dev_bf16(B_bits)
+    D = torch.empty((w.groups, w.M, w.N), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+    fns = {sched: (lambda i, sc=sched: ts.ts_gemm_bf16_grouped(A, B, D, off, sched=sc)) for sched in ("static", "clc")}
+    for f in fns.values():
+        for i in range(3):
+            f(i)
+    ms = _batched_ms(fns, reps, batch, stream, sampler, "grouped")
+    ts.ts_sync_and_check()
+    flops = 2.0 * w.M * w.N * off[-1]
+    peak = load_peaks()["bf16_tflops"]
+    runs = {}
+    for sched, v in ms.items():
+        med = statistics.median(v)
+        runs[sched] = {"us_median": round(med * 1e3, 2), "us_min": round(min(v) * 1e3, 2),
+                       "tflops": round(flops / (med * 1e-3) / 1e12, 1),
+                       "frac_of_burst": round(flops / (med * 1e-3) / 1e12 / peak, 4)}
+    del A, B, D
+    torch.cuda.empty_cache()
+    return {"metric": "grouped bf16 GEMM TFLOP/s, 16 groups of 2048x2048, K per group 64..8192 (skewed)",
+            "unit": "TFLOP/s", "value": max(r["tflops"] for r in runs.values()), "runs": runs,
+            "clc_speedup_over_static": round(runs["static"]["us_median"] / runs["clc"]["us_median"], 3),
+            "order": "groups longest K first (ts_gemm_grouped_order)", "k_offsets": off,
+            "samples": f"{reps} x {batch} back-to-back launches per scheduler, alternated"}
 
 
 def measure_gemm4096(ts, sampler, reps=5, batch=20, nset=4):

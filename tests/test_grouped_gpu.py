@@ -153,3 +153,13 @@ def test_grouped_units_follow_the_longest_first_order(lib):
     gaps = np.diff(tr[:, 3]).astype(np.float64)  # gaps[i]: end of unit i + 1 after the end of unit i
     long_gaps, short_gaps = gaps[0:3], gaps[4:11]
     assert long_gaps.mean() > 3 * short_gaps.mean(), (long_gaps, short_gaps)
+
+
+def test_automatic_tile_counts_every_group(lib):
+    # the automatic tile choice counts the tiles of every group: sixteen groups of 2048 x 2048 fill
+    # the GPU with 2-CTA 256 x 256 tiles, while one group alone takes the 128 x 128 tile
+    off16 = [64 * i for i in range(17)]
+    info = lib.ts_gemm_grouped_launch_info(2048, 2048, off16, lib.TS_OUT_BF16, "clc")
+    assert (info["cluster"], info["tile_m"], info["tile_n"]) == (2, 256, 256)
+    info = lib.ts_gemm_grouped_launch_info(2048, 2048, [0, 64], lib.TS_OUT_BF16, "clc")
+    assert (info["cluster"], info["tile_m"], info["tile_n"]) == (1, 128, 128)

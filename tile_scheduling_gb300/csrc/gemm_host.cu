@@ -222,8 +222,10 @@ ts_status plan_gemm(const void *D, int64_t M, int64_t N, int64_t K, int32_t out,
     if (tile == TS_TILE_AUTO) {
         // Largest tile that still gives every SM work: the 2-CTA tile halves
         // each SM's share of B traffic, the 128x128 tile suits small outputs.
-        const int64_t t256 = cdiv(M, 256) * cdiv(N, 256);
-        const int64_t t128x256 = cdiv(M, 128) * cdiv(N, 256);
+        // A grouped launch schedules every group's tiles, so all of them count.
+        const int64_t g = groups > 0 ? groups : 1;
+        const int64_t t256 = cdiv(M, 256) * cdiv(N, 256) * g;
+        const int64_t t128x256 = cdiv(M, 128) * cdiv(N, 256) * g;
         if (t256 * 2 >= sms && !o->row_sums)
             tile = TS_TILE_256x256_2CTA;
         else if (t128x256 >= sms)
