@@ -1095,17 +1095,22 @@ def run_e2e(args, ts, A_bits, B_bits, M, N, K, ws):
         step(i)
     torch.cuda.synchronize()
     steps = max(3, min(args.steps, args.e2e_steps))
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(streams[0])
-    for st in streams[1:]:
-        st.wait_event(e0)
-    for i in range(steps):
-        step(i)
-    for st in streams[1:]:
-        streams[0].wait_stream(st)
-    e1.record(streams[0])
-    torch.cuda.synchronize()
-    ms = reduce_times([e0.elapsed_time(e1)], "max")[0]
+    # three timed regions of `steps` steps each; the median region is reported (the host submits
+    # every step, so a region also shows any stall of the host that drives it)
+    regions = []
+    for _ in range(3):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(streams[0])
+        for st in streams[1:]:
+            st.wait_event(e0)
+        for i in range(steps):
+            step(i)
+        for st in streams[1:]:
+            streams[0].wait_stream(st)
+        e1.record(streams[0])
+        torch.cuda.synchronize()
+        regions.append(e0.elapsed_time(e1))
+    ms = reduce_times([statistics.median(regions)], "max")[0]
     ts.ts_sync_and_check()
     flops = 2.0 * M * N * K
     h2d = int(A_h.numel() * 2 + B_h.numel() * 2)
@@ -1115,6 +1120,7 @@ def run_e2e(args, ts, A_bits, B_bits, M, N, K, ws):
     return {"value": round(ws * flops * steps / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": steps, "ms_per_step": round(ms / steps, 4), "call": "ts_gemm_bf16_host",
+            "regions_ms": [round(r, 3) for r in regions], "reported": "the median of the three regions",
             "pipelining": f"one call per step (copy in, GEMM, copy out on one stream); steps round-robin over "
                           f"{nbuf} streams and buffer sets",
             "roofline": {"bound": "host link", "achieved": round(host_gbs, 1), "peak": link["both_gbs"],
