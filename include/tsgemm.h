@@ -88,8 +88,9 @@ typedef struct {
                              picks one; TS_TILE_256x256_2CTA is TS_ERR_UNSUPPORTED); no split tiles. */
     int32_t epi_warps;    /* epilogue warps per CTA: 4 (one per TMEM lane quarter), 8 or 16 (two or
                              four per quarter, taking its subtiles in turn: more latency hidden
-                             when the epilogue bounds the tile); 0 = automatic: for a plain GEMM
-                             16 with K <= 128 on a 256-column tile, 8 with K <= 256, else 4.
+                             when the epilogue bounds the tile); 0 = automatic: 16 with K <= 128
+                             on a 256-column tile, 8 with K <= 256, else 4 (K of a grouped GEMM:
+                             its longest group's range).
                              16 needs a 256-column tile (else TS_ERR_UNSUPPORTED) and never
                              splits the tail.  Anything else is TS_ERR_INVALID_ARG.  Results do
                              not depend on it. */

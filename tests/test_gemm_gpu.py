@@ -58,7 +58,7 @@ def test_gemm_integer_bit_exact(lib, tile, sched, out, ew, merge):
 
 def test_gemm_epilogue_warps_automatic_choice(lib):
     # sixteen epilogue warps for the shortest K loops on 256-column tiles, eight
-    # for short ones, four for a long one or a grouped GEMM
+    # for short ones, four for a long one; a grouped GEMM by its longest group
     for K, ew in ((64, 16), (128, 16), (192, 8), (256, 8)):
         assert lib.ts_gemm_launch_info(4096, 4096, K, lib.TS_OUT_BF16, "clc")["epi_warps"] == ew
         assert lib.ts_gemm_launch_info(4096, 4096, K, lib.TS_OUT_BF16, "static", tile="128x256")["epi_warps"] == ew
@@ -67,7 +67,11 @@ def test_gemm_epilogue_warps_automatic_choice(lib):
         lib.ts_gemm_launch_info(4096, 4096, 64, lib.TS_OUT_BF16, "clc", tile="128x128", epi_warps=16)
     assert lib.ts_gemm_launch_info(4096, 4096, 320, lib.TS_OUT_BF16, "clc")["epi_warps"] == 4
     assert lib.ts_gemm_launch_info(4096, 4096, 64, lib.TS_OUT_BF16, "clc", epi_warps=4)["epi_warps"] == 4
-    assert lib.ts_gemm_grouped_launch_info(512, 512, [0, 64, 128])["epi_warps"] == 4
+    assert lib.ts_gemm_grouped_launch_info(512, 512, [0, 64, 128])["epi_warps"] == 8  # 128 x 128 tiles
+    for widths, ew in (([64] * 16, 16), ([128, 64] * 8, 16), ([256, 0] * 8, 8), ([64] * 15 + [320], 4)):
+        off = [0] + list(np.cumsum(widths))
+        info = lib.ts_gemm_grouped_launch_info(2048, 2048, off, lib.TS_OUT_BF16, "clc")
+        assert info["cluster"] == 2 and info["epi_warps"] == ew, (widths[:2], info["epi_warps"])
     # the Merge layout is built with four
     info = lib.ts_gemm_launch_info(4096, 4096, 64, lib.TS_OUT_BF16, "clc", merge=1)
     assert info["epi_warps"] == 4 and info["merge"] == 1
