@@ -1,6 +1,6 @@
 """Run one named workload a few times (for profilers such as ncu); prints nothing but a summary line.
 
-Usage: python -m tile_scheduling_gb300.run_workload {gemm256,gemm4096,gemm8192,ragged,smallk,copy,rows}
+Usage: python -m tile_scheduling_gb300.run_workload {gemm256,gemm4096,gemm8192,ragged,smallk,grouped,copy,rows}
            [--launches N] [--sched static|clc|nonpersistent] [--tile auto|128x128|128x256|256x256]
 """
 from __future__ import annotations
@@ -26,7 +26,7 @@ GEMMS = {"gemm256": synth.GEMM_256, "gemm4096": synth.GEMM_4096, "gemm8192": syn
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("workload", choices=sorted(GEMMS) + ["copy", "rows"])
+    ap.add_argument("workload", choices=sorted(GEMMS) + ["grouped", "copy", "rows"])
     ap.add_argument("--launches", type=int, default=3)
     ap.add_argument("--sched", default=None, choices=["static", "clc", "nonpersistent"])
     ap.add_argument("--tile", default=None)
@@ -57,6 +57,20 @@ def main(argv=None):
             ts.ts_copy_i16_rows(src, dst, off, sched=sched, chunk=a.chunk, workspace=ws, pack=a.pack)
         ts.ts_sync_and_check()
         print(f"{synth.ROWS.name}: {sched} chunk {a.chunk} pack {a.pack} x{a.launches} ok")
+        return 0
+    if a.workload == "grouped":
+        w = synth.GROUPED
+        off = w.k_offsets()
+        A_bits, B_bits = w.inputs()
+        A = torch.from_numpy(A_bits.view(np.int16)).view(torch.bfloat16).cuda()
+        B = torch.from_numpy(B_bits.view(np.int16)).view(torch.bfloat16).cuda()
+        D = torch.empty((w.groups, w.M, w.N), dtype=torch.bfloat16, device="cuda")
+        sched = a.sched or "clc"
+        tile = a.tile or "auto"
+        for _ in range(a.launches):
+            ts.ts_gemm_bf16_grouped(A, B, D, off, sched=sched, tile=tile)
+        ts.ts_sync_and_check()
+        print(f"{w.name}: {sched} {tile} x{a.launches} ok")
         return 0
     w = GEMMS[a.workload]
     A_bits, B_bits = w.inputs()
