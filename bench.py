@@ -1252,7 +1252,7 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--workload", default="headline", choices=["headline", "gemm4096", "contended", "grouped", "causal", "fork",
                                                                    "rows", "smallk", "ingress"])
     ap.add_argument("--reps", type=int, default=10, help="static/CLC pairs of the contended workload (>= 10)")
